@@ -1,0 +1,400 @@
+"""Benchmark: FP32 matrix multiply throughput (TFLOP/s = 2MNK / time) on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME]
+
+One step is one C = A x B call on the named workload (default: the square
+4096^3 problem with standard-normal inputs, seed 3).  Inputs are resident in
+HBM before timing.  Between timed steps L2 is flushed by writing a 512 MiB
+buffer; each step is bracketed by CUDA events on the launching stream and the
+flush lies outside the bracket.  Rank 0 prints one JSON line.
+
+With N > 1 (launched by torch.distributed.run) every rank runs an independent
+replica on its own GPU (the product does not shard across GPUs); the timed
+region is bracketed by a barrier and synchronisation, and the slowest rank's
+time counts.
+
+``--impl reference`` times the CPU oracle (the double-accumulating triple
+loop) on a bounded sample of rows of the same workload, on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from workloads import PROBLEMS, problem_operands  # noqa: E402
+
+METRIC = "SGEMM TFLOPS (2MNK/s) and % of FP32 roofline at 1024^3-8192^3 on 1 GB300"
+UNIT = "TFLOP/s"
+DEFAULT_WORKLOAD = "square_4096"
+L2_FLUSH_BYTES = 512 << 20
+# FP32 CUDA-core roofline derived from unit counts and clock: 152 SMs x 128 FP32
+# lanes x 2 flops per FMA x 2070 MHz (maximum SM clock).
+SMS, FP32_LANES_PER_SM, SM_MAX_MHZ = 152, 128, 2070.0
+DERIVED_FP32_PEAK_TFLOPS = SMS * FP32_LANES_PER_SM * 2 * SM_MAX_MHZ * 1e6 / 1e12
+KERNEL_SOURCES = ["sgemm_ffma.cuh", "ptx.cuh", "sgemm_ffma_tma.cu"]
+
+
+# ----------------------------------------------------------------- distributed helpers
+
+def dist_env():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), int(
+        os.environ.get("LOCAL_RANK", "0"))
+
+
+def max_over_ranks(value: float, device=None) -> float:
+    """Maximum of a per-rank float over the process group (identity without one)."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(device=None):
+    import torch.distributed as dist
+
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        if device is not None and dist.get_backend() == "nccl":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+# ----------------------------------------------------------------- clocks sampler
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while running."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, period_ms: int = 50):
+        self.cmd = ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}",
+                    "--format=csv,noheader,nounits", "-lms", str(period_ms)]
+        self.proc = None
+        self.lines: list[str] = []
+        self.t0 = self.t1 = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(self.cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.reader = threading.Thread(target=self._read, daemon=True)
+            self.reader.start()
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None:
+            return None
+        rows = []
+        for t, line in self.lines:
+            if self.t0 is not None and not (self.t0 <= t <= (self.t1 or t) + 0.05):
+                continue
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            rows.append(parts)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        power = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows), "power_w_max": max(power) if power else None}
+
+
+# ----------------------------------------------------------------- oracle (CPU) timing
+
+def oracle_rows_rate(A, B, rows, threads):
+    """Times the oracle on whole rows; returns (seconds, flops)."""
+    import oracle
+
+    t = time.perf_counter()
+    oracle.default().gemm_rows_f64(A, B, rows)
+    dt = time.perf_counter() - t
+    return dt, 2.0 * len(rows) * B.shape[1] * A.shape[1]
+
+
+def cpu_baseline(p, target_s: float = 12.0):
+    """The oracle, as it stands, on a bounded sample of output rows."""
+    import numpy as np
+
+    import oracle
+
+    A, B = problem_operands(p)
+    A, B = A.numpy(), B.numpy()
+    threads = oracle.default_threads()
+    rng = np.random.default_rng(0)
+    probe = np.sort(rng.choice(p.M, size=min(p.M, max(threads, 8)), replace=False))
+    dt, _ = oracle_rows_rate(A, B, probe, threads)
+    per_row = dt / len(probe)
+    n = int(min(p.M, max(len(probe), target_s / max(per_row, 1e-9))))
+    rows = np.sort(rng.choice(p.M, size=n, replace=False))
+    dt, flops = oracle_rows_rate(A, B, rows, threads)
+    return {"value": flops / dt / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"{n} of {p.M} output rows of the {p.M}x{p.N}x{p.K} product "
+                      f"(double accumulation, {dt:.1f} s)"}
+
+
+# ----------------------------------------------------------------- traffic record
+
+def kernel_source_digest() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "dense_fp32_gemm_f32_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str, variant: str):
+    """DRAM bytes per launch from the committed ncu record, if it matches the
+    current kernel source, workload and variant; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        rec = json.load(open(path))
+    except (OSError, ValueError):
+        return None
+    for r in rec.get("records", []):
+        if (r.get("workload") == workload and r.get("variant") == variant
+                and r.get("kernel_src") == kernel_source_digest()):
+            return r.get("dram_bytes_per_launch")
+    return None
+
+
+# ----------------------------------------------------------------- the two arms
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return 0
+    import numpy as np
+
+    import oracle
+
+    p = PROBLEMS[args.workload]
+    A, B = problem_operands(p)
+    A, B = A.numpy(), B.numpy()
+    threads = oracle.default_threads()
+    rng = np.random.default_rng(1)
+    # size each step so that warmup + steps take about two minutes in total
+    probe = np.sort(rng.choice(p.M, size=min(p.M, max(threads, 8)), replace=False))
+    dt, _ = oracle_rows_rate(A, B, probe, threads)
+    per_row = dt / len(probe)
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    n = int(min(p.M, max(threads, budget / max(per_row, 1e-9))))
+    times, flops = [], 0.0
+    for i in range(args.warmup + args.steps):
+        rows = np.sort(rng.choice(p.M, size=n, replace=False))
+        t, f = oracle_rows_rate(A, B, rows, threads)
+        if i >= args.warmup:
+            times.append(t)
+            flops = f
+    ms = 1e3 * statistics.mean(times)
+    value = flops / (ms / 1e3) / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(p, l2="n/a (host)"),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": f"{n} of {p.M} output rows per step"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(p, l2):
+    return {"workload": f"{p.name}: C = A x B, M={p.M} N={p.N} K={p.K}, row-major float32, "
+                        f"A,B {p.dist} seed {p.seed}, C overwritten",
+            "M": p.M, "N": p.N, "K": p.K, "dist": p.dist, "seed": p.seed, "l2": l2}
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+
+    import dense_fp32_gemm_f32_gb300 as g
+    from dense_fp32_gemm_f32_gb300 import _lib
+
+    assert torch.cuda.is_available(), "bench.py needs a CUDA GPU"
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    lib = _lib.load()
+    p = PROBLEMS[args.workload]
+    A_cpu, B_cpu = problem_operands(p)
+    A = A_cpu.to(device)
+    B = B_cpu.to(device)
+    C = torch.empty((p.M, p.N), dtype=torch.float32, device=device)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device)
+    sp = stream.cuda_stream
+    variant = g.describe(A, B, C)
+
+    # FP32 FMA peak microbenchmark (both instruction forms), for context.
+    import ctypes
+
+    scratch = torch.empty(SMS * 8 * 256, dtype=torch.float32, device=device)
+    peaks = {}
+    for paired in (0, 1):
+        fl = ctypes.c_double(0)
+        for _ in range(2):
+            _lib.check(lib.sgemm_bench_fma_peak(paired, SMS * 8, 4096, scratch.data_ptr(), sp, ctypes.byref(fl)),
+                       "fma peak")
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        reps = 5
+        for _ in range(reps):
+            lib.sgemm_bench_fma_peak(paired, SMS * 8, 4096, scratch.data_ptr(), sp, ctypes.byref(fl))
+        e1.record(stream)
+        e1.synchronize()
+        peaks["ffma2" if paired else "ffma"] = fl.value * reps / (e0.elapsed_time(e1) / 1e3) / 1e12
+
+    def step():
+        _lib.check(lib.sgemm_f32(p.M, p.N, p.K, A.data_ptr(), p.K, B.data_ptr(), p.N, C.data_ptr(), p.N, sp),
+                   "sgemm_f32")
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert g.check_status() == 0
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    with ClockSampler(device.index if device.index is not None else 0) as clk:
+        barrier(device)
+        torch.cuda.synchronize()
+        clk.mark_start()
+        t_wall = time.perf_counter()
+        for i in range(args.steps):
+            flush.fill_(float(i))  # write > L2 so every step starts cold
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+        barrier(device)
+        wall = time.perf_counter() - t_wall
+        clk.mark_end()
+    status = g.check_status()
+    assert status == 0, f"kernel status {status}"
+    kernel_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms_local = statistics.mean(kernel_ms)
+    ms = max_over_ranks(ms_local, device)
+    value = world * p.flops / (ms / 1e3) / 1e12
+    achieved = p.flops / (statistics.mean(kernel_ms) / 1e3) / 1e12
+
+    # End to end through the host-buffer entry: pinned host A, B -> device,
+    # multiply, C -> pinned host, every step.
+    A_pin, B_pin = A_cpu.pin_memory(), B_cpu.pin_memory()
+    C_pin = torch.empty((p.M, p.N), dtype=torch.float32, pin_memory=True)
+    e2e_steps = max(3, min(args.steps, 20))
+    for _ in range(2):
+        g.sgemm_f32_host(A_pin, B_pin, C_pin, device=device)
+    barrier(device)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        g.sgemm_f32_host(A_pin, B_pin, C_pin, device=device)
+    e2e_s = max_over_ranks((time.perf_counter() - t0) / e2e_steps, device)
+    e2e_value = world * p.flops / e2e_s / 1e12
+
+    if rank != 0:
+        return 0
+    cpu = cpu_baseline(p) if world == 1 else None
+    clocks = clk.summary()
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": workload_config(p, l2=f"flushed before every step ({L2_FLUSH_BYTES >> 20} MiB write)"),
+        "variant": variant,
+        "roofline": {"bound": "alu", "achieved": achieved, "peak": DERIVED_FP32_PEAK_TFLOPS, "unit": UNIT,
+                     "frac": achieved / DERIVED_FP32_PEAK_TFLOPS,
+                     "traffic": recorded_traffic(p.name, variant),
+                     "peak_source": "derived: 152 SMs x 128 FP32 lanes x 2 flop x 2070 MHz",
+                     "measured_fma_peak": peaks,
+                     "frac_of_measured": achieved / max(peaks.values()),
+                     "algorithmic_flops_per_launch": p.flops, "min_bytes_per_launch": p.min_bytes},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": 4 * (p.M * p.K + p.K * p.N),
+                "d2h_bytes_per_step": 4 * p.M * p.N},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+        "cpu_baseline": cpu,
+        "wall_s_timed_region": wall,
+        "kernel_ms": {"mean": ms_local, "min": min(kernel_ms), "median": statistics.median(kernel_ms),
+                      "max": max(kernel_ms)},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(PROBLEMS), default=DEFAULT_WORKLOAD)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    rank, world, local_rank = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+
+        backend = "nccl" if args.impl == "ours" else "gloo"
+        if args.impl == "ours":
+            import torch
+
+            torch.cuda.set_device(local_rank)
+        dist.init_process_group(backend=backend)
+    try:
+        if args.impl == "reference":
+            return run_reference(args, rank, world)
+        return run_ours(args, rank, world, local_rank)
+    finally:
+        import torch.distributed as dist
+
+        if dist.is_available() and dist.is_initialized():
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

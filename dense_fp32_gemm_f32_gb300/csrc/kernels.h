@@ -1,0 +1,17 @@
+// Host-side registry of the compiled kernel variants (internal to the library).
+#pragma once
+
+namespace gb300 {
+
+struct KernelEntry {
+    const void* fn;   // host stub of the __global__ function, or nullptr if not built
+    int smem_bytes;   // dynamic shared memory the launch needs
+    int threads;      // threads per CTA
+};
+
+// FFMA kernels fed by tensor-map bulk copies; stages in {1,2,3,4,5,6}, math 1 = FFMA, 2 = paired FFMA.
+KernelEntry ffma_kernel_tma(int stages, int math);
+// FFMA kernels fed by 4-byte cp.async (any alignment); stages in {2,4}.
+KernelEntry ffma_kernel_cpasync(int stages, int math);
+
+}  // namespace gb300

@@ -1,0 +1,404 @@
+// C ABI of the library: argument validation, variant selection, tensor-map
+// encoding and launch.  See include/sgemm.h for the contract.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "../../include/sgemm.h"
+#include "kernels.h"
+#include "sgemm_ffma.cuh"
+
+namespace gb300 {
+
+// Sticky per-device status word; kernels OR error bits into it.
+__device__ unsigned int g_sgemm_status = 0;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;  // 2 s per wait
+constexpr long long kMaxGridY = 65535;
+
+struct DeviceState {
+    std::once_flag once;
+    int status = SGEMM_ERR_CUDA;  // result of the one-time set-up
+    int sm_count = 0;
+    int max_clusters_pair = 0;    // co-resident 2-CTA clusters of the FFMA kernel
+    int max_clusters_split[9] = {0};
+    unsigned int* status_word = nullptr;  // device address of g_sgemm_status
+};
+
+DeviceState g_dev[kMaxDevices];
+
+std::once_flag g_encode_once;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+void load_encoder() {
+    std::call_once(g_encode_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        else
+            (void)cudaGetLastError();
+    });
+}
+
+// Largest number of co-resident clusters of `cluster` CTAs (along x or z) for
+// one kernel variant; 0 on failure.
+int max_active_clusters(const KernelEntry& k, int cx, int cz) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(cx, 1, cz);
+    cfg.blockDim = dim3(k.threads, 1, 1);
+    cfg.dynamicSmemBytes = static_cast<size_t>(k.smem_bytes);
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = cx;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = cz;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, k.fn, &cfg) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    return n;
+}
+
+int set_smem_attr(const KernelEntry& k) {
+    if (!k.fn) return SGEMM_OK;
+    if (cudaFuncSetAttribute(k.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, k.smem_bytes) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return SGEMM_ERR_CUDA;
+    }
+    return SGEMM_OK;
+}
+
+int init_device(int dev, DeviceState& st) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&st.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return SGEMM_ERR_CUDA;
+    }
+    // The library carries sm_103a code only (compute capability 10.3).
+    if (major != 10 || minor != 3) return SGEMM_ERR_UNSUPPORTED;
+    void* addr = nullptr;
+    if (cudaGetSymbolAddress(&addr, g_sgemm_status) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return SGEMM_ERR_CUDA;
+    }
+    st.status_word = static_cast<unsigned int*>(addr);
+    for (int math = kMathFfma; math <= kMathFfma2; ++math) {
+        for (int s = 1; s <= 6; ++s)
+            if (set_smem_attr(ffma_kernel_tma(s, math)) != SGEMM_OK) return SGEMM_ERR_CUDA;
+        for (int s = 1; s <= 6; ++s)
+            if (set_smem_attr(ffma_kernel_cpasync(s, math)) != SGEMM_OK) return SGEMM_ERR_CUDA;
+    }
+    const KernelEntry ref = ffma_kernel_tma(4, kMathFfma2);
+    st.max_clusters_pair = max_active_clusters(ref, 2, 1);
+    st.max_clusters_split[1] = st.sm_count;
+    for (int s = 2; s <= 8; ++s) st.max_clusters_split[s] = max_active_clusters(ref, 1, s);
+    load_encoder();
+    return SGEMM_OK;
+}
+
+// Set-up of the current device (once per device per process).
+int current_device(int* dev_out, DeviceState** st_out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return SGEMM_ERR_CUDA;
+    }
+    if (dev < 0 || dev >= kMaxDevices) return SGEMM_ERR_UNSUPPORTED;
+    DeviceState& st = g_dev[dev];
+    std::call_once(st.once, [&] { st.status = init_device(dev, st); });
+    *dev_out = dev;
+    *st_out = &st;
+    return st.status;
+}
+
+bool ranges_overlap(const void* a, size_t abytes, const void* b, size_t bbytes) {
+    if (!abytes || !bbytes) return false;
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    return a0 < b0 + bbytes && b0 < a0 + abytes;
+}
+
+size_t span_bytes(long long rows, long long cols, long long ld) {
+    if (rows <= 0 || cols <= 0) return 0;
+    return static_cast<size_t>(((rows - 1) * ld + cols) * 4);
+}
+
+int validate(int M, int N, int K, const float* A, int lda, const float* B, int ldb, const float* C, int ldc) {
+    if (M < 0 || N < 0 || K < 0) return SGEMM_ERR_INVALID_ARG;
+    if (lda < K || ldb < N || ldc < N) return SGEMM_ERR_INVALID_ARG;
+    if (M > 0 && K > 0 && !A) return SGEMM_ERR_INVALID_ARG;
+    if (K > 0 && N > 0 && !B) return SGEMM_ERR_INVALID_ARG;
+    if (M > 0 && N > 0 && !C) return SGEMM_ERR_INVALID_ARG;
+    if (static_cast<long long>(M) > kMaxGridY * kBM) return SGEMM_ERR_INVALID_ARG;
+    const size_t cb = span_bytes(M, N, ldc);
+    if (ranges_overlap(C, cb, A, span_bytes(M, K, lda)) || ranges_overlap(C, cb, B, span_bytes(K, N, ldb)))
+        return SGEMM_ERR_INVALID_ARG;
+    return SGEMM_OK;
+}
+
+struct Plan {
+    int producer = kProducerTma;
+    int math = kMathFfma2;
+    int stages = 4;
+    int split = 1;
+    int mcast = 1;
+    int grid_x = 0, grid_y = 0;
+    int num_k_tiles = 0;
+};
+
+long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
+
+bool tma_ok(const float* p, int ld) {
+    return (reinterpret_cast<uintptr_t>(p) & 15u) == 0 && (static_cast<long long>(ld) * 4) % 16 == 0;
+}
+
+// Chooses the variant.  Any field of `opt` that is non-zero forces that choice.
+int make_plan(const DeviceState& st, int M, int N, int K, const float* A, int lda, const float* B, int ldb,
+              const sgemm_options* opt, Plan* out) {
+    Plan pl;
+    pl.num_k_tiles = static_cast<int>(ceil_div(K, kBK));
+    const long long tiles_n = ceil_div(N, kBN), tiles_m = ceil_div(M, kBM);
+    const long long tiles = tiles_n * tiles_m;
+
+    // Producer: tensor maps need 16-byte aligned bases and row strides, and K > 0.
+    const bool aligned = K > 0 && tma_ok(A, lda) && tma_ok(B, ldb);
+    const int want_prod = opt ? opt->producer : 0;
+    if (want_prod == SGEMM_PRODUCER_TMA) {
+        if (!aligned) return SGEMM_ERR_INVALID_ARG;
+        pl.producer = kProducerTma;
+    } else if (want_prod == SGEMM_PRODUCER_CPASYNC) {
+        pl.producer = kProducerCpAsync;
+    } else if (want_prod == SGEMM_PRODUCER_AUTO) {
+        pl.producer = aligned ? kProducerTma : kProducerCpAsync;
+    } else {
+        return SGEMM_ERR_INVALID_ARG;
+    }
+
+    if (opt && opt->math) {
+        if (opt->math != kMathFfma && opt->math != kMathFfma2) return SGEMM_ERR_INVALID_ARG;
+        pl.math = opt->math;
+    }
+    if (opt && opt->stages) {
+        if (opt->stages < 1 || opt->stages > 6) return SGEMM_ERR_INVALID_ARG;
+        pl.stages = opt->stages;
+    }
+    if (pl.producer == kProducerCpAsync && pl.stages != 2 && pl.stages != 4) {
+        if (opt && opt->stages) return SGEMM_ERR_INVALID_ARG;
+        pl.stages = 4;
+    }
+
+    // Split-K: pick s in 1..8 minimising (waves of clusters) x (K tiles per CTA).
+    if (opt && opt->split_k) {
+        if (opt->split_k < 1 || opt->split_k > 8) return SGEMM_ERR_INVALID_ARG;
+        pl.split = opt->split_k;
+    } else {
+        long long best = -1;
+        for (int s = 1; s <= 8; ++s) {
+            const int slots = st.max_clusters_split[s];
+            if (slots <= 0) continue;
+            if (s > 1 && pl.num_k_tiles < 2 * s) break;  // keep at least two K slices per CTA
+            const long long cost = ceil_div(tiles, slots) * ceil_div(pl.num_k_tiles, s);
+            if (best < 0 || cost < best) {
+                best = cost;
+                pl.split = s;
+            }
+        }
+    }
+    if (pl.split > 1 && pl.stages < 2) return SGEMM_ERR_INVALID_ARG;  // partial tile needs 64 KiB of ring
+
+    // Multicast pairs along N: only without split, with a TMA producer, and
+    // only when pairing leaves no SM idle.
+    const int want_mc = opt ? opt->multicast : 0;
+    if (want_mc == 2) {
+        if (pl.split > 1 || pl.producer != kProducerTma) return SGEMM_ERR_INVALID_ARG;
+        pl.mcast = 2;
+    } else if (want_mc == 1) {
+        pl.mcast = 1;
+    } else if (want_mc == 0) {
+        pl.mcast = (pl.split == 1 && pl.producer == kProducerTma && tiles_n >= 2 &&
+                    2LL * st.max_clusters_pair >= st.sm_count)
+                       ? 2
+                       : 1;
+    } else {
+        return SGEMM_ERR_INVALID_ARG;
+    }
+
+    pl.grid_x = static_cast<int>(pl.mcast == 2 ? 2 * ceil_div(tiles_n, 2) : tiles_n);
+    pl.grid_y = static_cast<int>(tiles_m);
+    *out = pl;
+    return SGEMM_OK;
+}
+
+int encode_2d(CUtensorMap* map, const float* base, long long inner, long long outer, long long ld, int box_inner,
+              int box_outer, CUtensorMapSwizzle swz) {
+    if (!g_encode) return SGEMM_ERR_UNSUPPORTED;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 4};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_inner), static_cast<cuuint32_t>(box_outer)};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims, strides, box,
+                                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? SGEMM_OK : SGEMM_ERR_CUDA;
+}
+
+const char* describe_plan(const Plan& pl) {
+    static thread_local char buf[96];
+    std::snprintf(buf, sizeof buf, "%s/%s/mc%d/s%d/st%d", pl.producer == kProducerTma ? "tma" : "cpasync",
+                  pl.math == kMathFfma2 ? "ffma2" : "ffma", pl.mcast, pl.split, pl.stages);
+    return buf;
+}
+
+int run_ffma(int M, int N, int K, const float* A, int lda, const float* B, int ldb, float* C, int ldc,
+             void* stream, const sgemm_options* opt) {
+    int rc = validate(M, N, K, A, lda, B, ldb, C, ldc);
+    if (rc != SGEMM_OK) return rc;
+    if (opt && opt->debug_skip_stage < 0) return SGEMM_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return SGEMM_OK;  // nothing to write; no device work
+    int dev = 0;
+    DeviceState* st = nullptr;
+    rc = current_device(&dev, &st);
+    if (rc != SGEMM_OK) return rc;
+
+    Plan pl;
+    rc = make_plan(*st, M, N, K, A, lda, B, ldb, opt, &pl);
+    if (rc != SGEMM_OK) return rc;
+
+    const KernelEntry k =
+        pl.producer == kProducerTma ? ffma_kernel_tma(pl.stages, pl.math) : ffma_kernel_cpasync(pl.stages, pl.math);
+    if (!k.fn) return SGEMM_ERR_INVALID_ARG;
+
+    alignas(64) CUtensorMap tmA;
+    alignas(64) CUtensorMap tmB;
+    std::memset(&tmA, 0, sizeof tmA);
+    std::memset(&tmB, 0, sizeof tmB);
+    if (pl.producer == kProducerTma) {
+        rc = encode_2d(&tmA, A, K, M, lda, kBK, kBM / pl.mcast, CU_TENSOR_MAP_SWIZZLE_128B);
+        if (rc == SGEMM_OK) rc = encode_2d(&tmB, B, N, K, ldb, kBN, kBK, CU_TENSOR_MAP_SWIZZLE_NONE);
+        if (rc != SGEMM_OK) return rc;
+    }
+
+    FfmaParams prm;
+    prm.M = M;
+    prm.N = N;
+    prm.K = K;
+    prm.A = A;
+    prm.lda = lda;
+    prm.B = B;
+    prm.ldb = ldb;
+    prm.C = C;
+    prm.ldc = ldc;
+    prm.num_k_tiles = pl.num_k_tiles;
+    prm.split = pl.split;
+    prm.mcast = pl.mcast;
+    prm.vec_store = ((reinterpret_cast<uintptr_t>(C) & 15u) == 0 && ldc % 4 == 0) ? 1 : 0;
+    prm.skip_stage = opt ? opt->debug_skip_stage : 0;
+    prm.timeout_ns = (opt && opt->timeout_ns) ? opt->timeout_ns : kDefaultTimeoutNs;
+    prm.status = st->status_word;
+
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(pl.grid_x, pl.grid_y, pl.split);
+    cfg.blockDim = dim3(k.threads, 1, 1);
+    cfg.dynamicSmemBytes = static_cast<size_t>(k.smem_bytes);
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = pl.mcast;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = pl.split;
+    cfg.attrs = &attr;
+    cfg.numAttrs = (pl.mcast > 1 || pl.split > 1) ? 1 : 0;
+    void* args[3] = {&tmA, &tmB, &prm};
+    if (cudaLaunchKernelExC(&cfg, k.fn, args) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return SGEMM_ERR_CUDA;
+    }
+    return SGEMM_OK;
+}
+
+}  // namespace
+}  // namespace gb300
+
+using namespace gb300;
+
+extern "C" {
+
+int sgemm_f32(int M, int N, int K, const float* A, int lda, const float* B, int ldb, float* C, int ldc,
+              void* stream) {
+    return run_ffma(M, N, K, A, lda, B, ldb, C, ldc, stream, nullptr);
+}
+
+int sgemm_f32_ex(int M, int N, int K, const float* A, int lda, const float* B, int ldb, float* C, int ldc,
+                 void* stream, const sgemm_options* opt) {
+    return run_ffma(M, N, K, A, lda, B, ldb, C, ldc, stream, opt);
+}
+
+int sgemm_3xtf32(int M, int N, int K, const float* A, int lda, const float* B, int ldb, float* C, int ldc,
+                 void* stream) {
+    (void)stream;
+    const int rc = validate(M, N, K, A, lda, B, ldb, C, ldc);
+    if (rc != SGEMM_OK) return rc;
+    return SGEMM_ERR_NOT_IMPLEMENTED;
+}
+
+int sgemm_check_status(void* stream) {
+    int dev = 0;
+    DeviceState* st = nullptr;
+    const int rc = current_device(&dev, &st);
+    if (rc != SGEMM_OK) return rc;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return SGEMM_ERR_CUDA;
+    }
+    unsigned int word = 0;
+    const unsigned int zero = 0;
+    if (cudaMemcpy(&word, st->status_word, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess ||
+        cudaMemcpy(st->status_word, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return SGEMM_ERR_CUDA;
+    }
+    return (word & kStatusTimeout) ? SGEMM_ERR_TIMEOUT : SGEMM_OK;
+}
+
+const char* sgemm_status_string(int status) {
+    switch (status) {
+        case SGEMM_OK: return "ok";
+        case SGEMM_ERR_INVALID_ARG: return "invalid argument";
+        case SGEMM_ERR_UNSUPPORTED: return "unsupported device or variant";
+        case SGEMM_ERR_CUDA: return "CUDA error";
+        case SGEMM_ERR_TIMEOUT: return "kernel wait timed out";
+        case SGEMM_ERR_NOT_IMPLEMENTED: return "not implemented";
+        default: return "unknown status";
+    }
+}
+
+const char* sgemm_describe(int M, int N, int K, const float* A, int lda, const float* B, int ldb, const float* C,
+                           int ldc) {
+    if (validate(M, N, K, A, lda, B, ldb, C, ldc) != SGEMM_OK) return "invalid";
+    int dev = 0;
+    DeviceState* st = nullptr;
+    if (current_device(&dev, &st) != SGEMM_OK) return "unavailable";
+    if (M == 0 || N == 0) return "noop";
+    Plan pl;
+    if (make_plan(*st, M, N, K, A, lda, B, ldb, nullptr, &pl) != SGEMM_OK) return "invalid";
+    return describe_plan(pl);
+}
+
+}  // extern "C"

@@ -1,0 +1,375 @@
+// FP32 matrix multiply on the CUDA cores (FFMA), sm_103a.
+//
+// C (M x N) = A (M x K) * B (K x N), all row-major float32.
+//
+// The method is the one the pages build up step by step, re-designed for
+// Blackwell:
+//  * block tiling with a K sliding window ("Matrix multiplication performance
+//    optimisation", section 1 "tiling"): each CTA owns a BM x BN = 128 x 128
+//    tile of C and walks K in slices of BK = 32;
+//  * shared-memory staging of the A and B slices (same page, section 3) --
+//    here written by the Tensor Memory Accelerator (cp.async.bulk.tensor) in
+//    one bulk copy per operand instead of by the threads, with the TMA 128-byte
+//    swizzle on A in place of the page's "+1" row padding (padding would break
+//    the 16-byte alignment of vector loads; the swizzle keeps it and still
+//    spreads eight consecutive rows over all banks);
+//  * out-of-range elements read as zero (same page, section 3 edge handling):
+//    the tensor map's out-of-bounds fill writes zeros, so no load is predicated;
+//  * double buffering (same page, section 4) generalised to a STAGES-deep ring
+//    of shared-memory slices with a "full" and an "empty" mbarrier per slot.  A
+//    dedicated producer warp issues the copies; eight consumer warps compute;
+//  * register tiling (same page, section 2; "[infra] 03" experiment 4): every
+//    consumer thread accumulates an 8 x 8 block of C in registers and updates
+//    it by outer products of 8 A values and 8 B values per k, read from shared
+//    memory as 16-byte vectors.
+//
+// Extra machinery not on the pages:
+//  * cluster multicast: two CTAs that share the same rows of A (neighbours
+//    along N) each fetch half of the A slice and the TMA multicasts it into
+//    both CTAs' shared memory, halving the L2->SM traffic for A;
+//  * split-K: for outputs with too few tiles to fill the GPU, a cluster of
+//    `split` CTAs along K computes partial tiles over disjoint K ranges and
+//    reduces them through distributed shared memory in a fixed rank order
+//    (deterministic, no global workspace);
+//  * paired FMA (fma.rn.f32x2, sm_100 family): two multiply-adds per
+//    instruction, halving the issue slots the outer product needs.
+//
+// Every wait is bounded by `timeout_ns` of global time; a thread that gives up
+// records SGEMM_ERR_TIMEOUT in the device status word, stops computing, and
+// still takes part in every CTA/cluster barrier so that no other thread waits
+// forever.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "ptx.cuh"
+
+namespace gb300 {
+
+constexpr int kBM = 128;
+constexpr int kBN = 128;
+constexpr int kBK = 32;
+constexpr int kConsumerWarps = 8;
+constexpr int kConsumerThreads = kConsumerWarps * 32;
+constexpr int kThreads = kConsumerThreads + 32;  // + one producer warp
+constexpr int kStageABytes = kBM * kBK * 4;      // 16 KiB, 128-byte swizzled rows of 32 floats
+constexpr int kStageBBytes = kBK * kBN * 4;      // 16 KiB, plain rows of 128 floats
+constexpr int kStageBytes = kStageABytes + kStageBBytes;
+constexpr int kPartialBytes = kBM * kBN * 4;     // split-K partial tile
+
+enum : int { kProducerTma = 1, kProducerCpAsync = 2 };
+enum : int { kMathFfma = 1, kMathFfma2 = 2 };
+enum : unsigned { kStatusTimeout = 4u };
+
+struct FfmaParams {
+    int M, N, K;
+    const float* A;
+    long long lda;
+    const float* B;
+    long long ldb;
+    float* C;
+    long long ldc;
+    int num_k_tiles;       // ceil(K / kBK)
+    int split;             // CTAs per cluster along K (== gridDim.z); 1 = no split
+    int mcast;             // 2 = pairs of CTAs along N share A by multicast; 1 = off
+    int vec_store;         // C base 16-byte aligned and ldc % 4 == 0
+    int skip_stage;        // debug: CTA (0,0,0)'s producer never issues K-slice skip_stage-1
+    unsigned long long timeout_ns;
+    unsigned int* status;  // per-device sticky status word (error bits)
+};
+
+template <int STAGES>
+constexpr int ffma_smem_bytes() {
+    return (STAGES * kStageBytes > kPartialBytes ? STAGES * kStageBytes : kPartialBytes) + 1024 /*align*/ +
+           256 /*barriers*/;
+}
+
+// Physical byte offset of float (row r, column c) inside a 128-byte-swizzled
+// tile of 32-float rows: the 16-byte chunk index c/4 is XORed with r mod 8.
+__device__ __forceinline__ uint32_t swz128(int r, int c) {
+    return static_cast<uint32_t>(r * 128 + ((((c >> 2) ^ r) & 7) << 4) + (c & 3) * 4);
+}
+
+template <int STAGES, int PRODUCER, int MATH>
+__global__ void __launch_bounds__(kThreads, 1)
+    sgemm_ffma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                      const FfmaParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    // 1024-byte alignment for the 128-byte swizzle pattern; identical offset in
+    // every CTA, which multicast relies on.
+    const uint32_t raw_base = smem_addr(smem_raw);
+    const uint32_t base = (raw_base + 1023u) & ~1023u;
+    uint8_t* const smem = smem_raw + (base - raw_base);
+    constexpr int kRingBytes = STAGES * kStageBytes > kPartialBytes ? STAGES * kStageBytes : kPartialBytes;
+    const uint32_t sA0 = base;                         // STAGES x 16 KiB
+    const uint32_t sB0 = base + STAGES * kStageABytes;  // STAGES x 16 KiB
+    const uint32_t bar0 = base + kRingBytes;           // full[STAGES], empty[STAGES]
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const bool is_producer = warp == kConsumerWarps;
+    const int split = p.split;
+    const int mcast = p.mcast;
+    const uint32_t crank = (split > 1 || mcast > 1) ? cluster_ctarank() : 0u;
+
+    // Tile coordinates.  gridDim.x runs over N tiles (the multicast pairs are
+    // neighbours along x), gridDim.y over M tiles, gridDim.z over K splits.
+    const int n0 = blockIdx.x * kBN;
+    const int m0 = blockIdx.y * kBM;
+    const int kz = (split > 1) ? static_cast<int>(blockIdx.z) : 0;
+    const int kt_begin = static_cast<int>((static_cast<long long>(p.num_k_tiles) * kz) / split);
+    const int kt_end = static_cast<int>((static_cast<long long>(p.num_k_tiles) * (kz + 1)) / split);
+    const int nkt = kt_end - kt_begin;
+
+    if (threadIdx.x == 0) {
+        const uint32_t full_count = (PRODUCER == kProducerTma) ? 1u : 32u;
+        const uint32_t empty_count = static_cast<uint32_t>(kConsumerWarps * mcast);
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full_bar(s), full_count);
+            mbar_init(empty_bar(s), empty_count);
+        }
+        fence_mbarrier_init();
+    }
+    if (PRODUCER == kProducerTma && is_producer && lane == 0) {
+        prefetch_tensormap(&tmA);
+        prefetch_tensormap(&tmB);
+    }
+    if (mcast > 1 || split > 1) {
+        cluster_sync_all();  // barrier init visible to the peer CTAs before any multicast
+    } else {
+        __syncthreads();
+    }
+
+    bool timed_out = false;
+    const unsigned long long tmo = p.timeout_ns;
+    const bool skip_here = p.skip_stage > 0 && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0;
+
+    // ------------------------------------------------------------ producer
+    if (is_producer) {
+        if (PRODUCER == kProducerTma) {
+            if (lane == 0) {
+                int issued_round[STAGES];
+#pragma unroll
+                for (int s = 0; s < STAGES; ++s) issued_round[s] = -1;
+                for (int it = 0; it < nkt; ++it) {
+                    const int s = it % STAGES;
+                    const int round = it / STAGES;
+                    if (round > 0 && !mbar_wait_bounded(empty_bar(s), (round - 1) & 1, tmo)) {
+                        timed_out = true;
+                        break;
+                    }
+                    if (skip_here && it == p.skip_stage - 1) continue;
+                    const int k0 = (kt_begin + it) * kBK;
+                    mbar_arrive_expect_tx(full_bar(s), kStageBytes);
+                    if (mcast > 1) {
+                        // This CTA fetches rows [crank*64, crank*64+64) of the A slice
+                        // and multicasts them into both CTAs of the pair.
+                        const uint32_t half = static_cast<uint32_t>(kStageABytes / 2) * crank;
+                        tma_load_2d_multicast(sA0 + s * kStageABytes + half, &tmA, full_bar(s), k0,
+                                              m0 + static_cast<int>(crank) * (kBM / 2), 0x3);
+                    } else {
+                        tma_load_2d(sA0 + s * kStageABytes, &tmA, full_bar(s), k0, m0);
+                    }
+                    tma_load_2d(sB0 + s * kStageBBytes, &tmB, full_bar(s), n0, k0);
+                    issued_round[s] = round;
+                }
+                // Drain: wait until every copy this thread issued has landed.
+#pragma unroll
+                for (int s = 0; s < STAGES; ++s) {
+                    if (issued_round[s] >= 0 && !mbar_wait_bounded(full_bar(s), issued_round[s] & 1, tmo))
+                        timed_out = true;
+                }
+            }
+        } else {
+            // cp.async producer: all 32 lanes copy 4-byte elements with zero fill.
+            for (int it = 0; it < nkt; ++it) {
+                const int s = it % STAGES;
+                const int round = it / STAGES;
+                if (round > 0 && !mbar_wait_bounded(empty_bar(s), (round - 1) & 1, tmo)) {
+                    timed_out = true;
+                    break;
+                }
+                if (skip_here && it == p.skip_stage - 1) continue;
+                const int k0 = (kt_begin + it) * kBK;
+                const uint32_t sa = sA0 + s * kStageABytes;
+                const uint32_t sb = sB0 + s * kStageBBytes;
+                // A slice: 128 rows x 32 floats; lane = column, one row per step.
+                {
+                    const int k = k0 + lane;
+                    const bool kin = k < p.K;
+                    for (int r = 0; r < kBM; ++r) {
+                        const int m = m0 + r;
+                        const bool in = kin && m < p.M;
+                        const float* src = in ? p.A + static_cast<long long>(m) * p.lda + k : p.A;
+                        cp_async_4(sa + swz128(r, lane), src, in ? 4u : 0u);
+                    }
+                }
+                // B slice: 32 rows x 128 floats; lane = column within a 32-wide strip.
+                for (int r = 0; r < kBK; ++r) {
+                    const int k = k0 + r;
+                    const bool kin = k < p.K;
+#pragma unroll
+                    for (int q = 0; q < kBN / 32; ++q) {
+                        const int n = n0 + q * 32 + lane;
+                        const bool in = kin && n < p.N;
+                        const float* src = in ? p.B + static_cast<long long>(k) * p.ldb + n : p.B;
+                        cp_async_4(sb + static_cast<uint32_t>(r * (kBN * 4) + (q * 32 + lane) * 4), src,
+                                   in ? 4u : 0u);
+                    }
+                }
+                cp_async_mbar_arrive_noinc(full_bar(s));
+            }
+            cp_async_wait_all();
+        }
+        if (timed_out) atomicOr(p.status, kStatusTimeout);
+    }
+
+    // ------------------------------------------------------------ consumers
+    // Warp layout: 4 (M) x 2 (N) warps of 32 x 64; lane layout 4 (M) x 8 (N).
+    // Thread rows: wm*32 + tm + 4*i (i = 0..7); thread columns:
+    // wn*64 + tn*4 + {0..3} and wn*64 + 32 + tn*4 + {0..3}.
+    // acc[i][q] holds columns (2q, 2q+1) of thread row i: q = 0,1 cover
+    // tn*4 + 0..3, q = 2,3 cover 32 + tn*4 + 0..3.
+    float2 acc[8][4];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) acc[i][q] = make_float2(0.f, 0.f);
+
+    const int wm = warp >> 1, wn = warp & 1;
+    const int tm = lane >> 3, tn = lane & 7;
+    if (!is_producer) {
+        // Byte offsets inside a stage.  A row r = wm*32 + tm + 4i has r mod 8 =
+        // tm + 4*(i & 1), so even i share one swizzle key and odd i the other.
+        const uint32_t a_row0 = static_cast<uint32_t>((wm * 32 + tm) * 128);
+        const uint32_t b_col0 = static_cast<uint32_t>((wn * 64 + tn * 4) * 4);
+        const uint8_t* const smem_a = smem;                          // generic pointers
+        const uint8_t* const smem_b = smem + STAGES * kStageABytes;  // for the vector loads
+
+        for (int it = 0; it < nkt; ++it) {
+            const int s = it % STAGES;
+            const int round = it / STAGES;
+            if (!mbar_wait_bounded(full_bar(s), round & 1, tmo)) {
+                timed_out = true;
+                break;
+            }
+            const uint8_t* sa = smem_a + s * kStageABytes + a_row0;
+            const uint8_t* sb = smem_b + s * kStageBBytes + b_col0;
+#pragma unroll
+            for (int kg = 0; kg < kBK / 4; ++kg) {
+                const uint32_t xe = static_cast<uint32_t>(((kg ^ tm) & 7) << 4);
+                const uint32_t xo = xe ^ 64u;
+                float4 a[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    a[i] = *reinterpret_cast<const float4*>(sa + i * 512 + ((i & 1) ? xo : xe));
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    const int k = kg * 4 + kk;
+                    const float4 b0 = *reinterpret_cast<const float4*>(sb + k * (kBN * 4));
+                    const float4 b1 = *reinterpret_cast<const float4*>(sb + k * (kBN * 4) + 128);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const float av = kk == 0 ? a[i].x : kk == 1 ? a[i].y : kk == 2 ? a[i].z : a[i].w;
+                        if (MATH == kMathFfma2) {
+                            const float2 aa = make_float2(av, av);
+                            acc[i][0] = __ffma2_rn(aa, make_float2(b0.x, b0.y), acc[i][0]);
+                            acc[i][1] = __ffma2_rn(aa, make_float2(b0.z, b0.w), acc[i][1]);
+                            acc[i][2] = __ffma2_rn(aa, make_float2(b1.x, b1.y), acc[i][2]);
+                            acc[i][3] = __ffma2_rn(aa, make_float2(b1.z, b1.w), acc[i][3]);
+                        } else {
+                            acc[i][0].x = fmaf(av, b0.x, acc[i][0].x);
+                            acc[i][0].y = fmaf(av, b0.y, acc[i][0].y);
+                            acc[i][1].x = fmaf(av, b0.z, acc[i][1].x);
+                            acc[i][1].y = fmaf(av, b0.w, acc[i][1].y);
+                            acc[i][2].x = fmaf(av, b1.x, acc[i][2].x);
+                            acc[i][2].y = fmaf(av, b1.y, acc[i][2].y);
+                            acc[i][3].x = fmaf(av, b1.z, acc[i][3].x);
+                            acc[i][3].y = fmaf(av, b1.w, acc[i][3].y);
+                        }
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(empty_bar(s));
+                if (mcast > 1) mbar_arrive_cluster(empty_bar(s), crank ^ 1u);
+            }
+        }
+        if (timed_out) atomicOr(p.status, kStatusTimeout);
+    }
+
+    // ------------------------------------------------------------ split-K reduction
+    if (split > 1) {
+        // All consumer reads of the ring are finished once every thread of the
+        // CTA passes this barrier; the ring is then reused for the partial tile.
+        __syncthreads();
+        // Partial layout: [e4 = 0..15][thread = 0..255][4 floats]; element
+        // group e4 = i*2 + h holds acc[i][2h] and acc[i][2h+1] (four columns).
+        // Consecutive threads write consecutive 16-byte words, so both the
+        // local stores and the remote vector loads are free of bank conflicts.
+        if (!is_producer && crank != 0) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+                    sts128(base + static_cast<uint32_t>(((i * 2 + h) * kConsumerThreads + threadIdx.x) * 16),
+                           make_float4(acc[i][2 * h].x, acc[i][2 * h].y, acc[i][2 * h + 1].x, acc[i][2 * h + 1].y));
+        }
+        cluster_sync_all();
+        if (!is_producer && crank == 0) {
+            for (int r = 1; r < split; ++r) {  // fixed order: deterministic sums
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const uint32_t off =
+                            base + static_cast<uint32_t>(((i * 2 + h) * kConsumerThreads + threadIdx.x) * 16);
+                        const float4 v = ld_shared_cluster_v4(map_shared_rank(off, static_cast<uint32_t>(r)));
+                        acc[i][2 * h].x += v.x;
+                        acc[i][2 * h].y += v.y;
+                        acc[i][2 * h + 1].x += v.z;
+                        acc[i][2 * h + 1].y += v.w;
+                    }
+            }
+        }
+        cluster_sync_all();  // peers keep their shared memory alive until rank 0 has read it
+        if (crank != 0) return;
+    } else if (mcast > 1) {
+        // No CTA may leave while its peer can still multicast into it or
+        // arrive on its barriers.
+        cluster_sync_all();
+    }
+
+    if (is_producer) return;
+
+    // ------------------------------------------------------------ epilogue
+    const int row0 = m0 + wm * 32 + tm;
+    const int col0 = n0 + wn * 64 + tn * 4;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int r = row0 + 4 * i;
+        if (r >= p.M) continue;
+        float* crow = p.C + static_cast<long long>(r) * p.ldc;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int c = col0 + 32 * h;
+            const float4 v = make_float4(acc[i][2 * h].x, acc[i][2 * h].y, acc[i][2 * h + 1].x, acc[i][2 * h + 1].y);
+            if (p.vec_store && c + 3 < p.N) {
+                *reinterpret_cast<float4*>(crow + c) = v;
+            } else {
+                if (c < p.N) crow[c] = v.x;
+                if (c + 1 < p.N) crow[c + 1] = v.y;
+                if (c + 2 < p.N) crow[c + 2] = v.z;
+                if (c + 3 < p.N) crow[c + 3] = v.w;
+            }
+        }
+    }
+}
+
+}  // namespace gb300

@@ -1,0 +1,151 @@
+/*
+ * sgemm.h -- C ABI of the GB300 (sm_103a) single-precision matrix multiply.
+ *
+ * Operation.  For row-major float32 matrices A (M x K) and B (K x N), every
+ * entry point below overwrites the row-major M x N matrix C with the product
+ *
+ *     C[i*ldc + j] = sum_{k=0}^{K-1} A[i*lda + k] * B[k*ldb + j],
+ *                    0 <= i < M, 0 <= j < N,
+ *
+ * the definition C_{i,j} = sum_k A_{i,k} B_{k,j} given in "Hardware
+ * acceleration: optimising the memory access pattern of CUDA kernels for
+ * matrix multiply", section "computational characteristics of matrix
+ * multiplication", with that page's row-major indexing (basic kernel listing)
+ * generalised to leading dimensions lda >= K, ldb >= N, ldc >= N.  There is no
+ * alpha/beta: C is written, never read.  K == 0 writes zeros (the empty sum);
+ * M == 0 or N == 0 is a no-op.
+ *
+ * Accuracy contract.  Summation order and fused multiply-add contraction are
+ * the library's choice.  For every entry, |C - exact| <= 5e-5 * sum_k |A_ik||B_kj|;
+ * inputs whose every partial sum is an integer below 2^24 in magnitude (for
+ * example entries in {-8..8} with K <= 2^18) give the exact result.
+ *
+ * Memory.  A, B and C are DEVICE pointers owned by the caller; the library
+ * allocates no device memory.  C must not overlap A or B.  Rows may be padded
+ * (ld > row width); padding is never written and never read.
+ *
+ * Streams.  `stream` is a cudaStream_t passed as void* (NULL selects the legacy
+ * default stream).  Every call enqueues work on that stream and returns without
+ * synchronising; the caller synchronises.  The library keeps only per-device,
+ * once-initialised state (kernel attributes and the driver's tensor-map encoder
+ * entry point), set up under a lock, so concurrent calls from several host
+ * threads are safe.
+ *
+ * Errors.  Each call returns an sgemm_status.  Argument errors are detected on
+ * the host before anything is enqueued.  A kernel that gives up on a bounded
+ * wait records SGEMM_ERR_TIMEOUT in a per-device status word, which
+ * sgemm_check_status() reads (and clears) after synchronising the stream.
+ * Nothing throws across this interface.
+ */
+#ifndef GB300_SGEMM_H
+#define GB300_SGEMM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum sgemm_status {
+    SGEMM_OK = 0,
+    SGEMM_ERR_INVALID_ARG = 1,     /* negative size, ld below row width, NULL with
+                                      non-empty operand, C overlapping A or B,
+                                      size beyond the documented limits, bad option */
+    SGEMM_ERR_UNSUPPORTED = 2,     /* current device is not an sm_100-family GPU
+                                      (compute capability 10.x), or the requested
+                                      variant cannot run on it */
+    SGEMM_ERR_CUDA = 3,            /* a CUDA runtime/driver call or the launch failed */
+    SGEMM_ERR_TIMEOUT = 4,         /* a kernel abandoned a bounded wait (see
+                                      sgemm_check_status) */
+    SGEMM_ERR_NOT_IMPLEMENTED = 5  /* the requested path is not built */
+} sgemm_status;
+
+/* Size limits: M, N, K and the leading dimensions are int (>= 0).  M is also
+ * limited to 65535 * 128 rows (grid height).  Larger requests return
+ * SGEMM_ERR_INVALID_ARG. */
+
+/*
+ * sgemm_f32 -- C = A x B in float32 on the CUDA cores (FFMA).
+ *
+ * The main entry.  Picks the kernel variant itself: TMA-fed when A, B have
+ * 16-byte aligned bases and row strides, a cp.async-fed variant otherwise;
+ * cluster split-K when the output has too few tiles to fill the GPU; a
+ * two-CTA cluster sharing A tiles through TMA multicast otherwise.
+ *   M, N, K      problem sizes (>= 0)
+ *   A, lda       device pointer to A, row stride in floats (lda >= K)
+ *   B, ldb       device pointer to B, row stride in floats (ldb >= N)
+ *   C, ldc       device pointer to C, row stride in floats (ldc >= N)
+ *   stream       cudaStream_t as void*
+ */
+int sgemm_f32(int M, int N, int K,
+              const float* A, int lda,
+              const float* B, int ldb,
+              float* C, int ldc,
+              void* stream);
+
+/*
+ * sgemm_3xtf32 -- same operation, signature, accuracy contract and error
+ * behaviour as sgemm_f32, computed on the tensor cores: each operand is split
+ * into a TF32 "big" part and a TF32 "small" remainder and three TF32 products
+ * (small*big + big*small + big*big) are accumulated in float32.  Returns
+ * SGEMM_ERR_NOT_IMPLEMENTED while that path is not built.
+ */
+int sgemm_3xtf32(int M, int N, int K,
+                 const float* A, int lda,
+                 const float* B, int ldb,
+                 float* C, int ldc,
+                 void* stream);
+
+/* Producer kinds for sgemm_options.producer. */
+enum {
+    SGEMM_PRODUCER_AUTO = 0,
+    SGEMM_PRODUCER_TMA = 1,      /* tensor-map bulk copies (needs 16-byte alignment) */
+    SGEMM_PRODUCER_CPASYNC = 2   /* 4-byte cp.async with zero fill (any alignment) */
+};
+
+/*
+ * Forced-variant options for ablations and tests.  A zero-initialised struct
+ * means "choose automatically" for every field.
+ */
+typedef struct sgemm_options {
+    int producer;       /* SGEMM_PRODUCER_* */
+    int split_k;        /* 0 = auto, 1 = none, 2..8 = CTAs per cluster along K */
+    int multicast;      /* 0 = auto, 1 = off, 2 = two CTAs share A via TMA multicast */
+    int math;           /* 0 = auto, 1 = scalar FFMA, 2 = paired FFMA (fma.rn.f32x2) */
+    int stages;         /* 0 = auto, else 2..6 shared-memory pipeline stages */
+    int debug_skip_stage; /* 0 = off; k > 0: the producer of CTA (0,0,0) never
+                             issues its k-th K-slice, so the consumers' bounded
+                             wait expires (tests the timeout path) */
+    uint64_t timeout_ns;  /* 0 = default (2 s); bound on every in-kernel wait */
+} sgemm_options;
+
+/* sgemm_f32 with forced choices.  Same contract; an unsupported combination
+ * returns SGEMM_ERR_INVALID_ARG or SGEMM_ERR_UNSUPPORTED before any launch. */
+int sgemm_f32_ex(int M, int N, int K,
+                 const float* A, int lda,
+                 const float* B, int ldb,
+                 float* C, int ldc,
+                 void* stream, const sgemm_options* opt);
+
+/* Synchronises `stream`, then returns and clears the current device's status
+ * word: SGEMM_OK, or SGEMM_ERR_TIMEOUT if any kernel since the last check gave
+ * up on a bounded wait (its output is then undefined).  SGEMM_ERR_CUDA if the
+ * synchronisation itself fails. */
+int sgemm_check_status(void* stream);
+
+/* Static, human-readable name of a status code ("unknown status" otherwise). */
+const char* sgemm_status_string(int status);
+
+/* Describes the variant sgemm_f32 would launch for these sizes and pointers on
+ * the current device, as a static string such as "tma/ffma2/mc2/s1/st4".
+ * Host-only; launches nothing. */
+const char* sgemm_describe(int M, int N, int K,
+                           const float* A, int lda,
+                           const float* B, int ldb,
+                           const float* C, int ldc);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GB300_SGEMM_H */

@@ -1,0 +1,106 @@
+"""The C ABI boundary on the host: the library loads, exports every declared
+symbol, and rejects bad arguments before touching a GPU (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from dense_fp32_gemm_f32_gb300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    names = []
+    for h in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if not h.endswith(".h"):
+            continue
+        text = open(os.path.join(ROOT, "include", h)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        # function declarations: "<type> name(" at statement start
+        names += re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(sgemm_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_headers_declare_the_abi():
+    names = declared_functions()
+    for required in ("sgemm_f32", "sgemm_3xtf32", "sgemm_f32_ex", "sgemm_check_status", "sgemm_status_string"):
+        assert required in names
+    assert set(names) == set(_lib.SIGNATURES), "binding signatures and headers disagree"
+
+
+def test_library_exports_every_declared_symbol():
+    lib = _lib.load()
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def test_status_strings():
+    lib = _lib.load()
+    assert lib.sgemm_status_string(0) == b"ok"
+    assert lib.sgemm_status_string(_lib.ERR_INVALID_ARG) == b"invalid argument"
+    assert lib.sgemm_status_string(_lib.ERR_TIMEOUT) == b"kernel wait timed out"
+    assert lib.sgemm_status_string(12345) == b"unknown status"
+
+
+FAKE_A, FAKE_B, FAKE_C = 0x10000000, 0x20000000, 0x30000000  # never dereferenced
+
+
+@pytest.mark.parametrize("fn", ["sgemm_f32", "sgemm_3xtf32"])
+@pytest.mark.parametrize(
+    "args",
+    [
+        (-1, 4, 4, FAKE_A, 4, FAKE_B, 4, FAKE_C, 4),  # negative M
+        (4, -1, 4, FAKE_A, 4, FAKE_B, 4, FAKE_C, 4),  # negative N
+        (4, 4, -1, FAKE_A, 4, FAKE_B, 4, FAKE_C, 4),  # negative K
+        (4, 4, 8, FAKE_A, 7, FAKE_B, 4, FAKE_C, 4),  # lda < K
+        (4, 8, 4, FAKE_A, 4, FAKE_B, 7, FAKE_C, 8),  # ldb < N
+        (4, 8, 4, FAKE_A, 4, FAKE_B, 8, FAKE_C, 7),  # ldc < N
+        (4, 4, 4, 0, 4, FAKE_B, 4, FAKE_C, 4),  # A NULL
+        (4, 4, 4, FAKE_A, 4, 0, 4, FAKE_C, 4),  # B NULL
+        (4, 4, 4, FAKE_A, 4, FAKE_B, 4, 0, 4),  # C NULL
+        (4, 4, 4, FAKE_A, 4, FAKE_B, 4, FAKE_A + 32, 4),  # C overlaps A
+        (4, 4, 4, FAKE_A, 4, FAKE_B, 4, FAKE_B - 16, 4),  # C overlaps B
+        (65535 * 128 + 1, 4, 4, FAKE_A, 4, FAKE_B, 4, FAKE_C, 4),  # M beyond grid limit
+    ],
+)
+def test_invalid_arguments_rejected_on_host(fn, args):
+    lib = _lib.load()
+    assert getattr(lib, fn)(*args, None) == _lib.ERR_INVALID_ARG
+
+
+def test_empty_output_is_a_noop_without_device():
+    lib = _lib.load()
+    # M == 0 or N == 0: nothing to do, returns OK without any CUDA call
+    assert lib.sgemm_f32(0, 4, 4, FAKE_A, 4, FAKE_B, 4, FAKE_C, 4, None) == _lib.OK
+    assert lib.sgemm_f32(4, 0, 4, FAKE_A, 4, FAKE_B, 0, FAKE_C, 0, None) == _lib.OK
+    # NULL operands are fine when they are empty
+    assert lib.sgemm_f32(0, 0, 0, 0, 0, 0, 0, 0, 0, None) == _lib.OK
+
+
+def test_bad_options_rejected():
+    lib = _lib.load()
+    opt = _lib.Options(0, 0, 0, 0, 0, -1, 0)  # negative debug_skip_stage
+    assert lib.sgemm_f32_ex(4, 4, 4, FAKE_A, 4, FAKE_B, 4, FAKE_C, 4, None, ctypes.byref(opt)) == _lib.ERR_INVALID_ARG
+
+
+def test_no_cpu_fallback_without_gpu():
+    """Without a usable GPU a valid call fails loudly instead of computing on the host."""
+    import torch
+
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    lib = _lib.load()
+    rc = lib.sgemm_f32(4, 4, 4, FAKE_A, 4, FAKE_B, 4, FAKE_C, 4, None)
+    assert rc in (_lib.ERR_CUDA, _lib.ERR_UNSUPPORTED)
+
+
+def test_binding_rejects_cpu_tensors():
+    import torch
+
+    import dense_fp32_gemm_f32_gb300 as g
+
+    with pytest.raises(TypeError):
+        g.sgemm_f32(torch.ones(2, 2), torch.ones(2, 2))

@@ -1,0 +1,269 @@
+"""GPU parity: the CUDA library against the CPU oracle, element by element.
+
+Every test goes through the C ABI (via the thin binding) and compares with
+``oracle`` on the same seeded inputs from ``workloads``.  Real-valued inputs
+must satisfy |C - C_oracle| <= 5e-5 * sum_k |A_ik||B_kj| for every element;
+integer-valued inputs must match exactly.
+"""
+import numpy as np
+import pytest
+import torch
+
+import dense_fp32_gemm_f32_gb300 as g
+import oracle
+from parity import check, sample_rows, to_device
+from workloads import PROBLEMS, make_operands, problem_operands
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def cuda_device():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    torch.cuda.set_device(0)
+    yield
+    assert g.check_status() == 0, "a kernel reported a timeout"
+
+
+def run(A, B, *, lda=None, ldb=None, ldc=None, fn=None, **opt):
+    dA = to_device(A, lda)
+    dB = to_device(B, ldb)
+    M, N = A.shape[0], B.shape[1]
+    dC = to_device(torch.full((M, N), float("nan")), ldc)
+    if fn is not None:
+        fn(dA, dB, dC)
+    elif opt:
+        g.sgemm_f32_ex(dA, dB, dC, **opt)
+    else:
+        g.sgemm_f32(dA, dB, dC)
+    torch.cuda.synchronize()
+    return dC.cpu().numpy()
+
+
+# ---------------------------------------------------------------- named problems, every element
+
+FULL = ["square_256", "ragged_1023x1025x1027", "square_1024", "square_2048", "flat_4096x4096x256",
+        "skinny_8192x128x8192", "skinny_128x8192x16384"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_named_problem_every_element(name):
+    p = PROBLEMS[name]
+    A, B = problem_operands(p)
+    C = run(A, B)
+    C64, bound = oracle.gemm_f64(A.numpy(), B.numpy())
+    worst = check(C, C64, bound, exact=False, what=name)
+    print(f"{name}: worst |err|/bound = {worst:.3e}")
+
+
+@pytest.mark.parametrize("name", ["square_256"] + FULL[1:])
+def test_named_problem_integer_exact(name):
+    p = PROBLEMS[name].int_variant()
+    A, B = problem_operands(p)
+    C = run(A, B)
+    C64, _ = oracle.gemm_f64(A.numpy(), B.numpy(), with_bound=False)
+    check(C, C64, None, exact=True, what=p.name)
+
+
+@pytest.mark.parametrize("name", ["square_4096", "square_8192"])
+@pytest.mark.parametrize("dist", ["real", "int"])
+def test_named_problem_sampled_rows(name, dist):
+    """Full-size launch as timed by the benchmark; whole rows on every tile edge
+    plus random rows are recomputed by the oracle."""
+    p = PROBLEMS[name] if dist == "real" else PROBLEMS[name].int_variant()
+    A, B = problem_operands(p)
+    C = run(A, B)
+    rows = sample_rows(p.M, n_random=8, seed=p.seed)
+    C64, bound = oracle.gemm_rows_f64(A.numpy(), B.numpy(), rows)
+    check(C[rows], C64, bound, exact=(dist == "int"), what=f"{p.name} rows")
+    # and single entries on the last columns of every sampled row's neighbours
+    ii = np.repeat(rows, 4)
+    jj = np.tile(np.array([0, 127, 128, p.N - 1]), rows.size)
+    ce, be = oracle.gemm_entries_f64(A.numpy(), B.numpy(), ii, jj)
+    check(C[ii, jj][None, :], ce[None, :], be[None, :], exact=(dist == "int"), what=f"{p.name} entries")
+
+
+# ---------------------------------------------------------------- every forced variant
+
+VARIANTS = (
+    [dict(producer=1, math=m, stages=s, split_k=1, multicast=1) for m in (1, 2) for s in (1, 2, 3, 4, 5, 6)]
+    + [dict(producer=1, math=m, multicast=2, split_k=1) for m in (1, 2)]
+    + [dict(producer=1, math=2, multicast=2, split_k=1, stages=s) for s in (2, 6)]
+    + [dict(producer=pr, math=m, split_k=s, multicast=1) for pr in (1, 2) for m in (1, 2) for s in (2, 3, 4, 8)]
+    + [dict(producer=2, math=m, stages=s, split_k=1) for m in (1, 2) for s in (2, 4)]
+)
+
+
+def _vid(v):
+    return "-".join(f"{k}{v[k]}" for k in sorted(v))
+
+
+@pytest.mark.parametrize("opt", VARIANTS, ids=_vid)
+def test_forced_variant(opt):
+    # 300 x 500 x 700: ragged against every tile size, several tiles per axis,
+    # 22 K slices (uneven over every split), 16-byte aligned rows (TMA allowed).
+    A, B = make_operands(300, 500, 700, "uniform", 31)
+    C = run(A, B, **opt)
+    C64, bound = oracle.gemm_f64(A.numpy(), B.numpy())
+    check(C, C64, bound, exact=False, what=_vid(opt))
+    Ai, Bi = make_operands(300, 500, 700, "int", 32)
+    Ci = run(Ai, Bi, **opt)
+    check(Ci, oracle.gemm_f64(Ai.numpy(), Bi.numpy(), with_bound=False)[0], None, exact=True, what=_vid(opt) + " int")
+
+
+def test_forced_tma_rejects_unaligned_rows():
+    A, B = make_operands(64, 64, 63, "uniform", 1)
+    with pytest.raises(g.SgemmError) as e:
+        run(A, B, producer=1)
+    assert e.value.status == 1
+
+
+# ---------------------------------------------------------------- ragged shapes, edges, layouts
+
+def test_ragged_shapes_sweep():
+    rng = np.random.default_rng(1234)
+    for t in range(24):
+        M, N, K = (int(x) for x in rng.integers(1, 301, size=3))
+        A, B = make_operands(M, N, K, "normal", 500 + t)
+        C = run(A, B)
+        C64, bound = oracle.gemm_f64(A.numpy(), B.numpy())
+        check(C, C64, bound, exact=False, what=f"{M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("shape", [(1, 1, 1), (1, 1, 10000), (1, 300, 7), (300, 1, 7), (129, 127, 1), (5, 3, 2),
+                                   (128, 128, 32), (129, 129, 33), (256, 256, 8192)])
+def test_small_and_degenerate_shapes(shape):
+    M, N, K = shape
+    A, B = make_operands(M, N, K, "uniform", 77)
+    C = run(A, B)
+    C64, bound = oracle.gemm_f64(A.numpy(), B.numpy())
+    check(C, C64, bound, exact=False, what=str(shape))
+
+
+def test_k_zero_writes_zeros():
+    A = torch.empty((37, 0))
+    B = torch.empty((0, 45))
+    C = run(A, B)
+    assert np.array_equal(C, np.zeros((37, 45), np.float32))
+
+
+@pytest.mark.parametrize("shape", [(0, 5, 3), (5, 0, 3), (0, 0, 0)])
+def test_empty_output_leaves_memory_untouched(shape):
+    M, N, K = shape
+    dA = torch.ones((M, K), device="cuda")
+    dB = torch.ones((K, N), device="cuda")
+    guard = torch.full((16,), 7.0, device="cuda")
+    dC = guard[:0].view(M, N) if M * N == 0 else None
+    g.sgemm_f32(dA, dB, dC)
+    torch.cuda.synchronize()
+    assert torch.all(guard == 7.0)
+
+
+def test_leading_dimensions_and_guard_bands():
+    """Padded rows hold NaN (never read); C's row padding and the floats around
+    C hold a sentinel (never written)."""
+    M, N, K = 200, 150, 90
+    A, B = make_operands(M, N, K, "uniform", 8)
+    lda, ldb, ldc = 96, 156, 160
+    dA, dB = to_device(A, lda), to_device(B, ldb)
+    sentinel = -12345.0
+    guard = 64
+    store = torch.full((guard + M * ldc + guard,), sentinel, device="cuda")
+    dC = store[guard:guard + M * ldc].view(M, ldc)[:, :N]
+    g.sgemm_f32(dA, dB, dC)
+    torch.cuda.synchronize()
+    C64, bound = oracle.gemm_f64(A.numpy(), B.numpy())
+    check(dC.cpu().numpy(), C64, bound, exact=False, what="padded")
+    s = store.cpu().numpy()
+    assert np.all(s[:guard] == sentinel) and np.all(s[-guard:] == sentinel)
+    pad = store[guard:guard + M * ldc].view(M, ldc)[:, N:].cpu().numpy()
+    assert np.all(pad == sentinel)
+
+
+@pytest.mark.parametrize("offsets", [(1, 0), (0, 3), (2, 1)])
+def test_unaligned_bases(offsets):
+    """Bases that are not 16-byte aligned take the cp.async producer."""
+    oa, ob = offsets
+    M, N, K = 190, 170, 260
+    A, B = make_operands(M, N, K, "uniform", 9)
+    dA, dB = to_device(A, offset=oa), to_device(B, offset=ob)
+    assert g.describe(dA, dB).startswith("cpasync")
+    C = g.sgemm_f32(dA, dB)
+    torch.cuda.synchronize()
+    C64, bound = oracle.gemm_f64(A.numpy(), B.numpy())
+    check(C.cpu().numpy(), C64, bound, exact=False, what=f"offsets {offsets}")
+
+
+def test_unaligned_output():
+    M, N, K = 70, 90, 50
+    A, B = make_operands(M, N, K, "uniform", 10)
+    store = torch.full((1 + M * N,), float("nan"), device="cuda")
+    dC = store[1:].view(M, N)
+    g.sgemm_f32(to_device(A), to_device(B), dC)
+    torch.cuda.synchronize()
+    C64, bound = oracle.gemm_f64(A.numpy(), B.numpy())
+    check(dC.cpu().numpy(), C64, bound, exact=False, what="unaligned C")
+
+
+def test_split_k_is_deterministic():
+    A, B = make_operands(256, 256, 8192, "normal", 11)
+    dA, dB = to_device(A), to_device(B)
+    outs = []
+    for _ in range(3):
+        C = g.sgemm_f32_ex(dA, dB, split_k=4)
+        torch.cuda.synchronize()
+        outs.append(C.cpu().numpy())
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[0], outs[2])
+
+
+def test_side_streams():
+    A, B = make_operands(384, 320, 448, "uniform", 12)
+    dA, dB = to_device(A), to_device(B)
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    C1 = torch.empty((384, 320), device="cuda")
+    C2 = torch.empty((384, 320), device="cuda")
+    s1.wait_stream(torch.cuda.current_stream())
+    s2.wait_stream(torch.cuda.current_stream())
+    g.sgemm_f32(dA, dB, C1, stream=s1)
+    g.sgemm_f32_ex(dA, dB, C2, stream=s2, split_k=2)
+    s1.synchronize()
+    s2.synchronize()
+    C64, bound = oracle.gemm_f64(A.numpy(), B.numpy())
+    check(C1.cpu().numpy(), C64, bound, exact=False, what="stream 1")
+    check(C2.cpu().numpy(), C64, bound, exact=False, what="stream 2")
+
+
+def test_host_buffer_entry():
+    A, B = make_operands(130, 260, 390, "uniform", 13)
+    C = g.sgemm_f32_host(A.pin_memory(), B.pin_memory())
+    C64, bound = oracle.gemm_f64(A.numpy(), B.numpy())
+    check(C.numpy(), C64, bound, exact=False, what="host buffers")
+
+
+def test_variant_choice():
+    def desc(M, N, K):
+        return g.describe(torch.empty((M, K), device="cuda"), torch.empty((K, N), device="cuda"))
+
+    assert desc(4096, 4096, 4096).startswith("tma/")
+    assert "/s1/" in desc(4096, 4096, 4096)
+    assert "/s1/" not in desc(8192, 128, 8192)  # skinny output: split-K
+    assert "/s1/" not in desc(128, 8192, 16384)
+    assert desc(1023, 1025, 1027).startswith("cpasync/")  # 1027-float rows are not 16-byte multiples
+
+
+# ---------------------------------------------------------------- bounded waits
+
+def test_timeout_is_reported_and_recovers():
+    """The producer of one CTA skips a K slice; its consumers' bounded wait
+    expires, the kernel returns, and the status word says so.  The next call is
+    unaffected."""
+    A, B = make_operands(128, 256, 256, "uniform", 14)
+    dA, dB = to_device(A), to_device(B)
+    assert g.check_status() == 0
+    for producer in (1, 2):
+        g.sgemm_f32_ex(dA, dB, producer=producer, split_k=1, debug_skip_stage=3, timeout_ns=20_000_000)
+        assert g.check_status() == 4
+    C = g.sgemm_f32(dA, dB)
+    assert g.check_status() == 0
+    C64, bound = oracle.gemm_f64(A.numpy(), B.numpy())
+    check(C.cpu().numpy(), C64, bound, exact=False, what="after timeout")
