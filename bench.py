@@ -2,6 +2,7 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload NAME]
+    python bench.py --sweep [--workload NAME ...]   # ablation table, one JSON line per run
 
 One step is one C = A x B call on the named workload (default: the square
 4096^3 problem with standard-normal inputs, seed 3).  Inputs are resident in
@@ -365,6 +366,63 @@ def run_ours(args, rank, world, local_rank):
     return 0
 
 
+SWEEP_OPTIONS = [
+    {},
+    {"math": 1},
+    {"multicast": 2},
+    {"stages": 1},
+    {"stages": 2},
+    {"stages": 6},
+    {"producer": 2},
+    {"split_k": 1},
+    {"split_k": 2},
+    {"split_k": 4},
+    {"split_k": 8},
+]
+
+
+def run_sweep(args):
+    """Ablations: every named workload x the forced variants of sgemm_f32_ex.
+    Median of ``--steps`` event-timed launches, L2 flushed before each."""
+    import torch
+
+    import dense_fp32_gemm_f32_gb300 as g
+
+    torch.cuda.set_device(0)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    names = args.sweep_workloads or [n for n in PROBLEMS if not n.endswith("_int")]
+    for name in names:
+        p = PROBLEMS[name]
+        A_cpu, B_cpu = problem_operands(p)
+        A, B = A_cpu.cuda(), B_cpu.cuda()
+        C = torch.empty((p.M, p.N), dtype=torch.float32, device="cuda")
+        for opt in SWEEP_OPTIONS:
+            try:
+                run = (lambda: g.sgemm_f32_ex(A, B, C, **opt)) if opt else (lambda: g.sgemm_f32(A, B, C))
+                for _ in range(3):
+                    run()
+                torch.cuda.synchronize()
+                ts = []
+                for i in range(args.steps):
+                    flush.fill_(float(i))
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record()
+                    run()
+                    e1.record()
+                    e1.synchronize()
+                    ts.append(e0.elapsed_time(e1))
+                assert g.check_status() == 0
+                ms = statistics.median(ts)
+                tf = p.flops / (ms / 1e3) / 1e12
+                rec = {"workload": name, "options": opt, "ms": ms, "tflops": tf,
+                       "frac_of_derived_peak": tf / DERIVED_FP32_PEAK_TFLOPS}
+            except Exception as e:  # an option the shape does not allow
+                rec = {"workload": name, "options": opt, "error": str(e)}
+            print(json.dumps(rec), flush=True)
+        del A, B, C
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -372,10 +430,14 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(PROBLEMS), default=DEFAULT_WORKLOAD)
+    ap.add_argument("--sweep", action="store_true", help="print the ablation table instead")
+    ap.add_argument("--sweep-workloads", nargs="*", choices=sorted(PROBLEMS), default=None)
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     rank, world, local_rank = dist_env()
+    if args.sweep:
+        return run_sweep(args)
     if world > 1:
         import torch.distributed as dist
 

@@ -223,19 +223,17 @@ int make_plan(const DeviceState& st, int M, int N, int K, const float* A, int ld
     }
     if (pl.split > 1 && pl.stages < 2) return SGEMM_ERR_INVALID_ARG;  // partial tile needs 64 KiB of ring
 
-    // Multicast pairs along N: only without split, with a TMA producer, and
-    // only when pairing leaves no SM idle.
+    // Multicast pairs along N (TMA producer, no split).  Measured on GB300 at
+    // 1024^3..8192^3 the pairing costs more (the two CTAs release every slot
+    // in lock step) than the halved L2->SM traffic for A saves, so it is off
+    // unless forced.
     const int want_mc = opt ? opt->multicast : 0;
     if (want_mc == 2) {
         if (pl.split > 1 || pl.producer != kProducerTma) return SGEMM_ERR_INVALID_ARG;
+        if (2LL * st.max_clusters_pair < 2) return SGEMM_ERR_UNSUPPORTED;
         pl.mcast = 2;
-    } else if (want_mc == 1) {
+    } else if (want_mc == 0 || want_mc == 1) {
         pl.mcast = 1;
-    } else if (want_mc == 0) {
-        pl.mcast = (pl.split == 1 && pl.producer == kProducerTma && tiles_n >= 2 &&
-                    2LL * st.max_clusters_pair >= st.sm_count)
-                       ? 2
-                       : 1;
     } else {
         return SGEMM_ERR_INVALID_ARG;
     }
