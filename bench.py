@@ -378,6 +378,7 @@ SWEEP_OPTIONS = [
     {"split_k": 2},
     {"split_k": 4},
     {"split_k": 8},
+    {"tail_split": 4},
 ]
 
 

@@ -39,6 +39,7 @@ class Options(ctypes.Structure):
         ("stages", _i),
         ("debug_skip_stage", _i),
         ("timeout_ns", _u64),
+        ("tail_split", _i),
     ]
 
 

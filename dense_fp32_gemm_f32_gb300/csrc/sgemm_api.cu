@@ -24,7 +24,6 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;  // 2 s per wait
-constexpr long long kMaxGridY = 65535;
 
 struct DeviceState {
     std::once_flag once;
@@ -146,21 +145,31 @@ int validate(int M, int N, int K, const float* A, int lda, const float* B, int l
     if (M > 0 && K > 0 && !A) return SGEMM_ERR_INVALID_ARG;
     if (K > 0 && N > 0 && !B) return SGEMM_ERR_INVALID_ARG;
     if (M > 0 && N > 0 && !C) return SGEMM_ERR_INVALID_ARG;
-    if (static_cast<long long>(M) > kMaxGridY * kBM) return SGEMM_ERR_INVALID_ARG;
+    // Output tiles are numbered with a 32-bit int.
+    if (((static_cast<long long>(M) + kBM - 1) / kBM) * (((static_cast<long long>(N) + kBN - 1) / kBN) + 1) >
+        0x7fffffffLL)
+        return SGEMM_ERR_INVALID_ARG;
     const size_t cb = span_bytes(M, N, ldc);
     if (ranges_overlap(C, cb, A, span_bytes(M, K, lda)) || ranges_overlap(C, cb, B, span_bytes(K, N, ldb)))
         return SGEMM_ERR_INVALID_ARG;
     return SGEMM_OK;
 }
 
+struct Launch {
+    int tile_base = 0;  // first output tile
+    int tiles = 0;      // output tiles in this launch (grid x)
+    int split = 1;      // CTAs per tile along K (cluster z)
+};
+
 struct Plan {
     int producer = kProducerTma;
     int math = kMathFfma2;
     int stages = 4;
-    int split = 1;
     int mcast = 1;
-    int grid_x = 0, grid_y = 0;
+    int tiles_n = 0;  // tiles per row of tiles (padded to even for multicast pairs)
     int num_k_tiles = 0;
+    int nlaunch = 1;
+    Launch launch[2];
 };
 
 long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
@@ -204,11 +213,14 @@ int make_plan(const DeviceState& st, int M, int N, int K, const float* A, int ld
         pl.stages = 4;
     }
 
-    // Split-K: pick s in 1..8 minimising (waves of clusters) x (K tiles per CTA).
+    // Split-K over the whole grid, only when the tiles do not fill one wave:
+    // pick s in 1..8 minimising (waves of clusters) x (K tiles per CTA).  (With
+    // a wave or more, only the last partial wave is split; see below.)
+    int split = 1;
     if (opt && opt->split_k) {
         if (opt->split_k < 1 || opt->split_k > 8) return SGEMM_ERR_INVALID_ARG;
-        pl.split = opt->split_k;
-    } else {
+        split = opt->split_k;
+    } else if (tiles < st.sm_count) {
         long long best = -1;
         for (int s = 1; s <= 8; ++s) {
             const int slots = st.max_clusters_split[s];
@@ -217,11 +229,11 @@ int make_plan(const DeviceState& st, int M, int N, int K, const float* A, int ld
             const long long cost = ceil_div(tiles, slots) * ceil_div(pl.num_k_tiles, s);
             if (best < 0 || cost < best) {
                 best = cost;
-                pl.split = s;
+                split = s;
             }
         }
     }
-    if (pl.split > 1 && pl.stages < 2) return SGEMM_ERR_INVALID_ARG;  // partial tile needs 64 KiB of ring
+    if (split > 1 && pl.stages < 2) return SGEMM_ERR_INVALID_ARG;  // partial tile needs 64 KiB of ring
 
     // Multicast pairs along N (TMA producer, no split).  Measured on GB300 at
     // 1024^3..8192^3 the pairing costs more (the two CTAs release every slot
@@ -229,17 +241,43 @@ int make_plan(const DeviceState& st, int M, int N, int K, const float* A, int ld
     // unless forced.
     const int want_mc = opt ? opt->multicast : 0;
     if (want_mc == 2) {
-        if (pl.split > 1 || pl.producer != kProducerTma) return SGEMM_ERR_INVALID_ARG;
-        if (2LL * st.max_clusters_pair < 2) return SGEMM_ERR_UNSUPPORTED;
+        if (split > 1 || pl.producer != kProducerTma) return SGEMM_ERR_INVALID_ARG;
+        if (st.max_clusters_pair < 1) return SGEMM_ERR_UNSUPPORTED;
         pl.mcast = 2;
     } else if (want_mc == 0 || want_mc == 1) {
         pl.mcast = 1;
     } else {
         return SGEMM_ERR_INVALID_ARG;
     }
+    pl.tiles_n = static_cast<int>(pl.mcast == 2 ? 2 * ceil_div(tiles_n, 2) : tiles_n);
+    const long long grid_tiles = static_cast<long long>(pl.tiles_n) * tiles_m;
 
-    pl.grid_x = static_cast<int>(pl.mcast == 2 ? 2 * ceil_div(tiles_n, 2) : tiles_n);
-    pl.grid_y = static_cast<int>(tiles_m);
+    // Last partial wave.  When the tiles do not fill a whole number of waves,
+    // the last wave leaves SMs idle for a full tile time.  Those tiles can run
+    // as a second launch split along K (clusters + shared-memory reduction),
+    // so that more CTAs share the tail at 1/s of the work each; the modelled
+    // tail time, in full-K tile times, is ceil(rem / clusters_s) / s.  On
+    // GB300 the measured tail is well above that model (4096^3: 112 tail tiles
+    // split 5 ways made the call 3 % slower; 2048^3: 104 tiles split 4 ways,
+    // 2.6 % faster), so it is taken only when forced (tail_split = 2..8).
+    pl.nlaunch = 1;
+    pl.launch[0].tile_base = 0;
+    pl.launch[0].tiles = static_cast<int>(grid_tiles);
+    pl.launch[0].split = split;
+    const int want_tail = opt ? opt->tail_split : 0;
+    if (want_tail < 0 || want_tail > 8) return SGEMM_ERR_INVALID_ARG;
+    if (split == 1 && pl.mcast == 1 && want_tail > 1 && grid_tiles > st.sm_count) {
+        const long long full = (grid_tiles / st.sm_count) * st.sm_count;
+        const long long rem = grid_tiles - full;
+        // keep at least four K slices per CTA of the tail
+        if (rem > 0 && st.max_clusters_split[want_tail] > 0 && pl.num_k_tiles >= 4 * want_tail) {
+            pl.nlaunch = 2;
+            pl.launch[0].tiles = static_cast<int>(full);
+            pl.launch[1].tile_base = static_cast<int>(full);
+            pl.launch[1].tiles = static_cast<int>(rem);
+            pl.launch[1].split = want_tail;
+        }
+    }
     *out = pl;
     return SGEMM_OK;
 }
@@ -258,9 +296,11 @@ int encode_2d(CUtensorMap* map, const float* base, long long inner, long long ou
 }
 
 const char* describe_plan(const Plan& pl) {
-    static thread_local char buf[96];
-    std::snprintf(buf, sizeof buf, "%s/%s/mc%d/s%d/st%d", pl.producer == kProducerTma ? "tma" : "cpasync",
-                  pl.math == kMathFfma2 ? "ffma2" : "ffma", pl.mcast, pl.split, pl.stages);
+    static thread_local char buf[128];
+    int n = std::snprintf(buf, sizeof buf, "%s/%s/mc%d/s%d/st%d", pl.producer == kProducerTma ? "tma" : "cpasync",
+                          pl.math == kMathFfma2 ? "ffma2" : "ffma", pl.mcast, pl.launch[0].split, pl.stages);
+    if (pl.nlaunch > 1 && n > 0 && n < static_cast<int>(sizeof buf))
+        std::snprintf(buf + n, sizeof buf - n, "/tail%d:%d", pl.launch[1].split, pl.launch[1].tiles);
     return buf;
 }
 
@@ -304,29 +344,35 @@ int run_ffma(int M, int N, int K, const float* A, int lda, const float* B, int l
     prm.C = C;
     prm.ldc = ldc;
     prm.num_k_tiles = pl.num_k_tiles;
-    prm.split = pl.split;
     prm.mcast = pl.mcast;
     prm.vec_store = ((reinterpret_cast<uintptr_t>(C) & 15u) == 0 && ldc % 4 == 0) ? 1 : 0;
+    prm.tiles_n = pl.tiles_n;
     prm.skip_stage = opt ? opt->debug_skip_stage : 0;
     prm.timeout_ns = (opt && opt->timeout_ns) ? opt->timeout_ns : kDefaultTimeoutNs;
     prm.status = st->status_word;
 
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(pl.grid_x, pl.grid_y, pl.split);
-    cfg.blockDim = dim3(k.threads, 1, 1);
-    cfg.dynamicSmemBytes = static_cast<size_t>(k.smem_bytes);
-    cfg.stream = static_cast<cudaStream_t>(stream);
-    cudaLaunchAttribute attr;
-    attr.id = cudaLaunchAttributeClusterDimension;
-    attr.val.clusterDim.x = pl.mcast;
-    attr.val.clusterDim.y = 1;
-    attr.val.clusterDim.z = pl.split;
-    cfg.attrs = &attr;
-    cfg.numAttrs = (pl.mcast > 1 || pl.split > 1) ? 1 : 0;
-    void* args[3] = {&tmA, &tmB, &prm};
-    if (cudaLaunchKernelExC(&cfg, k.fn, args) != cudaSuccess) {
-        (void)cudaGetLastError();
-        return SGEMM_ERR_CUDA;
+    for (int l = 0; l < pl.nlaunch; ++l) {
+        const Launch& ln = pl.launch[l];
+        if (ln.tiles <= 0) continue;
+        prm.tile_base = ln.tile_base;
+        prm.split = ln.split;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(ln.tiles), 1, static_cast<unsigned>(ln.split));
+        cfg.blockDim = dim3(k.threads, 1, 1);
+        cfg.dynamicSmemBytes = static_cast<size_t>(k.smem_bytes);
+        cfg.stream = static_cast<cudaStream_t>(stream);
+        cudaLaunchAttribute attr;
+        attr.id = cudaLaunchAttributeClusterDimension;
+        attr.val.clusterDim.x = pl.mcast;
+        attr.val.clusterDim.y = 1;
+        attr.val.clusterDim.z = ln.split;
+        cfg.attrs = &attr;
+        cfg.numAttrs = (pl.mcast > 1 || ln.split > 1) ? 1 : 0;
+        void* args[3] = {&tmA, &tmB, &prm};
+        if (cudaLaunchKernelExC(&cfg, k.fn, args) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return SGEMM_ERR_CUDA;
+        }
     }
     return SGEMM_OK;
 }

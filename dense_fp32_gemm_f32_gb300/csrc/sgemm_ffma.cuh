@@ -76,6 +76,8 @@ struct FfmaParams {
     int split;             // CTAs per cluster along K (== gridDim.z); 1 = no split
     int mcast;             // 2 = pairs of CTAs along N share A by multicast; 1 = off
     int vec_store;         // C base 16-byte aligned and ldc % 4 == 0
+    int tile_base;         // linear index of this launch's first output tile
+    int tiles_n;           // output tiles per row of tiles (even when mcast == 2)
     int skip_stage;        // debug: CTA (0,0,0)'s producer never issues K-slice skip_stage-1
     unsigned long long timeout_ns;
     unsigned int* status;  // per-device sticky status word (error bits)
@@ -117,10 +119,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int mcast = p.mcast;
     const uint32_t crank = (split > 1 || mcast > 1) ? cluster_ctarank() : 0u;
 
-    // Tile coordinates.  gridDim.x runs over N tiles (the multicast pairs are
-    // neighbours along x), gridDim.y over M tiles, gridDim.z over K splits.
-    const int n0 = blockIdx.x * kBN;
-    const int m0 = blockIdx.y * kBM;
+    // Tile coordinates.  gridDim.x runs over output tiles, row of tiles by row
+    // of tiles starting at tile_base (neighbours along x share the rows of A:
+    // the multicast pairs, and the A tiles they reuse from L2); gridDim.z runs
+    // over K splits.
+    const int tile = p.tile_base + static_cast<int>(blockIdx.x);
+    const int n0 = (tile % p.tiles_n) * kBN;
+    const int m0 = (tile / p.tiles_n) * kBM;
     const int kz = (split > 1) ? static_cast<int>(blockIdx.z) : 0;
     const int kt_begin = static_cast<int>((static_cast<long long>(p.num_k_tiles) * kz) / split);
     const int kt_end = static_cast<int>((static_cast<long long>(p.num_k_tiles) * (kz + 1)) / split);
@@ -147,7 +152,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     bool timed_out = false;
     const unsigned long long tmo = p.timeout_ns;
-    const bool skip_here = p.skip_stage > 0 && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0;
+    const bool skip_here = p.skip_stage > 0 && tile == 0 && blockIdx.z == 0;
 
     // ------------------------------------------------------------ producer
     if (is_producer) {
@@ -230,11 +235,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // ------------------------------------------------------------ consumers
-    // Warp layout: 4 (M) x 2 (N) warps of 32 x 64; lane layout 4 (M) x 8 (N).
-    // Thread rows: wm*32 + tm + 4*i (i = 0..7); thread columns:
-    // wn*64 + tn*4 + {0..3} and wn*64 + 32 + tn*4 + {0..3}.
+    // Warp layout: 4 (M) x 2 (N) warps of 32 x 64; each lane owns a 4 x 8
+    // grid position (tm, tn).  Thread rows: wm*32 + tm + 4*i (i = 0..7);
+    // thread columns: wn*64 + tn*4 + {0..3} and wn*64 + 32 + tn*4 + {0..3}.
     // acc[i][q] holds columns (2q, 2q+1) of thread row i: q = 0,1 cover
     // tn*4 + 0..3, q = 2,3 cover 32 + tn*4 + 0..3.
+    //
+    // Per k-group (4 consecutive k) a thread reads 8 A vectors (one per row,
+    // 4 k values each: the TMA lands A with k innermost) and, per k, 2 B
+    // vectors, and issues 128 paired multiply-adds (8 rows x 4 column pairs x
+    // 4 k).
+    //
+    // Lane order.  tm takes lane bits 0 and 2, tn lane bits 1, 3 and 4.
+    // Measured on GB300 (shared-memory wavefronts per 16-byte load, ncu): a
+    // load whose address changes with both lane bit 0 and lane bit 1 costs 4
+    // wavefronts, any other sharing pattern used here costs 2.  With this
+    // order neither the A loads (address set by tm) nor the B loads (set by
+    // tn) vary with both bits, so every fragment load costs 2 wavefronts
+    // instead of 2 (A) and 4 (B) with tn = lane & 7.
     float2 acc[8][4];
 #pragma unroll
     for (int i = 0; i < 8; ++i)
@@ -242,14 +260,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int q = 0; q < 4; ++q) acc[i][q] = make_float2(0.f, 0.f);
 
     const int wm = warp >> 1, wn = warp & 1;
-    const int tm = lane >> 3, tn = lane & 7;
+    const int tm = (lane & 1) | (((lane >> 2) & 1) << 1);
+    const int tn = ((lane >> 1) & 1) | (((lane >> 3) & 1) << 1) | (((lane >> 4) & 1) << 2);
     if (!is_producer) {
         // Byte offsets inside a stage.  A row r = wm*32 + tm + 4i has r mod 8 =
         // tm + 4*(i & 1), so even i share one swizzle key and odd i the other.
         const uint32_t a_row0 = static_cast<uint32_t>((wm * 32 + tm) * 128);
         const uint32_t b_col0 = static_cast<uint32_t>((wn * 64 + tn * 4) * 4);
-        const uint8_t* const smem_a = smem;                          // generic pointers
-        const uint8_t* const smem_b = smem + STAGES * kStageABytes;  // for the vector loads
+        const uint8_t* const smem_a = smem + a_row0;                          // generic pointers
+        const uint8_t* const smem_b = smem + STAGES * kStageABytes + b_col0;  // for the vector loads
 
         for (int it = 0; it < nkt; ++it) {
             const int s = it % STAGES;
@@ -258,8 +277,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 timed_out = true;
                 break;
             }
-            const uint8_t* sa = smem_a + s * kStageABytes + a_row0;
-            const uint8_t* sb = smem_b + s * kStageBBytes + b_col0;
+            const uint8_t* sa = smem_a + s * kStageABytes;
+            const uint8_t* sb = smem_b + s * kStageBBytes;
 #pragma unroll
             for (int kg = 0; kg < kBK / 4; ++kg) {
                 const uint32_t xe = static_cast<uint32_t>(((kg ^ tm) & 7) << 4);
@@ -273,28 +292,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int k = kg * 4 + kk;
                     const float4 b0 = *reinterpret_cast<const float4*>(sb + k * (kBN * 4));
                     const float4 b1 = *reinterpret_cast<const float4*>(sb + k * (kBN * 4) + 128);
+                    const float2 bp[4] = {make_float2(b0.x, b0.y), make_float2(b0.z, b0.w),
+                                          make_float2(b1.x, b1.y), make_float2(b1.z, b1.w)};
+                    // Column pair outermost: each B pair feeds 8 consecutive
+                    // multiply-adds (measured faster than row-outermost order).
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const float av = kk == 0 ? a[i].x : kk == 1 ? a[i].y : kk == 2 ? a[i].z : a[i].w;
-                        if (MATH == kMathFfma2) {
-                            const float2 aa = make_float2(av, av);
-                            acc[i][0] = __ffma2_rn(aa, make_float2(b0.x, b0.y), acc[i][0]);
-                            acc[i][1] = __ffma2_rn(aa, make_float2(b0.z, b0.w), acc[i][1]);
-                            acc[i][2] = __ffma2_rn(aa, make_float2(b1.x, b1.y), acc[i][2]);
-                            acc[i][3] = __ffma2_rn(aa, make_float2(b1.z, b1.w), acc[i][3]);
-                        } else {
-                            acc[i][0].x = fmaf(av, b0.x, acc[i][0].x);
-                            acc[i][0].y = fmaf(av, b0.y, acc[i][0].y);
-                            acc[i][1].x = fmaf(av, b0.z, acc[i][1].x);
-                            acc[i][1].y = fmaf(av, b0.w, acc[i][1].y);
-                            acc[i][2].x = fmaf(av, b1.x, acc[i][2].x);
-                            acc[i][2].y = fmaf(av, b1.y, acc[i][2].y);
-                            acc[i][3].x = fmaf(av, b1.z, acc[i][3].x);
-                            acc[i][3].y = fmaf(av, b1.w, acc[i][3].y);
+                    for (int q = 0; q < 4; ++q)
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const float av = kk == 0 ? a[i].x : kk == 1 ? a[i].y : kk == 2 ? a[i].z : a[i].w;
+                            if (MATH == kMathFfma2) {
+                                acc[i][q] = __ffma2_rn(make_float2(av, av), bp[q], acc[i][q]);
+                            } else {
+                                acc[i][q].x = fmaf(av, bp[q].x, acc[i][q].x);
+                                acc[i][q].y = fmaf(av, bp[q].y, acc[i][q].y);
+                            }
                         }
-                    }
                 }
             }
+            // Every load from stage s has returned (its values were consumed
+            // above): release the slot to the producer(s).
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(empty_bar(s));

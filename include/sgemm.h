@@ -51,17 +51,18 @@ typedef enum sgemm_status {
     SGEMM_ERR_INVALID_ARG = 1,     /* negative size, ld below row width, NULL with
                                       non-empty operand, C overlapping A or B,
                                       size beyond the documented limits, bad option */
-    SGEMM_ERR_UNSUPPORTED = 2,     /* current device is not an sm_100-family GPU
-                                      (compute capability 10.x), or the requested
-                                      variant cannot run on it */
+    SGEMM_ERR_UNSUPPORTED = 2,     /* current device is not compute capability
+                                      10.3 (the library carries sm_103a code
+                                      only), or the requested variant cannot
+                                      run on it */
     SGEMM_ERR_CUDA = 3,            /* a CUDA runtime/driver call or the launch failed */
     SGEMM_ERR_TIMEOUT = 4,         /* a kernel abandoned a bounded wait (see
                                       sgemm_check_status) */
     SGEMM_ERR_NOT_IMPLEMENTED = 5  /* the requested path is not built */
 } sgemm_status;
 
-/* Size limits: M, N, K and the leading dimensions are int (>= 0).  M is also
- * limited to 65535 * 128 rows (grid height).  Larger requests return
+/* Size limits: M, N, K and the leading dimensions are int (>= 0), and the
+ * number of 128 x 128 output tiles must fit in an int.  Larger requests return
  * SGEMM_ERR_INVALID_ARG. */
 
 /*
@@ -69,13 +70,16 @@ typedef enum sgemm_status {
  *
  * The main entry.  Picks the kernel variant itself: TMA-fed when A, B have
  * 16-byte aligned bases and row strides, a cp.async-fed variant otherwise;
- * cluster split-K when the output has too few tiles to fill the GPU; a
- * two-CTA cluster sharing A tiles through TMA multicast otherwise.
+ * cluster split-K when the output has too few tiles to fill the GPU.
+ * (Two-CTA multicast of A and a K-split second launch for the tiles of the
+ * last partial wave are available through sgemm_f32_ex; measured on GB300
+ * neither pays, so neither is chosen automatically.)
  *   M, N, K      problem sizes (>= 0)
  *   A, lda       device pointer to A, row stride in floats (lda >= K)
  *   B, ldb       device pointer to B, row stride in floats (ldb >= N)
  *   C, ldc       device pointer to C, row stride in floats (ldc >= N)
  *   stream       cudaStream_t as void*
+ * One call enqueues one kernel launch.
  */
 int sgemm_f32(int M, int N, int K,
               const float* A, int lda,
@@ -117,6 +121,11 @@ typedef struct sgemm_options {
                              issues its k-th K-slice, so the consumers' bounded
                              wait expires (tests the timeout path) */
     uint64_t timeout_ns;  /* 0 = default (2 s); bound on every in-kernel wait */
+    int tail_split;       /* 0 or 1 = off; 2..8 = run the tiles of the last
+                             partial wave as a second launch split that many
+                             ways along K (only when split_k resolves to 1,
+                             the grid exceeds one wave and K has at least
+                             4 x tail_split slices of 32) */
 } sgemm_options;
 
 /* sgemm_f32 with forced choices.  Same contract; an unsupported combination
@@ -137,8 +146,10 @@ int sgemm_check_status(void* stream);
 const char* sgemm_status_string(int status);
 
 /* Describes the variant sgemm_f32 would launch for these sizes and pointers on
- * the current device, as a static string such as "tma/ffma2/mc2/s1/st4".
- * Host-only; launches nothing. */
+ * the current device, as a thread-local string such as "tma/ffma2/mc1/s1/st4"
+ * (producer / math / multicast / split-K / stages), with "/tailS:T" appended
+ * when T tail tiles run as a second launch split S ways.  Host-only; it
+ * launches nothing, but sets up the current device on first use. */
 const char* sgemm_describe(int M, int N, int K,
                            const float* A, int lda,
                            const float* B, int ldb,

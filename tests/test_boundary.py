@@ -63,7 +63,7 @@ FAKE_A, FAKE_B, FAKE_C = 0x10000000, 0x20000000, 0x30000000  # never dereference
         (4, 4, 4, FAKE_A, 4, FAKE_B, 4, 0, 4),  # C NULL
         (4, 4, 4, FAKE_A, 4, FAKE_B, 4, FAKE_A + 32, 4),  # C overlaps A
         (4, 4, 4, FAKE_A, 4, FAKE_B, 4, FAKE_B - 16, 4),  # C overlaps B
-        (65535 * 128 + 1, 4, 4, FAKE_A, 4, FAKE_B, 4, FAKE_C, 4),  # M beyond grid limit
+        (2**31 - 1, 65536 * 128, 4, FAKE_A, 4, FAKE_B, 65536 * 128, 0x7000000000, 65536 * 128),  # tile count beyond int
     ],
 )
 def test_invalid_arguments_rejected_on_host(fn, args):
@@ -82,7 +82,7 @@ def test_empty_output_is_a_noop_without_device():
 
 def test_bad_options_rejected():
     lib = _lib.load()
-    opt = _lib.Options(0, 0, 0, 0, 0, -1, 0)  # negative debug_skip_stage
+    opt = _lib.Options(0, 0, 0, 0, 0, -1, 0, 0)  # negative debug_skip_stage
     assert lib.sgemm_f32_ex(4, 4, 4, FAKE_A, 4, FAKE_B, 4, FAKE_C, 4, None, ctypes.byref(opt)) == _lib.ERR_INVALID_ARG
 
 

@@ -111,6 +111,22 @@ def test_forced_variant(opt):
     check(Ci, oracle.gemm_f64(Ai.numpy(), Bi.numpy(), with_bound=False)[0], None, exact=True, what=_vid(opt) + " int")
 
 
+@pytest.mark.parametrize("tail", [2, 3, 4, 8])
+def test_tail_split(tail):
+    """169 output tiles (13 x 13) on 152 SMs: one full wave plus 17 tiles that
+    run as a second launch split along K; K = 1040 is ragged (33 K slices)."""
+    M = N = 1664
+    K = 1040
+    A, B = make_operands(M, N, K, "uniform", 41)
+    dA, dB = to_device(A), to_device(B)
+    C = g.sgemm_f32_ex(dA, dB, tail_split=tail).cpu().numpy()
+    C64, bound = oracle.gemm_f64(A.numpy(), B.numpy())
+    check(C, C64, bound, exact=False, what=f"tail {tail}")
+    Ai, Bi = make_operands(M, N, K, "int", 42)
+    Ci = g.sgemm_f32_ex(to_device(Ai), to_device(Bi), tail_split=tail).cpu().numpy()
+    check(Ci, oracle.gemm_f64(Ai.numpy(), Bi.numpy(), with_bound=False)[0], None, exact=True, what=f"tail {tail} int")
+
+
 def test_forced_tma_rejects_unaligned_rows():
     A, B = make_operands(64, 64, 63, "uniform", 1)
     with pytest.raises(g.SgemmError) as e:
@@ -246,6 +262,7 @@ def test_variant_choice():
 
     assert desc(4096, 4096, 4096).startswith("tma/")
     assert "/s1/" in desc(4096, 4096, 4096)
+    assert "/tail" not in desc(4096, 4096, 4096)  # the tail split is opt-in
     assert "/s1/" not in desc(8192, 128, 8192)  # skinny output: split-K
     assert "/s1/" not in desc(128, 8192, 16384)
     assert desc(1023, 1025, 1027).startswith("cpasync/")  # 1027-float rows are not 16-byte multiples
