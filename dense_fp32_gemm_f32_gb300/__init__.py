@@ -18,6 +18,7 @@ __all__ = [
     "sgemm_f32",
     "sgemm_f32_ex",
     "sgemm_3xtf32",
+    "sgemm_3xtf32_ex",
     "sgemm_f32_host",
     "check_status",
     "describe",
@@ -85,6 +86,12 @@ def sgemm_f32_ex(A, B, out=None, *, stream=None, producer=0, split_k=0, multicas
     """sgemm_f32 with forced variant choices (see struct sgemm_options)."""
     opt = Options(producer, split_k, multicast, math, stages, debug_skip_stage, timeout_ns, tail_split)
     return _call("sgemm_f32_ex", A, B, out, stream, opt)
+
+
+def sgemm_3xtf32_ex(A, B, out=None, *, stream=None, debug_skip_stage=0, timeout_ns=0) -> torch.Tensor:
+    """sgemm_3xtf32 with the bounded-wait test options."""
+    opt = Options(0, 0, 0, 0, 0, debug_skip_stage, timeout_ns, 0)
+    return _call("sgemm_3xtf32_ex", A, B, out, stream, opt)
 
 
 def sgemm_f32_host(A: torch.Tensor, B: torch.Tensor, out: torch.Tensor | None = None, *,

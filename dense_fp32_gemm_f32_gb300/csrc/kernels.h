@@ -13,5 +13,7 @@ struct KernelEntry {
 KernelEntry ffma_kernel_tma(int stages, int math);
 // FFMA kernels fed by 4-byte cp.async (any alignment); stages in {2,4}.
 KernelEntry ffma_kernel_cpasync(int stages, int math);
+// Three-product TF32 kernel on the tensor cores (TMA-fed, 128 x 128 tiles).
+KernelEntry tf32x3_kernel();
 
 }  // namespace gb300

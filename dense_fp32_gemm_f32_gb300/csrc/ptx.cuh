@@ -1,8 +1,10 @@
 // Inline-PTX wrappers for the sm_103a features the kernels use: mbarriers,
 // tensor-map bulk copies (TMA) with optional cluster multicast, cp.async with
-// zero fill, cluster ranks / barriers / distributed shared memory, and the
-// global nanosecond timer used to bound every wait.  Each wrapper is written
-// from the PTX ISA description of the instruction it emits.
+// zero fill, cluster ranks / barriers / distributed shared memory, the
+// fifth-generation tensor core (tcgen05: tensor-memory allocation, MMA,
+// commit, tensor-memory loads, fences), TF32 rounding, and the global
+// nanosecond timer used to bound every wait.  Each wrapper is written from the
+// PTX ISA description of the instruction it emits.
 #pragma once
 
 #include <cstdint>
@@ -70,6 +72,13 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
         if (mbar_try_wait(bar, parity)) return true;
         if (global_timer_ns() - t0 > limit_ns) return false;
     }
+}
+
+// Warp-uniform form: every lane of the (converged) warp waits, and all lanes
+// return false if any lane gave up, so the warp leaves its loop together.
+__device__ __forceinline__ bool mbar_wait_bounded_warp(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+    const bool ok = mbar_wait_bounded(bar, parity, limit_ns);
+    return __all_sync(0xffffffffu, ok) != 0;
 }
 
 // ---------------------------------------------------------------- TMA
@@ -160,5 +169,85 @@ __device__ __forceinline__ void sts128(uint32_t addr, float4 v) {
     asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w)
                  : "memory");
 }
+
+// ---------------------------------------------------------------- async proxy
+
+// Makes this thread's generic-proxy writes to shared memory visible to the
+// async proxy (tensor-core operand reads, bulk copies).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ---------------------------------------------------------------- TF32
+
+// Round-to-nearest (ties away from zero) to TF32: the result is a float whose
+// low 13 mantissa bits are zero.
+__device__ __forceinline__ float to_tf32_rna(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return __uint_as_float(r);
+}
+
+// ---------------------------------------------------------------- tcgen05
+
+// Allocates `ncols` (power of two, 32..512) tensor-memory columns for this CTA
+// and writes the base address to shared memory at `slot`.  Whole warp.
+__device__ __forceinline__ void tmem_alloc(uint32_t slot, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot), "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish_alloc_permit() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+// Whole warp.
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before_sync() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_fence_after_sync() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// D[tmem] (+)= A[smem] x B[smem], TF32 inputs, FP32 accumulator.  Issued by one
+// thread; `accumulate` = false overwrites D.
+__device__ __forceinline__ void umma_tf32(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                          bool accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1u : 0u)
+        : "memory");
+}
+
+// The mbarrier at `bar` receives one arrival once every tcgen05 operation
+// this thread issued before has completed.
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+// Loads 32 consecutive 32-bit tensor-memory columns of this thread's lane
+// (shape 32x32b: lane = warp's lane quarter + lane id).  Complete after
+// tmem_wait_ld().
+__device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 }  // namespace gb300

@@ -1,0 +1,269 @@
+// FP32 matrix multiply on the fifth-generation tensor cores (tcgen05), sm_103a,
+// with the three-product TF32 split.
+//
+// C (M x N) = A (M x K) * B (K x N), all row-major float32.
+//
+// Tensor cores have no FP32 multiply-add, but they multiply TF32 values (10
+// explicit mantissa bits) exactly and accumulate in FP32.  Each operand is
+// split into a TF32 "big" part and the TF32 rounding of what is left:
+//     a = a_big + a_small + e_a,  a_big = tf32(a),  a_small = tf32(a - a_big),
+// with |e_a| <= 2^-22 |a|, and the product is taken as
+//     a*b ~ a_small*b_big + a_big*b_small + a_big*b_big,
+// dropping a_small*b_small and the e terms, each below 2^-22 |a||b|: about
+// 1e-6 of sum_k |a||b| in all, far inside the 5e-5 contract.  Integers in
+// {-8..8} are exact in TF32, so their small parts are 0 and the result is
+// exact.  (The pages mention tensor cores only as a future direction of the
+// "Hardware acceleration" page's summary; nothing of this is on the pages.)
+//
+// One CTA computes a 128 x 128 tile of C; 6 warps:
+//   warp 0      TMA producer: A and B K-slices (BK = 32) into 2 raw stages;
+//   warp 1      allocates 128 tensor-memory columns (the FP32 accumulator)
+//               and one lane issues the MMAs: per K-slice 4 k-steps of 8,
+//               three tcgen05.mma.kind::tf32 each (small*big, big*small,
+//               big*big), then tcgen05.commit releases the split stage;
+//   warps 2..5  split the raw K-slice into four K-major, 128-byte-swizzled
+//               TF32 operand tiles (A_big, A_small, B_big, B_small) in 2
+//               split stages (B is transposed on the way: it arrives with n
+//               innermost), then, after the last MMA, read the accumulator
+//               out of tensor memory (tcgen05.ld) and store C.
+//
+// Every wait is bounded by `timeout_ns`; on expiry the thread records the
+// timeout in the status word, stops working, and still reaches the final CTA
+// barrier, after which warp 1 frees the tensor memory.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "ptx.cuh"
+#include "sgemm_3xtf32_params.h"
+
+namespace gb300 {
+
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
+// 128 bytes in groups of 8 that lie 1024 bytes apart.  Start address in bits
+// 0-13 (>> 4), leading byte offset (unused by swizzled K-major) in 16-29,
+// stride byte offset (>> 4) in 32-45, version 1 in 46-47, layout in 61-63.
+__device__ __forceinline__ uint64_t umma_desc_kmajor_sw128(uint32_t saddr) {
+    uint64_t d = static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>(1) << 16;
+    d |= static_cast<uint64_t>(1024 >> 4) << 32;
+    d |= static_cast<uint64_t>(1) << 46;
+    d |= static_cast<uint64_t>(2) << 61;
+    return d;
+}
+
+__device__ __forceinline__ void split_tf32(float x, float& big, float& small) {
+    big = to_tf32_rna(x);
+    small = to_tf32_rna(x - big);  // x - big is exact in FP32
+}
+
+__global__ void __launch_bounds__(kTcThreads, 1)
+    sgemm_3xtf32_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                        const TcParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_base = smem_addr(smem_raw);
+    const uint32_t base = (raw_base + 1023u) & ~1023u;
+    auto rawA = [&](int r) { return base + static_cast<uint32_t>(r * kTcRawABytes); };
+    auto rawB = [&](int r) { return base + static_cast<uint32_t>(kTcRawStages * kTcRawABytes + r * kTcRawBBytes); };
+    auto split = [&](int s) {
+        return base + static_cast<uint32_t>(kTcRawStages * (kTcRawABytes + kTcRawBBytes) + s * kTcSplitBytes);
+    };
+    const uint32_t bars = base + kTcRingBytes;
+    auto raw_full = [&](int r) { return bars + 8u * r; };
+    auto raw_empty = [&](int r) { return bars + 16u + 8u * r; };
+    auto split_full = [&](int s) { return bars + 32u + 8u * s; };
+    auto split_empty = [&](int s) { return bars + 48u + 8u * s; };
+    const uint32_t acc_full = bars + 64u;
+    const uint32_t tmem_slot = bars + 72u;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int tile = static_cast<int>(blockIdx.x);
+    const int n0 = (tile % p.tiles_n) * kTcBN;
+    const int m0 = (tile / p.tiles_n) * kTcBM;
+    const int nkt = p.num_k_tiles;
+    const unsigned long long tmo = p.timeout_ns;
+
+    if (threadIdx.x == 0) {
+        for (int r = 0; r < kTcRawStages; ++r) {
+            mbar_init(raw_full(r), 1);
+            mbar_init(raw_empty(r), 4);  // one arrival per transform warp
+        }
+        for (int s = 0; s < kTcSplitStages; ++s) {
+            mbar_init(split_full(s), 4);
+            mbar_init(split_empty(s), 1);  // tcgen05.commit
+        }
+        mbar_init(acc_full, 1);
+        fence_mbarrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, kTcTmemCols);
+        tmem_relinquish_alloc_permit();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tensormap(&tmA);
+        prefetch_tensormap(&tmB);
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    uint32_t tmem;
+    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(tmem) : "r"(tmem_slot) : "memory");
+
+    bool timed_out = false;
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            int issued_round[kTcRawStages] = {-1, -1};
+            const bool skip_here = p.skip_stage > 0 && tile == 0;
+            for (int kt = 0; kt < nkt; ++kt) {
+                const int r = kt % kTcRawStages;
+                const int round = kt / kTcRawStages;
+                if (round > 0 && !mbar_wait_bounded(raw_empty(r), (round - 1) & 1, tmo)) {
+                    timed_out = true;
+                    break;
+                }
+                if (skip_here && kt == p.skip_stage - 1) continue;
+                mbar_arrive_expect_tx(raw_full(r), kTcRawABytes + kTcRawBBytes);
+                tma_load_2d(rawA(r), &tmA, raw_full(r), kt * kTcBK, m0);
+                tma_load_2d(rawB(r), &tmB, raw_full(r), n0, kt * kTcBK);
+                issued_round[r] = round;
+            }
+            for (int r = 0; r < kTcRawStages; ++r)  // drain: every issued copy has landed
+                if (issued_round[r] >= 0 && !mbar_wait_bounded(raw_full(r), issued_round[r] & 1, tmo))
+                    timed_out = true;
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            for (int kt = 0; kt < nkt; ++kt) {
+                const int s = kt % kTcSplitStages;
+                if (!mbar_wait_bounded(split_full(s), (kt / kTcSplitStages) & 1, tmo)) {
+                    timed_out = true;
+                    break;
+                }
+                tc_fence_after_sync();
+                const uint32_t a_big = split(s), a_small = a_big + kTcOpBytes;
+                const uint32_t b_big = a_big + 2 * kTcOpBytes, b_small = a_big + 3 * kTcOpBytes;
+#pragma unroll
+                for (int kk = 0; kk < kTcBK / 8; ++kk) {  // k-steps of 8 TF32 = 32 bytes of each row
+                    const uint32_t off = static_cast<uint32_t>(kk * 32);
+                    umma_tf32(tmem, umma_desc_kmajor_sw128(a_small + off), umma_desc_kmajor_sw128(b_big + off),
+                              kTcIdesc, kt > 0 || kk > 0);
+                    umma_tf32(tmem, umma_desc_kmajor_sw128(a_big + off), umma_desc_kmajor_sw128(b_small + off),
+                              kTcIdesc, true);
+                    umma_tf32(tmem, umma_desc_kmajor_sw128(a_big + off), umma_desc_kmajor_sw128(b_big + off),
+                              kTcIdesc, true);
+                }
+                umma_commit(split_empty(s));  // stage s is free once these MMAs are done
+            }
+            umma_commit(acc_full);  // arrives when every MMA above has completed
+            if (!mbar_wait_bounded(acc_full, 0, tmo)) timed_out = true;
+        }
+    } else {
+        // ------------------------------------------------------------ split + epilogue
+        const int tt = threadIdx.x - 64;  // 0..127
+        for (int kt = 0; kt < nkt; ++kt) {
+            const int r = kt % kTcRawStages;
+            const int s = kt % kTcSplitStages;
+            if (!mbar_wait_bounded_warp(raw_full(r), (kt / kTcRawStages) & 1, tmo)) {
+                timed_out = true;
+                break;
+            }
+            if (kt >= kTcSplitStages &&
+                !mbar_wait_bounded_warp(split_empty(s), ((kt / kTcSplitStages) - 1) & 1, tmo)) {
+                timed_out = true;
+                break;
+            }
+            const uint32_t a_big = split(s), a_small = a_big + kTcOpBytes;
+            const uint32_t b_big = a_big + 2 * kTcOpBytes, b_small = a_big + 3 * kTcOpBytes;
+            // A: the TMA wrote the slice K-major with the same 128-byte swizzle
+            // the MMA reads, so the split is element-wise on 16-byte chunks.
+#pragma unroll
+            for (int j = 0; j < kTcRawABytes / 16 / 128; ++j) {
+                const uint32_t off = static_cast<uint32_t>((tt + 128 * j) * 16);
+                const float4 v = lds128(rawA(r) + off);
+                float4 hi, lo;
+                split_tf32(v.x, hi.x, lo.x);
+                split_tf32(v.y, hi.y, lo.y);
+                split_tf32(v.z, hi.z, lo.z);
+                split_tf32(v.w, hi.w, lo.w);
+                sts128(a_big + off, hi);
+                sts128(a_small + off, lo);
+            }
+            // B: the slice arrives as 32 rows (k) of 128 floats (n); thread tt
+            // takes column n = tt and writes it as row tt of the K-major tiles:
+            // 16-byte chunk c (k = 4c..4c+3) at chunk position c ^ (tt mod 8).
+            const uint32_t rb = rawB(r) + static_cast<uint32_t>(tt * 4);
+#pragma unroll
+            for (int c = 0; c < kTcBK / 4; ++c) {
+                float x[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    asm volatile("ld.shared.f32 %0, [%1];"
+                                 : "=f"(x[i])
+                                 : "r"(rb + static_cast<uint32_t>((4 * c + i) * kTcBN * 4))
+                                 : "memory");
+                float4 hi, lo;
+                split_tf32(x[0], hi.x, lo.x);
+                split_tf32(x[1], hi.y, lo.y);
+                split_tf32(x[2], hi.z, lo.z);
+                split_tf32(x[3], hi.w, lo.w);
+                const uint32_t off = static_cast<uint32_t>(tt * 128 + (((c ^ tt) & 7) << 4));
+                sts128(b_big + off, hi);
+                sts128(b_small + off, lo);
+            }
+            fence_proxy_async_smem();  // make the tiles visible to the tensor core
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(raw_empty(r));
+                mbar_arrive(split_full(s));
+            }
+        }
+
+        // Epilogue: accumulator row (32 * (warp % 4) + lane) lives in that
+        // tensor-memory lane; 4 loads of 32 columns each.
+        // (timed_out is warp-uniform here: every wait above voted across the warp)
+        if (!timed_out && nkt > 0 && mbar_wait_bounded_warp(acc_full, 0, tmo)) {
+            tc_fence_after_sync();
+            const int q = warp & 3;
+            const int row = m0 + 32 * q + lane;
+            float* crow = p.C + static_cast<long long>(row) * p.ldc;
+#pragma unroll
+            for (int ch = 0; ch < kTcBN / 32; ++ch) {
+                uint32_t v[32];
+                tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(32 * ch), v);
+                tmem_wait_ld();
+                const int col = n0 + 32 * ch;
+                if (row < p.M) {
+                    if (p.vec_store && col + 31 < p.N) {
+#pragma unroll
+                        for (int e = 0; e < 32; e += 4)
+                            *reinterpret_cast<float4*>(crow + col + e) =
+                                make_float4(__uint_as_float(v[e]), __uint_as_float(v[e + 1]),
+                                            __uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            if (col + e < p.N) crow[col + e] = __uint_as_float(v[e]);
+                    }
+                }
+            }
+        } else if (nkt > 0) {
+            timed_out = true;
+        }
+    }
+
+    if (timed_out) atomicOr(p.status, kTcStatusTimeout);
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, kTcTmemCols);
+    }
+}
+
+}  // namespace gb300

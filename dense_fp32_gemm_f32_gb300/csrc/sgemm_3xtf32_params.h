@@ -1,0 +1,42 @@
+// Tile shape, shared-memory budget, instruction descriptor and kernel
+// parameters of the three-product TF32 tensor-core kernel (host and device).
+#pragma once
+
+#include <cstdint>
+
+namespace gb300 {
+
+constexpr int kTcBM = 128;
+constexpr int kTcBN = 128;
+constexpr int kTcBK = 32;
+constexpr int kTcThreads = 192;
+constexpr int kTcRawABytes = kTcBM * kTcBK * 4;  // 16 KiB: TMA A slice, 128-byte swizzled rows
+constexpr int kTcRawBBytes = kTcBK * kTcBN * 4;  // 16 KiB: TMA B slice, 512-byte rows
+constexpr int kTcOpBytes = 128 * kTcBK * 4;      // 16 KiB: one K-major operand tile
+constexpr int kTcSplitBytes = 4 * kTcOpBytes;    // A_big, A_small, B_big, B_small
+constexpr int kTcRawStages = 2;
+constexpr int kTcSplitStages = 2;
+constexpr int kTcTmemCols = 128;
+constexpr unsigned kTcStatusTimeout = 4u;
+constexpr int kTcRingBytes = kTcRawStages * (kTcRawABytes + kTcRawBBytes) + kTcSplitStages * kTcSplitBytes;
+constexpr int kTcSmemBytes = kTcRingBytes + 1024 /*align*/ + 256 /*barriers*/;
+
+// Instruction descriptor of tcgen05.mma.kind::tf32: D FP32 (bits 4-5 = 1),
+// A and B TF32 (bits 7-9 = bits 10-12 = 2), both K-major (bits 15, 16 = 0),
+// N >> 3 in bits 17-22, M >> 4 in bits 24-28.
+constexpr uint32_t kTcIdesc = (1u << 4) | (2u << 7) | (2u << 10) | (static_cast<uint32_t>(kTcBN >> 3) << 17) |
+                              (static_cast<uint32_t>(kTcBM >> 4) << 24);
+
+struct TcParams {
+    int M, N, K;
+    float* C;
+    long long ldc;
+    int num_k_tiles;  // ceil(K / kTcBK)
+    int tiles_n;      // output tiles per row of tiles
+    int vec_store;    // C base 16-byte aligned and ldc % 4 == 0
+    int skip_stage;   // debug: CTA 0's producer never issues K-slice skip_stage-1
+    unsigned long long timeout_ns;
+    unsigned int* status;
+};
+
+}  // namespace gb300

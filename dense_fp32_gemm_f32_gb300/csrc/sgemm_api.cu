@@ -13,6 +13,7 @@
 
 #include "../../include/sgemm.h"
 #include "kernels.h"
+#include "sgemm_3xtf32_params.h"
 #include "sgemm_ffma.cuh"
 
 namespace gb300 {
@@ -105,6 +106,7 @@ int init_device(int dev, DeviceState& st) {
         for (int s = 1; s <= 6; ++s)
             if (set_smem_attr(ffma_kernel_cpasync(s, math)) != SGEMM_OK) return SGEMM_ERR_CUDA;
     }
+    if (set_smem_attr(tf32x3_kernel()) != SGEMM_OK) return SGEMM_ERR_CUDA;
     const KernelEntry ref = ffma_kernel_tma(4, kMathFfma2);
     st.max_clusters_pair = max_active_clusters(ref, 2, 1);
     st.max_clusters_split[1] = st.sm_count;
@@ -377,6 +379,56 @@ int run_ffma(int M, int N, int K, const float* A, int lda, const float* B, int l
     return SGEMM_OK;
 }
 
+int run_3xtf32(int M, int N, int K, const float* A, int lda, const float* B, int ldb, float* C, int ldc,
+               void* stream, const sgemm_options* opt) {
+    int rc = validate(M, N, K, A, lda, B, ldb, C, ldc);
+    if (rc != SGEMM_OK) return rc;
+    if (opt && opt->debug_skip_stage < 0) return SGEMM_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return SGEMM_OK;
+    int dev = 0;
+    DeviceState* st = nullptr;
+    rc = current_device(&dev, &st);
+    if (rc != SGEMM_OK) return rc;
+    // The tensor-core kernel is fed by tensor maps; operands the TMA cannot
+    // read (unaligned bases or row strides), and K == 0, take the FFMA kernel,
+    // which meets the same contract.
+    if (K == 0 || !tma_ok(A, lda) || !tma_ok(B, ldb)) return run_ffma(M, N, K, A, lda, B, ldb, C, ldc, stream, nullptr);
+
+    const KernelEntry k = tf32x3_kernel();
+    alignas(64) CUtensorMap tmA;
+    alignas(64) CUtensorMap tmB;
+    rc = encode_2d(&tmA, A, K, M, lda, kTcBK, kTcBM, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (rc == SGEMM_OK) rc = encode_2d(&tmB, B, N, K, ldb, kTcBN, kTcBK, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (rc != SGEMM_OK) return rc;
+
+    TcParams prm;
+    prm.M = M;
+    prm.N = N;
+    prm.K = K;
+    prm.C = C;
+    prm.ldc = ldc;
+    prm.num_k_tiles = static_cast<int>(ceil_div(K, kTcBK));
+    prm.tiles_n = static_cast<int>(ceil_div(N, kTcBN));
+    prm.vec_store = ((reinterpret_cast<uintptr_t>(C) & 15u) == 0 && ldc % 4 == 0) ? 1 : 0;
+    prm.skip_stage = opt ? opt->debug_skip_stage : 0;
+    prm.timeout_ns = (opt && opt->timeout_ns) ? opt->timeout_ns : kDefaultTimeoutNs;
+    prm.status = st->status_word;
+    const long long tiles = ceil_div(M, kTcBM) * static_cast<long long>(prm.tiles_n);
+
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(tiles), 1, 1);
+    cfg.blockDim = dim3(k.threads, 1, 1);
+    cfg.dynamicSmemBytes = static_cast<size_t>(k.smem_bytes);
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    cfg.numAttrs = 0;
+    void* args[3] = {&tmA, &tmB, &prm};
+    if (cudaLaunchKernelExC(&cfg, k.fn, args) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return SGEMM_ERR_CUDA;
+    }
+    return SGEMM_OK;
+}
+
 }  // namespace
 }  // namespace gb300
 
@@ -396,10 +448,12 @@ int sgemm_f32_ex(int M, int N, int K, const float* A, int lda, const float* B, i
 
 int sgemm_3xtf32(int M, int N, int K, const float* A, int lda, const float* B, int ldb, float* C, int ldc,
                  void* stream) {
-    (void)stream;
-    const int rc = validate(M, N, K, A, lda, B, ldb, C, ldc);
-    if (rc != SGEMM_OK) return rc;
-    return SGEMM_ERR_NOT_IMPLEMENTED;
+    return run_3xtf32(M, N, K, A, lda, B, ldb, C, ldc, stream, nullptr);
+}
+
+int sgemm_3xtf32_ex(int M, int N, int K, const float* A, int lda, const float* B, int ldb, float* C, int ldc,
+                    void* stream, const sgemm_options* opt) {
+    return run_3xtf32(M, N, K, A, lda, B, ldb, C, ldc, stream, opt);
 }
 
 int sgemm_check_status(void* stream) {

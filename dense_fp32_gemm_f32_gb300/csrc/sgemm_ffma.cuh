@@ -37,7 +37,7 @@
 // Every wait is bounded by `timeout_ns` of global time; a thread that gives up
 // records SGEMM_ERR_TIMEOUT in the device status word, stops computing, and
 // still takes part in every CTA/cluster barrier so that no other thread waits
-// forever.
+// forever.  Waits made by whole warps vote, so a warp leaves its loop as one.
 #pragma once
 
 #include <cuda.h>
@@ -195,7 +195,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int it = 0; it < nkt; ++it) {
                 const int s = it % STAGES;
                 const int round = it / STAGES;
-                if (round > 0 && !mbar_wait_bounded(empty_bar(s), (round - 1) & 1, tmo)) {
+                if (round > 0 && !mbar_wait_bounded_warp(empty_bar(s), (round - 1) & 1, tmo)) {
                     timed_out = true;
                     break;
                 }
@@ -273,7 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int it = 0; it < nkt; ++it) {
             const int s = it % STAGES;
             const int round = it / STAGES;
-            if (!mbar_wait_bounded(full_bar(s), round & 1, tmo)) {
+            if (!mbar_wait_bounded_warp(full_bar(s), round & 1, tmo)) {
                 timed_out = true;
                 break;
             }

@@ -89,10 +89,14 @@ int sgemm_f32(int M, int N, int K,
 
 /*
  * sgemm_3xtf32 -- same operation, signature, accuracy contract and error
- * behaviour as sgemm_f32, computed on the tensor cores: each operand is split
- * into a TF32 "big" part and a TF32 "small" remainder and three TF32 products
- * (small*big + big*small + big*big) are accumulated in float32.  Returns
- * SGEMM_ERR_NOT_IMPLEMENTED while that path is not built.
+ * behaviour as sgemm_f32, computed on the tensor cores (tcgen05): each operand
+ * is split into a TF32 "big" part, big = tf32(x), and a TF32 "small" part,
+ * small = tf32(x - big), and three TF32 products (small*big + big*small +
+ * big*big) are accumulated in float32 in tensor memory.  The dropped terms
+ * are below 2^-22 |a||b| each.  Needs TMA-readable operands (16-byte aligned
+ * bases and row strides) and K > 0; other calls run the sgemm_f32 kernels.
+ * Tensor cores are not on the pages' own path; this entry is reported
+ * separately from sgemm_f32.
  */
 int sgemm_3xtf32(int M, int N, int K,
                  const float* A, int lda,
@@ -135,6 +139,14 @@ int sgemm_f32_ex(int M, int N, int K,
                  const float* B, int ldb,
                  float* C, int ldc,
                  void* stream, const sgemm_options* opt);
+
+/* sgemm_3xtf32 with the debug_skip_stage and timeout_ns fields of `opt` (the
+ * other fields are ignored).  For tests of the bounded-wait path. */
+int sgemm_3xtf32_ex(int M, int N, int K,
+                    const float* A, int lda,
+                    const float* B, int ldb,
+                    float* C, int ldc,
+                    void* stream, const sgemm_options* opt);
 
 /* Synchronises `stream`, then returns and clears the current device's status
  * word: SGEMM_OK, or SGEMM_ERR_TIMEOUT if any kernel since the last check gave

@@ -1,0 +1,128 @@
+"""GPU parity of the tensor-core entry (sgemm_3xtf32) against the CPU oracle.
+
+Same contract as sgemm_f32: |C - C_oracle| <= 5e-5 * sum_k |A_ik||B_kj| for
+every element on real-valued inputs, exact equality on integer-valued inputs.
+"""
+import numpy as np
+import pytest
+import torch
+
+import dense_fp32_gemm_f32_gb300 as g
+import oracle
+from parity import check, sample_rows, to_device
+from workloads import PROBLEMS, make_operands, problem_operands
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def cuda_device():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    torch.cuda.set_device(0)
+    yield
+    assert g.check_status() == 0, "a kernel reported a timeout"
+
+
+def run(A, B, *, lda=None, ldb=None, ldc=None):
+    dA = to_device(A, lda)
+    dB = to_device(B, ldb)
+    dC = to_device(torch.full((A.shape[0], B.shape[1]), float("nan")), ldc)
+    g.sgemm_3xtf32(dA, dB, dC)
+    torch.cuda.synchronize()
+    return dC.cpu().numpy()
+
+
+def test_one_tile_first():
+    """One 128 x 128 tile, one K slice: the smallest launch of the kernel."""
+    A, B = make_operands(128, 128, 32, "uniform", 50)
+    C64, bound = oracle.gemm_f64(A.numpy(), B.numpy())
+    check(run(A, B), C64, bound, exact=False, what="128x128x32")
+    Ai, Bi = make_operands(128, 128, 32, "int", 51)
+    check(run(Ai, Bi), oracle.gemm_f64(Ai.numpy(), Bi.numpy(), with_bound=False)[0], None, exact=True,
+          what="128x128x32 int")
+
+
+FULL = ["square_256", "square_1024", "square_2048", "flat_4096x4096x256", "skinny_8192x128x8192",
+        "skinny_128x8192x16384"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_named_problem_every_element(name):
+    p = PROBLEMS[name]
+    A, B = problem_operands(p)
+    C64, bound = oracle.gemm_f64(A.numpy(), B.numpy())
+    worst = check(run(A, B), C64, bound, exact=False, what=name)
+    print(f"{name}: worst |err|/bound = {worst:.3e}")
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_named_problem_integer_exact(name):
+    p = PROBLEMS[name].int_variant()
+    A, B = problem_operands(p)
+    check(run(A, B), oracle.gemm_f64(A.numpy(), B.numpy(), with_bound=False)[0], None, exact=True, what=p.name)
+
+
+@pytest.mark.parametrize("name", ["square_4096", "square_8192"])
+@pytest.mark.parametrize("dist", ["real", "int"])
+def test_named_problem_sampled_rows(name, dist):
+    p = PROBLEMS[name] if dist == "real" else PROBLEMS[name].int_variant()
+    A, B = problem_operands(p)
+    C = run(A, B)
+    rows = sample_rows(p.M, n_random=8, seed=p.seed)
+    C64, bound = oracle.gemm_rows_f64(A.numpy(), B.numpy(), rows)
+    check(C[rows], C64, bound, exact=(dist == "int"), what=f"{p.name} rows")
+
+
+def test_ragged_problem_falls_back_and_matches():
+    """1023 x 1025 x 1027: rows of 1027 floats are not 16-byte multiples, so the
+    call runs the FFMA kernels; the contract is the same."""
+    p = PROBLEMS["ragged_1023x1025x1027"]
+    A, B = problem_operands(p)
+    C64, bound = oracle.gemm_f64(A.numpy(), B.numpy())
+    check(run(A, B), C64, bound, exact=False, what=p.name)
+
+
+def test_ragged_shapes_sweep():
+    rng = np.random.default_rng(4321)
+    for t in range(24):
+        M, N = (int(x) for x in rng.integers(1, 301, size=2))
+        K = 4 * int(rng.integers(1, 76))  # rows of A stay 16-byte multiples
+        N4 = 4 * ((N + 3) // 4)
+        A, B = make_operands(M, N4, K, "normal", 600 + t)
+        C64, bound = oracle.gemm_f64(A.numpy(), B.numpy())
+        check(run(A, B), C64, bound, exact=False, what=f"{M}x{N4}x{K}")
+
+
+@pytest.mark.parametrize("shape", [(1, 4, 4), (1, 128, 10000), (129, 132, 36), (300, 4, 8), (256, 256, 8192)])
+def test_small_and_degenerate_shapes(shape):
+    M, N, K = shape
+    A, B = make_operands(M, N, K, "uniform", 78)
+    C64, bound = oracle.gemm_f64(A.numpy(), B.numpy())
+    check(run(A, B), C64, bound, exact=False, what=str(shape))
+
+
+def test_padded_rows_and_unaligned_output():
+    M, N, K = 200, 152, 96
+    A, B = make_operands(M, N, K, "uniform", 79)
+    C64, bound = oracle.gemm_f64(A.numpy(), B.numpy())
+    check(run(A, B, lda=100, ldb=160, ldc=157), C64, bound, exact=False, what="padded")
+
+
+def test_k_zero_writes_zeros():
+    C = run(torch.empty((40, 0)), torch.empty((0, 36)))
+    assert np.array_equal(C, np.zeros((40, 36), np.float32))
+
+
+def test_timeout_is_reported_and_recovers():
+    """CTA 0's producer skips a K slice: its transform warps' bounded wait
+    expires, the MMA issuer and the epilogue give up in turn, tensor memory is
+    freed, and the status word says so.  The next call is unaffected."""
+    A, B = make_operands(128, 256, 256, "uniform", 80)
+    dA, dB = to_device(A), to_device(B)
+    assert g.check_status() == 0
+    g.sgemm_3xtf32_ex(dA, dB, debug_skip_stage=3, timeout_ns=20_000_000)
+    assert g.check_status() == 4
+    C = g.sgemm_3xtf32(dA, dB)
+    assert g.check_status() == 0
+    C64, bound = oracle.gemm_f64(A.numpy(), B.numpy())
+    check(C.cpu().numpy(), C64, bound, exact=False, what="after timeout")
