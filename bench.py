@@ -392,6 +392,8 @@ def run_ours(args, rank, world, local_rank):
     return 0
 
 
+# sgemm_3xtf32 kernels: 1 = split-tile, 2 = direct-A.
+SWEEP_TF32X3_VARIANTS = [1, 2]
 SWEEP_OPTIONS = [
     {},
     {"math": 1},
@@ -423,9 +425,12 @@ def run_sweep(args):
         A_cpu, B_cpu = problem_operands(p)
         A, B = A_cpu.cuda(), B_cpu.cuda()
         C = torch.empty((p.M, p.N), dtype=torch.float32, device="cuda")
-        for opt in SWEEP_OPTIONS:
+        runs = [(opt, (lambda o=opt: g.sgemm_f32_ex(A, B, C, **o)) if opt else (lambda: g.sgemm_f32(A, B, C)))
+                for opt in SWEEP_OPTIONS]
+        runs += [({"entry": "sgemm_3xtf32", "variant": v}, lambda v=v: g.sgemm_3xtf32_ex(A, B, C, variant=v))
+                 for v in SWEEP_TF32X3_VARIANTS]
+        for opt, run in runs:
             try:
-                run = (lambda: g.sgemm_f32_ex(A, B, C, **opt)) if opt else (lambda: g.sgemm_f32(A, B, C))
                 for _ in range(3):
                     run()
                 torch.cuda.synchronize()

@@ -88,9 +88,10 @@ def sgemm_f32_ex(A, B, out=None, *, stream=None, producer=0, split_k=0, multicas
     return _call("sgemm_f32_ex", A, B, out, stream, opt)
 
 
-def sgemm_3xtf32_ex(A, B, out=None, *, stream=None, debug_skip_stage=0, timeout_ns=0) -> torch.Tensor:
-    """sgemm_3xtf32 with the bounded-wait test options."""
-    opt = Options(0, 0, 0, 0, 0, debug_skip_stage, timeout_ns, 0)
+def sgemm_3xtf32_ex(A, B, out=None, *, stream=None, variant=0, debug_skip_stage=0, timeout_ns=0) -> torch.Tensor:
+    """sgemm_3xtf32 with forced choices: ``variant`` 1 = split-tile kernel,
+    2 = direct-A kernel (0 = automatic)."""
+    opt = Options(0, 0, 0, variant, 0, debug_skip_stage, timeout_ns, 0)
     return _call("sgemm_3xtf32_ex", A, B, out, stream, opt)
 
 

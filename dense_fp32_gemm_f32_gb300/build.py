@@ -16,7 +16,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB_NAME = "libgb300_sgemm.so"
-SOURCES = ["sgemm_api.cu", "sgemm_ffma_tma.cu", "sgemm_ffma_cpasync.cu", "sgemm_3xtf32.cu", "peak.cu"]
+SOURCES = ["sgemm_api.cu", "sgemm_ffma_tma.cu", "sgemm_ffma_cpasync.cu", "sgemm_3xtf32.cu", "sgemm_3xtf32_direct.cu", "peak.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas", "-v"]
 

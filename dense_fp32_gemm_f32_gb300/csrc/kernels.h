@@ -13,7 +13,11 @@ struct KernelEntry {
 KernelEntry ffma_kernel_tma(int stages, int math);
 // FFMA kernels fed by 4-byte cp.async (any alignment); stages in {2,4}.
 KernelEntry ffma_kernel_cpasync(int stages, int math);
-// Three-product TF32 kernel on the tensor cores (TMA-fed, 128 x 128 tiles).
+// Three-product TF32 kernel on the tensor cores (TMA-fed, 128 x 128 tiles,
+// all four TF32 parts stored in shared memory).
 KernelEntry tf32x3_kernel();
+// Direct-A three-product TF32 kernel: A's big part read from the TMA tile,
+// only A's small part and B's two parts stored (128 x 128 tiles).
+KernelEntry tf32x3_direct_kernel();
 
 }  // namespace gb300

@@ -15,17 +15,19 @@
 // exact.  (The pages mention tensor cores only as a future direction of the
 // "Hardware acceleration" page's summary; nothing of this is on the pages.)
 //
-// One CTA computes a 128 x 128 tile of C; 6 warps:
-//   warp 0      TMA producer: A and B K-slices (BK = 32) into 2 raw stages;
+// One CTA computes a 128 x 128 tile of C; 10 warps:
+//   warp 0      TMA producer: A and B K-slices (BK = 32) into 3 raw stages;
 //   warp 1      allocates 128 tensor-memory columns (the FP32 accumulator)
 //               and one lane issues the MMAs: per K-slice 4 k-steps of 8,
 //               three tcgen05.mma.kind::tf32 each (small*big, big*small,
 //               big*big), then tcgen05.commit releases the split stage;
-//   warps 2..5  split the raw K-slice into four K-major, 128-byte-swizzled
+//   warps 2..9  split the raw K-slice into four K-major, 128-byte-swizzled
 //               TF32 operand tiles (A_big, A_small, B_big, B_small) in 2
 //               split stages (B is transposed on the way: it arrives with n
 //               innermost), then, after the last MMA, read the accumulator
-//               out of tensor memory (tcgen05.ld) and store C.
+//               out of tensor memory (tcgen05.ld) and store C.  Eight warps
+//               (two per SM sub-partition) so that one warp's shared-memory
+//               latency hides behind the other's conversions.
 //
 // Every wait is bounded by `timeout_ns`; on expiry the thread records the
 // timeout in the status word, stops working, and still reaches the final CTA
@@ -41,19 +43,6 @@
 #include "sgemm_3xtf32_params.h"
 
 namespace gb300 {
-
-// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
-// 128 bytes in groups of 8 that lie 1024 bytes apart.  Start address in bits
-// 0-13 (>> 4), leading byte offset (unused by swizzled K-major) in 16-29,
-// stride byte offset (>> 4) in 32-45, version 1 in 46-47, layout in 61-63.
-__device__ __forceinline__ uint64_t umma_desc_kmajor_sw128(uint32_t saddr) {
-    uint64_t d = static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
-    d |= static_cast<uint64_t>(1) << 16;
-    d |= static_cast<uint64_t>(1024 >> 4) << 32;
-    d |= static_cast<uint64_t>(1) << 46;
-    d |= static_cast<uint64_t>(2) << 61;
-    return d;
-}
 
 __device__ __forceinline__ void split_tf32(float x, float& big, float& small) {
     big = to_tf32_rna(x);
@@ -72,12 +61,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         return base + static_cast<uint32_t>(kTcRawStages * (kTcRawABytes + kTcRawBBytes) + s * kTcSplitBytes);
     };
     const uint32_t bars = base + kTcRingBytes;
+    constexpr uint32_t R = kTcRawStages, S = kTcSplitStages;
     auto raw_full = [&](int r) { return bars + 8u * r; };
-    auto raw_empty = [&](int r) { return bars + 16u + 8u * r; };
-    auto split_full = [&](int s) { return bars + 32u + 8u * s; };
-    auto split_empty = [&](int s) { return bars + 48u + 8u * s; };
-    const uint32_t acc_full = bars + 64u;
-    const uint32_t tmem_slot = bars + 72u;
+    auto raw_empty = [&](int r) { return bars + 8u * (R + r); };
+    auto split_full = [&](int s) { return bars + 8u * (2 * R + s); };
+    auto split_empty = [&](int s) { return bars + 8u * (2 * R + S + s); };
+    const uint32_t acc_full = bars + 8u * (2 * R + 2 * S);
+    const uint32_t tmem_slot = acc_full + 8u;
+    static_assert(8 * (2 * kTcRawStages + 2 * kTcSplitStages + 1) + 4 <= 256, "barrier area");
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -90,10 +81,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (threadIdx.x == 0) {
         for (int r = 0; r < kTcRawStages; ++r) {
             mbar_init(raw_full(r), 1);
-            mbar_init(raw_empty(r), 4);  // one arrival per transform warp
+            mbar_init(raw_empty(r), kTcSplitWarps);  // one arrival per split warp
         }
         for (int s = 0; s < kTcSplitStages; ++s) {
-            mbar_init(split_full(s), 4);
+            mbar_init(split_full(s), kTcSplitWarps);
             mbar_init(split_empty(s), 1);  // tcgen05.commit
         }
         mbar_init(acc_full, 1);
@@ -117,7 +108,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
-            int issued_round[kTcRawStages] = {-1, -1};
+            int issued_round[kTcRawStages];
+#pragma unroll
+            for (int r = 0; r < kTcRawStages; ++r) issued_round[r] = -1;
             const bool skip_here = p.skip_stage > 0 && tile == 0;
             for (int kt = 0; kt < nkt; ++kt) {
                 const int r = kt % kTcRawStages;
@@ -165,7 +158,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
     } else {
         // ------------------------------------------------------------ split + epilogue
-        const int tt = threadIdx.x - 64;  // 0..127
+        const int tt = threadIdx.x - 64;  // 0 .. 32 * kTcSplitWarps - 1
+        constexpr int kSplitThreads = 32 * kTcSplitWarps;
+        constexpr int kAChunks = kTcRawABytes / 16 / kSplitThreads;  // 16-byte A chunks per thread
+        constexpr int kBGroups = (kTcBN * kTcBK / 4) / kSplitThreads;  // (column, 4-k) groups per thread
+        const int bn = tt % kTcBN;                                      // B column of this thread
+        const int bc0 = (tt / kTcBN) * kBGroups;                        // its first 4-k group
         for (int kt = 0; kt < nkt; ++kt) {
             const int r = kt % kTcRawStages;
             const int s = kt % kTcSplitStages;
@@ -173,6 +171,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 timed_out = true;
                 break;
             }
+            // Loads are issued back to back before any use, so their latencies overlap.
+            float4 av[kAChunks];
+#pragma unroll
+            for (int j = 0; j < kAChunks; ++j) av[j] = lds128(rawA(r) + static_cast<uint32_t>((tt + kSplitThreads * j) * 16));
+            float bv[kBGroups][4];
+            const uint32_t rb = rawB(r) + static_cast<uint32_t>(bn * 4);
+#pragma unroll
+            for (int c = 0; c < kBGroups; ++c)
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    asm volatile("ld.shared.f32 %0, [%1];"
+                                 : "=f"(bv[c][i])
+                                 : "r"(rb + static_cast<uint32_t>((4 * (bc0 + c) + i) * kTcBN * 4)));
             if (kt >= kTcSplitStages &&
                 !mbar_wait_bounded_warp(split_empty(s), ((kt / kTcSplitStages) - 1) & 1, tmo)) {
                 timed_out = true;
@@ -183,36 +194,27 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // A: the TMA wrote the slice K-major with the same 128-byte swizzle
             // the MMA reads, so the split is element-wise on 16-byte chunks.
 #pragma unroll
-            for (int j = 0; j < kTcRawABytes / 16 / 128; ++j) {
-                const uint32_t off = static_cast<uint32_t>((tt + 128 * j) * 16);
-                const float4 v = lds128(rawA(r) + off);
+            for (int j = 0; j < kAChunks; ++j) {
+                const uint32_t off = static_cast<uint32_t>((tt + kSplitThreads * j) * 16);
                 float4 hi, lo;
-                split_tf32(v.x, hi.x, lo.x);
-                split_tf32(v.y, hi.y, lo.y);
-                split_tf32(v.z, hi.z, lo.z);
-                split_tf32(v.w, hi.w, lo.w);
+                split_tf32(av[j].x, hi.x, lo.x);
+                split_tf32(av[j].y, hi.y, lo.y);
+                split_tf32(av[j].z, hi.z, lo.z);
+                split_tf32(av[j].w, hi.w, lo.w);
                 sts128(a_big + off, hi);
                 sts128(a_small + off, lo);
             }
-            // B: the slice arrives as 32 rows (k) of 128 floats (n); thread tt
-            // takes column n = tt and writes it as row tt of the K-major tiles:
-            // 16-byte chunk c (k = 4c..4c+3) at chunk position c ^ (tt mod 8).
-            const uint32_t rb = rawB(r) + static_cast<uint32_t>(tt * 4);
+            // B: the slice arrives as 32 rows (k) of 128 floats (n).  Column
+            // n = bn becomes row bn of the K-major tiles: the 16-byte chunk of
+            // k = 4c..4c+3 goes to chunk position c ^ (bn mod 8).
 #pragma unroll
-            for (int c = 0; c < kTcBK / 4; ++c) {
-                float x[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    asm volatile("ld.shared.f32 %0, [%1];"
-                                 : "=f"(x[i])
-                                 : "r"(rb + static_cast<uint32_t>((4 * c + i) * kTcBN * 4))
-                                 : "memory");
+            for (int c = 0; c < kBGroups; ++c) {
                 float4 hi, lo;
-                split_tf32(x[0], hi.x, lo.x);
-                split_tf32(x[1], hi.y, lo.y);
-                split_tf32(x[2], hi.z, lo.z);
-                split_tf32(x[3], hi.w, lo.w);
-                const uint32_t off = static_cast<uint32_t>(tt * 128 + (((c ^ tt) & 7) << 4));
+                split_tf32(bv[c][0], hi.x, lo.x);
+                split_tf32(bv[c][1], hi.y, lo.y);
+                split_tf32(bv[c][2], hi.z, lo.z);
+                split_tf32(bv[c][3], hi.w, lo.w);
+                const uint32_t off = static_cast<uint32_t>(bn * 128 + ((((bc0 + c) ^ bn) & 7) << 4));
                 sts128(b_big + off, hi);
                 sts128(b_small + off, lo);
             }
@@ -225,15 +227,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
 
         // Epilogue: accumulator row (32 * (warp % 4) + lane) lives in that
-        // tensor-memory lane; 4 loads of 32 columns each.
+        // tensor-memory lane; the split warps sharing a lane quarter take
+        // different 32-column chunks.
         // (timed_out is warp-uniform here: every wait above voted across the warp)
         if (!timed_out && nkt > 0 && mbar_wait_bounded_warp(acc_full, 0, tmo)) {
             tc_fence_after_sync();
             const int q = warp & 3;
+            const int half = (warp - 2) / 4;  // which of the warps on this quarter
+            constexpr int kChunksPerWarp = (kTcBN / 32) / (kTcSplitWarps / 4);
             const int row = m0 + 32 * q + lane;
             float* crow = p.C + static_cast<long long>(row) * p.ldc;
 #pragma unroll
-            for (int ch = 0; ch < kTcBN / 32; ++ch) {
+            for (int cc = 0; cc < kChunksPerWarp; ++cc) {
+                const int ch = half * kChunksPerWarp + cc;
                 uint32_t v[32];
                 tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(32 * ch), v);
                 tmem_wait_ld();

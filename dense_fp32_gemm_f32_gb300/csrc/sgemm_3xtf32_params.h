@@ -9,12 +9,13 @@ namespace gb300 {
 constexpr int kTcBM = 128;
 constexpr int kTcBN = 128;
 constexpr int kTcBK = 32;
-constexpr int kTcThreads = 192;
+constexpr int kTcSplitWarps = 8;                // warps that split K-slices into TF32 parts
+constexpr int kTcThreads = 64 + 32 * kTcSplitWarps;
 constexpr int kTcRawABytes = kTcBM * kTcBK * 4;  // 16 KiB: TMA A slice, 128-byte swizzled rows
 constexpr int kTcRawBBytes = kTcBK * kTcBN * 4;  // 16 KiB: TMA B slice, 512-byte rows
 constexpr int kTcOpBytes = 128 * kTcBK * 4;      // 16 KiB: one K-major operand tile
 constexpr int kTcSplitBytes = 4 * kTcOpBytes;    // A_big, A_small, B_big, B_small
-constexpr int kTcRawStages = 2;
+constexpr int kTcRawStages = 3;
 constexpr int kTcSplitStages = 2;
 constexpr int kTcTmemCols = 128;
 constexpr unsigned kTcStatusTimeout = 4u;
@@ -37,6 +38,24 @@ struct TcParams {
     int skip_stage;   // debug: CTA 0's producer never issues K-slice skip_stage-1
     unsigned long long timeout_ns;
     unsigned int* status;
+    int dbg;
 };
+
+// ---- "direct-A" variant: the TF32 big part of A is the FP32 tile itself
+// (the tensor core reads the top 19 bits of each 32-bit element), so only
+// A's small part is stored; B is split into big and small parts and
+// transposed to K-major as in the split-tile kernel.  One stage holds the raw
+// A and B slices and the three stored parts; it is released by the MMAs.
+constexpr int kTdSplitWarps = 8;
+constexpr int kTdThreads = 64 + 32 * kTdSplitWarps;
+constexpr int kTdBM = 128;
+constexpr int kTdBN = 128;
+constexpr int kTdBK = 32;
+constexpr int kTdTile = 128 * kTdBK * 4;         // 16 KiB: one 128-row x 32-float tile
+constexpr int kTdStageBytes = 5 * kTdTile;        // raw A, raw B, A small, B big, B small
+constexpr int kTdStages = 2;
+constexpr int kTdRingBytes = kTdStages * kTdStageBytes;
+constexpr int kTdSmemBytes = kTdRingBytes + 1024 + 256;
+constexpr int kTdTmemCols = kTdBN;
 
 }  // namespace gb300

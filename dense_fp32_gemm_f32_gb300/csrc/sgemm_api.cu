@@ -25,6 +25,8 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;  // 2 s per wait
+// sgemm_3xtf32 kernel chosen when not forced: 1 = split-tile, 2 = direct-A.
+constexpr int kTf32x3DefaultVariant = 1;
 
 struct DeviceState {
     std::once_flag once;
@@ -106,7 +108,8 @@ int init_device(int dev, DeviceState& st) {
         for (int s = 1; s <= 6; ++s)
             if (set_smem_attr(ffma_kernel_cpasync(s, math)) != SGEMM_OK) return SGEMM_ERR_CUDA;
     }
-    if (set_smem_attr(tf32x3_kernel()) != SGEMM_OK) return SGEMM_ERR_CUDA;
+    if (set_smem_attr(tf32x3_kernel()) != SGEMM_OK || set_smem_attr(tf32x3_direct_kernel()) != SGEMM_OK)
+        return SGEMM_ERR_CUDA;
     const KernelEntry ref = ffma_kernel_tma(4, kMathFfma2);
     st.max_clusters_pair = max_active_clusters(ref, 2, 1);
     st.max_clusters_split[1] = st.sm_count;
@@ -394,7 +397,11 @@ int run_3xtf32(int M, int N, int K, const float* A, int lda, const float* B, int
     // which meets the same contract.
     if (K == 0 || !tma_ok(A, lda) || !tma_ok(B, ldb)) return run_ffma(M, N, K, A, lda, B, ldb, C, ldc, stream, nullptr);
 
-    const KernelEntry k = tf32x3_kernel();
+    // Variant: 1 = split-tile kernel (all four TF32 parts in shared memory),
+    // 2 = direct-A kernel (A's big part is the TMA tile itself).
+    const int variant = (opt && opt->math) ? opt->math : kTf32x3DefaultVariant;
+    if (variant < 1 || variant > 2) return SGEMM_ERR_INVALID_ARG;
+    const KernelEntry k = variant == 1 ? tf32x3_kernel() : tf32x3_direct_kernel();
     alignas(64) CUtensorMap tmA;
     alignas(64) CUtensorMap tmB;
     rc = encode_2d(&tmA, A, K, M, lda, kTcBK, kTcBM, CU_TENSOR_MAP_SWIZZLE_128B);

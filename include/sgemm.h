@@ -140,8 +140,13 @@ int sgemm_f32_ex(int M, int N, int K,
                  float* C, int ldc,
                  void* stream, const sgemm_options* opt);
 
-/* sgemm_3xtf32 with the debug_skip_stage and timeout_ns fields of `opt` (the
- * other fields are ignored).  For tests of the bounded-wait path. */
+/* sgemm_3xtf32 with forced choices.  Uses the fields debug_skip_stage,
+ * timeout_ns and math, which here selects the tensor-core kernel: 0 = auto,
+ * 1 = split-tile kernel (TF32 big and small parts of both operands stored in
+ * shared memory), 2 = direct-A kernel (A's big part is the FP32 tile the TMA
+ * lands, read by the tensor core at TF32 precision; only A's small part and
+ * B's two parts are stored).  Both use 128 x 128 tiles.  Other fields are
+ * ignored. */
 int sgemm_3xtf32_ex(int M, int N, int K,
                     const float* A, int lda,
                     const float* B, int ldb,

@@ -23,51 +23,64 @@ def cuda_device():
     assert g.check_status() == 0, "a kernel reported a timeout"
 
 
-def run(A, B, *, lda=None, ldb=None, ldc=None):
+# 0 = the automatic choice of sgemm_3xtf32; 1 = split-tile kernel; 2 =
+# direct-A kernel.
+VARIANTS = [0, 1, 2]
+
+
+def run(A, B, *, lda=None, ldb=None, ldc=None, variant=0):
     dA = to_device(A, lda)
     dB = to_device(B, ldb)
     dC = to_device(torch.full((A.shape[0], B.shape[1]), float("nan")), ldc)
-    g.sgemm_3xtf32(dA, dB, dC)
+    if variant:
+        g.sgemm_3xtf32_ex(dA, dB, dC, variant=variant)
+    else:
+        g.sgemm_3xtf32(dA, dB, dC)
     torch.cuda.synchronize()
     return dC.cpu().numpy()
 
 
-def test_one_tile_first():
-    """One 128 x 128 tile, one K slice: the smallest launch of the kernel."""
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_one_tile_first(variant):
+    """One output tile, one K slice: the smallest launch of each kernel."""
     A, B = make_operands(128, 128, 32, "uniform", 50)
     C64, bound = oracle.gemm_f64(A.numpy(), B.numpy())
-    check(run(A, B), C64, bound, exact=False, what="128x128x32")
+    check(run(A, B, variant=variant), C64, bound, exact=False, what="128x128x32")
     Ai, Bi = make_operands(128, 128, 32, "int", 51)
-    check(run(Ai, Bi), oracle.gemm_f64(Ai.numpy(), Bi.numpy(), with_bound=False)[0], None, exact=True,
-          what="128x128x32 int")
+    check(run(Ai, Bi, variant=variant), oracle.gemm_f64(Ai.numpy(), Bi.numpy(), with_bound=False)[0], None,
+          exact=True, what="128x128x32 int")
 
 
 FULL = ["square_256", "square_1024", "square_2048", "flat_4096x4096x256", "skinny_8192x128x8192",
         "skinny_128x8192x16384"]
 
 
+@pytest.mark.parametrize("variant", VARIANTS)
 @pytest.mark.parametrize("name", FULL)
-def test_named_problem_every_element(name):
+def test_named_problem_every_element(name, variant):
     p = PROBLEMS[name]
     A, B = problem_operands(p)
     C64, bound = oracle.gemm_f64(A.numpy(), B.numpy())
-    worst = check(run(A, B), C64, bound, exact=False, what=name)
-    print(f"{name}: worst |err|/bound = {worst:.3e}")
+    worst = check(run(A, B, variant=variant), C64, bound, exact=False, what=name)
+    print(f"{name} variant {variant}: worst |err|/bound = {worst:.3e}")
 
 
+@pytest.mark.parametrize("variant", VARIANTS)
 @pytest.mark.parametrize("name", FULL)
-def test_named_problem_integer_exact(name):
+def test_named_problem_integer_exact(name, variant):
     p = PROBLEMS[name].int_variant()
     A, B = problem_operands(p)
-    check(run(A, B), oracle.gemm_f64(A.numpy(), B.numpy(), with_bound=False)[0], None, exact=True, what=p.name)
+    check(run(A, B, variant=variant), oracle.gemm_f64(A.numpy(), B.numpy(), with_bound=False)[0], None, exact=True,
+          what=p.name)
 
 
+@pytest.mark.parametrize("variant", VARIANTS)
 @pytest.mark.parametrize("name", ["square_4096", "square_8192"])
 @pytest.mark.parametrize("dist", ["real", "int"])
-def test_named_problem_sampled_rows(name, dist):
+def test_named_problem_sampled_rows(name, dist, variant):
     p = PROBLEMS[name] if dist == "real" else PROBLEMS[name].int_variant()
     A, B = problem_operands(p)
-    C = run(A, B)
+    C = run(A, B, variant=variant)
     rows = sample_rows(p.M, n_random=8, seed=p.seed)
     C64, bound = oracle.gemm_rows_f64(A.numpy(), B.numpy(), rows)
     check(C[rows], C64, bound, exact=(dist == "int"), what=f"{p.name} rows")
@@ -82,7 +95,8 @@ def test_ragged_problem_falls_back_and_matches():
     check(run(A, B), C64, bound, exact=False, what=p.name)
 
 
-def test_ragged_shapes_sweep():
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_ragged_shapes_sweep(variant):
     rng = np.random.default_rng(4321)
     for t in range(24):
         M, N = (int(x) for x in rng.integers(1, 301, size=2))
@@ -90,22 +104,25 @@ def test_ragged_shapes_sweep():
         N4 = 4 * ((N + 3) // 4)
         A, B = make_operands(M, N4, K, "normal", 600 + t)
         C64, bound = oracle.gemm_f64(A.numpy(), B.numpy())
-        check(run(A, B), C64, bound, exact=False, what=f"{M}x{N4}x{K}")
+        check(run(A, B, variant=variant), C64, bound, exact=False, what=f"{M}x{N4}x{K}")
 
 
-@pytest.mark.parametrize("shape", [(1, 4, 4), (1, 128, 10000), (129, 132, 36), (300, 4, 8), (256, 256, 8192)])
-def test_small_and_degenerate_shapes(shape):
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("shape", [(1, 4, 4), (1, 128, 10000), (129, 132, 36), (300, 4, 8), (256, 256, 8192),
+                                   (130, 260, 100)])
+def test_small_and_degenerate_shapes(shape, variant):
     M, N, K = shape
     A, B = make_operands(M, N, K, "uniform", 78)
     C64, bound = oracle.gemm_f64(A.numpy(), B.numpy())
-    check(run(A, B), C64, bound, exact=False, what=str(shape))
+    check(run(A, B, variant=variant), C64, bound, exact=False, what=str(shape))
 
 
-def test_padded_rows_and_unaligned_output():
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_padded_rows_and_unaligned_output(variant):
     M, N, K = 200, 152, 96
     A, B = make_operands(M, N, K, "uniform", 79)
     C64, bound = oracle.gemm_f64(A.numpy(), B.numpy())
-    check(run(A, B, lda=100, ldb=160, ldc=157), C64, bound, exact=False, what="padded")
+    check(run(A, B, lda=100, ldb=160, ldc=157, variant=variant), C64, bound, exact=False, what="padded")
 
 
 def test_k_zero_writes_zeros():
@@ -113,14 +130,15 @@ def test_k_zero_writes_zeros():
     assert np.array_equal(C, np.zeros((40, 36), np.float32))
 
 
-def test_timeout_is_reported_and_recovers():
-    """CTA 0's producer skips a K slice: its transform warps' bounded wait
+@pytest.mark.parametrize("variant", [1, 2])
+def test_timeout_is_reported_and_recovers(variant):
+    """CTA 0's producer skips a K slice: its split warps' bounded wait
     expires, the MMA issuer and the epilogue give up in turn, tensor memory is
     freed, and the status word says so.  The next call is unaffected."""
     A, B = make_operands(128, 256, 256, "uniform", 80)
     dA, dB = to_device(A), to_device(B)
     assert g.check_status() == 0
-    g.sgemm_3xtf32_ex(dA, dB, debug_skip_stage=3, timeout_ns=20_000_000)
+    g.sgemm_3xtf32_ex(dA, dB, variant=variant, debug_skip_stage=3, timeout_ns=20_000_000)
     assert g.check_status() == 4
     C = g.sgemm_3xtf32(dA, dB)
     assert g.check_status() == 0
