@@ -54,13 +54,24 @@ constexpr int kBN = 128;
 constexpr int kBK = 32;
 constexpr int kConsumerWarps = 8;
 constexpr int kConsumerThreads = kConsumerWarps * 32;
-constexpr int kThreads = kConsumerThreads + 32;  // + one producer warp
+
+enum : int { kProducerTma = 1, kProducerCpAsync = 2 };
+
+// Producer warps: one elected lane drives the TMA; the cp.async producer
+// issues every 4-byte copy itself, so it gets a full warpgroup.
+template <int PRODUCER>
+__host__ __device__ constexpr int ffma_producer_warps() {
+    return PRODUCER == kProducerCpAsync ? 4 : 1;
+}
+template <int PRODUCER>
+__host__ __device__ constexpr int ffma_threads() {
+    return kConsumerThreads + 32 * ffma_producer_warps<PRODUCER>();
+}
 constexpr int kStageABytes = kBM * kBK * 4;      // 16 KiB, 128-byte swizzled rows of 32 floats
 constexpr int kStageBBytes = kBK * kBN * 4;      // 16 KiB, plain rows of 128 floats
 constexpr int kStageBytes = kStageABytes + kStageBBytes;
 constexpr int kPartialBytes = kBM * kBN * 4;     // split-K partial tile
 
-enum : int { kProducerTma = 1, kProducerCpAsync = 2 };
 enum : int { kMathFfma = 1, kMathFfma2 = 2 };
 enum : unsigned { kStatusTimeout = 4u };
 
@@ -96,7 +107,7 @@ __device__ __forceinline__ uint32_t swz128(int r, int c) {
 }
 
 template <int STAGES, int PRODUCER, int MATH>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(ffma_threads<PRODUCER>(), 1)
     sgemm_ffma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                       const FfmaParams p) {
     extern __shared__ uint8_t smem_raw[];
@@ -114,7 +125,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const bool is_producer = warp == kConsumerWarps;
+    constexpr int PW = ffma_producer_warps<PRODUCER>();
+    const bool is_producer = warp >= kConsumerWarps;
+    const int pw = warp - kConsumerWarps;  // producer warp index (when is_producer)
     const int split = p.split;
     const int mcast = p.mcast;
     const uint32_t crank = (split > 1 || mcast > 1) ? cluster_ctarank() : 0u;
@@ -132,7 +145,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nkt = kt_end - kt_begin;
 
     if (threadIdx.x == 0) {
-        const uint32_t full_count = (PRODUCER == kProducerTma) ? 1u : 32u;
+        const uint32_t full_count = (PRODUCER == kProducerTma) ? 1u : 32u * PW;
         const uint32_t empty_count = static_cast<uint32_t>(kConsumerWarps * mcast);
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full_bar(s), full_count);
@@ -191,7 +204,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         } else {
-            // cp.async producer: all 32 lanes copy 4-byte elements with zero fill.
+            // cp.async producer: PW warps copy 4-byte elements with zero fill;
+            // every lane's copies arrive on the full barrier (32 * PW arrivals).
             for (int it = 0; it < nkt; ++it) {
                 const int s = it % STAGES;
                 const int round = it / STAGES;
@@ -203,19 +217,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int k0 = (kt_begin + it) * kBK;
                 const uint32_t sa = sA0 + s * kStageABytes;
                 const uint32_t sb = sB0 + s * kStageBBytes;
-                // A slice: 128 rows x 32 floats; lane = column, one row per step.
+                // A slice: 128 rows x 32 floats; lane = column, warp pw takes
+                // rows pw, pw + PW, ...
                 {
                     const int k = k0 + lane;
                     const bool kin = k < p.K;
-                    for (int r = 0; r < kBM; ++r) {
+                    for (int r = pw; r < kBM; r += PW) {
                         const int m = m0 + r;
                         const bool in = kin && m < p.M;
                         const float* src = in ? p.A + static_cast<long long>(m) * p.lda + k : p.A;
                         cp_async_4(sa + swz128(r, lane), src, in ? 4u : 0u);
                     }
                 }
-                // B slice: 32 rows x 128 floats; lane = column within a 32-wide strip.
-                for (int r = 0; r < kBK; ++r) {
+                // B slice: 32 rows x 128 floats; lane = column within a 32-wide
+                // strip, warp pw takes rows pw, pw + PW, ...
+                for (int r = pw; r < kBK; r += PW) {
                     const int k = k0 + r;
                     const bool kin = k < p.K;
 #pragma unroll

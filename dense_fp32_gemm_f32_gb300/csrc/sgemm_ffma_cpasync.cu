@@ -7,7 +7,7 @@ namespace gb300 {
 template <int S, int MATH>
 static KernelEntry entry() {
     return {reinterpret_cast<const void*>(&sgemm_ffma_kernel<S, kProducerCpAsync, MATH>), ffma_smem_bytes<S>(),
-            kThreads};
+            ffma_threads<kProducerCpAsync>()};
 }
 
 KernelEntry ffma_kernel_cpasync(int stages, int math) {

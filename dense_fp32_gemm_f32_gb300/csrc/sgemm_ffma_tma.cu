@@ -6,7 +6,8 @@ namespace gb300 {
 
 template <int S, int MATH>
 static KernelEntry entry() {
-    return {reinterpret_cast<const void*>(&sgemm_ffma_kernel<S, kProducerTma, MATH>), ffma_smem_bytes<S>(), kThreads};
+    return {reinterpret_cast<const void*>(&sgemm_ffma_kernel<S, kProducerTma, MATH>), ffma_smem_bytes<S>(),
+            ffma_threads<kProducerTma>()};
 }
 
 KernelEntry ffma_kernel_tma(int stages, int math) {
