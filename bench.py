@@ -407,6 +407,7 @@ SWEEP_OPTIONS = [
     {"split_k": 4},
     {"split_k": 8},
     {"tail_split": 4},
+    {"stream_k": 2},
 ]
 
 

@@ -40,6 +40,7 @@ class Options(ctypes.Structure):
         ("debug_skip_stage", _i),
         ("timeout_ns", _u64),
         ("tail_split", _i),
+        ("stream_k", _i),
     ]
 
 

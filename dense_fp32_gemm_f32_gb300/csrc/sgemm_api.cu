@@ -35,6 +35,8 @@ struct DeviceState {
     int max_clusters_pair = 0;    // co-resident 2-CTA clusters of the FFMA kernel
     int max_clusters_split[9] = {0};
     unsigned int* status_word = nullptr;  // device address of g_sgemm_status
+    std::once_flag pool_once;
+    cudaMemPool_t pool = nullptr;  // library-owned pool for per-call workspaces
 };
 
 DeviceState g_dev[kMaxDevices];
@@ -118,6 +120,29 @@ int init_device(int dev, DeviceState& st) {
     return SGEMM_OK;
 }
 
+// The library's own stream-ordered memory pool on device `dev`, created on
+// first use.  Its release threshold keeps freed workspaces cached in the pool
+// (the device's default pool would return them to the system at every
+// synchronisation and re-allocate on the next call).
+cudaMemPool_t workspace_pool(int dev, DeviceState& st) {
+    std::call_once(st.pool_once, [&] {
+        cudaMemPoolProps props = {};
+        props.allocType = cudaMemAllocationTypePinned;
+        props.location.type = cudaMemLocationTypeDevice;
+        props.location.id = dev;
+        cudaMemPool_t pool = nullptr;
+        if (cudaMemPoolCreate(&pool, &props) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return;
+        }
+        uint64_t threshold = ~0ull;
+        if (cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &threshold) != cudaSuccess)
+            (void)cudaGetLastError();
+        st.pool = pool;
+    });
+    return st.pool;
+}
+
 // Set-up of the current device (once per device per process).
 int current_device(int* dev_out, DeviceState** st_out) {
     int dev = -1;
@@ -175,6 +200,8 @@ struct Plan {
     int num_k_tiles = 0;
     int nlaunch = 1;
     Launch launch[2];
+    int sk = 0;           // stream-K: launch[0].tiles CTAs, one per SM
+    int sk_dp_tiles = 0;  // tiles taken whole (data-parallel waves) before the stream-K region
 };
 
 long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
@@ -218,6 +245,17 @@ int make_plan(const DeviceState& st, int M, int N, int K, const float* A, int ld
         pl.stages = 4;
     }
 
+    // Stream-K (decided first; see below for the schedule).  Automatic
+    // whenever nothing else is forced and there are at least two (tile, K
+    // slice) units per SM: measured on GB300 it beats the plain grid and
+    // cluster split-K (1024^3 +8 %, 2048^3 +16 %, 4096^3 +4 %, 8192^3 +1 %,
+    // 8192x128x8192 +22 %); tiny problems keep cluster split-K.
+    const int want_sk = opt ? opt->stream_k : 0;
+    if (want_sk < 0 || want_sk > 2) return SGEMM_ERR_INVALID_ARG;
+    const bool forced_other = opt && (opt->split_k || opt->multicast == 2 || opt->tail_split > 1);
+    const bool use_sk = want_sk == 2 || (want_sk == 0 && !forced_other && pl.num_k_tiles > 0 &&
+                                         tiles * pl.num_k_tiles >= 2LL * st.sm_count);
+
     // Split-K over the whole grid, only when the tiles do not fill one wave:
     // pick s in 1..8 minimising (waves of clusters) x (K tiles per CTA).  (With
     // a wave or more, only the last partial wave is split; see below.)
@@ -225,7 +263,7 @@ int make_plan(const DeviceState& st, int M, int N, int K, const float* A, int ld
     if (opt && opt->split_k) {
         if (opt->split_k < 1 || opt->split_k > 8) return SGEMM_ERR_INVALID_ARG;
         split = opt->split_k;
-    } else if (tiles < st.sm_count) {
+    } else if (tiles < st.sm_count && !use_sk) {
         long long best = -1;
         for (int s = 1; s <= 8; ++s) {
             const int slots = st.max_clusters_split[s];
@@ -283,6 +321,25 @@ int make_plan(const DeviceState& st, int M, int N, int K, const float* A, int ld
             pl.launch[1].split = want_tail;
         }
     }
+
+    // Stream-K schedule: one CTA per SM, partial tiles finished through a
+    // global workspace.
+    if (use_sk) {
+        if (split > 1 || pl.mcast > 1 || pl.nlaunch > 1 || pl.num_k_tiles == 0) return SGEMM_ERR_INVALID_ARG;
+        // All but the last full wave run data-parallel (raster order keeps
+        // the A and B panels in flight few, as in the plain launch); the last
+        // full wave and the partial one are dealt out as units.
+        const long long G = st.sm_count;
+        const long long waves = grid_tiles / G;
+        const long long dp = waves > 1 ? (waves - 1) * G : 0;
+        const long long units = (grid_tiles - dp) * pl.num_k_tiles;
+        pl.sk = 1;
+        pl.sk_dp_tiles = static_cast<int>(dp);
+        pl.nlaunch = 1;
+        pl.launch[0].tile_base = 0;
+        pl.launch[0].split = 1;
+        pl.launch[0].tiles = static_cast<int>(units < G ? units : G);
+    }
     *out = pl;
     return SGEMM_OK;
 }
@@ -306,6 +363,8 @@ const char* describe_plan(const Plan& pl) {
                           pl.math == kMathFfma2 ? "ffma2" : "ffma", pl.mcast, pl.launch[0].split, pl.stages);
     if (pl.nlaunch > 1 && n > 0 && n < static_cast<int>(sizeof buf))
         std::snprintf(buf + n, sizeof buf - n, "/tail%d:%d", pl.launch[1].split, pl.launch[1].tiles);
+    if (pl.sk && n > 0 && n < static_cast<int>(sizeof buf))
+        std::snprintf(buf + n, sizeof buf - n, "/sk%d", pl.launch[0].tiles);
     return buf;
 }
 
@@ -355,6 +414,34 @@ int run_ffma(int M, int N, int K, const float* A, int lda, const float* B, int l
     prm.skip_stage = opt ? opt->debug_skip_stage : 0;
     prm.timeout_ns = (opt && opt->timeout_ns) ? opt->timeout_ns : kDefaultTimeoutNs;
     prm.status = st->status_word;
+    prm.sk = pl.sk;
+    prm.sk_dp_tiles = pl.sk_dp_tiles;
+    prm.sk_units = (static_cast<long long>(pl.tiles_n) * ceil_div(M, kBM) - pl.sk_dp_tiles) * pl.num_k_tiles;
+    prm.ws = nullptr;
+    prm.flags = nullptr;
+
+    // Stream-K workspace: one partial tile and one flag per CTA, taken from
+    // the library's stream-ordered pool for this call and returned to it
+    // after the kernel (stream order makes concurrent calls on different
+    // streams use different workspaces).
+    void* ws = nullptr;
+    const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    if (pl.sk) {
+        const size_t G = static_cast<size_t>(pl.launch[0].tiles);
+        const size_t tile_bytes = static_cast<size_t>(kBM) * kBN * sizeof(float);
+        cudaMemPool_t pool = workspace_pool(dev, *st);
+        if (!pool || cudaMallocFromPoolAsync(&ws, G * tile_bytes + G * sizeof(unsigned int), pool, cs) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return SGEMM_ERR_CUDA;
+        }
+        prm.ws = static_cast<float*>(ws);
+        prm.flags = reinterpret_cast<unsigned int*>(static_cast<char*>(ws) + G * tile_bytes);
+        if (cudaMemsetAsync(prm.flags, 0, G * sizeof(unsigned int), cs) != cudaSuccess) {
+            (void)cudaGetLastError();
+            (void)cudaFreeAsync(ws, cs);
+            return SGEMM_ERR_CUDA;
+        }
+    }
 
     for (int l = 0; l < pl.nlaunch; ++l) {
         const Launch& ln = pl.launch[l];
@@ -367,17 +454,29 @@ int run_ffma(int M, int N, int K, const float* A, int lda, const float* B, int l
         cfg.dynamicSmemBytes = static_cast<size_t>(k.smem_bytes);
         cfg.stream = static_cast<cudaStream_t>(stream);
         cudaLaunchAttribute attr;
-        attr.id = cudaLaunchAttributeClusterDimension;
-        attr.val.clusterDim.x = pl.mcast;
-        attr.val.clusterDim.y = 1;
-        attr.val.clusterDim.z = ln.split;
+        if (pl.sk) {
+            // Finishing CTAs wait for the partial tiles of later CTAs: all of
+            // them must be resident at once.
+            attr.id = cudaLaunchAttributeCooperative;
+            attr.val.cooperative = 1;
+        } else {
+            attr.id = cudaLaunchAttributeClusterDimension;
+            attr.val.clusterDim.x = pl.mcast;
+            attr.val.clusterDim.y = 1;
+            attr.val.clusterDim.z = ln.split;
+        }
         cfg.attrs = &attr;
-        cfg.numAttrs = (pl.mcast > 1 || ln.split > 1) ? 1 : 0;
+        cfg.numAttrs = (pl.sk || pl.mcast > 1 || ln.split > 1) ? 1 : 0;
         void* args[3] = {&tmA, &tmB, &prm};
         if (cudaLaunchKernelExC(&cfg, k.fn, args) != cudaSuccess) {
             (void)cudaGetLastError();
+            if (ws) (void)cudaFreeAsync(ws, cs);
             return SGEMM_ERR_CUDA;
         }
+    }
+    if (ws && cudaFreeAsync(ws, cs) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return SGEMM_ERR_CUDA;
     }
     return SGEMM_OK;
 }

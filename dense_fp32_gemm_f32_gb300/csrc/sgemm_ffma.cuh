@@ -89,6 +89,17 @@ struct FfmaParams {
     int vec_store;         // C base 16-byte aligned and ldc % 4 == 0
     int tile_base;         // linear index of this launch's first output tile
     int tiles_n;           // output tiles per row of tiles (even when mcast == 2)
+    // Stream-K schedule (sk != 0), one CTA per SM: CTA g first takes whole
+    // tiles g, g + G, ... below sk_dp_tiles (data-parallel waves, raster
+    // order), then an even share of the units (one K slice of one tile each)
+    // of the remaining tiles, dealt out in order; a tile shared by several
+    // CTAs is finished by the one holding its first K slice, which adds the
+    // others' partial tiles from `ws`.
+    int sk;
+    int sk_dp_tiles;       // tiles handled whole before the stream-K region
+    long long sk_units;    // (tiles - sk_dp_tiles) * num_k_tiles
+    float* ws;             // gridDim.x partial tiles of kBM x kBN floats
+    unsigned int* flags;   // gridDim.x words, zero at launch; 1 = partial ready
     int skip_stage;        // debug: CTA (0,0,0)'s producer never issues K-slice skip_stage-1
     unsigned long long timeout_ns;
     unsigned int* status;  // per-device sticky status word (error bits)
@@ -132,17 +143,49 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), 1)
     const int mcast = p.mcast;
     const uint32_t crank = (split > 1 || mcast > 1) ? cluster_ctarank() : 0u;
 
-    // Tile coordinates.  gridDim.x runs over output tiles, row of tiles by row
-    // of tiles starting at tile_base (neighbours along x share the rows of A:
-    // the multicast pairs, and the A tiles they reuse from L2); gridDim.z runs
-    // over K splits.
-    const int tile = p.tile_base + static_cast<int>(blockIdx.x);
-    const int n0 = (tile % p.tiles_n) * kBN;
-    const int m0 = (tile / p.tiles_n) * kBM;
-    const int kz = (split > 1) ? static_cast<int>(blockIdx.z) : 0;
-    const int kt_begin = static_cast<int>((static_cast<long long>(p.num_k_tiles) * kz) / split);
-    const int kt_end = static_cast<int>((static_cast<long long>(p.num_k_tiles) * (kz + 1)) / split);
-    const int nkt = kt_end - kt_begin;
+    // Work.  A CTA processes a sequence of segments (tile, kb, ke): the K
+    // slices [kb, ke) of one output tile.  Tiles are numbered row of tiles by
+    // row of tiles from tile_base, so neighbouring CTAs share rows of A (the
+    // multicast pairs, and the A tiles reused from L2).  Without stream-K
+    // there is one segment: the CTA's tile (gridDim.x over tiles) and, with
+    // split-K, the K range of cluster rank blockIdx.z.  With stream-K: the
+    // data-parallel tiles first, then the CTA's even share of the stream-K
+    // units u (tile = sk_tile0 + u / NK, K slice u % NK).
+    const int NK = p.num_k_tiles;
+    const int G = static_cast<int>(gridDim.x);
+    const int sk_tile0 = p.sk ? p.sk_dp_tiles : p.tile_base + static_cast<int>(blockIdx.x);
+    long long u_begin, u_end;
+    if (p.sk) {
+        u_begin = (p.sk_units * blockIdx.x) / G;
+        u_end = (p.sk_units * (blockIdx.x + 1)) / G;
+    } else {
+        const int kz = (split > 1) ? static_cast<int>(blockIdx.z) : 0;
+        u_begin = (static_cast<long long>(NK) * kz) / split;
+        u_end = (static_cast<long long>(NK) * (kz + 1)) / split;
+    }
+    struct Work {
+        int dp_next, dp_step, dp_end, tile0, nk;
+        long long u, u_end;
+        __device__ __forceinline__ bool next(int& tile, int& kb, int& ke) {
+            if (dp_next < dp_end) {
+                tile = dp_next;
+                kb = 0;
+                ke = nk;
+                dp_next += dp_step;
+                return true;
+            }
+            if (u < u_end) {
+                tile = tile0 + static_cast<int>(u / nk);
+                kb = static_cast<int>(u % nk);
+                ke = static_cast<int>(min(static_cast<long long>(nk), kb + (u_end - u)));
+                u += ke - kb;
+                return true;
+            }
+            return false;
+        }
+    };
+    const Work work0{static_cast<int>(blockIdx.x), G, p.sk ? p.sk_dp_tiles : 0, sk_tile0, NK > 0 ? NK : 1,
+                     u_begin, NK > 0 ? u_end : u_begin};
 
     if (threadIdx.x == 0) {
         const uint32_t full_count = (PRODUCER == kProducerTma) ? 1u : 32u * PW;
@@ -165,28 +208,37 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), 1)
 
     bool timed_out = false;
     const unsigned long long tmo = p.timeout_ns;
-    const bool skip_here = p.skip_stage > 0 && tile == 0 && blockIdx.z == 0;
+    const bool skip_here = p.skip_stage > 0 && blockIdx.x == 0 && blockIdx.z == 0;
 
     // ------------------------------------------------------------ producer
     if (is_producer) {
-        if (PRODUCER == kProducerTma) {
-            if (lane == 0) {
-                int issued_round[STAGES];
+        const bool issuer = PRODUCER == kProducerCpAsync || lane == 0;
+        int issued_round[STAGES];
 #pragma unroll
-                for (int s = 0; s < STAGES; ++s) issued_round[s] = -1;
-                for (int it = 0; it < nkt; ++it) {
-                    const int s = it % STAGES;
-                    const int round = it / STAGES;
-                    if (round > 0 && !mbar_wait_bounded(empty_bar(s), (round - 1) & 1, tmo)) {
-                        timed_out = true;
-                        break;
-                    }
-                    if (skip_here && it == p.skip_stage - 1) continue;
-                    const int k0 = (kt_begin + it) * kBK;
+        for (int s = 0; s < STAGES; ++s) issued_round[s] = -1;
+        int it = 0;  // K slices so far, across tiles: position in the stage ring
+        Work work = work0;
+        int tile, kb, ke;
+        while (issuer && !timed_out && work.next(tile, kb, ke)) {
+            const int n0 = (tile % p.tiles_n) * kBN;
+            const int m0 = (tile / p.tiles_n) * kBM;
+            for (int kt = kb; kt < ke; ++kt, ++it) {
+                const int s = it % STAGES;
+                const int round = it / STAGES;
+                const bool ok = PRODUCER == kProducerTma
+                                    ? (round == 0 || mbar_wait_bounded(empty_bar(s), (round - 1) & 1, tmo))
+                                    : (round == 0 || mbar_wait_bounded_warp(empty_bar(s), (round - 1) & 1, tmo));
+                if (!ok) {
+                    timed_out = true;
+                    break;
+                }
+                if (skip_here && it == p.skip_stage - 1) continue;
+                const int k0 = kt * kBK;
+                if (PRODUCER == kProducerTma) {
                     mbar_arrive_expect_tx(full_bar(s), kStageBytes);
                     if (mcast > 1) {
-                        // This CTA fetches rows [crank*64, crank*64+64) of the A slice
-                        // and multicasts them into both CTAs of the pair.
+                        // This CTA fetches rows [crank*64, crank*64+64) of the A
+                        // slice and multicasts them into both CTAs of the pair.
                         const uint32_t half = static_cast<uint32_t>(kStageABytes / 2) * crank;
                         tma_load_2d_multicast(sA0 + s * kStageABytes + half, &tmA, full_bar(s), k0,
                                               m0 + static_cast<int>(crank) * (kBM / 2), 0x3);
@@ -194,57 +246,50 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), 1)
                         tma_load_2d(sA0 + s * kStageABytes, &tmA, full_bar(s), k0, m0);
                     }
                     tma_load_2d(sB0 + s * kStageBBytes, &tmB, full_bar(s), n0, k0);
-                    issued_round[s] = round;
-                }
-                // Drain: wait until every copy this thread issued has landed.
+                } else {
+                    // cp.async: PW warps copy 4-byte elements with zero fill;
+                    // every lane's copies arrive on the full barrier.
+                    const uint32_t sa = sA0 + s * kStageABytes;
+                    const uint32_t sb = sB0 + s * kStageBBytes;
+                    {  // A slice: 128 rows x 32 floats; lane = column, warp pw
+                       // takes rows pw, pw + PW, ...
+                        const int k = k0 + lane;
+                        const bool kin = k < p.K;
+                        for (int r = pw; r < kBM; r += PW) {
+                            const int m = m0 + r;
+                            const bool in = kin && m < p.M;
+                            const float* src = in ? p.A + static_cast<long long>(m) * p.lda + k : p.A;
+                            cp_async_4(sa + swz128(r, lane), src, in ? 4u : 0u);
+                        }
+                    }
+                    // B slice: 32 rows x 128 floats; lane = column within a
+                    // 32-wide strip, warp pw takes rows pw, pw + PW, ...
+                    for (int r = pw; r < kBK; r += PW) {
+                        const int k = k0 + r;
+                        const bool kin = k < p.K;
 #pragma unroll
-                for (int s = 0; s < STAGES; ++s) {
+                        for (int q = 0; q < kBN / 32; ++q) {
+                            const int n = n0 + q * 32 + lane;
+                            const bool in = kin && n < p.N;
+                            const float* src = in ? p.B + static_cast<long long>(k) * p.ldb + n : p.B;
+                            cp_async_4(sb + static_cast<uint32_t>(r * (kBN * 4) + (q * 32 + lane) * 4), src,
+                                       in ? 4u : 0u);
+                        }
+                    }
+                    cp_async_mbar_arrive_noinc(full_bar(s));
+                }
+                issued_round[s] = round;
+            }
+        }
+        // Drain: every copy this producer issued has landed before it leaves.
+        if (PRODUCER == kProducerTma) {
+            if (lane == 0) {
+#pragma unroll
+                for (int s = 0; s < STAGES; ++s)
                     if (issued_round[s] >= 0 && !mbar_wait_bounded(full_bar(s), issued_round[s] & 1, tmo))
                         timed_out = true;
-                }
             }
         } else {
-            // cp.async producer: PW warps copy 4-byte elements with zero fill;
-            // every lane's copies arrive on the full barrier (32 * PW arrivals).
-            for (int it = 0; it < nkt; ++it) {
-                const int s = it % STAGES;
-                const int round = it / STAGES;
-                if (round > 0 && !mbar_wait_bounded_warp(empty_bar(s), (round - 1) & 1, tmo)) {
-                    timed_out = true;
-                    break;
-                }
-                if (skip_here && it == p.skip_stage - 1) continue;
-                const int k0 = (kt_begin + it) * kBK;
-                const uint32_t sa = sA0 + s * kStageABytes;
-                const uint32_t sb = sB0 + s * kStageBBytes;
-                // A slice: 128 rows x 32 floats; lane = column, warp pw takes
-                // rows pw, pw + PW, ...
-                {
-                    const int k = k0 + lane;
-                    const bool kin = k < p.K;
-                    for (int r = pw; r < kBM; r += PW) {
-                        const int m = m0 + r;
-                        const bool in = kin && m < p.M;
-                        const float* src = in ? p.A + static_cast<long long>(m) * p.lda + k : p.A;
-                        cp_async_4(sa + swz128(r, lane), src, in ? 4u : 0u);
-                    }
-                }
-                // B slice: 32 rows x 128 floats; lane = column within a 32-wide
-                // strip, warp pw takes rows pw, pw + PW, ...
-                for (int r = pw; r < kBK; r += PW) {
-                    const int k = k0 + r;
-                    const bool kin = k < p.K;
-#pragma unroll
-                    for (int q = 0; q < kBN / 32; ++q) {
-                        const int n = n0 + q * 32 + lane;
-                        const bool in = kin && n < p.N;
-                        const float* src = in ? p.B + static_cast<long long>(k) * p.ldb + n : p.B;
-                        cp_async_4(sb + static_cast<uint32_t>(r * (kBN * 4) + (q * 32 + lane) * 4), src,
-                                   in ? 4u : 0u);
-                    }
-                }
-                cp_async_mbar_arrive_noinc(full_bar(s));
-            }
             cp_async_wait_all();
         }
         if (timed_out) atomicOr(p.status, kStatusTimeout);
@@ -273,11 +318,42 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), 1)
 #pragma unroll
     for (int i = 0; i < 8; ++i)
 #pragma unroll
-        for (int q = 0; q < 4; ++q) acc[i][q] = make_float2(0.f, 0.f);
-
+        for (int q = 0; q < 4; ++q) acc[i][q] = make_float2(0.f, 0.f);  // (K == 0: the empty sum)
     const int wm = warp >> 1, wn = warp & 1;
     const int tm = (lane & 1) | (((lane >> 2) & 1) << 1);
     const int tn = ((lane >> 1) & 1) | (((lane >> 3) & 1) << 1) | (((lane >> 4) & 1) << 2);
+
+    // Partial tiles (split-K through distributed shared memory, stream-K
+    // through global memory) use the layout [e4 = 0..15][thread = 0..255][4
+    // floats]; element group e4 = i*2 + h holds acc[i][2h] and acc[i][2h+1]
+    // (four columns).  Consecutive threads touch consecutive 16-byte words, so
+    // every partial store and load is conflict-free and coalesced.
+    auto store_c = [&](int tile) {
+        const int row0 = (tile / p.tiles_n) * kBM + wm * 32 + tm;
+        const int col0 = (tile % p.tiles_n) * kBN + wn * 64 + tn * 4;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int r = row0 + 4 * i;
+            if (r >= p.M) continue;
+            float* crow = p.C + static_cast<long long>(r) * p.ldc;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int c = col0 + 32 * h;
+                const float4 v =
+                    make_float4(acc[i][2 * h].x, acc[i][2 * h].y, acc[i][2 * h + 1].x, acc[i][2 * h + 1].y);
+                if (p.vec_store && c + 3 < p.N) {
+                    *reinterpret_cast<float4*>(crow + c) = v;
+                } else {
+                    if (c < p.N) crow[c] = v.x;
+                    if (c + 1 < p.N) crow[c + 1] = v.y;
+                    if (c + 2 < p.N) crow[c + 2] = v.z;
+                    if (c + 3 < p.N) crow[c + 3] = v.w;
+                }
+            }
+        }
+    };
+    auto consumer_sync = [] { asm volatile("bar.sync 1, %0;" ::"n"(kConsumerThreads) : "memory"); };
+
     if (!is_producer) {
         // Byte offsets inside a stage.  A row r = wm*32 + tm + 4i has r mod 8 =
         // tm + 4*(i & 1), so even i share one swizzle key and odd i the other.
@@ -286,52 +362,122 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), 1)
         const uint8_t* const smem_a = smem + a_row0;                          // generic pointers
         const uint8_t* const smem_b = smem + STAGES * kStageABytes + b_col0;  // for the vector loads
 
-        for (int it = 0; it < nkt; ++it) {
-            const int s = it % STAGES;
-            const int round = it / STAGES;
-            if (!mbar_wait_bounded_warp(full_bar(s), round & 1, tmo)) {
-                timed_out = true;
-                break;
-            }
-            const uint8_t* sa = smem_a + s * kStageABytes;
-            const uint8_t* sb = smem_b + s * kStageBBytes;
+        int it = 0;
+        Work work = work0;
+        int tile, kb, ke;
+        while (!timed_out && work.next(tile, kb, ke)) {
 #pragma unroll
-            for (int kg = 0; kg < kBK / 4; ++kg) {
-                const uint32_t xe = static_cast<uint32_t>(((kg ^ tm) & 7) << 4);
-                const uint32_t xo = xe ^ 64u;
-                float4 a[8];
+            for (int i = 0; i < 8; ++i)
 #pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    a[i] = *reinterpret_cast<const float4*>(sa + i * 512 + ((i & 1) ? xo : xe));
+                for (int q = 0; q < 4; ++q) acc[i][q] = make_float2(0.f, 0.f);
+
+            for (int kt = kb; kt < ke; ++kt, ++it) {
+                const int s = it % STAGES;
+                const int round = it / STAGES;
+                if (!mbar_wait_bounded_warp(full_bar(s), round & 1, tmo)) {
+                    timed_out = true;
+                    break;
+                }
+                const uint8_t* sa = smem_a + s * kStageABytes;
+                const uint8_t* sb = smem_b + s * kStageBBytes;
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    const int k = kg * 4 + kk;
-                    const float4 b0 = *reinterpret_cast<const float4*>(sb + k * (kBN * 4));
-                    const float4 b1 = *reinterpret_cast<const float4*>(sb + k * (kBN * 4) + 128);
-                    const float2 bp[4] = {make_float2(b0.x, b0.y), make_float2(b0.z, b0.w),
-                                          make_float2(b1.x, b1.y), make_float2(b1.z, b1.w)};
-                    // Column pair outermost: each B pair feeds 8 consecutive
-                    // multiply-adds (measured faster than row-outermost order).
+                for (int kg = 0; kg < kBK / 4; ++kg) {
+                    const uint32_t xe = static_cast<uint32_t>(((kg ^ tm) & 7) << 4);
+                    const uint32_t xo = xe ^ 64u;
+                    float4 a[8];
 #pragma unroll
-                    for (int q = 0; q < 4; ++q)
+                    for (int i = 0; i < 8; ++i)
+                        a[i] = *reinterpret_cast<const float4*>(sa + i * 512 + ((i & 1) ? xo : xe));
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            const float av = kk == 0 ? a[i].x : kk == 1 ? a[i].y : kk == 2 ? a[i].z : a[i].w;
-                            if (MATH == kMathFfma2) {
-                                acc[i][q] = __ffma2_rn(make_float2(av, av), bp[q], acc[i][q]);
-                            } else {
-                                acc[i][q].x = fmaf(av, bp[q].x, acc[i][q].x);
-                                acc[i][q].y = fmaf(av, bp[q].y, acc[i][q].y);
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const int k = kg * 4 + kk;
+                        const float4 b0 = *reinterpret_cast<const float4*>(sb + k * (kBN * 4));
+                        const float4 b1 = *reinterpret_cast<const float4*>(sb + k * (kBN * 4) + 128);
+                        const float2 bp[4] = {make_float2(b0.x, b0.y), make_float2(b0.z, b0.w),
+                                              make_float2(b1.x, b1.y), make_float2(b1.z, b1.w)};
+                        // Column pair outermost: each B pair feeds 8 consecutive
+                        // multiply-adds (measured faster than row-outermost order).
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) {
+                                const float av = kk == 0 ? a[i].x : kk == 1 ? a[i].y : kk == 2 ? a[i].z : a[i].w;
+                                if (MATH == kMathFfma2) {
+                                    acc[i][q] = __ffma2_rn(make_float2(av, av), bp[q], acc[i][q]);
+                                } else {
+                                    acc[i][q].x = fmaf(av, bp[q].x, acc[i][q].x);
+                                    acc[i][q].y = fmaf(av, bp[q].y, acc[i][q].y);
+                                }
                             }
-                        }
+                    }
+                }
+                // Every load from stage s has returned (its values were
+                // consumed above): release the slot to the producer(s).
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(empty_bar(s));
+                    if (mcast > 1) mbar_arrive_cluster(empty_bar(s), crank ^ 1u);
                 }
             }
-            // Every load from stage s has returned (its values were consumed
-            // above): release the slot to the producer(s).
-            __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(empty_bar(s));
-                if (mcast > 1) mbar_arrive_cluster(empty_bar(s), crank ^ 1u);
+            if (!p.sk || timed_out) break;  // one tile per CTA; its epilogue follows below
+
+            // ---------------------------------------------------- stream-K epilogue
+            float* const ws_mine = p.ws + static_cast<size_t>(blockIdx.x) * (kBM * kBN);
+            if (kb > 0) {
+                // Not the first K slice of the tile: leave the partial tile for
+                // the CTA that holds the first slice.
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+#pragma unroll
+                    for (int h = 0; h < 2; ++h)
+                        __stcg(reinterpret_cast<float4*>(ws_mine) + (i * 2 + h) * kConsumerThreads + threadIdx.x,
+                               make_float4(acc[i][2 * h].x, acc[i][2 * h].y, acc[i][2 * h + 1].x,
+                                           acc[i][2 * h + 1].y));
+                consumer_sync();
+                if (threadIdx.x == 0) {
+                    __threadfence();
+                    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p.flags + blockIdx.x), "r"(1u)
+                                 : "memory");
+                }
+            } else {
+                if (ke < NK) {
+                    // First slice but not the whole K range: add the partial
+                    // tiles of the CTAs whose runs start inside this tile, in
+                    // CTA order (a fixed order: deterministic sums).
+                    const long long tile_end = static_cast<long long>(tile - sk_tile0 + 1) * NK;  // in units
+                    for (long long g2 = blockIdx.x + 1; g2 < G && (p.sk_units * g2) / G < tile_end; ++g2) {
+                        bool ok = true;
+                        if (threadIdx.x == 0) {
+                            const uint64_t t0 = global_timer_ns();
+                            unsigned int f = 0;
+                            while (true) {
+                                asm volatile("ld.acquire.gpu.global.u32 %0, [%1];"
+                                             : "=r"(f)
+                                             : "l"(p.flags + g2)
+                                             : "memory");
+                                if (f != 0u) break;
+                                if (global_timer_ns() - t0 > tmo) {
+                                    ok = false;
+                                    break;
+                                }
+                            }
+                            if (!ok) atomicOr(p.status, kStatusTimeout);
+                        }
+                        consumer_sync();  // thread 0 saw the flag: the partial is complete
+                        const float4* src = reinterpret_cast<const float4*>(p.ws + g2 * (kBM * kBN));
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+#pragma unroll
+                            for (int h = 0; h < 2; ++h) {
+                                const float4 v = __ldcg(src + (i * 2 + h) * kConsumerThreads + threadIdx.x);
+                                acc[i][2 * h].x += v.x;
+                                acc[i][2 * h].y += v.y;
+                                acc[i][2 * h + 1].x += v.z;
+                                acc[i][2 * h + 1].y += v.w;
+                            }
+                    }
+                }
+                store_c(tile);
             }
         }
         if (timed_out) atomicOr(p.status, kStatusTimeout);
@@ -342,10 +488,6 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), 1)
         // All consumer reads of the ring are finished once every thread of the
         // CTA passes this barrier; the ring is then reused for the partial tile.
         __syncthreads();
-        // Partial layout: [e4 = 0..15][thread = 0..255][4 floats]; element
-        // group e4 = i*2 + h holds acc[i][2h] and acc[i][2h+1] (four columns).
-        // Consecutive threads write consecutive 16-byte words, so both the
-        // local stores and the remote vector loads are free of bank conflicts.
         if (!is_producer && crank != 0) {
 #pragma unroll
             for (int i = 0; i < 8; ++i)
@@ -379,30 +521,10 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), 1)
         cluster_sync_all();
     }
 
-    if (is_producer) return;
+    if (is_producer || p.sk) return;  // (stream-K CTAs stored their tiles above)
 
     // ------------------------------------------------------------ epilogue
-    const int row0 = m0 + wm * 32 + tm;
-    const int col0 = n0 + wn * 64 + tn * 4;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const int r = row0 + 4 * i;
-        if (r >= p.M) continue;
-        float* crow = p.C + static_cast<long long>(r) * p.ldc;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int c = col0 + 32 * h;
-            const float4 v = make_float4(acc[i][2 * h].x, acc[i][2 * h].y, acc[i][2 * h + 1].x, acc[i][2 * h + 1].y);
-            if (p.vec_store && c + 3 < p.N) {
-                *reinterpret_cast<float4*>(crow + c) = v;
-            } else {
-                if (c < p.N) crow[c] = v.x;
-                if (c + 1 < p.N) crow[c + 1] = v.y;
-                if (c + 2 < p.N) crow[c + 2] = v.z;
-                if (c + 3 < p.N) crow[c + 3] = v.w;
-            }
-        }
-    }
+    store_c(p.tile_base + static_cast<int>(blockIdx.x));
 }
 
 }  // namespace gb300

@@ -20,9 +20,11 @@
  * inputs whose every partial sum is an integer below 2^24 in magnitude (for
  * example entries in {-8..8} with K <= 2^18) give the exact result.
  *
- * Memory.  A, B and C are DEVICE pointers owned by the caller; the library
- * allocates no device memory.  C must not overlap A or B.  Rows may be padded
- * (ld > row width); padding is never written and never read.
+ * Memory.  A, B and C are DEVICE pointers owned by the caller.  C must not
+ * overlap A or B.  Rows may be padded (ld > row width); padding is never
+ * written and never read.  The only device memory the library takes is the
+ * stream-K workspace (see sgemm_options.stream_k), from its own stream-
+ * ordered pool.
  *
  * Streams.  `stream` is a cudaStream_t passed as void* (NULL selects the legacy
  * default stream).  Every call enqueues work on that stream and returns without
@@ -130,6 +132,16 @@ typedef struct sgemm_options {
                              ways along K (only when split_k resolves to 1,
                              the grid exceeds one wave and K has at least
                              4 x tail_split slices of 32) */
+    int stream_k;         /* 0 = auto, 1 = off, 2 = on: one CTA per SM; all
+                             but the last full wave of tiles run whole, the
+                             rest is dealt out evenly as (tile, K slice)
+                             units; a tile shared by several CTAs is finished
+                             by the CTA holding its first K slice from the
+                             others' partial tiles.  Needs a workspace of
+                             CTAs x (64 KiB + 4 bytes), taken per call from a
+                             stream-ordered pool the library creates on the
+                             device (cudaMallocFromPoolAsync / cudaFreeAsync
+                             on `stream`), which keeps it for reuse. */
 } sgemm_options;
 
 /* sgemm_f32 with forced choices.  Same contract; an unsupported combination

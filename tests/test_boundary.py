@@ -82,7 +82,7 @@ def test_empty_output_is_a_noop_without_device():
 
 def test_bad_options_rejected():
     lib = _lib.load()
-    opt = _lib.Options(0, 0, 0, 0, 0, -1, 0, 0)  # negative debug_skip_stage
+    opt = _lib.Options(0, 0, 0, 0, 0, -1, 0, 0, 0)  # negative debug_skip_stage
     assert lib.sgemm_f32_ex(4, 4, 4, FAKE_A, 4, FAKE_B, 4, FAKE_C, 4, None, ctypes.byref(opt)) == _lib.ERR_INVALID_ARG
 
 

@@ -91,6 +91,8 @@ VARIANTS = (
     + [dict(producer=1, math=2, multicast=2, split_k=1, stages=s) for s in (2, 6)]
     + [dict(producer=pr, math=m, split_k=s, multicast=1) for pr in (1, 2) for m in (1, 2) for s in (2, 3, 4, 8)]
     + [dict(producer=2, math=m, stages=s, split_k=1) for m in (1, 2) for s in (2, 4)]
+    + [dict(producer=pr, math=m, stream_k=2) for pr in (1, 2) for m in (1, 2)]
+    + [dict(stream_k=2, stages=s) for s in (2, 6)]
 )
 
 
@@ -125,6 +127,32 @@ def test_tail_split(tail):
     Ai, Bi = make_operands(M, N, K, "int", 42)
     Ci = g.sgemm_f32_ex(to_device(Ai), to_device(Bi), tail_split=tail).cpu().numpy()
     check(Ci, oracle.gemm_f64(Ai.numpy(), Bi.numpy(), with_bound=False)[0], None, exact=True, what=f"tail {tail} int")
+
+
+@pytest.mark.parametrize("name", ["square_2048", "ragged_1023x1025x1027", "flat_4096x4096x256",
+                                  "skinny_8192x128x8192"])
+def test_stream_k_every_element(name):
+    """Stream-K: one CTA per SM, tiles shared between CTAs finished through
+    the workspace; every element against the oracle, and bitwise repeatable."""
+    p = PROBLEMS[name]
+    A, B = problem_operands(p)
+    C = run(A, B, stream_k=2)
+    C64, bound = oracle.gemm_f64(A.numpy(), B.numpy())
+    check(C, C64, bound, exact=False, what=f"{name} stream-K")
+    assert np.array_equal(C, run(A, B, stream_k=2))
+    Ai, Bi = problem_operands(p.int_variant())
+    check(run(Ai, Bi, stream_k=2), oracle.gemm_f64(Ai.numpy(), Bi.numpy(), with_bound=False)[0], None,
+          exact=True, what=f"{name} stream-K int")
+
+
+@pytest.mark.parametrize("dist", ["real", "int"])
+def test_stream_k_sampled_rows_4096(dist):
+    p = PROBLEMS["square_4096"] if dist == "real" else PROBLEMS["square_4096"].int_variant()
+    A, B = problem_operands(p)
+    C = run(A, B, stream_k=2)
+    rows = sample_rows(p.M, n_random=8, seed=p.seed)
+    C64, bound = oracle.gemm_rows_f64(A.numpy(), B.numpy(), rows)
+    check(C[rows], C64, bound, exact=(dist == "int"), what=f"{p.name} stream-K rows")
 
 
 def test_forced_tma_rejects_unaligned_rows():
@@ -261,10 +289,10 @@ def test_variant_choice():
         return g.describe(torch.empty((M, K), device="cuda"), torch.empty((K, N), device="cuda"))
 
     assert desc(4096, 4096, 4096).startswith("tma/")
-    assert "/s1/" in desc(4096, 4096, 4096)
+    assert "/s1/" in desc(4096, 4096, 4096) and "/sk" in desc(4096, 4096, 4096)  # stream-K
     assert "/tail" not in desc(4096, 4096, 4096)  # the tail split is opt-in
-    assert "/s1/" not in desc(8192, 128, 8192)  # skinny output: split-K
-    assert "/s1/" not in desc(128, 8192, 16384)
+    assert "/sk" in desc(8192, 128, 8192) and "/sk" in desc(128, 8192, 16384)
+    assert "/sk" not in desc(256, 256, 256) and "/s1/" not in desc(256, 256, 256)  # tiny: cluster split-K
     assert desc(1023, 1025, 1027).startswith("cpasync/")  # 1027-float rows are not 16-byte multiples
 
 
@@ -279,6 +307,8 @@ def test_timeout_is_reported_and_recovers():
     assert g.check_status() == 0
     for producer in (1, 2):
         g.sgemm_f32_ex(dA, dB, producer=producer, split_k=1, debug_skip_stage=3, timeout_ns=20_000_000)
+        assert g.check_status() == 4
+        g.sgemm_f32_ex(dA, dB, producer=producer, stream_k=2, debug_skip_stage=1, timeout_ns=20_000_000)
         assert g.check_status() == 4
     C = g.sgemm_f32(dA, dB)
     assert g.check_status() == 0
