@@ -17,6 +17,7 @@ from ._lib import Options, SgemmError
 __all__ = [
     "sgemm_f32",
     "sgemm_f32_ex",
+    "sgemm_f32_noalloc",
     "sgemm_3xtf32",
     "sgemm_3xtf32_ex",
     "sgemm_f32_host",
@@ -74,6 +75,16 @@ def _call(fn_name, A, B, out, stream, opt=None):
 def sgemm_f32(A: torch.Tensor, B: torch.Tensor, out: torch.Tensor | None = None, *, stream=None) -> torch.Tensor:
     """C = A @ B on the CUDA cores (float32 FFMA kernels), enqueued on ``stream``."""
     return _call("sgemm_f32", A, B, out, stream)
+
+
+def sgemm_f32_noalloc(A: torch.Tensor, B: torch.Tensor, out: torch.Tensor, *, stream=None) -> torch.Tensor:
+    """sgemm_f32 without any device allocation in the call: the stream-K
+    scratch comes from a fixed array inside the library (shared by all calls
+    on the device: calls that overlap on the GPU race).  ``out`` is required,
+    so this wrapper allocates nothing either."""
+    if out is None:
+        raise ValueError("sgemm_f32_noalloc needs a preallocated `out`")
+    return _call("sgemm_f32_noalloc", A, B, out, stream)
 
 
 def sgemm_3xtf32(A: torch.Tensor, B: torch.Tensor, out: torch.Tensor | None = None, *, stream=None) -> torch.Tensor:

@@ -21,6 +21,16 @@ namespace gb300 {
 // Sticky per-device status word; kernels OR error bits into it.
 __device__ unsigned int g_sgemm_status = 0;
 
+// Scratch of sgemm_f32_noalloc: room for the stream-K partial tiles and
+// ready flags of up to kNoAllocMaxCtas CTAs (10 MiB + 640 bytes), a
+// file-scope device array so that the entry point needs no allocation.  Every
+// GPU that loads the library holds it until the process exits; all calls on a
+// device share it.
+constexpr int kNoAllocMaxCtas = 160;
+constexpr size_t kNoAllocTileFloats = static_cast<size_t>(kBM) * kBN;
+constexpr size_t kNoAllocFloats = kNoAllocMaxCtas * kNoAllocTileFloats + kNoAllocMaxCtas;
+static __device__ __align__(256) float g_noalloc_scratch[kNoAllocFloats];
+
 namespace {
 
 constexpr int kMaxDevices = 64;
@@ -37,6 +47,9 @@ struct DeviceState {
     unsigned int* status_word = nullptr;  // device address of g_sgemm_status
     std::once_flag pool_once;
     cudaMemPool_t pool = nullptr;  // library-owned pool for per-call workspaces
+    std::once_flag noalloc_once;
+    int noalloc_status = SGEMM_ERR_CUDA;  // result of looking up g_noalloc_scratch
+    float* noalloc_scratch = nullptr;     // its device address on this device
 };
 
 DeviceState g_dev[kMaxDevices];
@@ -481,6 +494,109 @@ int run_ffma(int M, int N, int K, const float* A, int lda, const float* B, int l
     return SGEMM_OK;
 }
 
+// sgemm_f32 with the stream-K workspace in g_noalloc_scratch instead of a
+// pool allocation (see sgemm_f32_noalloc in include/sgemm.h).
+int run_ffma_noalloc(int M, int N, int K, const float* A, int lda, const float* B, int ldb, float* C, int ldc,
+                     void* stream) {
+    int rc = validate(M, N, K, A, lda, B, ldb, C, ldc);
+    if (rc != SGEMM_OK) return rc;
+    if (M == 0 || N == 0) return SGEMM_OK;
+    int dev = 0;
+    DeviceState* st = nullptr;
+    rc = current_device(&dev, &st);
+    if (rc != SGEMM_OK) return rc;
+    // Set-up, once per device with that device current: the host-side name
+    // g_noalloc_scratch is only a stand-in; the kernel needs the array's
+    // device address.
+    std::call_once(st->noalloc_once, [&] {
+        void* addr = nullptr;
+        if (cudaGetSymbolAddress(&addr, g_noalloc_scratch) != cudaSuccess || !addr) {
+            (void)cudaGetLastError();
+            st->noalloc_status = SGEMM_ERR_CUDA;
+            return;
+        }
+        st->noalloc_scratch = static_cast<float*>(addr);
+        st->noalloc_status = SGEMM_OK;
+    });
+    if (st->noalloc_status != SGEMM_OK) return st->noalloc_status;
+
+    // Plan: stream-K whenever there is a K slice to deal out (K == 0 runs the
+    // plain grid, which writes zeros and needs no scratch).
+    sgemm_options o = {};
+    o.stream_k = K > 0 ? 2 : 1;
+    o.split_k = K > 0 ? 0 : 1;
+    Plan pl;
+    rc = make_plan(*st, M, N, K, A, lda, B, ldb, &o, &pl);
+    if (rc != SGEMM_OK) return rc;
+    if (pl.sk && pl.launch[0].tiles > kNoAllocMaxCtas) pl.launch[0].tiles = kNoAllocMaxCtas;
+    const size_t G = pl.sk ? static_cast<size_t>(pl.launch[0].tiles) : 0;
+    if (G * kNoAllocTileFloats + G > kNoAllocFloats) return SGEMM_ERR_INVALID_ARG;  // cannot happen with the cap
+
+    const KernelEntry k =
+        pl.producer == kProducerTma ? ffma_kernel_tma(pl.stages, pl.math) : ffma_kernel_cpasync(pl.stages, pl.math);
+    if (!k.fn) return SGEMM_ERR_INVALID_ARG;
+    alignas(64) CUtensorMap tmA;
+    alignas(64) CUtensorMap tmB;
+    std::memset(&tmA, 0, sizeof tmA);
+    std::memset(&tmB, 0, sizeof tmB);
+    if (pl.producer == kProducerTma) {
+        rc = encode_2d(&tmA, A, K, M, lda, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B);
+        if (rc == SGEMM_OK) rc = encode_2d(&tmB, B, N, K, ldb, kBN, kBK, CU_TENSOR_MAP_SWIZZLE_NONE);
+        if (rc != SGEMM_OK) return rc;
+    }
+
+    FfmaParams prm;
+    std::memset(&prm, 0, sizeof prm);
+    prm.M = M;
+    prm.N = N;
+    prm.K = K;
+    prm.A = A;
+    prm.lda = lda;
+    prm.B = B;
+    prm.ldb = ldb;
+    prm.C = C;
+    prm.ldc = ldc;
+    prm.num_k_tiles = pl.num_k_tiles;
+    prm.split = 1;
+    prm.mcast = 1;
+    prm.vec_store = ((reinterpret_cast<uintptr_t>(C) & 15u) == 0 && ldc % 4 == 0) ? 1 : 0;
+    prm.tile_base = 0;
+    prm.tiles_n = pl.tiles_n;
+    prm.timeout_ns = kDefaultTimeoutNs;
+    prm.status = st->status_word;
+    prm.sk = pl.sk;
+    prm.sk_dp_tiles = pl.sk_dp_tiles;
+    prm.sk_units = (static_cast<long long>(pl.tiles_n) * ceil_div(M, kBM) - pl.sk_dp_tiles) * pl.num_k_tiles;
+    const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    if (pl.sk) {
+        // Partial tiles are written before they are read; the ready flags
+        // must start at zero, and the array keeps the previous call's.
+        prm.ws = st->noalloc_scratch;
+        prm.flags = reinterpret_cast<unsigned int*>(st->noalloc_scratch + kNoAllocMaxCtas * kNoAllocTileFloats);
+        if (cudaMemsetAsync(prm.flags, 0, G * sizeof(unsigned int), cs) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return SGEMM_ERR_CUDA;
+        }
+    }
+
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(pl.launch[0].tiles), 1, 1);
+    cfg.blockDim = dim3(k.threads, 1, 1);
+    cfg.dynamicSmemBytes = static_cast<size_t>(k.smem_bytes);
+    cfg.stream = cs;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeCooperative;  // finishing CTAs wait on later CTAs
+    attr.val.cooperative = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = pl.sk ? 1 : 0;
+    void* args[3] = {&tmA, &tmB, &prm};
+    if (cudaLaunchKernelExC(&cfg, k.fn, args) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return SGEMM_ERR_CUDA;
+    }
+    return SGEMM_OK;
+}
+
 int run_3xtf32(int M, int N, int K, const float* A, int lda, const float* B, int ldb, float* C, int ldc,
                void* stream, const sgemm_options* opt) {
     int rc = validate(M, N, K, A, lda, B, ldb, C, ldc);
@@ -550,6 +666,11 @@ int sgemm_f32(int M, int N, int K, const float* A, int lda, const float* B, int 
 int sgemm_f32_ex(int M, int N, int K, const float* A, int lda, const float* B, int ldb, float* C, int ldc,
                  void* stream, const sgemm_options* opt) {
     return run_ffma(M, N, K, A, lda, B, ldb, C, ldc, stream, opt);
+}
+
+int sgemm_f32_noalloc(int M, int N, int K, const float* A, int lda, const float* B, int ldb, float* C, int ldc,
+                      void* stream) {
+    return run_ffma_noalloc(M, N, K, A, lda, B, ldb, C, ldc, stream);
 }
 
 int sgemm_3xtf32(int M, int N, int K, const float* A, int lda, const float* B, int ldb, float* C, int ldc,

@@ -90,6 +90,46 @@ int sgemm_f32(int M, int N, int K,
               void* stream);
 
 /*
+ * sgemm_f32_noalloc -- sgemm_f32 for callers that cannot allocate device
+ * memory while a call is made.  (The pages this library follows have no
+ * counterpart of this entry point.)
+ *
+ * Who needs it: programs that must keep a fixed device-memory footprint or
+ * that hand all device memory to their own allocator up front (a framework's
+ * caching allocator, a serving process that reserves everything at start),
+ * and latency-critical loops in which a pool allocation could block or fail.
+ * sgemm_f32 takes its stream-K scratch from a stream-ordered pool at every
+ * call; this entry point takes it from a fixed device array compiled into the
+ * library instead, and calls no cudaMalloc, cudaFree or other allocating
+ * routine.  It clears the scratch's ready flags with cudaMemsetAsync on
+ * `stream`, which allocates nothing.
+ *
+ * Same operation, arguments, accuracy contract and errors as sgemm_f32.  It
+ * always runs the FFMA kernel with the stream-K schedule (K == 0: the plain
+ * grid, which needs no scratch).
+ *
+ * Limits and rules:
+ *  - The array holds the scratch of at most 160 CTAs: 160 x 64 KiB partial
+ *    tiles + 160 flags = 10 MiB + 640 bytes on every GPU that loads the
+ *    library, kept until the process exits.  A call uses one CTA per SM, at
+ *    most 160 (a GPU with more SMs still gets a correct, slower result); the
+ *    scratch a call needs is bounded by that count, not by M, N or K, and a
+ *    call that would need more is rejected with SGEMM_ERR_INVALID_ARG.
+ *  - All calls on a device share the array, which keeps the last call's
+ *    contents: calls that overlap on the GPU (on different streams, or from
+ *    different host threads) race on it and give wrong results.  Order them
+ *    on one stream or synchronise between them.
+ *  - The first call on each device looks up the array's device address (the
+ *    name in host code is only a stand-in) with that device current; make
+ *    that first call before any stream capture.
+ */
+int sgemm_f32_noalloc(int M, int N, int K,
+                      const float* A, int lda,
+                      const float* B, int ldb,
+                      float* C, int ldc,
+                      void* stream);
+
+/*
  * sgemm_3xtf32 -- same operation, signature, accuracy contract and error
  * behaviour as sgemm_f32, computed on the tensor cores (tcgen05): each operand
  * is split into a TF32 "big" part, big = tf32(x), and a TF32 "small" part,
