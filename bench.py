@@ -402,6 +402,8 @@ SWEEP_OPTIONS = [
     {"stages": 2},
     {"stages": 6},
     {"producer": 2},
+    {"producer": 3},
+    {"producer": 3, "split_k": 1},
     {"split_k": 1},
     {"split_k": 2},
     {"split_k": 4},

@@ -11,6 +11,10 @@ struct KernelEntry {
 
 // FFMA kernels fed by tensor-map bulk copies; stages in {1,2,3,4,5,6}, math 1 = FFMA, 2 = paired FFMA.
 KernelEntry ffma_kernel_tma(int stages, int math);
+// The same with the producer in a warpgroup of its own and the register split
+// (producer 40, consumers 232 registers per thread); launched only when the
+// kernel was built with exactly 168 registers per thread.
+KernelEntry ffma_kernel_tma_wg(int stages, int math);
 // FFMA kernels fed by 4-byte cp.async (any alignment); stages in {2,4}.
 KernelEntry ffma_kernel_cpasync(int stages, int math);
 // Three-product TF32 kernel on the tensor cores (TMA-fed, 128 x 128 tiles,

@@ -2,9 +2,9 @@
 // tensor-map bulk copies (TMA) with optional cluster multicast, cp.async with
 // zero fill, cluster ranks / barriers / distributed shared memory, the
 // fifth-generation tensor core (tcgen05: tensor-memory allocation, MMA,
-// commit, tensor-memory loads, fences), TF32 rounding, and the global
-// nanosecond timer used to bound every wait.  Each wrapper is written from the
-// PTX ISA description of the instruction it emits.
+// commit, tensor-memory loads, fences), warpgroup register limits, TF32
+// rounding, and the global nanosecond timer used to bound every wait.  Each
+// wrapper is written from the PTX ISA description of the instruction it emits.
 #pragma once
 
 #include <cstdint>
@@ -168,6 +168,23 @@ __device__ __forceinline__ float4 lds128(uint32_t addr) {
 __device__ __forceinline__ void sts128(uint32_t addr, float4 v) {
     asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w)
                  : "memory");
+}
+
+// ---------------------------------------------------------------- registers
+
+// Per-thread register limit of the calling warpgroup (all four warps must
+// execute the same instruction).  `dec` returns registers to the CTA's pool;
+// `inc` takes them from it and waits until enough are free.  N is a multiple
+// of 8 in [24, 256].
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+    static_assert(N % 8 == 0 && N >= 24 && N <= 256, "register count");
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+    static_assert(N % 8 == 0 && N >= 24 && N <= 256, "register count");
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
 }
 
 // ---------------------------------------------------------------- async proxy

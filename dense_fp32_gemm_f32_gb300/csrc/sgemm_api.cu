@@ -44,6 +44,7 @@ struct DeviceState {
     int sm_count = 0;
     int max_clusters_pair = 0;    // co-resident 2-CTA clusters of the FFMA kernel
     int max_clusters_split[9] = {0};
+    bool regsplit_ok = false;     // the register-split kernels were built at kRegsLaunch registers
     unsigned int* status_word = nullptr;  // device address of g_sgemm_status
     std::once_flag pool_once;
     cudaMemPool_t pool = nullptr;  // library-owned pool for per-call workspaces
@@ -117,9 +118,21 @@ int init_device(int dev, DeviceState& st) {
         return SGEMM_ERR_CUDA;
     }
     st.status_word = static_cast<unsigned int*>(addr);
+    st.regsplit_ok = true;
     for (int math = kMathFfma; math <= kMathFfma2; ++math) {
-        for (int s = 1; s <= 6; ++s)
+        for (int s = 1; s <= 6; ++s) {
             if (set_smem_attr(ffma_kernel_tma(s, math)) != SGEMM_OK) return SGEMM_ERR_CUDA;
+            // setmaxnreg.inc waits until the registers it asks for are free;
+            // the split adds up to kRegsLaunch per thread of the CTA, so a
+            // kernel built with any other count must never be launched.
+            const KernelEntry wg = ffma_kernel_tma_wg(s, math);
+            if (set_smem_attr(wg) != SGEMM_OK) return SGEMM_ERR_CUDA;
+            cudaFuncAttributes fa;
+            if (!wg.fn || cudaFuncGetAttributes(&fa, wg.fn) != cudaSuccess || fa.numRegs != kRegsLaunch) {
+                (void)cudaGetLastError();
+                st.regsplit_ok = false;
+            }
+        }
         for (int s = 1; s <= 6; ++s)
             if (set_smem_attr(ffma_kernel_cpasync(s, math)) != SGEMM_OK) return SGEMM_ERR_CUDA;
     }
@@ -219,6 +232,26 @@ struct Plan {
 
 long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
 
+bool is_tma(int producer) { return producer == kProducerTma || producer == kProducerTmaWg; }
+
+KernelEntry ffma_kernel(const Plan& pl) {
+    switch (pl.producer) {
+        case kProducerTma: return ffma_kernel_tma(pl.stages, pl.math);
+        case kProducerTmaWg: return ffma_kernel_tma_wg(pl.stages, pl.math);
+        case kProducerCpAsync: return ffma_kernel_cpasync(pl.stages, pl.math);
+    }
+    return {nullptr, 0, 0};
+}
+
+const char* producer_name(int producer) {
+    switch (producer) {
+        case kProducerTma: return "tma";
+        case kProducerTmaWg: return "tmawg";
+        case kProducerCpAsync: return "cpasync";
+    }
+    return "?";
+}
+
 bool tma_ok(const float* p, int ld) {
     return (reinterpret_cast<uintptr_t>(p) & 15u) == 0 && (static_cast<long long>(ld) * 4) % 16 == 0;
 }
@@ -237,6 +270,10 @@ int make_plan(const DeviceState& st, int M, int N, int K, const float* A, int ld
     if (want_prod == SGEMM_PRODUCER_TMA) {
         if (!aligned) return SGEMM_ERR_INVALID_ARG;
         pl.producer = kProducerTma;
+    } else if (want_prod == SGEMM_PRODUCER_TMA_WG) {
+        if (!aligned) return SGEMM_ERR_INVALID_ARG;
+        if (!st.regsplit_ok) return SGEMM_ERR_UNSUPPORTED;
+        pl.producer = kProducerTmaWg;
     } else if (want_prod == SGEMM_PRODUCER_CPASYNC) {
         pl.producer = kProducerCpAsync;
     } else if (want_prod == SGEMM_PRODUCER_AUTO) {
@@ -297,7 +334,7 @@ int make_plan(const DeviceState& st, int M, int N, int K, const float* A, int ld
     // unless forced.
     const int want_mc = opt ? opt->multicast : 0;
     if (want_mc == 2) {
-        if (split > 1 || pl.producer != kProducerTma) return SGEMM_ERR_INVALID_ARG;
+        if (split > 1 || !is_tma(pl.producer)) return SGEMM_ERR_INVALID_ARG;
         if (st.max_clusters_pair < 1) return SGEMM_ERR_UNSUPPORTED;
         pl.mcast = 2;
     } else if (want_mc == 0 || want_mc == 1) {
@@ -372,7 +409,7 @@ int encode_2d(CUtensorMap* map, const float* base, long long inner, long long ou
 
 const char* describe_plan(const Plan& pl) {
     static thread_local char buf[128];
-    int n = std::snprintf(buf, sizeof buf, "%s/%s/mc%d/s%d/st%d", pl.producer == kProducerTma ? "tma" : "cpasync",
+    int n = std::snprintf(buf, sizeof buf, "%s/%s/mc%d/s%d/st%d", producer_name(pl.producer),
                           pl.math == kMathFfma2 ? "ffma2" : "ffma", pl.mcast, pl.launch[0].split, pl.stages);
     if (pl.nlaunch > 1 && n > 0 && n < static_cast<int>(sizeof buf))
         std::snprintf(buf + n, sizeof buf - n, "/tail%d:%d", pl.launch[1].split, pl.launch[1].tiles);
@@ -396,15 +433,14 @@ int run_ffma(int M, int N, int K, const float* A, int lda, const float* B, int l
     rc = make_plan(*st, M, N, K, A, lda, B, ldb, opt, &pl);
     if (rc != SGEMM_OK) return rc;
 
-    const KernelEntry k =
-        pl.producer == kProducerTma ? ffma_kernel_tma(pl.stages, pl.math) : ffma_kernel_cpasync(pl.stages, pl.math);
+    const KernelEntry k = ffma_kernel(pl);
     if (!k.fn) return SGEMM_ERR_INVALID_ARG;
 
     alignas(64) CUtensorMap tmA;
     alignas(64) CUtensorMap tmB;
     std::memset(&tmA, 0, sizeof tmA);
     std::memset(&tmB, 0, sizeof tmB);
-    if (pl.producer == kProducerTma) {
+    if (is_tma(pl.producer)) {
         rc = encode_2d(&tmA, A, K, M, lda, kBK, kBM / pl.mcast, CU_TENSOR_MAP_SWIZZLE_128B);
         if (rc == SGEMM_OK) rc = encode_2d(&tmB, B, N, K, ldb, kBN, kBK, CU_TENSOR_MAP_SWIZZLE_NONE);
         if (rc != SGEMM_OK) return rc;
@@ -532,14 +568,13 @@ int run_ffma_noalloc(int M, int N, int K, const float* A, int lda, const float* 
     const size_t G = pl.sk ? static_cast<size_t>(pl.launch[0].tiles) : 0;
     if (G * kNoAllocTileFloats + G > kNoAllocFloats) return SGEMM_ERR_INVALID_ARG;  // cannot happen with the cap
 
-    const KernelEntry k =
-        pl.producer == kProducerTma ? ffma_kernel_tma(pl.stages, pl.math) : ffma_kernel_cpasync(pl.stages, pl.math);
+    const KernelEntry k = ffma_kernel(pl);
     if (!k.fn) return SGEMM_ERR_INVALID_ARG;
     alignas(64) CUtensorMap tmA;
     alignas(64) CUtensorMap tmB;
     std::memset(&tmA, 0, sizeof tmA);
     std::memset(&tmB, 0, sizeof tmB);
-    if (pl.producer == kProducerTma) {
+    if (is_tma(pl.producer)) {
         rc = encode_2d(&tmA, A, K, M, lda, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B);
         if (rc == SGEMM_OK) rc = encode_2d(&tmB, B, N, K, ldb, kBN, kBK, CU_TENSOR_MAP_SWIZZLE_NONE);
         if (rc != SGEMM_OK) return rc;

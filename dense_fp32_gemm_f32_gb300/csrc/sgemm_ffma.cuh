@@ -55,14 +55,31 @@ constexpr int kBK = 32;
 constexpr int kConsumerWarps = 8;
 constexpr int kConsumerThreads = kConsumerWarps * 32;
 
-enum : int { kProducerTma = 1, kProducerCpAsync = 2 };
+enum : int { kProducerTma = 1, kProducerCpAsync = 2, kProducerTmaWg = 3 };
 
 // Producer warps: one elected lane drives the TMA; the cp.async producer
 // issues every 4-byte copy itself, so it gets a full warpgroup.
+//
+// kProducerTmaWg is the TMA producer in a warpgroup of its own, so that the
+// CTA is three whole warpgroups (384 threads) and the registers can be split
+// between them with setmaxnreg.  At 288 threads (8 consumer warps + 1
+// producer warp) one SM sub-partition holds three warps and the allocation
+// is capped at 168 registers per thread for every warp; the consumer loop
+// wants more (about 230 when unconstrained).  With the split the producer
+// warpgroup drops to kRegsProducer and each consumer warp rises to
+// kRegsConsumer, which together use exactly the 168 x 384 registers the CTA
+// is launched with (setmaxnreg.inc waits until the registers are free, so a
+// split that asked for more would never finish: the host launches this
+// variant only when the kernel was built with exactly kRegsLaunch).
 template <int PRODUCER>
 __host__ __device__ constexpr int ffma_producer_warps() {
-    return PRODUCER == kProducerCpAsync ? 4 : 1;
+    return PRODUCER == kProducerTma ? 1 : 4;
 }
+constexpr int kRegsLaunch = 168;
+constexpr int kRegsProducer = 40;
+constexpr int kRegsConsumer = 232;
+static_assert(4 * 32 * kRegsProducer + kConsumerWarps * 32 * kRegsConsumer == (kConsumerWarps + 4) * 32 * kRegsLaunch,
+              "the register split must use exactly the registers the CTA is launched with");
 template <int PRODUCER>
 __host__ __device__ constexpr int ffma_threads() {
     return kConsumerThreads + 32 * ffma_producer_warps<PRODUCER>();
@@ -134,6 +151,7 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), 1)
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
 
+    constexpr bool kTma = PRODUCER != kProducerCpAsync;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     constexpr int PW = ffma_producer_warps<PRODUCER>();
@@ -188,7 +206,7 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), 1)
                      u_begin, NK > 0 ? u_end : u_begin};
 
     if (threadIdx.x == 0) {
-        const uint32_t full_count = (PRODUCER == kProducerTma) ? 1u : 32u * PW;
+        const uint32_t full_count = kTma ? 1u : 32u * PW;
         const uint32_t empty_count = static_cast<uint32_t>(kConsumerWarps * mcast);
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full_bar(s), full_count);
@@ -196,7 +214,7 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), 1)
         }
         fence_mbarrier_init();
     }
-    if (PRODUCER == kProducerTma && is_producer && lane == 0) {
+    if (kTma && is_producer && pw == 0 && lane == 0) {
         prefetch_tensormap(&tmA);
         prefetch_tensormap(&tmB);
     }
@@ -211,8 +229,14 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), 1)
     const bool skip_here = p.skip_stage > 0 && blockIdx.x == 0 && blockIdx.z == 0;
 
     // ------------------------------------------------------------ producer
+    // The producer and consumer paths never merge again (each ends in its own
+    // share of the split-K / multicast barriers), so that code after a
+    // register-limit change is only reachable through it.
     if (is_producer) {
-        const bool issuer = PRODUCER == kProducerCpAsync || lane == 0;
+        // Warpgroup-uniform (warps 8-11).  The producer releases registers
+        // first; the consumers' requests are served from what it released.
+        if constexpr (PRODUCER == kProducerTmaWg) setmaxnreg_dec<kRegsProducer>();
+        const bool issuer = !kTma || (pw == 0 && lane == 0);
         int issued_round[STAGES];
 #pragma unroll
         for (int s = 0; s < STAGES; ++s) issued_round[s] = -1;
@@ -225,16 +249,15 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), 1)
             for (int kt = kb; kt < ke; ++kt, ++it) {
                 const int s = it % STAGES;
                 const int round = it / STAGES;
-                const bool ok = PRODUCER == kProducerTma
-                                    ? (round == 0 || mbar_wait_bounded(empty_bar(s), (round - 1) & 1, tmo))
-                                    : (round == 0 || mbar_wait_bounded_warp(empty_bar(s), (round - 1) & 1, tmo));
+                const bool ok = kTma ? (round == 0 || mbar_wait_bounded(empty_bar(s), (round - 1) & 1, tmo))
+                                     : (round == 0 || mbar_wait_bounded_warp(empty_bar(s), (round - 1) & 1, tmo));
                 if (!ok) {
                     timed_out = true;
                     break;
                 }
                 if (skip_here && it == p.skip_stage - 1) continue;
                 const int k0 = kt * kBK;
-                if (PRODUCER == kProducerTma) {
+                if (kTma) {
                     mbar_arrive_expect_tx(full_bar(s), kStageBytes);
                     if (mcast > 1) {
                         // This CTA fetches rows [crank*64, crank*64+64) of the A
@@ -282,8 +305,8 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), 1)
             }
         }
         // Drain: every copy this producer issued has landed before it leaves.
-        if (PRODUCER == kProducerTma) {
-            if (lane == 0) {
+        if (kTma) {
+            if (issuer) {
 #pragma unroll
                 for (int s = 0; s < STAGES; ++s)
                     if (issued_round[s] >= 0 && !mbar_wait_bounded(full_bar(s), issued_round[s] & 1, tmo))
@@ -293,9 +316,19 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), 1)
             cp_async_wait_all();
         }
         if (timed_out) atomicOr(p.status, kStatusTimeout);
+        // This CTA's share of the barriers at the end of the consumer path.
+        if (split > 1) {
+            __syncthreads();
+            cluster_sync_all();
+            cluster_sync_all();
+        } else if (mcast > 1) {
+            cluster_sync_all();
+        }
+        return;
     }
 
     // ------------------------------------------------------------ consumers
+    if constexpr (PRODUCER == kProducerTmaWg) setmaxnreg_inc<kRegsConsumer>();
     // Warp layout: 4 (M) x 2 (N) warps of 32 x 64; each lane owns a 4 x 8
     // grid position (tm, tn).  Thread rows: wm*32 + tm + 4*i (i = 0..7);
     // thread columns: wn*64 + tn*4 + {0..3} and wn*64 + 32 + tn*4 + {0..3}.
@@ -354,7 +387,7 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), 1)
     };
     auto consumer_sync = [] { asm volatile("bar.sync 1, %0;" ::"n"(kConsumerThreads) : "memory"); };
 
-    if (!is_producer) {
+    {
         // Byte offsets inside a stage.  A row r = wm*32 + tm + 4i has r mod 8 =
         // tm + 4*(i & 1), so even i share one swizzle key and odd i the other.
         const uint32_t a_row0 = static_cast<uint32_t>((wm * 32 + tm) * 128);
@@ -488,7 +521,7 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), 1)
         // All consumer reads of the ring are finished once every thread of the
         // CTA passes this barrier; the ring is then reused for the partial tile.
         __syncthreads();
-        if (!is_producer && crank != 0) {
+        if (crank != 0) {
 #pragma unroll
             for (int i = 0; i < 8; ++i)
 #pragma unroll
@@ -497,7 +530,7 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), 1)
                            make_float4(acc[i][2 * h].x, acc[i][2 * h].y, acc[i][2 * h + 1].x, acc[i][2 * h + 1].y));
         }
         cluster_sync_all();
-        if (!is_producer && crank == 0) {
+        if (crank == 0) {
             for (int r = 1; r < split; ++r) {  // fixed order: deterministic sums
 #pragma unroll
                 for (int i = 0; i < 8; ++i)
@@ -521,7 +554,7 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), 1)
         cluster_sync_all();
     }
 
-    if (is_producer || p.sk) return;  // (stream-K CTAs stored their tiles above)
+    if (p.sk) return;  // (stream-K CTAs stored their tiles above)
 
     // ------------------------------------------------------------ epilogue
     store_c(p.tile_base + static_cast<int>(blockIdx.x));

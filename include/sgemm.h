@@ -150,7 +150,11 @@ int sgemm_3xtf32(int M, int N, int K,
 enum {
     SGEMM_PRODUCER_AUTO = 0,
     SGEMM_PRODUCER_TMA = 1,      /* tensor-map bulk copies (needs 16-byte alignment) */
-    SGEMM_PRODUCER_CPASYNC = 2   /* 4-byte cp.async with zero fill (any alignment) */
+    SGEMM_PRODUCER_CPASYNC = 2,  /* 4-byte cp.async with zero fill (any alignment) */
+    SGEMM_PRODUCER_TMA_WG = 3    /* tensor-map bulk copies from a producer warpgroup of its own,
+                                    registers split between the warpgroups (producer 40,
+                                    consumers 232 per thread); SGEMM_ERR_UNSUPPORTED if the
+                                    library's build of that kernel does not allow the split */
 };
 
 /*

@@ -93,6 +93,11 @@ VARIANTS = (
     + [dict(producer=2, math=m, stages=s, split_k=1) for m in (1, 2) for s in (2, 4)]
     + [dict(producer=pr, math=m, stream_k=2) for pr in (1, 2) for m in (1, 2)]
     + [dict(stream_k=2, stages=s) for s in (2, 6)]
+    # producer warpgroup with the setmaxnreg register split
+    + [dict(producer=3, math=m, stages=s, split_k=1, multicast=1) for m in (1, 2) for s in (1, 4, 6)]
+    + [dict(producer=3, math=2, multicast=2, split_k=1)]
+    + [dict(producer=3, math=2, split_k=s, multicast=1) for s in (2, 4)]
+    + [dict(producer=3, math=m, stream_k=2) for m in (1, 2)]
 )
 
 
