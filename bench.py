@@ -404,6 +404,10 @@ SWEEP_OPTIONS = [
     {"producer": 2},
     {"producer": 3},
     {"producer": 3, "split_k": 1},
+    {"tile_n": 256},
+    {"tile_n": 256, "stages": 2},
+    {"tile_n": 256, "stages": 3},
+    {"tile_n": 256, "split_k": 1},
     {"split_k": 1},
     {"split_k": 2},
     {"split_k": 4},
@@ -421,6 +425,7 @@ def run_sweep(args):
     import dense_fp32_gemm_f32_gb300 as g
 
     torch.cuda.set_device(0)
+    torch.backends.cuda.matmul.allow_tf32 = False  # the library comparison runs in full FP32
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
     names = args.sweep_workloads or [n for n in PROBLEMS if not n.endswith("_int")]
     for name in names:
@@ -432,6 +437,9 @@ def run_sweep(args):
                 for opt in SWEEP_OPTIONS]
         runs += [({"entry": "sgemm_3xtf32", "variant": v}, lambda v=v: g.sgemm_3xtf32_ex(A, B, C, variant=v))
                  for v in SWEEP_TF32X3_VARIANTS]
+        # Context only (a library GEMM, on no path of this project): the
+        # FP32 GEMM torch runs with TF32 disabled, timed the same way.
+        runs += [({"entry": "torch.mm", "tf32": False}, lambda: torch.mm(A, B, out=C))]
         for opt, run in runs:
             try:
                 for _ in range(3):

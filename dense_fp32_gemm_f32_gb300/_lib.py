@@ -41,6 +41,7 @@ class Options(ctypes.Structure):
         ("timeout_ns", _u64),
         ("tail_split", _i),
         ("stream_k", _i),
+        ("tile_n", _i),
     ]
 
 

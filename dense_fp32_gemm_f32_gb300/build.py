@@ -17,11 +17,11 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB_NAME = "libgb300_sgemm.so"
-SOURCES = ["sgemm_api.cu", "sgemm_ffma_tma.cu", "sgemm_ffma_tma_wg.cu", "sgemm_ffma_cpasync.cu", "sgemm_3xtf32.cu",
-           "sgemm_3xtf32_direct.cu", "peak.cu"]
+SOURCES = ["sgemm_api.cu", "sgemm_ffma_tma.cu", "sgemm_ffma_tma_wg.cu", "sgemm_ffma_tma_wide.cu",
+           "sgemm_ffma_cpasync.cu", "sgemm_3xtf32.cu", "sgemm_3xtf32_direct.cu", "peak.cu"]
 # Kernels that split registers between warpgroups with setmaxnreg must be
 # built with exactly this many registers per thread (the split's total).
-REGSPLIT_SOURCE = "sgemm_ffma_tma_wg.cu"
+REGSPLIT_SOURCES = ("sgemm_ffma_tma_wg.cu", "sgemm_ffma_tma_wide.cu")
 REGSPLIT_LAUNCH_REGS = 168
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas", "-v"]
@@ -62,18 +62,18 @@ def _compile(src: str) -> tuple[str, str]:
     return obj, r.stdout + r.stderr
 
 
-def check_regsplit(log: str) -> None:
+def check_regsplit(src: str, log: str) -> None:
     """The register-split kernels' ptxas report: every entry uses exactly
     REGSPLIT_LAUNCH_REGS registers, and ptxas kept the setmaxnreg instructions
     (it says so when it drops them)."""
     used = re.findall(r"Compiling entry function '([^']+)'.*?Used (\d+) registers", log, re.S)
     if not used:
-        raise RuntimeError(f"{REGSPLIT_SOURCE}: no kernel entries in the ptxas report")
+        raise RuntimeError(f"{src}: no kernel entries in the ptxas report")
     bad = [(name, n) for name, n in used if int(n) != REGSPLIT_LAUNCH_REGS]
     if bad:
-        raise RuntimeError(f"{REGSPLIT_SOURCE}: kernels not at {REGSPLIT_LAUNCH_REGS} registers: {bad}")
+        raise RuntimeError(f"{src}: kernels not at {REGSPLIT_LAUNCH_REGS} registers: {bad}")
     if "setmaxnreg" in log:
-        raise RuntimeError(f"{REGSPLIT_SOURCE}: ptxas reported on setmaxnreg:\n{log}")
+        raise RuntimeError(f"{src}: ptxas reported on setmaxnreg:\n{log}")
 
 
 def build(force: bool = False, verbose: bool = False) -> str:
@@ -87,7 +87,9 @@ def build(force: bool = False, verbose: bool = False) -> str:
     with open(os.path.join(OUT_DIR, "ptxas.log"), "w") as f:
         for (o, log), src in zip(results, SOURCES):
             f.write(f"==== {src}\n{log}\n")
-    check_regsplit(dict(zip(SOURCES, (log for _, log in results)))[REGSPLIT_SOURCE])
+    logs = dict(zip(SOURCES, (log for _, log in results)))
+    for src in REGSPLIT_SOURCES:
+        check_regsplit(src, logs[src])
     tmp = lib_path() + f".tmp{os.getpid()}"
     cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *objs, "-cudart", "static"]
     r = subprocess.run(cmd, capture_output=True, text=True)

@@ -15,6 +15,9 @@ KernelEntry ffma_kernel_tma(int stages, int math);
 // (producer 40, consumers 232 registers per thread); launched only when the
 // kernel was built with exactly 168 registers per thread.
 KernelEntry ffma_kernel_tma_wg(int stages, int math);
+// 128 x 256 tiles (8 x 16 accumulators per thread) with the producer
+// warpgroup and the register split; stages in {2,3,4}.
+KernelEntry ffma_kernel_tma_wide(int stages, int math);
 // FFMA kernels fed by 4-byte cp.async (any alignment); stages in {2,4}.
 KernelEntry ffma_kernel_cpasync(int stages, int math);
 // Three-product TF32 kernel on the tensor cores (TMA-fed, 128 x 128 tiles,

@@ -27,7 +27,7 @@ __device__ unsigned int g_sgemm_status = 0;
 // GPU that loads the library holds it until the process exits; all calls on a
 // device share it.
 constexpr int kNoAllocMaxCtas = 160;
-constexpr size_t kNoAllocTileFloats = static_cast<size_t>(kBM) * kBN;
+constexpr size_t kNoAllocTileFloats = static_cast<size_t>(kBM) * kBN;  // 128 x 128 tiles only
 constexpr size_t kNoAllocFloats = kNoAllocMaxCtas * kNoAllocTileFloats + kNoAllocMaxCtas;
 static __device__ __align__(256) float g_noalloc_scratch[kNoAllocFloats];
 
@@ -125,12 +125,18 @@ int init_device(int dev, DeviceState& st) {
             // setmaxnreg.inc waits until the registers it asks for are free;
             // the split adds up to kRegsLaunch per thread of the CTA, so a
             // kernel built with any other count must never be launched.
-            const KernelEntry wg = ffma_kernel_tma_wg(s, math);
-            if (set_smem_attr(wg) != SGEMM_OK) return SGEMM_ERR_CUDA;
-            cudaFuncAttributes fa;
-            if (!wg.fn || cudaFuncGetAttributes(&fa, wg.fn) != cudaSuccess || fa.numRegs != kRegsLaunch) {
-                (void)cudaGetLastError();
-                st.regsplit_ok = false;
+            const KernelEntry split_kernels[2] = {ffma_kernel_tma_wg(s, math), ffma_kernel_tma_wide(s, math)};
+            for (const KernelEntry& wg : split_kernels) {
+                if (!wg.fn) {
+                    if (&wg == &split_kernels[0]) st.regsplit_ok = false;
+                    continue;  // (the wide tile is built for 2..4 stages only)
+                }
+                if (set_smem_attr(wg) != SGEMM_OK) return SGEMM_ERR_CUDA;
+                cudaFuncAttributes fa;
+                if (cudaFuncGetAttributes(&fa, wg.fn) != cudaSuccess || fa.numRegs != kRegsLaunch) {
+                    (void)cudaGetLastError();
+                    st.regsplit_ok = false;
+                }
             }
         }
         for (int s = 1; s <= 6; ++s)
@@ -222,6 +228,7 @@ struct Plan {
     int math = kMathFfma2;
     int stages = 4;
     int mcast = 1;
+    int bn = kBN;     // output tile width (kBN or kBNWide)
     int tiles_n = 0;  // tiles per row of tiles (padded to even for multicast pairs)
     int num_k_tiles = 0;
     int nlaunch = 1;
@@ -235,6 +242,8 @@ long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
 bool is_tma(int producer) { return producer == kProducerTma || producer == kProducerTmaWg; }
 
 KernelEntry ffma_kernel(const Plan& pl) {
+    if (pl.bn == kBNWide) return pl.producer == kProducerTmaWg ? ffma_kernel_tma_wide(pl.stages, pl.math)
+                                                                : KernelEntry{nullptr, 0, 0};
     switch (pl.producer) {
         case kProducerTma: return ffma_kernel_tma(pl.stages, pl.math);
         case kProducerTmaWg: return ffma_kernel_tma_wg(pl.stages, pl.math);
@@ -261,8 +270,8 @@ int make_plan(const DeviceState& st, int M, int N, int K, const float* A, int ld
               const sgemm_options* opt, Plan* out) {
     Plan pl;
     pl.num_k_tiles = static_cast<int>(ceil_div(K, kBK));
-    const long long tiles_n = ceil_div(N, kBN), tiles_m = ceil_div(M, kBM);
-    const long long tiles = tiles_n * tiles_m;
+    long long tiles_n = ceil_div(N, kBN);
+    const long long tiles_m = ceil_div(M, kBM);
 
     // Producer: tensor maps need 16-byte aligned bases and row strides, and K > 0.
     const bool aligned = K > 0 && tma_ok(A, lda) && tma_ok(B, ldb);
@@ -282,10 +291,30 @@ int make_plan(const DeviceState& st, int M, int N, int K, const float* A, int ld
         return SGEMM_ERR_INVALID_ARG;
     }
 
+    // Tile width: 128 x 256 tiles need the producer warpgroup (register
+    // split) and so tensor maps.
+    const int want_bn = opt ? opt->tile_n : 0;
+    if (want_bn == kBNWide) {
+        if (want_prod == SGEMM_PRODUCER_AUTO) {
+            if (!aligned) return SGEMM_ERR_INVALID_ARG;
+            if (!st.regsplit_ok) return SGEMM_ERR_UNSUPPORTED;
+            pl.producer = kProducerTmaWg;
+        }
+        if (pl.producer != kProducerTmaWg) return SGEMM_ERR_INVALID_ARG;
+        pl.bn = kBNWide;
+    } else if (want_bn != 0 && want_bn != kBN) {
+        return SGEMM_ERR_INVALID_ARG;
+    }
+
     if (opt && opt->math) {
         if (opt->math != kMathFfma && opt->math != kMathFfma2) return SGEMM_ERR_INVALID_ARG;
         pl.math = opt->math;
     }
+    // Stages: two for the tensor-map producers (measured on GB300 with the
+    // paired-FMA consumers: 0.3-2 % faster than 3-6 at every named problem,
+    // 20-25 % faster than one), four for cp.async, whose 4-byte copies have
+    // more latency to hide.
+    pl.stages = pl.producer == kProducerCpAsync ? 4 : 2;
     if (opt && opt->stages) {
         if (opt->stages < 1 || opt->stages > 6) return SGEMM_ERR_INVALID_ARG;
         pl.stages = opt->stages;
@@ -294,6 +323,10 @@ int make_plan(const DeviceState& st, int M, int N, int K, const float* A, int ld
         if (opt && opt->stages) return SGEMM_ERR_INVALID_ARG;
         pl.stages = 4;
     }
+    if (pl.bn == kBNWide && (pl.stages < 2 || pl.stages > 4)) return SGEMM_ERR_INVALID_ARG;
+
+    tiles_n = ceil_div(N, pl.bn);
+    const long long tiles = tiles_n * tiles_m;
 
     // Stream-K (decided first; see below for the schedule).  Automatic
     // whenever nothing else is forced and there are at least two (tile, K
@@ -412,9 +445,11 @@ const char* describe_plan(const Plan& pl) {
     int n = std::snprintf(buf, sizeof buf, "%s/%s/mc%d/s%d/st%d", producer_name(pl.producer),
                           pl.math == kMathFfma2 ? "ffma2" : "ffma", pl.mcast, pl.launch[0].split, pl.stages);
     if (pl.nlaunch > 1 && n > 0 && n < static_cast<int>(sizeof buf))
-        std::snprintf(buf + n, sizeof buf - n, "/tail%d:%d", pl.launch[1].split, pl.launch[1].tiles);
+        n += std::snprintf(buf + n, sizeof buf - n, "/tail%d:%d", pl.launch[1].split, pl.launch[1].tiles);
     if (pl.sk && n > 0 && n < static_cast<int>(sizeof buf))
-        std::snprintf(buf + n, sizeof buf - n, "/sk%d", pl.launch[0].tiles);
+        n += std::snprintf(buf + n, sizeof buf - n, "/sk%d", pl.launch[0].tiles);
+    if (pl.bn != kBN && n > 0 && n < static_cast<int>(sizeof buf))
+        std::snprintf(buf + n, sizeof buf - n, "/n%d", pl.bn);
     return buf;
 }
 
@@ -442,7 +477,7 @@ int run_ffma(int M, int N, int K, const float* A, int lda, const float* B, int l
     std::memset(&tmB, 0, sizeof tmB);
     if (is_tma(pl.producer)) {
         rc = encode_2d(&tmA, A, K, M, lda, kBK, kBM / pl.mcast, CU_TENSOR_MAP_SWIZZLE_128B);
-        if (rc == SGEMM_OK) rc = encode_2d(&tmB, B, N, K, ldb, kBN, kBK, CU_TENSOR_MAP_SWIZZLE_NONE);
+        if (rc == SGEMM_OK) rc = encode_2d(&tmB, B, N, K, ldb, pl.bn, kBK, CU_TENSOR_MAP_SWIZZLE_NONE);
         if (rc != SGEMM_OK) return rc;
     }
 
@@ -477,7 +512,7 @@ int run_ffma(int M, int N, int K, const float* A, int lda, const float* B, int l
     const cudaStream_t cs = static_cast<cudaStream_t>(stream);
     if (pl.sk) {
         const size_t G = static_cast<size_t>(pl.launch[0].tiles);
-        const size_t tile_bytes = static_cast<size_t>(kBM) * kBN * sizeof(float);
+        const size_t tile_bytes = static_cast<size_t>(kBM) * pl.bn * sizeof(float);
         cudaMemPool_t pool = workspace_pool(dev, *st);
         if (!pool || cudaMallocFromPoolAsync(&ws, G * tile_bytes + G * sizeof(unsigned int), pool, cs) != cudaSuccess) {
             (void)cudaGetLastError();
@@ -561,12 +596,13 @@ int run_ffma_noalloc(int M, int N, int K, const float* A, int lda, const float* 
     sgemm_options o = {};
     o.stream_k = K > 0 ? 2 : 1;
     o.split_k = K > 0 ? 0 : 1;
+    o.tile_n = kBN;
     Plan pl;
     rc = make_plan(*st, M, N, K, A, lda, B, ldb, &o, &pl);
     if (rc != SGEMM_OK) return rc;
     if (pl.sk && pl.launch[0].tiles > kNoAllocMaxCtas) pl.launch[0].tiles = kNoAllocMaxCtas;
     const size_t G = pl.sk ? static_cast<size_t>(pl.launch[0].tiles) : 0;
-    if (G * kNoAllocTileFloats + G > kNoAllocFloats) return SGEMM_ERR_INVALID_ARG;  // cannot happen with the cap
+    if (G * kBM * pl.bn + G > kNoAllocFloats) return SGEMM_ERR_INVALID_ARG;  // cannot happen with the cap
 
     const KernelEntry k = ffma_kernel(pl);
     if (!k.fn) return SGEMM_ERR_INVALID_ARG;
@@ -576,7 +612,7 @@ int run_ffma_noalloc(int M, int N, int K, const float* A, int lda, const float* 
     std::memset(&tmB, 0, sizeof tmB);
     if (is_tma(pl.producer)) {
         rc = encode_2d(&tmA, A, K, M, lda, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B);
-        if (rc == SGEMM_OK) rc = encode_2d(&tmB, B, N, K, ldb, kBN, kBK, CU_TENSOR_MAP_SWIZZLE_NONE);
+        if (rc == SGEMM_OK) rc = encode_2d(&tmB, B, N, K, ldb, pl.bn, kBK, CU_TENSOR_MAP_SWIZZLE_NONE);
         if (rc != SGEMM_OK) return rc;
     }
 

@@ -84,10 +84,20 @@ template <int PRODUCER>
 __host__ __device__ constexpr int ffma_threads() {
     return kConsumerThreads + 32 * ffma_producer_warps<PRODUCER>();
 }
+constexpr int kBNWide = 256;  // wide tile: 128 x 256, 8 x 16 per thread (producer warpgroup only)
 constexpr int kStageABytes = kBM * kBK * 4;      // 16 KiB, 128-byte swizzled rows of 32 floats
-constexpr int kStageBBytes = kBK * kBN * 4;      // 16 KiB, plain rows of 128 floats
-constexpr int kStageBytes = kStageABytes + kStageBBytes;
-constexpr int kPartialBytes = kBM * kBN * 4;     // split-K partial tile
+template <int BN>
+__host__ __device__ constexpr int ffma_stage_b_bytes() {
+    return kBK * BN * 4;  // plain rows of BN floats
+}
+template <int BN>
+__host__ __device__ constexpr int ffma_stage_bytes() {
+    return kStageABytes + ffma_stage_b_bytes<BN>();
+}
+template <int BN>
+__host__ __device__ constexpr int ffma_partial_bytes() {
+    return kBM * BN * 4;  // one partial tile (split-K, stream-K)
+}
 
 enum : int { kMathFfma = 1, kMathFfma2 = 2 };
 enum : unsigned { kStatusTimeout = 4u };
@@ -115,17 +125,18 @@ struct FfmaParams {
     int sk;
     int sk_dp_tiles;       // tiles handled whole before the stream-K region
     long long sk_units;    // (tiles - sk_dp_tiles) * num_k_tiles
-    float* ws;             // gridDim.x partial tiles of kBM x kBN floats
+    float* ws;             // gridDim.x partial tiles of kBM x BN floats
     unsigned int* flags;   // gridDim.x words, zero at launch; 1 = partial ready
     int skip_stage;        // debug: CTA (0,0,0)'s producer never issues K-slice skip_stage-1
     unsigned long long timeout_ns;
     unsigned int* status;  // per-device sticky status word (error bits)
 };
 
-template <int STAGES>
+template <int STAGES, int BN = kBN>
 constexpr int ffma_smem_bytes() {
-    return (STAGES * kStageBytes > kPartialBytes ? STAGES * kStageBytes : kPartialBytes) + 1024 /*align*/ +
-           256 /*barriers*/;
+    return (STAGES * ffma_stage_bytes<BN>() > ffma_partial_bytes<BN>() ? STAGES * ffma_stage_bytes<BN>()
+                                                                      : ffma_partial_bytes<BN>()) +
+           1024 /*align*/ + 256 /*barriers*/;
 }
 
 // Physical byte offset of float (row r, column c) inside a 128-byte-swizzled
@@ -134,10 +145,18 @@ __device__ __forceinline__ uint32_t swz128(int r, int c) {
     return static_cast<uint32_t>(r * 128 + ((((c >> 2) ^ r) & 7) << 4) + (c & 3) * 4);
 }
 
-template <int STAGES, int PRODUCER, int MATH>
+template <int STAGES, int PRODUCER, int MATH, int BN = kBN>
 __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), 1)
     sgemm_ffma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                       const FfmaParams p) {
+    // 128 accumulators per thread need the consumer register budget of the
+    // register split.
+    static_assert(BN == kBN || (BN == kBNWide && PRODUCER == kProducerTmaWg), "tile width");
+    constexpr int kStageBBytes = ffma_stage_b_bytes<BN>();
+    constexpr int kStageBytes = ffma_stage_bytes<BN>();
+    constexpr int kPartialBytes = ffma_partial_bytes<BN>();
+    constexpr int H = BN / 64;  // 4-column groups per thread row (2 or 4)
+    constexpr int TQ = 2 * H;   // column pairs per thread row
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte alignment for the 128-byte swizzle pattern; identical offset in
     // every CTA, which multicast relies on.
@@ -244,7 +263,7 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), 1)
         Work work = work0;
         int tile, kb, ke;
         while (issuer && !timed_out && work.next(tile, kb, ke)) {
-            const int n0 = (tile % p.tiles_n) * kBN;
+            const int n0 = (tile % p.tiles_n) * BN;
             const int m0 = (tile / p.tiles_n) * kBM;
             for (int kt = kb; kt < ke; ++kt, ++it) {
                 const int s = it % STAGES;
@@ -291,11 +310,11 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), 1)
                         const int k = k0 + r;
                         const bool kin = k < p.K;
 #pragma unroll
-                        for (int q = 0; q < kBN / 32; ++q) {
+                        for (int q = 0; q < BN / 32; ++q) {
                             const int n = n0 + q * 32 + lane;
                             const bool in = kin && n < p.N;
                             const float* src = in ? p.B + static_cast<long long>(k) * p.ldb + n : p.B;
-                            cp_async_4(sb + static_cast<uint32_t>(r * (kBN * 4) + (q * 32 + lane) * 4), src,
+                            cp_async_4(sb + static_cast<uint32_t>(r * (BN * 4) + (q * 32 + lane) * 4), src,
                                        in ? 4u : 0u);
                         }
                     }
@@ -329,16 +348,16 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), 1)
 
     // ------------------------------------------------------------ consumers
     if constexpr (PRODUCER == kProducerTmaWg) setmaxnreg_inc<kRegsConsumer>();
-    // Warp layout: 4 (M) x 2 (N) warps of 32 x 64; each lane owns a 4 x 8
+    // Warp layout: 4 (M) x 2 (N) warps of 32 x BN/2; each lane owns a 4 x 8
     // grid position (tm, tn).  Thread rows: wm*32 + tm + 4*i (i = 0..7);
-    // thread columns: wn*64 + tn*4 + {0..3} and wn*64 + 32 + tn*4 + {0..3}.
-    // acc[i][q] holds columns (2q, 2q+1) of thread row i: q = 0,1 cover
-    // tn*4 + 0..3, q = 2,3 cover 32 + tn*4 + 0..3.
+    // thread columns: wn*BN/2 + 32*h + tn*4 + {0..3} for h = 0..H-1 (H = 2
+    // for the 128-wide tile, 4 for the 256-wide one).  acc[i][q] holds
+    // columns (2q, 2q+1) of thread row i, counted over those 4H columns.
     //
     // Per k-group (4 consecutive k) a thread reads 8 A vectors (one per row,
-    // 4 k values each: the TMA lands A with k innermost) and, per k, 2 B
-    // vectors, and issues 128 paired multiply-adds (8 rows x 4 column pairs x
-    // 4 k).
+    // 4 k values each: the TMA lands A with k innermost) and, per k, H B
+    // vectors, and issues 64 H paired multiply-adds (8 rows x 2H column pairs
+    // x 4 k).
     //
     // Lane order.  tm takes lane bits 0 and 2, tn lane bits 1, 3 and 4.
     // Measured on GB300 (shared-memory wavefronts per 16-byte load, ncu): a
@@ -347,30 +366,30 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), 1)
     // order neither the A loads (address set by tm) nor the B loads (set by
     // tn) vary with both bits, so every fragment load costs 2 wavefronts
     // instead of 2 (A) and 4 (B) with tn = lane & 7.
-    float2 acc[8][4];
+    float2 acc[8][TQ];
 #pragma unroll
     for (int i = 0; i < 8; ++i)
 #pragma unroll
-        for (int q = 0; q < 4; ++q) acc[i][q] = make_float2(0.f, 0.f);  // (K == 0: the empty sum)
+        for (int q = 0; q < TQ; ++q) acc[i][q] = make_float2(0.f, 0.f);  // (K == 0: the empty sum)
     const int wm = warp >> 1, wn = warp & 1;
     const int tm = (lane & 1) | (((lane >> 2) & 1) << 1);
     const int tn = ((lane >> 1) & 1) | (((lane >> 3) & 1) << 1) | (((lane >> 4) & 1) << 2);
 
     // Partial tiles (split-K through distributed shared memory, stream-K
-    // through global memory) use the layout [e4 = 0..15][thread = 0..255][4
-    // floats]; element group e4 = i*2 + h holds acc[i][2h] and acc[i][2h+1]
-    // (four columns).  Consecutive threads touch consecutive 16-byte words, so
+    // through global memory) use the layout [e4 = 0..8H-1][thread = 0..255]
+    // [4 floats]; element group e4 = i*H + h holds acc[i][2h] and
+    // acc[i][2h+1] (four columns).  Consecutive threads touch consecutive 16-byte words, so
     // every partial store and load is conflict-free and coalesced.
     auto store_c = [&](int tile) {
         const int row0 = (tile / p.tiles_n) * kBM + wm * 32 + tm;
-        const int col0 = (tile % p.tiles_n) * kBN + wn * 64 + tn * 4;
+        const int col0 = (tile % p.tiles_n) * BN + wn * (BN / 2) + tn * 4;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const int r = row0 + 4 * i;
             if (r >= p.M) continue;
             float* crow = p.C + static_cast<long long>(r) * p.ldc;
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
+            for (int h = 0; h < H; ++h) {
                 const int c = col0 + 32 * h;
                 const float4 v =
                     make_float4(acc[i][2 * h].x, acc[i][2 * h].y, acc[i][2 * h + 1].x, acc[i][2 * h + 1].y);
@@ -391,7 +410,7 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), 1)
         // Byte offsets inside a stage.  A row r = wm*32 + tm + 4i has r mod 8 =
         // tm + 4*(i & 1), so even i share one swizzle key and odd i the other.
         const uint32_t a_row0 = static_cast<uint32_t>((wm * 32 + tm) * 128);
-        const uint32_t b_col0 = static_cast<uint32_t>((wn * 64 + tn * 4) * 4);
+        const uint32_t b_col0 = static_cast<uint32_t>((wn * (BN / 2) + tn * 4) * 4);
         const uint8_t* const smem_a = smem + a_row0;                          // generic pointers
         const uint8_t* const smem_b = smem + STAGES * kStageABytes + b_col0;  // for the vector loads
 
@@ -402,7 +421,7 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), 1)
 #pragma unroll
             for (int i = 0; i < 8; ++i)
 #pragma unroll
-                for (int q = 0; q < 4; ++q) acc[i][q] = make_float2(0.f, 0.f);
+                for (int q = 0; q < TQ; ++q) acc[i][q] = make_float2(0.f, 0.f);
 
             for (int kt = kb; kt < ke; ++kt, ++it) {
                 const int s = it % STAGES;
@@ -424,16 +443,20 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), 1)
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
                         const int k = kg * 4 + kk;
-                        const float4 b0 = *reinterpret_cast<const float4*>(sb + k * (kBN * 4));
-                        const float4 b1 = *reinterpret_cast<const float4*>(sb + k * (kBN * 4) + 128);
-                        const float2 bp[4] = {make_float2(b0.x, b0.y), make_float2(b0.z, b0.w),
-                                              make_float2(b1.x, b1.y), make_float2(b1.z, b1.w)};
+                        float2 bp[TQ];
+#pragma unroll
+                        for (int h = 0; h < H; ++h) {
+                            const float4 bv = *reinterpret_cast<const float4*>(sb + k * (BN * 4) + h * 128);
+                            bp[2 * h] = make_float2(bv.x, bv.y);
+                            bp[2 * h + 1] = make_float2(bv.z, bv.w);
+                        }
                         // Column pair outermost: each B pair feeds 8 consecutive
                         // multiply-adds (measured faster than row-outermost order).
 #pragma unroll
-                        for (int q = 0; q < 4; ++q)
+                        for (int q = 0; q < TQ; ++q)
 #pragma unroll
-                            for (int i = 0; i < 8; ++i) {
+                            for (int i0 = 0; i0 < 8; ++i0) {
+                                const int i = (q & 1) ? 7 - i0 : i0;  // serpentine: A value reused across q
                                 const float av = kk == 0 ? a[i].x : kk == 1 ? a[i].y : kk == 2 ? a[i].z : a[i].w;
                                 if (MATH == kMathFfma2) {
                                     acc[i][q] = __ffma2_rn(make_float2(av, av), bp[q], acc[i][q]);
@@ -455,15 +478,15 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), 1)
             if (!p.sk || timed_out) break;  // one tile per CTA; its epilogue follows below
 
             // ---------------------------------------------------- stream-K epilogue
-            float* const ws_mine = p.ws + static_cast<size_t>(blockIdx.x) * (kBM * kBN);
+            float* const ws_mine = p.ws + static_cast<size_t>(blockIdx.x) * (kBM * BN);
             if (kb > 0) {
                 // Not the first K slice of the tile: leave the partial tile for
                 // the CTA that holds the first slice.
 #pragma unroll
                 for (int i = 0; i < 8; ++i)
 #pragma unroll
-                    for (int h = 0; h < 2; ++h)
-                        __stcg(reinterpret_cast<float4*>(ws_mine) + (i * 2 + h) * kConsumerThreads + threadIdx.x,
+                    for (int h = 0; h < H; ++h)
+                        __stcg(reinterpret_cast<float4*>(ws_mine) + (i * H + h) * kConsumerThreads + threadIdx.x,
                                make_float4(acc[i][2 * h].x, acc[i][2 * h].y, acc[i][2 * h + 1].x,
                                            acc[i][2 * h + 1].y));
                 consumer_sync();
@@ -497,12 +520,12 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), 1)
                             if (!ok) atomicOr(p.status, kStatusTimeout);
                         }
                         consumer_sync();  // thread 0 saw the flag: the partial is complete
-                        const float4* src = reinterpret_cast<const float4*>(p.ws + g2 * (kBM * kBN));
+                        const float4* src = reinterpret_cast<const float4*>(p.ws + g2 * (kBM * BN));
 #pragma unroll
                         for (int i = 0; i < 8; ++i)
 #pragma unroll
-                            for (int h = 0; h < 2; ++h) {
-                                const float4 v = __ldcg(src + (i * 2 + h) * kConsumerThreads + threadIdx.x);
+                            for (int h = 0; h < H; ++h) {
+                                const float4 v = __ldcg(src + (i * H + h) * kConsumerThreads + threadIdx.x);
                                 acc[i][2 * h].x += v.x;
                                 acc[i][2 * h].y += v.y;
                                 acc[i][2 * h + 1].x += v.z;
@@ -525,8 +548,8 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), 1)
 #pragma unroll
             for (int i = 0; i < 8; ++i)
 #pragma unroll
-                for (int h = 0; h < 2; ++h)
-                    sts128(base + static_cast<uint32_t>(((i * 2 + h) * kConsumerThreads + threadIdx.x) * 16),
+                for (int h = 0; h < H; ++h)
+                    sts128(base + static_cast<uint32_t>(((i * H + h) * kConsumerThreads + threadIdx.x) * 16),
                            make_float4(acc[i][2 * h].x, acc[i][2 * h].y, acc[i][2 * h + 1].x, acc[i][2 * h + 1].y));
         }
         cluster_sync_all();
@@ -535,9 +558,9 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), 1)
 #pragma unroll
                 for (int i = 0; i < 8; ++i)
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
+                    for (int h = 0; h < H; ++h) {
                         const uint32_t off =
-                            base + static_cast<uint32_t>(((i * 2 + h) * kConsumerThreads + threadIdx.x) * 16);
+                            base + static_cast<uint32_t>(((i * H + h) * kConsumerThreads + threadIdx.x) * 16);
                         const float4 v = ld_shared_cluster_v4(map_shared_rank(off, static_cast<uint32_t>(r)));
                         acc[i][2 * h].x += v.x;
                         acc[i][2 * h].y += v.y;

@@ -186,6 +186,11 @@ typedef struct sgemm_options {
                              stream-ordered pool the library creates on the
                              device (cudaMallocFromPoolAsync / cudaFreeAsync
                              on `stream`), which keeps it for reuse. */
+    int tile_n;           /* 0 = auto; 128 = 128 x 128 output tiles (8 x 8 per
+                             thread); 256 = 128 x 256 tiles (8 x 16 per thread,
+                             TMA producer warpgroup with the register split,
+                             2..4 stages; the stream-K workspace is then
+                             CTAs x (128 KiB + 4 bytes)) */
 } sgemm_options;
 
 /* sgemm_f32 with forced choices.  Same contract; an unsupported combination

@@ -98,6 +98,11 @@ VARIANTS = (
     + [dict(producer=3, math=2, multicast=2, split_k=1)]
     + [dict(producer=3, math=2, split_k=s, multicast=1) for s in (2, 4)]
     + [dict(producer=3, math=m, stream_k=2) for m in (1, 2)]
+    # 128 x 256 tiles (8 x 16 accumulators per thread)
+    + [dict(tile_n=256, math=m, stages=s, split_k=1) for m in (1, 2) for s in (2, 3, 4)]
+    + [dict(tile_n=256, multicast=2, split_k=1)]
+    + [dict(tile_n=256, split_k=s) for s in (2, 4)]
+    + [dict(tile_n=256, stream_k=2, math=m) for m in (1, 2)]
 )
 
 
