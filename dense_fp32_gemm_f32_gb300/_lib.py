@@ -42,6 +42,7 @@ class Options(ctypes.Structure):
         ("tail_split", _i),
         ("stream_k", _i),
         ("tile_n", _i),
+        ("repack", _i),
     ]
 
 

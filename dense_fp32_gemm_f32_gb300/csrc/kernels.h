@@ -1,6 +1,8 @@
 // Host-side registry of the compiled kernel variants (internal to the library).
 #pragma once
 
+#include <cuda_runtime.h>
+
 namespace gb300 {
 
 struct KernelEntry {
@@ -26,5 +28,13 @@ KernelEntry tf32x3_kernel();
 // Direct-A three-product TF32 kernel: A's big part read from the TMA tile,
 // only A's small part and B's two parts stored (128 x 128 tiles).
 KernelEntry tf32x3_direct_kernel();
+
+// Copies up to two operands (a null dst skips one): `rows` rows of `cols`
+// floats from `src` (pitch ld_src floats, any alignment) to `dst` (pitch
+// ld_dst floats: a multiple of 4, >= cols; 16-byte aligned base), zero-filling
+// each row's padding; one launch, enqueued on `stream`.
+int pack_rows(const float* src0, long long ld_src0, float* dst0, long long ld_dst0, int rows0, int cols0,
+              const float* src1, long long ld_src1, float* dst1, long long ld_dst1, int rows1, int cols1,
+              cudaStream_t stream);
 
 }  // namespace gb300

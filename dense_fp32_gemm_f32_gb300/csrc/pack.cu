@@ -1,0 +1,82 @@
+// Row repacking for operands whose rows the tensor maps cannot address.
+//
+// A tensor map needs a 16-byte aligned base and a row pitch that is a multiple
+// of 16 bytes.  An operand without them (a leading dimension that is not a
+// multiple of 4 floats, or a base off a 16-byte boundary) is copied once into
+// a buffer whose pitch is the row width rounded up to 4 floats; the product
+// then runs on the tensor-map path.  The copy is plain element moves, so the
+// product's result is unchanged.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "kernels.h"
+#include "../../include/sgemm.h"
+
+namespace gb300 {
+namespace {
+
+constexpr int kPackThreads = 256;
+
+struct PackJob {
+    const float* src;
+    long long ld_src;
+    float* dst;
+    long long ld_dst;
+    int rows, cols;
+};
+
+// Job blockIdx.z: dst row r, floats [c4, c4 + 4) <- src row r, the same
+// columns (zeros past `cols`, i.e. in the pitch padding).  Reads are
+// coalesced scalar loads (the source rows have any alignment), writes 16-byte
+// stores.
+__global__ void __launch_bounds__(kPackThreads) pack_rows_kernel(const PackJob j0, const PackJob j1) {
+    const PackJob& j = blockIdx.z == 0 ? j0 : j1;
+    const long long c4 = (static_cast<long long>(blockIdx.x) * kPackThreads + threadIdx.x) * 4;
+    if (c4 >= j.ld_dst) return;
+    for (long long r = blockIdx.y; r < j.rows; r += gridDim.y) {
+        const float* s = j.src + r * j.ld_src;
+        float4 v;
+        v.x = c4 + 0 < j.cols ? s[c4 + 0] : 0.f;
+        v.y = c4 + 1 < j.cols ? s[c4 + 1] : 0.f;
+        v.z = c4 + 2 < j.cols ? s[c4 + 2] : 0.f;
+        v.w = c4 + 3 < j.cols ? s[c4 + 3] : 0.f;
+        *reinterpret_cast<float4*>(j.dst + r * j.ld_dst + c4) = v;
+    }
+}
+
+bool job_ok(const PackJob& j) {
+    return j.ld_dst >= j.cols && j.ld_dst % 4 == 0 && (reinterpret_cast<uintptr_t>(j.dst) & 15u) == 0;
+}
+
+}  // namespace
+
+int pack_rows(const float* src0, long long ld_src0, float* dst0, long long ld_dst0, int rows0, int cols0,
+              const float* src1, long long ld_src1, float* dst1, long long ld_dst1, int rows1, int cols1,
+              cudaStream_t stream) {
+    PackJob j[2] = {{src0, ld_src0, dst0, ld_dst0, rows0, cols0}, {src1, ld_src1, dst1, ld_dst1, rows1, cols1}};
+    int n = 0;
+    PackJob use[2];
+    for (const PackJob& x : j)
+        if (x.dst && x.rows > 0 && x.cols > 0) {
+            if (!job_ok(x)) return SGEMM_ERR_INVALID_ARG;
+            use[n++] = x;
+        }
+    if (n == 0) return SGEMM_OK;
+    if (n == 1) use[1] = use[0];
+    long long gx = 0;
+    int gy = 0;
+    for (int i = 0; i < n; ++i) {
+        const long long x = (use[i].ld_dst / 4 + kPackThreads - 1) / kPackThreads;
+        gx = x > gx ? x : gx;
+        const int y = use[i].rows < 65535 ? use[i].rows : 65535;
+        gy = y > gy ? y : gy;
+    }
+    if (gx > 0x7fffffffLL) return SGEMM_ERR_INVALID_ARG;
+    pack_rows_kernel<<<dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy), static_cast<unsigned>(n)),
+                       kPackThreads, 0, stream>>>(use[0], use[1]);
+    if (cudaGetLastError() != cudaSuccess) return SGEMM_ERR_CUDA;
+    return SGEMM_OK;
+}
+
+}  // namespace gb300

@@ -167,7 +167,10 @@ cudaMemPool_t workspace_pool(int dev, DeviceState& st) {
             (void)cudaGetLastError();
             return;
         }
-        uint64_t threshold = ~0ull;
+        // Keep up to 256 MiB cached (the stream-K workspaces, ~10-20 MiB, and
+        // repack buffers of moderate size); larger repack buffers go back to
+        // the system at the next synchronisation.
+        uint64_t threshold = 256ull << 20;
         if (cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &threshold) != cudaSuccess)
             (void)cudaGetLastError();
         st.pool = pool;
@@ -217,6 +220,53 @@ int validate(int M, int N, int K, const float* A, int lda, const float* B, int l
     return SGEMM_OK;
 }
 
+// Operands copied into 16-byte pitched rows (see pack_rows) for the length of
+// one call: the copies come from the library's pool and go back to it, in
+// stream order, by release().
+struct Repacked {
+    void* ws = nullptr;
+    cudaStream_t stream = nullptr;
+
+    // Copies operand A (mask bit 0) and/or B (bit 1) and points A / lda and
+    // B / ldb at the copies.  SGEMM_ERR_CUDA if the pool cannot serve them
+    // (nothing is enqueued then).
+    int make(int dev, DeviceState& st, int mask, int M, int N, int K, const float*& A, int& lda, const float*& B,
+             int& ldb, cudaStream_t cs) {
+        stream = cs;
+        const long long K4 = (static_cast<long long>(K) + 3) / 4 * 4;
+        const long long N4 = (static_cast<long long>(N) + 3) / 4 * 4;
+        if (K4 > 0x7fffffffLL || N4 > 0x7fffffffLL) return SGEMM_ERR_INVALID_ARG;
+        const size_t bytes_a = (mask & 1) ? ((static_cast<size_t>(M) * K4 * 4 + 255) & ~size_t{255}) : 0;
+        const size_t bytes_b = (mask & 2) ? static_cast<size_t>(K) * N4 * 4 : 0;
+        cudaMemPool_t pool = workspace_pool(dev, st);
+        if (!pool || cudaMallocFromPoolAsync(&ws, bytes_a + bytes_b, pool, cs) != cudaSuccess) {
+            (void)cudaGetLastError();
+            ws = nullptr;
+            return SGEMM_ERR_CUDA;
+        }
+        float* Ap = (mask & 1) ? static_cast<float*>(ws) : nullptr;
+        float* Bp = (mask & 2) ? reinterpret_cast<float*>(static_cast<char*>(ws) + bytes_a) : nullptr;
+        const int rc = pack_rows(A, lda, Ap, K4, M, K, B, ldb, Bp, N4, K, N, cs);
+        if (rc != SGEMM_OK) {
+            release();
+            return rc;
+        }
+        if (Ap) {
+            A = Ap;
+            lda = static_cast<int>(K4);
+        }
+        if (Bp) {
+            B = Bp;
+            ldb = static_cast<int>(N4);
+        }
+        return SGEMM_OK;
+    }
+    void release() {
+        if (ws) (void)cudaFreeAsync(ws, stream);
+        ws = nullptr;
+    }
+};
+
 struct Launch {
     int tile_base = 0;  // first output tile
     int tiles = 0;      // output tiles in this launch (grid x)
@@ -235,7 +285,14 @@ struct Plan {
     Launch launch[2];
     int sk = 0;           // stream-K: launch[0].tiles CTAs, one per SM
     int sk_dp_tiles = 0;  // tiles taken whole (data-parallel waves) before the stream-K region
+    int repack = 0;       // operands copied to 16-byte pitched rows first: bit 0 = A, bit 1 = B
 };
+
+// Repacking pays once the product is large next to the copy.  Measured on
+// GB300 (both operands misaligned, one copy launch for both): 1023 x 1025 x
+// 1027 (2^31 flop) 65 us against 69 us with cp.async, 2047 x 2049 x 2051
+// +23 %, 4095 x 4097 x 4099 and 8191 x 8193 x 8195 +30 %.
+constexpr double kRepackMinFlops = 1073741824.0;  // 2^30
 
 long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
 
@@ -273,9 +330,19 @@ int make_plan(const DeviceState& st, int M, int N, int K, const float* A, int ld
     long long tiles_n = ceil_div(N, kBN);
     const long long tiles_m = ceil_div(M, kBM);
 
-    // Producer: tensor maps need 16-byte aligned bases and row strides, and K > 0.
-    const bool aligned = K > 0 && tma_ok(A, lda) && tma_ok(B, ldb);
+    // Producer: tensor maps need 16-byte aligned bases and row strides, and
+    // K > 0.  An operand without them is either repacked into pitched rows
+    // (which the tensor maps can address) or read by the cp.async producer.
     const int want_prod = opt ? opt->producer : 0;
+    const int want_repack = opt ? opt->repack : 0;
+    if (want_repack < 0 || want_repack > 2) return SGEMM_ERR_INVALID_ARG;
+    const int misaligned = (tma_ok(A, lda) ? 0 : 1) | (tma_ok(B, ldb) ? 0 : 2);
+    if (K > 0 && misaligned &&
+        (want_repack == 2 ||
+         (want_repack == 0 && want_prod == SGEMM_PRODUCER_AUTO &&
+          2.0 * static_cast<double>(M) * static_cast<double>(N) * static_cast<double>(K) >= kRepackMinFlops)))
+        pl.repack = misaligned;
+    const bool aligned = K > 0 && (misaligned & ~pl.repack) == 0;
     if (want_prod == SGEMM_PRODUCER_TMA) {
         if (!aligned) return SGEMM_ERR_INVALID_ARG;
         pl.producer = kProducerTma;
@@ -449,7 +516,9 @@ const char* describe_plan(const Plan& pl) {
     if (pl.sk && n > 0 && n < static_cast<int>(sizeof buf))
         n += std::snprintf(buf + n, sizeof buf - n, "/sk%d", pl.launch[0].tiles);
     if (pl.bn != kBN && n > 0 && n < static_cast<int>(sizeof buf))
-        std::snprintf(buf + n, sizeof buf - n, "/n%d", pl.bn);
+        n += std::snprintf(buf + n, sizeof buf - n, "/n%d", pl.bn);
+    if (pl.repack && n > 0 && n < static_cast<int>(sizeof buf))
+        std::snprintf(buf + n, sizeof buf - n, "/repack%s", pl.repack == 1 ? "A" : pl.repack == 2 ? "B" : "AB");
     return buf;
 }
 
@@ -467,9 +536,29 @@ int run_ffma(int M, int N, int K, const float* A, int lda, const float* B, int l
     Plan pl;
     rc = make_plan(*st, M, N, K, A, lda, B, ldb, opt, &pl);
     if (rc != SGEMM_OK) return rc;
+    const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+
+    // Repacking: copy the misaligned operand(s) into pitched rows taken from
+    // the pool, and run the product on the copies.  If the pool cannot serve
+    // the copies, the automatic choice falls back to the cp.async producer.
+    Repacked packed;
+    if (pl.repack) {
+        rc = packed.make(dev, *st, pl.repack, M, N, K, A, lda, B, ldb, cs);
+        if (rc == SGEMM_ERR_CUDA && !(opt && opt->repack == 2)) {
+            sgemm_options o = opt ? *opt : sgemm_options{};
+            o.repack = 1;
+            rc = make_plan(*st, M, N, K, A, lda, B, ldb, &o, &pl);
+        }
+        if (rc != SGEMM_OK) return rc;
+    }
+    // Returns the repack buffers to the pool behind everything enqueued so far.
+    auto release_pack = [&] { packed.release(); };
 
     const KernelEntry k = ffma_kernel(pl);
-    if (!k.fn) return SGEMM_ERR_INVALID_ARG;
+    if (!k.fn) {
+        release_pack();
+        return SGEMM_ERR_INVALID_ARG;
+    }
 
     alignas(64) CUtensorMap tmA;
     alignas(64) CUtensorMap tmB;
@@ -478,7 +567,10 @@ int run_ffma(int M, int N, int K, const float* A, int lda, const float* B, int l
     if (is_tma(pl.producer)) {
         rc = encode_2d(&tmA, A, K, M, lda, kBK, kBM / pl.mcast, CU_TENSOR_MAP_SWIZZLE_128B);
         if (rc == SGEMM_OK) rc = encode_2d(&tmB, B, N, K, ldb, pl.bn, kBK, CU_TENSOR_MAP_SWIZZLE_NONE);
-        if (rc != SGEMM_OK) return rc;
+        if (rc != SGEMM_OK) {
+            release_pack();
+            return rc;
+        }
     }
 
     FfmaParams prm;
@@ -509,13 +601,13 @@ int run_ffma(int M, int N, int K, const float* A, int lda, const float* B, int l
     // after the kernel (stream order makes concurrent calls on different
     // streams use different workspaces).
     void* ws = nullptr;
-    const cudaStream_t cs = static_cast<cudaStream_t>(stream);
     if (pl.sk) {
         const size_t G = static_cast<size_t>(pl.launch[0].tiles);
         const size_t tile_bytes = static_cast<size_t>(kBM) * pl.bn * sizeof(float);
         cudaMemPool_t pool = workspace_pool(dev, *st);
         if (!pool || cudaMallocFromPoolAsync(&ws, G * tile_bytes + G * sizeof(unsigned int), pool, cs) != cudaSuccess) {
             (void)cudaGetLastError();
+            release_pack();
             return SGEMM_ERR_CUDA;
         }
         prm.ws = static_cast<float*>(ws);
@@ -523,6 +615,7 @@ int run_ffma(int M, int N, int K, const float* A, int lda, const float* B, int l
         if (cudaMemsetAsync(prm.flags, 0, G * sizeof(unsigned int), cs) != cudaSuccess) {
             (void)cudaGetLastError();
             (void)cudaFreeAsync(ws, cs);
+            release_pack();
             return SGEMM_ERR_CUDA;
         }
     }
@@ -555,9 +648,11 @@ int run_ffma(int M, int N, int K, const float* A, int lda, const float* B, int l
         if (cudaLaunchKernelExC(&cfg, k.fn, args) != cudaSuccess) {
             (void)cudaGetLastError();
             if (ws) (void)cudaFreeAsync(ws, cs);
+            release_pack();
             return SGEMM_ERR_CUDA;
         }
     }
+    release_pack();
     if (ws && cudaFreeAsync(ws, cs) != cudaSuccess) {
         (void)cudaGetLastError();
         return SGEMM_ERR_CUDA;
@@ -597,6 +692,7 @@ int run_ffma_noalloc(int M, int N, int K, const float* A, int lda, const float* 
     o.stream_k = K > 0 ? 2 : 1;
     o.split_k = K > 0 ? 0 : 1;
     o.tile_n = kBN;
+    o.repack = 1;  // repacking would allocate: misaligned operands take the cp.async producer
     Plan pl;
     rc = make_plan(*st, M, N, K, A, lda, B, ldb, &o, &pl);
     if (rc != SGEMM_OK) return rc;
@@ -678,21 +774,34 @@ int run_3xtf32(int M, int N, int K, const float* A, int lda, const float* B, int
     DeviceState* st = nullptr;
     rc = current_device(&dev, &st);
     if (rc != SGEMM_OK) return rc;
-    // The tensor-core kernel is fed by tensor maps; operands the TMA cannot
-    // read (unaligned bases or row strides), and K == 0, take the FFMA kernel,
-    // which meets the same contract.
-    if (K == 0 || !tma_ok(A, lda) || !tma_ok(B, ldb)) return run_ffma(M, N, K, A, lda, B, ldb, C, ldc, stream, nullptr);
-
+    // The tensor-core kernel is fed by tensor maps.  Operands the TMA cannot
+    // read (unaligned bases or row strides) are repacked into pitched rows
+    // when the product is large enough for that to pay (the same rule as
+    // sgemm_f32); otherwise they, and K == 0, take the FFMA kernel, which
+    // meets the same contract.
     // Variant: 1 = split-tile kernel (all four TF32 parts in shared memory),
     // 2 = direct-A kernel (A's big part is the TMA tile itself).
     const int variant = (opt && opt->math) ? opt->math : kTf32x3DefaultVariant;
     if (variant < 1 || variant > 2) return SGEMM_ERR_INVALID_ARG;
+    const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    const int misaligned = (tma_ok(A, lda) ? 0 : 1) | (tma_ok(B, ldb) ? 0 : 2);
+    Repacked packed;
+    if (K > 0 && misaligned &&
+        2.0 * static_cast<double>(M) * static_cast<double>(N) * static_cast<double>(K) >= kRepackMinFlops)
+        (void)packed.make(dev, *st, misaligned, M, N, K, A, lda, B, ldb, cs);  // (on failure: the FFMA kernel)
+    if (K == 0 || !tma_ok(A, lda) || !tma_ok(B, ldb)) {
+        packed.release();
+        return run_ffma(M, N, K, A, lda, B, ldb, C, ldc, stream, nullptr);
+    }
     const KernelEntry k = variant == 1 ? tf32x3_kernel() : tf32x3_direct_kernel();
     alignas(64) CUtensorMap tmA;
     alignas(64) CUtensorMap tmB;
     rc = encode_2d(&tmA, A, K, M, lda, kTcBK, kTcBM, CU_TENSOR_MAP_SWIZZLE_128B);
     if (rc == SGEMM_OK) rc = encode_2d(&tmB, B, N, K, ldb, kTcBN, kTcBK, CU_TENSOR_MAP_SWIZZLE_NONE);
-    if (rc != SGEMM_OK) return rc;
+    if (rc != SGEMM_OK) {
+        packed.release();
+        return rc;
+    }
 
     TcParams prm;
     prm.M = M;
@@ -715,11 +824,13 @@ int run_3xtf32(int M, int N, int K, const float* A, int lda, const float* B, int
     cfg.stream = static_cast<cudaStream_t>(stream);
     cfg.numAttrs = 0;
     void* args[3] = {&tmA, &tmB, &prm};
+    rc = SGEMM_OK;
     if (cudaLaunchKernelExC(&cfg, k.fn, args) != cudaSuccess) {
         (void)cudaGetLastError();
-        return SGEMM_ERR_CUDA;
+        rc = SGEMM_ERR_CUDA;
     }
-    return SGEMM_OK;
+    packed.release();
+    return rc;
 }
 
 }  // namespace

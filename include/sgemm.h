@@ -191,6 +191,14 @@ typedef struct sgemm_options {
                              TMA producer warpgroup with the register split,
                              2..4 stages; the stream-K workspace is then
                              CTAs x (128 KiB + 4 bytes)) */
+    int repack;           /* 0 = auto, 1 = off, 2 = on: an operand whose base
+                             or row pitch is not a multiple of 16 bytes is
+                             first copied into rows of ceil(width / 4) x 4
+                             floats (a pool workspace of M x K4 and/or
+                             K x N4 floats) and the product runs on the
+                             tensor-map path; auto = on when no producer is
+                             forced and 2MNK >= 2^30, else such operands are
+                             read by the cp.async producer */
 } sgemm_options;
 
 /* sgemm_f32 with forced choices.  Same contract; an unsupported combination

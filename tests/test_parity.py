@@ -303,7 +303,64 @@ def test_variant_choice():
     assert "/tail" not in desc(4096, 4096, 4096)  # the tail split is opt-in
     assert "/sk" in desc(8192, 128, 8192) and "/sk" in desc(128, 8192, 16384)
     assert "/sk" not in desc(256, 256, 256) and "/s1/" not in desc(256, 256, 256)  # tiny: cluster split-K
-    assert desc(1023, 1025, 1027).startswith("cpasync/")  # 1027-float rows are not 16-byte multiples
+    # 1027-float rows are not 16-byte multiples: the operands are repacked
+    # into pitched rows and the tensor-map path runs; small products read the
+    # rows as they are with cp.async
+    assert desc(1023, 1025, 1027).startswith("tma/") and desc(1023, 1025, 1027).endswith("/repackAB")
+    assert desc(300, 500, 701).startswith("cpasync/")
+    assert desc(2048, 2049, 2048).endswith("/repackB")
+
+
+# ---------------------------------------------------------------- repacking
+
+@pytest.mark.parametrize("case", [
+    # (M, N, K, lda, ldb, offset A, offset B): misaligned A only, B only, both,
+    # and misaligned bases with aligned pitches
+    (300, 500, 701, 701, 500, 0, 0),
+    (300, 501, 700, 700, 501, 0, 0),
+    (257, 333, 385, 387, 335, 0, 0),
+    (200, 256, 260, 260, 256, 1, 2),
+])
+def test_forced_repack(case):
+    M, N, K, lda, ldb, oa, ob = case
+    for dist, seed in (("uniform", 91), ("int", 92)):
+        A, B = make_operands(M, N, K, dist, seed)
+        dA, dB = to_device(A, lda, offset=oa), to_device(B, ldb, offset=ob)
+        C = g.sgemm_f32_ex(dA, dB, repack=2)
+        torch.cuda.synchronize()
+        C64, bound = oracle.gemm_f64(A.numpy(), B.numpy(), with_bound=(dist != "int"))
+        check(C.cpu().numpy(), C64, bound, exact=(dist == "int"), what=f"repack {case} {dist}")
+
+
+def test_ragged_problem_without_repacking():
+    """The ragged problem with repacking off: the cp.async producer reads the
+    misaligned rows directly."""
+    p = PROBLEMS["ragged_1023x1025x1027"]
+    A, B = problem_operands(p)
+    dA, dB = to_device(A), to_device(B)
+    C = g.sgemm_f32_ex(dA, dB, repack=1)
+    torch.cuda.synchronize()
+    C64, bound = oracle.gemm_f64(A.numpy(), B.numpy())
+    check(C.cpu().numpy(), C64, bound, exact=False, what="ragged, cp.async")
+    Ai, Bi = problem_operands(p.int_variant())
+    Ci = g.sgemm_f32_ex(to_device(Ai), to_device(Bi), repack=1)
+    torch.cuda.synchronize()
+    check(Ci.cpu().numpy(), oracle.gemm_f64(Ai.numpy(), Bi.numpy(), with_bound=False)[0], None, exact=True,
+          what="ragged int, cp.async")
+
+
+def test_repacked_large_ragged_sampled_rows():
+    """2047 x 2049 x 2051 (the automatic choice repacks both operands):
+    sampled full rows against the oracle."""
+    M, N, K = 2047, 2049, 2051
+    A, B = make_operands(M, N, K, "uniform", 93)
+    dA, dB = to_device(A), to_device(B)
+    assert g.describe(dA, dB).endswith("/repackAB")
+    C = g.sgemm_f32(dA, dB)
+    torch.cuda.synchronize()
+    rows = sample_rows(M, n_random=8, seed=93)
+    C64, bound = oracle.gemm_rows_f64(A.numpy(), B.numpy(), rows)
+    check(C.cpu().numpy()[rows], C64, bound, exact=False, what="2047x2049x2051 rows")
 
 
 # ---------------------------------------------------------------- bounded waits

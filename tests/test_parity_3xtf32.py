@@ -86,13 +86,25 @@ def test_named_problem_sampled_rows(name, dist, variant):
     check(C[rows], C64, bound, exact=(dist == "int"), what=f"{p.name} rows")
 
 
-def test_ragged_problem_falls_back_and_matches():
-    """1023 x 1025 x 1027: rows of 1027 floats are not 16-byte multiples, so the
-    call runs the FFMA kernels; the contract is the same."""
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_ragged_problem_repacked(variant):
+    """1023 x 1025 x 1027: rows of 1027 floats are not 16-byte multiples; the
+    operands are repacked into pitched rows and the tensor-core kernel runs."""
     p = PROBLEMS["ragged_1023x1025x1027"]
     A, B = problem_operands(p)
     C64, bound = oracle.gemm_f64(A.numpy(), B.numpy())
-    check(run(A, B), C64, bound, exact=False, what=p.name)
+    check(run(A, B, variant=variant), C64, bound, exact=False, what=p.name)
+    Ai, Bi = problem_operands(p.int_variant())
+    check(run(Ai, Bi, variant=variant), oracle.gemm_f64(Ai.numpy(), Bi.numpy(), with_bound=False)[0], None,
+          exact=True, what=p.name + " int")
+
+
+def test_small_misaligned_falls_back_and_matches():
+    """Small products with misaligned rows run the FFMA kernels (cp.async);
+    the contract is the same."""
+    A, B = make_operands(200, 301, 333, "uniform", 94)
+    C64, bound = oracle.gemm_f64(A.numpy(), B.numpy())
+    check(run(A, B), C64, bound, exact=False, what="200x301x333")
 
 
 @pytest.mark.parametrize("variant", VARIANTS)
