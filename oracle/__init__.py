@@ -80,7 +80,11 @@ class OracleLib:
         lib.oracle_sgemm_f64.argtypes = [i64, i64, i64, p, i64, p, i64, p, i64, p, i64, ctypes.c_int]
         lib.oracle_sgemm_rows_f64.argtypes = [i64, i64, i64, p, i64, p, i64, p, i64, p, p, ctypes.c_int]
         lib.oracle_sgemm_entries_f64.argtypes = [i64, i64, i64, p, i64, p, i64, p, p, i64, p, p]
-        for f in (lib.oracle_sgemm_f64, lib.oracle_sgemm_rows_f64, lib.oracle_sgemm_entries_f64):
+        f32, i32 = ctypes.c_float, ctypes.c_int
+        lib.oracle_gemm_general_f64.argtypes = [i32, i32, i64, i64, i64, f32, p, i64, p, i64, f32, p, i64, p, i64,
+                                                p, i64, p, i64, i32]
+        for f in (lib.oracle_sgemm_f64, lib.oracle_sgemm_rows_f64, lib.oracle_sgemm_entries_f64,
+                  lib.oracle_gemm_general_f64):
             f.restype = ctypes.c_int
         self.lib = lib
         self.path = path
@@ -136,6 +140,45 @@ class OracleLib:
         return c, bound
 
 
+    def gemm_general_f64(self, A, B, C=None, *, alpha=1.0, beta=0.0, transa=False, transb=False, rows=None,
+                         with_bound: bool = True, threads: int | None = None):
+        """C_out = alpha * op(A) op(B) + beta * C in float64, with its bound
+        |alpha| sum_k |a||b| + |beta||c|.
+
+        A and B are the stored operands (float32, row-major, any row stride):
+        A is (M, K), or (K, M) when ``transa``; B is (K, N), or (N, K) when
+        ``transb``.  C is (M, N) float32, needed only when beta != 0.  With
+        ``rows``, only those output rows are computed.  Returns (C_out, bound)
+        as float64 arrays (bound None if not requested).
+        """
+        A, lda = _as_f32_rows(A, "A")
+        B, ldb = _as_f32_rows(B, "B")
+        M, K = (A.shape[1], A.shape[0]) if transa else A.shape
+        KB, N = (B.shape[1], B.shape[0]) if transb else B.shape
+        if K != KB:
+            raise ValueError(f"inner dimensions differ: op(A) is {(M, K)}, op(B) is {(KB, N)}")
+        ldcin = 0
+        if beta != 0 and C is None:
+            raise ValueError("beta != 0 needs C")
+        if C is not None:  # passed even when beta == 0, which must leave it unread
+            C, ldcin = _as_f32_rows(C, "C")
+            if C.shape != (M, N):
+                raise ValueError(f"C must be {(M, N)}, got {C.shape}")
+        rows_arr = None if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
+        nrows = M if rows_arr is None else rows_arr.size
+        out = np.empty((nrows, N), dtype=np.float64)
+        bound = np.empty((nrows, N), dtype=np.float64) if with_bound else None
+        rc = self.lib.oracle_gemm_general_f64(int(bool(transa)), int(bool(transb)), M, N, K, float(alpha), _ptr(A),
+                                              lda, _ptr(B), ldb, float(beta),
+                                              _ptr(C) if C is not None else ctypes.c_void_p(0), ldcin,
+                                              _ptr(rows_arr) if rows_arr is not None else ctypes.c_void_p(0), nrows,
+                                              _ptr(out), max(N, 1), _ptr(bound), max(N, 1),
+                                              threads or default_threads())
+        if rc != 0:
+            raise RuntimeError(f"oracle_gemm_general_f64 failed with {rc}")
+        return out, bound
+
+
 def default() -> OracleLib:
     global _default
     with _lock:
@@ -154,3 +197,7 @@ def gemm_rows_f64(A, B, rows, **kw):
 
 def gemm_entries_f64(A, B, ii, jj):
     return default().gemm_entries_f64(A, B, ii, jj)
+
+
+def gemm_general_f64(A, B, C=None, **kw):
+    return default().gemm_general_f64(A, B, C, **kw)

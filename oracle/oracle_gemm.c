@@ -32,6 +32,20 @@
  * i -> j -> k triple loop (a test checks this).  Rows are split over POSIX
  * threads; each thread owns whole rows, so the threading changes no sum.
  *
+ * The general form (oracle_gemm_general_f64) computes the BLAS-style
+ *
+ *     C_out[i][j] = alpha * sum_k op(A)[i][k] * op(B)[k][j] + beta * C_in[i][j]
+ *
+ * where op(X) is X or its transpose (row-major storage: op(A)[i][k] is
+ * A[k][i] when A is stored transposed, K x M), and C_in is not read when
+ * beta == 0 (so NaN or uninitialised memory there has no effect).  The pages
+ * define only the plain product; scaling, accumulation into C and transposed
+ * storage are the standard GEMM interface (the "Column-major" remark of the
+ * optimisation-summary page is the pages' only mention of another layout).
+ * The k sum is formed exactly as for the plain product (ascending k, double
+ * accumulator, exact float products); then alpha * sum + beta * C_in in
+ * double.  Its bound is |alpha| * sum_k |a||b| + |beta| * |C_in|.
+ *
  * Build: gcc -O2 -fno-fast-math -ffp-contract=off -fPIC -shared -pthread
  * (no contraction into fused multiply-add, no reassociation).
  */
@@ -53,6 +67,11 @@ typedef struct {
     int64_t ldbound;
     const int64_t *rows; /* row indices into A; NULL = 0..nrows-1 */
     int64_t row_begin, row_end; /* range of output rows this worker owns */
+    /* general form only (general != 0) */
+    int general, transa, transb;
+    float alpha, beta;
+    const float *Cin;
+    int64_t ldcin;
 } oracle_job;
 
 /* One output row: C[r][:] = sum_k A[i][k] * B[k][:], k ascending. */
@@ -76,10 +95,48 @@ static void oracle_one_row(const oracle_job *jb, int64_t r)
     }
 }
 
+/* One output row of the general form.  op(A)[i][k] and op(B)[k][j] are read
+ * through the storage order of each operand; k ascending as above. */
+static void oracle_general_row(const oracle_job *jb, int64_t r)
+{
+    const int64_t i = jb->rows ? jb->rows[r] : r;
+    double *out = jb->C + r * jb->ldc;
+    double *bnd = jb->bound ? jb->bound + r * jb->ldbound : NULL;
+    for (int64_t j = 0; j < jb->N; ++j) {
+        out[j] = 0.0;
+        if (bnd) bnd[j] = 0.0;
+    }
+    for (int64_t k = 0; k < jb->K; ++k) {
+        const double aik = (double)(jb->transa ? jb->A[k * jb->lda + i] : jb->A[i * jb->lda + k]);
+        for (int64_t j = 0; j < jb->N; ++j) {
+            const double bkj = (double)(jb->transb ? jb->B[j * jb->ldb + k] : jb->B[k * jb->ldb + j]);
+            out[j] += aik * bkj;
+            if (bnd) bnd[j] += fabs(aik) * fabs(bkj);
+        }
+    }
+    const double alpha = (double)jb->alpha, beta = (double)jb->beta;
+    for (int64_t j = 0; j < jb->N; ++j) {
+        double v = alpha * out[j];
+        double vb = bnd ? fabs(alpha) * bnd[j] : 0.0;
+        if (jb->beta != 0.0f) { /* beta == 0: C_in is not read */
+            const double c = (double)jb->Cin[i * jb->ldcin + j];
+            v += beta * c;
+            vb += fabs(beta) * fabs(c);
+        }
+        out[j] = v;
+        if (bnd) bnd[j] = vb;
+    }
+}
+
 static void *oracle_worker(void *arg)
 {
     const oracle_job *jb = (const oracle_job *)arg;
-    for (int64_t r = jb->row_begin; r < jb->row_end; ++r) oracle_one_row(jb, r);
+    for (int64_t r = jb->row_begin; r < jb->row_end; ++r) {
+        if (jb->general)
+            oracle_general_row(jb, r);
+        else
+            oracle_one_row(jb, r);
+    }
     return NULL;
 }
 
@@ -202,4 +259,43 @@ int oracle_sgemm_entries_f64(int64_t M, int64_t N, int64_t K,
         if (bound) bound[t] = sb;
     }
     return 0;
+}
+
+/*
+ * General form, C_out = alpha * op(A) op(B) + beta * C_in (see the header).
+ * op(A) is M x K: A is stored M x K (lda >= K), or K x M (lda >= M) when
+ * transa != 0.  op(B) is K x N: B is stored K x N (ldb >= N), or N x K
+ * (ldb >= K) when transb != 0.  C_in is M x N with ldcin >= N (read only when
+ * beta != 0).  With rows != NULL, output row r (C, bound: nrows x ldc /
+ * ldbound) is row rows[r] of the result; with rows == NULL, nrows must be M.
+ */
+int oracle_gemm_general_f64(int transa, int transb, int64_t M, int64_t N, int64_t K,
+                            float alpha,
+                            const float *A, int64_t lda,
+                            const float *B, int64_t ldb,
+                            float beta,
+                            const float *Cin, int64_t ldcin,
+                            const int64_t *rows, int64_t nrows,
+                            double *C, int64_t ldc,
+                            double *bound, int64_t ldbound,
+                            int threads)
+{
+    if (M < 0 || N < 0 || K < 0 || nrows < 0) return -1;
+    if (lda < (transa ? M : K) || ldb < (transb ? K : N)) return -1;
+    if (M > 0 && K > 0 && !A) return -1;
+    if (K > 0 && N > 0 && !B) return -1;
+    if (beta != 0.0f && M > 0 && N > 0 && (!Cin || ldcin < N)) return -1;
+    if (ldc < N || (nrows > 0 && N > 0 && !C)) return -1;
+    if (bound && ldbound < N) return -1;
+    if (!rows && nrows != M) return -1;
+    if (rows)
+        for (int64_t r = 0; r < nrows; ++r)
+            if (rows[r] < 0 || rows[r] >= M) return -1;
+    oracle_job jb;
+    memset(&jb, 0, sizeof(jb));
+    jb.N = N; jb.K = K; jb.A = A; jb.lda = lda; jb.B = B; jb.ldb = ldb;
+    jb.C = C; jb.ldc = ldc; jb.bound = bound; jb.ldbound = ldbound; jb.rows = rows;
+    jb.general = 1; jb.transa = transa != 0; jb.transb = transb != 0;
+    jb.alpha = alpha; jb.beta = beta; jb.Cin = Cin; jb.ldcin = ldcin;
+    return oracle_run(jb, nrows, threads);
 }

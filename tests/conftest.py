@@ -35,7 +35,12 @@ def load_golden(name):
                 cur = {"name": tok[1], "M": int(tok[2]), "N": int(tok[3]), "K": int(tok[4])}
                 cases.append(cur)
                 section, rows = None, []
-            elif tok[0] in ("A", "B", "C", "BOUND"):
+            elif tok[0] == "opts":  # general form: transa transb alpha beta
+                flush()
+                cur["opts"] = {"transa": int(tok[1]), "transb": int(tok[2]), "alpha": float(tok[3]),
+                               "beta": float(tok[4])}
+                section, rows = None, []
+            elif tok[0] in ("A", "B", "C", "CIN", "BOUND"):
                 flush()
                 section, rows = tok[0], []
             else:

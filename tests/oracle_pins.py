@@ -164,6 +164,111 @@ def pin_thread_invariance(o):
     assert np.array_equal(C1, C7) and np.array_equal(b1, b7)
 
 
+# ---------------------------------------------------------------- general form
+
+def pin_general_hand_cases(o):
+    for case in load_golden("general_cases.txt"):
+        op = case["opts"]
+        A = case["A"].astype(np.float32)
+        B = case["B"].astype(np.float32)
+        Cin = case.get("CIN")
+        Cin = None if Cin is None else Cin.astype(np.float32)
+        C, bound = o.gemm_general_f64(A, B, Cin, alpha=op["alpha"], beta=op["beta"], transa=op["transa"],
+                                      transb=op["transb"])
+        assert C.shape == (case["M"], case["N"]), case["name"]
+        assert np.array_equal(C, case["C"]), (case["name"], C, case["C"])
+        assert np.array_equal(bound, case["BOUND"]), (case["name"], bound, case["BOUND"])
+
+
+def pin_general_transposed_storage(o):
+    """Transposed storage gives the plain product of the explicitly transposed
+    copies, bit for bit (alpha 1, beta 0), also with padded rows."""
+    M, N, K = 23, 19, 31
+    A, B = make_operands(M, N, K, "normal", 61)
+    A, B = _np(A), _np(B)
+    ref, rbound = o.gemm_f64(A, B)
+    At = np.full((K, M + 5), np.nan, np.float32)
+    At[:, :M] = A.T
+    Bt = np.full((N, K + 3), np.nan, np.float32)
+    Bt[:, :K] = B.T
+    for ta, tb in [(0, 0), (1, 0), (0, 1), (1, 1)]:
+        C, bound = o.gemm_general_f64(At[:, :M] if ta else A, Bt[:, :K] if tb else B, transa=ta, transb=tb)
+        assert np.array_equal(C, ref), (ta, tb)
+        assert np.array_equal(bound, rbound), (ta, tb)
+
+
+def pin_general_scaling(o):
+    """alpha = 0 leaves beta * C_in exactly; beta = 0 ignores C_in (NaN there
+    has no effect) and a power-of-two alpha scales the product exactly."""
+    A, B = make_operands(17, 13, 29, "uniform", 62)
+    A, B = _np(A), _np(B)
+    Cin = _np(make_operands(17, 1, 13, "uniform", 63)[0])
+    ref, rbound = o.gemm_f64(A, B)
+    C, bound = o.gemm_general_f64(A, B, Cin, alpha=0.0, beta=3.0)
+    assert np.array_equal(C, 3.0 * Cin.astype(np.float64))
+    assert np.array_equal(bound, 3.0 * np.abs(Cin).astype(np.float64))
+    nan = np.full((17, 13), np.nan, np.float32)
+    C, bound = o.gemm_general_f64(A, B, nan, alpha=-4.0, beta=0.0)
+    assert np.array_equal(C, -4.0 * ref) and np.array_equal(bound, 4.0 * rbound)
+    C, bound = o.gemm_general_f64(A, B, Cin, alpha=1.0, beta=1.0)
+    assert np.all(np.abs(C - (ref + Cin)) <= 2.0**-52 * np.abs(ref + Cin))
+
+
+def pin_general_integer_bruteforce(o):
+    """Integer inputs and integer alpha, beta: equal to Python-integer
+    arithmetic with the transposed indexing written out."""
+    M, N, K = 5, 4, 6
+    for ta, tb in [(0, 0), (1, 0), (0, 1), (1, 1)]:
+        a, b = make_operands(M, N, K, "int", 70 + 2 * ta + tb)
+        a, b = _np(a), _np(b)
+        cin = _np(make_operands(M, 1, N, "int", 80 + 2 * ta + tb)[0])
+        As = np.ascontiguousarray(a.T) if ta else a
+        Bs = np.ascontiguousarray(b.T) if tb else b
+        alpha, beta = 3, -2
+        C, _ = o.gemm_general_f64(As, Bs, cin, alpha=alpha, beta=beta, transa=ta, transb=tb)
+        for i in range(M):
+            for j in range(N):
+                s = 0
+                for k in range(K):
+                    aik = int(As[k, i]) if ta else int(As[i, k])
+                    bkj = int(Bs[j, k]) if tb else int(Bs[k, j])
+                    s += aik * bkj
+                assert C[i, j] == alpha * s + beta * int(cin[i, j]), (ta, tb, i, j)
+
+
+def pin_general_fraction(o):
+    """Exact rationals with non-trivial alpha, beta and transposed A: error
+    within (K + 2) * 2^-53 * bound."""
+    M, N, K = 3, 4, 5
+    a, b = make_operands(M, N, K, "normal", 64)
+    a, b = _np(a), _np(b)
+    cin = _np(make_operands(M, 1, N, "normal", 65)[0])
+    alpha, beta = float(np.float32(0.7)), float(np.float32(-1.3))
+    At = np.ascontiguousarray(a.T)
+    C, bound = o.gemm_general_f64(At, b, cin, alpha=alpha, beta=beta, transa=1)
+    for i in range(M):
+        for j in range(N):
+            prods = [Fraction(float(a[i, k])) * Fraction(float(b[k, j])) for k in range(K)]
+            exact = Fraction(alpha) * sum(prods) + Fraction(beta) * Fraction(float(cin[i, j]))
+            ebound = abs(Fraction(alpha)) * sum(abs(p) for p in prods) + abs(Fraction(beta)) * abs(
+                Fraction(float(cin[i, j])))
+            tol = Fraction(K + 2) * Fraction(1, 2**53) * ebound
+            assert abs(Fraction(C[i, j]) - exact) <= tol, (i, j)
+            assert abs(Fraction(bound[i, j]) - ebound) <= tol, (i, j)
+
+
+def pin_general_sampled_rows(o):
+    """The row-sampled general form equals the matching rows of the full one."""
+    A, B = make_operands(21, 9, 14, "normal", 66)
+    A, B = _np(A), _np(B)
+    Cin = _np(make_operands(21, 1, 9, "normal", 67)[0])
+    At = np.ascontiguousarray(A.T)
+    full, fb = o.gemm_general_f64(At, B, Cin, alpha=1.5, beta=-0.25, transa=1)
+    rows = np.array([0, 20, 7, 7, 13])
+    part, pb = o.gemm_general_f64(At, B, Cin, alpha=1.5, beta=-0.25, transa=1, rows=rows)
+    assert np.array_equal(part, full[rows]) and np.array_equal(pb, fb[rows])
+
+
 ALL_PINS = [
     pin_golden_hand_cases,
     pin_identity,
@@ -177,4 +282,10 @@ ALL_PINS = [
     pin_bound_dominates,
     pin_sampling_entry_points,
     pin_thread_invariance,
+    pin_general_hand_cases,
+    pin_general_transposed_storage,
+    pin_general_scaling,
+    pin_general_integer_bruteforce,
+    pin_general_fraction,
+    pin_general_sampled_rows,
 ]

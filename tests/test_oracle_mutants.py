@@ -31,8 +31,20 @@ MUTANTS = {
                             "for (int64_t j = 0; j + 1 < jb->N; ++j) crow[j] += a"),
     "signed_bound": ("const double aa = fabs(a);", "const double aa = a;"),
     "bound_missing_b": ("brow[j] += aa * fabs((double)bk[j]);", "brow[j] += aa;"),
-    "off_by_one_row": ("const int64_t i = jb->rows ? jb->rows[r] : r;",
-                       "const int64_t i = jb->rows ? jb->rows[r] : (r > 0 ? r - 1 : 0);"),
+    "off_by_one_row": ("const int64_t i = jb->rows ? jb->rows[r] : r;\n    double *crow",
+                       "const int64_t i = jb->rows ? jb->rows[r] : (r > 0 ? r - 1 : 0);\n    double *crow"),
+    # general form
+    "general_transa_ignored": ("jb->transa ? jb->A[k * jb->lda + i] : jb->A[i * jb->lda + k]",
+                               "jb->A[i * jb->lda + k]"),
+    "general_transb_wrong_index": ("jb->transb ? jb->B[j * jb->ldb + k]", "jb->transb ? jb->B[k * jb->ldb + j]"),
+    "general_beta_dropped": ("            v += beta * c;", "            v += 0.0 * c;"),
+    "general_alpha_dropped": ("double v = alpha * out[j];", "double v = out[j];"),
+    "general_alpha_on_c": ("            v += beta * c;", "            v += alpha * beta * c;"),
+    "general_reads_c_when_beta_zero": ("if (jb->beta != 0.0f) { /* beta == 0: C_in is not read */",
+                                       "if (jb->Cin) {"),
+    "general_bound_ignores_c": ("vb += fabs(beta) * fabs(c);", "vb += 0.0;"),
+    "general_rows_ignored": ("const int64_t i = jb->rows ? jb->rows[r] : r;\n    double *out",
+                             "const int64_t i = r;\n    double *out"),
 }
 
 
