@@ -438,6 +438,13 @@ def run_sweep(args):
                 for opt in SWEEP_OPTIONS]
         runs += [({"entry": "sgemm_3xtf32", "variant": v}, lambda v=v: g.sgemm_3xtf32_ex(A, B, C, variant=v))
                  for v in SWEEP_TF32X3_VARIANTS]
+        # The general entry: alpha = 1.5, beta = 0.5 (C read and written) in
+        # each storage order (a transposed operand is copied transposed first).
+        At, Bt = A.t().contiguous(), B.t().contiguous()
+        runs += [({"entry": "sgemm_f32_gemm", "transa": ta, "transb": tb, "alpha": 1.5, "beta": 0.5},
+                  lambda ta=ta, tb=tb: g.sgemm_f32_gemm(At if ta else A, Bt if tb else B, C, alpha=1.5, beta=0.5,
+                                                        transa=ta, transb=tb))
+                 for ta, tb in ((0, 0), (1, 0), (0, 1), (1, 1))]
         # Context only (a library GEMM, on no path of this project): the
         # FP32 GEMM torch runs with TF32 disabled, timed the same way.
         runs += [({"entry": "torch.mm", "tf32": False}, lambda: torch.mm(A, B, out=C))]
@@ -463,7 +470,7 @@ def run_sweep(args):
             except Exception as e:  # an option the shape does not allow
                 rec = {"workload": name, "options": opt, "error": str(e)}
             print(json.dumps(rec), flush=True)
-        del A, B, C
+        del A, B, C, At, Bt
     return 0
 
 

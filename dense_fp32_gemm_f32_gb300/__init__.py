@@ -18,6 +18,7 @@ __all__ = [
     "sgemm_f32",
     "sgemm_f32_ex",
     "sgemm_f32_noalloc",
+    "sgemm_f32_gemm",
     "sgemm_3xtf32",
     "sgemm_3xtf32_ex",
     "sgemm_f32_host",
@@ -85,6 +86,38 @@ def sgemm_f32_noalloc(A: torch.Tensor, B: torch.Tensor, out: torch.Tensor, *, st
     if out is None:
         raise ValueError("sgemm_f32_noalloc needs a preallocated `out`")
     return _call("sgemm_f32_noalloc", A, B, out, stream)
+
+
+def sgemm_f32_gemm(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor | None = None, *, alpha: float = 1.0,
+                   beta: float = 0.0, transa: bool = False, transb: bool = False, stream=None) -> torch.Tensor:
+    """C = alpha * op(A) @ op(B) + beta * C (float32 FFMA kernels).
+
+    ``A`` and ``B`` are the stored operands: A is (M, K), or (K, M) with
+    ``transa`` (op(A) = A.T); B is (K, N), or (N, K) with ``transb``.  ``C``
+    is (M, N); it is required when beta != 0 and not read when beta == 0.
+    """
+    for name, X in (("A", A), ("B", B)):
+        if not isinstance(X, torch.Tensor) or X.dtype != torch.float32 or not X.is_cuda or X.dim() != 2:
+            raise TypeError(f"{name} must be a 2-D CUDA float32 tensor")
+    M, K = (A.shape[1], A.shape[0]) if transa else tuple(A.shape)
+    KB, N = (B.shape[1], B.shape[0]) if transb else tuple(B.shape)
+    if K != KB:
+        raise ValueError(f"shapes do not multiply: op(A) {(M, K)} x op(B) {(KB, N)}")
+    if A.device != B.device:
+        raise ValueError("A and B are on different devices")
+    if C is None:
+        if beta != 0:
+            raise ValueError("beta != 0 needs C")
+        C = torch.empty((M, N), dtype=torch.float32, device=A.device)
+    elif C.dtype != torch.float32 or C.device != A.device or tuple(C.shape) != (M, N):
+        raise ValueError("C must be a float32 (M, N) tensor on A's device")
+    lib = _lib.load()
+    with torch.cuda.device(A.device):
+        rc = lib.sgemm_f32_gemm(int(bool(transa)), int(bool(transb)), M, N, K, float(alpha), A.data_ptr(),
+                                _row_stride(A, "A"), B.data_ptr(), _row_stride(B, "B"), float(beta), C.data_ptr(),
+                                _row_stride(C, "C"), _stream_ptr(stream))
+        _lib.check(rc, "sgemm_f32_gemm")
+    return C
 
 
 def sgemm_3xtf32(A: torch.Tensor, B: torch.Tensor, out: torch.Tensor | None = None, *, stream=None) -> torch.Tensor:

@@ -53,6 +53,7 @@ SIGNATURES = {
     "sgemm_3xtf32": (_i, _GEMM_ARGS),
     "sgemm_f32_ex": (_i, _GEMM_ARGS + [ctypes.POINTER(Options)]),
     "sgemm_3xtf32_ex": (_i, _GEMM_ARGS + [ctypes.POINTER(Options)]),
+    "sgemm_f32_gemm": (_i, [_i, _i, _i, _i, _i, ctypes.c_float, _p, _i, _p, _i, ctypes.c_float, _p, _i, _p]),
     "sgemm_check_status": (_i, [_p]),
     "sgemm_status_string": (ctypes.c_char_p, [_i]),
     "sgemm_describe": (ctypes.c_char_p, [_i, _i, _i, _p, _i, _p, _i, _p, _i]),

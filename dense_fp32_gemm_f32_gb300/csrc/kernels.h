@@ -36,5 +36,14 @@ KernelEntry tf32x3_direct_kernel();
 int pack_rows(const float* src0, long long ld_src0, float* dst0, long long ld_dst0, int rows0, int cols0,
               const float* src1, long long ld_src1, float* dst1, long long ld_dst1, int rows1, int cols1,
               cudaStream_t stream);
+// Transposing copies (a null dst skips one): dst (rows x cols, pitch ld_dst:
+// a multiple of 4, >= cols; 16-byte aligned base) = the transpose of src
+// (cols x rows, pitch ld_src >= rows), zero-filling each row's padding; one
+// launch, enqueued on `stream`.
+int transpose_rows(const float* src0, long long ld_src0, float* dst0, long long ld_dst0, int rows0, int cols0,
+                   const float* src1, long long ld_src1, float* dst1, long long ld_dst1, int rows1, int cols1,
+                   cudaStream_t stream);
+// C = beta * C over M x N with pitch ldc (beta == 0: zeros, C not read).
+int scale_c(float* C, long long ldc, int M, int N, float beta, cudaStream_t stream);
 
 }  // namespace gb300

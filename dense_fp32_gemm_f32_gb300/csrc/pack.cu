@@ -8,6 +8,7 @@
 // product's result is unchanged.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdint>
 
 #include "kernels.h"
@@ -45,6 +46,36 @@ __global__ void __launch_bounds__(kPackThreads) pack_rows_kernel(const PackJob j
     }
 }
 
+// Transposing copy, job blockIdx.z: dst[r][c] = src[c][r] for r < rows,
+// c < cols (dst is rows x cols with pitch ld_dst; src is cols x rows with
+// pitch ld_src); dst's padding columns [cols, ld_dst) are zero-filled.  A
+// 32 x 32 tile passes through shared memory with one padding column, so that
+// both the reads (along src rows) and the writes (along dst rows) are
+// coalesced and the column-wise shared-memory reads hit 32 different banks.
+constexpr int kTile = 32;
+constexpr int kTileRows = 8;
+
+__global__ void __launch_bounds__(kTile* kTileRows) transpose_kernel(const PackJob j0, const PackJob j1) {
+    __shared__ float tile[kTile][kTile + 1];
+    const PackJob& j = blockIdx.z == 0 ? j0 : j1;
+    const long long c0 = static_cast<long long>(blockIdx.x) * kTile;  // dst columns = src rows
+    if (c0 >= j.ld_dst) return;
+    const long long row_tiles = (j.rows + kTile - 1) / kTile;
+    for (long long ty = blockIdx.y; ty < row_tiles; ty += gridDim.y) {
+        const long long r0 = ty * kTile;  // dst rows = src columns
+        for (int y = threadIdx.y; y < kTile; y += kTileRows) {
+            const long long sr = c0 + y, sc = r0 + threadIdx.x;
+            tile[y][threadIdx.x] = (sr < j.cols && sc < j.rows) ? j.src[sr * j.ld_src + sc] : 0.f;
+        }
+        __syncthreads();
+        for (int y = threadIdx.y; y < kTile; y += kTileRows) {
+            const long long dr = r0 + y, dc = c0 + threadIdx.x;
+            if (dr < j.rows && dc < j.ld_dst) j.dst[dr * j.ld_dst + dc] = tile[threadIdx.x][y];
+        }
+        __syncthreads();
+    }
+}
+
 bool job_ok(const PackJob& j) {
     return j.ld_dst >= j.cols && j.ld_dst % 4 == 0 && (reinterpret_cast<uintptr_t>(j.dst) & 15u) == 0;
 }
@@ -75,6 +106,54 @@ int pack_rows(const float* src0, long long ld_src0, float* dst0, long long ld_ds
     if (gx > 0x7fffffffLL) return SGEMM_ERR_INVALID_ARG;
     pack_rows_kernel<<<dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy), static_cast<unsigned>(n)),
                        kPackThreads, 0, stream>>>(use[0], use[1]);
+    if (cudaGetLastError() != cudaSuccess) return SGEMM_ERR_CUDA;
+    return SGEMM_OK;
+}
+
+int transpose_rows(const float* src0, long long ld_src0, float* dst0, long long ld_dst0, int rows0, int cols0,
+                   const float* src1, long long ld_src1, float* dst1, long long ld_dst1, int rows1, int cols1,
+                   cudaStream_t stream) {
+    PackJob j[2] = {{src0, ld_src0, dst0, ld_dst0, rows0, cols0}, {src1, ld_src1, dst1, ld_dst1, rows1, cols1}};
+    int n = 0;
+    PackJob use[2];
+    for (const PackJob& x : j)
+        if (x.dst && x.rows > 0 && x.cols > 0) {
+            if (!job_ok(x) || x.ld_src < x.rows) return SGEMM_ERR_INVALID_ARG;
+            use[n++] = x;
+        }
+    if (n == 0) return SGEMM_OK;
+    if (n == 1) use[1] = use[0];
+    long long gx = 0, gy = 0;
+    for (int i = 0; i < n; ++i) {
+        gx = std::max(gx, (use[i].ld_dst + kTile - 1) / kTile);
+        gy = std::max(gy, std::min<long long>((use[i].rows + kTile - 1) / kTile, 65535));
+    }
+    if (gx > 0x7fffffffLL) return SGEMM_ERR_INVALID_ARG;
+    transpose_kernel<<<dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy), static_cast<unsigned>(n)),
+                       dim3(kTile, kTileRows), 0, stream>>>(use[0], use[1]);
+    if (cudaGetLastError() != cudaSuccess) return SGEMM_ERR_CUDA;
+    return SGEMM_OK;
+}
+
+namespace {
+
+// C = beta * C over M x N (pitch ldc); beta == 0 writes zeros without reading.
+__global__ void __launch_bounds__(256) scale_kernel(float* C, long long ldc, int M, int N, float beta) {
+    const long long c = static_cast<long long>(blockIdx.x) * 256 + threadIdx.x;
+    if (c >= N) return;
+    for (long long r = blockIdx.y; r < M; r += gridDim.y) {
+        float* p = C + r * ldc + c;
+        *p = beta == 0.f ? 0.f : beta * *p;
+    }
+}
+
+}  // namespace
+
+int scale_c(float* C, long long ldc, int M, int N, float beta, cudaStream_t stream) {
+    if (M <= 0 || N <= 0) return SGEMM_OK;
+    const long long gx = (static_cast<long long>(N) + 255) / 256;
+    const int gy = M < 65535 ? M : 65535;
+    scale_kernel<<<dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy)), 256, 0, stream>>>(C, ldc, M, N, beta);
     if (cudaGetLastError() != cudaSuccess) return SGEMM_ERR_CUDA;
     return SGEMM_OK;
 }

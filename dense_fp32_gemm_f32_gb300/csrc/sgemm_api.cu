@@ -228,10 +228,12 @@ struct Repacked {
     cudaStream_t stream = nullptr;
 
     // Copies operand A (mask bit 0) and/or B (bit 1) and points A / lda and
-    // B / ldb at the copies.  SGEMM_ERR_CUDA if the pool cannot serve them
-    // (nothing is enqueued then).
+    // B / ldb at the copies, which are always the plain (untransposed) M x K
+    // and K x N operands: with transa, A is stored K x M and its copy is the
+    // transpose; with transb, likewise B (stored N x K).  SGEMM_ERR_CUDA if
+    // the pool cannot serve them (nothing is enqueued then).
     int make(int dev, DeviceState& st, int mask, int M, int N, int K, const float*& A, int& lda, const float*& B,
-             int& ldb, cudaStream_t cs) {
+             int& ldb, cudaStream_t cs, bool transa = false, bool transb = false) {
         stream = cs;
         const long long K4 = (static_cast<long long>(K) + 3) / 4 * 4;
         const long long N4 = (static_cast<long long>(N) + 3) / 4 * 4;
@@ -246,7 +248,10 @@ struct Repacked {
         }
         float* Ap = (mask & 1) ? static_cast<float*>(ws) : nullptr;
         float* Bp = (mask & 2) ? reinterpret_cast<float*>(static_cast<char*>(ws) + bytes_a) : nullptr;
-        const int rc = pack_rows(A, lda, Ap, K4, M, K, B, ldb, Bp, N4, K, N, cs);
+        // Row copies in one launch, transposing copies in another.
+        int rc = pack_rows(A, lda, transa ? nullptr : Ap, K4, M, K, B, ldb, transb ? nullptr : Bp, N4, K, N, cs);
+        if (rc == SGEMM_OK)
+            rc = transpose_rows(A, lda, transa ? Ap : nullptr, K4, M, K, B, ldb, transb ? Bp : nullptr, N4, K, N, cs);
         if (rc != SGEMM_OK) {
             release();
             return rc;
@@ -522,8 +527,13 @@ const char* describe_plan(const Plan& pl) {
     return buf;
 }
 
+// Epilogue scaling of the general entry: C = alpha * A B + beta * C.
+struct Scale {
+    float alpha = 1.f, beta = 0.f;
+};
+
 int run_ffma(int M, int N, int K, const float* A, int lda, const float* B, int ldb, float* C, int ldc,
-             void* stream, const sgemm_options* opt) {
+             void* stream, const sgemm_options* opt, const Scale* scale = nullptr) {
     int rc = validate(M, N, K, A, lda, B, ldb, C, ldc);
     if (rc != SGEMM_OK) return rc;
     if (opt && opt->debug_skip_stage < 0) return SGEMM_ERR_INVALID_ARG;
@@ -590,6 +600,9 @@ int run_ffma(int M, int N, int K, const float* A, int lda, const float* B, int l
     prm.skip_stage = opt ? opt->debug_skip_stage : 0;
     prm.timeout_ns = (opt && opt->timeout_ns) ? opt->timeout_ns : kDefaultTimeoutNs;
     prm.status = st->status_word;
+    prm.scale = (scale && (scale->alpha != 1.f || scale->beta != 0.f)) ? 1 : 0;
+    prm.alpha = scale ? scale->alpha : 1.f;
+    prm.beta = scale ? scale->beta : 0.f;
     prm.sk = pl.sk;
     prm.sk_dp_tiles = pl.sk_dp_tiles;
     prm.sk_units = (static_cast<long long>(pl.tiles_n) * ceil_div(M, kBM) - pl.sk_dp_tiles) * pl.num_k_tiles;
@@ -833,6 +846,44 @@ int run_3xtf32(int M, int N, int K, const float* A, int lda, const float* B, int
     return rc;
 }
 
+// General form C = alpha * op(A) op(B) + beta * C (see sgemm_f32_gemm).
+int run_gemm(int transa, int transb, int M, int N, int K, float alpha, const float* A, int lda, const float* B,
+             int ldb, float beta, float* C, int ldc, void* stream) {
+    if (transa < 0 || transa > 1 || transb < 0 || transb > 1) return SGEMM_ERR_INVALID_ARG;
+    if (M < 0 || N < 0 || K < 0) return SGEMM_ERR_INVALID_ARG;
+    if (lda < (transa ? M : K) || ldb < (transb ? K : N) || ldc < N) return SGEMM_ERR_INVALID_ARG;
+    const bool product = K > 0 && alpha != 0.f;  // A and B are read
+    if (product && M > 0 && !A) return SGEMM_ERR_INVALID_ARG;
+    if (product && N > 0 && !B) return SGEMM_ERR_INVALID_ARG;
+    if (M > 0 && N > 0 && !C) return SGEMM_ERR_INVALID_ARG;
+    const size_t cb = span_bytes(M, N, ldc);
+    if (product && (ranges_overlap(C, cb, A, transa ? span_bytes(K, M, lda) : span_bytes(M, K, lda)) ||
+                    ranges_overlap(C, cb, B, transb ? span_bytes(N, K, ldb) : span_bytes(K, N, ldb))))
+        return SGEMM_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return SGEMM_OK;
+    int dev = 0;
+    DeviceState* st = nullptr;
+    int rc = current_device(&dev, &st);
+    if (rc != SGEMM_OK) return rc;
+    const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    // No product term (the empty sum, or alpha = 0: A and B are not read).
+    if (!product) return scale_c(C, ldc, M, N, beta, cs);
+    Scale sc;
+    sc.alpha = alpha;
+    sc.beta = beta;
+    if (!transa && !transb) return run_ffma(M, N, K, A, lda, B, ldb, C, ldc, stream, nullptr, &sc);
+    // Transposed storage: one transposing copy into pitched rows per
+    // transposed operand (HBM traffic of one read and one write of it, about
+    // 1 % of the product's time at 4096^3), then the product on the copies.
+    Repacked packed;
+    rc = packed.make(dev, *st, (transa ? 1 : 0) | (transb ? 2 : 0), M, N, K, A, lda, B, ldb, cs, transa != 0,
+                     transb != 0);
+    if (rc != SGEMM_OK) return rc;
+    rc = run_ffma(M, N, K, A, lda, B, ldb, C, ldc, stream, nullptr, &sc);
+    packed.release();
+    return rc;
+}
+
 }  // namespace
 }  // namespace gb300
 
@@ -853,6 +904,11 @@ int sgemm_f32_ex(int M, int N, int K, const float* A, int lda, const float* B, i
 int sgemm_f32_noalloc(int M, int N, int K, const float* A, int lda, const float* B, int ldb, float* C, int ldc,
                       void* stream) {
     return run_ffma_noalloc(M, N, K, A, lda, B, ldb, C, ldc, stream);
+}
+
+int sgemm_f32_gemm(int transa, int transb, int M, int N, int K, float alpha, const float* A, int lda, const float* B,
+                   int ldb, float beta, float* C, int ldc, void* stream) {
+    return run_gemm(transa, transb, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream);
 }
 
 int sgemm_3xtf32(int M, int N, int K, const float* A, int lda, const float* B, int ldb, float* C, int ldc,

@@ -130,6 +130,10 @@ struct FfmaParams {
     int skip_stage;        // debug: CTA (0,0,0)'s producer never issues K-slice skip_stage-1
     unsigned long long timeout_ns;
     unsigned int* status;  // per-device sticky status word (error bits)
+    // Epilogue C = alpha * (A B) + beta * C when `scale` is set (C is read
+    // only when beta != 0); scale == 0 stores A B as it is.
+    int scale;
+    float alpha, beta;
 };
 
 template <int STAGES, int BN = kBN>
@@ -391,9 +395,30 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), 1)
 #pragma unroll
             for (int h = 0; h < H; ++h) {
                 const int c = col0 + 32 * h;
-                const float4 v =
-                    make_float4(acc[i][2 * h].x, acc[i][2 * h].y, acc[i][2 * h + 1].x, acc[i][2 * h + 1].y);
-                if (p.vec_store && c + 3 < p.N) {
+                float4 v = make_float4(acc[i][2 * h].x, acc[i][2 * h].y, acc[i][2 * h + 1].x, acc[i][2 * h + 1].y);
+                const bool vec = p.vec_store && c + 3 < p.N;
+                if (p.scale) {
+                    v.x *= p.alpha;
+                    v.y *= p.alpha;
+                    v.z *= p.alpha;
+                    v.w *= p.alpha;
+                    if (p.beta != 0.f) {
+                        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+                        if (vec) {
+                            o = *reinterpret_cast<const float4*>(crow + c);
+                        } else {
+                            if (c < p.N) o.x = crow[c];
+                            if (c + 1 < p.N) o.y = crow[c + 1];
+                            if (c + 2 < p.N) o.z = crow[c + 2];
+                            if (c + 3 < p.N) o.w = crow[c + 3];
+                        }
+                        v.x = fmaf(p.beta, o.x, v.x);
+                        v.y = fmaf(p.beta, o.y, v.y);
+                        v.z = fmaf(p.beta, o.z, v.z);
+                        v.w = fmaf(p.beta, o.w, v.w);
+                    }
+                }
+                if (vec) {
                     *reinterpret_cast<float4*>(crow + c) = v;
                 } else {
                     if (c < p.N) crow[c] = v.x;

@@ -71,17 +71,23 @@ typedef enum sgemm_status {
  * sgemm_f32 -- C = A x B in float32 on the CUDA cores (FFMA).
  *
  * The main entry.  Picks the kernel variant itself: TMA-fed when A, B have
- * 16-byte aligned bases and row strides, a cp.async-fed variant otherwise;
- * cluster split-K when the output has too few tiles to fill the GPU.
- * (Two-CTA multicast of A and a K-split second launch for the tiles of the
- * last partial wave are available through sgemm_f32_ex; measured on GB300
- * neither pays, so neither is chosen automatically.)
+ * 16-byte aligned bases and row strides; otherwise the misaligned operands
+ * are first copied into 16-byte pitched rows (2MNK >= 2^30) or read by a
+ * cp.async-fed variant (smaller products).  The schedule is stream-K (one CTA
+ * per SM, the work after the last full wave dealt out as K slices) when there
+ * are at least two (tile, K slice) units per SM, cluster split-K for smaller
+ * outputs.  (Two-CTA multicast of A, 128 x 256 tiles and a K-split second
+ * launch for the last partial wave are available through sgemm_f32_ex;
+ * measured on GB300 none pays, so none is chosen automatically.)
  *   M, N, K      problem sizes (>= 0)
  *   A, lda       device pointer to A, row stride in floats (lda >= K)
  *   B, ldb       device pointer to B, row stride in floats (ldb >= N)
  *   C, ldc       device pointer to C, row stride in floats (ldc >= N)
  *   stream       cudaStream_t as void*
- * One call enqueues one kernel launch.
+ * A call enqueues the product kernel, preceded by a 4-byte-per-SM
+ * cudaMemsetAsync of the stream-K ready flags and, when repacking, by one
+ * copy kernel; its workspaces come from a pool the library keeps per device
+ * (see sgemm_options.stream_k and .repack).
  */
 int sgemm_f32(int M, int N, int K,
               const float* A, int lda,
@@ -128,6 +134,38 @@ int sgemm_f32_noalloc(int M, int N, int K,
                       const float* B, int ldb,
                       float* C, int ldc,
                       void* stream);
+
+/*
+ * sgemm_f32_gemm -- the general form
+ *
+ *     C = alpha * op(A) op(B) + beta * C      (float32, row-major storage)
+ *
+ * of the standard GEMM interface (the pages define only the plain product;
+ * their optimisation-summary page mentions other storage orders in passing).
+ *   transa       0: op(A) = A, stored M x K (lda >= K);
+ *                1: op(A) = A^T, A stored K x M (lda >= M)
+ *   transb       0: op(B) = B, stored K x N (ldb >= N);
+ *                1: op(B) = B^T, B stored N x K (ldb >= K)
+ *   alpha, beta  scalars; C is not read when beta == 0 (it may hold NaN or
+ *                garbage), and A and B are not read when alpha == 0 or K == 0
+ *                (C = beta * C then)
+ *   C, ldc       M x N, ldc >= N; must not overlap A or B
+ * Same kernels and accuracy contract as sgemm_f32, with the bound
+ * |alpha| sum_k |op(A)_ik||op(B)_kj| + |beta||C_ij| per element (exact on
+ * integer-valued inputs and integer alpha, beta while every value stays below
+ * 2^24).  The epilogue computes fma(beta, C, alpha * (op(A) op(B))).  A
+ * transposed operand is first copied, transposed, into pitched rows from the
+ * library's pool (one extra read and write of that operand).  Errors as
+ * sgemm_f32.
+ */
+int sgemm_f32_gemm(int transa, int transb,
+                   int M, int N, int K,
+                   float alpha,
+                   const float* A, int lda,
+                   const float* B, int ldb,
+                   float beta,
+                   float* C, int ldc,
+                   void* stream);
 
 /*
  * sgemm_3xtf32 -- same operation, signature, accuracy contract and error
