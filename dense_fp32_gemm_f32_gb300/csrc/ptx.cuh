@@ -110,6 +110,11 @@ __device__ __forceinline__ void tma_load_2d_multicast(uint32_t dst, const void* 
         : "memory");
 }
 
+// Prefetch of the global line holding `p` into L2.
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(p)));
+}
+
 // ---------------------------------------------------------------- cp.async
 
 // 4-byte asynchronous copy; `src_bytes` = 0 writes a zero instead of reading.

@@ -384,47 +384,95 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), 1)
     // [4 floats]; element group e4 = i*H + h holds acc[i][2h] and
     // acc[i][2h+1] (four columns).  Consecutive threads touch consecutive 16-byte words, so
     // every partial store and load is conflict-free and coalesced.
-    auto store_c = [&](int tile) {
+    // C (beta != 0 only): the thread's 8 x H four-column segments of the
+    // tile, prefetched into L2 when the CTA starts the segment it will store,
+    // so that the epilogue's reads of the old C do not wait on HBM.
+    const bool read_c = p.scale && p.beta != 0.f;
+    auto prefetch_c = [&](int tile) {
         const int row0 = (tile / p.tiles_n) * kBM + wm * 32 + tm;
         const int col0 = (tile % p.tiles_n) * BN + wn * (BN / 2) + tn * 4;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const int r = row0 + 4 * i;
-            if (r >= p.M) continue;
-            float* crow = p.C + static_cast<long long>(r) * p.ldc;
 #pragma unroll
-            for (int h = 0; h < H; ++h) {
-                const int c = col0 + 32 * h;
-                float4 v = make_float4(acc[i][2 * h].x, acc[i][2 * h].y, acc[i][2 * h + 1].x, acc[i][2 * h + 1].y);
-                const bool vec = p.vec_store && c + 3 < p.N;
-                if (p.scale) {
-                    v.x *= p.alpha;
-                    v.y *= p.alpha;
-                    v.z *= p.alpha;
-                    v.w *= p.alpha;
-                    if (p.beta != 0.f) {
-                        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-                        if (vec) {
-                            o = *reinterpret_cast<const float4*>(crow + c);
-                        } else {
-                            if (c < p.N) o.x = crow[c];
-                            if (c + 1 < p.N) o.y = crow[c + 1];
-                            if (c + 2 < p.N) o.z = crow[c + 2];
-                            if (c + 3 < p.N) o.w = crow[c + 3];
-                        }
-                        v.x = fmaf(p.beta, o.x, v.x);
-                        v.y = fmaf(p.beta, o.y, v.y);
-                        v.z = fmaf(p.beta, o.z, v.z);
-                        v.w = fmaf(p.beta, o.w, v.w);
+            for (int h = 0; h < H; ++h)
+                if (r < p.M && col0 + 32 * h < p.N)
+                    prefetch_l2(p.C + static_cast<long long>(r) * p.ldc + col0 + 32 * h);
+        }
+    };
+    auto store_c = [&](int tile) {
+        const int row0 = (tile / p.tiles_n) * kBM + wm * 32 + tm;
+        const int col0 = (tile % p.tiles_n) * BN + wn * (BN / 2) + tn * 4;
+        // Rows in groups of RG: with beta != 0 the group's old C values are
+        // all loaded before any of its stores, so the loads are in flight
+        // together (a load after a store to C could not be moved above it).
+        // The 256-wide tile, short of registers, takes one row at a time.
+        constexpr int RG = H == 2 ? 2 : 1;
+#pragma unroll
+        for (int i0 = 0; i0 < 8; i0 += RG) {
+            float4 o[RG][H];
+#pragma unroll
+            for (int ii = 0; ii < RG; ++ii) {
+                const int r = row0 + 4 * (i0 + ii);
+                const float* crow = p.C + static_cast<long long>(r) * p.ldc;
+#pragma unroll
+                for (int h = 0; h < H; ++h) {
+                    const int c = col0 + 32 * h;
+                    o[ii][h] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (!read_c || r >= p.M || RG == 1) continue;
+                    if (p.vec_store && c + 3 < p.N) {
+                        o[ii][h] = *reinterpret_cast<const float4*>(crow + c);
+                    } else {
+                        if (c < p.N) o[ii][h].x = crow[c];
+                        if (c + 1 < p.N) o[ii][h].y = crow[c + 1];
+                        if (c + 2 < p.N) o[ii][h].z = crow[c + 2];
+                        if (c + 3 < p.N) o[ii][h].w = crow[c + 3];
                     }
                 }
-                if (vec) {
-                    *reinterpret_cast<float4*>(crow + c) = v;
-                } else {
-                    if (c < p.N) crow[c] = v.x;
-                    if (c + 1 < p.N) crow[c + 1] = v.y;
-                    if (c + 2 < p.N) crow[c + 2] = v.z;
-                    if (c + 3 < p.N) crow[c + 3] = v.w;
+            }
+#pragma unroll
+            for (int ii = 0; ii < RG; ++ii) {
+                const int i = i0 + ii;
+                const int r = row0 + 4 * i;
+                if (r >= p.M) continue;
+                float* crow = p.C + static_cast<long long>(r) * p.ldc;
+#pragma unroll
+                for (int h = 0; h < H; ++h) {
+                    const int c = col0 + 32 * h;
+                    const bool vec = p.vec_store && c + 3 < p.N;
+                    float4 v =
+                        make_float4(acc[i][2 * h].x, acc[i][2 * h].y, acc[i][2 * h + 1].x, acc[i][2 * h + 1].y);
+                    if (p.scale) {
+                        v.x *= p.alpha;
+                        v.y *= p.alpha;
+                        v.z *= p.alpha;
+                        v.w *= p.alpha;
+                        if (read_c) {
+                            float4 q = o[ii][h];
+                            if (RG == 1) {  // loaded here, just before its store
+                                if (vec) {
+                                    q = *reinterpret_cast<const float4*>(crow + c);
+                                } else {
+                                    if (c < p.N) q.x = crow[c];
+                                    if (c + 1 < p.N) q.y = crow[c + 1];
+                                    if (c + 2 < p.N) q.z = crow[c + 2];
+                                    if (c + 3 < p.N) q.w = crow[c + 3];
+                                }
+                            }
+                            v.x = fmaf(p.beta, q.x, v.x);
+                            v.y = fmaf(p.beta, q.y, v.y);
+                            v.z = fmaf(p.beta, q.z, v.z);
+                            v.w = fmaf(p.beta, q.w, v.w);
+                        }
+                    }
+                    if (vec) {
+                        *reinterpret_cast<float4*>(crow + c) = v;
+                    } else {
+                        if (c < p.N) crow[c] = v.x;
+                        if (c + 1 < p.N) crow[c + 1] = v.y;
+                        if (c + 2 < p.N) crow[c + 2] = v.z;
+                        if (c + 3 < p.N) crow[c + 3] = v.w;
+                    }
                 }
             }
         }
@@ -447,6 +495,7 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), 1)
             for (int i = 0; i < 8; ++i)
 #pragma unroll
                 for (int q = 0; q < TQ; ++q) acc[i][q] = make_float2(0.f, 0.f);
+            if (read_c && kb == 0 && (split <= 1 || crank == 0)) prefetch_c(tile);  // this CTA stores it
 
             for (int kt = kb; kt < ke; ++kt, ++it) {
                 const int s = it % STAGES;
