@@ -141,6 +141,9 @@ int init_device(int dev, DeviceState& st) {
         }
         for (int s = 1; s <= 6; ++s)
             if (set_smem_attr(ffma_kernel_cpasync(s, math)) != SGEMM_OK) return SGEMM_ERR_CUDA;
+        for (int s = 1; s <= 6; ++s)
+            for (int prod : {static_cast<int>(kProducerTma), static_cast<int>(kProducerCpAsync)})
+                if (set_smem_attr(ffma_kernel_scaled(prod, s, math)) != SGEMM_OK) return SGEMM_ERR_CUDA;
     }
     if (set_smem_attr(tf32x3_kernel()) != SGEMM_OK || set_smem_attr(tf32x3_direct_kernel()) != SGEMM_OK)
         return SGEMM_ERR_CUDA;
@@ -564,7 +567,10 @@ int run_ffma(int M, int N, int K, const float* A, int lda, const float* B, int l
     // Returns the repack buffers to the pool behind everything enqueued so far.
     auto release_pack = [&] { packed.release(); };
 
-    const KernelEntry k = ffma_kernel(pl);
+    const bool scaled = scale && (scale->alpha != 1.f || scale->beta != 0.f);
+    const KernelEntry k = scaled ? (pl.bn == kBN ? ffma_kernel_scaled(pl.producer, pl.stages, pl.math)
+                                                 : KernelEntry{nullptr, 0, 0})
+                                 : ffma_kernel(pl);
     if (!k.fn) {
         release_pack();
         return SGEMM_ERR_INVALID_ARG;
@@ -600,7 +606,6 @@ int run_ffma(int M, int N, int K, const float* A, int lda, const float* B, int l
     prm.skip_stage = opt ? opt->debug_skip_stage : 0;
     prm.timeout_ns = (opt && opt->timeout_ns) ? opt->timeout_ns : kDefaultTimeoutNs;
     prm.status = st->status_word;
-    prm.scale = (scale && (scale->alpha != 1.f || scale->beta != 0.f)) ? 1 : 0;
     prm.alpha = scale ? scale->alpha : 1.f;
     prm.beta = scale ? scale->beta : 0.f;
     prm.sk = pl.sk;

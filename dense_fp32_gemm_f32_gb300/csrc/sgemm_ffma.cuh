@@ -130,9 +130,8 @@ struct FfmaParams {
     int skip_stage;        // debug: CTA (0,0,0)'s producer never issues K-slice skip_stage-1
     unsigned long long timeout_ns;
     unsigned int* status;  // per-device sticky status word (error bits)
-    // Epilogue C = alpha * (A B) + beta * C when `scale` is set (C is read
-    // only when beta != 0); scale == 0 stores A B as it is.
-    int scale;
+    // Epilogue of the SCALED kernels: C = alpha * (A B) + beta * C (C is read
+    // only when beta != 0).
     float alpha, beta;
 };
 
@@ -149,7 +148,10 @@ __device__ __forceinline__ uint32_t swz128(int r, int c) {
     return static_cast<uint32_t>(r * 128 + ((((c >> 2) ^ r) & 7) << 4) + (c & 3) * 4);
 }
 
-template <int STAGES, int PRODUCER, int MATH, int BN = kBN>
+// SCALED: the epilogue applies C = alpha * (A B) + beta * C (FfmaParams
+// alpha, beta); a separate instantiation, so that the plain kernels' code is
+// not touched by it.
+template <int STAGES, int PRODUCER, int MATH, int BN = kBN, bool SCALED = false>
 __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), 1)
     sgemm_ffma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                       const FfmaParams p) {
@@ -387,7 +389,7 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), 1)
     // C (beta != 0 only): the thread's 8 x H four-column segments of the
     // tile, prefetched into L2 when the CTA starts the segment it will store,
     // so that the epilogue's reads of the old C do not wait on HBM.
-    const bool read_c = p.scale && p.beta != 0.f;
+    const bool read_c = SCALED && p.beta != 0.f;
     auto prefetch_c = [&](int tile) {
         const int row0 = (tile / p.tiles_n) * kBM + wm * 32 + tm;
         const int col0 = (tile % p.tiles_n) * BN + wn * (BN / 2) + tn * 4;
@@ -400,7 +402,31 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), 1)
                     prefetch_l2(p.C + static_cast<long long>(r) * p.ldc + col0 + 32 * h);
         }
     };
-    auto store_c = [&](int tile) {
+    auto store_c_plain = [&](int tile) {
+        const int row0 = (tile / p.tiles_n) * kBM + wm * 32 + tm;
+        const int col0 = (tile % p.tiles_n) * BN + wn * (BN / 2) + tn * 4;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int r = row0 + 4 * i;
+            if (r >= p.M) continue;
+            float* crow = p.C + static_cast<long long>(r) * p.ldc;
+#pragma unroll
+            for (int h = 0; h < H; ++h) {
+                const int c = col0 + 32 * h;
+                const float4 v =
+                    make_float4(acc[i][2 * h].x, acc[i][2 * h].y, acc[i][2 * h + 1].x, acc[i][2 * h + 1].y);
+                if (p.vec_store && c + 3 < p.N) {
+                    *reinterpret_cast<float4*>(crow + c) = v;
+                } else {
+                    if (c < p.N) crow[c] = v.x;
+                    if (c + 1 < p.N) crow[c + 1] = v.y;
+                    if (c + 2 < p.N) crow[c + 2] = v.z;
+                    if (c + 3 < p.N) crow[c + 3] = v.w;
+                }
+            }
+        }
+    };
+    auto store_c_scaled = [&](int tile) {
         const int row0 = (tile / p.tiles_n) * kBM + wm * 32 + tm;
         const int col0 = (tile % p.tiles_n) * BN + wn * (BN / 2) + tn * 4;
         // Rows in groups of RG: with beta != 0 the group's old C values are
@@ -442,7 +468,7 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), 1)
                     const bool vec = p.vec_store && c + 3 < p.N;
                     float4 v =
                         make_float4(acc[i][2 * h].x, acc[i][2 * h].y, acc[i][2 * h + 1].x, acc[i][2 * h + 1].y);
-                    if (p.scale) {
+                    {
                         v.x *= p.alpha;
                         v.y *= p.alpha;
                         v.z *= p.alpha;
@@ -477,6 +503,13 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), 1)
             }
         }
     };
+    auto store_c = [&](int tile) {
+        if constexpr (SCALED) {
+            store_c_scaled(tile);
+        } else {
+            store_c_plain(tile);
+        }
+    };
     auto consumer_sync = [] { asm volatile("bar.sync 1, %0;" ::"n"(kConsumerThreads) : "memory"); };
 
     {
@@ -495,7 +528,8 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), 1)
             for (int i = 0; i < 8; ++i)
 #pragma unroll
                 for (int q = 0; q < TQ; ++q) acc[i][q] = make_float2(0.f, 0.f);
-            if (read_c && kb == 0 && (split <= 1 || crank == 0)) prefetch_c(tile);  // this CTA stores it
+            if (SCALED && read_c && kb == 0 && (split <= 1 || crank == 0))
+                prefetch_c(tile);  // this CTA stores the tile
 
             for (int kt = kb; kt < ke; ++kt, ++it) {
                 const int s = it % STAGES;
