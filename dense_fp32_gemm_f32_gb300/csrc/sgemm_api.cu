@@ -51,6 +51,9 @@ struct DeviceState {
     std::once_flag noalloc_once;
     int noalloc_status = SGEMM_ERR_CUDA;  // result of looking up g_noalloc_scratch
     float* noalloc_scratch = nullptr;     // its device address on this device
+    std::once_flag copy_once;
+    cudaStream_t copy_in = nullptr;   // host-buffer entry: host -> device copies
+    cudaStream_t copy_out = nullptr;  // host-buffer entry: device -> host copies
 };
 
 DeviceState g_dev[kMaxDevices];
@@ -889,6 +892,105 @@ int run_gemm(int transa, int transb, int M, int N, int K, float alpha, const flo
     return rc;
 }
 
+// Rows [r0, r0 + rows) of a rows x cols float matrix, pitch ld_src -> pitch
+// ld_dst, as one (2-D when pitched) asynchronous copy.
+cudaError_t copy_rows(float* dst, long long ld_dst, const float* src, long long ld_src, long long rows,
+                      long long cols, cudaMemcpyKind kind, cudaStream_t s) {
+    if (rows <= 0 || cols <= 0) return cudaSuccess;
+    if (ld_dst == cols && ld_src == cols)
+        return cudaMemcpyAsync(dst, src, static_cast<size_t>(rows * cols) * 4, kind, s);
+    return cudaMemcpy2DAsync(dst, static_cast<size_t>(ld_dst) * 4, src, static_cast<size_t>(ld_src) * 4,
+                             static_cast<size_t>(cols) * 4, static_cast<size_t>(rows), kind, s);
+}
+
+// Host-buffer form (see sgemm_f32_host): device copies of A, B, C from the
+// pool; B goes over first, then A and C move in row blocks so that block i's
+// product overlaps block i+1's copy in and block i-1's copy out.
+int run_host(int M, int N, int K, const float* A, int lda, const float* B, int ldb, float* C, int ldc,
+             void* stream) {
+    int rc = validate(M, N, K, A, lda, B, ldb, C, ldc);
+    if (rc != SGEMM_OK) return rc;
+    if (M == 0 || N == 0) return SGEMM_OK;
+    int dev = 0;
+    DeviceState* st = nullptr;
+    rc = current_device(&dev, &st);
+    if (rc != SGEMM_OK) return rc;
+    std::call_once(st->copy_once, [&] {
+        if (cudaStreamCreateWithFlags(&st->copy_in, cudaStreamNonBlocking) != cudaSuccess ||
+            cudaStreamCreateWithFlags(&st->copy_out, cudaStreamNonBlocking) != cudaSuccess) {
+            (void)cudaGetLastError();
+            st->copy_in = st->copy_out = nullptr;
+        }
+    });
+    if (!st->copy_in || !st->copy_out) return SGEMM_ERR_CUDA;
+    const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    cudaMemPool_t pool = workspace_pool(dev, *st);
+    if (!pool) return SGEMM_ERR_CUDA;
+
+    // Row blocks: a multiple of 128 rows, at most 8 blocks, none for small
+    // products (the copies then simply run before and after the product).
+    const long long flops2 = 2LL * M * N;
+    const int nblk = (static_cast<double>(flops2) * K < 4294967296.0) ? 1
+                                                                      : static_cast<int>(std::min<long long>(
+                                                                            8, (static_cast<long long>(M) + 511) / 512));
+    const long long rows_blk = ((static_cast<long long>(M) + nblk - 1) / nblk + kBM - 1) / kBM * kBM;
+
+    const size_t bytes_a = (static_cast<size_t>(M) * K * 4 + 255) & ~size_t{255};
+    const size_t bytes_b = (static_cast<size_t>(K) * N * 4 + 255) & ~size_t{255};
+    const size_t bytes_c = static_cast<size_t>(M) * N * 4;
+    void* ws = nullptr;
+    if (cudaMallocFromPoolAsync(&ws, bytes_a + bytes_b + bytes_c, pool, cs) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return SGEMM_ERR_CUDA;
+    }
+    float* dA = static_cast<float*>(ws);
+    float* dB = reinterpret_cast<float*>(static_cast<char*>(ws) + bytes_a);
+    float* dC = reinterpret_cast<float*>(static_cast<char*>(ws) + bytes_a + bytes_b);
+
+    constexpr int kMaxBlk = 8;
+    cudaEvent_t ev_start = nullptr, ev_in[kMaxBlk] = {}, ev_done[kMaxBlk] = {}, ev_out = nullptr;
+    auto make_event = [](cudaEvent_t* e) {
+        return cudaEventCreateWithFlags(e, cudaEventDisableTiming) == cudaSuccess;
+    };
+    bool ok = make_event(&ev_start) && make_event(&ev_out);
+    for (int i = 0; i < nblk && ok; ++i) ok = make_event(&ev_in[i]) && make_event(&ev_done[i]);
+    // The copy streams start after the workspace exists (stream order of cs).
+    ok = ok && cudaEventRecord(ev_start, cs) == cudaSuccess &&
+         cudaStreamWaitEvent(st->copy_in, ev_start, 0) == cudaSuccess &&
+         cudaStreamWaitEvent(st->copy_out, ev_start, 0) == cudaSuccess;
+    ok = ok && copy_rows(dB, N, B, ldb, K, N, cudaMemcpyHostToDevice, st->copy_in) == cudaSuccess;
+    for (int i = 0; i < nblk && ok && rc == SGEMM_OK; ++i) {
+        const long long r0 = i * rows_blk;
+        const long long rows = std::min<long long>(rows_blk, M - r0);
+        if (rows <= 0) break;
+        ok = copy_rows(dA + r0 * K, K, A + r0 * lda, lda, rows, K, cudaMemcpyHostToDevice, st->copy_in) ==
+                 cudaSuccess &&
+             cudaEventRecord(ev_in[i], st->copy_in) == cudaSuccess && cudaStreamWaitEvent(cs, ev_in[i], 0) == cudaSuccess;
+        if (!ok) break;
+        rc = run_ffma(static_cast<int>(rows), N, K, dA + r0 * K, K, dB, N, dC + r0 * N, N, stream, nullptr);
+        if (rc != SGEMM_OK) break;
+        ok = cudaEventRecord(ev_done[i], cs) == cudaSuccess &&
+             cudaStreamWaitEvent(st->copy_out, ev_done[i], 0) == cudaSuccess &&
+             copy_rows(C + r0 * ldc, ldc, dC + r0 * N, N, rows, N, cudaMemcpyDeviceToHost, st->copy_out) ==
+                 cudaSuccess;
+    }
+    // cs resumes (and the workspace returns to the pool) after the last copy
+    // out; also after a failure, so that nothing in flight uses freed memory.
+    const bool joined = cudaEventRecord(ev_out, st->copy_out) == cudaSuccess &&
+                        cudaStreamWaitEvent(cs, ev_out, 0) == cudaSuccess;
+    if (!ok || !joined) (void)cudaGetLastError();
+    if (!joined) (void)cudaStreamSynchronize(st->copy_out);
+    (void)cudaFreeAsync(ws, cs);
+    for (cudaEvent_t e : {ev_start, ev_out})
+        if (e) (void)cudaEventDestroy(e);
+    for (int i = 0; i < kMaxBlk; ++i) {
+        if (ev_in[i]) (void)cudaEventDestroy(ev_in[i]);
+        if (ev_done[i]) (void)cudaEventDestroy(ev_done[i]);
+    }
+    if (rc != SGEMM_OK) return rc;
+    return ok ? SGEMM_OK : SGEMM_ERR_CUDA;
+}
+
 }  // namespace
 }  // namespace gb300
 
@@ -909,6 +1011,11 @@ int sgemm_f32_ex(int M, int N, int K, const float* A, int lda, const float* B, i
 int sgemm_f32_noalloc(int M, int N, int K, const float* A, int lda, const float* B, int ldb, float* C, int ldc,
                       void* stream) {
     return run_ffma_noalloc(M, N, K, A, lda, B, ldb, C, ldc, stream);
+}
+
+int sgemm_f32_host(int M, int N, int K, const float* A, int lda, const float* B, int ldb, float* C, int ldc,
+                   void* stream) {
+    return run_host(M, N, K, A, lda, B, ldb, C, ldc, stream);
 }
 
 int sgemm_f32_gemm(int transa, int transb, int M, int N, int K, float alpha, const float* A, int lda, const float* B,
