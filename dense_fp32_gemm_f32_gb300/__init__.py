@@ -142,24 +142,28 @@ def sgemm_3xtf32_ex(A, B, out=None, *, stream=None, variant=0, debug_skip_stage=
 
 def sgemm_f32_host(A: torch.Tensor, B: torch.Tensor, out: torch.Tensor | None = None, *,
                    device: int | torch.device = 0, stream=None) -> torch.Tensor:
-    """Host-buffer form: copies A and B (CPU float32, ideally pinned) to the
-    device, runs sgemm_f32, copies C back into ``out`` (CPU) and returns it
-    once the copy has finished."""
+    """Host-buffer form (the C entry sgemm_f32_host): A, B and ``out`` are CPU
+    float32 tensors (pinned memory lets the copies overlap the product); the
+    library copies them to and from ``device`` itself.  Returns ``out`` once
+    the result is in it."""
     dev = torch.device("cuda", device) if isinstance(device, int) else torch.device(device)
     for name, X in (("A", A), ("B", B)):
-        if X.dtype != torch.float32 or X.is_cuda or X.dim() != 2:
+        if not isinstance(X, torch.Tensor) or X.dtype != torch.float32 or X.is_cuda or X.dim() != 2:
             raise TypeError(f"{name} must be a 2-D CPU float32 tensor")
-    M, N = A.shape[0], B.shape[1]
+    if A.shape[1] != B.shape[0]:
+        raise ValueError(f"shapes do not multiply: {tuple(A.shape)} x {tuple(B.shape)}")
+    M, K = A.shape
+    N = B.shape[1]
     if out is None:
         out = torch.empty((M, N), dtype=torch.float32, pin_memory=True)
+    elif out.dtype != torch.float32 or out.is_cuda or tuple(out.shape) != (M, N):
+        raise ValueError("out must be a CPU float32 (M, N) tensor")
+    lib = _lib.load()
     with torch.cuda.device(dev):
         s = stream if stream is not None else torch.cuda.current_stream(dev)
-        with torch.cuda.stream(s):
-            dA = A.to(dev, non_blocking=True)
-            dB = B.to(dev, non_blocking=True)
-            dC = torch.empty((M, N), dtype=torch.float32, device=dev)
-            sgemm_f32(dA, dB, dC, stream=s)
-            out.copy_(dC, non_blocking=True)
+        rc = lib.sgemm_f32_host(M, N, K, A.data_ptr(), _row_stride(A, "A"), B.data_ptr(), _row_stride(B, "B"),
+                                out.data_ptr(), _row_stride(out, "out"), _stream_ptr(s))
+        _lib.check(rc, "sgemm_f32_host")
         s.synchronize()
     return out
 

@@ -50,6 +50,7 @@ _GEMM_ARGS = [_i, _i, _i, _p, _i, _p, _i, _p, _i, _p]
 SIGNATURES = {
     "sgemm_f32": (_i, _GEMM_ARGS),
     "sgemm_f32_noalloc": (_i, _GEMM_ARGS),
+    "sgemm_f32_host": (_i, _GEMM_ARGS),
     "sgemm_3xtf32": (_i, _GEMM_ARGS),
     "sgemm_f32_ex": (_i, _GEMM_ARGS + [ctypes.POINTER(Options)]),
     "sgemm_3xtf32_ex": (_i, _GEMM_ARGS + [ctypes.POINTER(Options)]),

@@ -136,6 +136,28 @@ int sgemm_f32_noalloc(int M, int N, int K,
                       void* stream);
 
 /*
+ * sgemm_f32_host -- sgemm_f32 on HOST buffers: A, B and C are host pointers
+ * (page-locked memory, e.g. from cudaHostAlloc, lets the copies run
+ * asynchronously and overlap the product; pageable memory works but
+ * serialises).  Same operation, layout rules, accuracy contract and errors as
+ * sgemm_f32.
+ *
+ * The call takes device copies of A, B and C from the library's pool, copies
+ * B to the device, then A and C in up to eight row blocks of whole 128-row
+ * tiles on two library-owned copy streams, so that the product of block i
+ * (on `stream`) overlaps the copy in of block i+1 and the copy out of block
+ * i-1; products below 2^32 flop run as one block.  It returns once all of
+ * that is enqueued: C holds the result after `stream` is synchronised (all
+ * copies are ordered before `stream`'s later work).  The host buffers must
+ * stay valid and unmodified until then.
+ */
+int sgemm_f32_host(int M, int N, int K,
+                   const float* A, int lda,
+                   const float* B, int ldb,
+                   float* C, int ldc,
+                   void* stream);
+
+/*
  * sgemm_f32_gemm -- the general form
  *
  *     C = alpha * op(A) op(B) + beta * C      (float32, row-major storage)

@@ -294,6 +294,29 @@ def test_host_buffer_entry():
     check(C.numpy(), C64, bound, exact=False, what="host buffers")
 
 
+@pytest.mark.parametrize("dist", ["uniform", "int"])
+def test_host_buffer_entry_row_blocks(dist):
+    """2048 x 1536 x 2048 (2^34 flop): four row blocks whose copies overlap
+    the products; every element against the oracle."""
+    A, B = make_operands(2048, 1536, 2048, dist, 14)
+    C = g.sgemm_f32_host(A.pin_memory(), B.pin_memory())
+    C64, bound = oracle.gemm_f64(A.numpy(), B.numpy(), with_bound=(dist != "int"))
+    check(C.numpy(), C64, bound, exact=(dist == "int"), what=f"host row blocks {dist}")
+
+
+def test_host_buffer_entry_pitched_and_pageable():
+    """Padded host rows (odd pitches) and pageable (not pinned) memory on the
+    row-block path; the padding of C is left untouched."""
+    M, N, K = 1300, 700, 2400
+    A, B = make_operands(M, N, K, "uniform", 15, lda=K + 3, ldb=N + 1)
+    store = torch.full((M, N + 5), -7.0)
+    out = store[:, :N]
+    C = g.sgemm_f32_host(A, B, out)
+    C64, bound = oracle.gemm_f64(A.numpy(), B.numpy())
+    check(C.numpy(), C64, bound, exact=False, what="host pitched")
+    assert torch.all(store[:, N:] == -7.0)
+
+
 def test_variant_choice():
     def desc(M, N, K):
         return g.describe(torch.empty((M, K), device="cuda"), torch.empty((K, N), device="cuda"))
