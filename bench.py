@@ -408,6 +408,10 @@ SWEEP_OPTIONS = [
     {"tile_n": 256, "stages": 2},
     {"tile_n": 256, "stages": 3},
     {"tile_n": 256, "split_k": 1},
+    {"tile_n": 64},
+    {"tile_n": 64, "stages": 3},
+    {"tile_n": 64, "stages": 2},
+    {"tile_n": 64, "split_k": 1},
     {"repack": 1},
     {"split_k": 1},
     {"split_k": 2},

@@ -20,6 +20,9 @@ KernelEntry ffma_kernel_tma_wg(int stages, int math);
 // 128 x 256 tiles (8 x 16 accumulators per thread) with the producer
 // warpgroup and the register split; stages in {2,3,4}.
 KernelEntry ffma_kernel_tma_wide(int stages, int math);
+// Fused-producer FFMA kernels: 4-warp CTAs (no producer warp; thread 0
+// issues the TMA copies), 128 x 64 tiles, two CTAs per SM; stages in {2,3,4}.
+KernelEntry ffma_kernel_tma_fused(int stages, int math);
 // The scaled-epilogue FFMA kernels of the general entry: (TMA, 2 stages) and
 // (cp.async, 4 stages), paired FMA, 128 x 128 tiles; nullptr otherwise.
 KernelEntry ffma_kernel_scaled(int producer, int stages, int math);

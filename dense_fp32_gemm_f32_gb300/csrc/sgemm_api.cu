@@ -45,6 +45,7 @@ struct DeviceState {
     int max_clusters_pair = 0;    // co-resident 2-CTA clusters of the FFMA kernel
     int max_clusters_split[9] = {0};
     bool regsplit_ok = false;     // the register-split kernels were built at kRegsLaunch registers
+    int fused_per_sm[7] = {0};    // co-resident fused-producer CTAs per SM, by stage count
     unsigned int* status_word = nullptr;  // device address of g_sgemm_status
     std::once_flag pool_once;
     cudaMemPool_t pool = nullptr;  // library-owned pool for per-call workspaces
@@ -144,6 +145,17 @@ int init_device(int dev, DeviceState& st) {
         }
         for (int s = 1; s <= 6; ++s)
             if (set_smem_attr(ffma_kernel_cpasync(s, math)) != SGEMM_OK) return SGEMM_ERR_CUDA;
+        for (int s = 2; s <= 4; ++s) {
+            const KernelEntry f = ffma_kernel_tma_fused(s, math);
+            if (set_smem_attr(f) != SGEMM_OK) return SGEMM_ERR_CUDA;
+            int n = 0;
+            if (f.fn && cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, f.fn, f.threads,
+                                                                      static_cast<size_t>(f.smem_bytes)) != cudaSuccess) {
+                (void)cudaGetLastError();
+                n = 0;
+            }
+            if (math == kMathFfma2 || n < st.fused_per_sm[s] || st.fused_per_sm[s] == 0) st.fused_per_sm[s] = n;
+        }
         for (int s = 1; s <= 6; ++s)
             for (int prod : {static_cast<int>(kProducerTma), static_cast<int>(kProducerCpAsync)})
                 if (set_smem_attr(ffma_kernel_scaled(prod, s, math)) != SGEMM_OK) return SGEMM_ERR_CUDA;
@@ -307,9 +319,12 @@ constexpr double kRepackMinFlops = 1073741824.0;  // 2^30
 
 long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
 
-bool is_tma(int producer) { return producer == kProducerTma || producer == kProducerTmaWg; }
+bool is_tma(int producer) {
+    return producer == kProducerTma || producer == kProducerTmaWg || producer == kProducerFused;
+}
 
 KernelEntry ffma_kernel(const Plan& pl) {
+    if (pl.producer == kProducerFused) return ffma_kernel_tma_fused(pl.stages, pl.math);
     if (pl.bn == kBNWide) return pl.producer == kProducerTmaWg ? ffma_kernel_tma_wide(pl.stages, pl.math)
                                                                 : KernelEntry{nullptr, 0, 0};
     switch (pl.producer) {
@@ -324,6 +339,7 @@ const char* producer_name(int producer) {
     switch (producer) {
         case kProducerTma: return "tma";
         case kProducerTmaWg: return "tmawg";
+        case kProducerFused: return "fused";
         case kProducerCpAsync: return "cpasync";
     }
     return "?";
@@ -361,6 +377,9 @@ int make_plan(const DeviceState& st, int M, int N, int K, const float* A, int ld
         if (!aligned) return SGEMM_ERR_INVALID_ARG;
         if (!st.regsplit_ok) return SGEMM_ERR_UNSUPPORTED;
         pl.producer = kProducerTmaWg;
+    } else if (want_prod == SGEMM_PRODUCER_FUSED) {
+        if (!aligned) return SGEMM_ERR_INVALID_ARG;
+        pl.producer = kProducerFused;
     } else if (want_prod == SGEMM_PRODUCER_CPASYNC) {
         pl.producer = kProducerCpAsync;
     } else if (want_prod == SGEMM_PRODUCER_AUTO) {
@@ -380,9 +399,17 @@ int make_plan(const DeviceState& st, int M, int N, int K, const float* A, int ld
         }
         if (pl.producer != kProducerTmaWg) return SGEMM_ERR_INVALID_ARG;
         pl.bn = kBNWide;
+    } else if (want_bn == kBNFused) {
+        // 128 x 64 tiles: the fused-producer CTAs, two per SM.
+        if (want_prod == SGEMM_PRODUCER_AUTO) {
+            if (!aligned) return SGEMM_ERR_INVALID_ARG;
+            pl.producer = kProducerFused;
+        }
+        if (pl.producer != kProducerFused) return SGEMM_ERR_INVALID_ARG;
     } else if (want_bn != 0 && want_bn != kBN) {
         return SGEMM_ERR_INVALID_ARG;
     }
+    if (pl.producer == kProducerFused) pl.bn = kBNFused;
 
     if (opt && opt->math) {
         if (opt->math != kMathFfma && opt->math != kMathFfma2) return SGEMM_ERR_INVALID_ARG;
@@ -401,7 +428,12 @@ int make_plan(const DeviceState& st, int M, int N, int K, const float* A, int ld
         if (opt && opt->stages) return SGEMM_ERR_INVALID_ARG;
         pl.stages = 4;
     }
-    if (pl.bn == kBNWide && (pl.stages < 2 || pl.stages > 4)) return SGEMM_ERR_INVALID_ARG;
+    if (pl.producer == kProducerFused && !(opt && opt->stages)) pl.stages = 4;
+    if ((pl.bn == kBNWide || pl.bn == kBNFused) && (pl.stages < 2 || pl.stages > 4)) return SGEMM_ERR_INVALID_ARG;
+    // CTAs that can be resident at once, for the stream-K grid.
+    const int per_sm = pl.producer == kProducerFused ? st.fused_per_sm[pl.stages] : 1;
+    if (per_sm < 1) return SGEMM_ERR_UNSUPPORTED;
+    const long long slots = static_cast<long long>(st.sm_count) * per_sm;
 
     tiles_n = ceil_div(N, pl.bn);
     const long long tiles = tiles_n * tiles_m;
@@ -415,7 +447,7 @@ int make_plan(const DeviceState& st, int M, int N, int K, const float* A, int ld
     if (want_sk < 0 || want_sk > 2) return SGEMM_ERR_INVALID_ARG;
     const bool forced_other = opt && (opt->split_k || opt->multicast == 2 || opt->tail_split > 1);
     const bool use_sk = want_sk == 2 || (want_sk == 0 && !forced_other && pl.num_k_tiles > 0 &&
-                                         tiles * pl.num_k_tiles >= 2LL * st.sm_count);
+                                         tiles * pl.num_k_tiles >= 2LL * slots);
 
     // Split-K over the whole grid, only when the tiles do not fill one wave:
     // pick s in 1..8 minimising (waves of clusters) x (K tiles per CTA).  (With
@@ -424,7 +456,7 @@ int make_plan(const DeviceState& st, int M, int N, int K, const float* A, int ld
     if (opt && opt->split_k) {
         if (opt->split_k < 1 || opt->split_k > 8) return SGEMM_ERR_INVALID_ARG;
         split = opt->split_k;
-    } else if (tiles < st.sm_count && !use_sk) {
+    } else if (tiles < st.sm_count && !use_sk && pl.producer != kProducerFused) {
         long long best = -1;
         for (int s = 1; s <= 8; ++s) {
             const int slots = st.max_clusters_split[s];
@@ -438,6 +470,7 @@ int make_plan(const DeviceState& st, int M, int N, int K, const float* A, int ld
         }
     }
     if (split > 1 && pl.stages < 2) return SGEMM_ERR_INVALID_ARG;  // partial tile needs 64 KiB of ring
+    if (split > 1 && pl.producer == kProducerFused) return SGEMM_ERR_INVALID_ARG;  // two CTAs per SM: no clusters
 
     // Multicast pairs along N (TMA producer, no split).  Measured on GB300 at
     // 1024^3..8192^3 the pairing costs more (the two CTAs release every slot
@@ -445,7 +478,7 @@ int make_plan(const DeviceState& st, int M, int N, int K, const float* A, int ld
     // unless forced.
     const int want_mc = opt ? opt->multicast : 0;
     if (want_mc == 2) {
-        if (split > 1 || !is_tma(pl.producer)) return SGEMM_ERR_INVALID_ARG;
+        if (split > 1 || !is_tma(pl.producer) || pl.producer == kProducerFused) return SGEMM_ERR_INVALID_ARG;
         if (st.max_clusters_pair < 1) return SGEMM_ERR_UNSUPPORTED;
         pl.mcast = 2;
     } else if (want_mc == 0 || want_mc == 1) {
@@ -470,7 +503,7 @@ int make_plan(const DeviceState& st, int M, int N, int K, const float* A, int ld
     pl.launch[0].split = split;
     const int want_tail = opt ? opt->tail_split : 0;
     if (want_tail < 0 || want_tail > 8) return SGEMM_ERR_INVALID_ARG;
-    if (split == 1 && pl.mcast == 1 && want_tail > 1 && grid_tiles > st.sm_count) {
+    if (split == 1 && pl.mcast == 1 && want_tail > 1 && grid_tiles > st.sm_count && pl.producer != kProducerFused) {
         const long long full = (grid_tiles / st.sm_count) * st.sm_count;
         const long long rem = grid_tiles - full;
         // keep at least four K slices per CTA of the tail
@@ -483,14 +516,14 @@ int make_plan(const DeviceState& st, int M, int N, int K, const float* A, int ld
         }
     }
 
-    // Stream-K schedule: one CTA per SM, partial tiles finished through a
-    // global workspace.
+    // Stream-K schedule: one CTA per SM (two for the fused producer), partial
+    // tiles finished through a global workspace.
     if (use_sk) {
         if (split > 1 || pl.mcast > 1 || pl.nlaunch > 1 || pl.num_k_tiles == 0) return SGEMM_ERR_INVALID_ARG;
         // All but the last full wave run data-parallel (raster order keeps
         // the A and B panels in flight few, as in the plain launch); the last
         // full wave and the partial one are dealt out as units.
-        const long long G = st.sm_count;
+        const long long G = slots;
         const long long waves = grid_tiles / G;
         const long long dp = waves > 1 ? (waves - 1) * G : 0;
         const long long units = (grid_tiles - dp) * pl.num_k_tiles;

@@ -55,7 +55,7 @@ constexpr int kBK = 32;
 constexpr int kConsumerWarps = 8;
 constexpr int kConsumerThreads = kConsumerWarps * 32;
 
-enum : int { kProducerTma = 1, kProducerCpAsync = 2, kProducerTmaWg = 3 };
+enum : int { kProducerTma = 1, kProducerCpAsync = 2, kProducerTmaWg = 3, kProducerFused = 4 };
 
 // Producer warps: one elected lane drives the TMA; the cp.async producer
 // issues every 4-byte copy itself, so it gets a full warpgroup.
@@ -71,9 +71,22 @@ enum : int { kProducerTma = 1, kProducerCpAsync = 2, kProducerTmaWg = 3 };
 // is launched with (setmaxnreg.inc waits until the registers are free, so a
 // split that asked for more would never finish: the host launches this
 // variant only when the kernel was built with exactly kRegsLaunch).
+//
+// kProducerFused has no producer warp at all: a CTA of 4 warps that all
+// compute (128 x 64 tiles), thread 0 issuing the TMA copies between its own
+// multiply-adds, so that two CTAs fit on an SM (2 x 128 threads may use up to
+// 255 registers each) and run independently of each other.
 template <int PRODUCER>
 __host__ __device__ constexpr int ffma_producer_warps() {
-    return PRODUCER == kProducerTma ? 1 : 4;
+    return PRODUCER == kProducerFused ? 0 : PRODUCER == kProducerTma ? 1 : 4;
+}
+template <int PRODUCER>
+__host__ __device__ constexpr int ffma_consumer_warps() {
+    return PRODUCER == kProducerFused ? 4 : kConsumerWarps;
+}
+template <int PRODUCER>
+__host__ __device__ constexpr int ffma_min_blocks() {
+    return PRODUCER == kProducerFused ? 2 : 1;
 }
 constexpr int kRegsLaunch = 168;
 constexpr int kRegsProducer = 40;
@@ -82,9 +95,10 @@ static_assert(4 * 32 * kRegsProducer + kConsumerWarps * 32 * kRegsConsumer == (k
               "the register split must use exactly the registers the CTA is launched with");
 template <int PRODUCER>
 __host__ __device__ constexpr int ffma_threads() {
-    return kConsumerThreads + 32 * ffma_producer_warps<PRODUCER>();
+    return 32 * (ffma_consumer_warps<PRODUCER>() + ffma_producer_warps<PRODUCER>());
 }
 constexpr int kBNWide = 256;  // wide tile: 128 x 256, 8 x 16 per thread (producer warpgroup only)
+constexpr int kBNFused = 64;  // 128 x 64 tiles of the fused-producer CTAs
 constexpr int kStageABytes = kBM * kBK * 4;      // 16 KiB, 128-byte swizzled rows of 32 floats
 template <int BN>
 __host__ __device__ constexpr int ffma_stage_b_bytes() {
@@ -152,17 +166,23 @@ __device__ __forceinline__ uint32_t swz128(int r, int c) {
 // alpha, beta); a separate instantiation, so that the plain kernels' code is
 // not touched by it.
 template <int STAGES, int PRODUCER, int MATH, int BN = kBN, bool SCALED = false>
-__global__ void __launch_bounds__(ffma_threads<PRODUCER>(), 1)
+__global__ void __launch_bounds__(ffma_threads<PRODUCER>(), ffma_min_blocks<PRODUCER>())
     sgemm_ffma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                       const FfmaParams p) {
     // 128 accumulators per thread need the consumer register budget of the
     // register split.
-    static_assert(BN == kBN || (BN == kBNWide && PRODUCER == kProducerTmaWg), "tile width");
+    constexpr bool kFused = PRODUCER == kProducerFused;
+    static_assert((BN == kBN && !kFused) || (BN == kBNWide && PRODUCER == kProducerTmaWg) ||
+                      (BN == kBNFused && kFused),
+                  "tile width");
     constexpr int kStageBBytes = ffma_stage_b_bytes<BN>();
     constexpr int kStageBytes = ffma_stage_bytes<BN>();
     constexpr int kPartialBytes = ffma_partial_bytes<BN>();
-    constexpr int H = BN / 64;  // 4-column groups per thread row (2 or 4)
-    constexpr int TQ = 2 * H;   // column pairs per thread row
+    constexpr int CW = ffma_consumer_warps<PRODUCER>();  // computing warps
+    constexpr int CT = 32 * CW;                          // computing threads
+    constexpr int WN = kFused ? 1 : 2;                   // warps across the tile's width
+    constexpr int H = BN / WN / 32;                      // 4-column groups per thread row (2 or 4)
+    constexpr int TQ = 2 * H;                            // column pairs per thread row
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte alignment for the 128-byte swizzle pattern; identical offset in
     // every CTA, which multicast relies on.
@@ -180,8 +200,8 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     constexpr int PW = ffma_producer_warps<PRODUCER>();
-    const bool is_producer = warp >= kConsumerWarps;
-    const int pw = warp - kConsumerWarps;  // producer warp index (when is_producer)
+    const bool is_producer = !kFused && warp >= CW;
+    const int pw = warp - CW;  // producer warp index (when is_producer)
     const int split = p.split;
     const int mcast = p.mcast;
     const uint32_t crank = (split > 1 || mcast > 1) ? cluster_ctarank() : 0u;
@@ -232,14 +252,14 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), 1)
 
     if (threadIdx.x == 0) {
         const uint32_t full_count = kTma ? 1u : 32u * PW;
-        const uint32_t empty_count = static_cast<uint32_t>(kConsumerWarps * mcast);
+        const uint32_t empty_count = static_cast<uint32_t>(CW * mcast);
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full_bar(s), full_count);
             mbar_init(empty_bar(s), empty_count);
         }
         fence_mbarrier_init();
     }
-    if (kTma && is_producer && pw == 0 && lane == 0) {
+    if (kTma && (kFused ? threadIdx.x == 0 : (is_producer && pw == 0 && lane == 0))) {
         prefetch_tensormap(&tmA);
         prefetch_tensormap(&tmB);
     }
@@ -377,7 +397,7 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), 1)
     for (int i = 0; i < 8; ++i)
 #pragma unroll
         for (int q = 0; q < TQ; ++q) acc[i][q] = make_float2(0.f, 0.f);  // (K == 0: the empty sum)
-    const int wm = warp >> 1, wn = warp & 1;
+    const int wm = kFused ? warp : warp >> 1, wn = kFused ? 0 : warp & 1;
     const int tm = (lane & 1) | (((lane >> 2) & 1) << 1);
     const int tn = ((lane >> 1) & 1) | (((lane >> 3) & 1) << 1) | (((lane >> 4) & 1) << 2);
 
@@ -392,7 +412,7 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), 1)
     const bool read_c = SCALED && p.beta != 0.f;
     auto prefetch_c = [&](int tile) {
         const int row0 = (tile / p.tiles_n) * kBM + wm * 32 + tm;
-        const int col0 = (tile % p.tiles_n) * BN + wn * (BN / 2) + tn * 4;
+        const int col0 = (tile % p.tiles_n) * BN + wn * (BN / WN) + tn * 4;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const int r = row0 + 4 * i;
@@ -404,7 +424,7 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), 1)
     };
     auto store_c_plain = [&](int tile) {
         const int row0 = (tile / p.tiles_n) * kBM + wm * 32 + tm;
-        const int col0 = (tile % p.tiles_n) * BN + wn * (BN / 2) + tn * 4;
+        const int col0 = (tile % p.tiles_n) * BN + wn * (BN / WN) + tn * 4;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const int r = row0 + 4 * i;
@@ -428,7 +448,7 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), 1)
     };
     auto store_c_scaled = [&](int tile) {
         const int row0 = (tile / p.tiles_n) * kBM + wm * 32 + tm;
-        const int col0 = (tile % p.tiles_n) * BN + wn * (BN / 2) + tn * 4;
+        const int col0 = (tile % p.tiles_n) * BN + wn * (BN / WN) + tn * 4;
         // Rows in groups of RG: with beta != 0 the group's old C values are
         // all loaded before any of its stores, so the loads are in flight
         // together (a load after a store to C could not be moved above it).
@@ -510,15 +530,49 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), 1)
             store_c_plain(tile);
         }
     };
-    auto consumer_sync = [] { asm volatile("bar.sync 1, %0;" ::"n"(kConsumerThreads) : "memory"); };
+    auto consumer_sync = [] { asm volatile("bar.sync 1, %0;" ::"n"(CT) : "memory"); };
 
     {
         // Byte offsets inside a stage.  A row r = wm*32 + tm + 4i has r mod 8 =
         // tm + 4*(i & 1), so even i share one swizzle key and odd i the other.
         const uint32_t a_row0 = static_cast<uint32_t>((wm * 32 + tm) * 128);
-        const uint32_t b_col0 = static_cast<uint32_t>((wn * (BN / 2) + tn * 4) * 4);
+        const uint32_t b_col0 = static_cast<uint32_t>((wn * (BN / WN) + tn * 4) * 4);
         const uint8_t* const smem_a = smem + a_row0;                          // generic pointers
         const uint8_t* const smem_b = smem + STAGES * kStageABytes + b_col0;  // for the vector loads
+
+        // Fused producer (thread 0 of a kProducerFused CTA): the loads follow
+        // the same work sequence as the computation.  STAGES loads go out
+        // before the first K slice; at the start of K slice it (> 0) the slot
+        // of slice it-1 is refilled with load it-1+STAGES, once every warp has
+        // released it (usually already: the warps run side by side).
+        Work lwork = work0;
+        int ltile = 0, lkb = 0, lke = 0, lkt = 0, loads = 0;
+        bool lhave = false, lfail = false;
+        auto issue_load = [&]() {
+            if (!lhave || lfail) return;
+            const int s = loads % STAGES;
+            const int round = loads / STAGES;
+            if (round > 0 && !mbar_wait_bounded(empty_bar(s), (round - 1) & 1, tmo)) {
+                lfail = true;  // the consumers' own bounded waits then end the loop
+                return;
+            }
+            if (!(skip_here && loads == p.skip_stage - 1)) {
+                const int k0 = lkt * kBK;
+                mbar_arrive_expect_tx(full_bar(s), kStageBytes);
+                tma_load_2d(sA0 + s * kStageABytes, &tmA, full_bar(s), k0, (ltile / p.tiles_n) * kBM);
+                tma_load_2d(sB0 + s * kStageBBytes, &tmB, full_bar(s), (ltile % p.tiles_n) * BN, k0);
+            }
+            ++loads;
+            if (++lkt >= lke) {
+                lhave = lwork.next(ltile, lkb, lke);
+                lkt = lkb;
+            }
+        };
+        if (kFused && threadIdx.x == 0) {
+            lhave = lwork.next(ltile, lkb, lke);
+            lkt = lkb;
+            for (int j = 0; j < STAGES; ++j) issue_load();
+        }
 
         int it = 0;
         Work work = work0;
@@ -534,6 +588,7 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), 1)
             for (int kt = kb; kt < ke; ++kt, ++it) {
                 const int s = it % STAGES;
                 const int round = it / STAGES;
+                if (kFused && threadIdx.x == 0 && it > 0) issue_load();
                 if (!mbar_wait_bounded_warp(full_bar(s), round & 1, tmo)) {
                     timed_out = true;
                     break;
@@ -594,7 +649,7 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), 1)
                 for (int i = 0; i < 8; ++i)
 #pragma unroll
                     for (int h = 0; h < H; ++h)
-                        __stcg(reinterpret_cast<float4*>(ws_mine) + (i * H + h) * kConsumerThreads + threadIdx.x,
+                        __stcg(reinterpret_cast<float4*>(ws_mine) + (i * H + h) * CT + threadIdx.x,
                                make_float4(acc[i][2 * h].x, acc[i][2 * h].y, acc[i][2 * h + 1].x,
                                            acc[i][2 * h + 1].y));
                 consumer_sync();
@@ -633,7 +688,7 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), 1)
                         for (int i = 0; i < 8; ++i)
 #pragma unroll
                             for (int h = 0; h < H; ++h) {
-                                const float4 v = __ldcg(src + (i * H + h) * kConsumerThreads + threadIdx.x);
+                                const float4 v = __ldcg(src + (i * H + h) * CT + threadIdx.x);
                                 acc[i][2 * h].x += v.x;
                                 acc[i][2 * h].y += v.y;
                                 acc[i][2 * h + 1].x += v.z;
@@ -643,6 +698,17 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), 1)
                 }
                 store_c(tile);
             }
+        }
+        if (kFused && threadIdx.x == 0) {
+            // Loads still in flight (the loop ended early): let them land
+            // before the CTA's shared memory is released.  Slot j % STAGES
+            // holds no later load than j, so phase parity (j / STAGES) & 1
+            // identifies its completion.
+            for (int j = loads > STAGES ? loads - STAGES : 0; j < loads; ++j)
+                if (j >= it && !(skip_here && j == p.skip_stage - 1) &&
+                    !mbar_wait_bounded(full_bar(j % STAGES), (j / STAGES) & 1, tmo))
+                    timed_out = true;
+            if (lfail) timed_out = true;
         }
         if (timed_out) atomicOr(p.status, kStatusTimeout);
     }
@@ -657,7 +723,7 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), 1)
             for (int i = 0; i < 8; ++i)
 #pragma unroll
                 for (int h = 0; h < H; ++h)
-                    sts128(base + static_cast<uint32_t>(((i * H + h) * kConsumerThreads + threadIdx.x) * 16),
+                    sts128(base + static_cast<uint32_t>(((i * H + h) * CT + threadIdx.x) * 16),
                            make_float4(acc[i][2 * h].x, acc[i][2 * h].y, acc[i][2 * h + 1].x, acc[i][2 * h + 1].y));
         }
         cluster_sync_all();
@@ -668,7 +734,7 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), 1)
 #pragma unroll
                     for (int h = 0; h < H; ++h) {
                         const uint32_t off =
-                            base + static_cast<uint32_t>(((i * H + h) * kConsumerThreads + threadIdx.x) * 16);
+                            base + static_cast<uint32_t>(((i * H + h) * CT + threadIdx.x) * 16);
                         const float4 v = ld_shared_cluster_v4(map_shared_rank(off, static_cast<uint32_t>(r)));
                         acc[i][2 * h].x += v.x;
                         acc[i][2 * h].y += v.y;

@@ -211,10 +211,14 @@ enum {
     SGEMM_PRODUCER_AUTO = 0,
     SGEMM_PRODUCER_TMA = 1,      /* tensor-map bulk copies (needs 16-byte alignment) */
     SGEMM_PRODUCER_CPASYNC = 2,  /* 4-byte cp.async with zero fill (any alignment) */
-    SGEMM_PRODUCER_TMA_WG = 3    /* tensor-map bulk copies from a producer warpgroup of its own,
+    SGEMM_PRODUCER_TMA_WG = 3,   /* tensor-map bulk copies from a producer warpgroup of its own,
                                     registers split between the warpgroups (producer 40,
                                     consumers 232 per thread); SGEMM_ERR_UNSUPPORTED if the
                                     library's build of that kernel does not allow the split */
+    SGEMM_PRODUCER_FUSED = 4     /* no producer warp: 4-warp CTAs on 128 x 64 tiles, two per SM,
+                                    thread 0 issuing the tensor-map copies between its own
+                                    multiply-adds (implies tile_n = 64; 2..4 stages, default 4;
+                                    no split-K clusters, no multicast) */
 };
 
 /*
@@ -246,8 +250,10 @@ typedef struct sgemm_options {
                              stream-ordered pool the library creates on the
                              device (cudaMallocFromPoolAsync / cudaFreeAsync
                              on `stream`), which keeps it for reuse. */
-    int tile_n;           /* 0 = auto; 128 = 128 x 128 output tiles (8 x 8 per
-                             thread); 256 = 128 x 256 tiles (8 x 16 per thread,
+    int tile_n;           /* 0 = auto; 64 = 128 x 64 tiles of the fused
+                             producer (SGEMM_PRODUCER_FUSED); 128 = 128 x 128
+                             output tiles (8 x 8 per thread); 256 = 128 x 256
+                             tiles (8 x 16 per thread,
                              TMA producer warpgroup with the register split,
                              2..4 stages; the stream-K workspace is then
                              CTAs x (128 KiB + 4 bytes)) */

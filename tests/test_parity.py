@@ -103,6 +103,10 @@ VARIANTS = (
     + [dict(tile_n=256, multicast=2, split_k=1)]
     + [dict(tile_n=256, split_k=s) for s in (2, 4)]
     + [dict(tile_n=256, stream_k=2, math=m) for m in (1, 2)]
+    # fused producer: 4-warp CTAs on 128 x 64 tiles, two per SM
+    + [dict(producer=4, math=m, stages=s, split_k=1) for m in (1, 2) for s in (2, 3, 4)]
+    + [dict(tile_n=64, stream_k=2, math=m) for m in (1, 2)]
+    + [dict(tile_n=64, stream_k=2, stages=2)]
 )
 
 
@@ -139,20 +143,25 @@ def test_tail_split(tail):
     check(Ci, oracle.gemm_f64(Ai.numpy(), Bi.numpy(), with_bound=False)[0], None, exact=True, what=f"tail {tail} int")
 
 
+@pytest.mark.parametrize("tile_n", [128, 64])
 @pytest.mark.parametrize("name", ["square_2048", "ragged_1023x1025x1027", "flat_4096x4096x256",
                                   "skinny_8192x128x8192"])
-def test_stream_k_every_element(name):
-    """Stream-K: one CTA per SM, tiles shared between CTAs finished through
-    the workspace; every element against the oracle, and bitwise repeatable."""
+def test_stream_k_every_element(name, tile_n):
+    """Stream-K: one CTA per SM (two with the fused producer's 128 x 64
+    tiles), tiles shared between CTAs finished through the workspace; every
+    element against the oracle, and bitwise repeatable."""
     p = PROBLEMS[name]
     A, B = problem_operands(p)
-    C = run(A, B, stream_k=2)
+    opt = dict(stream_k=2, tile_n=tile_n)
+    if tile_n == 64:
+        opt["repack"] = 2  # the fused producer needs tensor-map-readable operands
+    C = run(A, B, **opt)
     C64, bound = oracle.gemm_f64(A.numpy(), B.numpy())
-    check(C, C64, bound, exact=False, what=f"{name} stream-K")
-    assert np.array_equal(C, run(A, B, stream_k=2))
+    check(C, C64, bound, exact=False, what=f"{name} stream-K n{tile_n}")
+    assert np.array_equal(C, run(A, B, **opt))
     Ai, Bi = problem_operands(p.int_variant())
-    check(run(Ai, Bi, stream_k=2), oracle.gemm_f64(Ai.numpy(), Bi.numpy(), with_bound=False)[0], None,
-          exact=True, what=f"{name} stream-K int")
+    check(run(Ai, Bi, **opt), oracle.gemm_f64(Ai.numpy(), Bi.numpy(), with_bound=False)[0], None,
+          exact=True, what=f"{name} stream-K n{tile_n} int")
 
 
 @pytest.mark.parametrize("dist", ["real", "int"])
@@ -395,7 +404,7 @@ def test_timeout_is_reported_and_recovers():
     A, B = make_operands(128, 256, 256, "uniform", 14)
     dA, dB = to_device(A), to_device(B)
     assert g.check_status() == 0
-    for producer in (1, 2):
+    for producer in (1, 2, 4):
         g.sgemm_f32_ex(dA, dB, producer=producer, split_k=1, debug_skip_stage=3, timeout_ns=20_000_000)
         assert g.check_status() == 4
         g.sgemm_f32_ex(dA, dB, producer=producer, stream_k=2, debug_skip_stage=1, timeout_ns=20_000_000)
@@ -404,3 +413,37 @@ def test_timeout_is_reported_and_recovers():
     assert g.check_status() == 0
     C64, bound = oracle.gemm_f64(A.numpy(), B.numpy())
     check(C.cpu().numpy(), C64, bound, exact=False, what="after timeout")
+
+
+# ---------------------------------------------------------------- CUDA graphs
+
+def test_cuda_graph_capture_and_replay():
+    """The entries enqueue only stream-ordered work (pool allocation and free,
+    a memset, kernels), so a call can be captured in a CUDA graph and
+    replayed; each replay recomputes from the current inputs."""
+    M, N, K = 1024, 768, 1536  # stream-K: the workspace and flags are captured too
+    A, B = make_operands(M, N, K, "uniform", 16)
+    dA, dB = to_device(A), to_device(B)
+    dC = torch.empty((M, N), device="cuda")
+    dG = torch.empty((M, N), device="cuda")
+    g.sgemm_f32(dA, dB, dC)  # first call on the device outside the capture (one-time set-up)
+    g.sgemm_f32_gemm(dA, dB, dG, alpha=2.0, beta=0.0)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            g.sgemm_f32(dA, dB, dC, stream=s)
+            g.sgemm_f32_gemm(dA, dB, dG, alpha=2.0, beta=0.0, stream=s)
+    for seed in (17, 18):
+        A2, B2 = make_operands(M, N, K, "uniform", seed)
+        dA.copy_(A2)
+        dB.copy_(B2)
+        dC.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        C64, bound = oracle.gemm_f64(A2.numpy(), B2.numpy())
+        check(dC.cpu().numpy(), C64, bound, exact=False, what=f"graph replay {seed}")
+        check(dG.cpu().numpy(), 2.0 * C64, 2.0 * bound, exact=False, what=f"graph replay gemm {seed}")
+    assert g.check_status() == 0
