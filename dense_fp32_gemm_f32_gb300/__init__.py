@@ -126,17 +126,18 @@ def sgemm_3xtf32(A: torch.Tensor, B: torch.Tensor, out: torch.Tensor | None = No
 
 
 def sgemm_f32_ex(A, B, out=None, *, stream=None, producer=0, split_k=0, multicast=0, math=0, stages=0,
-                 debug_skip_stage=0, timeout_ns=0, tail_split=0, stream_k=0, tile_n=0, repack=0) -> torch.Tensor:
+                 debug_skip_stage=0, timeout_ns=0, tail_split=0, stream_k=0, tile_n=0, repack=0,
+                 a_layout=0) -> torch.Tensor:
     """sgemm_f32 with forced variant choices (see struct sgemm_options)."""
     opt = Options(producer, split_k, multicast, math, stages, debug_skip_stage, timeout_ns, tail_split, stream_k,
-                  tile_n, repack)
+                  tile_n, repack, a_layout)
     return _call("sgemm_f32_ex", A, B, out, stream, opt)
 
 
 def sgemm_3xtf32_ex(A, B, out=None, *, stream=None, variant=0, debug_skip_stage=0, timeout_ns=0) -> torch.Tensor:
     """sgemm_3xtf32 with forced choices: ``variant`` 1 = split-tile kernel,
     2 = direct-A kernel (0 = automatic)."""
-    opt = Options(0, 0, 0, variant, 0, debug_skip_stage, timeout_ns, 0, 0, 0, 0)
+    opt = Options(0, 0, 0, variant, 0, debug_skip_stage, timeout_ns, 0, 0, 0, 0, 0)
     return _call("sgemm_3xtf32_ex", A, B, out, stream, opt)
 
 

@@ -43,6 +43,7 @@ class Options(ctypes.Structure):
         ("stream_k", _i),
         ("tile_n", _i),
         ("repack", _i),
+        ("a_layout", _i),
     ]
 
 

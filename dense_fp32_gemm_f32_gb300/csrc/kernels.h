@@ -26,6 +26,9 @@ KernelEntry ffma_kernel_tma_fused(int stages, int math);
 // The scaled-epilogue FFMA kernels of the general entry: (TMA, 2 stages) and
 // (cp.async, 4 stages), paired FMA, 128 x 128 tiles; nullptr otherwise.
 KernelEntry ffma_kernel_scaled(int producer, int stages, int math);
+// Transposed-A FFMA kernels (A stored K x M): TMA producer, 2 stages, paired
+// FMA, 128 x 128 tiles; `scaled` selects the scaled epilogue.
+KernelEntry ffma_kernel_amn(int stages, int math, bool scaled);
 // FFMA kernels fed by 4-byte cp.async (any alignment); stages in {2,4}.
 KernelEntry ffma_kernel_cpasync(int stages, int math);
 // Three-product TF32 kernel on the tensor cores (TMA-fed, 128 x 128 tiles,

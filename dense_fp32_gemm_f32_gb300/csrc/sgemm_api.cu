@@ -156,9 +156,12 @@ int init_device(int dev, DeviceState& st) {
             }
             if (math == kMathFfma2 || n < st.fused_per_sm[s] || st.fused_per_sm[s] == 0) st.fused_per_sm[s] = n;
         }
-        for (int s = 1; s <= 6; ++s)
+        for (int s = 1; s <= 6; ++s) {
             for (int prod : {static_cast<int>(kProducerTma), static_cast<int>(kProducerCpAsync)})
                 if (set_smem_attr(ffma_kernel_scaled(prod, s, math)) != SGEMM_OK) return SGEMM_ERR_CUDA;
+            for (bool scaled : {false, true})
+                if (set_smem_attr(ffma_kernel_amn(s, math, scaled)) != SGEMM_OK) return SGEMM_ERR_CUDA;
+        }
     }
     if (set_smem_attr(tf32x3_kernel()) != SGEMM_OK || set_smem_attr(tf32x3_direct_kernel()) != SGEMM_OK)
         return SGEMM_ERR_CUDA;
@@ -222,9 +225,11 @@ size_t span_bytes(long long rows, long long cols, long long ld) {
     return static_cast<size_t>(((rows - 1) * ld + cols) * 4);
 }
 
-int validate(int M, int N, int K, const float* A, int lda, const float* B, int ldb, const float* C, int ldc) {
+// a_mn: A is stored transposed (K x M, lda >= M).
+int validate(int M, int N, int K, const float* A, int lda, const float* B, int ldb, const float* C, int ldc,
+             bool a_mn = false) {
     if (M < 0 || N < 0 || K < 0) return SGEMM_ERR_INVALID_ARG;
-    if (lda < K || ldb < N || ldc < N) return SGEMM_ERR_INVALID_ARG;
+    if (lda < (a_mn ? M : K) || ldb < N || ldc < N) return SGEMM_ERR_INVALID_ARG;
     if (M > 0 && K > 0 && !A) return SGEMM_ERR_INVALID_ARG;
     if (K > 0 && N > 0 && !B) return SGEMM_ERR_INVALID_ARG;
     if (M > 0 && N > 0 && !C) return SGEMM_ERR_INVALID_ARG;
@@ -233,7 +238,8 @@ int validate(int M, int N, int K, const float* A, int lda, const float* B, int l
         0x7fffffffLL)
         return SGEMM_ERR_INVALID_ARG;
     const size_t cb = span_bytes(M, N, ldc);
-    if (ranges_overlap(C, cb, A, span_bytes(M, K, lda)) || ranges_overlap(C, cb, B, span_bytes(K, N, ldb)))
+    if (ranges_overlap(C, cb, A, a_mn ? span_bytes(K, M, lda) : span_bytes(M, K, lda)) ||
+        ranges_overlap(C, cb, B, span_bytes(K, N, ldb)))
         return SGEMM_ERR_INVALID_ARG;
     return SGEMM_OK;
 }
@@ -284,11 +290,61 @@ struct Repacked {
         }
         return SGEMM_OK;
     }
+    // A (M x K, pitch lda) -> its transpose (K x M, pitch M rounded up to 4
+    // floats) in a pool buffer; A / lda then point at the copy.
+    int make_transposed_a(int dev, DeviceState& st, int M, int K, const float*& A, int& lda, cudaStream_t cs) {
+        stream = cs;
+        const long long M4 = (static_cast<long long>(M) + 3) / 4 * 4;
+        if (M4 > 0x7fffffffLL) return SGEMM_ERR_INVALID_ARG;
+        cudaMemPool_t pool = workspace_pool(dev, st);
+        if (!pool || cudaMallocFromPoolAsync(&ws, static_cast<size_t>(K) * M4 * 4, pool, cs) != cudaSuccess) {
+            (void)cudaGetLastError();
+            ws = nullptr;
+            return SGEMM_ERR_CUDA;
+        }
+        float* At = static_cast<float*>(ws);
+        const int rc = transpose_rows(A, lda, At, M4, K, M, nullptr, 0, nullptr, 0, 0, 0, cs);
+        if (rc != SGEMM_OK) {
+            release();
+            return rc;
+        }
+        A = At;
+        lda = static_cast<int>(M4);
+        return SGEMM_OK;
+    }
     void release() {
         if (ws) (void)cudaFreeAsync(ws, stream);
         ws = nullptr;
     }
 };
+
+// A read in the transposed layout (sgemm_options.a_layout): the
+// transposed-A kernels' consumers read each k's A values as two 16-byte
+// vectors instead of a 4-k vector per row.  Measured on GB300, with the
+// transposing copy (one read and one write of A) included: 4096^3 65.5 ->
+// 68.5 TFLOP/s, 8192^3 66.3 -> 71.2, 128 x 8192 x 16384 64.3 -> 68.3,
+// 4096 x 4096 x 256 58.0 -> 59.2, 2048^3 even, 1024^3 43.1 -> 40.6 (the copy
+// launch does not pay there).  Automatic when no variant is forced, N >= 512
+// (the copy is small next to the product) and 2MNK >= 2^33.
+constexpr double kTransposeMinFlops = 8589934592.0;
+constexpr int kTransposeMinN = 512;
+
+bool options_force_variant(const sgemm_options* opt) {
+    return opt && (opt->producer || opt->split_k || opt->multicast || opt->math || opt->stages || opt->tail_split ||
+                   opt->stream_k || opt->tile_n || opt->repack);
+}
+
+// 0 = keep A as stored, 1 = copy it transposed; -1 = invalid option.
+int choose_a_layout(int M, int N, int K, const sgemm_options* opt) {
+    const int want = opt ? opt->a_layout : 0;
+    if (want < 0 || want > 2) return -1;
+    if (K == 0 || want == 1) return 0;
+    if (want == 2) return 1;
+    return (!options_force_variant(opt) && N >= kTransposeMinN &&
+            2.0 * static_cast<double>(M) * static_cast<double>(N) * static_cast<double>(K) >= kTransposeMinFlops)
+               ? 1
+               : 0;
+}
 
 struct Launch {
     int tile_base = 0;  // first output tile
@@ -309,6 +365,7 @@ struct Plan {
     int sk = 0;           // stream-K: launch[0].tiles CTAs, one per SM
     int sk_dp_tiles = 0;  // tiles taken whole (data-parallel waves) before the stream-K region
     int repack = 0;       // operands copied to 16-byte pitched rows first: bit 0 = A, bit 1 = B
+    bool a_mn = false;    // A stored transposed (K x M): the transposed-A kernels
 };
 
 // Repacking pays once the product is large next to the copy.  Measured on
@@ -324,6 +381,8 @@ bool is_tma(int producer) {
 }
 
 KernelEntry ffma_kernel(const Plan& pl) {
+    if (pl.a_mn) return pl.producer == kProducerTma ? ffma_kernel_amn(pl.stages, pl.math, false)
+                                                    : KernelEntry{nullptr, 0, 0};
     if (pl.producer == kProducerFused) return ffma_kernel_tma_fused(pl.stages, pl.math);
     if (pl.bn == kBNWide) return pl.producer == kProducerTmaWg ? ffma_kernel_tma_wide(pl.stages, pl.math)
                                                                 : KernelEntry{nullptr, 0, 0};
@@ -351,8 +410,14 @@ bool tma_ok(const float* p, int ld) {
 
 // Chooses the variant.  Any field of `opt` that is non-zero forces that choice.
 int make_plan(const DeviceState& st, int M, int N, int K, const float* A, int lda, const float* B, int ldb,
-              const sgemm_options* opt, Plan* out) {
+              const sgemm_options* opt, Plan* out, bool a_mn = false) {
     Plan pl;
+    // Transposed A (general entry only): tensor-map readable A, TMA producer
+    // warp, 2 stages, paired FMA, no multicast (see below).
+    if (a_mn && (K == 0 || !tma_ok(A, lda) || (opt && (opt->producer || opt->tile_n || opt->math || opt->stages ||
+                                                        opt->multicast == 2))))
+        return SGEMM_ERR_INVALID_ARG;
+    pl.a_mn = a_mn;
     pl.num_k_tiles = static_cast<int>(ceil_div(K, kBK));
     long long tiles_n = ceil_div(N, kBN);
     const long long tiles_m = ceil_div(M, kBM);
@@ -363,9 +428,9 @@ int make_plan(const DeviceState& st, int M, int N, int K, const float* A, int ld
     const int want_prod = opt ? opt->producer : 0;
     const int want_repack = opt ? opt->repack : 0;
     if (want_repack < 0 || want_repack > 2) return SGEMM_ERR_INVALID_ARG;
-    const int misaligned = (tma_ok(A, lda) ? 0 : 1) | (tma_ok(B, ldb) ? 0 : 2);
+    const int misaligned = (a_mn || tma_ok(A, lda) ? 0 : 1) | (tma_ok(B, ldb) ? 0 : 2);
     if (K > 0 && misaligned &&
-        (want_repack == 2 ||
+        (want_repack == 2 || a_mn ||  // (the transposed-A kernels have no cp.async form)
          (want_repack == 0 && want_prod == SGEMM_PRODUCER_AUTO &&
           2.0 * static_cast<double>(M) * static_cast<double>(N) * static_cast<double>(K) >= kRepackMinFlops)))
         pl.repack = misaligned;
@@ -562,7 +627,9 @@ const char* describe_plan(const Plan& pl) {
     if (pl.bn != kBN && n > 0 && n < static_cast<int>(sizeof buf))
         n += std::snprintf(buf + n, sizeof buf - n, "/n%d", pl.bn);
     if (pl.repack && n > 0 && n < static_cast<int>(sizeof buf))
-        std::snprintf(buf + n, sizeof buf - n, "/repack%s", pl.repack == 1 ? "A" : pl.repack == 2 ? "B" : "AB");
+        n += std::snprintf(buf + n, sizeof buf - n, "/repack%s", pl.repack == 1 ? "A" : pl.repack == 2 ? "B" : "AB");
+    if (pl.a_mn && n > 0 && n < static_cast<int>(sizeof buf))
+        std::snprintf(buf + n, sizeof buf - n, "/at");
     return buf;
 }
 
@@ -572,8 +639,8 @@ struct Scale {
 };
 
 int run_ffma(int M, int N, int K, const float* A, int lda, const float* B, int ldb, float* C, int ldc,
-             void* stream, const sgemm_options* opt, const Scale* scale = nullptr) {
-    int rc = validate(M, N, K, A, lda, B, ldb, C, ldc);
+             void* stream, const sgemm_options* opt, const Scale* scale = nullptr, bool a_mn = false) {
+    int rc = validate(M, N, K, A, lda, B, ldb, C, ldc, a_mn);
     if (rc != SGEMM_OK) return rc;
     if (opt && opt->debug_skip_stage < 0) return SGEMM_ERR_INVALID_ARG;
     if (M == 0 || N == 0) return SGEMM_OK;  // nothing to write; no device work
@@ -582,10 +649,27 @@ int run_ffma(int M, int N, int K, const float* A, int lda, const float* B, int l
     rc = current_device(&dev, &st);
     if (rc != SGEMM_OK) return rc;
 
-    Plan pl;
-    rc = make_plan(*st, M, N, K, A, lda, B, ldb, opt, &pl);
-    if (rc != SGEMM_OK) return rc;
     const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    // A copied transposed for the transposed-A kernels (see choose_a_layout).
+    Repacked a_t;
+    const int layout = a_mn ? 0 : choose_a_layout(M, N, K, opt);
+    if (layout < 0) return SGEMM_ERR_INVALID_ARG;
+    if (layout == 1) {
+        rc = a_t.make_transposed_a(dev, *st, M, K, A, lda, cs);
+        if (rc == SGEMM_OK) {
+            a_mn = true;
+        } else if (opt && opt->a_layout == 2) {
+            return rc;
+        }  // (automatic: without the pool's buffer, A is read as stored)
+    }
+    // (With a transposed A, make_plan rejects forced producer, tile, math,
+    // stage and multicast choices: the transposed-A kernels have one form.)
+    Plan pl;
+    rc = make_plan(*st, M, N, K, A, lda, B, ldb, opt, &pl, a_mn);
+    if (rc != SGEMM_OK) {
+        a_t.release();
+        return rc;
+    }
 
     // Repacking: copy the misaligned operand(s) into pitched rows taken from
     // the pool, and run the product on the copies.  If the pool cannot serve
@@ -596,17 +680,24 @@ int run_ffma(int M, int N, int K, const float* A, int lda, const float* B, int l
         if (rc == SGEMM_ERR_CUDA && !(opt && opt->repack == 2)) {
             sgemm_options o = opt ? *opt : sgemm_options{};
             o.repack = 1;
-            rc = make_plan(*st, M, N, K, A, lda, B, ldb, &o, &pl);
+            rc = make_plan(*st, M, N, K, A, lda, B, ldb, &o, &pl, a_mn);
         }
-        if (rc != SGEMM_OK) return rc;
+        if (rc != SGEMM_OK) {
+            a_t.release();
+            return rc;
+        }
     }
-    // Returns the repack buffers to the pool behind everything enqueued so far.
-    auto release_pack = [&] { packed.release(); };
+    // Returns the copies of A and B to the pool behind everything enqueued so far.
+    auto release_pack = [&] {
+        packed.release();
+        a_t.release();
+    };
 
     const bool scaled = scale && (scale->alpha != 1.f || scale->beta != 0.f);
-    const KernelEntry k = scaled ? (pl.bn == kBN ? ffma_kernel_scaled(pl.producer, pl.stages, pl.math)
-                                                 : KernelEntry{nullptr, 0, 0})
-                                 : ffma_kernel(pl);
+    const KernelEntry k = pl.a_mn ? ffma_kernel_amn(pl.stages, pl.math, scaled)
+                          : scaled ? (pl.bn == kBN ? ffma_kernel_scaled(pl.producer, pl.stages, pl.math)
+                                                   : KernelEntry{nullptr, 0, 0})
+                                   : ffma_kernel(pl);
     if (!k.fn) {
         release_pack();
         return SGEMM_ERR_INVALID_ARG;
@@ -617,7 +708,8 @@ int run_ffma(int M, int N, int K, const float* A, int lda, const float* B, int l
     std::memset(&tmA, 0, sizeof tmA);
     std::memset(&tmB, 0, sizeof tmB);
     if (is_tma(pl.producer)) {
-        rc = encode_2d(&tmA, A, K, M, lda, kBK, kBM / pl.mcast, CU_TENSOR_MAP_SWIZZLE_128B);
+        rc = pl.a_mn ? encode_2d(&tmA, A, M, K, lda, kBM, kBK, CU_TENSOR_MAP_SWIZZLE_NONE)  // {m, k} boxes of 128 x 32
+                     : encode_2d(&tmA, A, K, M, lda, kBK, kBM / pl.mcast, CU_TENSOR_MAP_SWIZZLE_128B);
         if (rc == SGEMM_OK) rc = encode_2d(&tmB, B, N, K, ldb, pl.bn, kBK, CU_TENSOR_MAP_SWIZZLE_NONE);
         if (rc != SGEMM_OK) {
             release_pack();
@@ -913,14 +1005,19 @@ int run_gemm(int transa, int transb, int M, int N, int K, float alpha, const flo
     sc.alpha = alpha;
     sc.beta = beta;
     if (!transa && !transb) return run_ffma(M, N, K, A, lda, B, ldb, C, ldc, stream, nullptr, &sc);
-    // Transposed storage: one transposing copy into pitched rows per
-    // transposed operand (HBM traffic of one read and one write of it, about
-    // 1 % of the product's time at 4096^3), then the product on the copies.
+    // Transposed A that the tensor maps can read stays where it is: the
+    // transposed-A kernels load it in its own storage order.  Otherwise, and
+    // for a transposed B, one transposing copy into pitched rows per operand
+    // (HBM traffic of one read and one write of it), then the product on the
+    // copies.
+    const bool a_native = transa && tma_ok(A, lda);
+    const int copies = (transa && !a_native ? 1 : 0) | (transb ? 2 : 0);
     Repacked packed;
-    rc = packed.make(dev, *st, (transa ? 1 : 0) | (transb ? 2 : 0), M, N, K, A, lda, B, ldb, cs, transa != 0,
-                     transb != 0);
-    if (rc != SGEMM_OK) return rc;
-    rc = run_ffma(M, N, K, A, lda, B, ldb, C, ldc, stream, nullptr, &sc);
+    if (copies) {
+        rc = packed.make(dev, *st, copies, M, N, K, A, lda, B, ldb, cs, transa != 0, transb != 0);
+        if (rc != SGEMM_OK) return rc;
+    }
+    rc = run_ffma(M, N, K, A, lda, B, ldb, C, ldc, stream, nullptr, &sc, a_native);
     packed.release();
     return rc;
 }
@@ -1148,6 +1245,13 @@ const char* sgemm_describe(int M, int N, int K, const float* A, int lda, const f
     if (current_device(&dev, &st) != SGEMM_OK) return "unavailable";
     if (M == 0 || N == 0) return "noop";
     Plan pl;
+    if (choose_a_layout(M, N, K, nullptr) == 1) {
+        // The call would run on a transposed copy of A (a pool buffer: aligned
+        // base, pitch M rounded up to 4 floats).
+        const float* At = reinterpret_cast<const float*>(uintptr_t{256});
+        const int ldat = (M + 3) / 4 * 4;
+        if (make_plan(*st, M, N, K, At, ldat, B, ldb, nullptr, &pl, true) == SGEMM_OK) return describe_plan(pl);
+    }
     if (make_plan(*st, M, N, K, A, lda, B, ldb, nullptr, &pl) != SGEMM_OK) return "invalid";
     return describe_plan(pl);
 }

@@ -165,13 +165,19 @@ __device__ __forceinline__ uint32_t swz128(int r, int c) {
 // SCALED: the epilogue applies C = alpha * (A B) + beta * C (FfmaParams
 // alpha, beta); a separate instantiation, so that the plain kernels' code is
 // not touched by it.
-template <int STAGES, int PRODUCER, int MATH, int BN = kBN, bool SCALED = false>
+//
+// AMN: A is stored transposed (K x M row-major, m innermost: the general
+// entry's op(A) = A^T).  The TMA then lands each stage's A slice as 32 rows of
+// 128 m values (no swizzle) and a thread reads its 8 rows' values for one k
+// as two 16-byte vectors; its rows become wm*32 + 16*(i/4) + 4*tm + i%4.
+template <int STAGES, int PRODUCER, int MATH, int BN = kBN, bool SCALED = false, bool AMN = false>
 __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), ffma_min_blocks<PRODUCER>())
     sgemm_ffma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                       const FfmaParams p) {
     // 128 accumulators per thread need the consumer register budget of the
     // register split.
     constexpr bool kFused = PRODUCER == kProducerFused;
+    static_assert(!AMN || PRODUCER == kProducerTma, "transposed A: TMA producer warp only");
     static_assert((BN == kBN && !kFused) || (BN == kBNWide && PRODUCER == kProducerTmaWg) ||
                       (BN == kBNFused && kFused),
                   "tile width");
@@ -304,7 +310,9 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), ffma_min_blocks<PROD
                 const int k0 = kt * kBK;
                 if (kTma) {
                     mbar_arrive_expect_tx(full_bar(s), kStageBytes);
-                    if (mcast > 1) {
+                    if (AMN) {  // (no multicast: the host pairs no CTAs for transposed A)
+                        tma_load_2d(sA0 + s * kStageABytes, &tmA, full_bar(s), m0, k0);
+                    } else if (mcast > 1) {
                         // This CTA fetches rows [crank*64, crank*64+64) of the A
                         // slice and multicasts them into both CTAs of the pair.
                         const uint32_t half = static_cast<uint32_t>(kStageABytes / 2) * crank;
@@ -406,16 +414,21 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), ffma_min_blocks<PROD
     // [4 floats]; element group e4 = i*H + h holds acc[i][2h] and
     // acc[i][2h+1] (four columns).  Consecutive threads touch consecutive 16-byte words, so
     // every partial store and load is conflict-free and coalesced.
+    // Output row of the thread's accumulator row i within the tile.
+    auto row_in_tile = [&](int i) {
+        return AMN ? wm * 32 + 16 * (i >> 2) + 4 * tm + (i & 3) : wm * 32 + tm + 4 * i;
+    };
+
     // C (beta != 0 only): the thread's 8 x H four-column segments of the
     // tile, prefetched into L2 when the CTA starts the segment it will store,
     // so that the epilogue's reads of the old C do not wait on HBM.
     const bool read_c = SCALED && p.beta != 0.f;
     auto prefetch_c = [&](int tile) {
-        const int row0 = (tile / p.tiles_n) * kBM + wm * 32 + tm;
+        const int row0 = (tile / p.tiles_n) * kBM;
         const int col0 = (tile % p.tiles_n) * BN + wn * (BN / WN) + tn * 4;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            const int r = row0 + 4 * i;
+            const int r = row0 + row_in_tile(i);
 #pragma unroll
             for (int h = 0; h < H; ++h)
                 if (r < p.M && col0 + 32 * h < p.N)
@@ -423,11 +436,11 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), ffma_min_blocks<PROD
         }
     };
     auto store_c_plain = [&](int tile) {
-        const int row0 = (tile / p.tiles_n) * kBM + wm * 32 + tm;
+        const int row0 = (tile / p.tiles_n) * kBM;
         const int col0 = (tile % p.tiles_n) * BN + wn * (BN / WN) + tn * 4;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            const int r = row0 + 4 * i;
+            const int r = row0 + row_in_tile(i);
             if (r >= p.M) continue;
             float* crow = p.C + static_cast<long long>(r) * p.ldc;
 #pragma unroll
@@ -447,7 +460,7 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), ffma_min_blocks<PROD
         }
     };
     auto store_c_scaled = [&](int tile) {
-        const int row0 = (tile / p.tiles_n) * kBM + wm * 32 + tm;
+        const int row0 = (tile / p.tiles_n) * kBM;
         const int col0 = (tile % p.tiles_n) * BN + wn * (BN / WN) + tn * 4;
         // Rows in groups of RG: with beta != 0 the group's old C values are
         // all loaded before any of its stores, so the loads are in flight
@@ -459,7 +472,7 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), ffma_min_blocks<PROD
             float4 o[RG][H];
 #pragma unroll
             for (int ii = 0; ii < RG; ++ii) {
-                const int r = row0 + 4 * (i0 + ii);
+                const int r = row0 + row_in_tile(i0 + ii);
                 const float* crow = p.C + static_cast<long long>(r) * p.ldc;
 #pragma unroll
                 for (int h = 0; h < H; ++h) {
@@ -479,7 +492,7 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), ffma_min_blocks<PROD
 #pragma unroll
             for (int ii = 0; ii < RG; ++ii) {
                 const int i = i0 + ii;
-                const int r = row0 + 4 * i;
+                const int r = row0 + row_in_tile(i);
                 if (r >= p.M) continue;
                 float* crow = p.C + static_cast<long long>(r) * p.ldc;
 #pragma unroll
@@ -535,7 +548,8 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), ffma_min_blocks<PROD
     {
         // Byte offsets inside a stage.  A row r = wm*32 + tm + 4i has r mod 8 =
         // tm + 4*(i & 1), so even i share one swizzle key and odd i the other.
-        const uint32_t a_row0 = static_cast<uint32_t>((wm * 32 + tm) * 128);
+        const uint32_t a_row0 =
+            AMN ? static_cast<uint32_t>((wm * 32 + 4 * tm) * 4) : static_cast<uint32_t>((wm * 32 + tm) * 128);
         const uint32_t b_col0 = static_cast<uint32_t>((wn * (BN / WN) + tn * 4) * 4);
         const uint8_t* const smem_a = smem + a_row0;                          // generic pointers
         const uint8_t* const smem_b = smem + STAGES * kStageABytes + b_col0;  // for the vector loads
@@ -600,12 +614,21 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), ffma_min_blocks<PROD
                     const uint32_t xe = static_cast<uint32_t>(((kg ^ tm) & 7) << 4);
                     const uint32_t xo = xe ^ 64u;
                     float4 a[8];
+                    if (!AMN) {
 #pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        a[i] = *reinterpret_cast<const float4*>(sa + i * 512 + ((i & 1) ? xo : xe));
+                        for (int i = 0; i < 8; ++i)
+                            a[i] = *reinterpret_cast<const float4*>(sa + i * 512 + ((i & 1) ? xo : xe));
+                    }
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
                         const int k = kg * 4 + kk;
+                        float am[8];  // AMN: rows 4*tm + {0..3} and 16 + 4*tm + {0..3} at this k
+                        if (AMN) {
+                            const float4 a0 = *reinterpret_cast<const float4*>(sa + k * (kBM * 4));
+                            const float4 a1 = *reinterpret_cast<const float4*>(sa + k * (kBM * 4) + 64);
+                            am[0] = a0.x, am[1] = a0.y, am[2] = a0.z, am[3] = a0.w;
+                            am[4] = a1.x, am[5] = a1.y, am[6] = a1.z, am[7] = a1.w;
+                        }
                         float2 bp[TQ];
 #pragma unroll
                         for (int h = 0; h < H; ++h) {
@@ -620,7 +643,11 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), ffma_min_blocks<PROD
 #pragma unroll
                             for (int i0 = 0; i0 < 8; ++i0) {
                                 const int i = (q & 1) ? 7 - i0 : i0;  // serpentine: A value reused across q
-                                const float av = kk == 0 ? a[i].x : kk == 1 ? a[i].y : kk == 2 ? a[i].z : a[i].w;
+                                const float av = AMN        ? am[i]
+                                                 : kk == 0 ? a[i].x
+                                                 : kk == 1 ? a[i].y
+                                                 : kk == 2 ? a[i].z
+                                                           : a[i].w;
                                 if (MATH == kMathFfma2) {
                                     acc[i][q] = __ffma2_rn(make_float2(av, av), bp[q], acc[i][q]);
                                 } else {

@@ -335,12 +335,51 @@ def test_variant_choice():
     assert "/tail" not in desc(4096, 4096, 4096)  # the tail split is opt-in
     assert "/sk" in desc(8192, 128, 8192) and "/sk" in desc(128, 8192, 16384)
     assert "/sk" not in desc(256, 256, 256) and "/s1/" not in desc(256, 256, 256)  # tiny: cluster split-K
-    # 1027-float rows are not 16-byte multiples: the operands are repacked
-    # into pitched rows and the tensor-map path runs; small products read the
-    # rows as they are with cp.async
+    # large products run on a transposed copy of A (the transposed-A kernels)
+    assert desc(4096, 4096, 4096).endswith("/at") and desc(2048, 2048, 2048).endswith("/at")
+    assert not desc(8192, 128, 8192).endswith("/at")  # N < 512: A read as stored
+    # 1027-float rows are not 16-byte multiples: A's transposed copy and B's
+    # repacked copy have pitched rows, and the tensor-map path runs; small
+    # products read the rows as they are with cp.async
     assert desc(1023, 1025, 1027).startswith("tma/") and desc(1023, 1025, 1027).endswith("/repackAB")
     assert desc(300, 500, 701).startswith("cpasync/")
-    assert desc(2048, 2049, 2048).endswith("/repackB")
+    assert desc(2048, 2049, 2048).endswith("/repackB/at")
+    assert not desc(1024, 1024, 1024).endswith("/at")  # 2^31 flop: the copy launch does not pay
+
+
+# ---------------------------------------------------------------- A's layout
+
+@pytest.mark.parametrize("shape", [(300, 500, 700), (257, 190, 333), (129, 130, 4), (1, 700, 64), (513, 64, 1000)])
+@pytest.mark.parametrize("dist", ["uniform", "int"])
+def test_forced_transposed_a(shape, dist):
+    """a_layout = 2: A copied transposed (pitch M rounded up to 4) and read by
+    the transposed-A kernel, whose threads own rows 16*(i/4) + 4*tm + i%4."""
+    M, N, K = shape
+    A, B = make_operands(M, N, K, dist, 95)
+    C = run(A, B, a_layout=2)
+    C64, bound = oracle.gemm_f64(A.numpy(), B.numpy(), with_bound=(dist != "int"))
+    check(C, C64, bound, exact=(dist == "int"), what=f"a_layout 2 {shape} {dist}")
+
+
+@pytest.mark.parametrize("opt", [dict(a_layout=2, stream_k=2), dict(a_layout=2, stream_k=1, split_k=1),
+                                 dict(a_layout=2, split_k=3), dict(a_layout=1)])
+def test_transposed_a_schedules(opt):
+    """The transposed-A kernel under each schedule (stream-K, plain grid,
+    cluster split-K), and a_layout = 1 (A as stored) on a size that would
+    otherwise be transposed."""
+    A, B = make_operands(700, 900, 1100, "uniform", 96)
+    C = run(A, B, **opt)
+    C64, bound = oracle.gemm_f64(A.numpy(), B.numpy())
+    check(C, C64, bound, exact=False, what=str(opt))
+
+
+def test_transposed_a_rejects_forced_kernel_choices():
+    A, B = make_operands(128, 128, 64, "uniform", 97)
+    dA, dB = to_device(A), to_device(B)
+    for bad in (dict(a_layout=2, producer=2), dict(a_layout=2, tile_n=256), dict(a_layout=2, multicast=2),
+                dict(a_layout=3)):
+        with pytest.raises(g._lib.SgemmError):
+            g.sgemm_f32_ex(dA, dB, **bad)
 
 
 # ---------------------------------------------------------------- repacking
@@ -387,7 +426,7 @@ def test_repacked_large_ragged_sampled_rows():
     M, N, K = 2047, 2049, 2051
     A, B = make_operands(M, N, K, "uniform", 93)
     dA, dB = to_device(A), to_device(B)
-    assert g.describe(dA, dB).endswith("/repackAB")
+    assert g.describe(dA, dB).endswith("/repackB/at")  # 2^34 flop: A copied transposed, B repacked
     C = g.sgemm_f32(dA, dB)
     torch.cuda.synchronize()
     rows = sample_rows(M, n_random=8, seed=93)
