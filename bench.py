@@ -450,6 +450,7 @@ SWEEP_OPTIONS = [
     {"tile_n": 64, "split_k": 1},
     {"repack": 1},
     {"a_layout": 1},
+    {"a_layout": 2, "tile_n": 256},
     {"split_k": 1},
     {"split_k": 2},
     {"split_k": 4},

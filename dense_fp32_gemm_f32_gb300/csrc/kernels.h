@@ -20,6 +20,8 @@ KernelEntry ffma_kernel_tma_wg(int stages, int math);
 // 128 x 256 tiles (8 x 16 accumulators per thread) with the producer
 // warpgroup and the register split; stages in {2,3,4}.
 KernelEntry ffma_kernel_tma_wide(int stages, int math);
+// The same on A stored transposed (K x M): 2 stages, paired FMA.
+KernelEntry ffma_kernel_tma_wide_amn(int stages, int math);
 // Fused-producer FFMA kernels: 4-warp CTAs (no producer warp; thread 0
 // issues the TMA copies), 128 x 64 tiles, two CTAs per SM; stages in {2,3,4}.
 KernelEntry ffma_kernel_tma_fused(int stages, int math);

@@ -129,7 +129,8 @@ int init_device(int dev, DeviceState& st) {
             // setmaxnreg.inc waits until the registers it asks for are free;
             // the split adds up to kRegsLaunch per thread of the CTA, so a
             // kernel built with any other count must never be launched.
-            const KernelEntry split_kernels[2] = {ffma_kernel_tma_wg(s, math), ffma_kernel_tma_wide(s, math)};
+            const KernelEntry split_kernels[3] = {ffma_kernel_tma_wg(s, math), ffma_kernel_tma_wide(s, math),
+                                                  ffma_kernel_tma_wide_amn(s, math)};
             for (const KernelEntry& wg : split_kernels) {
                 if (!wg.fn) {
                     if (&wg == &split_kernels[0]) st.regsplit_ok = false;
@@ -381,8 +382,9 @@ bool is_tma(int producer) {
 }
 
 KernelEntry ffma_kernel(const Plan& pl) {
-    if (pl.a_mn) return pl.producer == kProducerTma ? ffma_kernel_amn(pl.stages, pl.math, false)
-                                                    : KernelEntry{nullptr, 0, 0};
+    if (pl.a_mn) return pl.producer == kProducerTma     ? ffma_kernel_amn(pl.stages, pl.math, false)
+                        : pl.producer == kProducerTmaWg ? ffma_kernel_tma_wide_amn(pl.stages, pl.math)
+                                                        : KernelEntry{nullptr, 0, 0};
     if (pl.producer == kProducerFused) return ffma_kernel_tma_fused(pl.stages, pl.math);
     if (pl.bn == kBNWide) return pl.producer == kProducerTmaWg ? ffma_kernel_tma_wide(pl.stages, pl.math)
                                                                 : KernelEntry{nullptr, 0, 0};
@@ -414,8 +416,9 @@ int make_plan(const DeviceState& st, int M, int N, int K, const float* A, int ld
     Plan pl;
     // Transposed A (general entry only): tensor-map readable A, TMA producer
     // warp, 2 stages, paired FMA, no multicast (see below).
-    if (a_mn && (K == 0 || !tma_ok(A, lda) || (opt && (opt->producer || opt->tile_n || opt->math || opt->stages ||
-                                                        opt->multicast == 2))))
+    if (a_mn && (K == 0 || !tma_ok(A, lda) ||
+                 (opt && (opt->producer || (opt->tile_n && opt->tile_n != kBNWide) || opt->math || opt->stages ||
+                          opt->multicast == 2))))
         return SGEMM_ERR_INVALID_ARG;
     pl.a_mn = a_mn;
     pl.num_k_tiles = static_cast<int>(ceil_div(K, kBK));
@@ -694,7 +697,8 @@ int run_ffma(int M, int N, int K, const float* A, int lda, const float* B, int l
     };
 
     const bool scaled = scale && (scale->alpha != 1.f || scale->beta != 0.f);
-    const KernelEntry k = pl.a_mn ? ffma_kernel_amn(pl.stages, pl.math, scaled)
+    const KernelEntry k = pl.a_mn ? (pl.bn == kBN ? ffma_kernel_amn(pl.stages, pl.math, scaled)
+                                                  : scaled ? KernelEntry{nullptr, 0, 0} : ffma_kernel(pl))
                           : scaled ? (pl.bn == kBN ? ffma_kernel_scaled(pl.producer, pl.stages, pl.math)
                                                    : KernelEntry{nullptr, 0, 0})
                                    : ffma_kernel(pl);

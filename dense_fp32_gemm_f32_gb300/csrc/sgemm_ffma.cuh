@@ -177,7 +177,8 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), ffma_min_blocks<PROD
     // 128 accumulators per thread need the consumer register budget of the
     // register split.
     constexpr bool kFused = PRODUCER == kProducerFused;
-    static_assert(!AMN || PRODUCER == kProducerTma, "transposed A: TMA producer warp only");
+    static_assert(!AMN || PRODUCER == kProducerTma || PRODUCER == kProducerTmaWg,
+                  "transposed A: tensor-map producers only");
     static_assert((BN == kBN && !kFused) || (BN == kBNWide && PRODUCER == kProducerTmaWg) ||
                       (BN == kBNFused && kFused),
                   "tile width");

@@ -1,5 +1,6 @@
 // Instantiations of the FFMA kernel on 128 x 256 tiles (8 x 16 accumulators
-// per consumer thread), TMA producer warpgroup with the register split.
+// per consumer thread), TMA producer warpgroup with the register split; A as
+// stored, and (2 stages, paired FMA) A stored transposed.
 #include "kernels.h"
 #include "sgemm_ffma.cuh"
 
@@ -26,6 +27,12 @@ KernelEntry ffma_kernel_tma_wide(int stages, int math) {
         }
     }
     return {nullptr, 0, 0};
+}
+
+KernelEntry ffma_kernel_tma_wide_amn(int stages, int math) {
+    if (math != kMathFfma2 || stages != 2) return {nullptr, 0, 0};
+    return {reinterpret_cast<const void*>(&sgemm_ffma_kernel<2, kProducerTmaWg, kMathFfma2, kBNWide, false, true>),
+            ffma_smem_bytes<2, kBNWide>(), ffma_threads<kProducerTmaWg>()};
 }
 
 }  // namespace gb300

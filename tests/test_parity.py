@@ -362,7 +362,8 @@ def test_forced_transposed_a(shape, dist):
 
 
 @pytest.mark.parametrize("opt", [dict(a_layout=2, stream_k=2), dict(a_layout=2, stream_k=1, split_k=1),
-                                 dict(a_layout=2, split_k=3), dict(a_layout=1)])
+                                 dict(a_layout=2, split_k=3), dict(a_layout=1), dict(a_layout=2, tile_n=256),
+                                 dict(a_layout=2, tile_n=256, stream_k=2)])
 def test_transposed_a_schedules(opt):
     """The transposed-A kernel under each schedule (stream-K, plain grid,
     cluster split-K), and a_layout = 1 (A as stored) on a size that would
@@ -376,7 +377,7 @@ def test_transposed_a_schedules(opt):
 def test_transposed_a_rejects_forced_kernel_choices():
     A, B = make_operands(128, 128, 64, "uniform", 97)
     dA, dB = to_device(A), to_device(B)
-    for bad in (dict(a_layout=2, producer=2), dict(a_layout=2, tile_n=256), dict(a_layout=2, multicast=2),
+    for bad in (dict(a_layout=2, producer=2), dict(a_layout=2, tile_n=64), dict(a_layout=2, multicast=2),
                 dict(a_layout=3)):
         with pytest.raises(g._lib.SgemmError):
             g.sgemm_f32_ex(dA, dB, **bad)
