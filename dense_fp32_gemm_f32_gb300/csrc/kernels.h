@@ -22,6 +22,9 @@ KernelEntry ffma_kernel_tma_wg(int stages, int math);
 KernelEntry ffma_kernel_tma_wide(int stages, int math);
 // The same on A stored transposed (K x M): 2 stages, paired FMA.
 KernelEntry ffma_kernel_tma_wide_amn(int stages, int math);
+// FFMA kernels with A transposed in shared memory by a second producer warp
+// (128 x 128 tiles, stages in {2,3,4}; scaled epilogue: 2 stages, paired FMA).
+KernelEntry ffma_kernel_tma_x(int stages, int math, bool scaled);
 // Fused-producer FFMA kernels: 4-warp CTAs (no producer warp; thread 0
 // issues the TMA copies), 128 x 64 tiles, two CTAs per SM; stages in {2,3,4}.
 KernelEntry ffma_kernel_tma_fused(int stages, int math);

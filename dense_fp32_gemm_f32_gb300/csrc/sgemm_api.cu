@@ -160,8 +160,10 @@ int init_device(int dev, DeviceState& st) {
         for (int s = 1; s <= 6; ++s) {
             for (int prod : {static_cast<int>(kProducerTma), static_cast<int>(kProducerCpAsync)})
                 if (set_smem_attr(ffma_kernel_scaled(prod, s, math)) != SGEMM_OK) return SGEMM_ERR_CUDA;
-            for (bool scaled : {false, true})
+            for (bool scaled : {false, true}) {
                 if (set_smem_attr(ffma_kernel_amn(s, math, scaled)) != SGEMM_OK) return SGEMM_ERR_CUDA;
+                if (set_smem_attr(ffma_kernel_tma_x(s, math, scaled)) != SGEMM_OK) return SGEMM_ERR_CUDA;
+            }
         }
     }
     if (set_smem_attr(tf32x3_kernel()) != SGEMM_OK || set_smem_attr(tf32x3_direct_kernel()) != SGEMM_OK)
@@ -319,16 +321,21 @@ struct Repacked {
     }
 };
 
-// A read in the transposed layout (sgemm_options.a_layout): the
-// transposed-A kernels' consumers read each k's A values as two 16-byte
-// vectors instead of a 4-k vector per row.  Measured on GB300, with the
-// transposing copy (one read and one write of A) included: 4096^3 65.5 ->
-// 68.5 TFLOP/s, 8192^3 66.3 -> 71.2, 128 x 8192 x 16384 64.3 -> 68.3,
-// 4096 x 4096 x 256 58.0 -> 59.2, 2048^3 even, 1024^3 43.1 -> 40.6 (the copy
-// launch does not pay there).  Automatic when no variant is forced, N >= 512
-// (the copy is small next to the product) and 2MNK >= 2^33.
+// A read in the transposed layout: the consumers read each k's A values as
+// two 16-byte vectors instead of a 4-k vector per row (82 -> 89 % FMA-pipe
+// duty).  Two ways to get there: a transposing copy of A in HBM
+// (sgemm_options.a_layout = 2; the transposed-A kernels, no extra work in
+// the kernel) or a second producer warp transposing each A slice in shared
+// memory (SGEMM_PRODUCER_TMA_X; no copy, a little more shared-memory traffic
+// in the kernel).  Measured on GB300 (TFLOP/s, A read as stored / copy in HBM
+// / transposed in shared memory): 2048^3 62.0 / 62.7 / 65.4, 4096^3 65.4 /
+// 68.5 / 69.2, 8192^3 66.4 / 71.1 / 69.8, 128 x 8192 x 16384 64.2 / 68.2 /
+// 67.0, 8192 x 128 x 8192 62.0 / - / 64.7.  The copy costs one read and one
+// write of A, i.e. ~1/N of the product; it is taken automatically when no
+// variant is forced, N >= 6144 and 2MNK >= 2^33, and the transposition in
+// shared memory otherwise (make_plan).
 constexpr double kTransposeMinFlops = 8589934592.0;
-constexpr int kTransposeMinN = 512;
+constexpr int kTransposeMinN = 6144;
 
 bool options_force_variant(const sgemm_options* opt) {
     return opt && (opt->producer || opt->split_k || opt->multicast || opt->math || opt->stages || opt->tail_split ||
@@ -378,7 +385,8 @@ constexpr double kRepackMinFlops = 1073741824.0;  // 2^30
 long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
 
 bool is_tma(int producer) {
-    return producer == kProducerTma || producer == kProducerTmaWg || producer == kProducerFused;
+    return producer == kProducerTma || producer == kProducerTmaWg || producer == kProducerFused ||
+           producer == kProducerTmaX;
 }
 
 KernelEntry ffma_kernel(const Plan& pl) {
@@ -386,6 +394,7 @@ KernelEntry ffma_kernel(const Plan& pl) {
                         : pl.producer == kProducerTmaWg ? ffma_kernel_tma_wide_amn(pl.stages, pl.math)
                                                         : KernelEntry{nullptr, 0, 0};
     if (pl.producer == kProducerFused) return ffma_kernel_tma_fused(pl.stages, pl.math);
+    if (pl.producer == kProducerTmaX) return ffma_kernel_tma_x(pl.stages, pl.math, false);
     if (pl.bn == kBNWide) return pl.producer == kProducerTmaWg ? ffma_kernel_tma_wide(pl.stages, pl.math)
                                                                 : KernelEntry{nullptr, 0, 0};
     switch (pl.producer) {
@@ -401,6 +410,7 @@ const char* producer_name(int producer) {
         case kProducerTma: return "tma";
         case kProducerTmaWg: return "tmawg";
         case kProducerFused: return "fused";
+        case kProducerTmaX: return "tmax";
         case kProducerCpAsync: return "cpasync";
     }
     return "?";
@@ -445,13 +455,20 @@ int make_plan(const DeviceState& st, int M, int N, int K, const float* A, int ld
         if (!aligned) return SGEMM_ERR_INVALID_ARG;
         if (!st.regsplit_ok) return SGEMM_ERR_UNSUPPORTED;
         pl.producer = kProducerTmaWg;
+    } else if (want_prod == SGEMM_PRODUCER_TMA_X) {
+        if (!aligned || a_mn) return SGEMM_ERR_INVALID_ARG;
+        pl.producer = kProducerTmaX;
     } else if (want_prod == SGEMM_PRODUCER_FUSED) {
         if (!aligned) return SGEMM_ERR_INVALID_ARG;
         pl.producer = kProducerFused;
     } else if (want_prod == SGEMM_PRODUCER_CPASYNC) {
         pl.producer = kProducerCpAsync;
     } else if (want_prod == SGEMM_PRODUCER_AUTO) {
-        pl.producer = aligned ? kProducerTma : kProducerCpAsync;
+        // Tensor maps: A transposed in shared memory, unless it already is in
+        // HBM (a_mn) or another choice rules the second producer warp out.
+        const bool x_ok = !a_mn && !(opt && (opt->multicast == 2 || (opt->tile_n && opt->tile_n != kBN) ||
+                                             (opt->stages && (opt->stages < 2 || opt->stages > 4))));
+        pl.producer = !aligned ? kProducerCpAsync : x_ok ? kProducerTmaX : kProducerTma;
     } else {
         return SGEMM_ERR_INVALID_ARG;
     }
@@ -497,7 +514,9 @@ int make_plan(const DeviceState& st, int M, int N, int K, const float* A, int ld
         pl.stages = 4;
     }
     if (pl.producer == kProducerFused && !(opt && opt->stages)) pl.stages = 4;
-    if ((pl.bn == kBNWide || pl.bn == kBNFused) && (pl.stages < 2 || pl.stages > 4)) return SGEMM_ERR_INVALID_ARG;
+    if ((pl.bn == kBNWide || pl.bn == kBNFused || pl.producer == kProducerTmaX) && (pl.stages < 2 || pl.stages > 4))
+        return SGEMM_ERR_INVALID_ARG;
+    if (pl.producer == kProducerTmaX && pl.bn != kBN) return SGEMM_ERR_INVALID_ARG;
     // CTAs that can be resident at once, for the stream-K grid.
     const int per_sm = pl.producer == kProducerFused ? st.fused_per_sm[pl.stages] : 1;
     if (per_sm < 1) return SGEMM_ERR_UNSUPPORTED;
@@ -546,7 +565,8 @@ int make_plan(const DeviceState& st, int M, int N, int K, const float* A, int ld
     // unless forced.
     const int want_mc = opt ? opt->multicast : 0;
     if (want_mc == 2) {
-        if (split > 1 || !is_tma(pl.producer) || pl.producer == kProducerFused) return SGEMM_ERR_INVALID_ARG;
+        if (split > 1 || !is_tma(pl.producer) || pl.producer == kProducerFused || pl.producer == kProducerTmaX)
+            return SGEMM_ERR_INVALID_ARG;
         if (st.max_clusters_pair < 1) return SGEMM_ERR_UNSUPPORTED;
         pl.mcast = 2;
     } else if (want_mc == 0 || want_mc == 1) {
@@ -699,8 +719,9 @@ int run_ffma(int M, int N, int K, const float* A, int lda, const float* B, int l
     const bool scaled = scale && (scale->alpha != 1.f || scale->beta != 0.f);
     const KernelEntry k = pl.a_mn ? (pl.bn == kBN ? ffma_kernel_amn(pl.stages, pl.math, scaled)
                                                   : scaled ? KernelEntry{nullptr, 0, 0} : ffma_kernel(pl))
-                          : scaled ? (pl.bn == kBN ? ffma_kernel_scaled(pl.producer, pl.stages, pl.math)
-                                                   : KernelEntry{nullptr, 0, 0})
+                          : scaled ? (pl.producer == kProducerTmaX ? ffma_kernel_tma_x(pl.stages, pl.math, true)
+                                      : pl.bn == kBN               ? ffma_kernel_scaled(pl.producer, pl.stages, pl.math)
+                                                                   : KernelEntry{nullptr, 0, 0})
                                    : ffma_kernel(pl);
     if (!k.fn) {
         release_pack();

@@ -55,7 +55,7 @@ constexpr int kBK = 32;
 constexpr int kConsumerWarps = 8;
 constexpr int kConsumerThreads = kConsumerWarps * 32;
 
-enum : int { kProducerTma = 1, kProducerCpAsync = 2, kProducerTmaWg = 3, kProducerFused = 4 };
+enum : int { kProducerTma = 1, kProducerCpAsync = 2, kProducerTmaWg = 3, kProducerFused = 4, kProducerTmaX = 5 };
 
 // Producer warps: one elected lane drives the TMA; the cp.async producer
 // issues every 4-byte copy itself, so it gets a full warpgroup.
@@ -76,9 +76,14 @@ enum : int { kProducerTma = 1, kProducerCpAsync = 2, kProducerTmaWg = 3, kProduc
 // compute (128 x 64 tiles), thread 0 issuing the TMA copies between its own
 // multiply-adds, so that two CTAs fit on an SM (2 x 128 threads may use up to
 // 255 registers each) and run independently of each other.
+//
+// kProducerTmaX: the TMA producer warp plus a transposing warp, which copies
+// each stage's A slice (as stored: 128 rows of 32 k) into a second slice with
+// m innermost (32 rows of 128 m) for the consumers to read per k as two
+// 16-byte vectors (the transposed-A read, without a copy of A in HBM).
 template <int PRODUCER>
 __host__ __device__ constexpr int ffma_producer_warps() {
-    return PRODUCER == kProducerFused ? 0 : PRODUCER == kProducerTma ? 1 : 4;
+    return PRODUCER == kProducerFused ? 0 : PRODUCER == kProducerTma ? 1 : PRODUCER == kProducerTmaX ? 2 : 4;
 }
 template <int PRODUCER>
 __host__ __device__ constexpr int ffma_consumer_warps() {
@@ -149,11 +154,12 @@ struct FfmaParams {
     float alpha, beta;
 };
 
-template <int STAGES, int BN = kBN>
+// XA: the stage also holds the transposed copy of its A slice (kProducerTmaX).
+template <int STAGES, int BN = kBN, bool XA = false>
 constexpr int ffma_smem_bytes() {
-    return (STAGES * ffma_stage_bytes<BN>() > ffma_partial_bytes<BN>() ? STAGES * ffma_stage_bytes<BN>()
-                                                                      : ffma_partial_bytes<BN>()) +
-           1024 /*align*/ + 256 /*barriers*/;
+    constexpr int stage = ffma_stage_bytes<BN>() + (XA ? kStageABytes : 0);
+    return (STAGES * stage > ffma_partial_bytes<BN>() ? STAGES * stage : ffma_partial_bytes<BN>()) + 1024 /*align*/ +
+           256 /*barriers*/;
 }
 
 // Physical byte offset of float (row r, column c) inside a 128-byte-swizzled
@@ -179,6 +185,10 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), ffma_min_blocks<PROD
     constexpr bool kFused = PRODUCER == kProducerFused;
     static_assert(!AMN || PRODUCER == kProducerTma || PRODUCER == kProducerTmaWg,
                   "transposed A: tensor-map producers only");
+    constexpr bool kX = PRODUCER == kProducerTmaX;  // A transposed in shared memory
+    static_assert(!(kX && AMN), "A is transposed either in HBM or in shared memory");
+    static_assert(!kX || BN == kBN, "in-shared-memory transposition: 128 x 128 tiles");
+    constexpr bool kAT = AMN || kX;  // consumers read A with m innermost
     static_assert((BN == kBN && !kFused) || (BN == kBNWide && PRODUCER == kProducerTmaWg) ||
                       (BN == kBNFused && kFused),
                   "tile width");
@@ -196,12 +206,17 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), ffma_min_blocks<PROD
     const uint32_t raw_base = smem_addr(smem_raw);
     const uint32_t base = (raw_base + 1023u) & ~1023u;
     uint8_t* const smem = smem_raw + (base - raw_base);
-    constexpr int kRingBytes = STAGES * kStageBytes > kPartialBytes ? STAGES * kStageBytes : kPartialBytes;
-    const uint32_t sA0 = base;                         // STAGES x 16 KiB
-    const uint32_t sB0 = base + STAGES * kStageABytes;  // STAGES x 16 KiB
-    const uint32_t bar0 = base + kRingBytes;           // full[STAGES], empty[STAGES]
+    constexpr int kSlotBytes = kStageBytes + (kX ? kStageABytes : 0);
+    constexpr int kRingBytes = STAGES * kSlotBytes > kPartialBytes ? STAGES * kSlotBytes : kPartialBytes;
+    // Ring: A slices (as loaded), [transposed A slices], B slices.
+    constexpr int kTOff = STAGES * kStageABytes;                       // transposed A (kX)
+    constexpr int kBOff = (kX ? 2 : 1) * STAGES * kStageABytes;        // B
+    const uint32_t sA0 = base;                                         // STAGES x 16 KiB
+    const uint32_t sB0 = base + kBOff;                                 // STAGES x kStageBBytes
+    const uint32_t bar0 = base + kRingBytes;  // full[STAGES], empty[STAGES], tfull[STAGES]
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+    auto tfull_bar = [&](int s) { return bar0 + 8u * (2 * STAGES + s); };  // transposed A ready
 
     constexpr bool kTma = PRODUCER != kProducerCpAsync;
     const int warp = threadIdx.x >> 5;
@@ -259,10 +274,12 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), ffma_min_blocks<PROD
 
     if (threadIdx.x == 0) {
         const uint32_t full_count = kTma ? 1u : 32u * PW;
-        const uint32_t empty_count = static_cast<uint32_t>(CW * mcast);
+        // (kX: the transposing warp also releases each slot, for its A slice.)
+        const uint32_t empty_count = static_cast<uint32_t>(CW * mcast + (kX ? 1 : 0));
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full_bar(s), full_count);
             mbar_init(empty_bar(s), empty_count);
+            if (kX) mbar_init(tfull_bar(s), 32u);  // every lane of the transposing warp
         }
         fence_mbarrier_init();
     }
@@ -289,6 +306,45 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), ffma_min_blocks<PROD
         // first; the consumers' requests are served from what it released.
         if constexpr (PRODUCER == kProducerTmaWg) setmaxnreg_dec<kRegsProducer>();
         const bool issuer = !kTma || (pw == 0 && lane == 0);
+        if (kX && pw == 1) {
+            // Transposing warp: A slice s (row m: 32 floats in 128-byte
+            // swizzled chunks) -> transposed slice (row k: 128 floats).  Lane
+            // l takes rows l, l + 32, l + 64, l + 96: a 16-byte read of chunk c
+            // covers k = 4c..4c+3 of one row (the 8 lanes of each wavefront hit
+            // 8 different chunk positions), and each of its 4 floats is stored
+            // to row k at column m (32 consecutive floats per store).
+            int xit = 0;
+            Work xwork = work0;
+            int xtile, xkb, xke;
+            while (!timed_out && xwork.next(xtile, xkb, xke)) {
+                for (int kt = xkb; kt < xke; ++kt, ++xit) {
+                    const int s = xit % STAGES;
+                    const int round = xit / STAGES;
+                    if (!mbar_wait_bounded_warp(full_bar(s), round & 1, tmo)) {
+                        timed_out = true;
+                        break;
+                    }
+                    const uint8_t* const raw = smem + s * kStageABytes;
+                    float* const tr = reinterpret_cast<float*>(smem + kTOff + s * kStageABytes);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int m = lane + 32 * q;
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) {
+                            const float4 v =
+                                *reinterpret_cast<const float4*>(raw + m * 128 + (((c ^ m) & 7) << 4));
+                            tr[(4 * c + 0) * kBM + m] = v.x;
+                            tr[(4 * c + 1) * kBM + m] = v.y;
+                            tr[(4 * c + 2) * kBM + m] = v.z;
+                            tr[(4 * c + 3) * kBM + m] = v.w;
+                        }
+                    }
+                    __syncwarp();
+                    mbar_arrive(tfull_bar(s));           // transposed slice written (every lane)
+                    if (lane == 0) mbar_arrive(empty_bar(s));  // A slice read
+                }
+            }
+        }
         int issued_round[STAGES];
 #pragma unroll
         for (int s = 0; s < STAGES; ++s) issued_round[s] = -1;
@@ -417,7 +473,7 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), ffma_min_blocks<PROD
     // every partial store and load is conflict-free and coalesced.
     // Output row of the thread's accumulator row i within the tile.
     auto row_in_tile = [&](int i) {
-        return AMN ? wm * 32 + 16 * (i >> 2) + 4 * tm + (i & 3) : wm * 32 + tm + 4 * i;
+        return kAT ? wm * 32 + 16 * (i >> 2) + 4 * tm + (i & 3) : wm * 32 + tm + 4 * i;
     };
 
     // C (beta != 0 only): the thread's 8 x H four-column segments of the
@@ -549,11 +605,11 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), ffma_min_blocks<PROD
     {
         // Byte offsets inside a stage.  A row r = wm*32 + tm + 4i has r mod 8 =
         // tm + 4*(i & 1), so even i share one swizzle key and odd i the other.
-        const uint32_t a_row0 =
-            AMN ? static_cast<uint32_t>((wm * 32 + 4 * tm) * 4) : static_cast<uint32_t>((wm * 32 + tm) * 128);
+        const uint32_t a_row0 = kAT ? static_cast<uint32_t>((kX ? kTOff : 0) + (wm * 32 + 4 * tm) * 4)
+                                    : static_cast<uint32_t>((wm * 32 + tm) * 128);
         const uint32_t b_col0 = static_cast<uint32_t>((wn * (BN / WN) + tn * 4) * 4);
         const uint8_t* const smem_a = smem + a_row0;                          // generic pointers
-        const uint8_t* const smem_b = smem + STAGES * kStageABytes + b_col0;  // for the vector loads
+        const uint8_t* const smem_b = smem + kBOff + b_col0;  // for the vector loads
 
         // Fused producer (thread 0 of a kProducerFused CTA): the loads follow
         // the same work sequence as the computation.  STAGES loads go out
@@ -604,7 +660,8 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), ffma_min_blocks<PROD
                 const int s = it % STAGES;
                 const int round = it / STAGES;
                 if (kFused && threadIdx.x == 0 && it > 0) issue_load();
-                if (!mbar_wait_bounded_warp(full_bar(s), round & 1, tmo)) {
+                if (!mbar_wait_bounded_warp(full_bar(s), round & 1, tmo) ||
+                    (kX && !mbar_wait_bounded_warp(tfull_bar(s), round & 1, tmo))) {
                     timed_out = true;
                     break;
                 }
@@ -615,7 +672,7 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), ffma_min_blocks<PROD
                     const uint32_t xe = static_cast<uint32_t>(((kg ^ tm) & 7) << 4);
                     const uint32_t xo = xe ^ 64u;
                     float4 a[8];
-                    if (!AMN) {
+                    if (!kAT) {
 #pragma unroll
                         for (int i = 0; i < 8; ++i)
                             a[i] = *reinterpret_cast<const float4*>(sa + i * 512 + ((i & 1) ? xo : xe));
@@ -623,8 +680,8 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), ffma_min_blocks<PROD
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
                         const int k = kg * 4 + kk;
-                        float am[8];  // AMN: rows 4*tm + {0..3} and 16 + 4*tm + {0..3} at this k
-                        if (AMN) {
+                        float am[8];  // kAT: rows 4*tm + {0..3} and 16 + 4*tm + {0..3} at this k
+                        if (kAT) {
                             const float4 a0 = *reinterpret_cast<const float4*>(sa + k * (kBM * 4));
                             const float4 a1 = *reinterpret_cast<const float4*>(sa + k * (kBM * 4) + 64);
                             am[0] = a0.x, am[1] = a0.y, am[2] = a0.z, am[3] = a0.w;
@@ -644,7 +701,7 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), ffma_min_blocks<PROD
 #pragma unroll
                             for (int i0 = 0; i0 < 8; ++i0) {
                                 const int i = (q & 1) ? 7 - i0 : i0;  // serpentine: A value reused across q
-                                const float av = AMN        ? am[i]
+                                const float av = kAT        ? am[i]
                                                  : kk == 0 ? a[i].x
                                                  : kk == 1 ? a[i].y
                                                  : kk == 2 ? a[i].z

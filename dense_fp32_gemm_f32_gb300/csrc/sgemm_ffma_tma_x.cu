@@ -1,0 +1,32 @@
+// Instantiations of the FFMA kernel with A transposed in shared memory
+// (kProducerTmaX: TMA producer warp + transposing warp); 128 x 128 tiles.
+#include "kernels.h"
+#include "sgemm_ffma.cuh"
+
+namespace gb300 {
+
+template <int S, int MATH, bool SCALED>
+static KernelEntry entry() {
+    return {reinterpret_cast<const void*>(&sgemm_ffma_kernel<S, kProducerTmaX, MATH, kBN, SCALED>),
+            ffma_smem_bytes<S, kBN, true>(), ffma_threads<kProducerTmaX>()};
+}
+
+KernelEntry ffma_kernel_tma_x(int stages, int math, bool scaled) {
+    if (scaled) return (stages == 2 && math == kMathFfma2) ? entry<2, kMathFfma2, true>() : KernelEntry{nullptr, 0, 0};
+    if (math == kMathFfma) {
+        switch (stages) {
+            case 2: return entry<2, kMathFfma, false>();
+            case 3: return entry<3, kMathFfma, false>();
+            case 4: return entry<4, kMathFfma, false>();
+        }
+    } else if (math == kMathFfma2) {
+        switch (stages) {
+            case 2: return entry<2, kMathFfma2, false>();
+            case 3: return entry<3, kMathFfma2, false>();
+            case 4: return entry<4, kMathFfma2, false>();
+        }
+    }
+    return {nullptr, 0, 0};
+}
+
+}  // namespace gb300

@@ -215,10 +215,15 @@ enum {
                                     registers split between the warpgroups (producer 40,
                                     consumers 232 per thread); SGEMM_ERR_UNSUPPORTED if the
                                     library's build of that kernel does not allow the split */
-    SGEMM_PRODUCER_FUSED = 4     /* no producer warp: 4-warp CTAs on 128 x 64 tiles, two per SM,
+    SGEMM_PRODUCER_FUSED = 4,    /* no producer warp: 4-warp CTAs on 128 x 64 tiles, two per SM,
                                     thread 0 issuing the tensor-map copies between its own
                                     multiply-adds (implies tile_n = 64; 2..4 stages, default 4;
                                     no split-K clusters, no multicast) */
+    SGEMM_PRODUCER_TMA_X = 5     /* tensor-map copies, and a second producer warp that
+                                    transposes each stage's A slice in shared memory for the
+                                    consumers to read per k (the transposed-A read without a
+                                    copy of A in HBM; 128 x 128 tiles, 2..4 stages, no
+                                    multicast) */
 };
 
 /*
@@ -270,8 +275,10 @@ typedef struct sgemm_options {
                              workspace of K x M4 floats) and run the
                              transposed-A kernel, whose consumers read each
                              k's A values as two 16-byte vectors; auto = 2
-                             when no other option is forced, N >= 512 and
-                             2MNK >= 2^33 */
+                             when no other option is forced, N >= 6144 and
+                             2MNK >= 2^33 (otherwise the automatic producer
+                             transposes A in shared memory:
+                             SGEMM_PRODUCER_TMA_X) */
 } sgemm_options;
 
 /* sgemm_f32 with forced choices.  Same contract; an unsupported combination

@@ -107,6 +107,9 @@ VARIANTS = (
     + [dict(producer=4, math=m, stages=s, split_k=1) for m in (1, 2) for s in (2, 3, 4)]
     + [dict(tile_n=64, stream_k=2, math=m) for m in (1, 2)]
     + [dict(tile_n=64, stream_k=2, stages=2)]
+    # A transposed in shared memory by a second producer warp
+    + [dict(producer=5, math=m, stages=s, split_k=1) for m in (1, 2) for s in (2, 3, 4)]
+    + [dict(producer=5, stream_k=2), dict(producer=5, split_k=3)]
 )
 
 
@@ -330,21 +333,22 @@ def test_variant_choice():
     def desc(M, N, K):
         return g.describe(torch.empty((M, K), device="cuda"), torch.empty((K, N), device="cuda"))
 
-    assert desc(4096, 4096, 4096).startswith("tma/")
+    # A transposed in shared memory by the second producer warp ...
+    assert desc(4096, 4096, 4096).startswith("tmax/") and desc(2048, 2048, 2048).startswith("tmax/")
+    assert desc(8192, 128, 8192).startswith("tmax/") and desc(1024, 1024, 1024).startswith("tmax/")
+    # ... or, for wide products, copied transposed in HBM for the transposed-A kernel
+    assert desc(8192, 8192, 8192).startswith("tma/") and desc(8192, 8192, 8192).endswith("/at")
     assert "/s1/" in desc(4096, 4096, 4096) and "/sk" in desc(4096, 4096, 4096)  # stream-K
     assert "/tail" not in desc(4096, 4096, 4096)  # the tail split is opt-in
     assert "/sk" in desc(8192, 128, 8192) and "/sk" in desc(128, 8192, 16384)
     assert "/sk" not in desc(256, 256, 256) and "/s1/" not in desc(256, 256, 256)  # tiny: cluster split-K
-    # large products run on a transposed copy of A (the transposed-A kernels)
-    assert desc(4096, 4096, 4096).endswith("/at") and desc(2048, 2048, 2048).endswith("/at")
-    assert not desc(8192, 128, 8192).endswith("/at")  # N < 512: A read as stored
-    # 1027-float rows are not 16-byte multiples: A's transposed copy and B's
-    # repacked copy have pitched rows, and the tensor-map path runs; small
-    # products read the rows as they are with cp.async
-    assert desc(1023, 1025, 1027).startswith("tma/") and desc(1023, 1025, 1027).endswith("/repackAB")
+    # 1027-float rows are not 16-byte multiples: the operands are repacked
+    # into pitched rows and the tensor-map path runs; small products read the
+    # rows as they are with cp.async
+    assert desc(1023, 1025, 1027).startswith("tmax/") and desc(1023, 1025, 1027).endswith("/repackAB")
     assert desc(300, 500, 701).startswith("cpasync/")
-    assert desc(2048, 2049, 2048).endswith("/repackB/at")
-    assert not desc(1024, 1024, 1024).endswith("/at")  # 2^31 flop: the copy launch does not pay
+    assert desc(2048, 2049, 2048).endswith("/repackB")
+    assert desc(8192, 8193, 8192).endswith("/repackB/at")
 
 
 # ---------------------------------------------------------------- A's layout
@@ -427,7 +431,7 @@ def test_repacked_large_ragged_sampled_rows():
     M, N, K = 2047, 2049, 2051
     A, B = make_operands(M, N, K, "uniform", 93)
     dA, dB = to_device(A), to_device(B)
-    assert g.describe(dA, dB).endswith("/repackB/at")  # 2^34 flop: A copied transposed, B repacked
+    assert g.describe(dA, dB).endswith("/repackAB")
     C = g.sgemm_f32(dA, dB)
     torch.cuda.synchronize()
     rows = sample_rows(M, n_random=8, seed=93)
@@ -444,7 +448,7 @@ def test_timeout_is_reported_and_recovers():
     A, B = make_operands(128, 256, 256, "uniform", 14)
     dA, dB = to_device(A), to_device(B)
     assert g.check_status() == 0
-    for producer in (1, 2, 4):
+    for producer in (1, 2, 4, 5):
         g.sgemm_f32_ex(dA, dB, producer=producer, split_k=1, debug_skip_stage=3, timeout_ns=20_000_000)
         assert g.check_status() == 4
         g.sgemm_f32_ex(dA, dB, producer=producer, stream_k=2, debug_skip_stage=1, timeout_ns=20_000_000)
