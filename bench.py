@@ -148,24 +148,26 @@ class ClockSampler:
 # ----------------------------------------------------------------- oracle (CPU) timing
 
 def oracle_rows_rate(A, B, rows, threads):
-    """Times the oracle on whole rows; returns (seconds, flops)."""
+    """Times the oracle on whole rows with `threads` host threads; returns
+    (seconds, flops)."""
     import oracle
 
     t = time.perf_counter()
-    oracle.default().gemm_rows_f64(A, B, rows)
+    oracle.default().gemm_rows_f64(A, B, rows, threads=threads)
     dt = time.perf_counter() - t
     return dt, 2.0 * len(rows) * B.shape[1] * A.shape[1]
 
 
-def cpu_baseline(p, target_s: float = 12.0):
-    """The oracle, as it stands, on a bounded sample of output rows."""
+def cpu_baseline(p, target_s: float = 12.0, threads: int | None = None):
+    """The oracle, as it stands, on a bounded sample of output rows (all host
+    cores unless `threads` is given)."""
     import numpy as np
 
     import oracle
 
     A, B = problem_operands(p)
     A, B = A.numpy(), B.numpy()
-    threads = oracle.default_threads()
+    threads = threads or oracle.default_threads()
     rng = np.random.default_rng(0)
     probe = np.sort(rng.choice(p.M, size=min(p.M, max(threads, 8)), replace=False))
     dt, _ = oracle_rows_rate(A, B, probe, threads)
@@ -242,6 +244,28 @@ def run_reference(args, rank, world):
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
+    return 0
+
+
+def pct(xs, q):
+    """q-th percentile (nearest rank) of a list of numbers."""
+    ys = sorted(xs)
+    return ys[min(len(ys) - 1, max(0, int(round(q / 100 * (len(ys) - 1)))))]
+
+
+def run_cpu_table(args):
+    """The oracle timed on every named problem, on all host cores and on one
+    core, each on a bounded sample of output rows (a few seconds); one JSON
+    line per problem and core count.  Host only: no GPU is used."""
+    import oracle
+
+    for name, p in PROBLEMS.items():
+        if name.endswith("_int"):
+            continue
+        for threads in (oracle.default_threads(), 1):
+            rec = cpu_baseline(p, target_s=args.cpu_seconds, threads=threads)
+            rec.update({"workload": name, "flops": p.flops})
+            print(json.dumps(rec), flush=True)
     return 0
 
 
@@ -421,8 +445,8 @@ def run_ours(args, rank, world, local_rank):
         "clocks": clocks,
         "cpu_baseline": cpu,
         "wall_s_timed_region": wall,
-        "kernel_ms": {"mean": ms_local, "min": min(kernel_ms), "median": statistics.median(kernel_ms),
-                      "max": max(kernel_ms)},
+        "kernel_ms": {"mean": ms_local, "min": min(kernel_ms), "p10": pct(kernel_ms, 10),
+                      "median": statistics.median(kernel_ms), "p90": pct(kernel_ms, 90), "max": max(kernel_ms)},
     }
     print(json.dumps(line), flush=True)
     return 0
@@ -493,6 +517,9 @@ def run_sweep(args):
         # Context only (a library GEMM, on no path of this project): the
         # FP32 GEMM torch runs with TF32 disabled, timed the same way.
         runs += [({"entry": "torch.mm", "tf32": False}, lambda: torch.mm(A, B, out=C))]
+        # Sizes whose working set fits in L2: the automatic choice also with
+        # the operands left warm in L2 (no flush between calls).
+        warm = p.flops <= 2 * 2048**3
         for opt, run in runs:
             try:
                 for _ in range(3):
@@ -515,6 +542,25 @@ def run_sweep(args):
             except Exception as e:  # an option the shape does not allow
                 rec = {"workload": name, "options": opt, "error": str(e)}
             print(json.dumps(rec), flush=True)
+        if warm:
+            # Back to back without flushing (operands warm in L2), timed as one
+            # batch of --steps calls, so that no host launch gap is counted.
+            for opt, run in ((dict(l2="warm"), lambda: g.sgemm_f32(A, B, C)),
+                             (dict(entry="torch.mm", tf32=False, l2="warm"), lambda: torch.mm(A, B, out=C))):
+                for _ in range(3):
+                    run()
+                torch.cuda.synchronize()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                for _ in range(args.steps):
+                    run()
+                e1.record()
+                e1.synchronize()
+                assert g.check_status() == 0
+                ms = e0.elapsed_time(e1) / args.steps
+                tf = p.flops / (ms / 1e3) / 1e12
+                print(json.dumps({"workload": name, "options": opt, "ms": ms, "tflops": tf,
+                                  "frac_of_derived_peak": tf / DERIVED_FP32_PEAK_TFLOPS}), flush=True)
         del A, B, C, At, Bt
     return 0
 
@@ -528,12 +574,17 @@ def main(argv=None):
     ap.add_argument("--workload", choices=sorted(PROBLEMS), default=DEFAULT_WORKLOAD)
     ap.add_argument("--sweep", action="store_true", help="print the ablation table instead")
     ap.add_argument("--sweep-workloads", nargs="*", choices=sorted(PROBLEMS), default=None)
+    ap.add_argument("--cpu-table", action="store_true",
+                    help="time the oracle on every named problem, all cores and one core (host only)")
+    ap.add_argument("--cpu-seconds", type=float, default=4.0, help="bounded sample per --cpu-table entry")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     rank, world, local_rank = dist_env()
     if args.sweep:
         return run_sweep(args)
+    if args.cpu_table:
+        return run_cpu_table(args)
     if world > 1:
         import torch.distributed as dist
 
