@@ -21,18 +21,34 @@
 //  * register tiling (same page, section 2; "[infra] 03" experiment 4): every
 //    consumer thread accumulates an 8 x 8 block of C in registers and updates
 //    it by outer products of 8 A values and 8 B values per k, read from shared
-//    memory as 16-byte vectors.
+//    memory as 16-byte vectors.  The page reads its 8 A values per k down a
+//    column of the A tile; here that per-k read is kept by giving the
+//    consumers A with m innermost -- rewritten in shared memory by a second
+//    producer warp (kProducerTmaX, the default) or copied transposed in HBM
+//    beforehand (AMN) -- so that a thread's 8 rows at one k are two vectors.
+//    Reading A as stored (k innermost) instead takes 8 vectors of 4 k values
+//    per 4-k group, held for all 4 k, which stalls the first multiply-adds of
+//    every group (measured: 82 % FP32-pipe duty against 87-89 %).
 //
 // Extra machinery not on the pages:
-//  * cluster multicast: two CTAs that share the same rows of A (neighbours
-//    along N) each fetch half of the A slice and the TMA multicasts it into
-//    both CTAs' shared memory, halving the L2->SM traffic for A;
+//  * stream-K: one CTA per SM walks whole tiles, then an even share of
+//    (tile, K slice) units; tiles shared by several CTAs are finished through
+//    a global workspace of partial tiles, in a fixed CTA order;
 //  * split-K: for outputs with too few tiles to fill the GPU, a cluster of
 //    `split` CTAs along K computes partial tiles over disjoint K ranges and
 //    reduces them through distributed shared memory in a fixed rank order
 //    (deterministic, no global workspace);
+//  * cluster multicast: two CTAs that share the same rows of A (neighbours
+//    along N) each fetch half of the A slice and the TMA multicasts it into
+//    both CTAs' shared memory, halving the L2->SM traffic for A (slower on
+//    GB300; kept as an option);
 //  * paired FMA (fma.rn.f32x2, sm_100 family): two multiply-adds per
-//    instruction, halving the issue slots the outer product needs.
+//    instruction, halving the issue slots the outer product needs;
+//  * the scaled epilogue of the general entry (SCALED), and the producer
+//    variants measured against the default: a cp.async warpgroup (any
+//    alignment), a TMA warpgroup with a setmaxnreg register split, a fused
+//    producer (4-warp CTAs, two per SM, thread 0 issuing the TMA), 128 x 256
+//    tiles.
 //
 // Every wait is bounded by `timeout_ns` of global time; a thread that gives up
 // records SGEMM_ERR_TIMEOUT in the device status word, stops computing, and
