@@ -17,12 +17,14 @@
 // The dropped terms are below 2^-20 |a||b| per product, 20x inside the 5e-5
 // contract; integer inputs in {-8..8} have zero small parts (exact).
 //
-// Pipeline (one CTA per 128 x 128 tile of C, 10 warps, 2 stages of 80 KiB):
-// warp 0 issues the TMA copies of the A and B slices into a stage; warps 2..9
-// wait for them, write A_small, B_big and B_small next to them and arrive on
-// `ready`; warp 1 (lane 0) issues the 12 MMAs of the stage and commits them
-// to `empty`, which frees the whole stage for the producer.  After the last
-// stage the split warps read the accumulator from tensor memory and store C.
+// Pipeline (one CTA per 128 x 128 tile of C, 10 warps, 3 MMA stages of 64
+// KiB and 2 raw-B slots of 16 KiB): warp 0 issues the TMA copy of the A slice
+// into an MMA stage and of the B slice into a raw-B slot; warps 2..9 wait for
+// both, write A_small, B_big and B_small into the stage, release the raw-B
+// slot (`bfree`) and arrive on `ready`; warp 1 (lane 0) issues the 12 MMAs of
+// the stage and commits them to `empty`, which frees the stage for the
+// producer.  After the last stage the split warps read the accumulator from
+// tensor memory and store C.
 #pragma once
 
 #include <cuda.h>
@@ -44,18 +46,23 @@ __global__ void __launch_bounds__(kTdThreads, 1)
     sgemm_3xtf32_direct_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                                const TcParams p) {
     constexpr int S = kTdStages;
+    constexpr int RB = kTdRawBStages;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_base = smem_addr(smem_raw);
     const uint32_t base = (raw_base + 1023u) & ~1023u;
-    // Stage layout: [raw A | raw B | A small | B big | B small], 16 KiB each.
+    // MMA stage layout: [raw A | A small | B big | B small], 16 KiB each;
+    // then the raw-B slots.
     auto stage = [&](int st) { return base + static_cast<uint32_t>(st * kTdStageBytes); };
+    auto raw_b_slot = [&](int rb) { return base + static_cast<uint32_t>(S * kTdStageBytes + rb * kTdTile); };
     const uint32_t bars = base + kTdRingBytes;
-    auto full = [&](int st) { return bars + 8u * st; };
-    auto ready = [&](int st) { return bars + 8u * (S + st); };
-    auto empty = [&](int st) { return bars + 8u * (2 * S + st); };
-    const uint32_t acc_full = bars + 8u * (3 * S);
+    auto full = [&](int st) { return bars + 8u * st; };                // raw A landed
+    auto ready = [&](int st) { return bars + 8u * (S + st); };         // stored parts written
+    auto empty = [&](int st) { return bars + 8u * (2 * S + st); };     // MMAs of the stage done
+    auto bfull = [&](int rb) { return bars + 8u * (3 * S + rb); };     // raw B landed
+    auto bfree = [&](int rb) { return bars + 8u * (3 * S + RB + rb); };  // raw B read
+    const uint32_t acc_full = bars + 8u * (3 * S + 2 * RB);
     const uint32_t tmem_slot = acc_full + 8u;
-    static_assert(8 * (3 * S + 1) + 4 <= 256, "barrier area");
+    static_assert(8 * (3 * S + 2 * RB + 1) + 4 <= 256, "barrier area");
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -70,6 +77,10 @@ __global__ void __launch_bounds__(kTdThreads, 1)
             mbar_init(full(st), 1);
             mbar_init(ready(st), kTdSplitWarps);
             mbar_init(empty(st), 1);
+        }
+        for (int rb = 0; rb < RB; ++rb) {
+            mbar_init(bfull(rb), 1);
+            mbar_init(bfree(rb), kTdSplitWarps);
         }
         mbar_init(acc_full, 1);
         fence_mbarrier_init();
@@ -92,25 +103,34 @@ __global__ void __launch_bounds__(kTdThreads, 1)
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
-            int issued_round[S];
+            int issued_round[S], issued_round_b[RB];
 #pragma unroll
             for (int st = 0; st < S; ++st) issued_round[st] = -1;
+#pragma unroll
+            for (int rb = 0; rb < RB; ++rb) issued_round_b[rb] = -1;
             const bool skip_here = p.skip_stage > 0 && tile == 0;
             for (int kt = 0; kt < nkt; ++kt) {
-                const int st = kt % S;
-                const int round = kt / S;
-                if (round > 0 && !mbar_wait_bounded(empty(st), (round - 1) & 1, tmo)) {
+                const int st = kt % S, rb = kt % RB;
+                const int round = kt / S, round_b = kt / RB;
+                if ((round > 0 && !mbar_wait_bounded(empty(st), (round - 1) & 1, tmo)) ||
+                    (round_b > 0 && !mbar_wait_bounded(bfree(rb), (round_b - 1) & 1, tmo))) {
                     timed_out = true;
                     break;
                 }
                 if (skip_here && kt == p.skip_stage - 1) continue;
-                mbar_arrive_expect_tx(full(st), 2 * kTdTile);
+                mbar_arrive_expect_tx(full(st), kTdTile);
                 tma_load_2d(stage(st), &tmA, full(st), kt * kTdBK, m0);
-                tma_load_2d(stage(st) + kTdTile, &tmB, full(st), n0, kt * kTdBK);
+                mbar_arrive_expect_tx(bfull(rb), kTdTile);
+                tma_load_2d(raw_b_slot(rb), &tmB, bfull(rb), n0, kt * kTdBK);
                 issued_round[st] = round;
+                issued_round_b[rb] = round_b;
             }
-            for (int st = 0; st < S; ++st)  // drain: every issued copy has landed
+            // drain: every issued copy has landed
+            for (int st = 0; st < S; ++st)
                 if (issued_round[st] >= 0 && !mbar_wait_bounded(full(st), issued_round[st] & 1, tmo))
+                    timed_out = true;
+            for (int rb = 0; rb < RB; ++rb)
+                if (issued_round_b[rb] >= 0 && !mbar_wait_bounded(bfull(rb), issued_round_b[rb] & 1, tmo))
                     timed_out = true;
         }
     } else if (warp == 1) {
@@ -123,8 +143,8 @@ __global__ void __launch_bounds__(kTdThreads, 1)
                     break;
                 }
                 tc_fence_after_sync();
-                const uint32_t a_big = stage(st), a_small = a_big + 2 * kTdTile;
-                const uint32_t b_big = a_big + 3 * kTdTile, b_small = a_big + 4 * kTdTile;
+                const uint32_t a_big = stage(st), a_small = a_big + kTdTile;
+                const uint32_t b_big = a_big + 2 * kTdTile, b_small = a_big + 3 * kTdTile;
 #pragma unroll
                 for (int kk = 0; kk < kTdBK / 8; ++kk) {  // k-steps of 8 TF32 = 32 bytes of each row
                     const uint32_t off = static_cast<uint32_t>(kk * 32);
@@ -148,26 +168,27 @@ __global__ void __launch_bounds__(kTdThreads, 1)
         const int bn = tt % kTdBN;
         const int bc0 = (tt / kTdBN) * kBGroups;
         for (int kt = 0; kt < nkt; ++kt) {
-            const int st = kt % S;
-            if (!mbar_wait_bounded_warp(full(st), (kt / S) & 1, tmo)) {
+            const int st = kt % S, rb = kt % RB;
+            if (!mbar_wait_bounded_warp(full(st), (kt / S) & 1, tmo) ||
+                !mbar_wait_bounded_warp(bfull(rb), (kt / RB) & 1, tmo)) {
                 timed_out = true;
                 break;
             }
-            const uint32_t raw_a = stage(st), raw_b = raw_a + kTdTile;
-            const uint32_t a_small = raw_a + 2 * kTdTile, b_big = raw_a + 3 * kTdTile, b_small = raw_a + 4 * kTdTile;
+            const uint32_t raw_a = stage(st), raw_b = raw_b_slot(rb);
+            const uint32_t a_small = raw_a + kTdTile, b_big = raw_a + 2 * kTdTile, b_small = raw_a + 3 * kTdTile;
             // Loads first (their latencies overlap), then conversions and stores.
             float4 av[kAChunks];
 #pragma unroll
             for (int j = 0; j < kAChunks; ++j) av[j] = lds128(raw_a + static_cast<uint32_t>((tt + kSplitThreads * j) * 16));
             float bv[kBGroups][4];
-            const uint32_t rb = raw_b + static_cast<uint32_t>(bn * 4);
+            const uint32_t bcol = raw_b + static_cast<uint32_t>(bn * 4);
 #pragma unroll
             for (int c = 0; c < kBGroups; ++c)
 #pragma unroll
                 for (int i = 0; i < 4; ++i)
                     asm volatile("ld.shared.f32 %0, [%1];"
                                  : "=f"(bv[c][i])
-                                 : "r"(rb + static_cast<uint32_t>((4 * (bc0 + c) + i) * kTdBN * 4)));
+                                 : "r"(bcol + static_cast<uint32_t>((4 * (bc0 + c) + i) * kTdBN * 4)));
             // A: small parts, element-wise in the TMA's K-major swizzled layout.
 #pragma unroll
             for (int j = 0; j < kAChunks; ++j)
@@ -192,7 +213,10 @@ __global__ void __launch_bounds__(kTdThreads, 1)
             }
             fence_proxy_async_smem();  // make the tiles visible to the tensor core
             __syncwarp();
-            if (lane == 0) mbar_arrive(ready(st));
+            if (lane == 0) {
+                mbar_arrive(bfree(rb));  // the raw B slot has been read (and used)
+                mbar_arrive(ready(st));
+            }
         }
 
         // Epilogue: accumulator row (32 * (warp % 4) + lane) is that tensor-

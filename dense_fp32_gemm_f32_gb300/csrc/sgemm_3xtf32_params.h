@@ -44,17 +44,20 @@ struct TcParams {
 // ---- "direct-A" variant: the TF32 big part of A is the FP32 tile itself
 // (the tensor core reads the top 19 bits of each 32-bit element), so only
 // A's small part is stored; B is split into big and small parts and
-// transposed to K-major as in the split-tile kernel.  One stage holds the raw
-// A and B slices and the three stored parts; it is released by the MMAs.
+// transposed to K-major as in the split-tile kernel.  An MMA stage holds the
+// raw A slice and the three stored parts and is released by the MMAs; the raw
+// B slice has a ring of its own, released as soon as the split warps have
+// read it, so that three MMA stages fit.
 constexpr int kTdSplitWarps = 8;
 constexpr int kTdThreads = 64 + 32 * kTdSplitWarps;
 constexpr int kTdBM = 128;
 constexpr int kTdBN = 128;
 constexpr int kTdBK = 32;
 constexpr int kTdTile = 128 * kTdBK * 4;         // 16 KiB: one 128-row x 32-float tile
-constexpr int kTdStageBytes = 5 * kTdTile;        // raw A, raw B, A small, B big, B small
-constexpr int kTdStages = 2;
-constexpr int kTdRingBytes = kTdStages * kTdStageBytes;
+constexpr int kTdStageBytes = 4 * kTdTile;        // raw A, A small, B big, B small
+constexpr int kTdStages = 3;
+constexpr int kTdRawBStages = 2;                  // raw B slices
+constexpr int kTdRingBytes = kTdStages * kTdStageBytes + kTdRawBStages * kTdTile;
 constexpr int kTdSmemBytes = kTdRingBytes + 1024 + 256;
 constexpr int kTdTmemCols = kTdBN;
 
