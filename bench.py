@@ -489,6 +489,7 @@ SWEEP_OPTIONS = [
     {"a_layout": 2, "tile_n": 256},
     {"producer": 5},
     {"producer": 5, "stages": 3},
+    {"producer": 6},
     {"split_k": 1},
     {"split_k": 2},
     {"split_k": 4},

@@ -22,7 +22,7 @@ ERR_CUDA = 3
 ERR_TIMEOUT = 4
 ERR_NOT_IMPLEMENTED = 5
 
-PRODUCER_AUTO, PRODUCER_TMA, PRODUCER_CPASYNC, PRODUCER_TMA_WG, PRODUCER_FUSED, PRODUCER_TMA_X = 0, 1, 2, 3, 4, 5
+PRODUCER_AUTO, PRODUCER_TMA, PRODUCER_CPASYNC, PRODUCER_TMA_WG, PRODUCER_FUSED, PRODUCER_TMA_X, PRODUCER_SMALL = 0, 1, 2, 3, 4, 5, 6
 
 # Every symbol the headers declare, with its ctypes signature.
 _i, _p, _u64, _d = ctypes.c_int, ctypes.c_void_p, ctypes.c_uint64, ctypes.c_double

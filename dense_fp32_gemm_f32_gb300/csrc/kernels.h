@@ -57,6 +57,25 @@ int pack_rows(const float* src0, long long ld_src0, float* dst0, long long ld_ds
 int transpose_rows(const float* src0, long long ld_src0, float* dst0, long long ld_dst0, int rows0, int cols0,
                    const float* src1, long long ld_src1, float* dst1, long long ld_dst1, int rows1, int cols1,
                    cudaStream_t stream);
+// Small-problem FFMA kernel: one 8-warp CTA per 32 x 32 tile of C (grid
+// ceil(N / 32) x ceil(M / 32)), K split across the warps in 32-deep chunks
+// and the partials summed in a fixed order; bounds-checked 4-byte loads (any
+// alignment).  `a_mn`: A stored transposed (K x M); `scaled`: C = alpha A B +
+// beta C (beta == 0: C not read).
+constexpr int kSmallTile = 32;
+constexpr int kSmallWarps = 8;
+constexpr int kSmallSmemBytes = kSmallWarps * (kSmallTile * (kSmallTile + 4) + kSmallTile * kSmallTile) * 4;
+struct SmallParams {
+    int M, N, K;
+    const float* A;
+    long long lda;
+    const float* B;
+    long long ldb;
+    float* C;
+    long long ldc;
+    float alpha, beta;
+};
+KernelEntry small_kernel(bool a_mn, bool scaled);
 // C = beta * C over M x N with pitch ldc (beta == 0: zeros, C not read).
 int scale_c(float* C, long long ldc, int M, int N, float beta, cudaStream_t stream);
 

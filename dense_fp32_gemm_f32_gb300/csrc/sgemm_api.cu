@@ -146,6 +146,8 @@ int init_device(int dev, DeviceState& st) {
         }
         for (int s = 1; s <= 6; ++s)
             if (set_smem_attr(ffma_kernel_cpasync(s, math)) != SGEMM_OK) return SGEMM_ERR_CUDA;
+        for (int v = 0; v < 4; ++v)
+            if (set_smem_attr(small_kernel((v & 1) != 0, (v & 2) != 0)) != SGEMM_OK) return SGEMM_ERR_CUDA;
         for (int s = 2; s <= 4; ++s) {
             const KernelEntry f = ffma_kernel_tma_fused(s, math);
             if (set_smem_attr(f) != SGEMM_OK) return SGEMM_ERR_CUDA;
@@ -661,6 +663,54 @@ struct Scale {
     float alpha = 1.f, beta = 0.f;
 };
 
+// Small problems: the 32 x 32-tile kernel when the 128 x 128 tiles would be
+// too few to occupy the GPU and the product is small (see small_problem).
+constexpr double kSmallMaxFlops = 268435456.0;  // 2^28
+
+bool small_problem(const DeviceState& st, int M, int N, int K) {
+    const long long tiles = ceil_div(M, kBM) * ceil_div(N, kBN);
+    return 2.0 * static_cast<double>(M) * static_cast<double>(N) * static_cast<double>(K) <= kSmallMaxFlops &&
+           4 * tiles <= st.sm_count;
+}
+
+// A forced small kernel takes no other forced choice (it has no producer,
+// stages, split or tile options, and no waits for debug_skip_stage to time out).
+bool small_forced_ok(const sgemm_options* opt) {
+    return !(opt->split_k || opt->multicast || opt->math || opt->stages || opt->tail_split || opt->stream_k ||
+             opt->tile_n || opt->repack || opt->a_layout || opt->debug_skip_stage);
+}
+
+int launch_small(int M, int N, int K, const float* A, int lda, const float* B, int ldb, float* C, int ldc,
+                 void* stream, const Scale* scale, bool a_mn) {
+    const bool scaled = scale && (scale->alpha != 1.f || scale->beta != 0.f);
+    const KernelEntry k = small_kernel(a_mn, scaled);
+    SmallParams prm;
+    prm.M = M;
+    prm.N = N;
+    prm.K = K;
+    prm.A = A;
+    prm.lda = lda;
+    prm.B = B;
+    prm.ldb = ldb;
+    prm.C = C;
+    prm.ldc = ldc;
+    prm.alpha = scale ? scale->alpha : 1.f;
+    prm.beta = scale ? scale->beta : 0.f;
+    const long long gx = ceil_div(N, kSmallTile), gy = ceil_div(M, kSmallTile);
+    if (gy > 65535) return SGEMM_ERR_INVALID_ARG;  // (never: the rule and the forced form both bound M)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy), 1);
+    cfg.blockDim = dim3(k.threads, 1, 1);
+    cfg.dynamicSmemBytes = static_cast<size_t>(k.smem_bytes);
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    void* args[1] = {&prm};
+    if (cudaLaunchKernelExC(&cfg, k.fn, args) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return SGEMM_ERR_CUDA;
+    }
+    return SGEMM_OK;
+}
+
 int run_ffma(int M, int N, int K, const float* A, int lda, const float* B, int ldb, float* C, int ldc,
              void* stream, const sgemm_options* opt, const Scale* scale = nullptr, bool a_mn = false) {
     int rc = validate(M, N, K, A, lda, B, ldb, C, ldc, a_mn);
@@ -673,6 +723,14 @@ int run_ffma(int M, int N, int K, const float* A, int lda, const float* B, int l
     if (rc != SGEMM_OK) return rc;
 
     const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    if (opt && opt->producer == SGEMM_PRODUCER_SMALL) {
+        if (!small_forced_ok(opt)) return SGEMM_ERR_INVALID_ARG;
+        if (ceil_div(M, kSmallTile) > 65535) return SGEMM_ERR_INVALID_ARG;
+        return launch_small(M, N, K, A, lda, B, ldb, C, ldc, stream, scale, a_mn);
+    }
+    if (!options_force_variant(opt) && !(opt && (opt->a_layout || opt->debug_skip_stage)) &&
+        small_problem(*st, M, N, K))
+        return launch_small(M, N, K, A, lda, B, ldb, C, ldc, stream, scale, a_mn);
     // A copied transposed for the transposed-A kernels (see choose_a_layout).
     Repacked a_t;
     const int layout = a_mn ? 0 : choose_a_layout(M, N, K, opt);
@@ -856,6 +914,7 @@ int run_ffma_noalloc(int M, int N, int K, const float* A, int lda, const float* 
         st->noalloc_status = SGEMM_OK;
     });
     if (st->noalloc_status != SGEMM_OK) return st->noalloc_status;
+    if (small_problem(*st, M, N, K)) return launch_small(M, N, K, A, lda, B, ldb, C, ldc, stream, nullptr, false);
 
     // Plan: stream-K whenever there is a K slice to deal out (K == 0 runs the
     // plain grid, which writes zeros and needs no scratch).
@@ -1269,6 +1328,7 @@ const char* sgemm_describe(int M, int N, int K, const float* A, int lda, const f
     DeviceState* st = nullptr;
     if (current_device(&dev, &st) != SGEMM_OK) return "unavailable";
     if (M == 0 || N == 0) return "noop";
+    if (small_problem(*st, M, N, K)) return "small/t32/w8";
     Plan pl;
     if (choose_a_layout(M, N, K, nullptr) == 1) {
         // The call would run on a transposed copy of A (a pool buffer: aligned

@@ -219,11 +219,18 @@ enum {
                                     thread 0 issuing the tensor-map copies between its own
                                     multiply-adds (implies tile_n = 64; 2..4 stages, default 4;
                                     no split-K clusters, no multicast) */
-    SGEMM_PRODUCER_TMA_X = 5     /* tensor-map copies, and a second producer warp that
+    SGEMM_PRODUCER_TMA_X = 5,    /* tensor-map copies, and a second producer warp that
                                     transposes each stage's A slice in shared memory for the
                                     consumers to read per k (the transposed-A read without a
                                     copy of A in HBM; 128 x 128 tiles, 2..4 stages, no
                                     multicast) */
+    SGEMM_PRODUCER_SMALL = 6     /* the small-problem kernel: one 8-warp CTA per 32 x 32 tile
+                                    of C, K split across its warps in 32-deep chunks and the
+                                    partials summed in a fixed order; bounds-checked 4-byte
+                                    loads (any alignment), no pipeline and no waits.  Chosen
+                                    automatically when 2MNK <= 2^28 and the 128 x 128 tiles
+                                    number at most a quarter of the SMs.  Takes no other
+                                    forced field (SGEMM_ERR_INVALID_ARG otherwise) */
 };
 
 /*

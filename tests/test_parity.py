@@ -186,30 +186,39 @@ def test_forced_tma_rejects_unaligned_rows():
 
 # ---------------------------------------------------------------- ragged shapes, edges, layouts
 
-def test_ragged_shapes_sweep():
+# Small shapes run on the small-problem kernel when nothing is forced;
+# a_layout = 1 (A as stored) keeps the automatic choice among the 128 x 128
+# FFMA kernels, so that their edge handling is covered at the same shapes.
+AUTO_FORMS = [dict(), dict(a_layout=1)]
+
+
+@pytest.mark.parametrize("opt", AUTO_FORMS, ids=["auto", "ffma128"])
+def test_ragged_shapes_sweep(opt):
     rng = np.random.default_rng(1234)
     for t in range(24):
         M, N, K = (int(x) for x in rng.integers(1, 301, size=3))
         A, B = make_operands(M, N, K, "normal", 500 + t)
-        C = run(A, B)
+        C = run(A, B, **opt)
         C64, bound = oracle.gemm_f64(A.numpy(), B.numpy())
-        check(C, C64, bound, exact=False, what=f"{M}x{N}x{K}")
+        check(C, C64, bound, exact=False, what=f"{M}x{N}x{K} {opt}")
 
 
+@pytest.mark.parametrize("opt", AUTO_FORMS + [dict(producer=6)], ids=["auto", "ffma128", "small"])
 @pytest.mark.parametrize("shape", [(1, 1, 1), (1, 1, 10000), (1, 300, 7), (300, 1, 7), (129, 127, 1), (5, 3, 2),
                                    (128, 128, 32), (129, 129, 33), (256, 256, 8192)])
-def test_small_and_degenerate_shapes(shape):
+def test_small_and_degenerate_shapes(shape, opt):
     M, N, K = shape
     A, B = make_operands(M, N, K, "uniform", 77)
-    C = run(A, B)
+    C = run(A, B, **opt)
     C64, bound = oracle.gemm_f64(A.numpy(), B.numpy())
-    check(C, C64, bound, exact=False, what=str(shape))
+    check(C, C64, bound, exact=False, what=f"{shape} {opt}")
 
 
-def test_k_zero_writes_zeros():
+@pytest.mark.parametrize("opt", AUTO_FORMS + [dict(producer=6)], ids=["auto", "ffma128", "small"])
+def test_k_zero_writes_zeros(opt):
     A = torch.empty((37, 0))
     B = torch.empty((0, 45))
-    C = run(A, B)
+    C = run(A, B, **opt)
     assert np.array_equal(C, np.zeros((37, 45), np.float32))
 
 
@@ -247,13 +256,15 @@ def test_leading_dimensions_and_guard_bands():
 
 
 @pytest.mark.parametrize("offsets", [(1, 0), (0, 3), (2, 1)])
-def test_unaligned_bases(offsets):
-    """Bases that are not 16-byte aligned take the cp.async producer."""
+@pytest.mark.parametrize("shape", [(190, 170, 260), (700, 900, 260)])
+def test_unaligned_bases(offsets, shape):
+    """Bases that are not 16-byte aligned: the small-problem kernel (plain
+    loads) or, above its range, the cp.async producer."""
     oa, ob = offsets
-    M, N, K = 190, 170, 260
+    M, N, K = shape
     A, B = make_operands(M, N, K, "uniform", 9)
     dA, dB = to_device(A, offset=oa), to_device(B, offset=ob)
-    assert g.describe(dA, dB).startswith("cpasync")
+    assert g.describe(dA, dB).startswith("small" if M < 256 else "cpasync")
     C = g.sgemm_f32(dA, dB)
     torch.cuda.synchronize()
     C64, bound = oracle.gemm_f64(A.numpy(), B.numpy())
@@ -341,12 +352,16 @@ def test_variant_choice():
     assert "/s1/" in desc(4096, 4096, 4096) and "/sk" in desc(4096, 4096, 4096)  # stream-K
     assert "/tail" not in desc(4096, 4096, 4096)  # the tail split is opt-in
     assert "/sk" in desc(8192, 128, 8192) and "/sk" in desc(128, 8192, 16384)
-    assert "/sk" not in desc(256, 256, 256) and "/s1/" not in desc(256, 256, 256)  # tiny: cluster split-K
+    # small products (2MNK <= 2^28, 128 x 128 tiles at most a quarter of the
+    # SMs): the 32 x 32-tile kernel
+    assert desc(256, 256, 256) == "small/t32/w8" and desc(512, 512, 512) == "small/t32/w8"
+    assert desc(300, 500, 701) == "small/t32/w8" and desc(64, 64, 64) == "small/t32/w8"
+    assert desc(640, 640, 640).startswith("tmax/") and desc(1024, 1024, 128).startswith("tmax/")
     # 1027-float rows are not 16-byte multiples: the operands are repacked
-    # into pitched rows and the tensor-map path runs; small products read the
-    # rows as they are with cp.async
+    # into pitched rows and the tensor-map path runs; mid-sized products read
+    # the rows as they are with cp.async
     assert desc(1023, 1025, 1027).startswith("tmax/") and desc(1023, 1025, 1027).endswith("/repackAB")
-    assert desc(300, 500, 701).startswith("cpasync/")
+    assert desc(700, 900, 701).startswith("cpasync/")
     assert desc(2048, 2049, 2048).endswith("/repackB")
     assert desc(8192, 8193, 8192).endswith("/repackB/at")
 

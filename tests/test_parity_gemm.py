@@ -47,11 +47,17 @@ TRANS = [(0, 0), (1, 0), (0, 1), (1, 1)]
 SCALES = [(1.0, 0.0), (2.0, -1.0), (0.5, 2.0), (-1.0, 0.5), (1.0, 1.0)]
 
 
+# 300 x 500 x 700 runs on the small-problem kernel (32 x 32 tiles); 700 x 900
+# x 500 (48 tiles of 128 x 128) on the FFMA kernels with the scaled epilogue.
+# Both are ragged against their tiles, with several tiles per axis.
+SHAPES = [(300, 500, 700), (700, 900, 500)]
+
+
+@pytest.mark.parametrize("shape", SHAPES)
 @pytest.mark.parametrize("ta,tb", TRANS)
 @pytest.mark.parametrize("alpha,beta", SCALES)
-def test_general_form(ta, tb, alpha, beta):
-    # 300 x 500 x 700: ragged against the tile sizes, several tiles per axis
-    M, N, K = 300, 500, 700
+def test_general_form(ta, tb, alpha, beta, shape):
+    M, N, K = shape
     a, b = (x.numpy() for x in make_operands(M, N, K, "uniform", 201))
     cin = make_operands(M, 1, N, "uniform", 202)[0].numpy()
     A, B = stored(a, b, ta, tb)
@@ -60,9 +66,10 @@ def test_general_form(ta, tb, alpha, beta):
     check(C, ref, bound, exact=False, what=f"t{ta}{tb} a{alpha} b{beta}")
 
 
+@pytest.mark.parametrize("shape", [(257, 190, 333), (700, 900, 333)])
 @pytest.mark.parametrize("ta,tb", TRANS)
-def test_general_form_integer_exact(ta, tb):
-    M, N, K = 257, 190, 333
+def test_general_form_integer_exact(ta, tb, shape):
+    M, N, K = shape
     a, b = (x.numpy() for x in make_operands(M, N, K, "int", 203))
     cin = make_operands(M, 1, N, "int", 204)[0].numpy()
     A, B = stored(a, b, ta, tb)
@@ -71,8 +78,9 @@ def test_general_form_integer_exact(ta, tb):
     check(C, ref, None, exact=True, what=f"int t{ta}{tb}")
 
 
-def test_beta_zero_does_not_read_c():
-    a, b = (x.numpy() for x in make_operands(130, 140, 150, "uniform", 205))
+@pytest.mark.parametrize("shape", [(130, 140, 150), (700, 900, 150)])
+def test_beta_zero_does_not_read_c(shape):
+    a, b = (x.numpy() for x in make_operands(*shape, "uniform", 205))
     C = run(a, b, None, alpha=1.5, beta=0.0, ta=0, tb=0)  # C holds NaN
     ref, bound = oracle.gemm_general_f64(a, b, alpha=1.5, beta=0.0)
     assert np.isfinite(C).all()
@@ -91,10 +99,11 @@ def test_alpha_zero_or_empty_sum_scales_c(K):
         assert np.array_equal(C, (np.float32(beta) * cin) if beta else np.zeros_like(cin)), (alpha, beta)
 
 
+@pytest.mark.parametrize("shape", [(200, 152, 96), (1100, 700, 96)])
 @pytest.mark.parametrize("ta,tb", TRANS)
-def test_general_padded_and_odd_pitches(ta, tb):
+def test_general_padded_and_odd_pitches(ta, tb, shape):
     """Odd leading dimensions (no 16-byte rows) in every storage order."""
-    M, N, K = 200, 152, 96
+    M, N, K = shape
     a, b = (x.numpy() for x in make_operands(M, N, K, "uniform", 207))
     cin = make_operands(M, 1, N, "uniform", 208)[0].numpy()
     A, B = stored(a, b, ta, tb)
