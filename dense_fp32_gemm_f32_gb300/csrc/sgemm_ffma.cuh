@@ -161,7 +161,8 @@ struct FfmaParams {
     int sk_dp_tiles;       // tiles handled whole before the stream-K region
     long long sk_units;    // (tiles - sk_dp_tiles) * num_k_tiles
     float* ws;             // gridDim.x partial tiles of kBM x BN floats
-    unsigned int* flags;   // gridDim.x words, zero at launch; 1 = partial ready
+    unsigned int* flags;   // gridDim.x words; flags[g] == sk_seq: CTA g's partial is ready
+    unsigned int sk_seq;   // this call's number (nonzero; no flag holds it at launch)
     int skip_stage;        // debug: CTA (0,0,0)'s producer never issues K-slice skip_stage-1
     unsigned long long timeout_ns;
     unsigned int* status;  // per-device sticky status word (error bits)
@@ -756,7 +757,7 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), ffma_min_blocks<PROD
                 consumer_sync();
                 if (threadIdx.x == 0) {
                     __threadfence();
-                    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p.flags + blockIdx.x), "r"(1u)
+                    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p.flags + blockIdx.x), "r"(p.sk_seq)
                                  : "memory");
                 }
             } else {
@@ -775,7 +776,7 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), ffma_min_blocks<PROD
                                              : "=r"(f)
                                              : "l"(p.flags + g2)
                                              : "memory");
-                                if (f != 0u) break;
+                                if (f == p.sk_seq) break;
                                 if (global_timer_ns() - t0 > tmo) {
                                     ok = false;
                                     break;

@@ -491,18 +491,86 @@ def test_cuda_graph_capture_and_replay():
     graph = torch.cuda.CUDAGraph()
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
+    dN = torch.empty((M, N), device="cuda")
     with torch.cuda.stream(s):
         with torch.cuda.graph(graph, stream=s):
             g.sgemm_f32(dA, dB, dC, stream=s)
             g.sgemm_f32_gemm(dA, dB, dG, alpha=2.0, beta=0.0, stream=s)
-    for seed in (17, 18):
+            g.sgemm_f32_noalloc(dA, dB, dN, stream=s)
+    # Eager calls on the same stream between replays take the stream's own
+    # stream-K scratch (sequence-numbered flags); the graph's calls keep the
+    # workspaces and memsets recorded with them.
+    E1, E2 = make_operands(M, N, K, "int", 19)
+    dE1, dE2 = to_device(E1), to_device(E2)
+    dE, dEn = torch.empty((M, N), device="cuda"), torch.empty((M, N), device="cuda")
+    E64, _ = oracle.gemm_f64(E1.numpy(), E2.numpy(), with_bound=False)
+    for seed in (17, 18, 20):
         A2, B2 = make_operands(M, N, K, "uniform", seed)
         dA.copy_(A2)
         dB.copy_(B2)
-        dC.fill_(float("nan"))
-        graph.replay()
+        for X in (dC, dG, dN, dE, dEn):
+            X.fill_(float("nan"))
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            g.sgemm_f32(dE1, dE2, dE, stream=s)
+            graph.replay()
+            g.sgemm_f32_noalloc(dE1, dE2, dEn, stream=s)
         torch.cuda.synchronize()
         C64, bound = oracle.gemm_f64(A2.numpy(), B2.numpy())
         check(dC.cpu().numpy(), C64, bound, exact=False, what=f"graph replay {seed}")
         check(dG.cpu().numpy(), 2.0 * C64, 2.0 * bound, exact=False, what=f"graph replay gemm {seed}")
+        check(dN.cpu().numpy(), C64, bound, exact=False, what=f"graph replay noalloc {seed}")
+        check(dE.cpu().numpy(), E64, None, exact=True, what=f"eager between replays {seed}")
+        check(dEn.cpu().numpy(), E64, None, exact=True, what=f"eager noalloc between replays {seed}")
+    assert g.check_status() == 0
+
+
+# ---------------------------------------------------------------- stream-K scratch kept per stream
+
+# Shapes on the stream-K schedule with different CTA runs (so that different
+# CTAs publish partial tiles from one call to the next).
+STREAM_K_SHAPES = [(700, 900, 1100), (1024, 768, 1536), (640, 1300, 900), (1500, 300, 2000)]
+
+
+@pytest.mark.parametrize("fn", ["sgemm_f32", "sgemm_f32_noalloc"])
+def test_stream_k_scratch_back_to_back(fn):
+    """Calls on one stream reuse the same stream-K flags without zeroing them:
+    each call waits for its own sequence number, so flags left by an earlier
+    call (another schedule, other inputs) never match.  Integer inputs, all
+    calls enqueued back to back before one synchronisation, every result
+    exact."""
+    call = getattr(g, fn)
+    cases = []
+    for t, (M, N, K) in enumerate(STREAM_K_SHAPES * 2):
+        A, B = make_operands(M, N, K, "int", 600 + t)
+        dA, dB = to_device(A), to_device(B)
+        assert "/sk" in g.describe(dA, dB)
+        cases.append((A, B, dA, dB, torch.full((M, N), float("nan"), device="cuda")))
+    torch.cuda.synchronize()
+    for _, _, dA, dB, dC in cases:
+        call(dA, dB, dC)
+    torch.cuda.synchronize()
+    for A, B, _, _, dC in cases:
+        C64, _ = oracle.gemm_f64(A.numpy(), B.numpy(), with_bound=False)
+        check(dC.cpu().numpy(), C64, None, exact=True, what=f"{fn} back to back {tuple(dC.shape)}")
+
+
+def test_stream_k_scratch_more_streams_than_entries():
+    """20 streams, two calls each, all in flight together: the library keeps
+    stream-K scratch for 16 streams, so entries move to new streams (whose
+    work first waits for the entry's last call on its old stream)."""
+    M, N, K = 512, 640, 700
+    streams = [torch.cuda.Stream() for _ in range(20)]
+    cases = []
+    for t in range(2 * len(streams)):
+        A, B = make_operands(M, N, K, "int", 700 + t)
+        cases.append((A, B, to_device(A), to_device(B), torch.full((M, N), float("nan"), device="cuda")))
+    assert "/sk" in g.describe(cases[0][2], cases[0][3])
+    torch.cuda.synchronize()
+    for t, (_, _, dA, dB, dC) in enumerate(cases):
+        g.sgemm_f32(dA, dB, dC, stream=streams[t % len(streams)])
+    torch.cuda.synchronize()
+    for A, B, _, _, dC in cases:
+        C64, _ = oracle.gemm_f64(A.numpy(), B.numpy(), with_bound=False)
+        check(dC.cpu().numpy(), C64, None, exact=True, what="many streams")
     assert g.check_status() == 0
