@@ -510,6 +510,12 @@ def run_sweep(args):
     torch.backends.cuda.matmul.allow_tf32 = False  # the library comparison runs in full FP32
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
     names = args.sweep_workloads or [n for n in PROBLEMS if not n.endswith("_int")]
+    # An idle GPU runs the first calls below its working clock: keep it busy
+    # for a second before the first measurement.
+    t_end = time.perf_counter() + 1.0
+    while time.perf_counter() < t_end:
+        flush.fill_(0.0)
+        torch.cuda.synchronize()
     for name in names:
         p = PROBLEMS[name]
         A_cpu, B_cpu = problem_operands(p)
