@@ -475,12 +475,12 @@ struct Repacked {
 // two 16-byte vectors instead of a 4-k vector per row (82 -> 89 % FMA-pipe
 // duty).  Two ways to get there: a transposing copy of A in HBM
 // (sgemm_options.a_layout = 2; the transposed-A kernels, no extra work in
-// the kernel) or a second producer warp transposing each A slice in shared
+// the kernel) or two producer warps transposing each A slice in shared
 // memory (SGEMM_PRODUCER_TMA_X; no copy, a little more shared-memory traffic
 // in the kernel).  Measured on GB300 (TFLOP/s, A read as stored / copy in HBM
-// / transposed in shared memory): 2048^3 62.0 / 62.7 / 65.4, 4096^3 65.4 /
-// 68.5 / 69.2, 8192^3 66.4 / 71.1 / 69.8, 128 x 8192 x 16384 64.2 / 68.2 /
-// 67.0, 8192 x 128 x 8192 62.0 / - / 64.7.  The copy costs one read and one
+// / transposed in shared memory): 2048^3 62.0 / 62.7 / 66.9, 4096^3 65.4 /
+// 68.5 / 70.5, 8192^3 66.4 / 71.2 / 71.0, 128 x 8192 x 16384 64.2 / 68.2 /
+// 68.7, 8192 x 128 x 8192 62.0 / - / 66.4.  The copy costs one read and one
 // write of A, i.e. ~1/N of the product; it is taken automatically when no
 // variant is forced, N >= 6144 and 2MNK >= 2^33, and the transposition in
 // shared memory otherwise (make_plan).
@@ -615,7 +615,7 @@ int make_plan(const DeviceState& st, int M, int N, int K, const float* A, int ld
         pl.producer = kProducerCpAsync;
     } else if (want_prod == SGEMM_PRODUCER_AUTO) {
         // Tensor maps: A transposed in shared memory, unless it already is in
-        // HBM (a_mn) or another choice rules the second producer warp out.
+        // HBM (a_mn) or another choice rules the transposing warps out.
         const bool x_ok = !a_mn && !(opt && (opt->multicast == 2 || (opt->tile_n && opt->tile_n != kBN) ||
                                              (opt->stages && (opt->stages < 2 || opt->stages > 4))));
         pl.producer = !aligned ? kProducerCpAsync : x_ok ? kProducerTmaX : kProducerTma;

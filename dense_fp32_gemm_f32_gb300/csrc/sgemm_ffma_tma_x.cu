@@ -1,5 +1,5 @@
 // Instantiations of the FFMA kernel with A transposed in shared memory
-// (kProducerTmaX: TMA producer warp + transposing warp); 128 x 128 tiles.
+// (kProducerTmaX: TMA producer warp + two transposing warps); 128 x 128 tiles.
 #include "kernels.h"
 #include "sgemm_ffma.cuh"
 

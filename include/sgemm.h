@@ -219,8 +219,8 @@ enum {
                                     thread 0 issuing the tensor-map copies between its own
                                     multiply-adds (implies tile_n = 64; 2..4 stages, default 4;
                                     no split-K clusters, no multicast) */
-    SGEMM_PRODUCER_TMA_X = 5,    /* tensor-map copies, and a second producer warp that
-                                    transposes each stage's A slice in shared memory for the
+    SGEMM_PRODUCER_TMA_X = 5,    /* tensor-map copies, and two producer warps that
+                                    transpose each stage's A slice in shared memory for the
                                     consumers to read per k (the transposed-A read without a
                                     copy of A in HBM; 128 x 128 tiles, 2..4 stages, no
                                     multicast) */
