@@ -42,6 +42,9 @@ KernelEntry tf32x3_kernel();
 // Direct-A three-product TF32 kernel: A's big part read from the TMA tile,
 // only A's small part and B's two parts stored (128 x 128 tiles).
 KernelEntry tf32x3_direct_kernel();
+// The split-tile kernel on 128 x 256 tiles with K-slices of 16 (64-byte
+// swizzled operand rows, 256 tensor-memory columns).
+KernelEntry tf32x3_wide_kernel();
 
 // Copies up to two operands (a null dst skips one): `rows` rows of `cols`
 // floats from `src` (pitch ld_src floats, any alignment) to `dst` (pitch

@@ -249,6 +249,20 @@ __device__ __forceinline__ uint64_t umma_desc_kmajor_sw128(uint32_t saddr) {
     return d;
 }
 
+// Shared-memory matrix descriptor: K-major operand, 64-byte swizzle: rows of
+// 64 bytes (16 TF32 along K), groups of 8 rows 512 bytes apart (stride byte
+// offset); layout type 4.  The tile starts on a 512-byte boundary (the
+// swizzle pattern repeats every 8 rows); a k-step of 8 elements inside the
+// row advances the start address by 32 bytes, as with the 128-byte swizzle.
+__device__ __forceinline__ uint64_t umma_desc_kmajor_sw64(uint32_t saddr) {
+    uint64_t d = static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>(1) << 16;
+    d |= static_cast<uint64_t>(512 >> 4) << 32;
+    d |= static_cast<uint64_t>(1) << 46;
+    d |= static_cast<uint64_t>(4) << 61;
+    return d;
+}
+
 // Shared-memory matrix descriptor: MN-major operand (MN innermost), 128-byte
 // swizzle: rows of 128 bytes (32 elements along MN), one row per k, groups of
 // 8 k-rows 1024 bytes apart (stride byte offset), consecutive 32-element MN

@@ -15,15 +15,17 @@
 // exact.  (The pages mention tensor cores only as a future direction of the
 // "Hardware acceleration" page's summary; nothing of this is on the pages.)
 //
-// One CTA computes a 128 x 128 tile of C; 10 warps:
-//   warp 0      TMA producer: A and B K-slices (BK = 32) into 3 raw stages;
-//   warp 1      allocates 128 tensor-memory columns (the FP32 accumulator)
-//               and one lane issues the MMAs: per K-slice 4 k-steps of 8,
-//               three tcgen05.mma.kind::tf32 each (small*big, big*small,
+// One CTA computes a 128 x BN tile of C (TcShape<BN, BK>: 128 x 128 with
+// K-slices of 32 and 128-byte operand rows, or 128 x 256 with K-slices of 16
+// and 64-byte rows); 10 warps:
+//   warp 0      TMA producer: A and B K-slices into the raw stages;
+//   warp 1      allocates BN tensor-memory columns (the FP32 accumulator)
+//               and one lane issues the MMAs: per K-slice BK / 8 k-steps of
+//               8, three tcgen05.mma.kind::tf32 each (small*big, big*small,
 //               big*big), then tcgen05.commit releases the split stage;
-//   warps 2..9  split the raw K-slice into four K-major, 128-byte-swizzled
-//               TF32 operand tiles (A_big, A_small, B_big, B_small) in 2
-//               split stages (B is transposed on the way: it arrives with n
+//   warps 2..9  split the raw K-slice into four K-major, swizzled TF32
+//               operand tiles (A_big, A_small, B_big, B_small) in 2 split
+//               stages (B is transposed on the way: it arrives with n
 //               innermost), then, after the last MMA, read the accumulator
 //               out of tensor memory (tcgen05.ld) and store C.  Eight warps
 //               (two per SM sub-partition) so that one warp's shared-memory
@@ -49,41 +51,52 @@ __device__ __forceinline__ void split_tf32(float x, float& big, float& small) {
     small = to_tf32_rna(x - big);  // x - big is exact in FP32
 }
 
+// K-major operand descriptor for the shape's swizzle (128- or 64-byte rows).
+template <int BK>
+__device__ __forceinline__ uint64_t tc_operand_desc(uint32_t saddr) {
+    if constexpr (BK == 32)
+        return umma_desc_kmajor_sw128(saddr);
+    else
+        return umma_desc_kmajor_sw64(saddr);
+}
+
+template <int BN, int BK>
 __global__ void __launch_bounds__(kTcThreads, 1)
     sgemm_3xtf32_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const TcParams p) {
+    using T = TcShape<BN, BK>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_base = smem_addr(smem_raw);
     const uint32_t base = (raw_base + 1023u) & ~1023u;
-    auto rawA = [&](int r) { return base + static_cast<uint32_t>(r * kTcRawABytes); };
-    auto rawB = [&](int r) { return base + static_cast<uint32_t>(kTcRawStages * kTcRawABytes + r * kTcRawBBytes); };
+    auto rawA = [&](int r) { return base + static_cast<uint32_t>(r * T::kRawABytes); };
+    auto rawB = [&](int r) { return base + static_cast<uint32_t>(T::kRawStages * T::kRawABytes + r * T::kRawBBytes); };
     auto split = [&](int s) {
-        return base + static_cast<uint32_t>(kTcRawStages * (kTcRawABytes + kTcRawBBytes) + s * kTcSplitBytes);
+        return base + static_cast<uint32_t>(T::kRawStages * (T::kRawABytes + T::kRawBBytes) + s * T::kSplitBytes);
     };
-    const uint32_t bars = base + kTcRingBytes;
-    constexpr uint32_t R = kTcRawStages, S = kTcSplitStages;
+    const uint32_t bars = base + T::kRingBytes;
+    constexpr uint32_t R = T::kRawStages, S = T::kSplitStages;
     auto raw_full = [&](int r) { return bars + 8u * r; };
     auto raw_empty = [&](int r) { return bars + 8u * (R + r); };
     auto split_full = [&](int s) { return bars + 8u * (2 * R + s); };
     auto split_empty = [&](int s) { return bars + 8u * (2 * R + S + s); };
     const uint32_t acc_full = bars + 8u * (2 * R + 2 * S);
     const uint32_t tmem_slot = acc_full + 8u;
-    static_assert(8 * (2 * kTcRawStages + 2 * kTcSplitStages + 1) + 4 <= 256, "barrier area");
+    static_assert(8 * (2 * T::kRawStages + 2 * T::kSplitStages + 1) + 4 <= 256, "barrier area");
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int tile = static_cast<int>(blockIdx.x);
-    const int n0 = (tile % p.tiles_n) * kTcBN;
-    const int m0 = (tile / p.tiles_n) * kTcBM;
+    const int n0 = (tile % p.tiles_n) * BN;
+    const int m0 = (tile / p.tiles_n) * T::kBM;
     const int nkt = p.num_k_tiles;
     const unsigned long long tmo = p.timeout_ns;
 
     if (threadIdx.x == 0) {
-        for (int r = 0; r < kTcRawStages; ++r) {
+        for (int r = 0; r < T::kRawStages; ++r) {
             mbar_init(raw_full(r), 1);
             mbar_init(raw_empty(r), kTcSplitWarps);  // one arrival per split warp
         }
-        for (int s = 0; s < kTcSplitStages; ++s) {
+        for (int s = 0; s < T::kSplitStages; ++s) {
             mbar_init(split_full(s), kTcSplitWarps);
             mbar_init(split_empty(s), 1);  // tcgen05.commit
         }
@@ -91,7 +104,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         fence_mbarrier_init();
     }
     if (warp == 1) {
-        tmem_alloc(tmem_slot, kTcTmemCols);
+        tmem_alloc(tmem_slot, T::kTmemCols);
         tmem_relinquish_alloc_permit();
     }
     if (warp == 0 && lane == 0) {
@@ -108,24 +121,24 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
-            int issued_round[kTcRawStages];
+            int issued_round[T::kRawStages];
 #pragma unroll
-            for (int r = 0; r < kTcRawStages; ++r) issued_round[r] = -1;
+            for (int r = 0; r < T::kRawStages; ++r) issued_round[r] = -1;
             const bool skip_here = p.skip_stage > 0 && tile == 0;
             for (int kt = 0; kt < nkt; ++kt) {
-                const int r = kt % kTcRawStages;
-                const int round = kt / kTcRawStages;
+                const int r = kt % T::kRawStages;
+                const int round = kt / T::kRawStages;
                 if (round > 0 && !mbar_wait_bounded(raw_empty(r), (round - 1) & 1, tmo)) {
                     timed_out = true;
                     break;
                 }
                 if (skip_here && kt == p.skip_stage - 1) continue;
-                mbar_arrive_expect_tx(raw_full(r), kTcRawABytes + kTcRawBBytes);
-                tma_load_2d(rawA(r), &tmA, raw_full(r), kt * kTcBK, m0);
-                tma_load_2d(rawB(r), &tmB, raw_full(r), n0, kt * kTcBK);
+                mbar_arrive_expect_tx(raw_full(r), T::kRawABytes + T::kRawBBytes);
+                tma_load_2d(rawA(r), &tmA, raw_full(r), kt * BK, m0);
+                tma_load_2d(rawB(r), &tmB, raw_full(r), n0, kt * BK);
                 issued_round[r] = round;
             }
-            for (int r = 0; r < kTcRawStages; ++r)  // drain: every issued copy has landed
+            for (int r = 0; r < T::kRawStages; ++r)  // drain: every issued copy has landed
                 if (issued_round[r] >= 0 && !mbar_wait_bounded(raw_full(r), issued_round[r] & 1, tmo))
                     timed_out = true;
         }
@@ -133,23 +146,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             for (int kt = 0; kt < nkt; ++kt) {
-                const int s = kt % kTcSplitStages;
-                if (!mbar_wait_bounded(split_full(s), (kt / kTcSplitStages) & 1, tmo)) {
+                const int s = kt % T::kSplitStages;
+                if (!mbar_wait_bounded(split_full(s), (kt / T::kSplitStages) & 1, tmo)) {
                     timed_out = true;
                     break;
                 }
                 tc_fence_after_sync();
-                const uint32_t a_big = split(s), a_small = a_big + kTcOpBytes;
-                const uint32_t b_big = a_big + 2 * kTcOpBytes, b_small = a_big + 3 * kTcOpBytes;
+                const uint32_t a_big = split(s), a_small = a_big + T::kOpABytes;
+                const uint32_t b_big = a_big + 2 * T::kOpABytes, b_small = b_big + T::kOpBBytes;
 #pragma unroll
-                for (int kk = 0; kk < kTcBK / 8; ++kk) {  // k-steps of 8 TF32 = 32 bytes of each row
+                for (int kk = 0; kk < BK / 8; ++kk) {  // k-steps of 8 TF32 = 32 bytes of each row
                     const uint32_t off = static_cast<uint32_t>(kk * 32);
-                    umma_tf32(tmem, umma_desc_kmajor_sw128(a_small + off), umma_desc_kmajor_sw128(b_big + off),
-                              kTcIdesc, kt > 0 || kk > 0);
-                    umma_tf32(tmem, umma_desc_kmajor_sw128(a_big + off), umma_desc_kmajor_sw128(b_small + off),
-                              kTcIdesc, true);
-                    umma_tf32(tmem, umma_desc_kmajor_sw128(a_big + off), umma_desc_kmajor_sw128(b_big + off),
-                              kTcIdesc, true);
+                    umma_tf32(tmem, tc_operand_desc<BK>(a_small + off), tc_operand_desc<BK>(b_big + off), T::kIdesc,
+                              kt > 0 || kk > 0);
+                    umma_tf32(tmem, tc_operand_desc<BK>(a_big + off), tc_operand_desc<BK>(b_small + off), T::kIdesc,
+                              true);
+                    umma_tf32(tmem, tc_operand_desc<BK>(a_big + off), tc_operand_desc<BK>(b_big + off), T::kIdesc,
+                              true);
                 }
                 umma_commit(split_empty(s));  // stage s is free once these MMAs are done
             }
@@ -160,14 +173,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // ------------------------------------------------------------ split + epilogue
         const int tt = threadIdx.x - 64;  // 0 .. 32 * kTcSplitWarps - 1
         constexpr int kSplitThreads = 32 * kTcSplitWarps;
-        constexpr int kAChunks = kTcRawABytes / 16 / kSplitThreads;  // 16-byte A chunks per thread
-        constexpr int kBGroups = (kTcBN * kTcBK / 4) / kSplitThreads;  // (column, 4-k) groups per thread
-        const int bn = tt % kTcBN;                                      // B column of this thread
-        const int bc0 = (tt / kTcBN) * kBGroups;                        // its first 4-k group
+        constexpr int kAChunks = T::kRawABytes / 16 / kSplitThreads;  // 16-byte A chunks per thread
+        constexpr int kBGroups = (BN * BK / 4) / kSplitThreads;  // (column, 4-k) groups per thread
+        const int bn = tt % BN;                                      // B column of this thread
+        const int bc0 = (tt / BN) * kBGroups;                        // its first 4-k group
         for (int kt = 0; kt < nkt; ++kt) {
-            const int r = kt % kTcRawStages;
-            const int s = kt % kTcSplitStages;
-            if (!mbar_wait_bounded_warp(raw_full(r), (kt / kTcRawStages) & 1, tmo)) {
+            const int r = kt % T::kRawStages;
+            const int s = kt % T::kSplitStages;
+            if (!mbar_wait_bounded_warp(raw_full(r), (kt / T::kRawStages) & 1, tmo)) {
                 timed_out = true;
                 break;
             }
@@ -183,16 +196,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 for (int i = 0; i < 4; ++i)
                     asm volatile("ld.shared.f32 %0, [%1];"
                                  : "=f"(bv[c][i])
-                                 : "r"(rb + static_cast<uint32_t>((4 * (bc0 + c) + i) * kTcBN * 4)));
-            if (kt >= kTcSplitStages &&
-                !mbar_wait_bounded_warp(split_empty(s), ((kt / kTcSplitStages) - 1) & 1, tmo)) {
+                                 : "r"(rb + static_cast<uint32_t>((4 * (bc0 + c) + i) * BN * 4)));
+            if (kt >= T::kSplitStages &&
+                !mbar_wait_bounded_warp(split_empty(s), ((kt / T::kSplitStages) - 1) & 1, tmo)) {
                 timed_out = true;
                 break;
             }
-            const uint32_t a_big = split(s), a_small = a_big + kTcOpBytes;
-            const uint32_t b_big = a_big + 2 * kTcOpBytes, b_small = a_big + 3 * kTcOpBytes;
-            // A: the TMA wrote the slice K-major with the same 128-byte swizzle
-            // the MMA reads, so the split is element-wise on 16-byte chunks.
+            const uint32_t a_big = split(s), a_small = a_big + T::kOpABytes;
+            const uint32_t b_big = a_big + 2 * T::kOpABytes, b_small = b_big + T::kOpBBytes;
+            // A: the TMA wrote the slice K-major with the same swizzle the MMA
+            // reads, so the split is element-wise on 16-byte chunks.
 #pragma unroll
             for (int j = 0; j < kAChunks; ++j) {
                 const uint32_t off = static_cast<uint32_t>((tt + kSplitThreads * j) * 16);
@@ -204,9 +217,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 sts128(a_big + off, hi);
                 sts128(a_small + off, lo);
             }
-            // B: the slice arrives as 32 rows (k) of 128 floats (n).  Column
+            // B: the slice arrives as BK rows (k) of BN floats (n).  Column
             // n = bn becomes row bn of the K-major tiles: the 16-byte chunk of
-            // k = 4c..4c+3 goes to chunk position c ^ (bn mod 8).
+            // k = 4c..4c+3 goes to chunk position c XOR the row's swizzle key,
+            // address bits 7 and up of the row (bn mod 8 for 128-byte rows,
+            // (bn / 2) mod 4 for 64-byte rows).
 #pragma unroll
             for (int c = 0; c < kBGroups; ++c) {
                 float4 hi, lo;
@@ -214,7 +229,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 split_tf32(bv[c][1], hi.y, lo.y);
                 split_tf32(bv[c][2], hi.z, lo.z);
                 split_tf32(bv[c][3], hi.w, lo.w);
-                const uint32_t off = static_cast<uint32_t>(bn * 128 + ((((bc0 + c) ^ bn) & 7) << 4));
+                const int key = (bn * T::kRowBytes) >> 7;
+                const uint32_t off = static_cast<uint32_t>(bn * T::kRowBytes + ((((bc0 + c) ^ key) & (BK / 4 - 1)) << 4));
                 sts128(b_big + off, hi);
                 sts128(b_small + off, lo);
             }
@@ -234,7 +250,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             tc_fence_after_sync();
             const int q = warp & 3;
             const int half = (warp - 2) / 4;  // which of the warps on this quarter
-            constexpr int kChunksPerWarp = (kTcBN / 32) / (kTcSplitWarps / 4);
+            constexpr int kChunksPerWarp = (BN / 32) / (kTcSplitWarps / 4);
             const int row = m0 + 32 * q + lane;
             float* crow = p.C + static_cast<long long>(row) * p.ldc;
 #pragma unroll
@@ -268,7 +284,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     __syncthreads();
     if (warp == 1) {
         tc_fence_after_sync();
-        tmem_dealloc(tmem, kTcTmemCols);
+        tmem_dealloc(tmem, T::kTmemCols);
     }
 }
 

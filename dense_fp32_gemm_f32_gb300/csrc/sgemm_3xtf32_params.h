@@ -28,6 +28,36 @@ constexpr int kTcSmemBytes = kTcRingBytes + 1024 /*align*/ + 256 /*barriers*/;
 constexpr uint32_t kTcIdesc = (1u << 4) | (2u << 7) | (2u << 10) | (static_cast<uint32_t>(kTcBN >> 3) << 17) |
                               (static_cast<uint32_t>(kTcBM >> 4) << 24);
 
+// Shapes of the split-tile kernel, sgemm_3xtf32_kernel<BN, BK>: 128 x BN
+// output tiles, K-slices of BK.  <128, 32> (variant 1): 128-byte operand rows
+// (128-byte swizzle), 3 raw and 2 split stages, 224 KiB.  <256, 16> (variant
+// 3): 256-wide tiles, so that each A element read by the tensor core and each
+// A element split serves twice the columns (a quarter less shared-memory
+// traffic per product), on 64-byte rows (64-byte swizzle) to keep 4 raw and 2
+// split stages in 192 KiB; 256 tensor-memory columns.
+template <int BN, int BK>
+struct TcShape {
+    static_assert((BN == 128 && BK == 32) || (BN == 256 && BK == 16), "built shapes");
+    static constexpr int kBM = 128;
+    static constexpr int kRowBytes = BK * 4;          // one K-major operand row
+    static constexpr int kSwizzle = kRowBytes;        // 128- or 64-byte swizzle
+    static constexpr int kRawABytes = kBM * BK * 4;   // TMA A slice, swizzled rows
+    static constexpr int kRawBBytes = BK * BN * 4;    // TMA B slice, BN-float rows
+    static constexpr int kOpABytes = kBM * BK * 4;    // one K-major A operand tile
+    static constexpr int kOpBBytes = BN * BK * 4;     // one K-major B operand tile
+    static constexpr int kSplitBytes = 2 * kOpABytes + 2 * kOpBBytes;  // A_big, A_small, B_big, B_small
+    static constexpr int kRawStages = BK == 32 ? 3 : 4;
+    static constexpr int kSplitStages = 2;
+    static constexpr int kRingBytes = kRawStages * (kRawABytes + kRawBBytes) + kSplitStages * kSplitBytes;
+    static constexpr int kSmemBytes = kRingBytes + 1024 /*align*/ + 256 /*barriers*/;
+    static constexpr int kTmemCols = BN;
+    // Instruction descriptor as kTcIdesc, N = BN.
+    static constexpr uint32_t kIdesc = (1u << 4) | (2u << 7) | (2u << 10) | (static_cast<uint32_t>(BN >> 3) << 17) |
+                                       (static_cast<uint32_t>(kBM >> 4) << 24);
+};
+static_assert(TcShape<128, 32>::kSmemBytes == kTcSmemBytes, "variant 1 keeps its layout");
+static_assert(TcShape<256, 16>::kSmemBytes <= 227 * 1024, "shared memory of variant 3");
+
 struct TcParams {
     int M, N, K;
     float* C;

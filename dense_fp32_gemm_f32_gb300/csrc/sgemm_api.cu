@@ -35,8 +35,6 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;  // 2 s per wait
-// sgemm_3xtf32 kernel chosen when not forced: 1 = split-tile, 2 = direct-A.
-constexpr int kTf32x3DefaultVariant = 1;
 
 // Stream-K scratch kept for one stream (see sk_lease): partial tiles and
 // ready flags, allocated once and reused by every call on that stream.
@@ -190,7 +188,8 @@ int init_device(int dev, DeviceState& st) {
             }
         }
     }
-    if (set_smem_attr(tf32x3_kernel()) != SGEMM_OK || set_smem_attr(tf32x3_direct_kernel()) != SGEMM_OK)
+    if (set_smem_attr(tf32x3_kernel()) != SGEMM_OK || set_smem_attr(tf32x3_direct_kernel()) != SGEMM_OK ||
+        set_smem_attr(tf32x3_wide_kernel()) != SGEMM_OK)
         return SGEMM_ERR_CUDA;
     const KernelEntry ref = ffma_kernel_tma(4, kMathFfma2);
     st.max_clusters_pair = max_active_clusters(ref, 2, 1);
@@ -1187,9 +1186,15 @@ int run_3xtf32(int M, int N, int K, const float* A, int lda, const float* B, int
     // sgemm_f32); otherwise they, and K == 0, take the FFMA kernel, which
     // meets the same contract.
     // Variant: 1 = split-tile kernel (all four TF32 parts in shared memory),
-    // 2 = direct-A kernel (A's big part is the TMA tile itself).
-    const int variant = (opt && opt->math) ? opt->math : kTf32x3DefaultVariant;
-    if (variant < 1 || variant > 2) return SGEMM_ERR_INVALID_ARG;
+    // 2 = direct-A kernel (A's big part is the TMA tile itself), 3 = the
+    // split-tile kernel on 128 x 256 tiles with K-slices of 16.  Automatic:
+    // 3 when its tiles number at least half the SMs, else 1 (measured on
+    // GB300, TFLOP/s for 1 / 3: 2048^3 154 / 181, 4096^3 195 / 201, 8192^3
+    // 205 / 241, 4096 x 4096 x 256 102 / 112; with fewer tiles 1024^3 61 /
+    // 40, 8192 x 128 x 8192 82 / 51).
+    int variant = (opt && opt->math) ? opt->math : 0;
+    if (variant == 0) variant = 2 * ceil_div(M, kTcBM) * ceil_div(N, 256) >= st->sm_count ? 3 : 1;
+    if (variant < 1 || variant > 3) return SGEMM_ERR_INVALID_ARG;
     const cudaStream_t cs = static_cast<cudaStream_t>(stream);
     const int misaligned = (tma_ok(A, lda) ? 0 : 1) | (tma_ok(B, ldb) ? 0 : 2);
     Repacked packed;
@@ -1200,11 +1205,13 @@ int run_3xtf32(int M, int N, int K, const float* A, int lda, const float* B, int
         packed.release();
         return run_ffma(M, N, K, A, lda, B, ldb, C, ldc, stream, nullptr);
     }
-    const KernelEntry k = variant == 1 ? tf32x3_kernel() : tf32x3_direct_kernel();
+    const KernelEntry k = variant == 1 ? tf32x3_kernel() : variant == 2 ? tf32x3_direct_kernel() : tf32x3_wide_kernel();
+    const int bn = variant == 3 ? 256 : kTcBN;  // output tile width
+    const int bk = variant == 3 ? 16 : kTcBK;                          // K-slice
     alignas(64) CUtensorMap tmA;
     alignas(64) CUtensorMap tmB;
-    rc = encode_2d(&tmA, A, K, M, lda, kTcBK, kTcBM, CU_TENSOR_MAP_SWIZZLE_128B);
-    if (rc == SGEMM_OK) rc = encode_2d(&tmB, B, N, K, ldb, kTcBN, kTcBK, CU_TENSOR_MAP_SWIZZLE_NONE);
+    rc = encode_2d(&tmA, A, K, M, lda, bk, kTcBM, bk == 32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
+    if (rc == SGEMM_OK) rc = encode_2d(&tmB, B, N, K, ldb, bn, bk, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (rc != SGEMM_OK) {
         packed.release();
         return rc;
@@ -1216,8 +1223,8 @@ int run_3xtf32(int M, int N, int K, const float* A, int lda, const float* B, int
     prm.K = K;
     prm.C = C;
     prm.ldc = ldc;
-    prm.num_k_tiles = static_cast<int>(ceil_div(K, kTcBK));
-    prm.tiles_n = static_cast<int>(ceil_div(N, kTcBN));
+    prm.num_k_tiles = static_cast<int>(ceil_div(K, bk));
+    prm.tiles_n = static_cast<int>(ceil_div(N, bn));
     prm.vec_store = ((reinterpret_cast<uintptr_t>(C) & 15u) == 0 && ldc % 4 == 0) ? 1 : 0;
     prm.skip_stage = opt ? opt->debug_skip_stage : 0;
     prm.timeout_ns = (opt && opt->timeout_ns) ? opt->timeout_ns : kDefaultTimeoutNs;

@@ -195,8 +195,11 @@ int sgemm_f32_gemm(int transa, int transb,
  * is split into a TF32 "big" part, big = tf32(x), and a TF32 "small" part,
  * small = tf32(x - big), and three TF32 products (small*big + big*small +
  * big*big) are accumulated in float32 in tensor memory.  The dropped terms
- * are below 2^-22 |a||b| each.  Needs TMA-readable operands (16-byte aligned
- * bases and row strides) and K > 0; other calls run the sgemm_f32 kernels.
+ * are below 2^-22 |a||b| each.  The kernels read their operands through
+ * tensor maps: operands without 16-byte aligned bases and row strides are
+ * copied into pitched rows first when 2MNK >= 2^30; smaller such calls, and
+ * K = 0, run the sgemm_f32 kernels.  Tiles of 128 x 256 when those number at
+ * least half the SMs, else 128 x 128 (see sgemm_3xtf32_ex).
  * Tensor cores are not on the pages' own path; this entry is reported
  * separately from sgemm_f32.
  */
@@ -297,12 +300,14 @@ int sgemm_f32_ex(int M, int N, int K,
                  void* stream, const sgemm_options* opt);
 
 /* sgemm_3xtf32 with forced choices.  Uses the fields debug_skip_stage,
- * timeout_ns and math, which here selects the tensor-core kernel: 0 = auto,
+ * timeout_ns and math, which here selects the tensor-core kernel: 0 = auto
+ * (3 when the 128 x 256 tiles number at least half the SMs, else 1),
  * 1 = split-tile kernel (TF32 big and small parts of both operands stored in
  * shared memory), 2 = direct-A kernel (A's big part is the FP32 tile the TMA
  * lands, read by the tensor core at TF32 precision; only A's small part and
- * B's two parts are stored).  Both use 128 x 128 tiles.  Other fields are
- * ignored. */
+ * B's two parts are stored), both on 128 x 128 tiles; 3 = the split-tile
+ * kernel on 128 x 256 tiles with K-slices of 16 (each A element serves twice
+ * the columns).  Other fields are ignored. */
 int sgemm_3xtf32_ex(int M, int N, int K,
                     const float* A, int lda,
                     const float* B, int ldb,

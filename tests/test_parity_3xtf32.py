@@ -24,8 +24,8 @@ def cuda_device():
 
 
 # 0 = the automatic choice of sgemm_3xtf32; 1 = split-tile kernel; 2 =
-# direct-A kernel.
-VARIANTS = [0, 1, 2]
+# direct-A kernel; 3 = split-tile kernel on 128 x 256 tiles, K-slices of 16.
+VARIANTS = [0, 1, 2, 3]
 
 
 def run(A, B, *, lda=None, ldb=None, ldc=None, variant=0):
@@ -142,7 +142,7 @@ def test_k_zero_writes_zeros():
     assert np.array_equal(C, np.zeros((40, 36), np.float32))
 
 
-@pytest.mark.parametrize("variant", [1, 2])
+@pytest.mark.parametrize("variant", [1, 2, 3])
 def test_timeout_is_reported_and_recovers(variant):
     """CTA 0's producer skips a K slice: its split warps' bounded wait
     expires, the MMA issuer and the epilogue give up in turn, tensor memory is
