@@ -85,9 +85,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int tile = static_cast<int>(blockIdx.x);
-    const int n0 = (tile % p.tiles_n) * BN;
-    const int m0 = (tile / p.tiles_n) * T::kBM;
+    const int tile = p.tile_base + static_cast<int>(blockIdx.x);
+    int m0, n0;
+    if (p.wide_halves) {  // a 128 x BN half of a 128 x 2BN tile (the tail of the wide-tile launch)
+        const int w = p.tile_base + static_cast<int>(blockIdx.x >> 1);
+        m0 = (w / p.tiles_n) * T::kBM;
+        n0 = (w % p.tiles_n) * (2 * BN) + static_cast<int>(blockIdx.x & 1) * BN;
+    } else {
+        m0 = (tile / p.tiles_n) * T::kBM;
+        n0 = (tile % p.tiles_n) * BN;
+    }
     const int nkt = p.num_k_tiles;
     const unsigned long long tmo = p.timeout_ns;
 
@@ -124,7 +131,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             int issued_round[T::kRawStages];
 #pragma unroll
             for (int r = 0; r < T::kRawStages; ++r) issued_round[r] = -1;
-            const bool skip_here = p.skip_stage > 0 && tile == 0;
+            const bool skip_here = p.skip_stage > 0 && tile == 0 && !p.wide_halves;
             for (int kt = 0; kt < nkt; ++kt) {
                 const int r = kt % T::kRawStages;
                 const int round = kt / T::kRawStages;

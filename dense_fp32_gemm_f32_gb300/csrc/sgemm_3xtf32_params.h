@@ -62,13 +62,15 @@ struct TcParams {
     int M, N, K;
     float* C;
     long long ldc;
-    int num_k_tiles;  // ceil(K / kTcBK)
-    int tiles_n;      // output tiles per row of tiles
+    int num_k_tiles;  // ceil(K / BK)
+    int tiles_n;      // output tiles per row of tiles (of the wide tiles when wide_halves)
+    int tile_base;    // this launch's first tile (split-tile kernels)
+    int wide_halves;  // split-tile kernels: CTA j takes the (j & 1) half of tile
+                      // tile_base + j / 2 of twice the CTA's width
     int vec_store;    // C base 16-byte aligned and ldc % 4 == 0
     int skip_stage;   // debug: CTA 0's producer never issues K-slice skip_stage-1
     unsigned long long timeout_ns;
     unsigned int* status;
-    int dbg;
 };
 
 // ---- "direct-A" variant: the TF32 big part of A is the FP32 tile itself

@@ -1205,43 +1205,72 @@ int run_3xtf32(int M, int N, int K, const float* A, int lda, const float* B, int
         packed.release();
         return run_ffma(M, N, K, A, lda, B, ldb, C, ldc, stream, nullptr);
     }
-    const KernelEntry k = variant == 1 ? tf32x3_kernel() : variant == 2 ? tf32x3_direct_kernel() : tf32x3_wide_kernel();
-    const int bn = variant == 3 ? 256 : kTcBN;  // output tile width
-    const int bk = variant == 3 ? 16 : kTcBK;                          // K-slice
-    alignas(64) CUtensorMap tmA;
-    alignas(64) CUtensorMap tmB;
-    rc = encode_2d(&tmA, A, K, M, lda, bk, kTcBM, bk == 32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
-    if (rc == SGEMM_OK) rc = encode_2d(&tmB, B, N, K, ldb, bn, bk, CU_TENSOR_MAP_SWIZZLE_NONE);
-    if (rc != SGEMM_OK) {
-        packed.release();
-        return rc;
+    // Launches: (kernel, tile width, K-slice, grid, first tile, halves of wide
+    // tiles).  Variant 3 runs whole waves of 128 x 256 tiles; the wide tiles
+    // of a last partial wave run as twice as many 128 x 128 tiles of the
+    // variant-1 kernel (a second launch), which fill that wave better
+    // (4096^3: 3 waves of 152 wide tiles, then 112 narrow tiles).
+    struct TcLaunch {
+        KernelEntry k;
+        int bn, bk;
+        long long grid;
+        int tile_base, wide_halves;
+    };
+    TcLaunch launches[2];
+    int nl = 1;
+    const long long tiles_m = ceil_div(M, kTcBM);
+    if (variant == 3) {
+        const long long wide = tiles_m * ceil_div(N, 256);
+        const long long full = (wide / st->sm_count) * st->sm_count;
+        if (full > 0 && full < wide) {
+            launches[0] = {tf32x3_wide_kernel(), 256, 16, full, 0, 0};
+            launches[1] = {tf32x3_kernel(), kTcBN, kTcBK, 2 * (wide - full), static_cast<int>(full), 1};
+            nl = 2;
+        } else {
+            launches[0] = {tf32x3_wide_kernel(), 256, 16, wide, 0, 0};
+        }
+    } else {
+        const KernelEntry k = variant == 1 ? tf32x3_kernel() : tf32x3_direct_kernel();
+        launches[0] = {k, kTcBN, kTcBK, tiles_m * ceil_div(N, kTcBN), 0, 0};
     }
 
-    TcParams prm;
-    prm.M = M;
-    prm.N = N;
-    prm.K = K;
-    prm.C = C;
-    prm.ldc = ldc;
-    prm.num_k_tiles = static_cast<int>(ceil_div(K, bk));
-    prm.tiles_n = static_cast<int>(ceil_div(N, bn));
-    prm.vec_store = ((reinterpret_cast<uintptr_t>(C) & 15u) == 0 && ldc % 4 == 0) ? 1 : 0;
-    prm.skip_stage = opt ? opt->debug_skip_stage : 0;
-    prm.timeout_ns = (opt && opt->timeout_ns) ? opt->timeout_ns : kDefaultTimeoutNs;
-    prm.status = st->status_word;
-    const long long tiles = ceil_div(M, kTcBM) * static_cast<long long>(prm.tiles_n);
-
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(tiles), 1, 1);
-    cfg.blockDim = dim3(k.threads, 1, 1);
-    cfg.dynamicSmemBytes = static_cast<size_t>(k.smem_bytes);
-    cfg.stream = static_cast<cudaStream_t>(stream);
-    cfg.numAttrs = 0;
-    void* args[3] = {&tmA, &tmB, &prm};
     rc = SGEMM_OK;
-    if (cudaLaunchKernelExC(&cfg, k.fn, args) != cudaSuccess) {
-        (void)cudaGetLastError();
-        rc = SGEMM_ERR_CUDA;
+    for (int l = 0; l < nl && rc == SGEMM_OK; ++l) {
+        const TcLaunch& ln = launches[l];
+        alignas(64) CUtensorMap tmA;
+        alignas(64) CUtensorMap tmB;
+        rc = encode_2d(&tmA, A, K, M, lda, ln.bk, kTcBM,
+                       ln.bk == 32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
+        if (rc == SGEMM_OK) rc = encode_2d(&tmB, B, N, K, ldb, ln.bn, ln.bk, CU_TENSOR_MAP_SWIZZLE_NONE);
+        if (rc != SGEMM_OK) break;
+
+        TcParams prm;
+        prm.M = M;
+        prm.N = N;
+        prm.K = K;
+        prm.C = C;
+        prm.ldc = ldc;
+        prm.num_k_tiles = static_cast<int>(ceil_div(K, ln.bk));
+        // (halves of wide tiles: tiles are counted in wide tiles per row)
+        prm.tiles_n = static_cast<int>(ceil_div(N, ln.wide_halves ? 2 * ln.bn : ln.bn));
+        prm.tile_base = ln.tile_base;
+        prm.wide_halves = ln.wide_halves;
+        prm.vec_store = ((reinterpret_cast<uintptr_t>(C) & 15u) == 0 && ldc % 4 == 0) ? 1 : 0;
+        prm.skip_stage = opt ? opt->debug_skip_stage : 0;
+        prm.timeout_ns = (opt && opt->timeout_ns) ? opt->timeout_ns : kDefaultTimeoutNs;
+        prm.status = st->status_word;
+
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(ln.grid), 1, 1);
+        cfg.blockDim = dim3(ln.k.threads, 1, 1);
+        cfg.dynamicSmemBytes = static_cast<size_t>(ln.k.smem_bytes);
+        cfg.stream = static_cast<cudaStream_t>(stream);
+        cfg.numAttrs = 0;
+        void* args[3] = {&tmA, &tmB, &prm};
+        if (cudaLaunchKernelExC(&cfg, ln.k.fn, args) != cudaSuccess) {
+            (void)cudaGetLastError();
+            rc = SGEMM_ERR_CUDA;
+        }
     }
     packed.release();
     return rc;

@@ -142,6 +142,21 @@ def test_k_zero_writes_zeros():
     assert np.array_equal(C, np.zeros((40, 36), np.float32))
 
 
+@pytest.mark.parametrize("shape", [(1200, 4000, 300), (1200, 3852, 96), (1300, 4100, 40)])
+@pytest.mark.parametrize("dist", ["uniform", "int"])
+def test_wide_tiles_with_narrow_tail(shape, dist):
+    """Variant 3 with more 128 x 256 tiles than SMs: whole waves of wide
+    tiles, then the last partial wave's wide tiles as pairs of 128 x 128
+    tiles in a second launch (1200 x 4000: 160 wide tiles, the last wide
+    column 160 floats wide; 1200 x 3852: the second half of each last wide
+    tile lies wholly beyond N; K = 300 / 96 / 40 ragged against both K-slices)."""
+    M, N, K = shape
+    A, B = make_operands(M, N, K, dist, 81)
+    exact = dist == "int"
+    C64, bound = oracle.gemm_f64(A.numpy(), B.numpy(), with_bound=not exact)
+    check(run(A, B, variant=3), C64, bound, exact=exact, what=f"wide tail {shape} {dist}")
+
+
 @pytest.mark.parametrize("variant", [1, 2, 3])
 def test_timeout_is_reported_and_recovers(variant):
     """CTA 0's producer skips a K slice: its split warps' bounded wait
