@@ -463,8 +463,8 @@ def run_ours(args, rank, world, local_rank):
     return 0
 
 
-# sgemm_3xtf32 kernels: 1 = split-tile, 2 = direct-A, 3 = split-tile on 128 x 256 tiles.
-SWEEP_TF32X3_VARIANTS = [1, 2, 3]
+# sgemm_3xtf32 kernels: 1 = split-tile, 2 = direct-A, 3 = split-tile on 128 x 256 tiles, 4 = 3 with B pre-split.
+SWEEP_TF32X3_VARIANTS = [1, 2, 3, 4]
 SWEEP_OPTIONS = [
     {},
     {"producer": 1},

@@ -137,7 +137,8 @@ def sgemm_f32_ex(A, B, out=None, *, stream=None, producer=0, split_k=0, multicas
 def sgemm_3xtf32_ex(A, B, out=None, *, stream=None, variant=0, debug_skip_stage=0, timeout_ns=0) -> torch.Tensor:
     """sgemm_3xtf32 with forced choices: ``variant`` 1 = split-tile kernel,
     2 = direct-A kernel, 3 = split-tile kernel on 128 x 256 tiles with
-    K-slices of 16 (0 = automatic)."""
+    K-slices of 16, 4 = variant 3 with B's TF32 parts pre-split in HBM
+    (0 = automatic)."""
     opt = Options(0, 0, 0, variant, 0, debug_skip_stage, timeout_ns, 0, 0, 0, 0, 0)
     return _call("sgemm_3xtf32_ex", A, B, out, stream, opt)
 

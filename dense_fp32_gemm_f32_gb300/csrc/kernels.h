@@ -79,6 +79,14 @@ struct SmallParams {
     float alpha, beta;
 };
 KernelEntry small_kernel(bool a_mn, bool scaled);
+// B's TF32 parts, transposed: big (N x K, pitch ld_out: a multiple of 4, >= K;
+// 16-byte aligned base) = tf32(B^T), small = tf32(B^T - big); zeros in the
+// padding columns; B (K x N, pitch ldb) of any alignment.  One launch on `stream`.
+int split_transpose_b(const float* B, long long ldb, int K, int N, float* big, float* small, long long ld_out,
+                      cudaStream_t stream);
+// The split-tile kernel on 128 x 256 tiles with B's TF32 parts pre-split by
+// split_transpose_b (loaded by the TMA; the kernel splits A only).
+KernelEntry tf32x3_wide_pb_kernel();
 // C = beta * C over M x N with pitch ldc (beta == 0: zeros, C not read).
 int scale_c(float* C, long long ldc, int M, int N, float beta, cudaStream_t stream);
 

@@ -137,6 +137,63 @@ int transpose_rows(const float* src0, long long ld_src0, float* dst0, long long 
 
 namespace {
 
+__device__ __forceinline__ float tf32_rna(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return __uint_as_float(r);
+}
+
+// B (K x N, pitch ldb, any alignment) -> its TF32 parts transposed, N x K
+// with pitch ld_out: big[n][k] = tf32(b), small[n][k] = tf32(b - big) (the
+// same split as the tensor-core kernels' split warps), zeros in the padding
+// columns k in [K, ld_out).  32 x 32 tiles through shared memory with one
+// padding column (coalesced reads along n, writes along k); blocks walk the
+// K direction in steps of gridDim.y.
+__global__ void __launch_bounds__(kTile* kTileRows)
+    split_transpose_kernel(const float* B, long long ldb, int K, int N, float* big, float* small, long long ld_out) {
+    __shared__ float tile[kTile][kTile + 1];
+    const int n0 = static_cast<int>(blockIdx.x) * kTile;
+    for (long long k0 = static_cast<long long>(blockIdx.y) * kTile; k0 < ld_out;
+         k0 += static_cast<long long>(gridDim.y) * kTile) {
+#pragma unroll
+        for (int j = 0; j < kTile / kTileRows; ++j) {
+            const long long k = k0 + threadIdx.y + kTileRows * j;
+            const int n = n0 + static_cast<int>(threadIdx.x);
+            tile[threadIdx.y + kTileRows * j][threadIdx.x] = (k < K && n < N) ? B[k * ldb + n] : 0.f;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int j = 0; j < kTile / kTileRows; ++j) {
+            const int n = n0 + static_cast<int>(threadIdx.y) + kTileRows * j;
+            const long long k = k0 + threadIdx.x;
+            if (n < N && k < ld_out) {
+                const float v = tile[threadIdx.x][threadIdx.y + kTileRows * j];
+                const float hi = tf32_rna(v);
+                big[static_cast<long long>(n) * ld_out + k] = hi;
+                small[static_cast<long long>(n) * ld_out + k] = tf32_rna(v - hi);
+            }
+        }
+        __syncthreads();
+    }
+}
+
+}  // namespace
+
+int split_transpose_b(const float* B, long long ldb, int K, int N, float* big, float* small, long long ld_out,
+                      cudaStream_t stream) {
+    if (K <= 0 || N <= 0) return SGEMM_OK;
+    if (ld_out < K || ld_out % 4 != 0 || ldb < N) return SGEMM_ERR_INVALID_ARG;
+    const long long gx = (static_cast<long long>(N) + kTile - 1) / kTile;
+    const long long gy = std::min<long long>((ld_out + kTile - 1) / kTile, 65535);
+    if (gx > 0x7fffffffLL) return SGEMM_ERR_INVALID_ARG;
+    split_transpose_kernel<<<dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy)), dim3(kTile, kTileRows), 0,
+                             stream>>>(B, ldb, K, N, big, small, ld_out);
+    if (cudaGetLastError() != cudaSuccess) return SGEMM_ERR_CUDA;
+    return SGEMM_OK;
+}
+
+namespace {
+
 // C = beta * C over M x N (pitch ldc); beta == 0 writes zeros without reading.
 __global__ void __launch_bounds__(256) scale_kernel(float* C, long long ldc, int M, int N, float beta) {
     const long long c = static_cast<long long>(blockIdx.x) * 256 + threadIdx.x;

@@ -12,4 +12,9 @@ KernelEntry tf32x3_wide_kernel() {
     return {reinterpret_cast<const void*>(&sgemm_3xtf32_kernel<256, 16>), TcShape<256, 16>::kSmemBytes, kTcThreads};
 }
 
+KernelEntry tf32x3_wide_pb_kernel() {
+    return {reinterpret_cast<const void*>(&sgemm_3xtf32_kernel<256, 16, true>), TcShape<256, 16, true>::kSmemBytes,
+            kTcThreads};
+}
+
 }  // namespace gb300

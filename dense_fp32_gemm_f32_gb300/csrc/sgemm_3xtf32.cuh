@@ -60,11 +60,15 @@ __device__ __forceinline__ uint64_t tc_operand_desc(uint32_t saddr) {
         return umma_desc_kmajor_sw64(saddr);
 }
 
-template <int BN, int BK>
+// PB: B's TF32 parts come pre-split and transposed (N x K) from HBM: tmB maps
+// the big part and tmB2 the small part, each loaded by the TMA into its slot
+// of the split stage (arriving on split_full with the split warps, which then
+// write A's parts only).  Without PB, tmB maps B as stored and tmB2 is unused.
+template <int BN, int BK, bool PB = false>
 __global__ void __launch_bounds__(kTcThreads, 1)
     sgemm_3xtf32_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                        const TcParams p) {
-    using T = TcShape<BN, BK>;
+                        const __grid_constant__ CUtensorMap tmB2, const TcParams p) {
+    using T = TcShape<BN, BK, PB>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_base = smem_addr(smem_raw);
     const uint32_t base = (raw_base + 1023u) & ~1023u;
@@ -104,7 +108,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_init(raw_empty(r), kTcSplitWarps);  // one arrival per split warp
         }
         for (int s = 0; s < T::kSplitStages; ++s) {
-            mbar_init(split_full(s), kTcSplitWarps);
+            mbar_init(split_full(s), kTcSplitWarps + (PB ? 1 : 0));  // (+ the producer, for B's parts)
             mbar_init(split_empty(s), 1);  // tcgen05.commit
         }
         mbar_init(acc_full, 1);
@@ -117,6 +121,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (warp == 0 && lane == 0) {
         prefetch_tensormap(&tmA);
         prefetch_tensormap(&tmB);
+        if (PB) prefetch_tensormap(&tmB2);
     }
     tc_fence_before_sync();
     __syncthreads();
@@ -128,9 +133,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
-            int issued_round[T::kRawStages];
+            int issued_round[T::kRawStages], issued_sround[T::kSplitStages];
 #pragma unroll
             for (int r = 0; r < T::kRawStages; ++r) issued_round[r] = -1;
+#pragma unroll
+            for (int s = 0; s < T::kSplitStages; ++s) issued_sround[s] = -1;
             const bool skip_here = p.skip_stage > 0 && tile == 0 && !p.wide_halves;
             for (int kt = 0; kt < nkt; ++kt) {
                 const int r = kt % T::kRawStages;
@@ -139,15 +146,40 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     timed_out = true;
                     break;
                 }
+                if (PB) {
+                    // B's parts go straight into split stage s, once its MMAs are done.
+                    const int s = kt % T::kSplitStages;
+                    const int sround = kt / T::kSplitStages;
+                    if (sround > 0 && !mbar_wait_bounded(split_empty(s), (sround - 1) & 1, tmo)) {
+                        timed_out = true;
+                        break;
+                    }
+                }
                 if (skip_here && kt == p.skip_stage - 1) continue;
                 mbar_arrive_expect_tx(raw_full(r), T::kRawABytes + T::kRawBBytes);
                 tma_load_2d(rawA(r), &tmA, raw_full(r), kt * BK, m0);
-                tma_load_2d(rawB(r), &tmB, raw_full(r), n0, kt * BK);
+                if (PB) {
+                    const int s = kt % T::kSplitStages;
+                    const uint32_t b_big = split(s) + 2 * T::kOpABytes;
+                    mbar_arrive_expect_tx(split_full(s), 2 * T::kOpBBytes);
+                    tma_load_2d(b_big, &tmB, split_full(s), kt * BK, n0);
+                    tma_load_2d(b_big + T::kOpBBytes, &tmB2, split_full(s), kt * BK, n0);
+                    issued_sround[s] = kt / T::kSplitStages;
+                } else {
+                    tma_load_2d(rawB(r), &tmB, raw_full(r), n0, kt * BK);
+                }
                 issued_round[r] = round;
             }
             for (int r = 0; r < T::kRawStages; ++r)  // drain: every issued copy has landed
                 if (issued_round[r] >= 0 && !mbar_wait_bounded(raw_full(r), issued_round[r] & 1, tmo))
                     timed_out = true;
+            if (PB) {
+                // ... and B's parts: each split stage's last fill has completed
+                // (its earlier fills completed before the MMAs freed it).
+                for (int s = 0; s < T::kSplitStages; ++s)
+                    if (issued_sround[s] >= 0 && !mbar_wait_bounded(split_full(s), issued_sround[s] & 1, tmo))
+                        timed_out = true;
+            }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
@@ -195,15 +227,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             float4 av[kAChunks];
 #pragma unroll
             for (int j = 0; j < kAChunks; ++j) av[j] = lds128(rawA(r) + static_cast<uint32_t>((tt + kSplitThreads * j) * 16));
-            float bv[kBGroups][4];
-            const uint32_t rb = rawB(r) + static_cast<uint32_t>(bn * 4);
+            float bv[PB ? 1 : kBGroups][4];
+            if constexpr (!PB) {
+                const uint32_t rb = rawB(r) + static_cast<uint32_t>(bn * 4);
 #pragma unroll
-            for (int c = 0; c < kBGroups; ++c)
+                for (int c = 0; c < kBGroups; ++c)
 #pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    asm volatile("ld.shared.f32 %0, [%1];"
-                                 : "=f"(bv[c][i])
-                                 : "r"(rb + static_cast<uint32_t>((4 * (bc0 + c) + i) * BN * 4)));
+                    for (int i = 0; i < 4; ++i)
+                        asm volatile("ld.shared.f32 %0, [%1];"
+                                     : "=f"(bv[c][i])
+                                     : "r"(rb + static_cast<uint32_t>((4 * (bc0 + c) + i) * BN * 4)));
+            }
             if (kt >= T::kSplitStages &&
                 !mbar_wait_bounded_warp(split_empty(s), ((kt / T::kSplitStages) - 1) & 1, tmo)) {
                 timed_out = true;
@@ -229,17 +263,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // k = 4c..4c+3 goes to chunk position c XOR the row's swizzle key,
             // address bits 7 and up of the row (bn mod 8 for 128-byte rows,
             // (bn / 2) mod 4 for 64-byte rows).
+            // (PB: B's parts are already there, from the TMA.)
+            if constexpr (!PB) {
 #pragma unroll
-            for (int c = 0; c < kBGroups; ++c) {
-                float4 hi, lo;
-                split_tf32(bv[c][0], hi.x, lo.x);
-                split_tf32(bv[c][1], hi.y, lo.y);
-                split_tf32(bv[c][2], hi.z, lo.z);
-                split_tf32(bv[c][3], hi.w, lo.w);
-                const int key = (bn * T::kRowBytes) >> 7;
-                const uint32_t off = static_cast<uint32_t>(bn * T::kRowBytes + ((((bc0 + c) ^ key) & (BK / 4 - 1)) << 4));
-                sts128(b_big + off, hi);
-                sts128(b_small + off, lo);
+                for (int c = 0; c < kBGroups; ++c) {
+                    float4 hi, lo;
+                    split_tf32(bv[c][0], hi.x, lo.x);
+                    split_tf32(bv[c][1], hi.y, lo.y);
+                    split_tf32(bv[c][2], hi.z, lo.z);
+                    split_tf32(bv[c][3], hi.w, lo.w);
+                    const int key = (bn * T::kRowBytes) >> 7;
+                    const uint32_t off =
+                        static_cast<uint32_t>(bn * T::kRowBytes + ((((bc0 + c) ^ key) & (BK / 4 - 1)) << 4));
+                    sts128(b_big + off, hi);
+                    sts128(b_small + off, lo);
+                }
             }
             fence_proxy_async_smem();  // make the tiles visible to the tensor core
             __syncwarp();

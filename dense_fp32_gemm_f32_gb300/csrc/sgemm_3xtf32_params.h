@@ -35,19 +35,23 @@ constexpr uint32_t kTcIdesc = (1u << 4) | (2u << 7) | (2u << 10) | (static_cast<
 // A element split serves twice the columns (a quarter less shared-memory
 // traffic per product), on 64-byte rows (64-byte swizzle) to keep 4 raw and 2
 // split stages in 192 KiB; 256 tensor-memory columns.
-template <int BN, int BK>
+//
+// PB (pre-split B): B's TF32 parts come split and transposed from HBM (a
+// pass before the kernel), loaded by the TMA straight into the split stages;
+// the raw stages hold A only, so 4 raw and 4 split stages fit.
+template <int BN, int BK, bool PB = false>
 struct TcShape {
-    static_assert((BN == 128 && BK == 32) || (BN == 256 && BK == 16), "built shapes");
+    static_assert((BN == 128 && BK == 32 && !PB) || (BN == 256 && BK == 16), "built shapes");
     static constexpr int kBM = 128;
     static constexpr int kRowBytes = BK * 4;          // one K-major operand row
     static constexpr int kSwizzle = kRowBytes;        // 128- or 64-byte swizzle
     static constexpr int kRawABytes = kBM * BK * 4;   // TMA A slice, swizzled rows
-    static constexpr int kRawBBytes = BK * BN * 4;    // TMA B slice, BN-float rows
+    static constexpr int kRawBBytes = PB ? 0 : BK * BN * 4;  // TMA B slice, BN-float rows
     static constexpr int kOpABytes = kBM * BK * 4;    // one K-major A operand tile
     static constexpr int kOpBBytes = BN * BK * 4;     // one K-major B operand tile
     static constexpr int kSplitBytes = 2 * kOpABytes + 2 * kOpBBytes;  // A_big, A_small, B_big, B_small
     static constexpr int kRawStages = BK == 32 ? 3 : 4;
-    static constexpr int kSplitStages = 2;
+    static constexpr int kSplitStages = PB ? 4 : 2;
     static constexpr int kRingBytes = kRawStages * (kRawABytes + kRawBBytes) + kSplitStages * kSplitBytes;
     static constexpr int kSmemBytes = kRingBytes + 1024 /*align*/ + 256 /*barriers*/;
     static constexpr int kTmemCols = BN;
@@ -57,6 +61,7 @@ struct TcShape {
 };
 static_assert(TcShape<128, 32>::kSmemBytes == kTcSmemBytes, "variant 1 keeps its layout");
 static_assert(TcShape<256, 16>::kSmemBytes <= 227 * 1024, "shared memory of variant 3");
+static_assert(TcShape<256, 16, true>::kSmemBytes <= 227 * 1024, "shared memory of variant 4");
 
 struct TcParams {
     int M, N, K;

@@ -189,7 +189,7 @@ int init_device(int dev, DeviceState& st) {
         }
     }
     if (set_smem_attr(tf32x3_kernel()) != SGEMM_OK || set_smem_attr(tf32x3_direct_kernel()) != SGEMM_OK ||
-        set_smem_attr(tf32x3_wide_kernel()) != SGEMM_OK)
+        set_smem_attr(tf32x3_wide_kernel()) != SGEMM_OK || set_smem_attr(tf32x3_wide_pb_kernel()) != SGEMM_OK)
         return SGEMM_ERR_CUDA;
     const KernelEntry ref = ffma_kernel_tma(4, kMathFfma2);
     st.max_clusters_pair = max_active_clusters(ref, 2, 1);
@@ -1187,14 +1187,20 @@ int run_3xtf32(int M, int N, int K, const float* A, int lda, const float* B, int
     // meets the same contract.
     // Variant: 1 = split-tile kernel (all four TF32 parts in shared memory),
     // 2 = direct-A kernel (A's big part is the TMA tile itself), 3 = the
-    // split-tile kernel on 128 x 256 tiles with K-slices of 16.  Automatic:
-    // 3 when its tiles number at least half the SMs, else 1 (measured on
-    // GB300, TFLOP/s for 1 / 3: 2048^3 154 / 181, 4096^3 195 / 201, 8192^3
-    // 205 / 241, 4096 x 4096 x 256 102 / 112; with fewer tiles 1024^3 61 /
-    // 40, 8192 x 128 x 8192 82 / 51).
+    // split-tile kernel on 128 x 256 tiles with K-slices of 16, 4 = variant
+    // 3 with B's TF32 parts split and transposed in HBM by a pass before the
+    // kernel (one read of B and two writes of its size), which leaves the
+    // kernel's split warps A only.  Automatic: 4 when the 128 x 256 tiles
+    // number at least half the SMs and M >= 1024 (the pass costs ~6/M bytes
+    // per flop), 3 when they do with fewer rows, else 1.  Measured on GB300,
+    // TFLOP/s for 1 / 3 / 4: 2048^3 155 / 181 / 203, 4096^3 195 / 218 / 261,
+    // 8192^3 204 / 243 / 289, 4096 x 4096 x 256 102 / 112 / 116; with fewer
+    // tiles 1024^3 61 / 40 / 45, 8192 x 128 x 8192 82 / 51 / 71, 128 x 8192 x
+    // 16384 86 / 53 / 22.
     int variant = (opt && opt->math) ? opt->math : 0;
-    if (variant == 0) variant = 2 * ceil_div(M, kTcBM) * ceil_div(N, 256) >= st->sm_count ? 3 : 1;
-    if (variant < 1 || variant > 3) return SGEMM_ERR_INVALID_ARG;
+    if (variant == 0)
+        variant = 2 * ceil_div(M, kTcBM) * ceil_div(N, 256) < st->sm_count ? 1 : M >= 1024 ? 4 : 3;
+    if (variant < 1 || variant > 4) return SGEMM_ERR_INVALID_ARG;
     const cudaStream_t cs = static_cast<cudaStream_t>(stream);
     const int misaligned = (tma_ok(A, lda) ? 0 : 1) | (tma_ok(B, ldb) ? 0 : 2);
     Repacked packed;
@@ -1215,23 +1221,48 @@ int run_3xtf32(int M, int N, int K, const float* A, int lda, const float* B, int
         int bn, bk;
         long long grid;
         int tile_base, wide_halves;
+        bool pb;  // B's TF32 parts pre-split in HBM (variant 4)
     };
     TcLaunch launches[2];
     int nl = 1;
     const long long tiles_m = ceil_div(M, kTcBM);
-    if (variant == 3) {
+    if (variant >= 3) {
+        const KernelEntry wk = variant == 4 ? tf32x3_wide_pb_kernel() : tf32x3_wide_kernel();
+        const bool pb = variant == 4;
         const long long wide = tiles_m * ceil_div(N, 256);
         const long long full = (wide / st->sm_count) * st->sm_count;
         if (full > 0 && full < wide) {
-            launches[0] = {tf32x3_wide_kernel(), 256, 16, full, 0, 0};
-            launches[1] = {tf32x3_kernel(), kTcBN, kTcBK, 2 * (wide - full), static_cast<int>(full), 1};
+            launches[0] = {wk, 256, 16, full, 0, 0, pb};
+            launches[1] = {tf32x3_kernel(), kTcBN, kTcBK, 2 * (wide - full), static_cast<int>(full), 1, false};
             nl = 2;
         } else {
-            launches[0] = {tf32x3_wide_kernel(), 256, 16, wide, 0, 0};
+            launches[0] = {wk, 256, 16, wide, 0, 0, pb};
         }
     } else {
         const KernelEntry k = variant == 1 ? tf32x3_kernel() : tf32x3_direct_kernel();
-        launches[0] = {k, kTcBN, kTcBK, tiles_m * ceil_div(N, kTcBN), 0, 0};
+        launches[0] = {k, kTcBN, kTcBK, tiles_m * ceil_div(N, kTcBN), 0, 0, false};
+    }
+
+    // Variant 4: B's TF32 parts, transposed (N x K4), in a pool buffer.
+    void* ws = nullptr;
+    float *bt_big = nullptr, *bt_small = nullptr;
+    const long long K4 = (static_cast<long long>(K) + 3) / 4 * 4;
+    if (launches[0].pb) {
+        cudaMemPool_t pool = workspace_pool(dev, *st);
+        const size_t part = (static_cast<size_t>(N) * K4 * sizeof(float) + 255) & ~size_t{255};
+        if (!pool || cudaMallocFromPoolAsync(&ws, 2 * part, pool, cs) != cudaSuccess) {
+            (void)cudaGetLastError();
+            packed.release();
+            return SGEMM_ERR_CUDA;
+        }
+        bt_big = static_cast<float*>(ws);
+        bt_small = reinterpret_cast<float*>(static_cast<char*>(ws) + part);
+        rc = split_transpose_b(B, ldb, K, N, bt_big, bt_small, K4, cs);
+        if (rc != SGEMM_OK) {
+            (void)cudaFreeAsync(ws, cs);
+            packed.release();
+            return rc;
+        }
     }
 
     rc = SGEMM_OK;
@@ -1239,9 +1270,16 @@ int run_3xtf32(int M, int N, int K, const float* A, int lda, const float* B, int
         const TcLaunch& ln = launches[l];
         alignas(64) CUtensorMap tmA;
         alignas(64) CUtensorMap tmB;
-        rc = encode_2d(&tmA, A, K, M, lda, ln.bk, kTcBM,
-                       ln.bk == 32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
-        if (rc == SGEMM_OK) rc = encode_2d(&tmB, B, N, K, ldb, ln.bn, ln.bk, CU_TENSOR_MAP_SWIZZLE_NONE);
+        alignas(64) CUtensorMap tmB2;
+        const CUtensorMapSwizzle swz = ln.bk == 32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+        rc = encode_2d(&tmA, A, K, M, lda, ln.bk, kTcBM, swz);
+        if (ln.pb) {  // {k, n} boxes of the transposed parts, swizzled like A
+            if (rc == SGEMM_OK) rc = encode_2d(&tmB, bt_big, K, N, K4, ln.bk, ln.bn, swz);
+            if (rc == SGEMM_OK) rc = encode_2d(&tmB2, bt_small, K, N, K4, ln.bk, ln.bn, swz);
+        } else {
+            if (rc == SGEMM_OK) rc = encode_2d(&tmB, B, N, K, ldb, ln.bn, ln.bk, CU_TENSOR_MAP_SWIZZLE_NONE);
+            tmB2 = tmB;  // (unused)
+        }
         if (rc != SGEMM_OK) break;
 
         TcParams prm;
@@ -1266,12 +1304,14 @@ int run_3xtf32(int M, int N, int K, const float* A, int lda, const float* B, int
         cfg.dynamicSmemBytes = static_cast<size_t>(ln.k.smem_bytes);
         cfg.stream = static_cast<cudaStream_t>(stream);
         cfg.numAttrs = 0;
-        void* args[3] = {&tmA, &tmB, &prm};
-        if (cudaLaunchKernelExC(&cfg, ln.k.fn, args) != cudaSuccess) {
+        void* args4[4] = {&tmA, &tmB, &tmB2, &prm};
+        void* args3[3] = {&tmA, &tmB, &prm};  // (the direct-A kernel takes no second B map)
+        if (cudaLaunchKernelExC(&cfg, ln.k.fn, variant == 2 ? args3 : args4) != cudaSuccess) {
             (void)cudaGetLastError();
             rc = SGEMM_ERR_CUDA;
         }
     }
+    if (ws) (void)cudaFreeAsync(ws, cs);
     packed.release();
     return rc;
 }

@@ -199,7 +199,8 @@ int sgemm_f32_gemm(int transa, int transb,
  * tensor maps: operands without 16-byte aligned bases and row strides are
  * copied into pitched rows first when 2MNK >= 2^30; smaller such calls, and
  * K = 0, run the sgemm_f32 kernels.  Tiles of 128 x 256 when those number at
- * least half the SMs, else 128 x 128 (see sgemm_3xtf32_ex).
+ * least half the SMs (with B's TF32 parts split in a pass before the kernel
+ * when M >= 1024), else 128 x 128 (see sgemm_3xtf32_ex).
  * Tensor cores are not on the pages' own path; this entry is reported
  * separately from sgemm_f32.
  */
@@ -301,13 +302,18 @@ int sgemm_f32_ex(int M, int N, int K,
 
 /* sgemm_3xtf32 with forced choices.  Uses the fields debug_skip_stage,
  * timeout_ns and math, which here selects the tensor-core kernel: 0 = auto
- * (3 when the 128 x 256 tiles number at least half the SMs, else 1),
+ * (when the 128 x 256 tiles number at least half the SMs: 4 if M >= 1024,
+ * else 3; otherwise 1),
  * 1 = split-tile kernel (TF32 big and small parts of both operands stored in
  * shared memory), 2 = direct-A kernel (A's big part is the FP32 tile the TMA
  * lands, read by the tensor core at TF32 precision; only A's small part and
  * B's two parts are stored), both on 128 x 128 tiles; 3 = the split-tile
  * kernel on 128 x 256 tiles with K-slices of 16 (each A element serves twice
- * the columns).  Other fields are ignored. */
+ * the columns); 4 = variant 3 with B's TF32 parts split and transposed into a
+ * pool buffer first (2 x N x K floats; the kernel loads them with the TMA and
+ * splits A only).  3 and 4 run whole waves of 128 x 256 tiles and the tiles
+ * of a last partial wave as pairs of variant-1 tiles.  Other fields are
+ * ignored. */
 int sgemm_3xtf32_ex(int M, int N, int K,
                     const float* A, int lda,
                     const float* B, int ldb,

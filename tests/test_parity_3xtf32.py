@@ -24,8 +24,9 @@ def cuda_device():
 
 
 # 0 = the automatic choice of sgemm_3xtf32; 1 = split-tile kernel; 2 =
-# direct-A kernel; 3 = split-tile kernel on 128 x 256 tiles, K-slices of 16.
-VARIANTS = [0, 1, 2, 3]
+# direct-A kernel; 3 = split-tile kernel on 128 x 256 tiles, K-slices of 16;
+# 4 = the same with B's TF32 parts split and transposed in HBM first.
+VARIANTS = [0, 1, 2, 3, 4]
 
 
 def run(A, B, *, lda=None, ldb=None, ldc=None, variant=0):
@@ -142,9 +143,10 @@ def test_k_zero_writes_zeros():
     assert np.array_equal(C, np.zeros((40, 36), np.float32))
 
 
+@pytest.mark.parametrize("variant", [3, 4])
 @pytest.mark.parametrize("shape", [(1200, 4000, 300), (1200, 3852, 96), (1300, 4100, 40)])
 @pytest.mark.parametrize("dist", ["uniform", "int"])
-def test_wide_tiles_with_narrow_tail(shape, dist):
+def test_wide_tiles_with_narrow_tail(shape, dist, variant):
     """Variant 3 with more 128 x 256 tiles than SMs: whole waves of wide
     tiles, then the last partial wave's wide tiles as pairs of 128 x 128
     tiles in a second launch (1200 x 4000: 160 wide tiles, the last wide
@@ -154,10 +156,10 @@ def test_wide_tiles_with_narrow_tail(shape, dist):
     A, B = make_operands(M, N, K, dist, 81)
     exact = dist == "int"
     C64, bound = oracle.gemm_f64(A.numpy(), B.numpy(), with_bound=not exact)
-    check(run(A, B, variant=3), C64, bound, exact=exact, what=f"wide tail {shape} {dist}")
+    check(run(A, B, variant=variant), C64, bound, exact=exact, what=f"wide tail v{variant} {shape} {dist}")
 
 
-@pytest.mark.parametrize("variant", [1, 2, 3])
+@pytest.mark.parametrize("variant", [1, 2, 3, 4])
 def test_timeout_is_reported_and_recovers(variant):
     """CTA 0's producer skips a K slice: its split warps' bounded wait
     expires, the MMA issuer and the epilogue give up in turn, tensor memory is
