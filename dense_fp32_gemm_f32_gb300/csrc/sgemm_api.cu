@@ -480,11 +480,11 @@ struct Repacked {
 // / transposed in shared memory): 2048^3 62.0 / 62.7 / 66.9, 4096^3 65.4 /
 // 68.5 / 70.5, 8192^3 66.4 / 71.2 / 71.0, 128 x 8192 x 16384 64.2 / 68.2 /
 // 68.7, 8192 x 128 x 8192 62.0 / - / 66.4.  The copy costs one read and one
-// write of A, i.e. ~1/N of the product; it is taken automatically when no
-// variant is forced, N >= 6144 and 2MNK >= 2^33, and the transposition in
-// shared memory otherwise (make_plan).
-constexpr double kTransposeMinFlops = 8589934592.0;
-constexpr int kTransposeMinN = 6144;
+// write of A (~1/N of the product) and a pool buffer of A's size; with the
+// two transposing warps it no longer wins anywhere, so it is taken only when
+// forced (a_layout = 2) and the transposition in shared memory is automatic
+// (make_plan).  (The general entry's A stored transposed is read in place by
+// the transposed-A kernels: no copy.)
 
 bool options_force_variant(const sgemm_options* opt) {
     return opt && (opt->producer || opt->split_k || opt->multicast || opt->math || opt->stages || opt->tail_split ||
@@ -492,15 +492,10 @@ bool options_force_variant(const sgemm_options* opt) {
 }
 
 // 0 = keep A as stored, 1 = copy it transposed; -1 = invalid option.
-int choose_a_layout(int M, int N, int K, const sgemm_options* opt) {
+int choose_a_layout(int K, const sgemm_options* opt) {
     const int want = opt ? opt->a_layout : 0;
     if (want < 0 || want > 2) return -1;
-    if (K == 0 || want == 1) return 0;
-    if (want == 2) return 1;
-    return (!options_force_variant(opt) && N >= kTransposeMinN &&
-            2.0 * static_cast<double>(M) * static_cast<double>(N) * static_cast<double>(K) >= kTransposeMinFlops)
-               ? 1
-               : 0;
+    return (K > 0 && want == 2) ? 1 : 0;
 }
 
 struct Launch {
@@ -880,7 +875,7 @@ int run_ffma(int M, int N, int K, const float* A, int lda, const float* B, int l
         return launch_small(M, N, K, A, lda, B, ldb, C, ldc, stream, scale, a_mn);
     // A copied transposed for the transposed-A kernels (see choose_a_layout).
     Repacked a_t;
-    const int layout = a_mn ? 0 : choose_a_layout(M, N, K, opt);
+    const int layout = a_mn ? 0 : choose_a_layout(K, opt);
     if (layout < 0) return SGEMM_ERR_INVALID_ARG;
     if (layout == 1) {
         rc = a_t.make_transposed_a(dev, *st, M, K, A, lda, cs);
@@ -1583,13 +1578,6 @@ const char* sgemm_describe(int M, int N, int K, const float* A, int lda, const f
     if (M == 0 || N == 0) return "noop";
     if (small_problem(*st, M, N, K)) return "small/t32/w8";
     Plan pl;
-    if (choose_a_layout(M, N, K, nullptr) == 1) {
-        // The call would run on a transposed copy of A (a pool buffer: aligned
-        // base, pitch M rounded up to 4 floats).
-        const float* At = reinterpret_cast<const float*>(uintptr_t{256});
-        const int ldat = (M + 3) / 4 * 4;
-        if (make_plan(*st, M, N, K, At, ldat, B, ldb, nullptr, &pl, true) == SGEMM_OK) return describe_plan(pl);
-    }
     if (make_plan(*st, M, N, K, A, lda, B, ldb, nullptr, &pl) != SGEMM_OK) return "invalid";
     return describe_plan(pl);
 }

@@ -281,15 +281,13 @@ typedef struct sgemm_options {
                              tensor-map path; auto = on when no producer is
                              forced and 2MNK >= 2^30, else such operands are
                              read by the cp.async producer */
-    int a_layout;         /* 0 = auto, 1 = read A as stored (k innermost),
+    int a_layout;         /* 0 = auto (A stays where it is: the automatic
+                             producer transposes its slices in shared memory,
+                             SGEMM_PRODUCER_TMA_X), 1 = read A as stored,
                              2 = first copy A transposed (m innermost, a pool
                              workspace of K x M4 floats) and run the
                              transposed-A kernel, whose consumers read each
-                             k's A values as two 16-byte vectors; auto = 2
-                             when no other option is forced, N >= 6144 and
-                             2MNK >= 2^33 (otherwise the automatic producer
-                             transposes A in shared memory:
-                             SGEMM_PRODUCER_TMA_X) */
+                             k's A values as two 16-byte vectors */
 } sgemm_options;
 
 /* sgemm_f32 with forced choices.  Same contract; an unsupported combination
