@@ -70,24 +70,31 @@ typedef enum sgemm_status {
 /*
  * sgemm_f32 -- C = A x B in float32 on the CUDA cores (FFMA).
  *
- * The main entry.  Picks the kernel variant itself: TMA-fed when A, B have
- * 16-byte aligned bases and row strides; otherwise the misaligned operands
- * are first copied into 16-byte pitched rows (2MNK >= 2^30) or read by a
- * cp.async-fed variant (smaller products).  The schedule is stream-K (one CTA
- * per SM, the work after the last full wave dealt out as K slices) when there
- * are at least two (tile, K slice) units per SM, cluster split-K for smaller
- * outputs.  (Two-CTA multicast of A, 128 x 256 tiles and a K-split second
- * launch for the last partial wave are available through sgemm_f32_ex;
- * measured on GB300 none pays, so none is chosen automatically.)
+ * The main entry.  Picks the kernel variant itself: for small products
+ * (2MNK <= 2^28 with at most a quarter as many 128 x 128 tiles as SMs) the
+ * 32 x 32-tile small-problem kernel; otherwise 128 x 128 tiles, TMA-fed when
+ * A, B have 16-byte aligned bases and row strides (with two warps transposing
+ * each A slice in shared memory); misaligned operands are first copied into
+ * 16-byte pitched rows (2MNK >= 2^30) or read by a cp.async-fed variant
+ * (smaller products).  The schedule is stream-K (one CTA per SM, the work
+ * after the last full wave dealt out as K slices) when there are at least two
+ * (tile, K slice) units per SM, cluster split-K for smaller outputs.
+ * (Two-CTA multicast of A, 128 x 256 tiles, a copy of A transposed in HBM and
+ * a K-split second launch for the last partial wave are available through
+ * sgemm_f32_ex; measured on GB300 none pays, so none is chosen
+ * automatically.)
  *   M, N, K      problem sizes (>= 0)
  *   A, lda       device pointer to A, row stride in floats (lda >= K)
  *   B, ldb       device pointer to B, row stride in floats (ldb >= N)
  *   C, ldc       device pointer to C, row stride in floats (ldc >= N)
  *   stream       cudaStream_t as void*
- * A call enqueues the product kernel, preceded by a 4-byte-per-SM
- * cudaMemsetAsync of the stream-K ready flags and, when repacking, by one
- * copy kernel; its workspaces come from a pool the library keeps per device
- * (see sgemm_options.stream_k and .repack).
+ * A call enqueues the product kernel, preceded, when repacking, by one copy
+ * kernel (a pool buffer the library keeps per device).  The stream-K partial
+ * tiles and ready flags live in a workspace the library keeps per stream
+ * (allocated on the stream's first such call, 152 x 128 KiB, for up to 16
+ * streams; its flags carry each call's sequence number, so no memset is
+ * needed); a call recorded into a CUDA graph takes a pool workspace whose
+ * flags a memset node zeroes instead.
  */
 int sgemm_f32(int M, int N, int K,
               const float* A, int lda,
@@ -104,15 +111,18 @@ int sgemm_f32(int M, int N, int K,
  * that hand all device memory to their own allocator up front (a framework's
  * caching allocator, a serving process that reserves everything at start),
  * and latency-critical loops in which a pool allocation could block or fail.
- * sgemm_f32 takes its stream-K scratch from a stream-ordered pool at every
- * call; this entry point takes it from a fixed device array compiled into the
- * library instead, and calls no cudaMalloc, cudaFree or other allocating
- * routine.  It clears the scratch's ready flags with cudaMemsetAsync on
- * `stream`, which allocates nothing.
+ * sgemm_f32 allocates its stream-K scratch on a stream's first call (and
+ * repack buffers from a pool); this entry point takes the scratch from a
+ * fixed device array compiled into the library instead, and calls no
+ * cudaMalloc, cudaFree or other allocating routine.  The array's ready flags
+ * carry each call's sequence number (no memset), except in a stream capture,
+ * where a cudaMemsetAsync node (which allocates nothing) clears them ahead
+ * of each replay.
  *
  * Same operation, arguments, accuracy contract and errors as sgemm_f32.  It
- * always runs the FFMA kernel with the stream-K schedule (K == 0: the plain
- * grid, which needs no scratch).
+ * runs the small-problem kernel where sgemm_f32 would, else the FFMA kernel
+ * with the stream-K schedule (K == 0: the plain grid, which needs no
+ * scratch); misaligned operands are read by cp.async, never repacked.
  *
  * Limits and rules:
  *  - The array holds the scratch of at most 160 CTAs: 160 x 64 KiB partial
