@@ -126,6 +126,8 @@ int set_smem_attr(const KernelEntry& k) {
     return SGEMM_OK;
 }
 
+cudaMemPool_t workspace_pool(int dev, DeviceState& st);
+
 int init_device(int dev, DeviceState& st) {
     int major = 0, minor = 0;
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
@@ -196,6 +198,12 @@ int init_device(int dev, DeviceState& st) {
     st.max_clusters_split[1] = st.sm_count;
     for (int s = 2; s <= 8; ++s) st.max_clusters_split[s] = max_active_clusters(ref, 1, s);
     load_encoder();
+    // The pool of per-call workspaces (repack buffers, and the stream-K
+    // workspace of calls recorded into a graph) is created here, with the
+    // library's first call on the device, so that no call made inside a
+    // stream capture has to create it (which the capture would not allow).
+    // (Without it, those calls fail; the rest work.)
+    (void)workspace_pool(dev, st);
     return SGEMM_OK;
 }
 
@@ -359,6 +367,18 @@ int current_device(int* dev_out, DeviceState** st_out) {
         return SGEMM_ERR_CUDA;
     }
     if (dev < 0 || dev >= kMaxDevices) return SGEMM_ERR_UNSUPPORTED;
+    // A host thread whose only CUDA calls so far were queries like the one
+    // above has no current context, which the driver calls of the library
+    // (tensor-map encoding) need: bind the device's primary context, once per
+    // thread and device.
+    thread_local uint64_t bound = 0;
+    if (!(bound & (uint64_t{1} << dev))) {
+        if (cudaSetDevice(dev) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return SGEMM_ERR_CUDA;
+        }
+        bound |= uint64_t{1} << dev;
+    }
     DeviceState& st = g_dev[dev];
     std::call_once(st.once, [&] { st.status = init_device(dev, st); });
     *dev_out = dev;

@@ -94,7 +94,9 @@ typedef enum sgemm_status {
  * (allocated on the stream's first such call, 152 x 128 KiB, for up to 16
  * streams; its flags carry each call's sequence number, so no memset is
  * needed); a call recorded into a CUDA graph takes a pool workspace whose
- * flags a memset node zeroes instead.
+ * flags a memset node zeroes instead.  The first stream-K call on a stream
+ * allocates (cudaMalloc): make it before any stream capture in the global
+ * mode, which such an allocation would invalidate.
  */
 int sgemm_f32(int M, int N, int K,
               const float* A, int lda,

@@ -555,6 +555,47 @@ def test_stream_k_scratch_back_to_back(fn):
         check(dC.cpu().numpy(), C64, None, exact=True, what=f"{fn} back to back {tuple(dC.shape)}")
 
 
+def test_stream_k_scratch_from_many_host_threads():
+    """8 host threads, each with a stream of its own, 4 stream-K calls each,
+    all at once: the library's per-device table of stream-K scratch is shared
+    by the threads (under its lock), and each stream's calls use its own
+    scratch with their own sequence numbers."""
+    import threading
+
+    M, N, K = 512, 640, 700
+    cases = []
+    for t in range(8):
+        row = []
+        for i in range(4):
+            A, B = make_operands(M, N, K, "int", 800 + 4 * t + i)
+            row.append((A, B, to_device(A), to_device(B), torch.full((M, N), float("nan"), device="cuda")))
+        cases.append(row)
+    assert "/sk" in g.describe(cases[0][0][2], cases[0][0][3])
+    torch.cuda.synchronize()
+    errors = []
+
+    def work(t):
+        try:
+            s = torch.cuda.Stream()
+            for _, _, dA, dB, dC in cases[t]:
+                g.sgemm_f32(dA, dB, dC, stream=s)
+            s.synchronize()
+        except Exception as e:  # reported below, in the test's own thread
+            errors.append(e)
+
+    threads = [threading.Thread(target=work, args=(t,)) for t in range(len(cases))]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    assert not errors, errors
+    for row in cases:
+        for A, B, _, _, dC in row:
+            C64, _ = oracle.gemm_f64(A.numpy(), B.numpy(), with_bound=False)
+            check(dC.cpu().numpy(), C64, None, exact=True, what="host threads")
+    assert g.check_status() == 0
+
+
 def test_stream_k_scratch_more_streams_than_entries():
     """20 streams, two calls each, all in flight together: the library keeps
     stream-K scratch for 16 streams, so entries move to new streams (whose
