@@ -89,17 +89,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int tile = p.tile_base + static_cast<int>(blockIdx.x);
-    int m0, n0;
-    if (p.wide_halves) {  // a 128 x BN half of a 128 x 2BN tile (the tail of the wide-tile launch)
-        const int w = p.tile_base + static_cast<int>(blockIdx.x >> 1);
-        m0 = (w / p.tiles_n) * T::kBM;
-        n0 = (w % p.tiles_n) * (2 * BN) + static_cast<int>(blockIdx.x & 1) * BN;
-    } else {
-        m0 = (tile / p.tiles_n) * T::kBM;
-        n0 = (tile % p.tiles_n) * BN;
-    }
-    const int nkt = p.num_k_tiles;
+    // Tile and K range: the whole K for one tile per CTA, or (k_split) half of
+    // it, CTAs 2t and 2t + 1 sharing tile tile_base + t.  K slices are counted
+    // from kbase: nkt slices here.
+    const bool ksplit = p.k_split == 2;
+    const int tile = p.tile_base + static_cast<int>(ksplit ? blockIdx.x >> 1 : blockIdx.x);
+    const int m0 = (tile / p.tiles_n) * T::kBM;
+    const int n0 = (tile % p.tiles_n) * BN;
+    const int khalf = p.num_k_tiles / 2;
+    const bool second = ksplit && (blockIdx.x & 1);
+    const int kbase = second ? khalf : 0;
+    const int nkt = ksplit ? (second ? p.num_k_tiles - khalf : khalf) : p.num_k_tiles;
     const unsigned long long tmo = p.timeout_ns;
 
     if (threadIdx.x == 0) {
@@ -138,7 +138,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             for (int r = 0; r < T::kRawStages; ++r) issued_round[r] = -1;
 #pragma unroll
             for (int s = 0; s < T::kSplitStages; ++s) issued_sround[s] = -1;
-            const bool skip_here = p.skip_stage > 0 && tile == 0 && !p.wide_halves;
+            const bool skip_here = p.skip_stage > 0 && blockIdx.x == 0 && p.tile_base == 0 && !ksplit;
             for (int kt = 0; kt < nkt; ++kt) {
                 const int r = kt % T::kRawStages;
                 const int round = kt / T::kRawStages;
@@ -156,17 +156,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     }
                 }
                 if (skip_here && kt == p.skip_stage - 1) continue;
+                const int kc = (kbase + kt) * BK;  // K coordinate of the slice
                 mbar_arrive_expect_tx(raw_full(r), T::kRawABytes + T::kRawBBytes);
-                tma_load_2d(rawA(r), &tmA, raw_full(r), kt * BK, m0);
+                tma_load_2d(rawA(r), &tmA, raw_full(r), kc, m0);
                 if (PB) {
                     const int s = kt % T::kSplitStages;
                     const uint32_t b_big = split(s) + 2 * T::kOpABytes;
                     mbar_arrive_expect_tx(split_full(s), 2 * T::kOpBBytes);
-                    tma_load_2d(b_big, &tmB, split_full(s), kt * BK, n0);
-                    tma_load_2d(b_big + T::kOpBBytes, &tmB2, split_full(s), kt * BK, n0);
+                    tma_load_2d(b_big, &tmB, split_full(s), kc, n0);
+                    tma_load_2d(b_big + T::kOpBBytes, &tmB2, split_full(s), kc, n0);
                     issued_sround[s] = kt / T::kSplitStages;
                 } else {
-                    tma_load_2d(rawB(r), &tmB, raw_full(r), n0, kt * BK);
+                    tma_load_2d(rawB(r), &tmB, raw_full(r), n0, kc);
                 }
                 issued_round[r] = round;
             }
@@ -298,6 +299,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             constexpr int kChunksPerWarp = (BN / 32) / (kTcSplitWarps / 4);
             const int row = m0 + 32 * q + lane;
             float* crow = p.C + static_cast<long long>(row) * p.ldc;
+            // (the second half of a split tile: its whole partial tile, rows
+            // and columns beyond M and N included, into the workspace tile)
+            float* wrow = second ? p.ws + (static_cast<long long>(blockIdx.x >> 1) * T::kBM + 32 * q + lane) * BN
+                                 : nullptr;
 #pragma unroll
             for (int cc = 0; cc < kChunksPerWarp; ++cc) {
                 const int ch = half * kChunksPerWarp + cc;
@@ -305,7 +310,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(32 * ch), v);
                 tmem_wait_ld();
                 const int col = n0 + 32 * ch;
-                if (row < p.M) {
+                if (second) {
+#pragma unroll
+                    for (int e = 0; e < 32; e += 4)
+                        *reinterpret_cast<float4*>(wrow + 32 * ch + e) =
+                            make_float4(__uint_as_float(v[e]), __uint_as_float(v[e + 1]), __uint_as_float(v[e + 2]),
+                                        __uint_as_float(v[e + 3]));
+                } else if (row < p.M) {
                     if (p.vec_store && col + 31 < p.N) {
 #pragma unroll
                         for (int e = 0; e < 32; e += 4)

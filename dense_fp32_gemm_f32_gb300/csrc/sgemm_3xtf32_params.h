@@ -68,10 +68,13 @@ struct TcParams {
     float* C;
     long long ldc;
     int num_k_tiles;  // ceil(K / BK)
-    int tiles_n;      // output tiles per row of tiles (of the wide tiles when wide_halves)
+    int tiles_n;      // output tiles per row of tiles
     int tile_base;    // this launch's first tile (split-tile kernels)
-    int wide_halves;  // split-tile kernels: CTA j takes the (j & 1) half of tile
-                      // tile_base + j / 2 of twice the CTA's width
+    int k_split;      // split-tile kernels, 2: CTAs 2t and 2t + 1 take the first
+                      // and second halves of the K slices of tile tile_base + t;
+                      // the second stores its partial tile to ws (t-th tile of
+                      // 128 x BN floats, pitch BN), added to C afterwards
+    float* ws;
     int vec_store;    // C base 16-byte aligned and ldc % 4 == 0
     int skip_stage;   // debug: CTA 0's producer never issues K-slice skip_stage-1
     unsigned long long timeout_ns;

@@ -1226,29 +1226,36 @@ int run_3xtf32(int M, int N, int K, const float* A, int lda, const float* B, int
         packed.release();
         return run_ffma(M, N, K, A, lda, B, ldb, C, ldc, stream, nullptr);
     }
-    // Launches: (kernel, tile width, K-slice, grid, first tile, halves of wide
-    // tiles).  Variant 3 runs whole waves of 128 x 256 tiles; the wide tiles
-    // of a last partial wave run as twice as many 128 x 128 tiles of the
-    // variant-1 kernel (a second launch), which fill that wave better
-    // (4096^3: 3 waves of 152 wide tiles, then 112 narrow tiles).
+    // Launches: (kernel, tile width, K-slice, grid, first tile, K split).
+    // Variants 3 and 4 run whole waves of 128 x 256 tiles; the tiles of a
+    // last partial wave run in a second launch of the same kernel with their K
+    // slices split between two CTAs each (twice the CTAs at half the work: a
+    // fuller wave), the second halves' partial tiles then added into C by
+    // add_tiles (a fixed order: deterministic).  4096^3: 3 waves of 152 wide
+    // tiles, then 112 CTAs on the last 56 (262 -> 277 TFLOP/s).  Only for
+    // K >= 1024: with shorter K the halves' pipeline fill and the pass adding
+    // them cost more than the fuller wave gains (4096 x 4096 x 256: 117 ->
+    // 105), and the tiles run as one launch.
     struct TcLaunch {
         KernelEntry k;
         int bn, bk;
         long long grid;
-        int tile_base, wide_halves;
+        int tile_base, k_split;
         bool pb;  // B's TF32 parts pre-split in HBM (variant 4)
     };
     TcLaunch launches[2];
     int nl = 1;
     const long long tiles_m = ceil_div(M, kTcBM);
+    long long split_tiles = 0;  // tiles of the K-split launch
     if (variant >= 3) {
         const KernelEntry wk = variant == 4 ? tf32x3_wide_pb_kernel() : tf32x3_wide_kernel();
         const bool pb = variant == 4;
         const long long wide = tiles_m * ceil_div(N, 256);
         const long long full = (wide / st->sm_count) * st->sm_count;
-        if (full > 0 && full < wide) {
+        if (full > 0 && full < wide && K >= 1024) {
+            split_tiles = wide - full;
             launches[0] = {wk, 256, 16, full, 0, 0, pb};
-            launches[1] = {tf32x3_kernel(), kTcBN, kTcBK, 2 * (wide - full), static_cast<int>(full), 1, false};
+            launches[1] = {wk, 256, 16, 2 * split_tiles, static_cast<int>(full), 2, pb};
             nl = 2;
         } else {
             launches[0] = {wk, 256, 16, wide, 0, 0, pb};
@@ -1256,6 +1263,17 @@ int run_3xtf32(int M, int N, int K, const float* A, int lda, const float* B, int
     } else {
         const KernelEntry k = variant == 1 ? tf32x3_kernel() : tf32x3_direct_kernel();
         launches[0] = {k, kTcBN, kTcBK, tiles_m * ceil_div(N, kTcBN), 0, 0, false};
+    }
+    // The second halves' partial tiles (128 x 256 floats each), from the pool.
+    void* ws_split = nullptr;
+    if (split_tiles > 0) {
+        cudaMemPool_t pool = workspace_pool(dev, *st);
+        if (!pool || cudaMallocFromPoolAsync(&ws_split, static_cast<size_t>(split_tiles) * kTcBM * 256 * sizeof(float),
+                                             pool, cs) != cudaSuccess) {
+            (void)cudaGetLastError();
+            packed.release();
+            return SGEMM_ERR_CUDA;
+        }
     }
 
     // Variant 4: B's TF32 parts, transposed (N x K4), in a pool buffer.
@@ -1267,6 +1285,7 @@ int run_3xtf32(int M, int N, int K, const float* A, int lda, const float* B, int
         const size_t part = (static_cast<size_t>(N) * K4 * sizeof(float) + 255) & ~size_t{255};
         if (!pool || cudaMallocFromPoolAsync(&ws, 2 * part, pool, cs) != cudaSuccess) {
             (void)cudaGetLastError();
+            if (ws_split) (void)cudaFreeAsync(ws_split, cs);
             packed.release();
             return SGEMM_ERR_CUDA;
         }
@@ -1275,6 +1294,7 @@ int run_3xtf32(int M, int N, int K, const float* A, int lda, const float* B, int
         rc = split_transpose_b(B, ldb, K, N, bt_big, bt_small, K4, cs);
         if (rc != SGEMM_OK) {
             (void)cudaFreeAsync(ws, cs);
+            if (ws_split) (void)cudaFreeAsync(ws_split, cs);
             packed.release();
             return rc;
         }
@@ -1304,10 +1324,10 @@ int run_3xtf32(int M, int N, int K, const float* A, int lda, const float* B, int
         prm.C = C;
         prm.ldc = ldc;
         prm.num_k_tiles = static_cast<int>(ceil_div(K, ln.bk));
-        // (halves of wide tiles: tiles are counted in wide tiles per row)
-        prm.tiles_n = static_cast<int>(ceil_div(N, ln.wide_halves ? 2 * ln.bn : ln.bn));
+        prm.tiles_n = static_cast<int>(ceil_div(N, ln.bn));
         prm.tile_base = ln.tile_base;
-        prm.wide_halves = ln.wide_halves;
+        prm.k_split = ln.k_split;
+        prm.ws = ln.k_split == 2 ? static_cast<float*>(ws_split) : nullptr;
         prm.vec_store = ((reinterpret_cast<uintptr_t>(C) & 15u) == 0 && ldc % 4 == 0) ? 1 : 0;
         prm.skip_stage = opt ? opt->debug_skip_stage : 0;
         prm.timeout_ns = (opt && opt->timeout_ns) ? opt->timeout_ns : kDefaultTimeoutNs;
@@ -1326,6 +1346,10 @@ int run_3xtf32(int M, int N, int K, const float* A, int lda, const float* B, int
             rc = SGEMM_ERR_CUDA;
         }
     }
+    if (rc == SGEMM_OK && split_tiles > 0)
+        rc = add_tiles(C, ldc, M, N, static_cast<float*>(ws_split), kTcBM, 256, launches[1].tile_base,
+                       static_cast<int>(ceil_div(N, 256)), static_cast<int>(split_tiles), cs);
+    if (ws_split) (void)cudaFreeAsync(ws_split, cs);
     if (ws) (void)cudaFreeAsync(ws, cs);
     packed.release();
     return rc;

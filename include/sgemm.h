@@ -321,9 +321,10 @@ int sgemm_f32_ex(int M, int N, int K,
  * kernel on 128 x 256 tiles with K-slices of 16 (each A element serves twice
  * the columns); 4 = variant 3 with B's TF32 parts split and transposed into a
  * pool buffer first (2 x N x K floats; the kernel loads them with the TMA and
- * splits A only).  3 and 4 run whole waves of 128 x 256 tiles and the tiles
- * of a last partial wave as pairs of variant-1 tiles.  Other fields are
- * ignored. */
+ * splits A only).  3 and 4 run whole waves of 128 x 256 tiles; when K >=
+ * 1024 the tiles of a last partial wave run in a second launch with their K
+ * slices split between two CTAs, the second halves added into C by a third
+ * (a pool workspace of 128 KiB per such tile).  Other fields are ignored. */
 int sgemm_3xtf32_ex(int M, int N, int K,
                     const float* A, int lda,
                     const float* B, int ldb,

@@ -144,14 +144,17 @@ def test_k_zero_writes_zeros():
 
 
 @pytest.mark.parametrize("variant", [3, 4])
-@pytest.mark.parametrize("shape", [(1200, 4000, 300), (1200, 3852, 96), (1300, 4100, 40)])
+@pytest.mark.parametrize("shape", [(1200, 4000, 1040), (1200, 3852, 1100), (1300, 4100, 1025), (1200, 4000, 300)])
 @pytest.mark.parametrize("dist", ["uniform", "int"])
-def test_wide_tiles_with_narrow_tail(shape, dist, variant):
-    """Variant 3 with more 128 x 256 tiles than SMs: whole waves of wide
-    tiles, then the last partial wave's wide tiles as pairs of 128 x 128
-    tiles in a second launch (1200 x 4000: 160 wide tiles, the last wide
-    column 160 floats wide; 1200 x 3852: the second half of each last wide
-    tile lies wholly beyond N; K = 300 / 96 / 40 ragged against both K-slices)."""
+def test_wide_tiles_with_split_tail(shape, dist, variant):
+    """Variants 3 and 4 with more 128 x 256 tiles than SMs: whole waves of
+    wide tiles, then the last partial wave's tiles in a second launch with
+    their K slices split between two CTAs, the second halves added into C
+    afterwards (1200 x 4000: 160 wide tiles, the last wide column 160 floats
+    wide; 1200 x 3852: the second half of each last wide tile lies wholly
+    beyond N; K = 1040 / 1100 / 1025 ragged against the 16-deep slices, split
+    32 + 33, 34 + 35 and 32 + 33; K = 300: below the split's threshold, one
+    launch of four waves)."""
     M, N, K = shape
     A, B = make_operands(M, N, K, dist, 81)
     exact = dist == "int"
