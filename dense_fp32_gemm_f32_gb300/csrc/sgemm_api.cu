@@ -1280,15 +1280,21 @@ int run_3xtf32(int M, int N, int K, const float* A, int lda, const float* B, int
     void* ws = nullptr;
     float *bt_big = nullptr, *bt_small = nullptr;
     const long long K4 = (static_cast<long long>(K) + 3) / 4 * 4;
+    const size_t part = (static_cast<size_t>(N) * K4 * sizeof(float) + 255) & ~size_t{255};
     if (launches[0].pb) {
         cudaMemPool_t pool = workspace_pool(dev, *st);
-        const size_t part = (static_cast<size_t>(N) * K4 * sizeof(float) + 255) & ~size_t{255};
         if (!pool || cudaMallocFromPoolAsync(&ws, 2 * part, pool, cs) != cudaSuccess) {
+            // No room for B's parts (2 N K floats): variant 3's kernels, which
+            // split B in shared memory, on the same tiles.
             (void)cudaGetLastError();
-            if (ws_split) (void)cudaFreeAsync(ws_split, cs);
-            packed.release();
-            return SGEMM_ERR_CUDA;
+            ws = nullptr;
+            for (int l = 0; l < nl; ++l) {
+                launches[l].k = tf32x3_wide_kernel();
+                launches[l].pb = false;
+            }
         }
+    }
+    if (launches[0].pb) {
         bt_big = static_cast<float*>(ws);
         bt_small = reinterpret_cast<float*>(static_cast<char*>(ws) + part);
         rc = split_transpose_b(B, ldb, K, N, bt_big, bt_small, K4, cs);
