@@ -1,0 +1,227 @@
+// Internal interface of the library's host code, shared by the translation
+// units behind the C entry points (not part of the installed interface): the
+// per-device state, the plan of an FFMA call, and the functions those units
+// call in one another.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/sgemm.h"
+#include "kernels.h"
+#include "sgemm_3xtf32_params.h"
+#include "sgemm_ffma.cuh"
+
+namespace gb300 {
+namespace detail {
+
+constexpr int kMaxDevices = 64;
+constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;  // 2 s per wait
+
+// Stream-K scratch kept for one stream (see sk_lease): partial tiles and
+// ready flags, allocated once and reused by every call on that stream.
+constexpr int kSkCacheEntries = 16;
+// Sequence number of calls recorded into a graph: their flags come from a
+// fresh workspace zeroed by a memset node, and the counters never hand it out.
+constexpr unsigned int kSkSeqCaptured = 0xFFFFFFFFu;
+struct SkScratch {
+    bool allocated = false;
+    unsigned long long stream_id = 0;  // cudaStreamGetId of the stream it serves
+    float* ws = nullptr;               // partial tiles
+    unsigned int* flags = nullptr;     // one word per CTA
+    size_t ws_bytes = 0, nflags = 0;
+    unsigned int seq = 0;              // last number handed out
+    cudaEvent_t last_use = nullptr;    // recorded on the stream after each call's launch
+    int busy = 0;                      // leases not yet returned
+    unsigned long long tick = 0;       // last use, for eviction
+};
+
+struct DeviceState {
+    std::once_flag once;
+    int status = SGEMM_ERR_CUDA;  // result of the one-time set-up
+    int sm_count = 0;
+    int max_clusters_pair = 0;    // co-resident 2-CTA clusters of the FFMA kernel
+    int max_clusters_split[9] = {0};
+    bool regsplit_ok = false;     // the register-split kernels were built at kRegsLaunch registers
+    int fused_per_sm[7] = {0};    // co-resident fused-producer CTAs per SM, by stage count
+    unsigned int* status_word = nullptr;  // device address of g_sgemm_status
+    std::once_flag pool_once;
+    cudaMemPool_t pool = nullptr;  // library-owned pool for per-call workspaces
+    std::once_flag noalloc_once;
+    int noalloc_status = SGEMM_ERR_CUDA;  // result of looking up g_noalloc_scratch
+    float* noalloc_scratch = nullptr;     // its device address on this device
+    std::once_flag copy_once;
+    cudaStream_t copy_in = nullptr;   // host-buffer entry: host -> device copies
+    cudaStream_t copy_out = nullptr;  // host-buffer entry: device -> host copies
+    std::mutex sk_mu;                        // guards sk_cache, sk_tick and noalloc_seq
+    SkScratch sk_cache[kSkCacheEntries];     // per-stream stream-K scratch (sk_lease)
+    unsigned long long sk_tick = 0;
+    unsigned int noalloc_seq = 0;            // last sequence number of sgemm_f32_noalloc
+};
+
+// cuTensorMapEncodeTiled, looked up once (api_device.cu).
+extern PFN_cuTensorMapEncodeTiled_v12000 g_encode;
+
+struct SkLease {
+    SkScratch* e = nullptr;
+    float* ws = nullptr;
+    unsigned int* flags = nullptr;
+    unsigned int seq = 0;
+};
+
+inline long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
+
+// Repacking pays once the product is large next to the copy.  Measured on
+// GB300 (both operands misaligned, one copy launch for both): 1023 x 1025 x
+// 1027 (2^31 flop) 65 us against 69 us with cp.async, 2047 x 2049 x 2051
+// +23 %, 4095 x 4097 x 4099 and 8191 x 8193 x 8195 +30 %.
+constexpr double kRepackMinFlops = 1073741824.0;  // 2^30
+
+// The library's stream-ordered pool on device `dev` (api_device.cu).
+cudaMemPool_t workspace_pool(int dev, DeviceState& st);
+
+// Operands copied into 16-byte pitched rows (see pack_rows) for the length of
+// one call: the copies come from the library's pool and go back to it, in
+// stream order, by release().
+struct Repacked {
+    void* ws = nullptr;
+    cudaStream_t stream = nullptr;
+
+    // Copies operand A (mask bit 0) and/or B (bit 1) and points A / lda and
+    // B / ldb at the copies, which are always the plain (untransposed) M x K
+    // and K x N operands: with transa, A is stored K x M and its copy is the
+    // transpose; with transb, likewise B (stored N x K).  SGEMM_ERR_CUDA if
+    // the pool cannot serve them (nothing is enqueued then).
+    int make(int dev, DeviceState& st, int mask, int M, int N, int K, const float*& A, int& lda, const float*& B,
+             int& ldb, cudaStream_t cs, bool transa = false, bool transb = false) {
+        stream = cs;
+        const long long K4 = (static_cast<long long>(K) + 3) / 4 * 4;
+        const long long N4 = (static_cast<long long>(N) + 3) / 4 * 4;
+        if (K4 > 0x7fffffffLL || N4 > 0x7fffffffLL) return SGEMM_ERR_INVALID_ARG;
+        const size_t bytes_a = (mask & 1) ? ((static_cast<size_t>(M) * K4 * 4 + 255) & ~size_t{255}) : 0;
+        const size_t bytes_b = (mask & 2) ? static_cast<size_t>(K) * N4 * 4 : 0;
+        cudaMemPool_t pool = workspace_pool(dev, st);
+        if (!pool || cudaMallocFromPoolAsync(&ws, bytes_a + bytes_b, pool, cs) != cudaSuccess) {
+            (void)cudaGetLastError();
+            ws = nullptr;
+            return SGEMM_ERR_CUDA;
+        }
+        float* Ap = (mask & 1) ? static_cast<float*>(ws) : nullptr;
+        float* Bp = (mask & 2) ? reinterpret_cast<float*>(static_cast<char*>(ws) + bytes_a) : nullptr;
+        // Row copies in one launch, transposing copies in another.
+        int rc = pack_rows(A, lda, transa ? nullptr : Ap, K4, M, K, B, ldb, transb ? nullptr : Bp, N4, K, N, cs);
+        if (rc == SGEMM_OK)
+            rc = transpose_rows(A, lda, transa ? Ap : nullptr, K4, M, K, B, ldb, transb ? Bp : nullptr, N4, K, N, cs);
+        if (rc != SGEMM_OK) {
+            release();
+            return rc;
+        }
+        if (Ap) {
+            A = Ap;
+            lda = static_cast<int>(K4);
+        }
+        if (Bp) {
+            B = Bp;
+            ldb = static_cast<int>(N4);
+        }
+        return SGEMM_OK;
+    }
+    // A (M x K, pitch lda) -> its transpose (K x M, pitch M rounded up to 4
+    // floats) in a pool buffer; A / lda then point at the copy.
+    int make_transposed_a(int dev, DeviceState& st, int M, int K, const float*& A, int& lda, cudaStream_t cs) {
+        stream = cs;
+        const long long M4 = (static_cast<long long>(M) + 3) / 4 * 4;
+        if (M4 > 0x7fffffffLL) return SGEMM_ERR_INVALID_ARG;
+        cudaMemPool_t pool = workspace_pool(dev, st);
+        if (!pool || cudaMallocFromPoolAsync(&ws, static_cast<size_t>(K) * M4 * 4, pool, cs) != cudaSuccess) {
+            (void)cudaGetLastError();
+            ws = nullptr;
+            return SGEMM_ERR_CUDA;
+        }
+        float* At = static_cast<float*>(ws);
+        const int rc = transpose_rows(A, lda, At, M4, K, M, nullptr, 0, nullptr, 0, 0, 0, cs);
+        if (rc != SGEMM_OK) {
+            release();
+            return rc;
+        }
+        A = At;
+        lda = static_cast<int>(M4);
+        return SGEMM_OK;
+    }
+    void release() {
+        if (ws) (void)cudaFreeAsync(ws, stream);
+        ws = nullptr;
+    }
+};
+
+struct Launch {
+    int tile_base = 0;  // first output tile
+    int tiles = 0;      // output tiles in this launch (grid x)
+    int split = 1;      // CTAs per tile along K (cluster z)
+};
+
+struct Plan {
+    int producer = kProducerTma;
+    int math = kMathFfma2;
+    int stages = 4;
+    int mcast = 1;
+    int bn = kBN;     // output tile width (kBN or kBNWide)
+    int tiles_n = 0;  // tiles per row of tiles (padded to even for multicast pairs)
+    int num_k_tiles = 0;
+    int nlaunch = 1;
+    Launch launch[2];
+    int sk = 0;           // stream-K: launch[0].tiles CTAs, one per SM
+    int sk_dp_tiles = 0;  // tiles taken whole (data-parallel waves) before the stream-K region
+    int repack = 0;       // operands copied to 16-byte pitched rows first: bit 0 = A, bit 1 = B
+    bool a_mn = false;    // A stored transposed (K x M): the transposed-A kernels
+};
+
+// Epilogue scaling of the general entry: C = alpha * A B + beta * C.
+struct Scale {
+    float alpha = 1.f, beta = 0.f;
+};
+
+// ---- api_device.cu: device set-up, per-stream stream-K scratch
+int current_device(int* dev_out, DeviceState** st_out);
+int sk_lease(DeviceState& st, cudaStream_t cs, size_t ws_bytes, size_t nflags, SkLease* out);
+void sk_return(DeviceState& st, cudaStream_t cs, SkLease& lease);
+
+// ---- api_plan.cu: argument checks and the choice of variant
+bool ranges_overlap(const void* a, size_t abytes, const void* b, size_t bbytes);
+size_t span_bytes(long long rows, long long cols, long long ld);
+int validate(int M, int N, int K, const float* A, int lda, const float* B, int ldb, const float* C, int ldc,
+             bool a_mn = false);
+bool options_force_variant(const sgemm_options* opt);
+int choose_a_layout(int K, const sgemm_options* opt);
+bool is_tma(int producer);
+KernelEntry ffma_kernel(const Plan& pl);
+bool tma_ok(const float* p, int ld);
+int make_plan(const DeviceState& st, int M, int N, int K, const float* A, int lda, const float* B, int ldb,
+              const sgemm_options* opt, Plan* out, bool a_mn = false);
+int encode_2d(CUtensorMap* map, const float* base, long long inner, long long outer, long long ld, int box_inner,
+              int box_outer, CUtensorMapSwizzle swz);
+const char* describe_plan(const Plan& pl);
+bool small_problem(const DeviceState& st, int M, int N, int K);
+bool small_forced_ok(const sgemm_options* opt);
+
+// ---- api_ffma.cu, api_tf32.cu, api_host.cu: the entries' work
+int run_ffma(int M, int N, int K, const float* A, int lda, const float* B, int ldb, float* C, int ldc, void* stream,
+             const sgemm_options* opt, const Scale* scale = nullptr, bool a_mn = false);
+int run_ffma_noalloc(int M, int N, int K, const float* A, int lda, const float* B, int ldb, float* C, int ldc,
+                     void* stream);
+int run_gemm(int transa, int transb, int M, int N, int K, float alpha, const float* A, int lda, const float* B,
+             int ldb, float beta, float* C, int ldc, void* stream);
+int run_3xtf32(int M, int N, int K, const float* A, int lda, const float* B, int ldb, float* C, int ldc,
+               void* stream, const sgemm_options* opt);
+int run_host(int M, int N, int K, const float* A, int lda, const float* B, int ldb, float* C, int ldc,
+             void* stream);
+
+}  // namespace detail
+}  // namespace gb300

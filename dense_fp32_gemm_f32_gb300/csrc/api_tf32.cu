@@ -1,0 +1,185 @@
+// The three-product TF32 entries' work: variant choice, the pass splitting B,
+// and the launches (sgemm_3xtf32, sgemm_3xtf32_ex).
+#include "api_internal.h"
+
+namespace gb300 {
+namespace detail {
+
+int run_3xtf32(int M, int N, int K, const float* A, int lda, const float* B, int ldb, float* C, int ldc,
+               void* stream, const sgemm_options* opt) {
+    int rc = validate(M, N, K, A, lda, B, ldb, C, ldc);
+    if (rc != SGEMM_OK) return rc;
+    if (opt && opt->debug_skip_stage < 0) return SGEMM_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return SGEMM_OK;
+    int dev = 0;
+    DeviceState* st = nullptr;
+    rc = current_device(&dev, &st);
+    if (rc != SGEMM_OK) return rc;
+    // The tensor-core kernel is fed by tensor maps.  Operands the TMA cannot
+    // read (unaligned bases or row strides) are repacked into pitched rows
+    // when the product is large enough for that to pay (the same rule as
+    // sgemm_f32); otherwise they, and K == 0, take the FFMA kernel, which
+    // meets the same contract.
+    // Variant: 1 = split-tile kernel (all four TF32 parts in shared memory),
+    // 2 = direct-A kernel (A's big part is the TMA tile itself), 3 = the
+    // split-tile kernel on 128 x 256 tiles with K-slices of 16, 4 = variant
+    // 3 with B's TF32 parts split and transposed in HBM by a pass before the
+    // kernel (one read of B and two writes of its size), which leaves the
+    // kernel's split warps A only.  Automatic: 4 when the 128 x 256 tiles
+    // number at least half the SMs and M >= 1024 (the pass costs ~6/M bytes
+    // per flop), 3 when they do with fewer rows, else 1.  Measured on GB300,
+    // TFLOP/s for 1 / 3 / 4: 2048^3 155 / 181 / 203, 4096^3 195 / 218 / 261,
+    // 8192^3 204 / 243 / 289, 4096 x 4096 x 256 102 / 112 / 116; with fewer
+    // tiles 1024^3 61 / 40 / 45, 8192 x 128 x 8192 82 / 51 / 71, 128 x 8192 x
+    // 16384 86 / 53 / 22.
+    int variant = (opt && opt->math) ? opt->math : 0;
+    if (variant == 0)
+        variant = 2 * ceil_div(M, kTcBM) * ceil_div(N, 256) < st->sm_count ? 1 : M >= 1024 ? 4 : 3;
+    if (variant < 1 || variant > 4) return SGEMM_ERR_INVALID_ARG;
+    const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    const int misaligned = (tma_ok(A, lda) ? 0 : 1) | (tma_ok(B, ldb) ? 0 : 2);
+    Repacked packed;
+    if (K > 0 && misaligned &&
+        2.0 * static_cast<double>(M) * static_cast<double>(N) * static_cast<double>(K) >= kRepackMinFlops)
+        (void)packed.make(dev, *st, misaligned, M, N, K, A, lda, B, ldb, cs);  // (on failure: the FFMA kernel)
+    if (K == 0 || !tma_ok(A, lda) || !tma_ok(B, ldb)) {
+        packed.release();
+        return run_ffma(M, N, K, A, lda, B, ldb, C, ldc, stream, nullptr);
+    }
+    // Launches: (kernel, tile width, K-slice, grid, first tile, K split).
+    // Variants 3 and 4 run whole waves of 128 x 256 tiles; the tiles of a
+    // last partial wave run in a second launch of the same kernel with their K
+    // slices split between two CTAs each (twice the CTAs at half the work: a
+    // fuller wave), the second halves' partial tiles then added into C by
+    // add_tiles (a fixed order: deterministic).  4096^3: 3 waves of 152 wide
+    // tiles, then 112 CTAs on the last 56 (262 -> 277 TFLOP/s).  Only for
+    // K >= 1024: with shorter K the halves' pipeline fill and the pass adding
+    // them cost more than the fuller wave gains (4096 x 4096 x 256: 117 ->
+    // 105), and the tiles run as one launch.
+    struct TcLaunch {
+        KernelEntry k;
+        int bn, bk;
+        long long grid;
+        int tile_base, k_split;
+        bool pb;  // B's TF32 parts pre-split in HBM (variant 4)
+    };
+    TcLaunch launches[2];
+    int nl = 1;
+    const long long tiles_m = ceil_div(M, kTcBM);
+    long long split_tiles = 0;  // tiles of the K-split launch
+    if (variant >= 3) {
+        const KernelEntry wk = variant == 4 ? tf32x3_wide_pb_kernel() : tf32x3_wide_kernel();
+        const bool pb = variant == 4;
+        const long long wide = tiles_m * ceil_div(N, 256);
+        const long long full = (wide / st->sm_count) * st->sm_count;
+        if (full > 0 && full < wide && K >= 1024) {
+            split_tiles = wide - full;
+            launches[0] = {wk, 256, 16, full, 0, 0, pb};
+            launches[1] = {wk, 256, 16, 2 * split_tiles, static_cast<int>(full), 2, pb};
+            nl = 2;
+        } else {
+            launches[0] = {wk, 256, 16, wide, 0, 0, pb};
+        }
+    } else {
+        const KernelEntry k = variant == 1 ? tf32x3_kernel() : tf32x3_direct_kernel();
+        launches[0] = {k, kTcBN, kTcBK, tiles_m * ceil_div(N, kTcBN), 0, 0, false};
+    }
+    // The second halves' partial tiles (128 x 256 floats each), from the pool.
+    void* ws_split = nullptr;
+    if (split_tiles > 0) {
+        cudaMemPool_t pool = workspace_pool(dev, *st);
+        if (!pool || cudaMallocFromPoolAsync(&ws_split, static_cast<size_t>(split_tiles) * kTcBM * 256 * sizeof(float),
+                                             pool, cs) != cudaSuccess) {
+            (void)cudaGetLastError();
+            packed.release();
+            return SGEMM_ERR_CUDA;
+        }
+    }
+
+    // Variant 4: B's TF32 parts, transposed (N x K4), in a pool buffer.
+    void* ws = nullptr;
+    float *bt_big = nullptr, *bt_small = nullptr;
+    const long long K4 = (static_cast<long long>(K) + 3) / 4 * 4;
+    const size_t part = (static_cast<size_t>(N) * K4 * sizeof(float) + 255) & ~size_t{255};
+    if (launches[0].pb) {
+        cudaMemPool_t pool = workspace_pool(dev, *st);
+        if (!pool || cudaMallocFromPoolAsync(&ws, 2 * part, pool, cs) != cudaSuccess) {
+            // No room for B's parts (2 N K floats): variant 3's kernels, which
+            // split B in shared memory, on the same tiles.
+            (void)cudaGetLastError();
+            ws = nullptr;
+            for (int l = 0; l < nl; ++l) {
+                launches[l].k = tf32x3_wide_kernel();
+                launches[l].pb = false;
+            }
+        }
+    }
+    if (launches[0].pb) {
+        bt_big = static_cast<float*>(ws);
+        bt_small = reinterpret_cast<float*>(static_cast<char*>(ws) + part);
+        rc = split_transpose_b(B, ldb, K, N, bt_big, bt_small, K4, cs);
+        if (rc != SGEMM_OK) {
+            (void)cudaFreeAsync(ws, cs);
+            if (ws_split) (void)cudaFreeAsync(ws_split, cs);
+            packed.release();
+            return rc;
+        }
+    }
+
+    rc = SGEMM_OK;
+    for (int l = 0; l < nl && rc == SGEMM_OK; ++l) {
+        const TcLaunch& ln = launches[l];
+        alignas(64) CUtensorMap tmA;
+        alignas(64) CUtensorMap tmB;
+        alignas(64) CUtensorMap tmB2;
+        const CUtensorMapSwizzle swz = ln.bk == 32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+        rc = encode_2d(&tmA, A, K, M, lda, ln.bk, kTcBM, swz);
+        if (ln.pb) {  // {k, n} boxes of the transposed parts, swizzled like A
+            if (rc == SGEMM_OK) rc = encode_2d(&tmB, bt_big, K, N, K4, ln.bk, ln.bn, swz);
+            if (rc == SGEMM_OK) rc = encode_2d(&tmB2, bt_small, K, N, K4, ln.bk, ln.bn, swz);
+        } else {
+            if (rc == SGEMM_OK) rc = encode_2d(&tmB, B, N, K, ldb, ln.bn, ln.bk, CU_TENSOR_MAP_SWIZZLE_NONE);
+            tmB2 = tmB;  // (unused)
+        }
+        if (rc != SGEMM_OK) break;
+
+        TcParams prm;
+        prm.M = M;
+        prm.N = N;
+        prm.K = K;
+        prm.C = C;
+        prm.ldc = ldc;
+        prm.num_k_tiles = static_cast<int>(ceil_div(K, ln.bk));
+        prm.tiles_n = static_cast<int>(ceil_div(N, ln.bn));
+        prm.tile_base = ln.tile_base;
+        prm.k_split = ln.k_split;
+        prm.ws = ln.k_split == 2 ? static_cast<float*>(ws_split) : nullptr;
+        prm.vec_store = ((reinterpret_cast<uintptr_t>(C) & 15u) == 0 && ldc % 4 == 0) ? 1 : 0;
+        prm.skip_stage = opt ? opt->debug_skip_stage : 0;
+        prm.timeout_ns = (opt && opt->timeout_ns) ? opt->timeout_ns : kDefaultTimeoutNs;
+        prm.status = st->status_word;
+
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(ln.grid), 1, 1);
+        cfg.blockDim = dim3(ln.k.threads, 1, 1);
+        cfg.dynamicSmemBytes = static_cast<size_t>(ln.k.smem_bytes);
+        cfg.stream = static_cast<cudaStream_t>(stream);
+        cfg.numAttrs = 0;
+        void* args4[4] = {&tmA, &tmB, &tmB2, &prm};
+        void* args3[3] = {&tmA, &tmB, &prm};  // (the direct-A kernel takes no second B map)
+        if (cudaLaunchKernelExC(&cfg, ln.k.fn, variant == 2 ? args3 : args4) != cudaSuccess) {
+            (void)cudaGetLastError();
+            rc = SGEMM_ERR_CUDA;
+        }
+    }
+    if (rc == SGEMM_OK && split_tiles > 0)
+        rc = add_tiles(C, ldc, M, N, static_cast<float*>(ws_split), kTcBM, 256, launches[1].tile_base,
+                       static_cast<int>(ceil_div(N, 256)), static_cast<int>(split_tiles), cs);
+    if (ws_split) (void)cudaFreeAsync(ws_split, cs);
+    if (ws) (void)cudaFreeAsync(ws, cs);
+    packed.release();
+    return rc;
+}
+
+}  // namespace detail
+}  // namespace gb300
