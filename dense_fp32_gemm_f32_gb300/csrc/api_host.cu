@@ -32,14 +32,22 @@ int run_host(int M, int N, int K, const float* A, int lda, const float* B, int l
     DeviceState* st = nullptr;
     rc = current_device(&dev, &st);
     if (rc != SGEMM_OK) return rc;
+    // The copy streams and the events of the pipeline, made once per device.
+    // Calls share them, so one call enqueues at a time (host_mu); reusing the
+    // events is safe because a stream's wait on an event waits for the event's
+    // last record at the time the wait is enqueued.
     std::call_once(st->copy_once, [&] {
-        if (cudaStreamCreateWithFlags(&st->copy_in, cudaStreamNonBlocking) != cudaSuccess ||
-            cudaStreamCreateWithFlags(&st->copy_out, cudaStreamNonBlocking) != cudaSuccess) {
+        bool made = cudaStreamCreateWithFlags(&st->copy_in, cudaStreamNonBlocking) == cudaSuccess &&
+                    cudaStreamCreateWithFlags(&st->copy_out, cudaStreamNonBlocking) == cudaSuccess;
+        for (int e = 0; e < kHostEvents && made; ++e)
+            made = cudaEventCreateWithFlags(&st->host_ev[e], cudaEventDisableTiming) == cudaSuccess;
+        if (!made) {
             (void)cudaGetLastError();
             st->copy_in = st->copy_out = nullptr;
         }
     });
     if (!st->copy_in || !st->copy_out) return SGEMM_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(st->host_mu);
     const cudaStream_t cs = static_cast<cudaStream_t>(stream);
     cudaMemPool_t pool = workspace_pool(dev, *st);
     if (!pool) return SGEMM_ERR_CUDA;
@@ -47,7 +55,7 @@ int run_host(int M, int N, int K, const float* A, int lda, const float* B, int l
     // Row blocks: whole 128-row tiles, up to 8 blocks of >= 512 rows; one
     // block below 2^32 flop (the copies then run before and after the
     // product).  K chunks of B (multiples of 32): 4 when blocked and K >= 1024.
-    constexpr int kMaxBlk = 8, kMaxKc = 4;
+    constexpr int kMaxBlk = kHostMaxBlk, kMaxKc = kHostMaxKc;
     const bool big = 2.0 * static_cast<double>(M) * N * K >= 4294967296.0;
     const int nblk = big ? static_cast<int>(std::min<long long>(kMaxBlk, (static_cast<long long>(M) + 511) / 512)) : 1;
     const long long rows_blk = ((static_cast<long long>(M) + nblk - 1) / nblk + kBM - 1) / kBM * kBM;
@@ -72,16 +80,13 @@ int run_host(int M, int N, int K, const float* A, int lda, const float* B, int l
     float* dC = reinterpret_cast<float*>(static_cast<char*>(ws) + bytes_a + bytes_b);
     const int lda_d = static_cast<int>(K4), ldb_d = static_cast<int>(N4), ldc_d = static_cast<int>(N4);
 
-    cudaEvent_t ev_start = nullptr, ev_in_end = nullptr, ev_out_end = nullptr;
-    cudaEvent_t ev_a[kMaxBlk] = {}, ev_b[kMaxKc] = {}, ev_done[kMaxBlk] = {};
-    auto make_event = [](cudaEvent_t* e) {
-        return cudaEventCreateWithFlags(e, cudaEventDisableTiming) == cudaSuccess;
-    };
-    bool ok = make_event(&ev_start) && make_event(&ev_in_end) && make_event(&ev_out_end);
-    for (int i = 0; i < nblk && ok; ++i) ok = make_event(&ev_a[i]) && make_event(&ev_done[i]);
-    for (int c = 0; c < nkc && ok; ++c) ok = make_event(&ev_b[c]);
+    cudaEvent_t* const ev = st->host_ev;
+    const cudaEvent_t ev_start = ev[0], ev_in_end = ev[1], ev_out_end = ev[2];
+    cudaEvent_t* const ev_a = ev + 3;                 // [kMaxBlk]
+    cudaEvent_t* const ev_done = ev + 3 + kMaxBlk;    // [kMaxBlk]
+    cudaEvent_t* const ev_b = ev + 3 + 2 * kMaxBlk;   // [kMaxKc]
     // The copy streams start after the workspace exists (stream order of cs).
-    ok = ok && cudaEventRecord(ev_start, cs) == cudaSuccess &&
+    bool ok = cudaEventRecord(ev_start, cs) == cudaSuccess &&
          cudaStreamWaitEvent(st->copy_in, ev_start, 0) == cudaSuccess &&
          cudaStreamWaitEvent(st->copy_out, ev_start, 0) == cudaSuccess;
 
@@ -135,14 +140,6 @@ int run_host(int M, int N, int K, const float* A, int lda, const float* B, int l
         (void)cudaStreamSynchronize(st->copy_out);
     }
     (void)cudaFreeAsync(ws, cs);
-    for (cudaEvent_t e : {ev_start, ev_in_end, ev_out_end})
-        if (e) (void)cudaEventDestroy(e);
-    for (int i = 0; i < kMaxBlk; ++i) {
-        if (ev_a[i]) (void)cudaEventDestroy(ev_a[i]);
-        if (ev_done[i]) (void)cudaEventDestroy(ev_done[i]);
-    }
-    for (int c = 0; c < kMaxKc; ++c)
-        if (ev_b[c]) (void)cudaEventDestroy(ev_b[c]);
     if (rc != SGEMM_OK) return rc;
     return ok ? SGEMM_OK : SGEMM_ERR_CUDA;
 }

@@ -43,6 +43,12 @@ struct SkScratch {
     unsigned long long tick = 0;       // last use, for eviction
 };
 
+// Row blocks and K chunks of the host-buffer entry's pipeline (api_host.cu).
+constexpr int kHostMaxBlk = 8, kHostMaxKc = 4;
+// Its events: start, copies-in done, copies-out done, then per row block
+// "A block in" and "block's product done", then per K chunk "B chunk in".
+constexpr int kHostEvents = 3 + 2 * kHostMaxBlk + kHostMaxKc;
+
 struct DeviceState {
     std::once_flag once;
     int status = SGEMM_ERR_CUDA;  // result of the one-time set-up
@@ -60,6 +66,8 @@ struct DeviceState {
     std::once_flag copy_once;
     cudaStream_t copy_in = nullptr;   // host-buffer entry: host -> device copies
     cudaStream_t copy_out = nullptr;  // host-buffer entry: device -> host copies
+    cudaEvent_t host_ev[kHostEvents] = {};  // host-buffer entry: its events, made with the streams
+    std::mutex host_mu;               // host-buffer entry: one call enqueues at a time
     std::mutex sk_mu;                        // guards sk_cache, sk_tick and noalloc_seq
     SkScratch sk_cache[kSkCacheEntries];     // per-stream stream-K scratch (sk_lease)
     unsigned long long sk_tick = 0;
