@@ -66,30 +66,48 @@ int run_3xtf32(int M, int N, int K, const float* A, int lda, const float* B, int
     TcLaunch launches[2];
     int nl = 1;
     const long long tiles_m = ceil_div(M, kTcBM);
-    long long split_tiles = 0;  // tiles of the K-split launch
+    // The launch whose tiles are split along K (if any): split_s parts per
+    // tile, split_tiles tiles of width split_bn.
+    int split_l = -1, split_s = 1, split_bn = 0;
+    long long split_tiles = 0;
     if (variant >= 3) {
         const KernelEntry wk = variant == 4 ? tf32x3_wide_pb_kernel() : tf32x3_wide_kernel();
         const bool pb = variant == 4;
         const long long wide = tiles_m * ceil_div(N, 256);
         const long long full = (wide / st->sm_count) * st->sm_count;
         if (full > 0 && full < wide && K >= 1024) {
-            split_tiles = wide - full;
+            split_l = 1, split_s = 2, split_bn = 256, split_tiles = wide - full;
             launches[0] = {wk, 256, 16, full, 0, 0, pb};
-            launches[1] = {wk, 256, 16, 2 * split_tiles, static_cast<int>(full), 2, pb};
+            launches[1] = {wk, 256, 16, split_s * split_tiles, static_cast<int>(full), split_s, pb};
             nl = 2;
         } else {
             launches[0] = {wk, 256, 16, wide, 0, 0, pb};
         }
     } else {
         const KernelEntry k = variant == 1 ? tf32x3_kernel() : tf32x3_direct_kernel();
-        launches[0] = {k, kTcBN, kTcBK, tiles_m * ceil_div(N, kTcBN), 0, 0, false};
+        const long long tiles = tiles_m * ceil_div(N, kTcBN);
+        // Variant 1 with at most half as many tiles as SMs and K >= 2048: each
+        // tile's K slices split among s = min(4, SMs / tiles) CTAs, two slices
+        // each at least (8192 x 128 x 8192: 64 tiles, s = 2, 82 -> 137
+        // TFLOP/s; 128 x 8192 x 16384: 87 -> 157).  With shorter K the later
+        // parts' pass and the parts' own pipeline fill cost more than the
+        // fuller GPU gains (1024^3: 61 -> 54).
+        long long s = 1;
+        if (variant == 1 && 2 * tiles <= st->sm_count && K >= 2048)
+            s = std::min<long long>({4, st->sm_count / tiles, ceil_div(K, kTcBK) / 2});
+        if (s >= 2) {
+            split_l = 0, split_s = static_cast<int>(s), split_bn = kTcBN, split_tiles = tiles;
+            launches[0] = {k, kTcBN, kTcBK, split_s * tiles, 0, split_s, false};
+        } else {
+            launches[0] = {k, kTcBN, kTcBK, tiles, 0, 0, false};
+        }
     }
-    // The second halves' partial tiles (128 x 256 floats each), from the pool.
+    // The later parts' partial tiles (128 x split_bn floats each), from the pool.
     void* ws_split = nullptr;
-    if (split_tiles > 0) {
+    if (split_l >= 0) {
         cudaMemPool_t pool = workspace_pool(dev, *st);
-        if (!pool || cudaMallocFromPoolAsync(&ws_split, static_cast<size_t>(split_tiles) * kTcBM * 256 * sizeof(float),
-                                             pool, cs) != cudaSuccess) {
+        const size_t bytes = static_cast<size_t>(split_tiles) * (split_s - 1) * kTcBM * split_bn * sizeof(float);
+        if (!pool || cudaMallocFromPoolAsync(&ws_split, bytes, pool, cs) != cudaSuccess) {
             (void)cudaGetLastError();
             packed.release();
             return SGEMM_ERR_CUDA;
@@ -153,7 +171,7 @@ int run_3xtf32(int M, int N, int K, const float* A, int lda, const float* B, int
         prm.tiles_n = static_cast<int>(ceil_div(N, ln.bn));
         prm.tile_base = ln.tile_base;
         prm.k_split = ln.k_split;
-        prm.ws = ln.k_split == 2 ? static_cast<float*>(ws_split) : nullptr;
+        prm.ws = ln.k_split > 1 ? static_cast<float*>(ws_split) : nullptr;
         prm.vec_store = ((reinterpret_cast<uintptr_t>(C) & 15u) == 0 && ldc % 4 == 0) ? 1 : 0;
         prm.skip_stage = opt ? opt->debug_skip_stage : 0;
         prm.timeout_ns = (opt && opt->timeout_ns) ? opt->timeout_ns : kDefaultTimeoutNs;
@@ -172,9 +190,9 @@ int run_3xtf32(int M, int N, int K, const float* A, int lda, const float* B, int
             rc = SGEMM_ERR_CUDA;
         }
     }
-    if (rc == SGEMM_OK && split_tiles > 0)
-        rc = add_tiles(C, ldc, M, N, static_cast<float*>(ws_split), kTcBM, 256, launches[1].tile_base,
-                       static_cast<int>(ceil_div(N, 256)), static_cast<int>(split_tiles), cs);
+    if (rc == SGEMM_OK && split_l >= 0)
+        rc = add_tiles(C, ldc, M, N, static_cast<float*>(ws_split), kTcBM, split_bn, launches[split_l].tile_base,
+                       static_cast<int>(ceil_div(N, split_bn)), static_cast<int>(split_tiles), split_s - 1, cs);
     if (ws_split) (void)cudaFreeAsync(ws_split, cs);
     if (ws) (void)cudaFreeAsync(ws, cs);
     packed.release();

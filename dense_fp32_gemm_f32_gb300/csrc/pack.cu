@@ -181,30 +181,36 @@ __global__ void __launch_bounds__(kTile* kTileRows)
 
 namespace {
 
-// C[tile] += ws[t] for the tiles tile_base + t (t < gridDim.x) of tm x tn
-// floats, tiles_n tiles per row of tiles; ws tile t is tm x tn with pitch tn.
-// Elements beyond M or N are skipped.  One block row of 4 tile rows, 256
+// C[tile] += ws[t parts] + ... + ws[t parts + parts - 1], added in that
+// order, for the tiles tile_base + t (t < gridDim.x) of tm x tn floats,
+// tiles_n tiles per row of tiles; each ws tile is tm x tn with pitch tn.
+// Elements beyond M or N are skipped.  One block per 4 tile rows, 256
 // threads across the tile's width.
 __global__ void __launch_bounds__(256) add_tiles_kernel(float* C, long long ldc, int M, int N, const float* ws,
-                                                       int tm, int tn, int tile_base, int tiles_n) {
+                                                       int tm, int tn, int tile_base, int tiles_n, int parts) {
     const int tile = tile_base + static_cast<int>(blockIdx.x);
     const int m0 = (tile / tiles_n) * tm, n0 = (tile % tiles_n) * tn;
-    const float* w = ws + static_cast<long long>(blockIdx.x) * tm * tn;
+    const long long tile_floats = static_cast<long long>(tm) * tn;
+    const float* w = ws + static_cast<long long>(blockIdx.x) * parts * tile_floats;
     for (int r = static_cast<int>(blockIdx.y) * 4; r < min(tm, static_cast<int>(blockIdx.y) * 4 + 4); ++r) {
         if (m0 + r >= M) break;
-        for (int c = static_cast<int>(threadIdx.x); c < tn && n0 + c < N; c += 256)
-            C[static_cast<long long>(m0 + r) * ldc + n0 + c] += w[static_cast<long long>(r) * tn + c];
+        for (int c = static_cast<int>(threadIdx.x); c < tn && n0 + c < N; c += 256) {
+            float* out = C + static_cast<long long>(m0 + r) * ldc + n0 + c;
+            float acc = *out;
+            for (int q = 0; q < parts; ++q) acc += w[q * tile_floats + static_cast<long long>(r) * tn + c];
+            *out = acc;
+        }
     }
 }
 
 }  // namespace
 
 int add_tiles(float* C, long long ldc, int M, int N, const float* ws, int tm, int tn, int tile_base, int tiles_n,
-              int ntiles, cudaStream_t stream) {
+              int ntiles, int parts, cudaStream_t stream) {
     if (ntiles <= 0) return SGEMM_OK;
-    if (tm <= 0 || tn <= 0 || tiles_n <= 0 || ntiles > 0x7fffffff) return SGEMM_ERR_INVALID_ARG;
+    if (tm <= 0 || tn <= 0 || tiles_n <= 0 || parts < 1 || ntiles > 0x7fffffff) return SGEMM_ERR_INVALID_ARG;
     add_tiles_kernel<<<dim3(static_cast<unsigned>(ntiles), static_cast<unsigned>((tm + 3) / 4)), 256, 0, stream>>>(
-        C, ldc, M, N, ws, tm, tn, tile_base, tiles_n);
+        C, ldc, M, N, ws, tm, tn, tile_base, tiles_n, parts);
     if (cudaGetLastError() != cudaSuccess) return SGEMM_ERR_CUDA;
     return SGEMM_OK;
 }

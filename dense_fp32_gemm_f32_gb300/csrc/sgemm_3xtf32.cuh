@@ -89,17 +89,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    // Tile and K range: the whole K for one tile per CTA, or (k_split) half of
-    // it, CTAs 2t and 2t + 1 sharing tile tile_base + t.  K slices are counted
-    // from kbase: nkt slices here.
-    const bool ksplit = p.k_split == 2;
-    const int tile = p.tile_base + static_cast<int>(ksplit ? blockIdx.x >> 1 : blockIdx.x);
+    // Tile and K range: the whole K for one tile per CTA, or (k_split = s) one
+    // of s parts of it, CTAs s t .. s t + s - 1 sharing tile tile_base + t.
+    // K slices are counted from kbase: nkt slices here.
+    const int ks = p.k_split > 1 ? p.k_split : 1;
+    const bool ksplit = ks > 1;
+    const int local = static_cast<int>(blockIdx.x) / ks;  // this launch's tile index
+    const int part = static_cast<int>(blockIdx.x) % ks;
+    const int tile = p.tile_base + local;
     const int m0 = (tile / p.tiles_n) * T::kBM;
     const int n0 = (tile % p.tiles_n) * BN;
-    const int khalf = p.num_k_tiles / 2;
-    const bool second = ksplit && (blockIdx.x & 1);
-    const int kbase = second ? khalf : 0;
-    const int nkt = ksplit ? (second ? p.num_k_tiles - khalf : khalf) : p.num_k_tiles;
+    const int kbase = (p.num_k_tiles * part) / ks;
+    const int nkt = (p.num_k_tiles * (part + 1)) / ks - kbase;
+    const bool second = part > 0;  // a later part: its partial tile goes to ws
     const unsigned long long tmo = p.timeout_ns;
 
     if (threadIdx.x == 0) {
@@ -138,7 +140,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             for (int r = 0; r < T::kRawStages; ++r) issued_round[r] = -1;
 #pragma unroll
             for (int s = 0; s < T::kSplitStages; ++s) issued_sround[s] = -1;
-            const bool skip_here = p.skip_stage > 0 && blockIdx.x == 0 && p.tile_base == 0 && !ksplit;
+            // (debug: the first CTA of the launch, with K split its first part)
+            const bool skip_here = p.skip_stage > 0 && blockIdx.x == 0 && p.tile_base == 0;
             for (int kt = 0; kt < nkt; ++kt) {
                 const int r = kt % T::kRawStages;
                 const int round = kt / T::kRawStages;
@@ -299,10 +302,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             constexpr int kChunksPerWarp = (BN / 32) / (kTcSplitWarps / 4);
             const int row = m0 + 32 * q + lane;
             float* crow = p.C + static_cast<long long>(row) * p.ldc;
-            // (the second half of a split tile: its whole partial tile, rows
-            // and columns beyond M and N included, into the workspace tile)
-            float* wrow = second ? p.ws + (static_cast<long long>(blockIdx.x >> 1) * T::kBM + 32 * q + lane) * BN
-                                 : nullptr;
+            // (a later part of a split tile: its whole partial tile, rows and
+            // columns beyond M and N included, into its workspace tile)
+            float* wrow =
+                second ? p.ws + ((static_cast<long long>(local) * (ks - 1) + part - 1) * T::kBM + 32 * q + lane) * BN
+                       : nullptr;
 #pragma unroll
             for (int cc = 0; cc < kChunksPerWarp; ++cc) {
                 const int ch = half * kChunksPerWarp + cc;

@@ -70,10 +70,11 @@ struct TcParams {
     int num_k_tiles;  // ceil(K / BK)
     int tiles_n;      // output tiles per row of tiles
     int tile_base;    // this launch's first tile (split-tile kernels)
-    int k_split;      // split-tile kernels, 2: CTAs 2t and 2t + 1 take the first
-                      // and second halves of the K slices of tile tile_base + t;
-                      // the second stores its partial tile to ws (t-th tile of
-                      // 128 x BN floats, pitch BN), added to C afterwards
+    int k_split;      // split-tile kernels, s >= 2: CTAs s t .. s t + s - 1 take
+                      // the s parts of the K slices of tile tile_base + t; part 0
+                      // stores to C, part q > 0 its partial tile to ws tile
+                      // t (s - 1) + q - 1 (128 x BN floats, pitch BN), added to
+                      // C afterwards in part order
     float* ws;
     int vec_store;    // C base 16-byte aligned and ldc % 4 == 0
     int skip_stage;   // debug: CTA 0's producer never issues K-slice skip_stage-1

@@ -324,7 +324,9 @@ int sgemm_f32_ex(int M, int N, int K,
  * splits A only).  3 and 4 run whole waves of 128 x 256 tiles; when K >=
  * 1024 the tiles of a last partial wave run in a second launch with their K
  * slices split between two CTAs, the second halves added into C by a third
- * (a pool workspace of 128 KiB per such tile).  Other fields are ignored. */
+ * (a pool workspace of 128 KiB per such tile).  Variant 1 with at most half
+ * as many tiles as SMs and K >= 2048 splits every tile's K slices among up to
+ * 4 CTAs in the same way.  Other fields are ignored. */
 int sgemm_3xtf32_ex(int M, int N, int K,
                     const float* A, int lda,
                     const float* B, int ldb,

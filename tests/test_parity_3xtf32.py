@@ -162,15 +162,34 @@ def test_wide_tiles_with_split_tail(shape, dist, variant):
     check(run(A, B, variant=variant), C64, bound, exact=exact, what=f"wide tail v{variant} {shape} {dist}")
 
 
+@pytest.mark.parametrize("shape", [(256, 256, 2500), (128, 1024, 4096), (1000, 700, 2100), (300, 500, 1000),
+                                   (1023, 1025, 3001)])
+@pytest.mark.parametrize("dist", ["uniform", "int"])
+def test_variant1_k_split(shape, dist):
+    """Variant 1 with at most half as many tiles as SMs and K >= 2048: each
+    tile's K slices split among s CTAs (256 x 256 x 2500: 4 tiles, s = 4, 79
+    slices in parts of 19 and 20; 128 x 1024 x 4096: s = 4; 1000 x 700 x
+    2100: 48 tiles, s = 3; 300 x 500 x 1000: K too short, no split; 1023 x
+    1025 x 3001: 72 tiles on repacked operands, s = 2), the later parts added
+    into C in order."""
+    M, N, K = shape
+    A, B = make_operands(M, N, K, dist, 82)
+    exact = dist == "int"
+    C64, bound = oracle.gemm_f64(A.numpy(), B.numpy(), with_bound=not exact)
+    check(run(A, B, variant=1), C64, bound, exact=exact, what=f"v1 split {shape} {dist}")
+
+
 @pytest.mark.parametrize("variant", [1, 2, 3, 4])
 def test_timeout_is_reported_and_recovers(variant):
-    """CTA 0's producer skips a K slice: its split warps' bounded wait
-    expires, the MMA issuer and the epilogue give up in turn, tensor memory is
-    freed, and the status word says so.  The next call is unaffected."""
+    """CTA 0's producer skips its second K slice (CTA 0 takes the first part
+    of a tile whose K slices are split among CTAs, as variant 1 does here):
+    its split warps' bounded wait expires, the MMA issuer and the epilogue
+    give up in turn, tensor memory is freed, and the status word says so.
+    The next call is unaffected."""
     A, B = make_operands(128, 256, 256, "uniform", 80)
     dA, dB = to_device(A), to_device(B)
     assert g.check_status() == 0
-    g.sgemm_3xtf32_ex(dA, dB, variant=variant, debug_skip_stage=3, timeout_ns=20_000_000)
+    g.sgemm_3xtf32_ex(dA, dB, variant=variant, debug_skip_stage=2, timeout_ns=20_000_000)
     assert g.check_status() == 4
     C = g.sgemm_3xtf32(dA, dB)
     assert g.check_status() == 0
