@@ -2,7 +2,8 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload NAME]
-    python bench.py --sweep [--workload NAME ...]   # ablation table, one JSON line per run
+    python bench.py --sweep [--sweep-workloads NAME ...]   # ablation table, one JSON line per run
+    python bench.py --cpu-table [--cpu-seconds S]          # the oracle on every named problem
 
 One step is one C = A x B call on the named workload (default: the square
 4096^3 problem with standard-normal inputs, seed 3).  Inputs are resident in
