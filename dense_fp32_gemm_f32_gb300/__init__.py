@@ -134,12 +134,14 @@ def sgemm_f32_ex(A, B, out=None, *, stream=None, producer=0, split_k=0, multicas
     return _call("sgemm_f32_ex", A, B, out, stream, opt)
 
 
-def sgemm_3xtf32_ex(A, B, out=None, *, stream=None, variant=0, debug_skip_stage=0, timeout_ns=0) -> torch.Tensor:
+def sgemm_3xtf32_ex(A, B, out=None, *, stream=None, variant=0, split_k=0, debug_skip_stage=0,
+                    timeout_ns=0) -> torch.Tensor:
     """sgemm_3xtf32 with forced choices: ``variant`` 1 = split-tile kernel,
     2 = direct-A kernel, 3 = split-tile kernel on 128 x 256 tiles with
     K-slices of 16, 4 = variant 3 with B's TF32 parts pre-split in HBM
-    (0 = automatic)."""
-    opt = Options(0, 0, 0, variant, 0, debug_skip_stage, timeout_ns, 0, 0, 0, 0, 0)
+    (0 = automatic); ``split_k`` 1 = no K split, 2..4 = each tile's K slices
+    split among that many CTAs (variant 1; 0 = automatic)."""
+    opt = Options(0, split_k, 0, variant, 0, debug_skip_stage, timeout_ns, 0, 0, 0, 0, 0)
     return _call("sgemm_3xtf32_ex", A, B, out, stream, opt)
 
 

@@ -10,6 +10,9 @@ int run_3xtf32(int M, int N, int K, const float* A, int lda, const float* B, int
     int rc = validate(M, N, K, A, lda, B, ldb, C, ldc);
     if (rc != SGEMM_OK) return rc;
     if (opt && opt->debug_skip_stage < 0) return SGEMM_ERR_INVALID_ARG;
+    // Forced K split: 1 = none, 2..4 = CTAs per tile (variant 1 only).
+    const int force_s = opt ? opt->split_k : 0;
+    if (force_s < 0 || force_s > 4) return SGEMM_ERR_INVALID_ARG;
     if (M == 0 || N == 0) return SGEMM_OK;
     int dev = 0;
     DeviceState* st = nullptr;
@@ -35,7 +38,8 @@ int run_3xtf32(int M, int N, int K, const float* A, int lda, const float* B, int
     int variant = (opt && opt->math) ? opt->math : 0;
     if (variant == 0)
         variant = 2 * ceil_div(M, kTcBM) * ceil_div(N, 256) < st->sm_count ? 1 : M >= 1024 ? 4 : 3;
-    if (variant < 1 || variant > 4) return SGEMM_ERR_INVALID_ARG;
+    if (variant < 1 || variant > 4 || (force_s >= 2 && variant != 1)) return SGEMM_ERR_INVALID_ARG;
+    if (force_s >= 2 && force_s > ceil_div(K, kTcBK)) return SGEMM_ERR_INVALID_ARG;  // a slice per part at least
     const cudaStream_t cs = static_cast<cudaStream_t>(stream);
     const int misaligned = (tma_ok(A, lda) ? 0 : 1) | (tma_ok(B, ldb) ? 0 : 2);
     Repacked packed;
@@ -75,7 +79,7 @@ int run_3xtf32(int M, int N, int K, const float* A, int lda, const float* B, int
         const bool pb = variant == 4;
         const long long wide = tiles_m * ceil_div(N, 256);
         const long long full = (wide / st->sm_count) * st->sm_count;
-        if (full > 0 && full < wide && K >= 1024) {
+        if (full > 0 && full < wide && K >= 1024 && force_s != 1) {
             split_l = 1, split_s = 2, split_bn = 256, split_tiles = wide - full;
             launches[0] = {wk, 256, 16, full, 0, 0, pb};
             launches[1] = {wk, 256, 16, split_s * split_tiles, static_cast<int>(full), split_s, pb};
@@ -86,15 +90,23 @@ int run_3xtf32(int M, int N, int K, const float* A, int lda, const float* B, int
     } else {
         const KernelEntry k = variant == 1 ? tf32x3_kernel() : tf32x3_direct_kernel();
         const long long tiles = tiles_m * ceil_div(N, kTcBN);
-        // Variant 1 with at most half as many tiles as SMs and K >= 2048: each
-        // tile's K slices split among s = min(4, SMs / tiles) CTAs, two slices
-        // each at least (8192 x 128 x 8192: 64 tiles, s = 2, 82 -> 137
-        // TFLOP/s; 128 x 8192 x 16384: 87 -> 157).  With shorter K the later
-        // parts' pass and the parts' own pipeline fill cost more than the
-        // fuller GPU gains (1024^3: 61 -> 54).
+        // Variant 1 with at most half as many tiles as SMs: each tile's nk K
+        // slices split among s = min(4, SMs / tiles, nk / 2) CTAs when that
+        // takes at least 14 slices off each CTA (nk (s - 1) / s >= 14).  A
+        // split costs about as much as 11 slices of one CTA (a second launch,
+        // the partial tiles written and added, each part's pipeline fill).
+        // Measured, TFLOP/s without / with: 1024^3 (s = 2) 61 / 64, 1024^2 x
+        // 2048 72 / 94, 768^3 (s = 4) 31 / 36, 8192 x 128 x 8192 85 / 144, 128
+        // x 8192 x 16384 89 / 162; 1024^2 x 768 55 / 51 and 256^3 2.0 / 1.7
+        // stay whole.
+        const long long nk = ceil_div(K, kTcBK);
         long long s = 1;
-        if (variant == 1 && 2 * tiles <= st->sm_count && K >= 2048)
-            s = std::min<long long>({4, st->sm_count / tiles, ceil_div(K, kTcBK) / 2});
+        if (force_s >= 1) {
+            s = force_s;
+        } else if (variant == 1 && 2 * tiles <= st->sm_count) {
+            s = std::min<long long>({4, st->sm_count / tiles, nk / 2});
+            if (s >= 2 && nk * (s - 1) < 14 * s) s = 1;
+        }
         if (s >= 2) {
             split_l = 0, split_s = static_cast<int>(s), split_bn = kTcBN, split_tiles = tiles;
             launches[0] = {k, kTcBN, kTcBK, split_s * tiles, 0, split_s, false};

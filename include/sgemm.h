@@ -325,8 +325,12 @@ int sgemm_f32_ex(int M, int N, int K,
  * 1024 the tiles of a last partial wave run in a second launch with their K
  * slices split between two CTAs, the second halves added into C by a third
  * (a pool workspace of 128 KiB per such tile).  Variant 1 with at most half
- * as many tiles as SMs and K >= 2048 splits every tile's K slices among up to
- * 4 CTAs in the same way.  Other fields are ignored. */
+ * as many tiles as SMs splits every tile's nk = ceil(K / 32) K slices among
+ * s = min(4, SMs / tiles, nk / 2) CTAs in the same way when nk (s - 1) / s >=
+ * 14 (1024^3: s = 2).  split_k: 0 = automatic, 1 = no K split (any
+ * variant), 2..4 = every tile's K slices split among that many CTAs (variant
+ * 1, forced or automatic, and at least one 32-deep slice per CTA; otherwise
+ * SGEMM_ERR_INVALID_ARG).  Other fields are ignored. */
 int sgemm_3xtf32_ex(int M, int N, int K,
                     const float* A, int lda,
                     const float* B, int ldb,

@@ -29,12 +29,12 @@ def cuda_device():
 VARIANTS = [0, 1, 2, 3, 4]
 
 
-def run(A, B, *, lda=None, ldb=None, ldc=None, variant=0):
+def run(A, B, *, lda=None, ldb=None, ldc=None, variant=0, split_k=0):
     dA = to_device(A, lda)
     dB = to_device(B, ldb)
     dC = to_device(torch.full((A.shape[0], B.shape[1]), float("nan")), ldc)
-    if variant:
-        g.sgemm_3xtf32_ex(dA, dB, dC, variant=variant)
+    if variant or split_k:
+        g.sgemm_3xtf32_ex(dA, dB, dC, variant=variant, split_k=split_k)
     else:
         g.sgemm_3xtf32(dA, dB, dC)
     torch.cuda.synchronize()
@@ -163,15 +163,16 @@ def test_wide_tiles_with_split_tail(shape, dist, variant):
 
 
 @pytest.mark.parametrize("shape", [(256, 256, 2500), (128, 1024, 4096), (1000, 700, 2100), (300, 500, 1000),
-                                   (1023, 1025, 3001)])
+                                   (300, 500, 500), (1023, 1025, 3001), (1024, 1024, 1024)])
 @pytest.mark.parametrize("dist", ["uniform", "int"])
 def test_variant1_k_split(shape, dist):
-    """Variant 1 with at most half as many tiles as SMs and K >= 2048: each
-    tile's K slices split among s CTAs (256 x 256 x 2500: 4 tiles, s = 4, 79
-    slices in parts of 19 and 20; 128 x 1024 x 4096: s = 4; 1000 x 700 x
-    2100: 48 tiles, s = 3; 300 x 500 x 1000: K too short, no split; 1023 x
-    1025 x 3001: 72 tiles on repacked operands, s = 2), the later parts added
-    into C in order."""
+    """Variant 1 with at most half as many tiles as SMs: each tile's nk K
+    slices split among s CTAs when that takes 14 slices off each (256 x 256 x
+    2500: 4 tiles, s = 4, 79 slices in parts of 19 and 20; 128 x 1024 x 4096:
+    s = 4; 1000 x 700 x 2100: 48 tiles, s = 3; 300 x 500 x 1000: 12 tiles,
+    s = 4; 300 x 500 x 500: 16 slices, too few, no split; 1023 x 1025 x 3001:
+    72 tiles on repacked operands, s = 2; 1024 x 1024 x 1024: s = 2), the
+    later parts added into C in order."""
     M, N, K = shape
     A, B = make_operands(M, N, K, dist, 82)
     exact = dist == "int"
@@ -179,17 +180,57 @@ def test_variant1_k_split(shape, dist):
     check(run(A, B, variant=1), C64, bound, exact=exact, what=f"v1 split {shape} {dist}")
 
 
-@pytest.mark.parametrize("variant", [1, 2, 3, 4])
-def test_timeout_is_reported_and_recovers(variant):
-    """CTA 0's producer skips its second K slice (CTA 0 takes the first part
-    of a tile whose K slices are split among CTAs, as variant 1 does here):
-    its split warps' bounded wait expires, the MMA issuer and the epilogue
-    give up in turn, tensor memory is freed, and the status word says so.
-    The next call is unaffected."""
+@pytest.mark.parametrize("shape,s", [((1000, 700, 300), 2), ((257, 516, 100), 4), ((256, 256, 1000), 3),
+                                     ((129, 132, 64), 2), ((300, 260, 36), 2), ((1024, 1024, 1024), 1),
+                                     ((2048, 2048, 512), 4)])
+@pytest.mark.parametrize("dist", ["uniform", "int"])
+def test_variant1_forced_k_split(shape, s, dist):
+    """split_k forces the CTAs per tile along K (1 = none), down to one
+    32-deep slice per CTA (257 x 516 x 100: 4 slices in 4 parts; 300 x 260 x
+    36: a full slice and a 4-deep one), also with more CTAs than SMs (2048 x
+    2048 x 512: 256 tiles x 4).  Row pitches are multiples of 16 bytes, so the
+    tensor maps read the operands in place."""
+    M, N, K = shape
+    A, B = make_operands(M, N, K, dist, 83)
+    exact = dist == "int"
+    C64, bound = oracle.gemm_f64(A.numpy(), B.numpy(), with_bound=not exact)
+    check(run(A, B, variant=1, split_k=s), C64, bound, exact=exact, what=f"v1 split_k={s} {shape} {dist}")
+
+
+@pytest.mark.parametrize("variant", [0, 3, 4])
+def test_wide_tiles_without_split_tail(variant):
+    """split_k = 1 on the 128 x 256 tiles: the last partial wave runs whole."""
+    M, N, K = 1200, 4000, 1040
+    A, B = make_operands(M, N, K, "uniform", 84)
+    C64, bound = oracle.gemm_f64(A.numpy(), B.numpy())
+    check(run(A, B, variant=variant, split_k=1), C64, bound, exact=False, what=f"v{variant} split_k=1")
+
+
+@pytest.mark.parametrize("kw,K", [(dict(split_k=5), 256), (dict(split_k=-1), 256), (dict(variant=3, split_k=2), 256),
+                                  (dict(variant=2, split_k=2), 256), (dict(variant=4, split_k=4), 256),
+                                  (dict(variant=1, split_k=3), 64), (dict(split_k=2), 4096)])
+def test_forced_k_split_refusals(kw, K):
+    """Refused before any launch: split_k out of 0..4, a K split on the
+    direct-A or wide-tile kernels (also when the automatic choice is a wide
+    one: 2048 x 2048 tiles fill half the SMs), more parts than 32-deep slices."""
+    M = N = 2048 if K == 4096 else 256
+    dA = torch.zeros((M, K), device="cuda")
+    dB = torch.zeros((K, N), device="cuda")
+    with pytest.raises(g._lib.SgemmError) as e:
+        g.sgemm_3xtf32_ex(dA, dB, **kw)
+    assert e.value.status == 1
+
+
+@pytest.mark.parametrize("variant,split_k", [(1, 0), (1, 4), (2, 0), (3, 0), (4, 0)])
+def test_timeout_is_reported_and_recovers(variant, split_k):
+    """CTA 0's producer skips its second K slice (with split_k = 4 CTA 0 takes
+    the first two of the tile's 8 slices): its split warps' bounded wait
+    expires, the MMA issuer and the epilogue give up in turn, tensor memory is
+    freed, and the status word says so.  The next call is unaffected."""
     A, B = make_operands(128, 256, 256, "uniform", 80)
     dA, dB = to_device(A), to_device(B)
     assert g.check_status() == 0
-    g.sgemm_3xtf32_ex(dA, dB, variant=variant, debug_skip_stage=2, timeout_ns=20_000_000)
+    g.sgemm_3xtf32_ex(dA, dB, variant=variant, split_k=split_k, debug_skip_stage=2, timeout_ns=20_000_000)
     assert g.check_status() == 4
     C = g.sgemm_3xtf32(dA, dB)
     assert g.check_status() == 0
