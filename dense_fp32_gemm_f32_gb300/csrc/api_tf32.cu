@@ -54,12 +54,12 @@ int run_3xtf32(int M, int N, int K, const float* A, int lda, const float* B, int
     // Variants 3 and 4 run whole waves of 128 x 256 tiles; the tiles of a
     // last partial wave run in a second launch of the same kernel with their K
     // slices split between two CTAs each (twice the CTAs at half the work: a
-    // fuller wave), the second halves' partial tiles then added into C by
-    // add_tiles (a fixed order: deterministic).  4096^3: 3 waves of 152 wide
-    // tiles, then 112 CTAs on the last 56 (262 -> 277 TFLOP/s).  Only for
-    // K >= 1024: with shorter K the halves' pipeline fill and the pass adding
-    // them cost more than the fuller wave gains (4096 x 4096 x 256: 117 ->
-    // 105), and the tiles run as one launch.
+    // fuller wave), the second halves' partial tiles added into C by the
+    // tile's CTA that finishes last (in part order: deterministic).  4096^3:
+    // 3 waves of 152 wide tiles, then 112 CTAs on the last 56 (262 -> 277
+    // TFLOP/s).  Only for K >= 1024: with shorter K the halves' pipeline fill
+    // and the partial tiles' traffic cost more than the fuller wave gains
+    // (4096 x 4096 x 256: 117 -> 105), and the tiles run as one launch.
     struct TcLaunch {
         KernelEntry k;
         int bn, bk;
@@ -91,13 +91,14 @@ int run_3xtf32(int M, int N, int K, const float* A, int lda, const float* B, int
         const KernelEntry k = variant == 1 ? tf32x3_kernel() : tf32x3_direct_kernel();
         const long long tiles = tiles_m * ceil_div(N, kTcBN);
         // Variant 1 with at most half as many tiles as SMs: each tile's nk K
-        // slices split among s = min(4, SMs / tiles, nk / 2) CTAs when that
-        // takes at least 14 slices off each CTA (nk (s - 1) / s >= 14).  A
-        // split costs about as much as 11 slices of one CTA (a second launch,
-        // the partial tiles written and added, each part's pipeline fill).
-        // Measured, TFLOP/s without / with: 1024^3 (s = 2) 61 / 64, 1024^2 x
-        // 2048 72 / 94, 768^3 (s = 4) 31 / 36, 8192 x 128 x 8192 85 / 144, 128
-        // x 8192 x 16384 89 / 162; 1024^2 x 768 55 / 51 and 256^3 2.0 / 1.7
+        // slices split among s = min(4, SMs / tiles, nk / 2) CTAs when the
+        // slices that takes off each CTA, nk (s - 1) / s, outnumber the
+        // split's cost, measured as about 7 + 2 (s - 1) slices of one CTA (the
+        // counters' reset, each part's pipeline fill, the partial tiles
+        // written, read and added).  Measured, TFLOP/s without / with: 1024^3
+        // (s = 2) 61 / 71, 1024^2 x 768 55 / 61, 1024^2 x 2048 72 / 101, 768^3
+        // (s = 4) 31 / 34, 8192 x 128 x 8192 85 / 148, 128 x 8192 x 16384 89 /
+        // 165; 1024^2 x 512 46 / 44, 512^3 12.1 / 11.6 and 256^3 2.0 / 1.6
         // stay whole.
         const long long nk = ceil_div(K, kTcBK);
         long long s = 1;
@@ -105,7 +106,7 @@ int run_3xtf32(int M, int N, int K, const float* A, int lda, const float* B, int
             s = force_s;
         } else if (variant == 1 && 2 * tiles <= st->sm_count) {
             s = std::min<long long>({4, st->sm_count / tiles, nk / 2});
-            if (s >= 2 && nk * (s - 1) < 14 * s) s = 1;
+            if (s >= 2 && nk * (s - 1) < s * (7 + 2 * (s - 1))) s = 1;
         }
         if (s >= 2) {
             split_l = 0, split_s = static_cast<int>(s), split_bn = kTcBN, split_tiles = tiles;
@@ -114,13 +115,25 @@ int run_3xtf32(int M, int N, int K, const float* A, int lda, const float* B, int
             launches[0] = {k, kTcBN, kTcBK, tiles, 0, 0, false};
         }
     }
-    // The later parts' partial tiles (128 x split_bn floats each), from the pool.
+    // The later parts' partial tiles (128 x split_bn floats each) and a
+    // counter of arrived parts per split tile (zeroed here), from the pool.
     void* ws_split = nullptr;
+    unsigned int* split_count = nullptr;
     if (split_l >= 0) {
         cudaMemPool_t pool = workspace_pool(dev, *st);
-        const size_t bytes = static_cast<size_t>(split_tiles) * (split_s - 1) * kTcBM * split_bn * sizeof(float);
-        if (!pool || cudaMallocFromPoolAsync(&ws_split, bytes, pool, cs) != cudaSuccess) {
+        const size_t part_bytes =
+            (static_cast<size_t>(split_tiles) * (split_s - 1) * kTcBM * split_bn * sizeof(float) + 255) &
+            ~size_t{255};
+        const size_t count_bytes = static_cast<size_t>(split_tiles) * sizeof(unsigned int);
+        if (!pool || cudaMallocFromPoolAsync(&ws_split, part_bytes + count_bytes, pool, cs) != cudaSuccess) {
             (void)cudaGetLastError();
+            packed.release();
+            return SGEMM_ERR_CUDA;
+        }
+        split_count = reinterpret_cast<unsigned int*>(static_cast<char*>(ws_split) + part_bytes);
+        if (cudaMemsetAsync(split_count, 0, count_bytes, cs) != cudaSuccess) {
+            (void)cudaGetLastError();
+            (void)cudaFreeAsync(ws_split, cs);
             packed.release();
             return SGEMM_ERR_CUDA;
         }
@@ -184,6 +197,7 @@ int run_3xtf32(int M, int N, int K, const float* A, int lda, const float* B, int
         prm.tile_base = ln.tile_base;
         prm.k_split = ln.k_split;
         prm.ws = ln.k_split > 1 ? static_cast<float*>(ws_split) : nullptr;
+        prm.split_count = ln.k_split > 1 ? split_count : nullptr;
         prm.vec_store = ((reinterpret_cast<uintptr_t>(C) & 15u) == 0 && ldc % 4 == 0) ? 1 : 0;
         prm.skip_stage = opt ? opt->debug_skip_stage : 0;
         prm.timeout_ns = (opt && opt->timeout_ns) ? opt->timeout_ns : kDefaultTimeoutNs;
@@ -202,9 +216,6 @@ int run_3xtf32(int M, int N, int K, const float* A, int lda, const float* B, int
             rc = SGEMM_ERR_CUDA;
         }
     }
-    if (rc == SGEMM_OK && split_l >= 0)
-        rc = add_tiles(C, ldc, M, N, static_cast<float*>(ws_split), kTcBM, split_bn, launches[split_l].tile_base,
-                       static_cast<int>(ceil_div(N, split_bn)), static_cast<int>(split_tiles), split_s - 1, cs);
     if (ws_split) (void)cudaFreeAsync(ws_split, cs);
     if (ws) (void)cudaFreeAsync(ws, cs);
     packed.release();

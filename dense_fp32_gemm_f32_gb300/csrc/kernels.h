@@ -84,13 +84,6 @@ KernelEntry small_kernel(bool a_mn, bool scaled);
 // padding columns; B (K x N, pitch ldb) of any alignment.  One launch on `stream`.
 int split_transpose_b(const float* B, long long ldb, int K, int N, float* big, float* small, long long ld_out,
                       cudaStream_t stream);
-// C[tile] += ws[t parts + q] for q = 0 .. parts - 1 in that order, t <
-// ntiles, tile = tile_base + t (tm x tn tiles, tiles_n per row of tiles; ws
-// tiles of tm x tn floats, pitch tn), elements beyond M or N skipped: the
-// later K parts of the tensor-core kernels' split tiles.  One launch on
-// `stream`.
-int add_tiles(float* C, long long ldc, int M, int N, const float* ws, int tm, int tn, int tile_base, int tiles_n,
-              int ntiles, int parts, cudaStream_t stream);
 // The split-tile kernel on 128 x 256 tiles with B's TF32 parts pre-split by
 // split_transpose_b (loaded by the TMA; the kernel splits A only).
 KernelEntry tf32x3_wide_pb_kernel();

@@ -179,57 +179,6 @@ __global__ void __launch_bounds__(kTile* kTileRows)
 
 }  // namespace
 
-namespace {
-
-// C[tile] += ws[t parts] + ... + ws[t parts + parts - 1], added in that
-// order, for the tiles tile_base + t (t < gridDim.x) of tm x tn floats,
-// tiles_n tiles per row of tiles; each ws tile is tm x tn with pitch tn (tn
-// divides 256).  Elements beyond M or N are skipped.  Block (t, y) takes rows
-// [8y, 8y + 8) of tile t: thread i column i % tn of rows i / tn + (256 / tn) j,
-// all its loads issued before its stores (C and ws do not overlap).
-constexpr int kAddRows = 8;
-
-__global__ void __launch_bounds__(256)
-    add_tiles_kernel(float* __restrict__ C, long long ldc, int M, int N, const float* __restrict__ ws, int tm, int tn,
-                     int tile_base, int tiles_n, int parts) {
-    const int tile = tile_base + static_cast<int>(blockIdx.x);
-    const int m0 = (tile / tiles_n) * tm, n0 = (tile % tiles_n) * tn;
-    const long long tile_floats = static_cast<long long>(tm) * tn;
-    const float* __restrict__ w = ws + static_cast<long long>(blockIdx.x) * parts * tile_floats;
-    const int c = static_cast<int>(threadIdx.x) % tn;
-    const int step = 256 / tn;  // rows a pass of the block covers
-    const int r0 = static_cast<int>(blockIdx.y) * kAddRows + static_cast<int>(threadIdx.x) / tn;
-    float acc[kAddRows];
-    bool in[kAddRows];
-#pragma unroll
-    for (int j = 0; j < kAddRows; ++j) {
-        const int r = r0 + step * j;
-        in[j] = step * j < kAddRows && r < tm && m0 + r < M && n0 + c < N;
-        acc[j] = in[j] ? C[static_cast<long long>(m0 + r) * ldc + n0 + c] : 0.f;
-    }
-    for (int q = 0; q < parts; ++q)
-#pragma unroll
-        for (int j = 0; j < kAddRows; ++j)
-            if (in[j]) acc[j] += w[q * tile_floats + static_cast<long long>(r0 + step * j) * tn + c];
-#pragma unroll
-    for (int j = 0; j < kAddRows; ++j)
-        if (in[j]) C[static_cast<long long>(m0 + r0 + step * j) * ldc + n0 + c] = acc[j];
-}
-
-}  // namespace
-
-int add_tiles(float* C, long long ldc, int M, int N, const float* ws, int tm, int tn, int tile_base, int tiles_n,
-              int ntiles, int parts, cudaStream_t stream) {
-    if (ntiles <= 0) return SGEMM_OK;
-    if (tm <= 0 || tn <= 0 || tn > 256 || 256 % tn != 0 || tiles_n <= 0 || parts < 1 || ntiles > 0x7fffffff)
-        return SGEMM_ERR_INVALID_ARG;
-    add_tiles_kernel<<<dim3(static_cast<unsigned>(ntiles), static_cast<unsigned>((tm + kAddRows - 1) / kAddRows)), 256,
-                       0, stream>>>(
-        C, ldc, M, N, ws, tm, tn, tile_base, tiles_n, parts);
-    if (cudaGetLastError() != cudaSuccess) return SGEMM_ERR_CUDA;
-    return SGEMM_OK;
-}
-
 int split_transpose_b(const float* B, long long ldb, int K, int N, float* big, float* small, long long ld_out,
                       cudaStream_t stream) {
     if (K <= 0 || N <= 0) return SGEMM_OK;

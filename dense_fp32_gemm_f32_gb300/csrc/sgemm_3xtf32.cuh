@@ -60,6 +60,70 @@ __device__ __forceinline__ uint64_t tc_operand_desc(uint32_t saddr) {
         return umma_desc_kmajor_sw64(saddr);
 }
 
+// The last CTA of a K-split tile: C[tile] = ((C + P_1) + P_2) + ... over the
+// later parts' partial tiles P_q in ws, element by element in part order (C
+// holds part 0's result).  Elements beyond M or N are not touched.  One SM
+// does this alone, so it is bound by the latency of its loads: each thread
+// takes 13 groups of 4 columns (g, g + 320, ...; a whole 128 x 128 tile in
+// one pass) and issues all their loads before any add or store.  L2 reads
+// (__ldcg), since other SMs wrote these lines during this launch.
+template <int BN>
+__device__ __forceinline__ void tc_split_finish(const TcParams& p, int local, int ks, int m0, int n0) {
+    constexpr int kBM = kTcBM;
+    constexpr int kGroups = kBM * BN / 4;
+    constexpr int kPer = (kTcBM * kTcBN / 4 + kTcThreads - 1) / kTcThreads;
+    const int rows = min(kBM, p.M - m0), cols = min(BN, p.N - n0);
+    const long long part_floats = static_cast<long long>(kBM) * BN;
+    const float* const w = p.ws + static_cast<long long>(local) * (ks - 1) * part_floats;
+    for (int g0 = static_cast<int>(threadIdx.x); g0 < kGroups; g0 += kPer * kTcThreads) {
+        float4 a[kPer];
+#pragma unroll
+        for (int j = 0; j < kPer; ++j) {
+            const int g = g0 + j * kTcThreads;
+            const int r = g / (BN / 4), c = 4 * (g % (BN / 4));
+            const bool row_in = g < kGroups && r < rows;
+            const float* out = p.C + static_cast<long long>(m0 + r) * p.ldc + n0 + c;
+            if (p.vec_store && row_in && c + 3 < cols) {
+                a[j] = __ldcg(reinterpret_cast<const float4*>(out));
+            } else {
+                a[j].x = row_in && c < cols ? __ldcg(out) : 0.f;
+                a[j].y = row_in && c + 1 < cols ? __ldcg(out + 1) : 0.f;
+                a[j].z = row_in && c + 2 < cols ? __ldcg(out + 2) : 0.f;
+                a[j].w = row_in && c + 3 < cols ? __ldcg(out + 3) : 0.f;
+            }
+        }
+        for (int q = 0; q < ks - 1; ++q) {
+#pragma unroll
+            for (int j = 0; j < kPer; ++j) {
+                const int g = g0 + j * kTcThreads;
+                if (g < kGroups) {
+                    const float4 v = __ldcg(reinterpret_cast<const float4*>(
+                        w + q * part_floats + static_cast<long long>(g / (BN / 4)) * BN + 4 * (g % (BN / 4))));
+                    a[j].x += v.x;
+                    a[j].y += v.y;
+                    a[j].z += v.z;
+                    a[j].w += v.w;
+                }
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < kPer; ++j) {
+            const int g = g0 + j * kTcThreads;
+            const int r = g / (BN / 4), c = 4 * (g % (BN / 4));
+            if (g >= kGroups || r >= rows) continue;
+            float* out = p.C + static_cast<long long>(m0 + r) * p.ldc + n0 + c;
+            if (p.vec_store && c + 3 < cols) {
+                *reinterpret_cast<float4*>(out) = a[j];
+            } else {
+                if (c < cols) out[0] = a[j].x;
+                if (c + 1 < cols) out[1] = a[j].y;
+                if (c + 2 < cols) out[2] = a[j].z;
+                if (c + 3 < cols) out[3] = a[j].w;
+            }
+        }
+    }
+}
+
 // PB: B's TF32 parts come pre-split and transposed (N x K) from HBM: tmB maps
 // the big part and tmB2 the small part, each loaded by the TMA into its slot
 // of the split stage (arriving on split_full with the split warps, which then
@@ -85,7 +149,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     auto split_empty = [&](int s) { return bars + 8u * (2 * R + S + s); };
     const uint32_t acc_full = bars + 8u * (2 * R + 2 * S);
     const uint32_t tmem_slot = acc_full + 8u;
-    static_assert(8 * (2 * T::kRawStages + 2 * T::kSplitStages + 1) + 4 <= 256, "barrier area");
+    int* const last_part = reinterpret_cast<int*>(smem_raw + (tmem_slot + 4u - raw_base));  // K split
+    static_assert(8 * (2 * T::kRawStages + 2 * T::kSplitStages + 1) + 8 <= 256, "barrier area");
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -340,11 +405,24 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
 
     if (timed_out) atomicOr(p.status, kTcStatusTimeout);
+    if (ksplit) __threadfence();  // this thread's partial-tile stores, before the arrival below
     tc_fence_before_sync();
-    __syncthreads();
+    const int any_timed_out = __syncthreads_or(timed_out ? 1 : 0);
     if (warp == 1) {
         tc_fence_after_sync();
         tmem_dealloc(tmem, T::kTmemCols);
+    }
+    // K split: every part that stored its partial tile arrives on the tile's
+    // counter; the CTA whose arrival is the last adds the parts into C.  No
+    // CTA waits on another, and the sum does not depend on which CTA that is.
+    if (ksplit && !any_timed_out) {
+        if (threadIdx.x == 0) {
+            const unsigned int prev = atomicAdd(p.split_count + local, 1u);
+            *last_part = prev == static_cast<unsigned int>(ks - 1) ? 1 : 0;
+            __threadfence();  // (the other parts' stores precede their arrivals)
+        }
+        __syncthreads();
+        if (*last_part) tc_split_finish<BN>(p, local, ks, m0, n0);
     }
 }
 

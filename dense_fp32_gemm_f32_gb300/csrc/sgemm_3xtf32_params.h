@@ -73,9 +73,11 @@ struct TcParams {
     int k_split;      // split-tile kernels, s >= 2: CTAs s t .. s t + s - 1 take
                       // the s parts of the K slices of tile tile_base + t; part 0
                       // stores to C, part q > 0 its partial tile to ws tile
-                      // t (s - 1) + q - 1 (128 x BN floats, pitch BN), added to
-                      // C afterwards in part order
+                      // t (s - 1) + q - 1 (128 x BN floats, pitch BN); the CTA
+                      // whose arrival on split_count[t] (zero at launch) is the
+                      // s-th adds the partial tiles into C in part order
     float* ws;
+    unsigned int* split_count;
     int vec_store;    // C base 16-byte aligned and ldc % 4 == 0
     int skip_stage;   // debug: CTA 0's producer never issues K-slice skip_stage-1
     unsigned long long timeout_ns;

@@ -323,11 +323,12 @@ int sgemm_f32_ex(int M, int N, int K,
  * pool buffer first (2 x N x K floats; the kernel loads them with the TMA and
  * splits A only).  3 and 4 run whole waves of 128 x 256 tiles; when K >=
  * 1024 the tiles of a last partial wave run in a second launch with their K
- * slices split between two CTAs, the second halves added into C by a third
- * (a pool workspace of 128 KiB per such tile).  Variant 1 with at most half
- * as many tiles as SMs splits every tile's nk = ceil(K / 32) K slices among
- * s = min(4, SMs / tiles, nk / 2) CTAs in the same way when nk (s - 1) / s >=
- * 14 (1024^3: s = 2).  split_k: 0 = automatic, 1 = no K split (any
+ * slices split between two CTAs, the second halves' partial tiles (a pool
+ * workspace of 128 KiB per such tile) added into C, in part order, by the
+ * tile's CTA that finishes last.  Variant 1 with at most half as many tiles as
+ * SMs splits every tile's nk = ceil(K / 32) K slices among s = min(4, SMs /
+ * tiles, nk / 2) CTAs in the same way when nk (s - 1) / s >= 7 + 2 (s - 1)
+ * (1024^3: s = 2).  split_k: 0 = automatic, 1 = no K split (any
  * variant), 2..4 = every tile's K slices split among that many CTAs (variant
  * 1, forced or automatic, and at least one 32-deep slice per CTA; otherwise
  * SGEMM_ERR_INVALID_ARG).  Other fields are ignored. */

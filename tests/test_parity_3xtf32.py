@@ -167,7 +167,8 @@ def test_wide_tiles_with_split_tail(shape, dist, variant):
 @pytest.mark.parametrize("dist", ["uniform", "int"])
 def test_variant1_k_split(shape, dist):
     """Variant 1 with at most half as many tiles as SMs: each tile's nk K
-    slices split among s CTAs when that takes 14 slices off each (256 x 256 x
+    slices split among s CTAs when that takes 7 + 2 (s - 1) slices off each,
+    the CTA of a tile that finishes last adding the parts (256 x 256 x
     2500: 4 tiles, s = 4, 79 slices in parts of 19 and 20; 128 x 1024 x 4096:
     s = 4; 1000 x 700 x 2100: 48 tiles, s = 3; 300 x 500 x 1000: 12 tiles,
     s = 4; 300 x 500 x 500: 16 slices, too few, no split; 1023 x 1025 x 3001:
@@ -195,6 +196,35 @@ def test_variant1_forced_k_split(shape, s, dist):
     exact = dist == "int"
     C64, bound = oracle.gemm_f64(A.numpy(), B.numpy(), with_bound=not exact)
     check(run(A, B, variant=1, split_k=s), C64, bound, exact=exact, what=f"v1 split_k={s} {shape} {dist}")
+
+
+@pytest.mark.parametrize("M,N,K,s,ldc", [(256, 384, 1000, 3, None), (200, 300, 700, 2, 301), (130, 260, 2048, 4, None)])
+def test_k_split_sums_parts_in_order(M, N, K, s, ldc):
+    """The K-split result is the float32 sum, in part order, of the parts'
+    own products: part q covers the 32-deep slices [floor(nk q / s),
+    floor(nk (q + 1) / s)), and its product, computed alone by the unsplit
+    kernel on that K range (the same MMAs in the same order), is bit-identical
+    to the part's partial tile.  So C must equal ((P_0 + P_1) + ...) exactly,
+    whichever CTA of a tile finishes last and adds the parts, on the
+    vector path and (ldc = 301) the element path with ragged edge tiles."""
+    A, B = make_operands(M, N, K, "normal", 85)
+    dA, dB = to_device(A), to_device(B)
+    nk = -(-K // 32)
+    parts = []
+    for q in range(s):
+        k0, k1 = 32 * (nk * q // s), min(K, 32 * (nk * (q + 1) // s))
+        parts.append(g.sgemm_3xtf32_ex(dA[:, k0:k1], dB[k0:k1, :], variant=1, split_k=1))
+    torch.cuda.synchronize()
+    expect = parts[0].cpu().numpy()
+    for P in parts[1:]:
+        expect = expect + P.cpu().numpy()
+    for _ in range(3):
+        dC = to_device(torch.full((M, N), float("nan")), ldc)
+        g.sgemm_3xtf32_ex(dA, dB, dC, variant=1, split_k=s)
+        torch.cuda.synchronize()
+        assert np.array_equal(dC.cpu().numpy().view(np.uint32), expect.view(np.uint32))
+    C64, bound = oracle.gemm_f64(A.numpy(), B.numpy())
+    check(expect, C64, bound, exact=False, what=f"split parts {M}x{N}x{K}")
 
 
 @pytest.mark.parametrize("variant", [0, 3, 4])
