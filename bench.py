@@ -464,8 +464,9 @@ def run_ours(args, rank, world, local_rank):
     return 0
 
 
-# sgemm_3xtf32 kernels: 1 = split-tile, 2 = direct-A, 3 = split-tile on 128 x 256 tiles, 4 = 3 with B pre-split.
-SWEEP_TF32X3_VARIANTS = [1, 2, 3, 4]
+# sgemm_3xtf32 kernels: 1 = split-tile (also with its K split off), 2 = direct-A, 3 = split-tile on 128 x 256
+# tiles, 4 = 3 with B pre-split.
+SWEEP_TF32X3 = [{"variant": 1, "split_k": 1}, {"variant": 1}, {"variant": 2}, {"variant": 3}, {"variant": 4}]
 SWEEP_OPTIONS = [
     {},
     {"producer": 1},
@@ -524,8 +525,7 @@ def run_sweep(args):
         C = torch.empty((p.M, p.N), dtype=torch.float32, device="cuda")
         runs = [(opt, (lambda o=opt: g.sgemm_f32_ex(A, B, C, **o)) if opt else (lambda: g.sgemm_f32(A, B, C)))
                 for opt in SWEEP_OPTIONS]
-        runs += [({"entry": "sgemm_3xtf32", "variant": v}, lambda v=v: g.sgemm_3xtf32_ex(A, B, C, variant=v))
-                 for v in SWEEP_TF32X3_VARIANTS]
+        runs += [({"entry": "sgemm_3xtf32", **o}, lambda o=o: g.sgemm_3xtf32_ex(A, B, C, **o)) for o in SWEEP_TF32X3]
         # The general entry: alpha = 1.5, beta = 0.5 (C read and written) in
         # each storage order (a transposed operand is copied transposed first).
         At, Bt = A.t().contiguous(), B.t().contiguous()
