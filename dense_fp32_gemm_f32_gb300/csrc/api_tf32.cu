@@ -31,10 +31,10 @@ int run_3xtf32(int M, int N, int K, const float* A, int lda, const float* B, int
     // kernel's split warps A only.  Automatic: 4 when the 128 x 256 tiles
     // number at least half the SMs and M >= 1024 (the pass costs ~6/M bytes
     // per flop), 3 when they do with fewer rows, else 1.  Measured on GB300,
-    // TFLOP/s for 1 / 3 / 4: 2048^3 155 / 181 / 203, 4096^3 195 / 218 / 261,
-    // 8192^3 204 / 243 / 289, 4096 x 4096 x 256 102 / 112 / 116; with fewer
-    // tiles 1024^3 61 / 40 / 45, 8192 x 128 x 8192 82 / 51 / 71, 128 x 8192 x
-    // 16384 86 / 53 / 22.
+    // TFLOP/s for 1 / 3 / 4: 2048^3 152 / 181 / 205, 4096^3 195 / 221 / 274,
+    // 8192^3 208 / 246 / 289, 4096 x 4096 x 256 99 / 112 / 117; with fewer
+    // tiles (variant 1 with its K split, below) 1024^3 72 / 40 / 46, 8192 x
+    // 128 x 8192 148 / 51 / 70, 128 x 8192 x 16384 162 / 54 / 23.
     int variant = (opt && opt->math) ? opt->math : 0;
     if (variant == 0)
         variant = 2 * ceil_div(M, kTcBM) * ceil_div(N, 256) < st->sm_count ? 1 : M >= 1024 ? 4 : 3;
