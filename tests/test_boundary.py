@@ -86,6 +86,16 @@ def test_bad_options_rejected():
     assert lib.sgemm_f32_ex(4, 4, 4, FAKE_A, 4, FAKE_B, 4, FAKE_C, 4, None, ctypes.byref(opt)) == _lib.ERR_INVALID_ARG
 
 
+@pytest.mark.parametrize("split_k", [-1, 5, 9])
+def test_tensor_core_split_count_rejected_on_host(split_k):
+    """sgemm_3xtf32_ex takes 0..4 CTAs per tile along K; anything else is
+    refused before any device call."""
+    lib = _lib.load()
+    opt = _lib.Options(0, split_k, 0, 0, 0, 0, 0, 0, 0)
+    assert lib.sgemm_3xtf32_ex(4, 4, 4, FAKE_A, 4, FAKE_B, 4, FAKE_C, 4, None, ctypes.byref(opt)) == \
+        _lib.ERR_INVALID_ARG
+
+
 def test_no_cpu_fallback_without_gpu():
     """Without a usable GPU a valid call fails loudly instead of computing on the host."""
     import torch
