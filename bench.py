@@ -471,7 +471,6 @@ SWEEP_OPTIONS = [
     {},
     {"producer": 1},
     {"math": 1},
-    {"multicast": 2},
     {"stages": 1},
     {"stages": 2},
     {"stages": 6},

@@ -125,7 +125,6 @@ int init_device(int dev, DeviceState& st) {
         set_smem_attr(tf32x3_wide_kernel()) != SGEMM_OK || set_smem_attr(tf32x3_wide_pb_kernel()) != SGEMM_OK)
         return SGEMM_ERR_CUDA;
     const KernelEntry ref = ffma_kernel_tma(4, kMathFfma2);
-    st.max_clusters_pair = max_active_clusters(ref, 2, 1);
     st.max_clusters_split[1] = st.sm_count;
     for (int s = 2; s <= 8; ++s) st.max_clusters_split[s] = max_active_clusters(ref, 1, s);
     load_encoder();

@@ -81,7 +81,7 @@ int run_ffma(int M, int N, int K, const float* A, int lda, const float* B, int l
         }  // (automatic: without the pool's buffer, A is read as stored)
     }
     // (With a transposed A, make_plan rejects forced producer, tile, math,
-    // stage and multicast choices: the transposed-A kernels have one form.)
+    // and stage choices: the transposed-A kernels have one form.)
     Plan pl;
     rc = make_plan(*st, M, N, K, A, lda, B, ldb, opt, &pl, a_mn);
     if (rc != SGEMM_OK) {
@@ -129,7 +129,7 @@ int run_ffma(int M, int N, int K, const float* A, int lda, const float* B, int l
     std::memset(&tmB, 0, sizeof tmB);
     if (is_tma(pl.producer)) {
         rc = pl.a_mn ? encode_2d(&tmA, A, M, K, lda, kBM, kBK, CU_TENSOR_MAP_SWIZZLE_NONE)  // {m, k} boxes of 128 x 32
-                     : encode_2d(&tmA, A, K, M, lda, kBK, kBM / pl.mcast, CU_TENSOR_MAP_SWIZZLE_128B);
+                     : encode_2d(&tmA, A, K, M, lda, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B);
         if (rc == SGEMM_OK) rc = encode_2d(&tmB, B, N, K, ldb, pl.bn, kBK, CU_TENSOR_MAP_SWIZZLE_NONE);
         if (rc != SGEMM_OK) {
             release_pack();
@@ -148,7 +148,6 @@ int run_ffma(int M, int N, int K, const float* A, int lda, const float* B, int l
     prm.C = C;
     prm.ldc = ldc;
     prm.num_k_tiles = pl.num_k_tiles;
-    prm.mcast = pl.mcast;
     prm.vec_store = ((reinterpret_cast<uintptr_t>(C) & 15u) == 0 && ldc % 4 == 0) ? 1 : 0;
     prm.tiles_n = pl.tiles_n;
     prm.skip_stage = opt ? opt->debug_skip_stage : 0;
@@ -214,12 +213,12 @@ int run_ffma(int M, int N, int K, const float* A, int lda, const float* B, int l
             attr.val.cooperative = 1;
         } else {
             attr.id = cudaLaunchAttributeClusterDimension;
-            attr.val.clusterDim.x = pl.mcast;
+            attr.val.clusterDim.x = 1;
             attr.val.clusterDim.y = 1;
             attr.val.clusterDim.z = ln.split;
         }
         cfg.attrs = &attr;
-        cfg.numAttrs = (pl.sk || pl.mcast > 1 || ln.split > 1) ? 1 : 0;
+        cfg.numAttrs = (pl.sk || ln.split > 1) ? 1 : 0;
         void* args[3] = {&tmA, &tmB, &prm};
         if (cudaLaunchKernelExC(&cfg, k.fn, args) != cudaSuccess) {
             (void)cudaGetLastError();
@@ -304,7 +303,6 @@ int run_ffma_noalloc(int M, int N, int K, const float* A, int lda, const float* 
     prm.ldc = ldc;
     prm.num_k_tiles = pl.num_k_tiles;
     prm.split = 1;
-    prm.mcast = 1;
     prm.vec_store = ((reinterpret_cast<uintptr_t>(C) & 15u) == 0 && ldc % 4 == 0) ? 1 : 0;
     prm.tile_base = 0;
     prm.tiles_n = pl.tiles_n;

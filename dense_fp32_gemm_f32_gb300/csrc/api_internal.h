@@ -53,7 +53,6 @@ struct DeviceState {
     std::once_flag once;
     int status = SGEMM_ERR_CUDA;  // result of the one-time set-up
     int sm_count = 0;
-    int max_clusters_pair = 0;    // co-resident 2-CTA clusters of the FFMA kernel
     int max_clusters_split[9] = {0};
     bool regsplit_ok = false;     // the register-split kernels were built at kRegsLaunch registers
     int fused_per_sm[7] = {0};    // co-resident fused-producer CTAs per SM, by stage count
@@ -179,9 +178,8 @@ struct Plan {
     int producer = kProducerTma;
     int math = kMathFfma2;
     int stages = 4;
-    int mcast = 1;
     int bn = kBN;     // output tile width (kBN or kBNWide)
-    int tiles_n = 0;  // tiles per row of tiles (padded to even for multicast pairs)
+    int tiles_n = 0;  // tiles per row of tiles
     int num_k_tiles = 0;
     int nlaunch = 1;
     Launch launch[2];

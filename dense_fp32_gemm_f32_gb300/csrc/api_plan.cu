@@ -105,11 +105,14 @@ bool tma_ok(const float* p, int ld) {
 int make_plan(const DeviceState& st, int M, int N, int K, const float* A, int lda, const float* B, int ldb,
               const sgemm_options* opt, Plan* out, bool a_mn) {
     Plan pl;
+    // Cluster multicast of the operand slices is not built (see the
+    // multicast field of sgemm_options).
+    if (opt && (opt->multicast < 0 || opt->multicast > 2)) return SGEMM_ERR_INVALID_ARG;
+    if (opt && opt->multicast == 2) return SGEMM_ERR_NOT_IMPLEMENTED;
     // Transposed A (general entry only): tensor-map readable A, TMA producer
-    // warp, 2 stages, paired FMA, no multicast (see below).
+    // warp, 2 stages, paired FMA.
     if (a_mn && (K == 0 || !tma_ok(A, lda) ||
-                 (opt && (opt->producer || (opt->tile_n && opt->tile_n != kBNWide) || opt->math || opt->stages ||
-                          opt->multicast == 2))))
+                 (opt && (opt->producer || (opt->tile_n && opt->tile_n != kBNWide) || opt->math || opt->stages))))
         return SGEMM_ERR_INVALID_ARG;
     pl.a_mn = a_mn;
     pl.num_k_tiles = static_cast<int>(ceil_div(K, kBK));
@@ -147,7 +150,7 @@ int make_plan(const DeviceState& st, int M, int N, int K, const float* A, int ld
     } else if (want_prod == SGEMM_PRODUCER_AUTO) {
         // Tensor maps: A transposed in shared memory, unless it already is in
         // HBM (a_mn) or another choice rules the transposing warps out.
-        const bool x_ok = !a_mn && !(opt && (opt->multicast == 2 || (opt->tile_n && opt->tile_n != kBN) ||
+        const bool x_ok = !a_mn && !(opt && ((opt->tile_n && opt->tile_n != kBN) ||
                                              (opt->stages && (opt->stages < 2 || opt->stages > 4))));
         pl.producer = !aligned ? kProducerCpAsync : x_ok ? kProducerTmaX : kProducerTma;
     } else {
@@ -213,7 +216,7 @@ int make_plan(const DeviceState& st, int M, int N, int K, const float* A, int ld
     // 8192x128x8192 +22 %); tiny problems keep cluster split-K.
     const int want_sk = opt ? opt->stream_k : 0;
     if (want_sk < 0 || want_sk > 2) return SGEMM_ERR_INVALID_ARG;
-    const bool forced_other = opt && (opt->split_k || opt->multicast == 2 || opt->tail_split > 1);
+    const bool forced_other = opt && (opt->split_k || opt->tail_split > 1);
     const bool use_sk = want_sk == 2 || (want_sk == 0 && !forced_other && pl.num_k_tiles > 0 &&
                                          tiles * pl.num_k_tiles >= 2LL * slots);
 
@@ -240,22 +243,7 @@ int make_plan(const DeviceState& st, int M, int N, int K, const float* A, int ld
     if (split > 1 && pl.stages < 2) return SGEMM_ERR_INVALID_ARG;  // partial tile needs 64 KiB of ring
     if (split > 1 && pl.producer == kProducerFused) return SGEMM_ERR_INVALID_ARG;  // two CTAs per SM: no clusters
 
-    // Multicast pairs along N (TMA producer, no split).  Measured on GB300 at
-    // 1024^3..8192^3 the pairing costs more (the two CTAs release every slot
-    // in lock step) than the halved L2->SM traffic for A saves, so it is off
-    // unless forced.
-    const int want_mc = opt ? opt->multicast : 0;
-    if (want_mc == 2) {
-        if (split > 1 || !is_tma(pl.producer) || pl.producer == kProducerFused || pl.producer == kProducerTmaX)
-            return SGEMM_ERR_INVALID_ARG;
-        if (st.max_clusters_pair < 1) return SGEMM_ERR_UNSUPPORTED;
-        pl.mcast = 2;
-    } else if (want_mc == 0 || want_mc == 1) {
-        pl.mcast = 1;
-    } else {
-        return SGEMM_ERR_INVALID_ARG;
-    }
-    pl.tiles_n = static_cast<int>(pl.mcast == 2 ? 2 * ceil_div(tiles_n, 2) : tiles_n);
+    pl.tiles_n = static_cast<int>(tiles_n);
     const long long grid_tiles = static_cast<long long>(pl.tiles_n) * tiles_m;
 
     // Last partial wave.  When the tiles do not fill a whole number of waves,
@@ -272,7 +260,7 @@ int make_plan(const DeviceState& st, int M, int N, int K, const float* A, int ld
     pl.launch[0].split = split;
     const int want_tail = opt ? opt->tail_split : 0;
     if (want_tail < 0 || want_tail > 8) return SGEMM_ERR_INVALID_ARG;
-    if (split == 1 && pl.mcast == 1 && want_tail > 1 && grid_tiles > st.sm_count && pl.producer != kProducerFused) {
+    if (split == 1 && want_tail > 1 && grid_tiles > st.sm_count && pl.producer != kProducerFused) {
         const long long full = (grid_tiles / st.sm_count) * st.sm_count;
         const long long rem = grid_tiles - full;
         // keep at least four K slices per CTA of the tail
@@ -288,7 +276,7 @@ int make_plan(const DeviceState& st, int M, int N, int K, const float* A, int ld
     // Stream-K schedule: one CTA per SM (two for the fused producer), partial
     // tiles finished through a global workspace.
     if (use_sk) {
-        if (split > 1 || pl.mcast > 1 || pl.nlaunch > 1 || pl.num_k_tiles == 0) return SGEMM_ERR_INVALID_ARG;
+        if (split > 1 || pl.nlaunch > 1 || pl.num_k_tiles == 0) return SGEMM_ERR_INVALID_ARG;
         // All but the last full wave run data-parallel (raster order keeps
         // the A and B panels in flight few, as in the plain launch); the last
         // full wave and the partial one are dealt out as units.
@@ -322,8 +310,8 @@ int encode_2d(CUtensorMap* map, const float* base, long long inner, long long ou
 
 const char* describe_plan(const Plan& pl) {
     static thread_local char buf[128];
-    int n = std::snprintf(buf, sizeof buf, "%s/%s/mc%d/s%d/st%d", producer_name(pl.producer),
-                          pl.math == kMathFfma2 ? "ffma2" : "ffma", pl.mcast, pl.launch[0].split, pl.stages);
+    int n = std::snprintf(buf, sizeof buf, "%s/%s/s%d/st%d", producer_name(pl.producer),
+                          pl.math == kMathFfma2 ? "ffma2" : "ffma", pl.launch[0].split, pl.stages);
     if (pl.nlaunch > 1 && n > 0 && n < static_cast<int>(sizeof buf))
         n += std::snprintf(buf + n, sizeof buf - n, "/tail%d:%d", pl.launch[1].split, pl.launch[1].tiles);
     if (pl.sk && n > 0 && n < static_cast<int>(sizeof buf))

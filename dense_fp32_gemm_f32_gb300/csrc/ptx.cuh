@@ -1,5 +1,5 @@
 // Inline-PTX wrappers for the sm_103a features the kernels use: mbarriers,
-// tensor-map bulk copies (TMA) with optional cluster multicast, cp.async with
+// tensor-map bulk copies (TMA), cp.async with
 // zero fill, cluster ranks / barriers / distributed shared memory, the
 // fifth-generation tensor core (tcgen05: tensor-memory allocation, MMA,
 // commit, tensor-memory loads, fences), warpgroup register limits, TF32
@@ -38,17 +38,6 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
 
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
-// Arrive on the barrier at shared address `bar` (this CTA's offset) in CTA
-// `rank` of the cluster, with release semantics at cluster scope.
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar, uint32_t rank) {
-    asm volatile(
-        "{\n\t.reg .b32 ra;\n\t"
-        "mapa.shared::cluster.u32 ra, %0, %1;\n\t"
-        "mbarrier.arrive.release.cluster.shared::cluster.b64 _, [ra];\n\t}" ::"r"(bar),
-        "r"(rank)
-        : "memory");
 }
 
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
@@ -95,18 +84,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* map, uint3
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
-        : "memory");
-}
-
-// Same copy delivered to the same shared offset in every CTA of the cluster
-// whose bit is set in `mask`; each destination's barrier at offset `bar`
-// receives the bytes that land in that CTA.
-__device__ __forceinline__ void tma_load_2d_multicast(uint32_t dst, const void* map, uint32_t bar, int c0, int c1,
-                                                      uint16_t mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "h"(mask)
         : "memory");
 }
 

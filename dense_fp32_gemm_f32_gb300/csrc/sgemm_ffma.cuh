@@ -38,10 +38,6 @@
 //    `split` CTAs along K computes partial tiles over disjoint K ranges and
 //    reduces them through distributed shared memory in a fixed rank order
 //    (deterministic, no global workspace);
-//  * cluster multicast: two CTAs that share the same rows of A (neighbours
-//    along N) each fetch half of the A slice and the TMA multicasts it into
-//    both CTAs' shared memory, halving the L2->SM traffic for A (slower on
-//    GB300; kept as an option);
 //  * paired FMA (fma.rn.f32x2, sm_100 family): two multiply-adds per
 //    instruction, halving the issue slots the outer product needs;
 //  * the scaled epilogue of the general entry (SCALED), and the producer
@@ -155,10 +151,9 @@ struct FfmaParams {
     long long ldc;
     int num_k_tiles;       // ceil(K / kBK)
     int split;             // CTAs per cluster along K (== gridDim.z); 1 = no split
-    int mcast;             // 2 = pairs of CTAs along N share A by multicast; 1 = off
     int vec_store;         // C base 16-byte aligned and ldc % 4 == 0
     int tile_base;         // linear index of this launch's first output tile
-    int tiles_n;           // output tiles per row of tiles (even when mcast == 2)
+    int tiles_n;           // output tiles per row of tiles
     // Stream-K schedule (sk != 0), one CTA per SM: CTA g first takes whole
     // tiles g, g + G, ... below sk_dp_tiles (data-parallel waves, raster
     // order), then an even share of the units (one K slice of one tile each)
@@ -226,8 +221,7 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), ffma_min_blocks<PROD
     constexpr int H = BN / WN / 32;                      // 4-column groups per thread row (2 or 4)
     constexpr int TQ = 2 * H;                            // column pairs per thread row
     extern __shared__ uint8_t smem_raw[];
-    // 1024-byte alignment for the 128-byte swizzle pattern; identical offset in
-    // every CTA, which multicast relies on.
+    // 1024-byte alignment for the 128-byte swizzle pattern.
     const uint32_t raw_base = smem_addr(smem_raw);
     const uint32_t base = (raw_base + 1023u) & ~1023u;
     uint8_t* const smem = smem_raw + (base - raw_base);
@@ -250,13 +244,12 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), ffma_min_blocks<PROD
     const bool is_producer = !kFused && warp >= CW;
     const int pw = warp - CW;  // producer warp index (when is_producer)
     const int split = p.split;
-    const int mcast = p.mcast;
-    const uint32_t crank = (split > 1 || mcast > 1) ? cluster_ctarank() : 0u;
+    const uint32_t crank = split > 1 ? cluster_ctarank() : 0u;
 
     // Work.  A CTA processes a sequence of segments (tile, kb, ke): the K
     // slices [kb, ke) of one output tile.  Tiles are numbered row of tiles by
     // row of tiles from tile_base, so neighbouring CTAs share rows of A (the
-    // multicast pairs, and the A tiles reused from L2).  Without stream-K
+    // A tiles reused from L2).  Without stream-K
     // there is one segment: the CTA's tile (gridDim.x over tiles) and, with
     // split-K, the K range of cluster rank blockIdx.z.  With stream-K: the
     // data-parallel tiles first, then the CTA's even share of the stream-K
@@ -300,7 +293,7 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), ffma_min_blocks<PROD
     if (threadIdx.x == 0) {
         const uint32_t full_count = kTma ? 1u : 32u * PW;
         // (kX: the transposing warps also release each slot, for its A slice.)
-        const uint32_t empty_count = static_cast<uint32_t>(CW * mcast + (kX ? kTransposeWarps : 0));
+        const uint32_t empty_count = static_cast<uint32_t>(CW + (kX ? kTransposeWarps : 0));
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full_bar(s), full_count);
             mbar_init(empty_bar(s), empty_count);
@@ -312,8 +305,8 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), ffma_min_blocks<PROD
         prefetch_tensormap(&tmA);
         prefetch_tensormap(&tmB);
     }
-    if (mcast > 1 || split > 1) {
-        cluster_sync_all();  // barrier init visible to the peer CTAs before any multicast
+    if (split > 1) {
+        cluster_sync_all();  // the whole cluster has started before any peer access
     } else {
         __syncthreads();
     }
@@ -324,7 +317,7 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), ffma_min_blocks<PROD
 
     // ------------------------------------------------------------ producer
     // The producer and consumer paths never merge again (each ends in its own
-    // share of the split-K / multicast barriers), so that code after a
+    // share of the split-K barriers), so that code after a
     // register-limit change is only reachable through it.
     if (is_producer) {
         // Warpgroup-uniform (warps 8-11).  The producer releases registers
@@ -393,14 +386,8 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), ffma_min_blocks<PROD
                 const int k0 = kt * kBK;
                 if (kTma) {
                     mbar_arrive_expect_tx(full_bar(s), kStageBytes);
-                    if (AMN) {  // (no multicast: the host pairs no CTAs for transposed A)
+                    if (AMN) {
                         tma_load_2d(sA0 + s * kStageABytes, &tmA, full_bar(s), m0, k0);
-                    } else if (mcast > 1) {
-                        // This CTA fetches rows [crank*64, crank*64+64) of the A
-                        // slice and multicasts them into both CTAs of the pair.
-                        const uint32_t half = static_cast<uint32_t>(kStageABytes / 2) * crank;
-                        tma_load_2d_multicast(sA0 + s * kStageABytes + half, &tmA, full_bar(s), k0,
-                                              m0 + static_cast<int>(crank) * (kBM / 2), 0x3);
                     } else {
                         tma_load_2d(sA0 + s * kStageABytes, &tmA, full_bar(s), k0, m0);
                     }
@@ -456,8 +443,6 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), ffma_min_blocks<PROD
         if (split > 1) {
             __syncthreads();
             cluster_sync_all();
-            cluster_sync_all();
-        } else if (mcast > 1) {
             cluster_sync_all();
         }
         return;
@@ -744,10 +729,7 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), ffma_min_blocks<PROD
                 // Every load from stage s has returned (its values were
                 // consumed above): release the slot to the producer(s).
                 __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(empty_bar(s));
-                    if (mcast > 1) mbar_arrive_cluster(empty_bar(s), crank ^ 1u);
-                }
+                if (lane == 0) mbar_arrive(empty_bar(s));
             }
             if (!p.sk || timed_out) break;  // one tile per CTA; its epilogue follows below
 
@@ -856,10 +838,6 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), ffma_min_blocks<PROD
         }
         cluster_sync_all();  // peers keep their shared memory alive until rank 0 has read it
         if (crank != 0) return;
-    } else if (mcast > 1) {
-        // No CTA may leave while its peer can still multicast into it or
-        // arrive on its barriers.
-        cluster_sync_all();
     }
 
     if (p.sk) return;  // (stream-K CTAs stored their tiles above)

@@ -79,10 +79,9 @@ typedef enum sgemm_status {
  * (smaller products).  The schedule is stream-K (one CTA per SM, the work
  * after the last full wave dealt out as K slices) when there are at least two
  * (tile, K slice) units per SM, cluster split-K for smaller outputs.
- * (Two-CTA multicast of A, 128 x 256 tiles, a copy of A transposed in HBM and
- * a K-split second launch for the last partial wave are available through
- * sgemm_f32_ex; measured on GB300 none pays, so none is chosen
- * automatically.)
+ * (128 x 256 tiles, a copy of A transposed in HBM and a K-split second
+ * launch for the last partial wave are available through sgemm_f32_ex;
+ * measured on GB300 none pays, so none is chosen automatically.)
  *   M, N, K      problem sizes (>= 0)
  *   A, lda       device pointer to A, row stride in floats (lda >= K)
  *   B, ldb       device pointer to B, row stride in floats (ldb >= N)
@@ -234,12 +233,11 @@ enum {
     SGEMM_PRODUCER_FUSED = 4,    /* no producer warp: 4-warp CTAs on 128 x 64 tiles, two per SM,
                                     thread 0 issuing the tensor-map copies between its own
                                     multiply-adds (implies tile_n = 64; 2..4 stages, default 4;
-                                    no split-K clusters, no multicast) */
+                                    no split-K clusters) */
     SGEMM_PRODUCER_TMA_X = 5,    /* tensor-map copies, and two producer warps that
                                     transpose each stage's A slice in shared memory for the
                                     consumers to read per k (the transposed-A read without a
-                                    copy of A in HBM; 128 x 128 tiles, 2..4 stages, no
-                                    multicast) */
+                                    copy of A in HBM; 128 x 128 tiles, 2..4 stages) */
     SGEMM_PRODUCER_SMALL = 6     /* the small-problem kernel: one 8-warp CTA per 32 x 32 tile
                                     of C, K split across its warps in 32-deep chunks and the
                                     partials summed in a fixed order; bounds-checked 4-byte
@@ -256,7 +254,10 @@ enum {
 typedef struct sgemm_options {
     int producer;       /* SGEMM_PRODUCER_* */
     int split_k;        /* 0 = auto, 1 = none, 2..8 = CTAs per cluster along K */
-    int multicast;      /* 0 = auto, 1 = off, 2 = two CTAs share A via TMA multicast */
+    int multicast;      /* 0 or 1 = off (the only form built); 2 (two CTAs sharing
+                           A's slices by cluster multicast) returns
+                           SGEMM_ERR_NOT_IMPLEMENTED: that form is not in
+                           this library */
     int math;           /* 0 = auto, 1 = scalar FFMA, 2 = paired FFMA (fma.rn.f32x2) */
     int stages;         /* 0 = auto, else 2..6 shared-memory pipeline stages */
     int debug_skip_stage; /* 0 = off; k > 0: the producer of CTA (0,0,0) never
@@ -348,8 +349,8 @@ int sgemm_check_status(void* stream);
 const char* sgemm_status_string(int status);
 
 /* Describes the variant sgemm_f32 would launch for these sizes and pointers on
- * the current device, as a thread-local string such as "tma/ffma2/mc1/s1/st4"
- * (producer / math / multicast / split-K / stages), with "/tailS:T" appended
+ * the current device, as a thread-local string such as "tma/ffma2/s1/st4"
+ * (producer / math / split-K / stages), with "/tailS:T" appended
  * when T tail tiles run as a second launch split S ways.  Host-only; it
  * launches nothing, but sets up the current device on first use. */
 const char* sgemm_describe(int M, int N, int K,

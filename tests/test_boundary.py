@@ -146,3 +146,15 @@ def test_general_entry_empty_and_unread_operands():
     # needs a device, and without one the call fails loudly
     rc = lib.sgemm_f32_gemm(0, 0, 4, 4, 4, 0.0, 0, 4, 0, 4, 2.0, FAKE_C, 4, None)
     assert rc in (_lib.ERR_CUDA, _lib.ERR_UNSUPPORTED)
+
+
+def test_no_cluster_multicast_load_in_library_or_bench():
+    # The library runs on every rank of a multi-GPU bench; no cluster-multicast
+    # bulk copy may be compiled into it.
+    offenders = []
+    for d in (os.path.join(ROOT, "dense_fp32_gemm_f32_gb300", "csrc"), ROOT):
+        for f in sorted(os.listdir(d)):
+            if f.endswith((".cu", ".cuh", ".h", ".py")):
+                if "multicast::cluster" in open(os.path.join(d, f)).read():
+                    offenders.append(f)
+    assert offenders == []

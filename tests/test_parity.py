@@ -87,20 +87,16 @@ def test_named_problem_sampled_rows(name, dist):
 
 VARIANTS = (
     [dict(producer=1, math=m, stages=s, split_k=1, multicast=1) for m in (1, 2) for s in (1, 2, 3, 4, 5, 6)]
-    + [dict(producer=1, math=m, multicast=2, split_k=1) for m in (1, 2)]
-    + [dict(producer=1, math=2, multicast=2, split_k=1, stages=s) for s in (2, 6)]
     + [dict(producer=pr, math=m, split_k=s, multicast=1) for pr in (1, 2) for m in (1, 2) for s in (2, 3, 4, 8)]
     + [dict(producer=2, math=m, stages=s, split_k=1) for m in (1, 2) for s in (2, 4)]
     + [dict(producer=pr, math=m, stream_k=2) for pr in (1, 2) for m in (1, 2)]
     + [dict(stream_k=2, stages=s) for s in (2, 6)]
     # producer warpgroup with the setmaxnreg register split
     + [dict(producer=3, math=m, stages=s, split_k=1, multicast=1) for m in (1, 2) for s in (1, 4, 6)]
-    + [dict(producer=3, math=2, multicast=2, split_k=1)]
     + [dict(producer=3, math=2, split_k=s, multicast=1) for s in (2, 4)]
     + [dict(producer=3, math=m, stream_k=2) for m in (1, 2)]
     # 128 x 256 tiles (8 x 16 accumulators per thread)
     + [dict(tile_n=256, math=m, stages=s, split_k=1) for m in (1, 2) for s in (2, 3, 4)]
-    + [dict(tile_n=256, multicast=2, split_k=1)]
     + [dict(tile_n=256, split_k=s) for s in (2, 4)]
     + [dict(tile_n=256, stream_k=2, math=m) for m in (1, 2)]
     # fused producer: 4-warp CTAs on 128 x 64 tiles, two per SM
@@ -182,6 +178,19 @@ def test_forced_tma_rejects_unaligned_rows():
     with pytest.raises(g.SgemmError) as e:
         run(A, B, producer=1)
     assert e.value.status == 1
+
+
+def test_multicast_form_is_not_built():
+    # The cluster-multicast form of the operand loads is not in the library:
+    # asking for it is refused before any launch, for every tile width.
+    A, B = make_operands(512, 512, 256, "uniform", 2)
+    for extra in (dict(), dict(tile_n=256), dict(producer=3)):
+        with pytest.raises(g.SgemmError) as e:
+            run(A, B, multicast=2, split_k=1, **extra)
+        assert e.value.status == 5
+    # 0 and 1 both mean "off"
+    C64, bound = oracle.gemm_f64(A.numpy(), B.numpy())
+    check(run(A, B, multicast=1), C64, bound, exact=False, what="multicast=1")
 
 
 # ---------------------------------------------------------------- ragged shapes, edges, layouts
@@ -396,8 +405,7 @@ def test_transposed_a_schedules(opt):
 def test_transposed_a_rejects_forced_kernel_choices():
     A, B = make_operands(128, 128, 64, "uniform", 97)
     dA, dB = to_device(A), to_device(B)
-    for bad in (dict(a_layout=2, producer=2), dict(a_layout=2, tile_n=64), dict(a_layout=2, multicast=2),
-                dict(a_layout=3)):
+    for bad in (dict(a_layout=2, producer=2), dict(a_layout=2, tile_n=64), dict(a_layout=3)):
         with pytest.raises(g._lib.SgemmError):
             g.sgemm_f32_ex(dA, dB, **bad)
 
