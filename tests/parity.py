@@ -7,6 +7,8 @@ exactly 0; on integer-valued inputs the result must equal the oracle exactly.
 """
 from __future__ import annotations
 
+import functools
+
 import numpy as np
 import torch
 
@@ -63,3 +65,16 @@ def sample_rows(M: int, n_random: int = 16, seed: int = 0, tile: int = 128):
     rng = np.random.default_rng(seed)
     rows.update(rng.integers(0, M, size=n_random).tolist())
     return np.array(sorted(r for r in rows if 0 <= r < M), dtype=np.int64)
+
+
+@functools.lru_cache(maxsize=4)
+def oracle_named(name: str):
+    """The oracle's full result (C64, bound) for a named problem (or its
+    ``_int`` twin), computed once per test process: at 4096^3 it takes a few
+    seconds on the host cores, and several test files compare against it."""
+    import oracle
+    from workloads import PROBLEMS, problem_operands
+
+    p = PROBLEMS[name[:-4]].int_variant() if name.endswith("_int") and name not in PROBLEMS else PROBLEMS[name]
+    A, B = problem_operands(p)
+    return oracle.gemm_f64(A.numpy(), B.numpy())

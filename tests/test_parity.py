@@ -11,7 +11,7 @@ import torch
 
 import dense_fp32_gemm_f32_gb300 as g
 import oracle
-from parity import check, sample_rows, to_device
+from parity import check, oracle_named, sample_rows, to_device
 from workloads import PROBLEMS, make_operands, problem_operands
 
 pytestmark = pytest.mark.gpu
@@ -65,18 +65,30 @@ def test_named_problem_integer_exact(name):
     check(C, C64, None, exact=True, what=p.name)
 
 
-@pytest.mark.parametrize("name", ["square_4096", "square_8192"])
 @pytest.mark.parametrize("dist", ["real", "int"])
-def test_named_problem_sampled_rows(name, dist):
-    """Full-size launch as timed by the benchmark; whole rows on every tile edge
-    plus random rows are recomputed by the oracle."""
-    p = PROBLEMS[name] if dist == "real" else PROBLEMS[name].int_variant()
+def test_named_problem_4096_every_element(dist):
+    """The benchmark's workload, in the launch the benchmark times: every
+    element against the oracle (real inputs within the bound, integer inputs
+    exactly)."""
+    p = PROBLEMS["square_4096"] if dist == "real" else PROBLEMS["square_4096"].int_variant()
+    A, B = problem_operands(p)
+    C = run(A, B)
+    C64, bound = oracle_named(p.name)
+    worst = check(C, C64, None if dist == "int" else bound, exact=(dist == "int"), what=p.name)
+    print(f"{p.name}: worst |err|/bound = {worst:.3e}")
+
+
+@pytest.mark.parametrize("dist", ["real", "int"])
+def test_named_problem_8192_sampled_rows(dist):
+    """8192^3 (the full oracle would take over half a minute on the host):
+    whole rows on every tile edge plus random rows, and single entries on the
+    tile-edge columns of those rows."""
+    p = PROBLEMS["square_8192"] if dist == "real" else PROBLEMS["square_8192"].int_variant()
     A, B = problem_operands(p)
     C = run(A, B)
     rows = sample_rows(p.M, n_random=8, seed=p.seed)
     C64, bound = oracle.gemm_rows_f64(A.numpy(), B.numpy(), rows)
     check(C[rows], C64, bound, exact=(dist == "int"), what=f"{p.name} rows")
-    # and single entries on the last columns of every sampled row's neighbours
     ii = np.repeat(rows, 4)
     jj = np.tile(np.array([0, 127, 128, p.N - 1]), rows.size)
     ce, be = oracle.gemm_entries_f64(A.numpy(), B.numpy(), ii, jj)
@@ -91,6 +103,10 @@ VARIANTS = (
     + [dict(producer=2, math=m, stages=s, split_k=1) for m in (1, 2) for s in (2, 4)]
     + [dict(producer=pr, math=m, stream_k=2) for pr in (1, 2) for m in (1, 2)]
     + [dict(stream_k=2, stages=s) for s in (2, 6)]
+    # tile order: row by row, and groups of 2 rows of tiles (the last group short)
+    + [dict(group_m=gm) for gm in (1, 2)]
+    + [dict(group_m=2, stream_k=2), dict(group_m=2, split_k=2), dict(group_m=2, producer=4),
+       dict(group_m=2, tile_n=256, split_k=1)]
     # producer warpgroup with the setmaxnreg register split
     + [dict(producer=3, math=m, stages=s, split_k=1, multicast=1) for m in (1, 2) for s in (1, 4, 6)]
     + [dict(producer=3, math=2, split_k=s, multicast=1) for s in (2, 4)]
@@ -171,6 +187,20 @@ def test_stream_k_sampled_rows_4096(dist):
     rows = sample_rows(p.M, n_random=8, seed=p.seed)
     C64, bound = oracle.gemm_rows_f64(A.numpy(), B.numpy(), rows)
     check(C[rows], C64, bound, exact=(dist == "int"), what=f"{p.name} stream-K rows")
+
+
+@pytest.mark.parametrize("group_m", [1, 5, 7, 16, 24, 100])
+def test_tile_order_every_element(group_m):
+    # 3000 x 2500: 24 x 20 tiles of 128 x 128, two whole data-parallel waves of
+    # 152 CTAs then stream-K units; groups of 5 and 7 rows leave a short last
+    # group, 24 and 100 make one group.  Every output tile must be computed
+    # once, whatever the order.
+    A, B = make_operands(3000, 2500, 256, "uniform", 41)
+    C64, bound = oracle.gemm_f64(A.numpy(), B.numpy())
+    check(run(A, B, group_m=group_m), C64, bound, exact=False, what=f"group_m={group_m}")
+    Ai, Bi = make_operands(3000, 2500, 256, "int", 42)
+    check(run(Ai, Bi, group_m=group_m), oracle.gemm_f64(Ai.numpy(), Bi.numpy(), with_bound=False)[0], None,
+          exact=True, what=f"group_m={group_m} int")
 
 
 def test_forced_tma_rejects_unaligned_rows():

@@ -9,7 +9,7 @@ import torch
 
 import dense_fp32_gemm_f32_gb300 as g
 import oracle
-from parity import check, sample_rows, to_device
+from parity import check, oracle_named, sample_rows, to_device
 from workloads import PROBLEMS, make_operands, problem_operands
 
 pytestmark = pytest.mark.gpu
@@ -76,10 +76,18 @@ def test_named_problem_integer_exact(name, variant):
 
 
 @pytest.mark.parametrize("variant", VARIANTS)
-@pytest.mark.parametrize("name", ["square_4096", "square_8192"])
 @pytest.mark.parametrize("dist", ["real", "int"])
-def test_named_problem_sampled_rows(name, dist, variant):
-    p = PROBLEMS[name] if dist == "real" else PROBLEMS[name].int_variant()
+def test_named_problem_4096_every_element(dist, variant):
+    p = PROBLEMS["square_4096"] if dist == "real" else PROBLEMS["square_4096"].int_variant()
+    A, B = problem_operands(p)
+    C64, bound = oracle_named(p.name)
+    check(run(A, B, variant=variant), C64, None if dist == "int" else bound, exact=(dist == "int"), what=p.name)
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("dist", ["real", "int"])
+def test_named_problem_8192_sampled_rows(dist, variant):
+    p = PROBLEMS["square_8192"] if dist == "real" else PROBLEMS["square_8192"].int_variant()
     A, B = problem_operands(p)
     C = run(A, B, variant=variant)
     rows = sample_rows(p.M, n_random=8, seed=p.seed)

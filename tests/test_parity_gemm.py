@@ -11,7 +11,7 @@ import torch
 
 import dense_fp32_gemm_f32_gb300 as g
 import oracle
-from parity import check, sample_rows, to_device
+from parity import check, to_device
 from workloads import make_operands
 
 pytestmark = pytest.mark.gpu
@@ -125,18 +125,29 @@ def test_general_split_k_shapes(ta, tb):
     check(C, ref, bound, exact=False, what=f"split-K t{ta}{tb}")
 
 
-@pytest.mark.parametrize("ta,tb", [(1, 0), (0, 1)])
-def test_general_4096_sampled_rows(ta, tb):
-    """4096^3 (stream-K schedule, finishing CTAs apply the epilogue): full
-    sampled rows against the oracle."""
+@pytest.mark.parametrize("ta,tb", [(0, 0), (1, 0), (0, 1), (1, 1)])
+def test_general_4096_every_element(ta, tb):
+    """4096^3 (stream-K schedule, finishing CTAs apply the epilogue) in every
+    storage order: every element against the oracle."""
     M = N = K = 4096
     a, b = (x.numpy() for x in make_operands(M, N, K, "normal", 211))
     cin = make_operands(M, 1, N, "normal", 212)[0].numpy()
     A, B = stored(a, b, ta, tb)
     C = run(A, B, cin, alpha=1.25, beta=0.75, ta=ta, tb=tb)
-    rows = sample_rows(M, n_random=6, seed=213)
-    ref, bound = oracle.gemm_general_f64(A, B, cin, alpha=1.25, beta=0.75, transa=ta, transb=tb, rows=rows)
-    check(C[rows], ref, bound, exact=False, what=f"4096 t{ta}{tb}")
+    ref, bound = oracle.gemm_general_f64(A, B, cin, alpha=1.25, beta=0.75, transa=ta, transb=tb)
+    check(C, ref, bound, exact=False, what=f"4096 t{ta}{tb}")
+
+
+@pytest.mark.parametrize("ta,tb", [(0, 1), (1, 1)])
+def test_general_4096_integer_exact(ta, tb):
+    """Transposed B at 4096^3 on integer inputs, alpha = 2, beta = -1: exact."""
+    M = N = K = 4096
+    a, b = (x.numpy() for x in make_operands(M, N, K, "int", 214))
+    cin = make_operands(M, 1, N, "int", 215)[0].numpy()
+    A, B = stored(a, b, ta, tb)
+    C = run(A, B, cin, alpha=2.0, beta=-1.0, ta=ta, tb=tb)
+    ref, _ = oracle.gemm_general_f64(A, B, cin, alpha=2.0, beta=-1.0, transa=ta, transb=tb, with_bound=False)
+    check(C, ref, None, exact=True, what=f"4096 int t{ta}{tb}")
 
 
 def test_general_rejects_bad_arguments():
