@@ -44,6 +44,7 @@ class Options(ctypes.Structure):
         ("tile_n", _i),
         ("repack", _i),
         ("a_layout", _i),
+        ("group_m", _i),
     ]
 
 

@@ -150,6 +150,8 @@ int run_ffma(int M, int N, int K, const float* A, int lda, const float* B, int l
     prm.num_k_tiles = pl.num_k_tiles;
     prm.vec_store = ((reinterpret_cast<uintptr_t>(C) & 15u) == 0 && ldc % 4 == 0) ? 1 : 0;
     prm.tiles_n = pl.tiles_n;
+    prm.tiles_m = pl.tiles_m;
+    prm.group_m = pl.group_m;
     prm.skip_stage = opt ? opt->debug_skip_stage : 0;
     prm.timeout_ns = (opt && opt->timeout_ns) ? opt->timeout_ns : kDefaultTimeoutNs;
     prm.status = st->status_word;
@@ -306,6 +308,8 @@ int run_ffma_noalloc(int M, int N, int K, const float* A, int lda, const float* 
     prm.vec_store = ((reinterpret_cast<uintptr_t>(C) & 15u) == 0 && ldc % 4 == 0) ? 1 : 0;
     prm.tile_base = 0;
     prm.tiles_n = pl.tiles_n;
+    prm.tiles_m = pl.tiles_m;
+    prm.group_m = pl.group_m;
     prm.timeout_ns = kDefaultTimeoutNs;
     prm.status = st->status_word;
     prm.sk = pl.sk;

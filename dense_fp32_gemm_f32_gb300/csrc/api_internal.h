@@ -91,6 +91,9 @@ inline long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
 // +23 %, 4095 x 4097 x 4099 and 8191 x 8193 x 8195 +30 %.
 constexpr double kRepackMinFlops = 1073741824.0;  // 2^30
 
+// Rows of tiles per group of the FFMA kernels' tile order (tile_rc).
+constexpr int kGroupRows = 16;
+
 // The library's stream-ordered pool on device `dev` (api_device.cu).
 cudaMemPool_t workspace_pool(int dev, DeviceState& st);
 
@@ -180,6 +183,8 @@ struct Plan {
     int stages = 4;
     int bn = kBN;     // output tile width (kBN or kBNWide)
     int tiles_n = 0;  // tiles per row of tiles
+    int tiles_m = 0;  // rows of tiles
+    int group_m = 1;  // tile order: rows of tiles per group (tile_rc)
     int num_k_tiles = 0;
     int nlaunch = 1;
     Launch launch[2];

@@ -53,7 +53,7 @@ int validate(int M, int N, int K, const float* A, int lda, const float* B, int l
 
 bool options_force_variant(const sgemm_options* opt) {
     return opt && (opt->producer || opt->split_k || opt->multicast || opt->math || opt->stages || opt->tail_split ||
-                   opt->stream_k || opt->tile_n || opt->repack);
+                   opt->stream_k || opt->tile_n || opt->repack || opt->group_m);
 }
 
 // 0 = keep A as stored, 1 = copy it transposed; -1 = invalid option.
@@ -244,7 +244,18 @@ int make_plan(const DeviceState& st, int M, int N, int K, const float* A, int ld
     if (split > 1 && pl.producer == kProducerFused) return SGEMM_ERR_INVALID_ARG;  // two CTAs per SM: no clusters
 
     pl.tiles_n = static_cast<int>(tiles_n);
+    pl.tiles_m = static_cast<int>(tiles_m);
     const long long grid_tiles = static_cast<long long>(pl.tiles_n) * tiles_m;
+
+    // Tile order (see tile_rc): groups of kGroupRows rows of tiles, walked
+    // column by column, so that a wave of 152 CTAs covers about 16 x 9.5
+    // tiles.  Row by row, a wave of the 4096^3 product needs ~5 A row panels
+    // and all 32 B column panels, and B is read from HBM once per wave (ncu:
+    // 531 MB read per launch against 134 MB of A and B).
+    const int want_group = opt ? opt->group_m : 0;
+    if (want_group < 0) return SGEMM_ERR_INVALID_ARG;
+    pl.group_m = want_group > 0 ? want_group : kGroupRows;
+    if (pl.group_m > pl.tiles_m) pl.group_m = pl.tiles_m > 0 ? pl.tiles_m : 1;
 
     // Last partial wave.  When the tiles do not fill a whole number of waves,
     // the last wave leaves SMs idle for a full tile time.  Those tiles can run
@@ -340,6 +351,7 @@ bool small_problem(const DeviceState& st, int M, int N, int K) {
 // stages, split or tile options, and no waits for debug_skip_stage to time out).
 bool small_forced_ok(const sgemm_options* opt) {
     return !(opt->split_k || opt->multicast || opt->math || opt->stages || opt->tail_split || opt->stream_k ||
+             opt->group_m ||
              opt->tile_n || opt->repack || opt->a_layout || opt->debug_skip_stage);
 }
 

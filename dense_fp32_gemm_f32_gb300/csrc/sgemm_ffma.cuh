@@ -154,6 +154,8 @@ struct FfmaParams {
     int vec_store;         // C base 16-byte aligned and ldc % 4 == 0
     int tile_base;         // linear index of this launch's first output tile
     int tiles_n;           // output tiles per row of tiles
+    int tiles_m;           // rows of output tiles
+    int group_m;           // tile order: groups of group_m rows of tiles (1 = row by row; see tile_rc)
     // Stream-K schedule (sk != 0), one CTA per SM: CTA g first takes whole
     // tiles g, g + G, ... below sk_dp_tiles (data-parallel waves, raster
     // order), then an even share of the units (one K slice of one tile each)
@@ -180,6 +182,28 @@ constexpr int ffma_smem_bytes() {
     constexpr int stage = ffma_stage_bytes<BN>() + (XA ? kStageABytes : 0);
     return (STAGES * stage > ffma_partial_bytes<BN>() ? STAGES * stage : ffma_partial_bytes<BN>()) + 1024 /*align*/ +
            256 /*barriers*/;
+}
+
+// Output tile number -> (row of tiles tm, column of tiles tn).  Tiles are
+// numbered in groups of `group_m` rows of tiles, column by column inside a
+// group (the last group may hold fewer rows), so that the tiles of one wave
+// of CTAs form a block of about group_m x (CTAs / group_m) tiles: each B
+// column panel a wave loads then serves group_m tiles instead of one, and
+// the group's A row panels serve its consecutive waves.  group_m = 1 is the
+// row-by-row order.
+__device__ __forceinline__ void tile_rc(int t, int tiles_n, int tiles_m, int group_m, int& tm, int& tn) {
+    if (group_m <= 1) {
+        tm = t / tiles_n;
+        tn = t - tm * tiles_n;
+        return;
+    }
+    const int per_group = group_m * tiles_n;
+    const int g = t / per_group;
+    const int r = t - g * per_group;
+    const int rows = min(group_m, tiles_m - g * group_m);
+    const int q = r / rows;
+    tm = g * group_m + (r - q * rows);
+    tn = q;
 }
 
 // Physical byte offset of float (row r, column c) inside a 128-byte-swizzled
@@ -247,9 +271,9 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), ffma_min_blocks<PROD
     const uint32_t crank = split > 1 ? cluster_ctarank() : 0u;
 
     // Work.  A CTA processes a sequence of segments (tile, kb, ke): the K
-    // slices [kb, ke) of one output tile.  Tiles are numbered row of tiles by
-    // row of tiles from tile_base, so neighbouring CTAs share rows of A (the
-    // A tiles reused from L2).  Without stream-K
+    // slices [kb, ke) of one output tile.  Tiles are numbered from tile_base
+    // in the grouped order of tile_rc, so that CTAs running at the same time
+    // share A row panels and B column panels in L2.  Without stream-K
     // there is one segment: the CTA's tile (gridDim.x over tiles) and, with
     // split-K, the K range of cluster rank blockIdx.z.  With stream-K: the
     // data-parallel tiles first, then the CTA's even share of the stream-K
@@ -371,8 +395,10 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), ffma_min_blocks<PROD
         Work work = work0;
         int tile, kb, ke;
         while (issuer && !timed_out && work.next(tile, kb, ke)) {
-            const int n0 = (tile % p.tiles_n) * BN;
-            const int m0 = (tile / p.tiles_n) * kBM;
+            int tm_, tn_;
+            tile_rc(tile, p.tiles_n, p.tiles_m, p.group_m, tm_, tn_);
+            const int n0 = tn_ * BN;
+            const int m0 = tm_ * kBM;
             for (int kt = kb; kt < ke; ++kt, ++it) {
                 const int s = it % STAGES;
                 const int round = it / STAGES;
@@ -492,8 +518,10 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), ffma_min_blocks<PROD
     // so that the epilogue's reads of the old C do not wait on HBM.
     const bool read_c = SCALED && p.beta != 0.f;
     auto prefetch_c = [&](int tile) {
-        const int row0 = (tile / p.tiles_n) * kBM;
-        const int col0 = (tile % p.tiles_n) * BN + wn * (BN / WN) + tn * 4;
+        int tm_, tn_;
+        tile_rc(tile, p.tiles_n, p.tiles_m, p.group_m, tm_, tn_);
+        const int row0 = tm_ * kBM;
+        const int col0 = tn_ * BN + wn * (BN / WN) + tn * 4;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const int r = row0 + row_in_tile(i);
@@ -504,8 +532,10 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), ffma_min_blocks<PROD
         }
     };
     auto store_c_plain = [&](int tile) {
-        const int row0 = (tile / p.tiles_n) * kBM;
-        const int col0 = (tile % p.tiles_n) * BN + wn * (BN / WN) + tn * 4;
+        int tm_, tn_;
+        tile_rc(tile, p.tiles_n, p.tiles_m, p.group_m, tm_, tn_);
+        const int row0 = tm_ * kBM;
+        const int col0 = tn_ * BN + wn * (BN / WN) + tn * 4;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const int r = row0 + row_in_tile(i);
@@ -528,8 +558,10 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), ffma_min_blocks<PROD
         }
     };
     auto store_c_scaled = [&](int tile) {
-        const int row0 = (tile / p.tiles_n) * kBM;
-        const int col0 = (tile % p.tiles_n) * BN + wn * (BN / WN) + tn * 4;
+        int tm_, tn_;
+        tile_rc(tile, p.tiles_n, p.tiles_m, p.group_m, tm_, tn_);
+        const int row0 = tm_ * kBM;
+        const int col0 = tn_ * BN + wn * (BN / WN) + tn * 4;
         // Rows in groups of RG: with beta != 0 the group's old C values are
         // all loaded before any of its stores, so the loads are in flight
         // together (a load after a store to C could not be moved above it).
@@ -641,8 +673,10 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), ffma_min_blocks<PROD
             if (!(skip_here && loads == p.skip_stage - 1)) {
                 const int k0 = lkt * kBK;
                 mbar_arrive_expect_tx(full_bar(s), kStageBytes);
-                tma_load_2d(sA0 + s * kStageABytes, &tmA, full_bar(s), k0, (ltile / p.tiles_n) * kBM);
-                tma_load_2d(sB0 + s * kStageBBytes, &tmB, full_bar(s), (ltile % p.tiles_n) * BN, k0);
+                int tm_, tn_;
+                tile_rc(ltile, p.tiles_n, p.tiles_m, p.group_m, tm_, tn_);
+                tma_load_2d(sA0 + s * kStageABytes, &tmA, full_bar(s), k0, tm_ * kBM);
+                tma_load_2d(sB0 + s * kStageBBytes, &tmB, full_bar(s), tn_ * BN, k0);
             }
             ++loads;
             if (++lkt >= lke) {

@@ -20,18 +20,41 @@
  * inputs whose every partial sum is an integer below 2^24 in magnitude (for
  * example entries in {-8..8} with K <= 2^18) give the exact result.
  *
- * Memory.  A, B and C are DEVICE pointers owned by the caller.  C must not
- * overlap A or B.  Rows may be padded (ld > row width); padding is never
- * written and never read.  The only device memory the library takes is the
- * stream-K workspace (see sgemm_options.stream_k), from its own stream-
- * ordered pool.
+ * Memory.  A, B and C are DEVICE pointers owned by the caller (host
+ * pointers for sgemm_f32_host).  C must not overlap A or B.  Rows may be
+ * padded (ld > row width); padding is never written and never read.
+ *
+ * Device memory the library takes itself.  The pages' host code allocates
+ * every buffer in the caller; this library also takes scratch of its own,
+ * where measurement showed that it pays:
+ *  - the stream-K scratch (partial tiles and ready flags, 152 x 128 KiB +
+ *    flags on a 152-SM GB300), cudaMalloc'ed on a stream's first stream-K
+ *    call and kept for that stream (up to 16 streams) until the process
+ *    exits; a call recorded into a CUDA graph takes its stream-K workspace
+ *    from the pool below instead;
+ *  - from a stream-ordered pool the library creates on each device (cached
+ *    up to 256 MiB between calls), freed in stream order at the end of each
+ *    call: 16-byte pitched copies of misaligned operands (2MNK >= 2^30),
+ *    A's transposed copy (sgemm_options.a_layout = 2), transposed copies of
+ *    op(B) = B^T and of an op(A) = A^T the tensor maps cannot read
+ *    (sgemm_f32_gemm), B's TF32 parts and the K-split partial tiles and
+ *    counters (sgemm_3xtf32), and the device copies of A, B and C
+ *    (sgemm_f32_host, which also keeps two copy streams and their events per
+ *    device).
+ * Entry points that may allocate device memory (machine-read by the tests):
+ *   ALLOCATING: sgemm_f32 sgemm_f32_ex sgemm_f32_gemm sgemm_3xtf32 sgemm_3xtf32_ex sgemm_f32_host
+ *   NON-ALLOCATING: sgemm_f32_noalloc sgemm_check_status sgemm_status_string sgemm_describe
+ * The library's first call on a device (any entry point except
+ * sgemm_status_string) also does the one-time device set-up: kernel
+ * attributes, occupancy figures, the pool's creation (cudaMemPoolCreate,
+ * which reserves no memory by itself) and the tensor-map encoder lookup.
+ * Make that first call outside any stream capture.
  *
  * Streams.  `stream` is a cudaStream_t passed as void* (NULL selects the legacy
  * default stream).  Every call enqueues work on that stream and returns without
- * synchronising; the caller synchronises.  The library keeps only per-device,
- * once-initialised state (kernel attributes and the driver's tensor-map encoder
- * entry point), set up under a lock, so concurrent calls from several host
- * threads are safe.
+ * synchronising; the caller synchronises.  Per-device state (the set-up above,
+ * the per-stream scratch table, the pool) is created once under locks, so
+ * concurrent calls from several host threads are safe.
  *
  * Errors.  Each call returns an sgemm_status.  Argument errors are detected on
  * the host before anything is enqueued.  A kernel that gives up on a bounded
@@ -88,14 +111,13 @@ typedef enum sgemm_status {
  *   C, ldc       device pointer to C, row stride in floats (ldc >= N)
  *   stream       cudaStream_t as void*
  * A call enqueues the product kernel, preceded, when repacking, by one copy
- * kernel (a pool buffer the library keeps per device).  The stream-K partial
- * tiles and ready flags live in a workspace the library keeps per stream
- * (allocated on the stream's first such call, 152 x 128 KiB, for up to 16
- * streams; its flags carry each call's sequence number, so no memset is
- * needed); a call recorded into a CUDA graph takes a pool workspace whose
- * flags a memset node zeroes instead.  The first stream-K call on a stream
- * allocates (cudaMalloc): make it before any stream capture in the global
- * mode, which such an allocation would invalidate.
+ * kernel (into a buffer from the library's pool).  The stream-K partial tiles
+ * and ready flags live in the scratch the library keeps per stream (its
+ * flags carry each call's sequence number, so no memset is needed); a call
+ * recorded into a CUDA graph takes a pool workspace whose flags a memset
+ * node zeroes instead.  The first stream-K call on a stream allocates
+ * (cudaMalloc): make it before any stream capture in the global mode, which
+ * such an allocation would invalidate.
  */
 int sgemm_f32(int M, int N, int K,
               const float* A, int lda,
@@ -137,8 +159,12 @@ int sgemm_f32(int M, int N, int K,
  *    different host threads) race on it and give wrong results.  Order them
  *    on one stream or synchronise between them.
  *  - The first call on each device looks up the array's device address (the
- *    name in host code is only a stand-in) with that device current; make
- *    that first call before any stream capture.
+ *    name in host code is only a stand-in) with that device current.  When
+ *    it is also the process's first call of this library on the device, it
+ *    does the library's one-time device set-up as well (see "Device memory
+ *    the library takes itself" above: kernel attributes, the pool's
+ *    creation, the tensor-map encoder).  Make that first call before any
+ *    stream capture; later calls allocate nothing and create nothing.
  */
 int sgemm_f32_noalloc(int M, int N, int K,
                       const float* A, int lda,
@@ -275,10 +301,11 @@ typedef struct sgemm_options {
                              units; a tile shared by several CTAs is finished
                              by the CTA holding its first K slice from the
                              others' partial tiles.  Needs a workspace of
-                             CTAs x (64 KiB + 4 bytes), taken per call from a
-                             stream-ordered pool the library creates on the
-                             device (cudaMallocFromPoolAsync / cudaFreeAsync
-                             on `stream`), which keeps it for reuse. */
+                             CTAs x (partial tile + 4 bytes): the scratch
+                             the library keeps per stream (cudaMalloc'ed on
+                             the stream's first such call), or, in a stream
+                             capture, a pool workspace (see "Device memory
+                             the library takes itself"). */
     int tile_n;           /* 0 = auto; 64 = 128 x 64 tiles of the fused
                              producer (SGEMM_PRODUCER_FUSED); 128 = 128 x 128
                              output tiles (8 x 8 per thread); 256 = 128 x 256
@@ -301,6 +328,12 @@ typedef struct sgemm_options {
                              workspace of K x M4 floats) and run the
                              transposed-A kernel, whose consumers read each
                              k's A values as two 16-byte vectors */
+    int group_m;          /* 0 = auto (16); n >= 1: the output tiles are
+                             taken in groups of n rows of tiles, column by
+                             column inside a group, so that the CTAs running
+                             at one time share B column panels (n of them per
+                             panel) and A row panels in L2; 1 = row by row.
+                             Larger than the rows of tiles: one group. */
 } sgemm_options;
 
 /* sgemm_f32 with forced choices.  Same contract; an unsupported combination

@@ -158,3 +158,61 @@ def test_no_cluster_multicast_load_in_library_or_bench():
                 if "multicast::cluster" in open(os.path.join(d, f)).read():
                     offenders.append(f)
     assert offenders == []
+
+
+def _header_list(tag):
+    text = open(os.path.join(ROOT, "include", "sgemm.h")).read()
+    m = re.search(r"^\s*\*\s*" + re.escape(tag) + r":\s*([\w ]+)$", text, flags=re.M)
+    assert m, f"sgemm.h has no '{tag}:' line"
+    return m.group(1).split()
+
+
+def test_header_states_which_entry_points_allocate():
+    # Every entry point of sgemm.h is listed exactly once as allocating device
+    # memory or not.
+    alloc, none = _header_list("ALLOCATING"), _header_list("NON-ALLOCATING")
+    text = open(os.path.join(ROOT, "include", "sgemm.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    declared = set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(sgemm_\w+)\s*\(", text, flags=re.M))
+    assert sorted(alloc + none) == sorted(declared)
+    assert not set(alloc) & set(none)
+
+
+def _function_body(src, name):
+    """Code of the function `name` (comments removed)."""
+    src = re.sub(r"//[^\n]*", "", re.sub(r"/\*.*?\*/", "", src, flags=re.S))
+    i = src.index(name + "(")
+    i = src.index("{", i)
+    depth, j = 0, i
+    while True:
+        depth += {"{": 1, "}": -1}.get(src[j], 0)
+        j += 1
+        if depth == 0:
+            return src[i:j]
+
+
+def test_non_allocating_entries_reach_no_allocation_in_source():
+    # The host code behind the entries listed as non-allocating names no
+    # allocating call, pool, per-stream scratch or repack buffer.
+    csrc = os.path.join(ROOT, "dense_fp32_gemm_f32_gb300", "csrc")
+    banned = ("cudaMalloc", "cudaFree", "MallocFromPool", "workspace_pool", "sk_lease", "Repacked", "malloc(",
+              "cudaStreamCreate", "cudaEventCreate", "at::", "torch")
+    bodies = {
+        "run_ffma_noalloc": _function_body(open(os.path.join(csrc, "api_ffma.cu")).read(), "int run_ffma_noalloc"),
+        "sgemm_check_status": _function_body(open(os.path.join(csrc, "sgemm_api.cu")).read(),
+                                             "int sgemm_check_status"),
+        "sgemm_status_string": _function_body(open(os.path.join(csrc, "sgemm_api.cu")).read(),
+                                              "const char* sgemm_status_string"),
+        "sgemm_describe": _function_body(open(os.path.join(csrc, "sgemm_api.cu")).read(),
+                                         "const char* sgemm_describe"),
+    }
+    for name, body in bodies.items():
+        for b in banned:
+            assert b not in body, f"{name} names {b}"
+    # the small-problem launch and the plan it shares with sgemm_f32 allocate nothing either
+    plan = _function_body("int f(){" + open(os.path.join(csrc, "api_plan.cu")).read() + "}", "int f")
+    for b in banned:
+        assert b not in plan, f"api_plan.cu names {b}"
+    launch_small = _function_body(open(os.path.join(csrc, "api_ffma.cu")).read(), "int launch_small")
+    for b in banned:
+        assert b not in launch_small, f"launch_small names {b}"

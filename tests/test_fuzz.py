@@ -17,7 +17,7 @@ OPTIONS = [
     {}, dict(producer=1), dict(producer=2), dict(producer=3), dict(producer=5), dict(producer=4),
     dict(stream_k=2), dict(stream_k=1), dict(split_k=2), dict(split_k=3), dict(tile_n=256), dict(tile_n=64),
     dict(a_layout=2), dict(a_layout=1), dict(repack=2), dict(math=1), dict(stages=3),
-    dict(producer=5, stream_k=2), dict(a_layout=2, stream_k=2), dict(tile_n=256, stream_k=2), dict(producer=6),
+    dict(group_m=1), dict(group_m=3), dict(producer=5, stream_k=2), dict(a_layout=2, stream_k=2), dict(tile_n=256, stream_k=2), dict(producer=6),
 ]
 
 
