@@ -45,6 +45,7 @@ class Options(ctypes.Structure):
         ("repack", _i),
         ("a_layout", _i),
         ("group_m", _i),
+        ("l2_hint", _i),
     ]
 
 

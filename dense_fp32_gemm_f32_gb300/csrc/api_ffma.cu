@@ -49,8 +49,8 @@ int launch_small(int M, int N, int K, const float* A, int lda, const float* B, i
 }
 
 int run_ffma(int M, int N, int K, const float* A, int lda, const float* B, int ldb, float* C, int ldc,
-             void* stream, const sgemm_options* opt, const Scale* scale, bool a_mn) {
-    int rc = validate(M, N, K, A, lda, B, ldb, C, ldc, a_mn);
+             void* stream, const sgemm_options* opt, const Scale* scale, bool a_mn, bool b_nk) {
+    int rc = validate(M, N, K, A, lda, B, ldb, C, ldc, a_mn, b_nk);
     if (rc != SGEMM_OK) return rc;
     if (opt && opt->debug_skip_stage < 0) return SGEMM_ERR_INVALID_ARG;
     if (M == 0 || N == 0) return SGEMM_OK;  // nothing to write; no device work
@@ -61,16 +61,16 @@ int run_ffma(int M, int N, int K, const float* A, int lda, const float* B, int l
 
     const cudaStream_t cs = static_cast<cudaStream_t>(stream);
     if (opt && opt->producer == SGEMM_PRODUCER_SMALL) {
-        if (!small_forced_ok(opt)) return SGEMM_ERR_INVALID_ARG;
+        if (!small_forced_ok(opt) || b_nk) return SGEMM_ERR_INVALID_ARG;
         if (ceil_div(M, kSmallTile) > 65535) return SGEMM_ERR_INVALID_ARG;
         return launch_small(M, N, K, A, lda, B, ldb, C, ldc, stream, scale, a_mn);
     }
-    if (!options_force_variant(opt) && !(opt && (opt->a_layout || opt->debug_skip_stage)) &&
+    if (!b_nk && !options_force_variant(opt) && !(opt && (opt->a_layout || opt->debug_skip_stage)) &&
         small_problem(*st, M, N, K))
         return launch_small(M, N, K, A, lda, B, ldb, C, ldc, stream, scale, a_mn);
     // A copied transposed for the transposed-A kernels (see choose_a_layout).
     Repacked a_t;
-    const int layout = a_mn ? 0 : choose_a_layout(K, opt);
+    const int layout = (a_mn || b_nk) ? 0 : choose_a_layout(K, opt);
     if (layout < 0) return SGEMM_ERR_INVALID_ARG;
     if (layout == 1) {
         rc = a_t.make_transposed_a(dev, *st, M, K, A, lda, cs);
@@ -83,7 +83,7 @@ int run_ffma(int M, int N, int K, const float* A, int lda, const float* B, int l
     // (With a transposed A, make_plan rejects forced producer, tile, math,
     // and stage choices: the transposed-A kernels have one form.)
     Plan pl;
-    rc = make_plan(*st, M, N, K, A, lda, B, ldb, opt, &pl, a_mn);
+    rc = make_plan(*st, M, N, K, A, lda, B, ldb, opt, &pl, a_mn, b_nk);
     if (rc != SGEMM_OK) {
         a_t.release();
         return rc;
@@ -98,7 +98,7 @@ int run_ffma(int M, int N, int K, const float* A, int lda, const float* B, int l
         if (rc == SGEMM_ERR_CUDA && !(opt && opt->repack == 2)) {
             sgemm_options o = opt ? *opt : sgemm_options{};
             o.repack = 1;
-            rc = make_plan(*st, M, N, K, A, lda, B, ldb, &o, &pl, a_mn);
+            rc = make_plan(*st, M, N, K, A, lda, B, ldb, &o, &pl, a_mn, b_nk);
         }
         if (rc != SGEMM_OK) {
             a_t.release();
@@ -112,7 +112,8 @@ int run_ffma(int M, int N, int K, const float* A, int lda, const float* B, int l
     };
 
     const bool scaled = scale && (scale->alpha != 1.f || scale->beta != 0.f);
-    const KernelEntry k = pl.a_mn ? (pl.bn == kBN ? ffma_kernel_amn(pl.stages, pl.math, scaled)
+    const KernelEntry k = pl.b_nk ? ffma_kernel_bnk(pl.a_mn, scaled)
+                          : pl.a_mn ? (pl.bn == kBN ? ffma_kernel_amn(pl.stages, pl.math, scaled)
                                                   : scaled ? KernelEntry{nullptr, 0, 0} : ffma_kernel(pl))
                           : scaled ? (pl.producer == kProducerTmaX ? ffma_kernel_tma_x(pl.stages, pl.math, true)
                                       : pl.bn == kBN               ? ffma_kernel_scaled(pl.producer, pl.stages, pl.math)
@@ -130,7 +131,9 @@ int run_ffma(int M, int N, int K, const float* A, int lda, const float* B, int l
     if (is_tma(pl.producer)) {
         rc = pl.a_mn ? encode_2d(&tmA, A, M, K, lda, kBM, kBK, CU_TENSOR_MAP_SWIZZLE_NONE)  // {m, k} boxes of 128 x 32
                      : encode_2d(&tmA, A, K, M, lda, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B);
-        if (rc == SGEMM_OK) rc = encode_2d(&tmB, B, N, K, ldb, pl.bn, kBK, CU_TENSOR_MAP_SWIZZLE_NONE);
+        if (rc == SGEMM_OK)
+            rc = pl.b_nk ? encode_2d(&tmB, B, K, N, ldb, kBK, kBN, CU_TENSOR_MAP_SWIZZLE_128B)  // {k, n} boxes of 32 x 128
+                         : encode_2d(&tmB, B, N, K, ldb, pl.bn, kBK, CU_TENSOR_MAP_SWIZZLE_NONE);
         if (rc != SGEMM_OK) {
             release_pack();
             return rc;
@@ -152,6 +155,7 @@ int run_ffma(int M, int N, int K, const float* A, int lda, const float* B, int l
     prm.tiles_n = pl.tiles_n;
     prm.tiles_m = pl.tiles_m;
     prm.group_m = pl.group_m;
+    prm.a_evict_last = pl.a_evict_last;
     prm.skip_stage = opt ? opt->debug_skip_stage : 0;
     prm.timeout_ns = (opt && opt->timeout_ns) ? opt->timeout_ns : kDefaultTimeoutNs;
     prm.status = st->status_word;
@@ -310,6 +314,7 @@ int run_ffma_noalloc(int M, int N, int K, const float* A, int lda, const float* 
     prm.tiles_n = pl.tiles_n;
     prm.tiles_m = pl.tiles_m;
     prm.group_m = pl.group_m;
+    prm.a_evict_last = pl.a_evict_last;
     prm.timeout_ns = kDefaultTimeoutNs;
     prm.status = st->status_word;
     prm.sk = pl.sk;
@@ -388,19 +393,23 @@ int run_gemm(int transa, int transb, int M, int N, int K, float alpha, const flo
     sc.alpha = alpha;
     sc.beta = beta;
     if (!transa && !transb) return run_ffma(M, N, K, A, lda, B, ldb, C, ldc, stream, nullptr, &sc);
-    // Transposed A that the tensor maps can read stays where it is: the
-    // transposed-A kernels load it in its own storage order.  Otherwise, and
-    // for a transposed B, one transposing copy into pitched rows per operand
-    // (HBM traffic of one read and one write of it), then the product on the
+    // A transposed operand that the tensor maps can read stays where it is:
+    // the transposed-A kernels load A in its own storage order, and a B
+    // stored N x K is loaded in slices of 128 n x 32 k that a producer warp
+    // transposes in shared memory (products too small for the 128 x 128
+    // kernels, which go to the small-problem kernel, take the copy below).
+    // Otherwise one transposing copy into pitched rows per operand (HBM
+    // traffic of one read and one write of it), then the product on the
     // copies.
     const bool a_native = transa && tma_ok(A, lda);
-    const int copies = (transa && !a_native ? 1 : 0) | (transb ? 2 : 0);
+    const bool b_native = transb && tma_ok(B, ldb) && !small_problem(*st, M, N, K);
+    const int copies = (transa && !a_native ? 1 : 0) | (transb && !b_native ? 2 : 0);
     Repacked packed;
     if (copies) {
         rc = packed.make(dev, *st, copies, M, N, K, A, lda, B, ldb, cs, transa != 0, transb != 0);
         if (rc != SGEMM_OK) return rc;
     }
-    rc = run_ffma(M, N, K, A, lda, B, ldb, C, ldc, stream, nullptr, &sc, a_native);
+    rc = run_ffma(M, N, K, A, lda, B, ldb, C, ldc, stream, nullptr, &sc, a_native, b_native);
     packed.release();
     return rc;
 }

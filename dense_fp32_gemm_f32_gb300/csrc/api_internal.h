@@ -94,6 +94,10 @@ constexpr double kRepackMinFlops = 1073741824.0;  // 2^30
 // Rows of tiles per group of the FFMA kernels' tile order (tile_rc).
 constexpr int kGroupRows = 16;
 
+// Shortest K for which the tensor-core entry splits the tiles of a last
+// partial wave of 128 x 256 tiles along K (variants 3 and 4).
+constexpr int kTcTailSplitMinK = 1024;
+
 // The library's stream-ordered pool on device `dev` (api_device.cu).
 cudaMemPool_t workspace_pool(int dev, DeviceState& st);
 
@@ -185,6 +189,7 @@ struct Plan {
     int tiles_n = 0;  // tiles per row of tiles
     int tiles_m = 0;  // rows of tiles
     int group_m = 1;  // tile order: rows of tiles per group (tile_rc)
+    int a_evict_last = 0;  // A's slices loaded with the L2 evict-last policy
     int num_k_tiles = 0;
     int nlaunch = 1;
     Launch launch[2];
@@ -192,6 +197,7 @@ struct Plan {
     int sk_dp_tiles = 0;  // tiles taken whole (data-parallel waves) before the stream-K region
     int repack = 0;       // operands copied to 16-byte pitched rows first: bit 0 = A, bit 1 = B
     bool a_mn = false;    // A stored transposed (K x M): the transposed-A kernels
+    bool b_nk = false;    // B stored transposed (N x K): the kernels with a B-transposing warp
 };
 
 // Epilogue scaling of the general entry: C = alpha * A B + beta * C.
@@ -208,14 +214,14 @@ void sk_return(DeviceState& st, cudaStream_t cs, SkLease& lease);
 bool ranges_overlap(const void* a, size_t abytes, const void* b, size_t bbytes);
 size_t span_bytes(long long rows, long long cols, long long ld);
 int validate(int M, int N, int K, const float* A, int lda, const float* B, int ldb, const float* C, int ldc,
-             bool a_mn = false);
+             bool a_mn = false, bool b_nk = false);
 bool options_force_variant(const sgemm_options* opt);
 int choose_a_layout(int K, const sgemm_options* opt);
 bool is_tma(int producer);
 KernelEntry ffma_kernel(const Plan& pl);
 bool tma_ok(const float* p, int ld);
 int make_plan(const DeviceState& st, int M, int N, int K, const float* A, int lda, const float* B, int ldb,
-              const sgemm_options* opt, Plan* out, bool a_mn = false);
+              const sgemm_options* opt, Plan* out, bool a_mn = false, bool b_nk = false);
 int encode_2d(CUtensorMap* map, const float* base, long long inner, long long outer, long long ld, int box_inner,
               int box_outer, CUtensorMapSwizzle swz);
 const char* describe_plan(const Plan& pl);
@@ -224,7 +230,7 @@ bool small_forced_ok(const sgemm_options* opt);
 
 // ---- api_ffma.cu, api_tf32.cu, api_host.cu: the entries' work
 int run_ffma(int M, int N, int K, const float* A, int lda, const float* B, int ldb, float* C, int ldc, void* stream,
-             const sgemm_options* opt, const Scale* scale = nullptr, bool a_mn = false);
+             const sgemm_options* opt, const Scale* scale = nullptr, bool a_mn = false, bool b_nk = false);
 int run_ffma_noalloc(int M, int N, int K, const float* A, int lda, const float* B, int ldb, float* C, int ldc,
                      void* stream);
 int run_gemm(int transa, int transb, int M, int N, int K, float alpha, const float* A, int lda, const float* B,

@@ -16,11 +16,12 @@ size_t span_bytes(long long rows, long long cols, long long ld) {
     return static_cast<size_t>(((rows - 1) * ld + cols) * 4);
 }
 
-// a_mn: A is stored transposed (K x M, lda >= M).
+// a_mn: A is stored transposed (K x M, lda >= M); b_nk: B is stored
+// transposed (N x K, ldb >= K).
 int validate(int M, int N, int K, const float* A, int lda, const float* B, int ldb, const float* C, int ldc,
-             bool a_mn) {
+             bool a_mn, bool b_nk) {
     if (M < 0 || N < 0 || K < 0) return SGEMM_ERR_INVALID_ARG;
-    if (lda < (a_mn ? M : K) || ldb < N || ldc < N) return SGEMM_ERR_INVALID_ARG;
+    if (lda < (a_mn ? M : K) || ldb < (b_nk ? K : N) || ldc < N) return SGEMM_ERR_INVALID_ARG;
     if (M > 0 && K > 0 && !A) return SGEMM_ERR_INVALID_ARG;
     if (K > 0 && N > 0 && !B) return SGEMM_ERR_INVALID_ARG;
     if (M > 0 && N > 0 && !C) return SGEMM_ERR_INVALID_ARG;
@@ -30,7 +31,7 @@ int validate(int M, int N, int K, const float* A, int lda, const float* B, int l
         return SGEMM_ERR_INVALID_ARG;
     const size_t cb = span_bytes(M, N, ldc);
     if (ranges_overlap(C, cb, A, a_mn ? span_bytes(K, M, lda) : span_bytes(M, K, lda)) ||
-        ranges_overlap(C, cb, B, span_bytes(K, N, ldb)))
+        ranges_overlap(C, cb, B, b_nk ? span_bytes(N, K, ldb) : span_bytes(K, N, ldb)))
         return SGEMM_ERR_INVALID_ARG;
     return SGEMM_OK;
 }
@@ -53,7 +54,7 @@ int validate(int M, int N, int K, const float* A, int lda, const float* B, int l
 
 bool options_force_variant(const sgemm_options* opt) {
     return opt && (opt->producer || opt->split_k || opt->multicast || opt->math || opt->stages || opt->tail_split ||
-                   opt->stream_k || opt->tile_n || opt->repack || opt->group_m);
+                   opt->stream_k || opt->tile_n || opt->repack || opt->group_m || opt->l2_hint);
 }
 
 // 0 = keep A as stored, 1 = copy it transposed; -1 = invalid option.
@@ -103,8 +104,13 @@ bool tma_ok(const float* p, int ld) {
 
 // Chooses the variant.  Any field of `opt` that is non-zero forces that choice.
 int make_plan(const DeviceState& st, int M, int N, int K, const float* A, int lda, const float* B, int ldb,
-              const sgemm_options* opt, Plan* out, bool a_mn) {
+              const sgemm_options* opt, Plan* out, bool a_mn, bool b_nk) {
     Plan pl;
+    // B stored N x K (general entry only): tensor-map readable B, 128 x 128
+    // tiles, 2 stages, paired FMA, and a transposing warp for B.
+    if (b_nk && (K == 0 || !tma_ok(B, ldb) || (opt && options_force_variant(opt))))
+        return SGEMM_ERR_INVALID_ARG;
+    pl.b_nk = b_nk;
     // Cluster multicast of the operand slices is not built (see the
     // multicast field of sgemm_options).
     if (opt && (opt->multicast < 0 || opt->multicast > 2)) return SGEMM_ERR_INVALID_ARG;
@@ -127,7 +133,7 @@ int make_plan(const DeviceState& st, int M, int N, int K, const float* A, int ld
     if (want_repack < 0 || want_repack > 2) return SGEMM_ERR_INVALID_ARG;
     const int misaligned = (a_mn || tma_ok(A, lda) ? 0 : 1) | (tma_ok(B, ldb) ? 0 : 2);
     if (K > 0 && misaligned &&
-        (want_repack == 2 || a_mn ||  // (the transposed-A kernels have no cp.async form)
+        (want_repack == 2 || a_mn || b_nk ||  // (the transposed-operand kernels have no cp.async form)
          (want_repack == 0 && want_prod == SGEMM_PRODUCER_AUTO &&
           2.0 * static_cast<double>(M) * static_cast<double>(N) * static_cast<double>(K) >= kRepackMinFlops)))
         pl.repack = misaligned;
@@ -152,6 +158,7 @@ int make_plan(const DeviceState& st, int M, int N, int K, const float* A, int ld
         // HBM (a_mn) or another choice rules the transposing warps out.
         const bool x_ok = !a_mn && !(opt && ((opt->tile_n && opt->tile_n != kBN) ||
                                              (opt->stages && (opt->stages < 2 || opt->stages > 4))));
+        // (b_nk: B is aligned, checked above; A is aligned or repacked.)
         pl.producer = !aligned ? kProducerCpAsync : x_ok ? kProducerTmaX : kProducerTma;
     } else {
         return SGEMM_ERR_INVALID_ARG;
@@ -256,6 +263,9 @@ int make_plan(const DeviceState& st, int M, int N, int K, const float* A, int ld
     if (want_group < 0) return SGEMM_ERR_INVALID_ARG;
     pl.group_m = want_group > 0 ? want_group : kGroupRows;
     if (pl.group_m > pl.tiles_m) pl.group_m = pl.tiles_m > 0 ? pl.tiles_m : 1;
+    const int want_hint = opt ? opt->l2_hint : 0;
+    if (want_hint < 0 || want_hint > 2) return SGEMM_ERR_INVALID_ARG;
+    pl.a_evict_last = want_hint == 2 ? 1 : 0;
 
     // Last partial wave.  When the tiles do not fill a whole number of waves,
     // the last wave leaves SMs idle for a full tile time.  Those tiles can run
@@ -332,7 +342,9 @@ const char* describe_plan(const Plan& pl) {
     if (pl.repack && n > 0 && n < static_cast<int>(sizeof buf))
         n += std::snprintf(buf + n, sizeof buf - n, "/repack%s", pl.repack == 1 ? "A" : pl.repack == 2 ? "B" : "AB");
     if (pl.a_mn && n > 0 && n < static_cast<int>(sizeof buf))
-        std::snprintf(buf + n, sizeof buf - n, "/at");
+        n += std::snprintf(buf + n, sizeof buf - n, "/at");
+    if (pl.b_nk && n > 0 && n < static_cast<int>(sizeof buf))
+        std::snprintf(buf + n, sizeof buf - n, "/bt");
     return buf;
 }
 
@@ -351,7 +363,7 @@ bool small_problem(const DeviceState& st, int M, int N, int K) {
 // stages, split or tile options, and no waits for debug_skip_stage to time out).
 bool small_forced_ok(const sgemm_options* opt) {
     return !(opt->split_k || opt->multicast || opt->math || opt->stages || opt->tail_split || opt->stream_k ||
-             opt->group_m ||
+             opt->group_m || opt->l2_hint ||
              opt->tile_n || opt->repack || opt->a_layout || opt->debug_skip_stage);
 }
 

@@ -10,7 +10,8 @@ int run_3xtf32(int M, int N, int K, const float* A, int lda, const float* B, int
     int rc = validate(M, N, K, A, lda, B, ldb, C, ldc);
     if (rc != SGEMM_OK) return rc;
     if (opt && opt->debug_skip_stage < 0) return SGEMM_ERR_INVALID_ARG;
-    // Forced K split: 1 = none, 2..4 = CTAs per tile (variant 1 only).
+    // Forced K split: 1 = none, 2..4 = CTAs per tile (variant 1); for
+    // variants 3 and 4, 2 = split the last partial wave's tiles whatever K.
     const int force_s = opt ? opt->split_k : 0;
     if (force_s < 0 || force_s > 4) return SGEMM_ERR_INVALID_ARG;
     if (M == 0 || N == 0) return SGEMM_OK;
@@ -38,7 +39,8 @@ int run_3xtf32(int M, int N, int K, const float* A, int lda, const float* B, int
     int variant = (opt && opt->math) ? opt->math : 0;
     if (variant == 0)
         variant = 2 * ceil_div(M, kTcBM) * ceil_div(N, 256) < st->sm_count ? 1 : M >= 1024 ? 4 : 3;
-    if (variant < 1 || variant > 4 || (force_s >= 2 && variant != 1)) return SGEMM_ERR_INVALID_ARG;
+    if (variant < 1 || variant > 4 || (force_s >= 2 && variant == 2) || (force_s >= 3 && variant >= 3))
+        return SGEMM_ERR_INVALID_ARG;
     if (force_s >= 2 && force_s > ceil_div(K, kTcBK)) return SGEMM_ERR_INVALID_ARG;  // a slice per part at least
     const cudaStream_t cs = static_cast<cudaStream_t>(stream);
     const int misaligned = (tma_ok(A, lda) ? 0 : 1) | (tma_ok(B, ldb) ? 0 : 2);
@@ -79,7 +81,8 @@ int run_3xtf32(int M, int N, int K, const float* A, int lda, const float* B, int
         const bool pb = variant == 4;
         const long long wide = tiles_m * ceil_div(N, 256);
         const long long full = (wide / st->sm_count) * st->sm_count;
-        if (full > 0 && full < wide && K >= 1024 && force_s != 1) {
+        const bool want_split = force_s == 2 || (force_s == 0 && K >= kTcTailSplitMinK);
+        if (full > 0 && full < wide && want_split && ceil_div(K, 16) >= 2) {
             split_l = 1, split_s = 2, split_bn = 256, split_tiles = wide - full;
             launches[0] = {wk, 256, 16, full, 0, 0, pb};
             launches[1] = {wk, 256, 16, split_s * split_tiles, static_cast<int>(full), split_s, pb};

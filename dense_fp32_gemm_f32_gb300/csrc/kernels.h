@@ -34,6 +34,11 @@ KernelEntry ffma_kernel_scaled(int producer, int stages, int math);
 // Transposed-A FFMA kernels (A stored K x M): TMA producer, 2 stages, paired
 // FMA, 128 x 128 tiles; `scaled` selects the scaled epilogue.
 KernelEntry ffma_kernel_amn(int stages, int math, bool scaled);
+// FFMA kernels on B stored N x K (op(B) = B^T, read in place and transposed
+// in shared memory by a producer warp): A stored M x K (transposed in shared
+// memory too) or, with `a_mn`, K x M; 2 stages, paired FMA, 128 x 128 tiles;
+// `scaled` selects the scaled epilogue.
+KernelEntry ffma_kernel_bnk(bool a_mn, bool scaled);
 // FFMA kernels fed by 4-byte cp.async (any alignment); stages in {2,4}.
 KernelEntry ffma_kernel_cpasync(int stages, int math);
 // Three-product TF32 kernel on the tensor cores (TMA-fed, 128 x 128 tiles,

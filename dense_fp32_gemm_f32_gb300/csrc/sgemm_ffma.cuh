@@ -98,12 +98,19 @@ enum : int { kProducerTma = 1, kProducerCpAsync = 2, kProducerTmaWg = 3, kProduc
 // 1024^3 +4.7 % over one warp); 11 warps leave up to 184 registers a thread.
 // Transposing warps of kProducerTmaX (each rewrites half of the slice's rows).
 constexpr int kTransposeWarps = 2;
-template <int PRODUCER>
+// BNK (B stored N x K, k innermost: the general entry's op(B) = B^T read in
+// place): one more producer warp transposes each stage's B slice (as loaded:
+// 128 rows of 32 k, 128-byte swizzled, the layout of an A slice) into rows of
+// k for the consumers.  With the two A-transposing warps that is 12 warps,
+// whose 384 threads still get 168 registers each.
+constexpr int kTransposeWarpsB = 1;
+template <int PRODUCER, bool BNK = false>
 __host__ __device__ constexpr int ffma_producer_warps() {
-    return PRODUCER == kProducerFused ? 0
-           : PRODUCER == kProducerTma ? 1
-           : PRODUCER == kProducerTmaX ? 1 + kTransposeWarps
-                                       : 4;
+    return (PRODUCER == kProducerFused ? 0
+            : PRODUCER == kProducerTma ? 1
+            : PRODUCER == kProducerTmaX ? 1 + kTransposeWarps
+                                        : 4) +
+           (BNK ? kTransposeWarpsB : 0);
 }
 template <int PRODUCER>
 __host__ __device__ constexpr int ffma_consumer_warps() {
@@ -118,9 +125,9 @@ constexpr int kRegsProducer = 40;
 constexpr int kRegsConsumer = 232;
 static_assert(4 * 32 * kRegsProducer + kConsumerWarps * 32 * kRegsConsumer == (kConsumerWarps + 4) * 32 * kRegsLaunch,
               "the register split must use exactly the registers the CTA is launched with");
-template <int PRODUCER>
+template <int PRODUCER, bool BNK = false>
 __host__ __device__ constexpr int ffma_threads() {
-    return 32 * (ffma_consumer_warps<PRODUCER>() + ffma_producer_warps<PRODUCER>());
+    return 32 * (ffma_consumer_warps<PRODUCER>() + ffma_producer_warps<PRODUCER, BNK>());
 }
 constexpr int kBNWide = 256;  // wide tile: 128 x 256, 8 x 16 per thread (producer warpgroup only)
 constexpr int kBNFused = 64;  // 128 x 64 tiles of the fused-producer CTAs
@@ -156,6 +163,7 @@ struct FfmaParams {
     int tiles_n;           // output tiles per row of tiles
     int tiles_m;           // rows of output tiles
     int group_m;           // tile order: groups of group_m rows of tiles (1 = row by row; see tile_rc)
+    int a_evict_last;      // A's slices are loaded with the L2 evict-last policy
     // Stream-K schedule (sk != 0), one CTA per SM: CTA g first takes whole
     // tiles g, g + G, ... below sk_dp_tiles (data-parallel waves, raster
     // order), then an even share of the units (one K slice of one tile each)
@@ -176,10 +184,11 @@ struct FfmaParams {
     float alpha, beta;
 };
 
-// XA: the stage also holds the transposed copy of its A slice (kProducerTmaX).
-template <int STAGES, int BN = kBN, bool XA = false>
+// XA: the stage also holds the transposed copy of its A slice (kProducerTmaX);
+// XB: and of its B slice (BNK).
+template <int STAGES, int BN = kBN, bool XA = false, bool XB = false>
 constexpr int ffma_smem_bytes() {
-    constexpr int stage = ffma_stage_bytes<BN>() + (XA ? kStageABytes : 0);
+    constexpr int stage = ffma_stage_bytes<BN>() + (XA ? kStageABytes : 0) + (XB ? ffma_stage_b_bytes<BN>() : 0);
     return (STAGES * stage > ffma_partial_bytes<BN>() ? STAGES * stage : ffma_partial_bytes<BN>()) + 1024 /*align*/ +
            256 /*barriers*/;
 }
@@ -220,8 +229,13 @@ __device__ __forceinline__ uint32_t swz128(int r, int c) {
 // entry's op(A) = A^T).  The TMA then lands each stage's A slice as 32 rows of
 // 128 m values (no swizzle) and a thread reads its 8 rows' values for one k
 // as two 16-byte vectors; its rows become wm*32 + 16*(i/4) + 4*tm + i%4.
-template <int STAGES, int PRODUCER, int MATH, int BN = kBN, bool SCALED = false, bool AMN = false>
-__global__ void __launch_bounds__(ffma_threads<PRODUCER>(), ffma_min_blocks<PRODUCER>())
+//
+// BNK: B is stored transposed (N x K row-major, k innermost: the general
+// entry's op(B) = B^T).  The TMA lands each stage's B slice as 128 rows (n)
+// of 32 k with the 128-byte swizzle, and a transposing producer warp rewrites
+// it as 32 rows (k) of 128 n, the layout the consumers read.
+template <int STAGES, int PRODUCER, int MATH, int BN = kBN, bool SCALED = false, bool AMN = false, bool BNK = false>
+__global__ void __launch_bounds__(ffma_threads<PRODUCER, BNK>(), ffma_min_blocks<PRODUCER>())
     sgemm_ffma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                       const FfmaParams p) {
     // 128 accumulators per thread need the consumer register budget of the
@@ -233,6 +247,10 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), ffma_min_blocks<PROD
     static_assert(!(kX && AMN), "A is transposed either in HBM or in shared memory");
     static_assert(!kX || BN == kBN, "in-shared-memory transposition: 128 x 128 tiles");
     constexpr bool kAT = AMN || kX;  // consumers read A with m innermost
+    static_assert(!BNK || (BN == kBN && (PRODUCER == kProducerTmaX || (PRODUCER == kProducerTma && AMN))),
+                  "B stored N x K: 128 x 128 tiles, transposing producer");
+    constexpr int kXA = kX ? kTransposeWarps : 0;    // A-transposing warps
+    constexpr int kXB = BNK ? kTransposeWarpsB : 0;  // B-transposing warps
     static_assert((BN == kBN && !kFused) || (BN == kBNWide && PRODUCER == kProducerTmaWg) ||
                       (BN == kBNFused && kFused),
                   "tile width");
@@ -249,13 +267,15 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), ffma_min_blocks<PROD
     const uint32_t raw_base = smem_addr(smem_raw);
     const uint32_t base = (raw_base + 1023u) & ~1023u;
     uint8_t* const smem = smem_raw + (base - raw_base);
-    constexpr int kSlotBytes = kStageBytes + (kX ? kStageABytes : 0);
+    constexpr int kSlotBytes = kStageBytes + (kX ? kStageABytes : 0) + (BNK ? kStageBBytes : 0);
     constexpr int kRingBytes = STAGES * kSlotBytes > kPartialBytes ? STAGES * kSlotBytes : kPartialBytes;
-    // Ring: A slices (as loaded), [transposed A slices], B slices.
+    // Ring: A slices (as loaded), [transposed A slices], B slices (as
+    // loaded), [transposed B slices].
     constexpr int kTOff = STAGES * kStageABytes;                       // transposed A (kX)
-    constexpr int kBOff = (kX ? 2 : 1) * STAGES * kStageABytes;        // B
+    constexpr int kBLoadOff = (kX ? 2 : 1) * STAGES * kStageABytes;    // B as loaded
+    constexpr int kBOff = kBLoadOff + (BNK ? STAGES * kStageBBytes : 0);  // B as the consumers read it
     const uint32_t sA0 = base;                                         // STAGES x 16 KiB
-    const uint32_t sB0 = base + kBOff;                                 // STAGES x kStageBBytes
+    const uint32_t sB0 = base + kBLoadOff;                             // STAGES x kStageBBytes
     const uint32_t bar0 = base + kRingBytes;  // full[STAGES], empty[STAGES], tfull[STAGES]
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
@@ -317,11 +337,11 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), ffma_min_blocks<PROD
     if (threadIdx.x == 0) {
         const uint32_t full_count = kTma ? 1u : 32u * PW;
         // (kX: the transposing warps also release each slot, for its A slice.)
-        const uint32_t empty_count = static_cast<uint32_t>(CW + (kX ? kTransposeWarps : 0));
+        const uint32_t empty_count = static_cast<uint32_t>(CW + kXA + kXB);
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full_bar(s), full_count);
             mbar_init(empty_bar(s), empty_count);
-            if (kX) mbar_init(tfull_bar(s), 32u * kTransposeWarps);  // every lane of the transposing warps
+            if (kXA + kXB) mbar_init(tfull_bar(s), 32u * (kXA + kXB));  // every lane of the transposing warps
         }
         fence_mbarrier_init();
     }
@@ -348,14 +368,21 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), ffma_min_blocks<PROD
         // first; the consumers' requests are served from what it released.
         if constexpr (PRODUCER == kProducerTmaWg) setmaxnreg_dec<kRegsProducer>();
         const bool issuer = !kTma || (pw == 0 && lane == 0);
-        if (kX && pw >= 1) {
+        if ((kXA + kXB) > 0 && pw >= 1) {
             // Transposing warps: A slice s (row m: 32 floats in 128-byte
-            // swizzled chunks) -> transposed slice (row k: 128 floats).  Lane
-            // l of transposing warp x takes rows l + 32q for its share of q
-            // (x = 0: q = 0, 1; x = 1: q = 2, 3): a 16-byte read of chunk c
-            // covers k = 4c..4c+3 of one row (the 8 lanes of each wavefront hit
-            // 8 different chunk positions), and each of its 4 floats is stored
-            // to row k at column m (32 consecutive floats per store).
+            // swizzled chunks) -> transposed slice (row k: 128 floats); the
+            // same for B stored N x K (row n -> row k).  Lane l of an
+            // A-transposing warp x takes rows l + 32q for its share of q
+            // (x = 0: q = 0, 1; x = 1: q = 2, 3), the B-transposing warp all
+            // four q: a 16-byte read of chunk c covers k = 4c..4c+3 of one
+            // row (the 8 lanes of each wavefront hit 8 different chunk
+            // positions), and each of its 4 floats is stored to row k at
+            // column m (or n) (32 consecutive floats per store).
+            const bool xb = BNK && pw - 1 >= kXA;  // this warp transposes B
+            const int qn = xb ? 4 : 4 / kTransposeWarps;
+            const int q0 = xb ? 0 : (pw - 1) * qn;
+            const int src_off = xb ? kBLoadOff : 0;
+            const int dst_off = xb ? kBOff : kTOff;
             int xit = 0;
             Work xwork = work0;
             int xtile, xkb, xke;
@@ -367,11 +394,11 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), ffma_min_blocks<PROD
                         timed_out = true;
                         break;
                     }
-                    const uint8_t* const raw = smem + s * kStageABytes;
-                    float* const tr = reinterpret_cast<float*>(smem + kTOff + s * kStageABytes);
+                    const uint8_t* const raw = smem + src_off + s * kStageABytes;
+                    float* const tr = reinterpret_cast<float*>(smem + dst_off + s * kStageABytes);
 #pragma unroll
-                    for (int qq = 0; qq < 4 / kTransposeWarps; ++qq) {
-                        const int m = lane + 32 * ((pw - 1) * (4 / kTransposeWarps) + qq);
+                    for (int qq = 0; qq < qn; ++qq) {
+                        const int m = lane + 32 * (q0 + qq);
 #pragma unroll
                         for (int c = 0; c < 8; ++c) {
                             const float4 v =
@@ -384,7 +411,7 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), ffma_min_blocks<PROD
                     }
                     __syncwarp();
                     mbar_arrive(tfull_bar(s));           // transposed slice written (every lane)
-                    if (lane == 0) mbar_arrive(empty_bar(s));  // A slice read
+                    if (lane == 0) mbar_arrive(empty_bar(s));  // slice as loaded read
                 }
             }
         }
@@ -394,6 +421,10 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), ffma_min_blocks<PROD
         int it = 0;  // K slices so far, across tiles: position in the stage ring
         Work work = work0;
         int tile, kb, ke;
+        // With the grouped tile order, the A row panels of a group serve the
+        // group's consecutive waves of tiles: loaded evict-last, they stay in
+        // L2 while the B column panels stream past.
+        const uint64_t a_policy = (kTma && p.a_evict_last) ? l2_policy_evict_last() : 0;
         while (issuer && !timed_out && work.next(tile, kb, ke)) {
             int tm_, tn_;
             tile_rc(tile, p.tiles_n, p.tiles_m, p.group_m, tm_, tn_);
@@ -414,10 +445,16 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), ffma_min_blocks<PROD
                     mbar_arrive_expect_tx(full_bar(s), kStageBytes);
                     if (AMN) {
                         tma_load_2d(sA0 + s * kStageABytes, &tmA, full_bar(s), m0, k0);
+                    } else if (p.a_evict_last) {
+                        tma_load_2d_hint(sA0 + s * kStageABytes, &tmA, full_bar(s), k0, m0, a_policy);
                     } else {
                         tma_load_2d(sA0 + s * kStageABytes, &tmA, full_bar(s), k0, m0);
                     }
-                    tma_load_2d(sB0 + s * kStageBBytes, &tmB, full_bar(s), n0, k0);
+                    if (BNK) {
+                        tma_load_2d(sB0 + s * kStageBBytes, &tmB, full_bar(s), k0, n0);
+                    } else {
+                        tma_load_2d(sB0 + s * kStageBBytes, &tmB, full_bar(s), n0, k0);
+                    }
                 } else {
                     // cp.async: PW warps copy 4-byte elements with zero fill;
                     // every lane's copies arrive on the full barrier.
@@ -706,7 +743,7 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER>(), ffma_min_blocks<PROD
                 const int round = it / STAGES;
                 if (kFused && threadIdx.x == 0 && it > 0) issue_load();
                 if (!mbar_wait_bounded_warp(full_bar(s), round & 1, tmo) ||
-                    (kX && !mbar_wait_bounded_warp(tfull_bar(s), round & 1, tmo))) {
+                    ((kXA + kXB) > 0 && !mbar_wait_bounded_warp(tfull_bar(s), round & 1, tmo))) {
                     timed_out = true;
                     break;
                 }

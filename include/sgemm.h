@@ -334,6 +334,10 @@ typedef struct sgemm_options {
                              at one time share B column panels (n of them per
                              panel) and A row panels in L2; 1 = row by row.
                              Larger than the rows of tiles: one group. */
+    int l2_hint;          /* 0 = auto, 1 = no cache policy, 2 = A's slices
+                             loaded with the L2 evict-last policy (the A row
+                             panels of a tile group stay in L2 across its
+                             waves); tensor-map producers on A as stored */
 } sgemm_options;
 
 /* sgemm_f32 with forced choices.  Same contract; an unsupported combination
@@ -364,8 +368,9 @@ int sgemm_f32_ex(int M, int N, int K,
  * tiles, nk / 2) CTAs in the same way when nk (s - 1) / s >= 7 + 2 (s - 1)
  * (1024^3: s = 2).  split_k: 0 = automatic, 1 = no K split (any
  * variant), 2..4 = every tile's K slices split among that many CTAs (variant
- * 1, forced or automatic, and at least one 32-deep slice per CTA; otherwise
- * SGEMM_ERR_INVALID_ARG).  Other fields are ignored. */
+ * 1, forced or automatic, and at least one 32-deep slice per CTA; for variants
+ * 3 and 4, 2 = split the last partial wave's tiles along K whatever K;
+ * otherwise SGEMM_ERR_INVALID_ARG).  Other fields are ignored. */
 int sgemm_3xtf32_ex(int M, int N, int K,
                     const float* A, int lda,
                     const float* B, int ldb,

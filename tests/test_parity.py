@@ -107,6 +107,8 @@ VARIANTS = (
     + [dict(group_m=gm) for gm in (1, 2)]
     + [dict(group_m=2, stream_k=2), dict(group_m=2, split_k=2), dict(group_m=2, producer=4),
        dict(group_m=2, tile_n=256, split_k=1)]
+    # A's slices with the L2 evict-last policy
+    + [dict(l2_hint=h) for h in (1, 2)] + [dict(l2_hint=2, group_m=2, stream_k=2), dict(l2_hint=2, producer=1)]
     # producer warpgroup with the setmaxnreg register split
     + [dict(producer=3, math=m, stages=s, split_k=1, multicast=1) for m in (1, 2) for s in (1, 4, 6)]
     + [dict(producer=3, math=2, split_k=s, multicast=1) for s in (2, 4)]

@@ -166,3 +166,35 @@ def test_general_rejects_bad_arguments():
         g.sgemm_f32_gemm(A, B, C)  # op(A) is 64 x 32: does not multiply 64 x 48
     with pytest.raises(ValueError):
         g.sgemm_f32_gemm(A, B, None, beta=1.0, transa=True)  # beta != 0 needs C
+
+
+@pytest.mark.parametrize("ta", [0, 1])
+@pytest.mark.parametrize("pad_a,pad_b", [(0, 4), (3, 0), (3, 8)])
+def test_transposed_b_read_in_place(ta, pad_a, pad_b):
+    """op(B) = B^T with 16-byte B rows is read in place (a producer warp
+    transposes its slices in shared memory), also with padded B rows and
+    with an A whose odd pitch makes the library copy it first; ragged against
+    the 128 x 128 tiles in M, N and K."""
+    M, N, K = 650, 900, 1000
+    a, b = (x.numpy() for x in make_operands(M, N, K, "uniform", 216))
+    cin = make_operands(M, 1, N, "uniform", 217)[0].numpy()
+    A, B = stored(a, b, ta, 1)
+    C = run(A, B, cin, alpha=-0.75, beta=0.5, ta=ta, tb=1, lda=A.shape[1] + pad_a, ldb=B.shape[1] + pad_b)
+    ref, bound = oracle.gemm_general_f64(A, B, cin, alpha=-0.75, beta=0.5, transa=ta, transb=1)
+    check(C, ref, bound, exact=False, what=f"t{ta}1 pads {pad_a},{pad_b}")
+    C1 = run(A, B, None, alpha=1.0, beta=0.0, ta=ta, tb=1, ldb=B.shape[1] + pad_b)  # plain epilogue
+    ref1, bound1 = oracle.gemm_general_f64(A, B, alpha=1.0, beta=0.0, transa=ta, transb=1)
+    check(C1, ref1, bound1, exact=False, what=f"t{ta}1 plain")
+
+
+@pytest.mark.parametrize("ta", [0, 1])
+@pytest.mark.parametrize("dist", ["uniform", "int"])
+def test_transposed_b_skinny_every_element(ta, dist):
+    """128 x 8192 x 16384 with op(B) = B^T (one row of 64 tiles, stream-K over
+    512 K slices each): every element; integer inputs exactly."""
+    M, N, K = 128, 8192, 16384
+    a, b = (x.numpy() for x in make_operands(M, N, K, dist, 218))
+    A, B = stored(a, b, ta, 1)
+    C = run(A, B, None, alpha=1.0, beta=0.0, ta=ta, tb=1)
+    ref, bound = oracle.gemm_general_f64(A, B, alpha=1.0, beta=0.0, transa=ta, transb=1, with_bound=dist != "int")
+    check(C, ref, None if dist == "int" else bound, exact=dist == "int", what=f"skinny t{ta}1 {dist}")
