@@ -126,8 +126,23 @@ int run_ffma(int M, int N, int K, const float* A, int lda, const float* B, int l
 
     alignas(64) CUtensorMap tmA;
     alignas(64) CUtensorMap tmB;
+    alignas(64) CUtensorMap tmC;
     std::memset(&tmA, 0, sizeof tmA);
     std::memset(&tmB, 0, sizeof tmB);
+    std::memset(&tmC, 0, sizeof tmC);
+    // Tensor-map stores of C need 16-byte rows and base, and N a multiple of
+    // 4: measured on GB300, a store whose box crosses the end of a row also
+    // writes the rest of the 16-byte group holding the last column (the row
+    // padding of C, which the contract leaves untouched).  They pay only for
+    // long K loops (kTmaStoreMinSlices).
+    const bool c_aligned = tma_ok(C, ldc) && N % 4 == 0 && pl.num_k_tiles >= kTmaStoreMinSlices;
+    if (k.tma_store && c_aligned) {
+        rc = encode_2d(&tmC, C, N, M, ldc, kBN, kBM, CU_TENSOR_MAP_SWIZZLE_NONE);  // {n, m} boxes of 128 x 128
+        if (rc != SGEMM_OK) {
+            release_pack();
+            return rc;
+        }
+    }
     if (is_tma(pl.producer)) {
         rc = pl.a_mn ? encode_2d(&tmA, A, M, K, lda, kBM, kBK, CU_TENSOR_MAP_SWIZZLE_NONE)  // {m, k} boxes of 128 x 32
                      : encode_2d(&tmA, A, K, M, lda, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B);
@@ -156,6 +171,7 @@ int run_ffma(int M, int N, int K, const float* A, int lda, const float* B, int l
     prm.tiles_m = pl.tiles_m;
     prm.group_m = pl.group_m;
     prm.a_evict_last = pl.a_evict_last;
+    prm.tma_store = (k.tma_store && c_aligned) ? 1 : 0;
     prm.skip_stage = opt ? opt->debug_skip_stage : 0;
     prm.timeout_ns = (opt && opt->timeout_ns) ? opt->timeout_ns : kDefaultTimeoutNs;
     prm.status = st->status_word;
@@ -225,7 +241,7 @@ int run_ffma(int M, int N, int K, const float* A, int lda, const float* B, int l
         }
         cfg.attrs = &attr;
         cfg.numAttrs = (pl.sk || ln.split > 1) ? 1 : 0;
-        void* args[3] = {&tmA, &tmB, &prm};
+        void* args[4] = {&tmA, &tmB, &tmC, &prm};
         if (cudaLaunchKernelExC(&cfg, k.fn, args) != cudaSuccess) {
             (void)cudaGetLastError();
             sk_return(*st, cs, lease);
@@ -288,8 +304,16 @@ int run_ffma_noalloc(int M, int N, int K, const float* A, int lda, const float* 
     if (!k.fn) return SGEMM_ERR_INVALID_ARG;
     alignas(64) CUtensorMap tmA;
     alignas(64) CUtensorMap tmB;
+    alignas(64) CUtensorMap tmC;
     std::memset(&tmA, 0, sizeof tmA);
     std::memset(&tmB, 0, sizeof tmB);
+    std::memset(&tmC, 0, sizeof tmC);
+    const bool c_tma = k.tma_store && tma_ok(C, ldc) && N % 4 == 0 &&
+                       pl.num_k_tiles >= kTmaStoreMinSlices;  // (as in run_ffma)
+    if (c_tma) {
+        rc = encode_2d(&tmC, C, N, M, ldc, kBN, kBM, CU_TENSOR_MAP_SWIZZLE_NONE);
+        if (rc != SGEMM_OK) return rc;
+    }
     if (is_tma(pl.producer)) {
         rc = encode_2d(&tmA, A, K, M, lda, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B);
         if (rc == SGEMM_OK) rc = encode_2d(&tmB, B, N, K, ldb, pl.bn, kBK, CU_TENSOR_MAP_SWIZZLE_NONE);
@@ -315,6 +339,7 @@ int run_ffma_noalloc(int M, int N, int K, const float* A, int lda, const float* 
     prm.tiles_m = pl.tiles_m;
     prm.group_m = pl.group_m;
     prm.a_evict_last = pl.a_evict_last;
+    prm.tma_store = c_tma ? 1 : 0;
     prm.timeout_ns = kDefaultTimeoutNs;
     prm.status = st->status_word;
     prm.sk = pl.sk;
@@ -359,7 +384,7 @@ int run_ffma_noalloc(int M, int N, int K, const float* A, int lda, const float* 
     attr.val.cooperative = 1;
     cfg.attrs = &attr;
     cfg.numAttrs = pl.sk ? 1 : 0;
-    void* args[3] = {&tmA, &tmB, &prm};
+    void* args[4] = {&tmA, &tmB, &tmC, &prm};
     if (cudaLaunchKernelExC(&cfg, k.fn, args) != cudaSuccess) {
         (void)cudaGetLastError();
         return SGEMM_ERR_CUDA;

@@ -1,5 +1,5 @@
 // The host-buffer entry sgemm_f32_host: copies in and out on the library's
-// copy streams, overlapped with the products of row blocks and K chunks.
+// copy streams, overlapped with the products of K chunks and row blocks.
 #include "api_internal.h"
 
 namespace gb300 {
@@ -18,11 +18,22 @@ cudaError_t copy_rows(float* dst, long long ld_dst, const float* src, long long 
 
 // Host-buffer form (see sgemm_f32_host): pitched device copies of A, B, C
 // from the pool (rows of ceil(width / 4) x 4 floats, so that the tensor maps
-// can always read them).  A and C move in row blocks so that block i's
-// product overlaps block i+1's copy in and block i-1's copy out; B moves in K
-// chunks, and the first block's product is split the same way (accumulating
-// into C), so that the first product starts after A's first block and B's
-// first chunk rather than after all of B.
+// can always read them).
+//
+// Schedule of products of 2^32 flop and more.  The host link moves far fewer
+// bytes per second than the product consumes (measured on GB300: ~210 GB/s
+// in, ~195 GB/s out; a 4096 x 4096 output consumes a column of A and a row
+// of B, 32 KB, every 0.5 us), so no product may wait for whole operands.  K
+// is cut into chunks that grow (to 1/32, 1/8, 1/2 and all of K): chunk c's
+// columns of A and rows of B cross the link together, and the product
+// C (+)= A[:, c] B[c, :] over all rows starts once they are in, while the
+// next chunk crosses.  The first chunk is short, so that the first product
+// starts early; each later chunk is in before the product of the one before
+// it ends.  The last chunk's product runs in row blocks that shrink towards
+// the end (to 1/4, 1/2, 3/4, 7/8, 15/16 and all of the rows), each block's
+// rows of C going back over the link while the next block computes, so that
+// only the last, small block of C crosses after the last product.  Smaller
+// products run as one block: copies in, product, copy out.
 int run_host(int M, int N, int K, const float* A, int lda, const float* B, int ldb, float* C, int ldc,
              void* stream) {
     int rc = validate(M, N, K, A, lda, B, ldb, C, ldc);
@@ -52,17 +63,31 @@ int run_host(int M, int N, int K, const float* A, int lda, const float* B, int l
     cudaMemPool_t pool = workspace_pool(dev, *st);
     if (!pool) return SGEMM_ERR_CUDA;
 
-    // Row blocks: whole 128-row tiles, up to 8 blocks of >= 512 rows; one
-    // block below 2^32 flop (the copies then run before and after the
-    // product).  K chunks of B (multiples of 32): 4 when blocked and K >= 1024.
-    constexpr int kMaxBlk = kHostMaxBlk, kMaxKc = kHostMaxKc;
+    // K chunks (boundaries multiples of 32) and the row blocks of the last
+    // chunk (boundaries multiples of 128 rows); empty ones are dropped.
     const bool big = 2.0 * static_cast<double>(M) * N * K >= 4294967296.0;
-    const int nblk = big ? static_cast<int>(std::min<long long>(kMaxBlk, (static_cast<long long>(M) + 511) / 512)) : 1;
-    const long long rows_blk = ((static_cast<long long>(M) + nblk - 1) / nblk + kBM - 1) / kBM * kBM;
-    const int nkc = (big && nblk > 1 && K >= 1024) ? kMaxKc : 1;
-    auto k_at = [&](int c) -> long long {
-        return c >= nkc ? K : (static_cast<long long>(K) * c / nkc) / 32 * 32;
-    };
+    long long kb[kHostMaxKc + 1] = {0};
+    int nkc = 0;
+    {
+        const int den = 32, num[kHostMaxKc] = {1, 4, 16, 32};
+        for (int c = 0; c < kHostMaxKc; ++c) {
+            const long long b = (!big || c == kHostMaxKc - 1) ? K : (static_cast<long long>(K) * num[c] / den) / 32 * 32;
+            if (b > kb[nkc]) kb[++nkc] = b;
+            if (!big) break;
+        }
+        if (nkc == 0) kb[++nkc] = K;  // K == 0: one (empty) chunk
+    }
+    long long rb[kHostMaxBlk + 1] = {0};
+    int nblk = 0;
+    {
+        const int den = 16, num[kHostMaxBlk] = {4, 8, 12, 14, 15, 16};
+        for (int i = 0; i < kHostMaxBlk; ++i) {
+            const long long b =
+                (!big || i == kHostMaxBlk - 1) ? M : (static_cast<long long>(M) * num[i] / den) / kBM * kBM;
+            if (b > rb[nblk]) rb[++nblk] = b;
+            if (!big) break;
+        }
+    }
 
     const long long K4 = (static_cast<long long>(K) + 3) / 4 * 4;
     const long long N4 = (static_cast<long long>(N) + 3) / 4 * 4;
@@ -82,46 +107,45 @@ int run_host(int M, int N, int K, const float* A, int lda, const float* B, int l
 
     cudaEvent_t* const ev = st->host_ev;
     const cudaEvent_t ev_start = ev[0], ev_in_end = ev[1], ev_out_end = ev[2];
-    cudaEvent_t* const ev_a = ev + 3;                 // [kMaxBlk]
-    cudaEvent_t* const ev_done = ev + 3 + kMaxBlk;    // [kMaxBlk]
-    cudaEvent_t* const ev_b = ev + 3 + 2 * kMaxBlk;   // [kMaxKc]
+    cudaEvent_t* const ev_done = ev + 3;              // [kHostMaxBlk]: row block's product done
+    cudaEvent_t* const ev_in = ev + 3 + kHostMaxBlk;  // [kHostMaxKc]: K chunk's copies in
     // The copy streams start after the workspace exists (stream order of cs).
     bool ok = cudaEventRecord(ev_start, cs) == cudaSuccess &&
-         cudaStreamWaitEvent(st->copy_in, ev_start, 0) == cudaSuccess &&
-         cudaStreamWaitEvent(st->copy_out, ev_start, 0) == cudaSuccess;
+              cudaStreamWaitEvent(st->copy_in, ev_start, 0) == cudaSuccess &&
+              cudaStreamWaitEvent(st->copy_out, ev_start, 0) == cudaSuccess;
 
-    // Copies in, in the order the products need them: A's first block, B's
-    // chunks, A's other blocks.
-    auto copy_a = [&](int i) {
-        const long long r0 = i * rows_blk, rows = std::min<long long>(rows_blk, M - r0);
-        return rows <= 0 || (copy_rows(dA + r0 * K4, K4, A + r0 * lda, lda, rows, K, cudaMemcpyHostToDevice,
-                                       st->copy_in) == cudaSuccess &&
-                             cudaEventRecord(ev_a[i], st->copy_in) == cudaSuccess);
-    };
-    ok = ok && copy_a(0);
-    for (int c = 0; c < nkc && ok; ++c)
-        ok = copy_rows(dB + k_at(c) * N4, N4, B + k_at(c) * ldb, ldb, k_at(c + 1) - k_at(c), N,
-                       cudaMemcpyHostToDevice, st->copy_in) == cudaSuccess &&
-             cudaEventRecord(ev_b[c], st->copy_in) == cudaSuccess;
-    for (int i = 1; i < nblk && ok; ++i) ok = copy_a(i);
+    // Copies in: per K chunk, A's columns (a pitched copy) and B's rows.
+    for (int c = 0; c < nkc && ok; ++c) {
+        const long long k0 = kb[c], kw = kb[c + 1] - kb[c];
+        ok = (kw == 0 ||
+              ((K4 == kw && lda == kw
+                    ? cudaMemcpyAsync(dA, A, static_cast<size_t>(M) * kw * 4, cudaMemcpyHostToDevice, st->copy_in)
+                    : cudaMemcpy2DAsync(dA + k0, static_cast<size_t>(K4) * 4, A + k0, static_cast<size_t>(lda) * 4,
+                                        static_cast<size_t>(kw) * 4, static_cast<size_t>(M), cudaMemcpyHostToDevice,
+                                        st->copy_in)) == cudaSuccess &&
+               copy_rows(dB + k0 * N4, N4, B + k0 * ldb, ldb, kw, N, cudaMemcpyHostToDevice, st->copy_in) ==
+                   cudaSuccess)) &&
+             cudaEventRecord(ev_in[c], st->copy_in) == cudaSuccess;
+    }
 
-    // Products on cs, copies out on copy_out.
-    Scale accumulate;  // C += A_chunk B_chunk for the first block's later K chunks
+    // Products on cs: the chunks before the last over all rows, the last in
+    // row blocks; each block's rows of C out on copy_out.
+    Scale accumulate;  // C += A_chunk B_chunk for every chunk after the first
     accumulate.alpha = 1.f;
     accumulate.beta = 1.f;
+    for (int c = 0; c + 1 < nkc && ok && rc == SGEMM_OK; ++c) {
+        ok = cudaStreamWaitEvent(cs, ev_in[c], 0) == cudaSuccess;
+        if (ok)
+            rc = run_ffma(M, N, static_cast<int>(kb[c + 1] - kb[c]), dA + kb[c], lda_d, dB + kb[c] * N4, ldb_d, dC,
+                          ldc_d, stream, nullptr, c > 0 ? &accumulate : nullptr);
+    }
+    const long long kl0 = kb[nkc - 1], klw = kb[nkc] - kb[nkc - 1];
+    if (ok && rc == SGEMM_OK) ok = cudaStreamWaitEvent(cs, ev_in[nkc - 1], 0) == cudaSuccess;
     for (int i = 0; i < nblk && ok && rc == SGEMM_OK; ++i) {
-        const long long r0 = i * rows_blk, rows = std::min<long long>(rows_blk, M - r0);
-        if (rows <= 0) break;
-        ok = cudaStreamWaitEvent(cs, ev_a[i], 0) == cudaSuccess;
-        const int chunks = i == 0 ? nkc : 1;
-        for (int c = 0; c < chunks && ok && rc == SGEMM_OK; ++c) {
-            const long long k0 = i == 0 ? k_at(c) : 0, k1 = i == 0 ? k_at(c + 1) : K;
-            ok = cudaStreamWaitEvent(cs, ev_b[i == 0 ? c : nkc - 1], 0) == cudaSuccess;
-            if (ok)
-                rc = run_ffma(static_cast<int>(rows), N, static_cast<int>(k1 - k0), dA + r0 * K4 + k0, lda_d,
-                              dB + k0 * N4, ldb_d, dC + r0 * N4, ldc_d, stream, nullptr, c > 0 ? &accumulate : nullptr);
-        }
-        if (!ok || rc != SGEMM_OK) break;
+        const long long r0 = rb[i], rows = rb[i + 1] - rb[i];
+        rc = run_ffma(static_cast<int>(rows), N, static_cast<int>(klw), dA + r0 * K4 + kl0, lda_d, dB + kl0 * N4,
+                      ldb_d, dC + r0 * N4, ldc_d, stream, nullptr, nkc > 1 ? &accumulate : nullptr);
+        if (rc != SGEMM_OK) break;
         ok = cudaEventRecord(ev_done[i], cs) == cudaSuccess &&
              cudaStreamWaitEvent(st->copy_out, ev_done[i], 0) == cudaSuccess &&
              copy_rows(C + r0 * ldc, ldc, dC + r0 * N4, N4, rows, N, cudaMemcpyDeviceToHost, st->copy_out) ==

@@ -44,10 +44,10 @@ struct SkScratch {
 };
 
 // Row blocks and K chunks of the host-buffer entry's pipeline (api_host.cu).
-constexpr int kHostMaxBlk = 8, kHostMaxKc = 4;
+constexpr int kHostMaxBlk = 6, kHostMaxKc = 4;
 // Its events: start, copies-in done, copies-out done, then per row block
-// "A block in" and "block's product done", then per K chunk "B chunk in".
-constexpr int kHostEvents = 3 + 2 * kHostMaxBlk + kHostMaxKc;
+// "block's product done", then per K chunk "chunk's copies in".
+constexpr int kHostEvents = 3 + kHostMaxBlk + kHostMaxKc;
 
 struct DeviceState {
     std::once_flag once;
@@ -91,12 +91,27 @@ inline long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
 // +23 %, 4095 x 4097 x 4099 and 8191 x 8193 x 8195 +30 %.
 constexpr double kRepackMinFlops = 1073741824.0;  // 2^30
 
-// Rows of tiles per group of the FFMA kernels' tile order (tile_rc).
-constexpr int kGroupRows = 16;
+// Rows of tiles per group of the FFMA kernels' tile order (tile_rc): as many
+// as keep the group's A row panels within kGroupABytes, between 4 and 16.
+constexpr int kGroupRowsMax = 16, kGroupRowsMin = 4;
+constexpr long long kGroupABytes = 32ll << 20;
+
+// Fewest 32-deep K slices per tile for which the FFMA kernels write finished
+// tiles by tensor-map stores from the staging tile.  Measured on GB300
+// (TFLOP/s, direct stores / tensor-map stores): 4096^3 70.0 / 70.3, 8192^3
+// 70.4 / 71.0, 128 x 8192 x 16384 68.3 / 68.6, 2048^3 66.8 / 66.6, 1024^3
+// 45.9 / 45.5, 4096 x 4096 x 256 62.0 / 59.0 (a barrier pair and 64 KiB of
+// shared-memory stores every 8 slices).
+constexpr int kTmaStoreMinSlices = 128;
 
 // Shortest K for which the tensor-core entry splits the tiles of a last
-// partial wave of 128 x 256 tiles along K (variants 3 and 4).
-constexpr int kTcTailSplitMinK = 1024;
+// partial wave of 128 x 256 tiles along K (variants 3 and 4).  Measured on
+// GB300 with the partial tiles summed in the kernel (TFLOP/s, variant 3 /
+// 4, whole / split): 4096^2 x 256 112 / 117 against 93 / 97, x 512 146 / 168
+// against 135 / 152, x 768 165 / 195 against 159 / 184, x 1024 174 / 213
+// against 174 / 206, 2048^3 181 / 205 either way, 4096^2 x 2048 193 / 240
+// against 203 / 244.
+constexpr int kTcTailSplitMinK = 2048;
 
 // The library's stream-ordered pool on device `dev` (api_device.cu).
 cudaMemPool_t workspace_pool(int dev, DeviceState& st);

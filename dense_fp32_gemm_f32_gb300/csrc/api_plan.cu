@@ -254,14 +254,22 @@ int make_plan(const DeviceState& st, int M, int N, int K, const float* A, int ld
     pl.tiles_m = static_cast<int>(tiles_m);
     const long long grid_tiles = static_cast<long long>(pl.tiles_n) * tiles_m;
 
-    // Tile order (see tile_rc): groups of kGroupRows rows of tiles, walked
-    // column by column, so that a wave of 152 CTAs covers about 16 x 9.5
-    // tiles.  Row by row, a wave of the 4096^3 product needs ~5 A row panels
-    // and all 32 B column panels, and B is read from HBM once per wave (ncu:
-    // 531 MB read per launch against 134 MB of A and B).
+    // Tile order (see tile_rc): groups of rows of tiles, walked column by
+    // column (odd groups from the right), so that a wave of 152 CTAs covers
+    // about 16 x 9.5 tiles at 4096^3.  Row by row, a wave of the 4096^3
+    // product needs ~5 A row panels and all 32 B column panels, and B is read
+    // from HBM once per wave.  Measured with ncu on GB300 (DRAM bytes read
+    // per launch; A and B hold 134 MB at 4096^3, 537 MB at 8192^3): 4096^3
+    // 533 MB row by row, 376 / 290 / 556 MB in groups of 8 / 16 / 32 rows,
+    // 276 MB in groups of 16 walked alternately; 8192^3 8.3 GB row by row,
+    // 3.4 / 3.7 GB in groups of 8 / 16 walked alternately.  The time does
+    // not change (the kernel is bound by the FP32 pipe, HBM ~4 % busy).  The
+    // group holds as many rows as keep its A panels within kGroupABytes.
     const int want_group = opt ? opt->group_m : 0;
     if (want_group < 0) return SGEMM_ERR_INVALID_ARG;
-    pl.group_m = want_group > 0 ? want_group : kGroupRows;
+    const long long panel = static_cast<long long>(kBM) * (K > 0 ? K : 1) * 4;
+    const long long auto_group = std::max<long long>(kGroupRowsMin, std::min<long long>(kGroupRowsMax, kGroupABytes / panel));
+    pl.group_m = want_group > 0 ? want_group : static_cast<int>(auto_group);
     if (pl.group_m > pl.tiles_m) pl.group_m = pl.tiles_m > 0 ? pl.tiles_m : 1;
     const int want_hint = opt ? opt->l2_hint : 0;
     if (want_hint < 0 || want_hint > 2) return SGEMM_ERR_INVALID_ARG;

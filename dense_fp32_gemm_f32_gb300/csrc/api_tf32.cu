@@ -59,9 +59,10 @@ int run_3xtf32(int M, int N, int K, const float* A, int lda, const float* B, int
     // fuller wave), the second halves' partial tiles added into C by the
     // tile's CTA that finishes last (in part order: deterministic).  4096^3:
     // 3 waves of 152 wide tiles, then 112 CTAs on the last 56 (262 -> 277
-    // TFLOP/s).  Only for K >= 1024: with shorter K the halves' pipeline fill
-    // and the partial tiles' traffic cost more than the fuller wave gains
-    // (4096 x 4096 x 256: 117 -> 105), and the tiles run as one launch.
+    // TFLOP/s).  Only for K >= kTcTailSplitMinK: with shorter K the halves'
+    // pipeline fill and the partial tiles' traffic cost more than the fuller
+    // wave gains (figures beside the constant), and the tiles run as one
+    // launch.
     struct TcLaunch {
         KernelEntry k;
         int bn, bk;

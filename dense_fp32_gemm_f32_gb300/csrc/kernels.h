@@ -9,6 +9,7 @@ struct KernelEntry {
     const void* fn;   // host stub of the __global__ function, or nullptr if not built
     int smem_bytes;   // dynamic shared memory the launch needs
     int threads;      // threads per CTA
+    bool tma_store = false;  // FFMA kernels: can write C by tensor-map stores (FfmaParams::tma_store)
 };
 
 // FFMA kernels fed by tensor-map bulk copies; stages in {1,2,3,4,5,6}, math 1 = FFMA, 2 = paired FFMA.

@@ -164,6 +164,7 @@ struct FfmaParams {
     int tiles_m;           // rows of output tiles
     int group_m;           // tile order: groups of group_m rows of tiles (1 = row by row; see tile_rc)
     int a_evict_last;      // A's slices are loaded with the L2 evict-last policy
+    int tma_store;         // finished tiles of C go out by tensor-map stores (kernels with a staging tile)
     // Stream-K schedule (sk != 0), one CTA per SM: CTA g first takes whole
     // tiles g, g + G, ... below sk_dp_tiles (data-parallel waves, raster
     // order), then an even share of the units (one K slice of one tile each)
@@ -184,12 +185,31 @@ struct FfmaParams {
     float alpha, beta;
 };
 
+// Largest dynamic shared memory of a CTA on sm_100-family GPUs.
+constexpr int kMaxSmemBytes = 232448;
+
 // XA: the stage also holds the transposed copy of its A slice (kProducerTmaX);
 // XB: and of its B slice (BNK).
 template <int STAGES, int BN = kBN, bool XA = false, bool XB = false>
+__host__ __device__ constexpr int ffma_ring_bytes() {
+    return STAGES * (ffma_stage_bytes<BN>() + (XA ? kStageABytes : 0) + (XB ? ffma_stage_b_bytes<BN>() : 0)) >
+                   ffma_partial_bytes<BN>()
+               ? STAGES * (ffma_stage_bytes<BN>() + (XA ? kStageABytes : 0) + (XB ? ffma_stage_b_bytes<BN>() : 0))
+               : ffma_partial_bytes<BN>();
+}
+
+// The kernels of the transposing producer with the plain epilogue write each
+// finished tile of C by a tensor-map store from a staging tile in shared
+// memory (when C's base and rows are 16-byte aligned), where it fits.
+template <int STAGES, int PRODUCER, int BN, bool SCALED, bool BNK>
+__host__ __device__ constexpr bool ffma_tma_store() {
+    return PRODUCER == kProducerTmaX && BN == kBN && !SCALED &&
+           ffma_ring_bytes<STAGES, BN, true, BNK>() + ffma_partial_bytes<BN>() + 1024 + 256 <= kMaxSmemBytes;
+}
+
+template <int STAGES, int BN = kBN, bool XA = false, bool XB = false, bool STG = false>
 constexpr int ffma_smem_bytes() {
-    constexpr int stage = ffma_stage_bytes<BN>() + (XA ? kStageABytes : 0) + (XB ? ffma_stage_b_bytes<BN>() : 0);
-    return (STAGES * stage > ffma_partial_bytes<BN>() ? STAGES * stage : ffma_partial_bytes<BN>()) + 1024 /*align*/ +
+    return ffma_ring_bytes<STAGES, BN, XA, XB>() + (STG ? ffma_partial_bytes<BN>() : 0) + 1024 /*align*/ +
            256 /*barriers*/;
 }
 
@@ -198,8 +218,10 @@ constexpr int ffma_smem_bytes() {
 // group (the last group may hold fewer rows), so that the tiles of one wave
 // of CTAs form a block of about group_m x (CTAs / group_m) tiles: each B
 // column panel a wave loads then serves group_m tiles instead of one, and
-// the group's A row panels serve its consecutive waves.  group_m = 1 is the
-// row-by-row order.
+// the group's A row panels serve its consecutive waves.  Odd groups walk
+// the columns from the right, so that a group starts on the B panels the
+// previous group used last (still in L2).  group_m = 1 is the row-by-row
+// order.
 __device__ __forceinline__ void tile_rc(int t, int tiles_n, int tiles_m, int group_m, int& tm, int& tn) {
     if (group_m <= 1) {
         tm = t / tiles_n;
@@ -212,7 +234,7 @@ __device__ __forceinline__ void tile_rc(int t, int tiles_n, int tiles_m, int gro
     const int rows = min(group_m, tiles_m - g * group_m);
     const int q = r / rows;
     tm = g * group_m + (r - q * rows);
-    tn = q;
+    tn = (g & 1) ? tiles_n - 1 - q : q;
 }
 
 // Physical byte offset of float (row r, column c) inside a 128-byte-swizzled
@@ -237,7 +259,7 @@ __device__ __forceinline__ uint32_t swz128(int r, int c) {
 template <int STAGES, int PRODUCER, int MATH, int BN = kBN, bool SCALED = false, bool AMN = false, bool BNK = false>
 __global__ void __launch_bounds__(ffma_threads<PRODUCER, BNK>(), ffma_min_blocks<PRODUCER>())
     sgemm_ffma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                      const FfmaParams p) {
+                      const __grid_constant__ CUtensorMap tmC, const FfmaParams p) {
     // 128 accumulators per thread need the consumer register budget of the
     // register split.
     constexpr bool kFused = PRODUCER == kProducerFused;
@@ -267,8 +289,10 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER, BNK>(), ffma_min_blocks
     const uint32_t raw_base = smem_addr(smem_raw);
     const uint32_t base = (raw_base + 1023u) & ~1023u;
     uint8_t* const smem = smem_raw + (base - raw_base);
-    constexpr int kSlotBytes = kStageBytes + (kX ? kStageABytes : 0) + (BNK ? kStageBBytes : 0);
-    constexpr int kRingBytes = STAGES * kSlotBytes > kPartialBytes ? STAGES * kSlotBytes : kPartialBytes;
+    constexpr int kRingBytes = ffma_ring_bytes<STAGES, BN, kX, BNK>();
+    // Staging tile of the tensor-map stores of C, after the ring.
+    constexpr bool kStg = ffma_tma_store<STAGES, PRODUCER, BN, SCALED, BNK>();
+    constexpr int kStgOff = kRingBytes;
     // Ring: A slices (as loaded), [transposed A slices], B slices (as
     // loaded), [transposed B slices].
     constexpr int kTOff = STAGES * kStageABytes;                       // transposed A (kX)
@@ -276,7 +300,7 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER, BNK>(), ffma_min_blocks
     constexpr int kBOff = kBLoadOff + (BNK ? STAGES * kStageBBytes : 0);  // B as the consumers read it
     const uint32_t sA0 = base;                                         // STAGES x 16 KiB
     const uint32_t sB0 = base + kBLoadOff;                             // STAGES x kStageBBytes
-    const uint32_t bar0 = base + kRingBytes;  // full[STAGES], empty[STAGES], tfull[STAGES]
+    const uint32_t bar0 = base + kRingBytes + (kStg ? kPartialBytes : 0);  // full[STAGES], empty[STAGES], tfull[STAGES]
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
     auto tfull_bar = [&](int s) { return bar0 + 8u * (2 * STAGES + s); };  // transposed A ready
@@ -673,14 +697,53 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER, BNK>(), ffma_min_blocks
             }
         }
     };
+    auto consumer_sync = [] { asm volatile("bar.sync 1, %0;" ::"n"(CT) : "memory"); };
+    // Tensor-map store of a finished tile: the consumers write it into the
+    // staging tile (row-major, BN floats a row: a warp's 16-byte stores take
+    // the minimum 4 wavefronts, its lanes' four rows landing on the same
+    // banks 8 lanes at a time), then one thread hands it to the TMA and the
+    // consumers go on to their next tile while it is written out; the TMA
+    // clips the rows and columns outside C.  Before the staging tile is
+    // written again, that thread waits until the previous store has read it.
+    auto store_c_tma = [&](int tile) {
+        int tm_, tn_;
+        tile_rc(tile, p.tiles_n, p.tiles_m, p.group_m, tm_, tn_);
+        float* const stg = reinterpret_cast<float*>(smem + kStgOff);
+        if (threadIdx.x == 0) bulk_wait_read_all();
+        consumer_sync();
+        const int col0 = wn * (BN / WN) + tn * 4;
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+#pragma unroll
+            for (int h = 0; h < H; ++h)
+                *reinterpret_cast<float4*>(stg + row_in_tile(i) * BN + col0 + 32 * h) =
+                    make_float4(acc[i][2 * h].x, acc[i][2 * h].y, acc[i][2 * h + 1].x, acc[i][2 * h + 1].y);
+        fence_proxy_async_smem();  // the generic-proxy writes, visible to the TMA
+        consumer_sync();
+        if (threadIdx.x == 0) {
+            tma_store_2d(&tmC, smem_addr(stg), tn_ * BN, tm_ * kBM);
+            bulk_commit_group();
+        }
+    };
     auto store_c = [&](int tile) {
         if constexpr (SCALED) {
             store_c_scaled(tile);
+        } else if constexpr (kStg) {
+            if (p.tma_store) {
+                store_c_tma(tile);
+            } else {
+                store_c_plain(tile);
+            }
         } else {
             store_c_plain(tile);
         }
     };
-    auto consumer_sync = [] { asm volatile("bar.sync 1, %0;" ::"n"(CT) : "memory"); };
+    // The TMA has finished the last store of this CTA (reading the staging
+    // tile and writing C) before the CTA's shared memory is released.
+    auto drain_stores = [&] {
+        if constexpr (kStg)
+            if (p.tma_store && threadIdx.x == 0) bulk_wait_all();
+    };
 
     {
         // Byte offsets inside a stage.  A row r = wm*32 + tm + 4i has r mod 8 =
@@ -911,10 +974,14 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER, BNK>(), ffma_min_blocks
         if (crank != 0) return;
     }
 
-    if (p.sk) return;  // (stream-K CTAs stored their tiles above)
+    if (p.sk) {  // (stream-K CTAs stored their tiles above)
+        drain_stores();
+        return;
+    }
 
     // ------------------------------------------------------------ epilogue
     store_c(p.tile_base + static_cast<int>(blockIdx.x));
+    drain_stores();
 }
 
 }  // namespace gb300

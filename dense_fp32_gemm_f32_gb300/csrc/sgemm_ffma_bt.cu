@@ -10,8 +10,9 @@ namespace gb300 {
 
 template <int PROD, bool SCALED, bool AMN>
 static KernelEntry entry() {
+    constexpr bool kStg = ffma_tma_store<2, PROD, kBN, SCALED, true>();
     return {reinterpret_cast<const void*>(&sgemm_ffma_kernel<2, PROD, kMathFfma2, kBN, SCALED, AMN, true>),
-            ffma_smem_bytes<2, kBN, PROD == kProducerTmaX, true>(), ffma_threads<PROD, true>()};
+            ffma_smem_bytes<2, kBN, PROD == kProducerTmaX, true, kStg>(), ffma_threads<PROD, true>(), kStg};
 }
 
 KernelEntry ffma_kernel_bnk(bool a_mn, bool scaled) {

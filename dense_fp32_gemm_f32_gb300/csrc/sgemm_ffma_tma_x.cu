@@ -8,7 +8,8 @@ namespace gb300 {
 template <int S, int MATH, bool SCALED>
 static KernelEntry entry() {
     return {reinterpret_cast<const void*>(&sgemm_ffma_kernel<S, kProducerTmaX, MATH, kBN, SCALED>),
-            ffma_smem_bytes<S, kBN, true>(), ffma_threads<kProducerTmaX>()};
+            ffma_smem_bytes<S, kBN, true, false, ffma_tma_store<S, kProducerTmaX, kBN, SCALED, false>()>(),
+            ffma_threads<kProducerTmaX>(), ffma_tma_store<S, kProducerTmaX, kBN, SCALED, false>()};
 }
 
 KernelEntry ffma_kernel_tma_x(int stages, int math, bool scaled) {

@@ -179,14 +179,16 @@ int sgemm_f32_noalloc(int M, int N, int K,
  * serialises).  Same operation, layout rules, accuracy contract and errors as
  * sgemm_f32.
  *
- * The call takes device copies of A, B and C from the library's pool, copies
- * B to the device, then A and C in up to eight row blocks of whole 128-row
- * tiles on two library-owned copy streams, so that the product of block i
- * (on `stream`) overlaps the copy in of block i+1 and the copy out of block
- * i-1; products below 2^32 flop run as one block.  It returns once all of
- * that is enqueued: C holds the result after `stream` is synchronised (all
- * copies are ordered before `stream`'s later work).  The host buffers must
- * stay valid and unmodified until then.
+ * The call takes device copies of A, B and C from the library's pool and
+ * moves them on two library-owned copy streams.  Products of 2^32 flop and
+ * more are pipelined: K is cut into up to four growing chunks, each chunk's
+ * columns of A and rows of B are copied in while the product of the chunk
+ * before runs (C accumulating on the device), and the last chunk's product
+ * runs in up to six shrinking blocks of whole 128-row tiles whose rows of C
+ * are copied out while the next block computes.  Smaller products run as
+ * one block.  It returns once all of that is enqueued: C holds the result
+ * after `stream` is synchronised (all copies are ordered before `stream`'s
+ * later work).  The host buffers must stay valid and unmodified until then.
  */
 int sgemm_f32_host(int M, int N, int K,
                    const float* A, int lda,
@@ -328,12 +330,16 @@ typedef struct sgemm_options {
                              workspace of K x M4 floats) and run the
                              transposed-A kernel, whose consumers read each
                              k's A values as two 16-byte vectors */
-    int group_m;          /* 0 = auto (16); n >= 1: the output tiles are
-                             taken in groups of n rows of tiles, column by
-                             column inside a group, so that the CTAs running
-                             at one time share B column panels (n of them per
-                             panel) and A row panels in L2; 1 = row by row.
-                             Larger than the rows of tiles: one group. */
+    int group_m;          /* 0 = auto (as many rows of tiles, 4 to 16, as
+                             keep the group's A row panels within 32 MiB:
+                             16 at K = 4096, 8 at K = 8192); n >= 1: the
+                             output tiles are taken in groups of n rows of
+                             tiles, column by column inside a group (odd
+                             groups from the right), so that the CTAs
+                             running at one time share B column panels (n of
+                             them per panel) and A row panels in L2; 1 = row
+                             by row.  Larger than the rows of tiles: one
+                             group. */
     int l2_hint;          /* 0 = auto, 1 = no cache policy, 2 = A's slices
                              loaded with the L2 evict-last policy (the A row
                              panels of a tile group stay in L2 across its
@@ -360,7 +366,7 @@ int sgemm_f32_ex(int M, int N, int K,
  * the columns); 4 = variant 3 with B's TF32 parts split and transposed into a
  * pool buffer first (2 x N x K floats; the kernel loads them with the TMA and
  * splits A only).  3 and 4 run whole waves of 128 x 256 tiles; when K >=
- * 1024 the tiles of a last partial wave run in a second launch with their K
+ * 2048 the tiles of a last partial wave run in a second launch with their K
  * slices split between two CTAs, the second halves' partial tiles (a pool
  * workspace of 128 KiB per such tile) added into C, in part order, by the
  * tile's CTA that finishes last.  Variant 1 with at most half as many tiles as

@@ -296,6 +296,38 @@ def test_leading_dimensions_and_guard_bands():
     assert np.all(pad == sentinel)
 
 
+@pytest.mark.parametrize("opt", [dict(), dict(producer=5, stages=3), dict(producer=5, stream_k=1, split_k=1),
+                                 dict(producer=5, split_k=2), dict(producer=5, stages=4)],
+                         ids=["auto", "stages3", "plain-grid", "split2", "stages4-no-staging"])
+@pytest.mark.parametrize("c_offset,N", [(0, 1004), (0, 1001), (1, 1004)])
+def test_tensor_map_stores_of_c_and_guard_bands(opt, c_offset, N):
+    """The 128 x 128 kernels that write finished tiles of C through a staging
+    tile and tensor-map stores (K of 128 slices or more, C 16-byte aligned,
+    ldc % 4 == 0 and N % 4 == 0; with N = 1001, or c_offset = 1 making C's
+    base misaligned, the same kernels store directly): outputs of 600 rows
+    ragged against the tiles in both directions; C's row padding and the
+    floats around C hold a sentinel that must survive."""
+    M, K = 600, 4096
+    A, B = make_operands(M, N, K, "uniform", 17)
+    ldc, guard = 1012, 64 + c_offset
+    sentinel = -12345.0
+    store = torch.full((guard + M * ldc + 64,), sentinel, device="cuda")
+    dC = store[guard:guard + M * ldc].view(M, ldc)[:, :N]
+    dA, dB = to_device(A), to_device(B, 1004)  # 16-byte rows of B: the tensor-map kernels
+    if opt:
+        g.sgemm_f32_ex(dA, dB, dC, **opt)
+    else:
+        assert g.describe(dA, dB, dC).startswith("tmax/")
+        g.sgemm_f32(dA, dB, dC)
+    torch.cuda.synchronize()
+    C64, bound = oracle.gemm_f64(A.numpy(), B.numpy())
+    check(dC.cpu().numpy(), C64, bound, exact=False, what=f"tma-store {opt} offset {c_offset}")
+    s = store.cpu().numpy()
+    assert np.all(s[:guard] == sentinel) and np.all(s[guard + M * ldc:] == sentinel)
+    pad = store[guard:guard + M * ldc].view(M, ldc)[:, N:].cpu().numpy()
+    assert np.all(pad == sentinel)
+
+
 @pytest.mark.parametrize("offsets", [(1, 0), (0, 3), (2, 1)])
 @pytest.mark.parametrize("shape", [(190, 170, 260), (700, 900, 260)])
 def test_unaligned_bases(offsets, shape):
@@ -360,12 +392,33 @@ def test_host_buffer_entry():
 
 @pytest.mark.parametrize("dist", ["uniform", "int"])
 def test_host_buffer_entry_row_blocks(dist):
-    """2048 x 1536 x 2048 (2^34 flop): four row blocks whose copies overlap
-    the products; every element against the oracle."""
+    """2048 x 1536 x 2048 (2^34 flop): four K chunks, the last in six row
+    blocks, whose copies overlap the products; every element."""
     A, B = make_operands(2048, 1536, 2048, dist, 14)
     C = g.sgemm_f32_host(A.pin_memory(), B.pin_memory())
     C64, bound = oracle.gemm_f64(A.numpy(), B.numpy(), with_bound=(dist != "int"))
     check(C.numpy(), C64, bound, exact=(dist == "int"), what=f"host row blocks {dist}")
+
+
+@pytest.mark.parametrize("dist", ["uniform", "int"])
+def test_host_buffer_entry_ragged_chunks(dist):
+    """1500 x 1300 x 2500: K chunks of 64, 224, 960 and 1252, the last in row
+    blocks of 256, 384, 384, 256 and 220 rows (the last one ragged against
+    the 128-row tiles); every element."""
+    A, B = make_operands(1500, 1300, 2500, dist, 16)
+    C = g.sgemm_f32_host(A.pin_memory(), B.pin_memory())
+    C64, bound = oracle.gemm_f64(A.numpy(), B.numpy(), with_bound=(dist != "int"))
+    check(C.numpy(), C64, bound, exact=(dist == "int"), what=f"host ragged chunks {dist}")
+
+
+def test_host_buffer_entry_4096_every_element():
+    """The end-to-end leg of the benchmark (4096^3 through the host-buffer
+    entry on pinned buffers): every element against the oracle."""
+    p = PROBLEMS["square_4096"]
+    A, B = problem_operands(p)
+    C = g.sgemm_f32_host(A.pin_memory(), B.pin_memory())
+    C64, bound = oracle_named(p.name)
+    check(C.numpy(), C64, bound, exact=False, what="host 4096")
 
 
 def test_host_buffer_entry_pitched_and_pageable():

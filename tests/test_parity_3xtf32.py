@@ -152,22 +152,25 @@ def test_k_zero_writes_zeros():
 
 
 @pytest.mark.parametrize("variant", [3, 4])
-@pytest.mark.parametrize("shape", [(1200, 4000, 1040), (1200, 3852, 1100), (1300, 4100, 1025), (1200, 4000, 300)])
+@pytest.mark.parametrize("shape,split_k", [((1200, 4000, 1040), 2), ((1200, 3852, 1100), 2), ((1300, 4100, 1025), 2),
+                                           ((1200, 4000, 2080), 0), ((1200, 4000, 300), 0)])
 @pytest.mark.parametrize("dist", ["uniform", "int"])
-def test_wide_tiles_with_split_tail(shape, dist, variant):
+def test_wide_tiles_with_split_tail(shape, split_k, dist, variant):
     """Variants 3 and 4 with more 128 x 256 tiles than SMs: whole waves of
     wide tiles, then the last partial wave's tiles in a second launch with
     their K slices split between two CTAs, the second halves added into C
     afterwards (1200 x 4000: 160 wide tiles, the last wide column 160 floats
     wide; 1200 x 3852: the second half of each last wide tile lies wholly
     beyond N; K = 1040 / 1100 / 1025 ragged against the 16-deep slices, split
-    32 + 33, 34 + 35 and 32 + 33; K = 300: below the split's threshold, one
-    launch of four waves)."""
+    32 + 33, 34 + 35 and 32 + 33 when forced (split_k = 2); K = 2080: split by
+    the automatic rule; K = 300: below the rule's threshold, one launch of
+    four waves)."""
     M, N, K = shape
     A, B = make_operands(M, N, K, dist, 81)
     exact = dist == "int"
     C64, bound = oracle.gemm_f64(A.numpy(), B.numpy(), with_bound=not exact)
-    check(run(A, B, variant=variant), C64, bound, exact=exact, what=f"wide tail v{variant} {shape} {dist}")
+    check(run(A, B, variant=variant, split_k=split_k), C64, bound, exact=exact,
+          what=f"wide tail v{variant} {shape} {dist}")
 
 
 @pytest.mark.parametrize("shape", [(256, 256, 2500), (128, 1024, 4096), (1000, 700, 2100), (300, 500, 1000),
@@ -244,13 +247,28 @@ def test_wide_tiles_without_split_tail(variant):
     check(run(A, B, variant=variant, split_k=1), C64, bound, exact=False, what=f"v{variant} split_k=1")
 
 
-@pytest.mark.parametrize("kw,K", [(dict(split_k=5), 256), (dict(split_k=-1), 256), (dict(variant=3, split_k=2), 256),
+@pytest.mark.parametrize("variant", [3, 4])
+@pytest.mark.parametrize("K", [48, 300, 700])
+def test_wide_tiles_forced_split_tail_short_k(variant, K):
+    """split_k = 2 on the 128 x 256 tiles splits the last partial wave along
+    K below the automatic threshold too (1200 x 4000: 160 wide tiles, 8 in
+    the last wave; K = 48: three 16-deep slices, split 1 + 2)."""
+    A, B = make_operands(1200, 4000, K, "uniform", 85)
+    C64, bound = oracle.gemm_f64(A.numpy(), B.numpy())
+    check(run(A, B, variant=variant, split_k=2), C64, bound, exact=False, what=f"v{variant} K={K} split_k=2")
+    Ai, Bi = make_operands(1200, 4000, K, "int", 86)
+    check(run(Ai, Bi, variant=variant, split_k=2), oracle.gemm_f64(Ai.numpy(), Bi.numpy(), with_bound=False)[0],
+          None, exact=True, what=f"v{variant} K={K} split_k=2 int")
+
+
+@pytest.mark.parametrize("kw,K", [(dict(split_k=5), 256), (dict(split_k=-1), 256), (dict(variant=3, split_k=3), 256),
                                   (dict(variant=2, split_k=2), 256), (dict(variant=4, split_k=4), 256),
-                                  (dict(variant=1, split_k=3), 64), (dict(split_k=2), 4096)])
+                                  (dict(variant=1, split_k=3), 64), (dict(split_k=3), 4096)])
 def test_forced_k_split_refusals(kw, K):
     """Refused before any launch: split_k out of 0..4, a K split on the
-    direct-A or wide-tile kernels (also when the automatic choice is a wide
-    one: 2048 x 2048 tiles fill half the SMs), more parts than 32-deep slices."""
+    direct-A kernel, more than two parts on the wide-tile kernels (also when
+    the automatic choice is a wide one: 2048 x 2048 tiles fill half the SMs),
+    more parts than 32-deep slices."""
     M = N = 2048 if K == 4096 else 256
     dA = torch.zeros((M, K), device="cuda")
     dB = torch.zeros((K, N), device="cuda")
