@@ -4,6 +4,7 @@
                     [--workload NAME]
     python bench.py --sweep [--sweep-workloads NAME ...]   # ablation table, one JSON line per run
     python bench.py --cpu-table [--cpu-seconds S]          # the oracle on every named problem
+    python bench.py --e2e-only [--workload NAME]           # the host-buffer leg alone (profiling)
 
 One step is one C = A x B call on the named workload (default: the square
 4096^3 problem with standard-normal inputs, seed 3).  Inputs are resident in
@@ -264,6 +265,31 @@ def pct(xs, q):
     """q-th percentile (nearest rank) of a list of numbers."""
     ys = sorted(xs)
     return ys[min(len(ys) - 1, max(0, int(round(q / 100 * (len(ys) - 1)))))]
+
+
+def run_e2e_only(args):
+    """The end-to-end leg alone (sgemm_f32_host on pinned host buffers of the
+    named workload, --warmup untimed then --steps timed calls), for profiling
+    its pipeline of copies and products; prints one diagnostic JSON line."""
+    import torch
+
+    import dense_fp32_gemm_f32_gb300 as g
+
+    torch.cuda.set_device(0)
+    p = PROBLEMS[args.workload]
+    A_cpu, B_cpu = problem_operands(p)
+    A_pin, B_pin = A_cpu.pin_memory(), B_cpu.pin_memory()
+    C_pin = torch.empty((p.M, p.N), dtype=torch.float32, pin_memory=True)
+    for _ in range(args.warmup):
+        g.sgemm_f32_host(A_pin, B_pin, C_pin)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        g.sgemm_f32_host(A_pin, B_pin, C_pin)
+    dt = (time.perf_counter() - t0) / args.steps
+    print(json.dumps({"leg": "e2e", "workload": p.name, "ms_per_step": 1e3 * dt,
+                      "tflops": p.flops / dt / 1e12, "steps": args.steps, "warmup": args.warmup}), flush=True)
+    return 0
 
 
 def run_cpu_table(args):
@@ -687,12 +713,16 @@ def main(argv=None):
     ap.add_argument("--cpu-table", action="store_true",
                     help="time the oracle on every named problem, all cores and one core (host only)")
     ap.add_argument("--cpu-seconds", type=float, default=4.0, help="bounded sample per --cpu-table entry")
+    ap.add_argument("--e2e-only", action="store_true",
+                    help="time only the end-to-end leg (host buffers) of --workload; a diagnostic line")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     rank, world, local_rank = dist_env()
     if args.sweep:
         return run_sweep(args)
+    if args.e2e_only:
+        return run_e2e_only(args)
     if args.cpu_table:
         return run_cpu_table(args)
     if world > 1:
