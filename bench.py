@@ -615,6 +615,11 @@ SWEEP_OPTIONS = [
     {"split_k": 8},
     {"tail_split": 4},
     {"stream_k": 2},
+    {"tile_k": 16},
+    {"tile_k": 16, "stages": 2},
+    {"tile_k": 16, "stages": 6},
+    {"group_m": 1},
+    {"l2_hint": 2},
 ]
 
 

@@ -46,6 +46,7 @@ class Options(ctypes.Structure):
         ("a_layout", _i),
         ("group_m", _i),
         ("l2_hint", _i),
+        ("tile_k", _i),
     ]
 
 

@@ -145,10 +145,11 @@ int run_ffma(int M, int N, int K, const float* A, int lda, const float* B, int l
     }
     if (is_tma(pl.producer)) {
         rc = pl.a_mn ? encode_2d(&tmA, A, M, K, lda, kBM, kBK, CU_TENSOR_MAP_SWIZZLE_NONE)  // {m, k} boxes of 128 x 32
-                     : encode_2d(&tmA, A, K, M, lda, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B);
+             : pl.bk == kBK16 ? encode_2d(&tmA, A, K, M, lda, kBK16, kBM, CU_TENSOR_MAP_SWIZZLE_64B)
+                              : encode_2d(&tmA, A, K, M, lda, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B);
         if (rc == SGEMM_OK)
             rc = pl.b_nk ? encode_2d(&tmB, B, K, N, ldb, kBK, kBN, CU_TENSOR_MAP_SWIZZLE_128B)  // {k, n} boxes of 32 x 128
-                         : encode_2d(&tmB, B, N, K, ldb, pl.bn, kBK, CU_TENSOR_MAP_SWIZZLE_NONE);
+                         : encode_2d(&tmB, B, N, K, ldb, pl.bn, pl.bk, CU_TENSOR_MAP_SWIZZLE_NONE);
         if (rc != SGEMM_OK) {
             release_pack();
             return rc;

@@ -213,6 +213,7 @@ struct Plan {
     int repack = 0;       // operands copied to 16-byte pitched rows first: bit 0 = A, bit 1 = B
     bool a_mn = false;    // A stored transposed (K x M): the transposed-A kernels
     bool b_nk = false;    // B stored transposed (N x K): the kernels with a B-transposing warp
+    int bk = kBK;         // K slice depth (32, or 16 for sgemm_options.tile_k = 16)
 };
 
 // Epilogue scaling of the general entry: C = alpha * A B + beta * C.

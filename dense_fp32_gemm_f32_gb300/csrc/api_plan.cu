@@ -54,7 +54,7 @@ int validate(int M, int N, int K, const float* A, int lda, const float* B, int l
 
 bool options_force_variant(const sgemm_options* opt) {
     return opt && (opt->producer || opt->split_k || opt->multicast || opt->math || opt->stages || opt->tail_split ||
-                   opt->stream_k || opt->tile_n || opt->repack || opt->group_m || opt->l2_hint);
+                   opt->stream_k || opt->tile_n || opt->repack || opt->group_m || opt->l2_hint || opt->tile_k);
 }
 
 // 0 = keep A as stored, 1 = copy it transposed; -1 = invalid option.
@@ -76,7 +76,8 @@ KernelEntry ffma_kernel(const Plan& pl) {
                         : pl.producer == kProducerTmaWg ? ffma_kernel_tma_wide_amn(pl.stages, pl.math)
                                                         : KernelEntry{nullptr, 0, 0};
     if (pl.producer == kProducerFused) return ffma_kernel_tma_fused(pl.stages, pl.math);
-    if (pl.producer == kProducerTmaX) return ffma_kernel_tma_x(pl.stages, pl.math, false);
+    if (pl.producer == kProducerTmaX)
+        return pl.bk == kBK16 ? ffma_kernel_tma_x16(pl.stages, pl.math) : ffma_kernel_tma_x(pl.stages, pl.math, false);
     if (pl.bn == kBNWide) return pl.producer == kProducerTmaWg ? ffma_kernel_tma_wide(pl.stages, pl.math)
                                                                 : KernelEntry{nullptr, 0, 0};
     switch (pl.producer) {
@@ -121,7 +122,12 @@ int make_plan(const DeviceState& st, int M, int N, int K, const float* A, int ld
                  (opt && (opt->producer || (opt->tile_n && opt->tile_n != kBNWide) || opt->math || opt->stages))))
         return SGEMM_ERR_INVALID_ARG;
     pl.a_mn = a_mn;
-    pl.num_k_tiles = static_cast<int>(ceil_div(K, kBK));
+    // K slice depth: 32, or 16 when forced (the transposing producer only).
+    const int want_bk = opt ? opt->tile_k : 0;
+    if (want_bk != 0 && want_bk != kBK && want_bk != kBK16) return SGEMM_ERR_INVALID_ARG;
+    pl.bk = want_bk == kBK16 ? kBK16 : kBK;
+    if (pl.bk == kBK16 && (a_mn || b_nk)) return SGEMM_ERR_INVALID_ARG;
+    pl.num_k_tiles = static_cast<int>(ceil_div(K, pl.bk));
     long long tiles_n = ceil_div(N, kBN);
     const long long tiles_m = ceil_div(M, kBM);
 
@@ -156,8 +162,9 @@ int make_plan(const DeviceState& st, int M, int N, int K, const float* A, int ld
     } else if (want_prod == SGEMM_PRODUCER_AUTO) {
         // Tensor maps: A transposed in shared memory, unless it already is in
         // HBM (a_mn) or another choice rules the transposing warps out.
+        const int max_x_stages = (opt && opt->tile_k == kBK16) ? 6 : 4;
         const bool x_ok = !a_mn && !(opt && ((opt->tile_n && opt->tile_n != kBN) ||
-                                             (opt->stages && (opt->stages < 2 || opt->stages > 4))));
+                                             (opt->stages && (opt->stages < 2 || opt->stages > max_x_stages))));
         // (b_nk: B is aligned, checked above; A is aligned or repacked.)
         pl.producer = !aligned ? kProducerCpAsync : x_ok ? kProducerTmaX : kProducerTma;
     } else {
@@ -205,9 +212,14 @@ int make_plan(const DeviceState& st, int M, int N, int K, const float* A, int ld
         pl.stages = 4;
     }
     if (pl.producer == kProducerFused && !(opt && opt->stages)) pl.stages = 4;
-    if ((pl.bn == kBNWide || pl.bn == kBNFused || pl.producer == kProducerTmaX) && (pl.stages < 2 || pl.stages > 4))
+    // (16-deep slices: 4 stages by default, the same 64 k of lookahead as two
+    // 32-deep ones; up to 6.)
+    if (pl.bk == kBK16 && !(opt && opt->stages)) pl.stages = 4;
+    if ((pl.bn == kBNWide || pl.bn == kBNFused || pl.producer == kProducerTmaX) &&
+        (pl.stages < 2 || pl.stages > (pl.producer == kProducerTmaX && pl.bk == kBK16 ? 6 : 4)))
         return SGEMM_ERR_INVALID_ARG;
     if (pl.producer == kProducerTmaX && pl.bn != kBN) return SGEMM_ERR_INVALID_ARG;
+    if (pl.bk == kBK16 && (pl.producer != kProducerTmaX || pl.stages == 5)) return SGEMM_ERR_INVALID_ARG;
     // CTAs that can be resident at once, for the stream-K grid.
     const int per_sm = pl.producer == kProducerFused ? st.fused_per_sm[pl.stages] : 1;
     if (per_sm < 1) return SGEMM_ERR_UNSUPPORTED;
@@ -352,7 +364,9 @@ const char* describe_plan(const Plan& pl) {
     if (pl.a_mn && n > 0 && n < static_cast<int>(sizeof buf))
         n += std::snprintf(buf + n, sizeof buf - n, "/at");
     if (pl.b_nk && n > 0 && n < static_cast<int>(sizeof buf))
-        std::snprintf(buf + n, sizeof buf - n, "/bt");
+        n += std::snprintf(buf + n, sizeof buf - n, "/bt");
+    if (pl.bk != kBK && n > 0 && n < static_cast<int>(sizeof buf))
+        std::snprintf(buf + n, sizeof buf - n, "/k%d", pl.bk);
     return buf;
 }
 
@@ -371,7 +385,7 @@ bool small_problem(const DeviceState& st, int M, int N, int K) {
 // stages, split or tile options, and no waits for debug_skip_stage to time out).
 bool small_forced_ok(const sgemm_options* opt) {
     return !(opt->split_k || opt->multicast || opt->math || opt->stages || opt->tail_split || opt->stream_k ||
-             opt->group_m || opt->l2_hint ||
+             opt->group_m || opt->l2_hint || opt->tile_k ||
              opt->tile_n || opt->repack || opt->a_layout || opt->debug_skip_stage);
 }
 

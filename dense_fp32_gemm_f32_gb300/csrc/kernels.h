@@ -35,6 +35,9 @@ KernelEntry ffma_kernel_scaled(int producer, int stages, int math);
 // Transposed-A FFMA kernels (A stored K x M): TMA producer, 2 stages, paired
 // FMA, 128 x 128 tiles; `scaled` selects the scaled epilogue.
 KernelEntry ffma_kernel_amn(int stages, int math, bool scaled);
+// FFMA kernels with A transposed in shared memory on 16-deep K slices
+// (128 x 128 tiles, paired FMA, plain epilogue); stages in {2,3,4,6}.
+KernelEntry ffma_kernel_tma_x16(int stages, int math);
 // FFMA kernels on B stored N x K (op(B) = B^T, read in place and transposed
 // in shared memory by a producer warp): A stored M x K (transposed in shared
 // memory too) or, with `a_mn`, K x M; 2 stages, paired FMA, 128 x 128 tiles;

@@ -132,13 +132,20 @@ __host__ __device__ constexpr int ffma_threads() {
 constexpr int kBNWide = 256;  // wide tile: 128 x 256, 8 x 16 per thread (producer warpgroup only)
 constexpr int kBNFused = 64;  // 128 x 64 tiles of the fused-producer CTAs
 constexpr int kStageABytes = kBM * kBK * 4;      // 16 KiB, 128-byte swizzled rows of 32 floats
-template <int BN>
-__host__ __device__ constexpr int ffma_stage_b_bytes() {
-    return kBK * BN * 4;  // plain rows of BN floats
+// BK = 16 (the tile_k = 16 variant): A slices of 128 rows of 16 floats,
+// 64-byte swizzled; B slices of 16 rows.
+constexpr int kBK16 = 16;
+template <int BK = kBK>
+__host__ __device__ constexpr int ffma_stage_a_bytes() {
+    return kBM * BK * 4;
 }
-template <int BN>
+template <int BN, int BK = kBK>
+__host__ __device__ constexpr int ffma_stage_b_bytes() {
+    return BK * BN * 4;  // plain rows of BN floats
+}
+template <int BN, int BK = kBK>
 __host__ __device__ constexpr int ffma_stage_bytes() {
-    return kStageABytes + ffma_stage_b_bytes<BN>();
+    return ffma_stage_a_bytes<BK>() + ffma_stage_b_bytes<BN, BK>();
 }
 template <int BN>
 __host__ __device__ constexpr int ffma_partial_bytes() {
@@ -156,7 +163,7 @@ struct FfmaParams {
     long long ldb;
     float* C;
     long long ldc;
-    int num_k_tiles;       // ceil(K / kBK)
+    int num_k_tiles;       // ceil(K / BK): K slices
     int split;             // CTAs per cluster along K (== gridDim.z); 1 = no split
     int vec_store;         // C base 16-byte aligned and ldc % 4 == 0
     int tile_base;         // linear index of this launch's first output tile
@@ -190,26 +197,27 @@ constexpr int kMaxSmemBytes = 232448;
 
 // XA: the stage also holds the transposed copy of its A slice (kProducerTmaX);
 // XB: and of its B slice (BNK).
-template <int STAGES, int BN = kBN, bool XA = false, bool XB = false>
+template <int STAGES, int BN = kBN, bool XA = false, bool XB = false, int BK = kBK>
 __host__ __device__ constexpr int ffma_ring_bytes() {
-    return STAGES * (ffma_stage_bytes<BN>() + (XA ? kStageABytes : 0) + (XB ? ffma_stage_b_bytes<BN>() : 0)) >
-                   ffma_partial_bytes<BN>()
-               ? STAGES * (ffma_stage_bytes<BN>() + (XA ? kStageABytes : 0) + (XB ? ffma_stage_b_bytes<BN>() : 0))
+    return STAGES * (ffma_stage_bytes<BN, BK>() + (XA ? ffma_stage_a_bytes<BK>() : 0) +
+                     (XB ? ffma_stage_b_bytes<BN, BK>() : 0)) > ffma_partial_bytes<BN>()
+               ? STAGES * (ffma_stage_bytes<BN, BK>() + (XA ? ffma_stage_a_bytes<BK>() : 0) +
+                           (XB ? ffma_stage_b_bytes<BN, BK>() : 0))
                : ffma_partial_bytes<BN>();
 }
 
 // The kernels of the transposing producer with the plain epilogue write each
 // finished tile of C by a tensor-map store from a staging tile in shared
 // memory (when C's base and rows are 16-byte aligned), where it fits.
-template <int STAGES, int PRODUCER, int BN, bool SCALED, bool BNK>
+template <int STAGES, int PRODUCER, int BN, bool SCALED, bool BNK, int BK = kBK>
 __host__ __device__ constexpr bool ffma_tma_store() {
     return PRODUCER == kProducerTmaX && BN == kBN && !SCALED &&
-           ffma_ring_bytes<STAGES, BN, true, BNK>() + ffma_partial_bytes<BN>() + 1024 + 256 <= kMaxSmemBytes;
+           ffma_ring_bytes<STAGES, BN, true, BNK, BK>() + ffma_partial_bytes<BN>() + 1024 + 256 <= kMaxSmemBytes;
 }
 
-template <int STAGES, int BN = kBN, bool XA = false, bool XB = false, bool STG = false>
+template <int STAGES, int BN = kBN, bool XA = false, bool XB = false, bool STG = false, int BK = kBK>
 constexpr int ffma_smem_bytes() {
-    return ffma_ring_bytes<STAGES, BN, XA, XB>() + (STG ? ffma_partial_bytes<BN>() : 0) + 1024 /*align*/ +
+    return ffma_ring_bytes<STAGES, BN, XA, XB, BK>() + (STG ? ffma_partial_bytes<BN>() : 0) + 1024 /*align*/ +
            256 /*barriers*/;
 }
 
@@ -256,7 +264,13 @@ __device__ __forceinline__ uint32_t swz128(int r, int c) {
 // entry's op(B) = B^T).  The TMA lands each stage's B slice as 128 rows (n)
 // of 32 k with the 128-byte swizzle, and a transposing producer warp rewrites
 // it as 32 rows (k) of 128 n, the layout the consumers read.
-template <int STAGES, int PRODUCER, int MATH, int BN = kBN, bool SCALED = false, bool AMN = false, bool BNK = false>
+//
+// BK: depth of a K slice, 32 (A slices of 128-byte rows, 128-byte swizzle)
+// or 16 (64-byte rows, 64-byte swizzle; the transposing producer on A and B
+// as stored only): half the shared memory per stage and twice the slices, so
+// that small problems' work divides into finer stream-K units.
+template <int STAGES, int PRODUCER, int MATH, int BN = kBN, bool SCALED = false, bool AMN = false, bool BNK = false,
+          int BK = kBK>
 __global__ void __launch_bounds__(ffma_threads<PRODUCER, BNK>(), ffma_min_blocks<PRODUCER>())
     sgemm_ffma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                       const __grid_constant__ CUtensorMap tmC, const FfmaParams p) {
@@ -276,8 +290,11 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER, BNK>(), ffma_min_blocks
     static_assert((BN == kBN && !kFused) || (BN == kBNWide && PRODUCER == kProducerTmaWg) ||
                       (BN == kBNFused && kFused),
                   "tile width");
-    constexpr int kStageBBytes = ffma_stage_b_bytes<BN>();
-    constexpr int kStageBytes = ffma_stage_bytes<BN>();
+    static_assert(BK == kBK || (BK == kBK16 && PRODUCER == kProducerTmaX && !BNK && BN == kBN),
+                  "16-deep slices: the transposing producer on A and B as stored");
+    constexpr int kStageABytes = ffma_stage_a_bytes<BK>();  // (shadows the 32-deep figure)
+    constexpr int kStageBBytes = ffma_stage_b_bytes<BN, BK>();
+    constexpr int kStageBytes = ffma_stage_bytes<BN, BK>();
     constexpr int kPartialBytes = ffma_partial_bytes<BN>();
     constexpr int CW = ffma_consumer_warps<PRODUCER>();  // computing warps
     constexpr int CT = 32 * CW;                          // computing threads
@@ -289,9 +306,9 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER, BNK>(), ffma_min_blocks
     const uint32_t raw_base = smem_addr(smem_raw);
     const uint32_t base = (raw_base + 1023u) & ~1023u;
     uint8_t* const smem = smem_raw + (base - raw_base);
-    constexpr int kRingBytes = ffma_ring_bytes<STAGES, BN, kX, BNK>();
+    constexpr int kRingBytes = ffma_ring_bytes<STAGES, BN, kX, BNK, BK>();
     // Staging tile of the tensor-map stores of C, after the ring.
-    constexpr bool kStg = ffma_tma_store<STAGES, PRODUCER, BN, SCALED, BNK>();
+    constexpr bool kStg = ffma_tma_store<STAGES, PRODUCER, BN, SCALED, BNK, BK>();
     constexpr int kStgOff = kRingBytes;
     // Ring: A slices (as loaded), [transposed A slices], B slices (as
     // loaded), [transposed B slices].
@@ -424,9 +441,12 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER, BNK>(), ffma_min_blocks
                     for (int qq = 0; qq < qn; ++qq) {
                         const int m = lane + 32 * (q0 + qq);
 #pragma unroll
-                        for (int c = 0; c < 8; ++c) {
-                            const float4 v =
-                                *reinterpret_cast<const float4*>(raw + m * 128 + (((c ^ m) & 7) << 4));
+                        for (int c = 0; c < BK / 4; ++c) {
+                            // 16-byte chunk c of row m: the 128-byte swizzle
+                            // XORs the chunk index with m mod 8, the 64-byte
+                            // one with (m / 2) mod 4.
+                            const int pc = BK == kBK ? ((c ^ m) & 7) : ((c ^ (m >> 1)) & 3);
+                            const float4 v = *reinterpret_cast<const float4*>(raw + m * (BK * 4) + (pc << 4));
                             tr[(4 * c + 0) * kBM + m] = v.x;
                             tr[(4 * c + 1) * kBM + m] = v.y;
                             tr[(4 * c + 2) * kBM + m] = v.z;
@@ -464,7 +484,7 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER, BNK>(), ffma_min_blocks
                     break;
                 }
                 if (skip_here && it == p.skip_stage - 1) continue;
-                const int k0 = kt * kBK;
+                const int k0 = kt * BK;
                 if (kTma) {
                     mbar_arrive_expect_tx(full_bar(s), kStageBytes);
                     if (AMN) {
@@ -497,7 +517,7 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER, BNK>(), ffma_min_blocks
                     }
                     // B slice: 32 rows x 128 floats; lane = column within a
                     // 32-wide strip, warp pw takes rows pw, pw + PW, ...
-                    for (int r = pw; r < kBK; r += PW) {
+                    for (int r = pw; r < BK; r += PW) {
                         const int k = k0 + r;
                         const bool kin = k < p.K;
 #pragma unroll
@@ -771,7 +791,7 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER, BNK>(), ffma_min_blocks
                 return;
             }
             if (!(skip_here && loads == p.skip_stage - 1)) {
-                const int k0 = lkt * kBK;
+                const int k0 = lkt * BK;
                 mbar_arrive_expect_tx(full_bar(s), kStageBytes);
                 int tm_, tn_;
                 tile_rc(ltile, p.tiles_n, p.tiles_m, p.group_m, tm_, tn_);
@@ -813,7 +833,7 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER, BNK>(), ffma_min_blocks
                 const uint8_t* sa = smem_a + s * kStageABytes;
                 const uint8_t* sb = smem_b + s * kStageBBytes;
 #pragma unroll
-                for (int kg = 0; kg < kBK / 4; ++kg) {
+                for (int kg = 0; kg < BK / 4; ++kg) {
                     const uint32_t xe = static_cast<uint32_t>(((kg ^ tm) & 7) << 4);
                     const uint32_t xo = xe ^ 64u;
                     float4 a[8];

@@ -344,6 +344,11 @@ typedef struct sgemm_options {
                              loaded with the L2 evict-last policy (the A row
                              panels of a tile group stay in L2 across its
                              waves); tensor-map producers on A as stored */
+    int tile_k;           /* 0 = auto (32), 32, or 16: depth of the K slices
+                             the pipeline stages hold (16: the transposing
+                             producer, SGEMM_PRODUCER_TMA_X, only; A slices
+                             of 64-byte rows with the 64-byte swizzle; 2, 3,
+                             4 (default) or 6 stages) */
 } sgemm_options;
 
 /* sgemm_f32 with forced choices.  Same contract; an unsupported combination

@@ -107,6 +107,10 @@ VARIANTS = (
     + [dict(group_m=gm) for gm in (1, 2)]
     + [dict(group_m=2, stream_k=2), dict(group_m=2, split_k=2), dict(group_m=2, producer=4),
        dict(group_m=2, tile_n=256, split_k=1)]
+    # 16-deep K slices (the transposing producer): stages, schedules
+    + [dict(tile_k=16, stages=s) for s in (2, 3, 4, 6)]
+    + [dict(tile_k=16, split_k=2), dict(tile_k=16, stream_k=1, split_k=1), dict(tile_k=16, stream_k=2),
+       dict(tile_k=16, group_m=1)]
     # A's slices with the L2 evict-last policy
     + [dict(l2_hint=h) for h in (1, 2)] + [dict(l2_hint=2, group_m=2, stream_k=2), dict(l2_hint=2, producer=1)]
     # producer warpgroup with the setmaxnreg register split
@@ -203,6 +207,30 @@ def test_tile_order_every_element(group_m):
     Ai, Bi = make_operands(3000, 2500, 256, "int", 42)
     check(run(Ai, Bi, group_m=group_m), oracle.gemm_f64(Ai.numpy(), Bi.numpy(), with_bound=False)[0], None,
           exact=True, what=f"group_m={group_m} int")
+
+
+@pytest.mark.parametrize("shape", [(1024, 1024, 1024), (1000, 1001, 1000), (640, 768, 2000), (4096, 4096, 4096)])
+def test_sixteen_deep_slices_every_element(shape):
+    """tile_k = 16 (64-byte swizzled A slices, 16 k per stage) against the
+    oracle on square, ragged (K = 1000: a last slice of 8 k) and stream-K
+    shapes; integer inputs exactly."""
+    M, N, K = shape
+    A, B = make_operands(M, N, K, "uniform", 43)
+    ldb = (N + 3) // 4 * 4  # 16-byte rows of B: the tensor-map kernels
+    C64, bound = oracle.gemm_f64(A.numpy(), B.numpy())
+    check(run(A, B, ldb=ldb, tile_k=16), C64, bound, exact=False, what=f"tile_k=16 {shape}")
+    Ai, Bi = make_operands(M, N, K, "int", 44)
+    check(run(Ai, Bi, ldb=ldb, tile_k=16), oracle.gemm_f64(Ai.numpy(), Bi.numpy(), with_bound=False)[0], None,
+          exact=True, what=f"tile_k=16 {shape} int")
+
+
+def test_sixteen_deep_slices_refusals():
+    A, B = make_operands(512, 512, 512, "uniform", 45)
+    for bad in (dict(tile_k=8), dict(tile_k=64), dict(tile_k=16, producer=1), dict(tile_k=16, stages=5),
+                dict(tile_k=16, tile_n=256)):
+        with pytest.raises(g.SgemmError) as e:
+            run(A, B, **bad)
+        assert e.value.status == 1, bad
 
 
 def test_forced_tma_rejects_unaligned_rows():
