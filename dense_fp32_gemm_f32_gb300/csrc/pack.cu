@@ -27,22 +27,36 @@ struct PackJob {
     int rows, cols;
 };
 
-// Job blockIdx.z: dst row r, floats [c4, c4 + 4) <- src row r, the same
-// columns (zeros past `cols`, i.e. in the pitch padding).  Reads are
-// coalesced scalar loads (the source rows have any alignment), writes 16-byte
-// stores.
+// Job blockIdx.z, rows [kPackRows * blockIdx.x, + kPackRows): dst row r,
+// floats [c4, c4 + 4) <- src row r, the same columns (zeros past `cols`, i.e.
+// in the pitch padding), for every 4-float group c4 of the dst row, threads
+// striding along the row.  Reads are coalesced scalar loads (the source rows
+// have any alignment), writes 16-byte stores; the loads of the CTA's rows
+// are all issued before the first store, so that a CTA waits one memory
+// round trip per group of rows rather than one per row.
+constexpr int kPackRows = 4;
+
 __global__ void __launch_bounds__(kPackThreads) pack_rows_kernel(const PackJob j0, const PackJob j1) {
     const PackJob& j = blockIdx.z == 0 ? j0 : j1;
-    const long long c4 = (static_cast<long long>(blockIdx.x) * kPackThreads + threadIdx.x) * 4;
-    if (c4 >= j.ld_dst) return;
-    for (long long r = blockIdx.y; r < j.rows; r += gridDim.y) {
-        const float* s = j.src + r * j.ld_src;
-        float4 v;
-        v.x = c4 + 0 < j.cols ? s[c4 + 0] : 0.f;
-        v.y = c4 + 1 < j.cols ? s[c4 + 1] : 0.f;
-        v.z = c4 + 2 < j.cols ? s[c4 + 2] : 0.f;
-        v.w = c4 + 3 < j.cols ? s[c4 + 3] : 0.f;
-        *reinterpret_cast<float4*>(j.dst + r * j.ld_dst + c4) = v;
+    const long long r0 = static_cast<long long>(blockIdx.x) * kPackRows;
+    if (r0 >= j.rows) return;
+    const long long groups = j.ld_dst / 4;
+    for (long long q = threadIdx.x; q < groups; q += kPackThreads) {
+        const long long c4 = 4 * q;
+        float4 v[kPackRows];
+#pragma unroll
+        for (int i = 0; i < kPackRows; ++i) {
+            v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (r0 + i >= j.rows) continue;
+            const float* s = j.src + (r0 + i) * j.ld_src;
+            if (c4 + 0 < j.cols) v[i].x = s[c4 + 0];
+            if (c4 + 1 < j.cols) v[i].y = s[c4 + 1];
+            if (c4 + 2 < j.cols) v[i].z = s[c4 + 2];
+            if (c4 + 3 < j.cols) v[i].w = s[c4 + 3];
+        }
+#pragma unroll
+        for (int i = 0; i < kPackRows; ++i)
+            if (r0 + i < j.rows) *reinterpret_cast<float4*>(j.dst + (r0 + i) * j.ld_dst + c4) = v[i];
     }
 }
 
@@ -96,16 +110,13 @@ int pack_rows(const float* src0, long long ld_src0, float* dst0, long long ld_ds
     if (n == 0) return SGEMM_OK;
     if (n == 1) use[1] = use[0];
     long long gx = 0;
-    int gy = 0;
     for (int i = 0; i < n; ++i) {
-        const long long x = (use[i].ld_dst / 4 + kPackThreads - 1) / kPackThreads;
+        const long long x = (static_cast<long long>(use[i].rows) + kPackRows - 1) / kPackRows;
         gx = x > gx ? x : gx;
-        const int y = use[i].rows < 65535 ? use[i].rows : 65535;
-        gy = y > gy ? y : gy;
     }
     if (gx > 0x7fffffffLL) return SGEMM_ERR_INVALID_ARG;
-    pack_rows_kernel<<<dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy), static_cast<unsigned>(n)),
-                       kPackThreads, 0, stream>>>(use[0], use[1]);
+    pack_rows_kernel<<<dim3(static_cast<unsigned>(gx), 1, static_cast<unsigned>(n)), kPackThreads, 0, stream>>>(
+        use[0], use[1]);
     if (cudaGetLastError() != cudaSuccess) return SGEMM_ERR_CUDA;
     return SGEMM_OK;
 }
