@@ -604,6 +604,8 @@ SWEEP_OPTIONS = [
     {"tile_n": 64, "stages": 2},
     {"tile_n": 64, "split_k": 1},
     {"repack": 1},
+    {"repack": 2},
+    {"producer": 7},
     {"a_layout": 1},
     {"a_layout": 2, "tile_n": 256},
     {"producer": 5},

@@ -115,7 +115,7 @@ int run_ffma(int M, int N, int K, const float* A, int lda, const float* B, int l
     const KernelEntry k = pl.b_nk ? ffma_kernel_bnk(pl.a_mn, scaled)
                           : pl.a_mn ? (pl.bn == kBN ? ffma_kernel_amn(pl.stages, pl.math, scaled)
                                                   : scaled ? KernelEntry{nullptr, 0, 0} : ffma_kernel(pl))
-                          : scaled ? (pl.producer == kProducerTmaX ? ffma_kernel_tma_x(pl.stages, pl.math, true)
+                          : scaled ? (pl.producer == kProducerTmaX  ? ffma_kernel_tma_x(pl.stages, pl.math, true)
                                       : pl.bn == kBN               ? ffma_kernel_scaled(pl.producer, pl.stages, pl.math)
                                                                    : KernelEntry{nullptr, 0, 0})
                                    : ffma_kernel(pl);
@@ -172,6 +172,7 @@ int run_ffma(int M, int N, int K, const float* A, int lda, const float* B, int l
     prm.tiles_m = pl.tiles_m;
     prm.group_m = pl.group_m;
     prm.a_evict_last = pl.a_evict_last;
+    prm.b_evict_first = pl.b_evict_first;
     prm.tma_store = (k.tma_store && c_aligned) ? 1 : 0;
     prm.skip_stage = opt ? opt->debug_skip_stage : 0;
     prm.timeout_ns = (opt && opt->timeout_ns) ? opt->timeout_ns : kDefaultTimeoutNs;
@@ -340,6 +341,7 @@ int run_ffma_noalloc(int M, int N, int K, const float* A, int lda, const float* 
     prm.tiles_m = pl.tiles_m;
     prm.group_m = pl.group_m;
     prm.a_evict_last = pl.a_evict_last;
+    prm.b_evict_first = pl.b_evict_first;
     prm.tma_store = c_tma ? 1 : 0;
     prm.timeout_ns = kDefaultTimeoutNs;
     prm.status = st->status_word;

@@ -76,6 +76,7 @@ KernelEntry ffma_kernel(const Plan& pl) {
                         : pl.producer == kProducerTmaWg ? ffma_kernel_tma_wide_amn(pl.stages, pl.math)
                                                         : KernelEntry{nullptr, 0, 0};
     if (pl.producer == kProducerFused) return ffma_kernel_tma_fused(pl.stages, pl.math);
+    if (pl.producer == kProducerLdg) return ffma_kernel_ldg(pl.stages, pl.math);
     if (pl.producer == kProducerTmaX)
         return pl.bk == kBK16 ? ffma_kernel_tma_x16(pl.stages, pl.math) : ffma_kernel_tma_x(pl.stages, pl.math, false);
     if (pl.bn == kBNWide) return pl.producer == kProducerTmaWg ? ffma_kernel_tma_wide(pl.stages, pl.math)
@@ -95,6 +96,7 @@ const char* producer_name(int producer) {
         case kProducerFused: return "fused";
         case kProducerTmaX: return "tmax";
         case kProducerCpAsync: return "cpasync";
+        case kProducerLdg: return "ldg";
     }
     return "?";
 }
@@ -133,7 +135,12 @@ int make_plan(const DeviceState& st, int M, int N, int K, const float* A, int ld
 
     // Producer: tensor maps need 16-byte aligned bases and row strides, and
     // K > 0.  An operand without them is either repacked into pitched rows
-    // (which the tensor maps can address) or read by the cp.async producer.
+    // (which the tensor maps can address) or read by the cp.async producer;
+    // the loader warps (kProducerLdg) read any alignment too, but only when
+    // forced: measured on GB300 they run at 19-25 TFLOP/s on 1023 x 1025 x
+    // 1027 ... 8191 x 8193 x 8195 with 2, 3 or 4 stages alike, against 35-67
+    // repacked and 32-50 with cp.async (each slice's row loads cost them a
+    // memory round trip that the consumers' 2 us per slice does not cover).
     const int want_prod = opt ? opt->producer : 0;
     const int want_repack = opt ? opt->repack : 0;
     if (want_repack < 0 || want_repack > 2) return SGEMM_ERR_INVALID_ARG;
@@ -159,6 +166,9 @@ int make_plan(const DeviceState& st, int M, int N, int K, const float* A, int ld
         pl.producer = kProducerFused;
     } else if (want_prod == SGEMM_PRODUCER_CPASYNC) {
         pl.producer = kProducerCpAsync;
+    } else if (want_prod == SGEMM_PRODUCER_LDG) {
+        if (K == 0 || a_mn || b_nk) return SGEMM_ERR_INVALID_ARG;
+        pl.producer = kProducerLdg;
     } else if (want_prod == SGEMM_PRODUCER_AUTO) {
         // Tensor maps: A transposed in shared memory, unless it already is in
         // HBM (a_mn) or another choice rules the transposing warps out.
@@ -202,7 +212,7 @@ int make_plan(const DeviceState& st, int M, int N, int K, const float* A, int ld
     // paired-FMA consumers: 0.3-2 % faster than 3-6 at every named problem,
     // 20-25 % faster than one), four for cp.async, whose 4-byte copies have
     // more latency to hide.
-    pl.stages = pl.producer == kProducerCpAsync ? 4 : 2;
+    pl.stages = pl.producer == kProducerCpAsync ? 4 : pl.producer == kProducerLdg ? 3 : 2;
     if (opt && opt->stages) {
         if (opt->stages < 1 || opt->stages > 6) return SGEMM_ERR_INVALID_ARG;
         pl.stages = opt->stages;
@@ -219,6 +229,8 @@ int make_plan(const DeviceState& st, int M, int N, int K, const float* A, int ld
         (pl.stages < 2 || pl.stages > (pl.producer == kProducerTmaX && pl.bk == kBK16 ? 6 : 4)))
         return SGEMM_ERR_INVALID_ARG;
     if (pl.producer == kProducerTmaX && pl.bn != kBN) return SGEMM_ERR_INVALID_ARG;
+    if (pl.producer == kProducerLdg && (pl.bn != kBN || pl.bk != kBK || pl.stages < 2 || pl.stages > 4))
+        return SGEMM_ERR_INVALID_ARG;
     if (pl.bk == kBK16 && (pl.producer != kProducerTmaX || pl.stages == 5)) return SGEMM_ERR_INVALID_ARG;
     // CTAs that can be resident at once, for the stream-K grid.
     const int per_sm = pl.producer == kProducerFused ? st.fused_per_sm[pl.stages] : 1;
@@ -284,8 +296,9 @@ int make_plan(const DeviceState& st, int M, int N, int K, const float* A, int ld
     pl.group_m = want_group > 0 ? want_group : static_cast<int>(auto_group);
     if (pl.group_m > pl.tiles_m) pl.group_m = pl.tiles_m > 0 ? pl.tiles_m : 1;
     const int want_hint = opt ? opt->l2_hint : 0;
-    if (want_hint < 0 || want_hint > 2) return SGEMM_ERR_INVALID_ARG;
-    pl.a_evict_last = want_hint == 2 ? 1 : 0;
+    if (want_hint < 0 || want_hint > 3) return SGEMM_ERR_INVALID_ARG;
+    pl.a_evict_last = want_hint >= 2 ? 1 : 0;
+    pl.b_evict_first = want_hint == 3 ? 1 : 0;
 
     // Last partial wave.  When the tiles do not fill a whole number of waves,
     // the last wave leaves SMs idle for a full tile time.  Those tiles can run

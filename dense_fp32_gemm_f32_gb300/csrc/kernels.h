@@ -43,6 +43,9 @@ KernelEntry ffma_kernel_tma_x16(int stages, int math);
 // memory too) or, with `a_mn`, K x M; 2 stages, paired FMA, 128 x 128 tiles;
 // `scaled` selects the scaled epilogue.
 KernelEntry ffma_kernel_bnk(bool a_mn, bool scaled);
+// FFMA kernels fed by loader warps (operands of any alignment, no tensor
+// maps): 128 x 128 tiles, paired FMA, plain epilogue; stages {2,3,4}.
+KernelEntry ffma_kernel_ldg(int stages, int math);
 // FFMA kernels fed by 4-byte cp.async (any alignment); stages in {2,4}.
 KernelEntry ffma_kernel_cpasync(int stages, int math);
 // Three-product TF32 kernel on the tensor cores (TMA-fed, 128 x 128 tiles,

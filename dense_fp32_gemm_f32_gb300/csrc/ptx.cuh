@@ -105,6 +105,13 @@ __device__ __forceinline__ uint64_t l2_policy_evict_last() {
     return p;
 }
 
+// L2 cache policy: the lines an access brings in are the first to be evicted.
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
 // 2-D tiled bulk copy this CTA's shared memory -> global through a tensor
 // map (elements outside the tensor are not written), added to the thread's
 // current bulk group.  c0 is the innermost coordinate in elements.

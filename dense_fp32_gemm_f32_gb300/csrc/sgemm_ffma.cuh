@@ -67,7 +67,14 @@ constexpr int kBK = 32;
 constexpr int kConsumerWarps = 8;
 constexpr int kConsumerThreads = kConsumerWarps * 32;
 
-enum : int { kProducerTma = 1, kProducerCpAsync = 2, kProducerTmaWg = 3, kProducerFused = 4, kProducerTmaX = 5 };
+enum : int {
+    kProducerTma = 1,
+    kProducerCpAsync = 2,
+    kProducerTmaWg = 3,
+    kProducerFused = 4,
+    kProducerTmaX = 5,
+    kProducerLdg = 7
+};
 
 // Producer warps: one elected lane drives the TMA; the cp.async producer
 // issues every 4-byte copy itself, so it gets a full warpgroup.
@@ -96,8 +103,14 @@ enum : int { kProducerTma = 1, kProducerCpAsync = 2, kProducerTmaWg = 3, kProduc
 // HBM).  Two warps, each taking half of the rows, halve the time from a
 // slice's arrival to its transposed form (measured on GB300: 4096^3 +1.6 %,
 // 1024^3 +4.7 % over one warp); 11 warps leave up to 184 registers a thread.
+// kProducerLdg: no tensor maps (operands of any alignment).  Two loader
+// warps read A's slice rows from global memory as aligned 16-byte vectors,
+// shift each row into place and store it transposed (m innermost), as the
+// transposing warps do; two more read B's slice rows the same way and store
+// them as they are.  The consumers are those of kProducerTmaX.
 // Transposing warps of kProducerTmaX (each rewrites half of the slice's rows).
 constexpr int kTransposeWarps = 2;
+constexpr int kLoaderWarpsA = 2, kLoaderWarpsB = 2;
 // BNK (B stored N x K, k innermost: the general entry's op(B) = B^T read in
 // place): one more producer warp transposes each stage's B slice (as loaded:
 // 128 rows of 32 k, 128-byte swizzled, the layout of an A slice) into rows of
@@ -109,6 +122,7 @@ __host__ __device__ constexpr int ffma_producer_warps() {
     return (PRODUCER == kProducerFused ? 0
             : PRODUCER == kProducerTma ? 1
             : PRODUCER == kProducerTmaX ? 1 + kTransposeWarps
+            : PRODUCER == kProducerLdg  ? kLoaderWarpsA + kLoaderWarpsB
                                         : 4) +
            (BNK ? kTransposeWarpsB : 0);
 }
@@ -171,6 +185,7 @@ struct FfmaParams {
     int tiles_m;           // rows of output tiles
     int group_m;           // tile order: groups of group_m rows of tiles (1 = row by row; see tile_rc)
     int a_evict_last;      // A's slices are loaded with the L2 evict-last policy
+    int b_evict_first;     // B's slices are loaded with the L2 evict-first policy
     int tma_store;         // finished tiles of C go out by tensor-map stores (kernels with a staging tile)
     // Stream-K schedule (sk != 0), one CTA per SM: CTA g first takes whole
     // tiles g, g + G, ... below sk_dp_tiles (data-parallel waves, raster
@@ -211,8 +226,10 @@ __host__ __device__ constexpr int ffma_ring_bytes() {
 // memory (when C's base and rows are 16-byte aligned), where it fits.
 template <int STAGES, int PRODUCER, int BN, bool SCALED, bool BNK, int BK = kBK>
 __host__ __device__ constexpr bool ffma_tma_store() {
-    return PRODUCER == kProducerTmaX && BN == kBN && !SCALED &&
-           ffma_ring_bytes<STAGES, BN, true, BNK, BK>() + ffma_partial_bytes<BN>() + 1024 + 256 <= kMaxSmemBytes;
+    return (PRODUCER == kProducerTmaX || PRODUCER == kProducerLdg) && BN == kBN && !SCALED &&
+           ffma_ring_bytes<STAGES, BN, PRODUCER == kProducerTmaX, BNK, BK>() + ffma_partial_bytes<BN>() + 1024 +
+                   256 <=
+               kMaxSmemBytes;
 }
 
 template <int STAGES, int BN = kBN, bool XA = false, bool XB = false, bool STG = false, int BK = kBK>
@@ -282,7 +299,9 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER, BNK>(), ffma_min_blocks
     constexpr bool kX = PRODUCER == kProducerTmaX;  // A transposed in shared memory
     static_assert(!(kX && AMN), "A is transposed either in HBM or in shared memory");
     static_assert(!kX || BN == kBN, "in-shared-memory transposition: 128 x 128 tiles");
-    constexpr bool kAT = AMN || kX;  // consumers read A with m innermost
+    constexpr bool kLdg = PRODUCER == kProducerLdg;  // loader warps, no tensor maps
+    static_assert(!kLdg || (BN == kBN && !AMN && !BNK && BK == kBK), "loader warps: 128 x 128 tiles, A, B as stored");
+    constexpr bool kAT = AMN || kX || kLdg;  // consumers read A with m innermost
     static_assert(!BNK || (BN == kBN && (PRODUCER == kProducerTmaX || (PRODUCER == kProducerTma && AMN))),
                   "B stored N x K: 128 x 128 tiles, transposing producer");
     constexpr int kXA = kX ? kTransposeWarps : 0;    // A-transposing warps
@@ -311,8 +330,9 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER, BNK>(), ffma_min_blocks
     constexpr bool kStg = ffma_tma_store<STAGES, PRODUCER, BN, SCALED, BNK, BK>();
     constexpr int kStgOff = kRingBytes;
     // Ring: A slices (as loaded), [transposed A slices], B slices (as
-    // loaded), [transposed B slices].
-    constexpr int kTOff = STAGES * kStageABytes;                       // transposed A (kX)
+    // loaded), [transposed B slices]; with loader warps, transposed A slices
+    // and B slices.
+    constexpr int kTOff = kLdg ? 0 : STAGES * kStageABytes;            // transposed A (kX, kLdg)
     constexpr int kBLoadOff = (kX ? 2 : 1) * STAGES * kStageABytes;    // B as loaded
     constexpr int kBOff = kBLoadOff + (BNK ? STAGES * kStageBBytes : 0);  // B as the consumers read it
     const uint32_t sA0 = base;                                         // STAGES x 16 KiB
@@ -322,7 +342,7 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER, BNK>(), ffma_min_blocks
     auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
     auto tfull_bar = [&](int s) { return bar0 + 8u * (2 * STAGES + s); };  // transposed A ready
 
-    constexpr bool kTma = PRODUCER != kProducerCpAsync;
+    constexpr bool kTma = PRODUCER != kProducerCpAsync && !kLdg;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     constexpr int PW = ffma_producer_warps<PRODUCER>();
@@ -408,7 +428,117 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER, BNK>(), ffma_min_blocks
         // Warpgroup-uniform (warps 8-11).  The producer releases registers
         // first; the consumers' requests are served from what it released.
         if constexpr (PRODUCER == kProducerTmaWg) setmaxnreg_dec<kRegsProducer>();
-        const bool issuer = !kTma || (pw == 0 && lane == 0);
+        const bool issuer = !kLdg && (!kTma || (pw == 0 && lane == 0));
+        if constexpr (kLdg) {
+            // Loader warps.  pw 0, 1: A's rows 64 pw + lane and 64 pw + 32 +
+            // lane of the slice; pw 2, 3: B's rows 16 (pw - 2) .. + 15.  A
+            // row's 32 floats of A (B's 128 floats) start at any 4-byte
+            // boundary: the lane reads the aligned 16-byte vectors covering
+            // them (only those holding an element inside the operand, so
+            // nothing outside its rows' extent is touched; the padding and
+            // neighbouring elements they also hold are discarded), then
+            // picks element j as element sh + j of those vectors, sh = the
+            // start's offset in floats within its 16-byte block.  Elements
+            // past M, N or K are zeros.  Every lane arrives on the slot's
+            // full barrier once its part is stored.
+            float* const trA = reinterpret_cast<float*>(smem + kTOff);
+            float* const sBp = reinterpret_cast<float*>(smem + kBLoadOff);
+            int lit = 0;
+            Work lwork = work0;
+            int ltile, lkb, lke;
+            while (!timed_out && lwork.next(ltile, lkb, lke)) {
+                int tm_, tn_;
+                tile_rc(ltile, p.tiles_n, p.tiles_m, p.group_m, tm_, tn_);
+                const int m0 = tm_ * kBM, n0 = tn_ * BN;
+                for (int kt = lkb; kt < lke; ++kt, ++lit) {
+                    const int s = lit % STAGES;
+                    const int round = lit / STAGES;
+                    if (round > 0 && !mbar_wait_bounded_warp(empty_bar(s), (round - 1) & 1, tmo)) {
+                        timed_out = true;
+                        break;
+                    }
+                    if (skip_here && lit == p.skip_stage - 1) continue;  // debug: this slice never arrives
+                    const int k0 = kt * kBK;
+                    const int kval = min(kBK, p.K - k0);  // valid k of the slice (> 0)
+                    if (pw < kLoaderWarpsA) {
+                        float4 va[2][9];
+                        int sh[2];
+#pragma unroll
+                        for (int qq = 0; qq < 2; ++qq) {
+                            const int gm = m0 + lane + 32 * (2 * pw + qq);
+                            const bool rin = gm < p.M;
+                            const uintptr_t a = reinterpret_cast<uintptr_t>(
+                                rin ? p.A + static_cast<long long>(gm) * p.lda + k0 : p.A);
+                            const float4* const src = reinterpret_cast<const float4*>(a & ~static_cast<uintptr_t>(15));
+                            sh[qq] = static_cast<int>((a >> 2) & 3);
+#pragma unroll
+                            for (int i = 0; i < 9; ++i) {
+                                const int lo = 4 * i - sh[qq];  // offset of the vector's first element
+                                va[qq][i] = (rin && lo < kval && lo + 3 >= 0) ? __ldg(src + i)
+                                                                             : make_float4(0.f, 0.f, 0.f, 0.f);
+                            }
+                        }
+                        float* const tr = trA + s * (kStageABytes / 4);
+#pragma unroll
+                        for (int qq = 0; qq < 2; ++qq) {
+                            const int m = lane + 32 * (2 * pw + qq);
+                            const int t = sh[qq];
+                            auto el = [&](int f) -> float {  // float f of the row's vectors (f static)
+                                const float4 v = va[qq][f >> 2];
+                                return (f & 3) == 0 ? v.x : (f & 3) == 1 ? v.y : (f & 3) == 2 ? v.z : v.w;
+                            };
+#pragma unroll
+                            for (int j = 0; j < kBK; ++j) {
+                                float x = t == 0 ? el(j) : t == 1 ? el(j + 1) : t == 2 ? el(j + 2) : el(j + 3);
+                                tr[j * kBM + m] = j < kval ? x : 0.f;
+                            }
+                        }
+                    } else {
+                        const int nval = min(BN, p.N - n0);  // valid columns of the tile (> 0)
+                        float* const sb = sBp + s * (kStageBBytes / 4);
+                        const int c = 4 * lane;
+#pragma unroll
+                        for (int half = 0; half < 2; ++half) {
+                            float4 v0[8], v1[8];
+                            int shb[8];
+#pragma unroll
+                            for (int r = 0; r < 8; ++r) {
+                                const int kr = 16 * (pw - kLoaderWarpsA) + 8 * half + r;
+                                const bool kin = kr < kval;
+                                const uintptr_t a = reinterpret_cast<uintptr_t>(
+                                    kin ? p.B + static_cast<long long>(k0 + kr) * p.ldb + n0 : p.B);
+                                const float4* const src =
+                                    reinterpret_cast<const float4*>(a & ~static_cast<uintptr_t>(15));
+                                shb[r] = static_cast<int>((a >> 2) & 3);
+                                const int lo0 = c - shb[r], lo1 = lo0 + 4;
+                                v0[r] = (kin && lo0 < nval && lo0 + 3 >= 0) ? __ldg(src + lane)
+                                                                            : make_float4(0.f, 0.f, 0.f, 0.f);
+                                v1[r] = (kin && shb[r] > 0 && lo1 < nval) ? __ldg(src + lane + 1)
+                                                                         : make_float4(0.f, 0.f, 0.f, 0.f);
+                            }
+#pragma unroll
+                            for (int r = 0; r < 8; ++r) {
+                                const int kr = 16 * (pw - kLoaderWarpsA) + 8 * half + r;
+                                const int t = shb[r];
+                                const float4 a0 = v0[r], a1 = v1[r];
+                                float4 o;
+                                o.x = t == 0 ? a0.x : t == 1 ? a0.y : t == 2 ? a0.z : a0.w;
+                                o.y = t == 0 ? a0.y : t == 1 ? a0.z : t == 2 ? a0.w : a1.x;
+                                o.z = t == 0 ? a0.z : t == 1 ? a0.w : t == 2 ? a1.x : a1.y;
+                                o.w = t == 0 ? a0.w : t == 1 ? a1.x : t == 2 ? a1.y : a1.z;
+                                if (c + 0 >= nval) o.x = 0.f;
+                                if (c + 1 >= nval) o.y = 0.f;
+                                if (c + 2 >= nval) o.z = 0.f;
+                                if (c + 3 >= nval) o.w = 0.f;
+                                *reinterpret_cast<float4*>(sb + kr * BN + c) = o;
+                            }
+                        }
+                    }
+                    __syncwarp();
+                    mbar_arrive(full_bar(s));  // this lane's part of the slice is stored
+                }
+            }
+        }
         if ((kXA + kXB) > 0 && pw >= 1) {
             // Transposing warps: A slice s (row m: 32 floats in 128-byte
             // swizzled chunks) -> transposed slice (row k: 128 floats); the
@@ -469,6 +599,7 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER, BNK>(), ffma_min_blocks
         // group's consecutive waves of tiles: loaded evict-last, they stay in
         // L2 while the B column panels stream past.
         const uint64_t a_policy = (kTma && p.a_evict_last) ? l2_policy_evict_last() : 0;
+        const uint64_t b_policy = (kTma && p.b_evict_first) ? l2_policy_evict_first() : 0;
         while (issuer && !timed_out && work.next(tile, kb, ke)) {
             int tm_, tn_;
             tile_rc(tile, p.tiles_n, p.tiles_m, p.group_m, tm_, tn_);
@@ -496,6 +627,8 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER, BNK>(), ffma_min_blocks
                     }
                     if (BNK) {
                         tma_load_2d(sB0 + s * kStageBBytes, &tmB, full_bar(s), k0, n0);
+                    } else if (p.b_evict_first) {
+                        tma_load_2d_hint(sB0 + s * kStageBBytes, &tmB, full_bar(s), n0, k0, b_policy);
                     } else {
                         tma_load_2d(sB0 + s * kStageBBytes, &tmB, full_bar(s), n0, k0);
                     }

@@ -266,6 +266,12 @@ enum {
                                     transpose each stage's A slice in shared memory for the
                                     consumers to read per k (the transposed-A read without a
                                     copy of A in HBM; 128 x 128 tiles, 2..4 stages) */
+    SGEMM_PRODUCER_LDG = 7,      /* no tensor maps: four producer warps read A's and B's
+                                    slice rows from global memory as aligned 16-byte vectors
+                                    (any alignment of bases and rows), shift them into place
+                                    and store A transposed (m innermost) and B as it is;
+                                    128 x 128 tiles, 2..4 stages (default 3).  Measured
+                                    slower than repacking or cp.async, so only forced */
     SGEMM_PRODUCER_SMALL = 6     /* the small-problem kernel: one 8-warp CTA per 32 x 32 tile
                                     of C, K split across its warps in 32-deep chunks and the
                                     partials summed in a fixed order; bounds-checked 4-byte
@@ -343,7 +349,9 @@ typedef struct sgemm_options {
     int l2_hint;          /* 0 = auto, 1 = no cache policy, 2 = A's slices
                              loaded with the L2 evict-last policy (the A row
                              panels of a tile group stay in L2 across its
-                             waves); tensor-map producers on A as stored */
+                             waves), 3 = that and B's slices with the
+                             evict-first policy; tensor-map producers on A
+                             and B as stored */
     int tile_k;           /* 0 = auto (32), 32, or 16: depth of the K slices
                              the pipeline stages hold (16: the transposing
                              producer, SGEMM_PRODUCER_TMA_X, only; A slices

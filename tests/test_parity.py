@@ -111,8 +111,11 @@ VARIANTS = (
     + [dict(tile_k=16, stages=s) for s in (2, 3, 4, 6)]
     + [dict(tile_k=16, split_k=2), dict(tile_k=16, stream_k=1, split_k=1), dict(tile_k=16, stream_k=2),
        dict(tile_k=16, group_m=1)]
+    # loader warps (operands of any alignment; here aligned)
+    + [dict(producer=7, stages=s) for s in (2, 3, 4)]
+    + [dict(producer=7, split_k=2), dict(producer=7, stream_k=1, split_k=1), dict(producer=7, group_m=1)]
     # A's slices with the L2 evict-last policy
-    + [dict(l2_hint=h) for h in (1, 2)] + [dict(l2_hint=2, group_m=2, stream_k=2), dict(l2_hint=2, producer=1)]
+    + [dict(l2_hint=h) for h in (1, 2, 3)] + [dict(l2_hint=2, group_m=2, stream_k=2), dict(l2_hint=3, producer=1)]
     # producer warpgroup with the setmaxnreg register split
     + [dict(producer=3, math=m, stages=s, split_k=1, multicast=1) for m in (1, 2) for s in (1, 4, 6)]
     + [dict(producer=3, math=2, split_k=s, multicast=1) for s in (2, 4)]
@@ -544,31 +547,30 @@ def test_forced_repack(case):
         check(C.cpu().numpy(), C64, bound, exact=(dist == "int"), what=f"repack {case} {dist}")
 
 
-def test_ragged_problem_without_repacking():
-    """The ragged problem with repacking off: the cp.async producer reads the
-    misaligned rows directly."""
+def test_ragged_problem_cp_async():
+    """The ragged problem on the cp.async producer (forced): 4-byte copies of
+    the misaligned rows."""
     p = PROBLEMS["ragged_1023x1025x1027"]
     A, B = problem_operands(p)
     dA, dB = to_device(A), to_device(B)
-    C = g.sgemm_f32_ex(dA, dB, repack=1)
+    C = g.sgemm_f32_ex(dA, dB, producer=2)
     torch.cuda.synchronize()
     C64, bound = oracle.gemm_f64(A.numpy(), B.numpy())
     check(C.cpu().numpy(), C64, bound, exact=False, what="ragged, cp.async")
     Ai, Bi = problem_operands(p.int_variant())
-    Ci = g.sgemm_f32_ex(to_device(Ai), to_device(Bi), repack=1)
+    Ci = g.sgemm_f32_ex(to_device(Ai), to_device(Bi), producer=2)
     torch.cuda.synchronize()
     check(Ci.cpu().numpy(), oracle.gemm_f64(Ai.numpy(), Bi.numpy(), with_bound=False)[0], None, exact=True,
           what="ragged int, cp.async")
 
 
 def test_repacked_large_ragged_sampled_rows():
-    """2047 x 2049 x 2051 (the automatic choice repacks both operands):
-    sampled full rows against the oracle."""
+    """2047 x 2049 x 2051 with both operands repacked (forced): sampled full
+    rows against the oracle."""
     M, N, K = 2047, 2049, 2051
     A, B = make_operands(M, N, K, "uniform", 93)
     dA, dB = to_device(A), to_device(B)
-    assert g.describe(dA, dB).endswith("/repackAB")
-    C = g.sgemm_f32(dA, dB)
+    C = g.sgemm_f32_ex(dA, dB, repack=2)
     torch.cuda.synchronize()
     rows = sample_rows(M, n_random=8, seed=93)
     C64, bound = oracle.gemm_rows_f64(A.numpy(), B.numpy(), rows)
@@ -584,7 +586,7 @@ def test_timeout_is_reported_and_recovers():
     A, B = make_operands(128, 256, 256, "uniform", 14)
     dA, dB = to_device(A), to_device(B)
     assert g.check_status() == 0
-    for producer in (1, 2, 4, 5):
+    for producer in (1, 2, 4, 5, 7):
         g.sgemm_f32_ex(dA, dB, producer=producer, split_k=1, debug_skip_stage=3, timeout_ns=20_000_000)
         assert g.check_status() == 4
         g.sgemm_f32_ex(dA, dB, producer=producer, stream_k=2, debug_skip_stage=1, timeout_ns=20_000_000)
@@ -736,3 +738,38 @@ def test_stream_k_scratch_more_streams_than_entries():
         C64, _ = oracle.gemm_f64(A.numpy(), B.numpy(), with_bound=False)
         check(dC.cpu().numpy(), C64, None, exact=True, what="many streams")
     assert g.check_status() == 0
+
+
+# ---------------------------------------------------------------- loader warps
+
+@pytest.mark.parametrize("shape", [(1024, 1024, 1024), (700, 900, 701), (1500, 1300, 2000)])
+def test_loader_warps_match_tensor_map_kernel_bitwise(shape):
+    """Aligned operands: the loader warps feed the consumers the same slices
+    as the tensor maps, so the result equals the transposing-producer
+    kernel's bit for bit (same schedule, same order of multiply-adds)."""
+    M, N, K = shape
+    A, B = make_operands(M, N, K, "normal", 47)
+    ldb = (N + 3) // 4 * 4
+    lda = (K + 3) // 4 * 4
+    C_ldg = run(A, B, lda=lda, ldb=ldb, producer=7)
+    C_tma = run(A, B, lda=lda, ldb=ldb, producer=5)
+    assert np.array_equal(C_ldg, C_tma)
+
+
+@pytest.mark.parametrize("offsets", [(0, 0), (1, 0), (0, 2), (3, 1), (2, 3)])
+@pytest.mark.parametrize("pads", [(0, 0), (1, 3), (5, 2)])
+def test_loader_warps_any_alignment_every_element(offsets, pads):
+    """Bases 0-3 floats off a 16-byte boundary and rows of any length (pads
+    added to K and N): every element against the oracle, integer inputs
+    exactly; M, N, K ragged against the tiles and slices."""
+    M, N, K = 777, 1153, 611
+    oa, ob = offsets
+    lda, ldb = K + pads[0], N + pads[1]
+    for dist in ("uniform", "int"):
+        A, B = make_operands(M, N, K, dist, 48)
+        dA, dB = to_device(A, lda, offset=oa), to_device(B, ldb, offset=ob)
+        C = g.sgemm_f32_ex(dA, dB, producer=7)
+        torch.cuda.synchronize()
+        C64, bound = oracle.gemm_f64(A.numpy(), B.numpy(), with_bound=(dist != "int"))
+        check(C.cpu().numpy(), C64, bound, exact=(dist == "int"), what=f"ldg {offsets} {pads} {dist}")
+
