@@ -24,13 +24,15 @@ cudaError_t copy_rows(float* dst, long long ld_dst, const float* src, long long 
 // bytes per second than the product consumes (measured on GB300: ~210 GB/s
 // in, ~195 GB/s out; a 4096 x 4096 output consumes a column of A and a row
 // of B, 32 KB, every 0.5 us), so no product may wait for whole operands.  K
-// is cut into chunks that grow (to 1/32, 1/8, 1/2 and all of K): chunk c's
+// is cut into chunks that grow (to 1/32, 5/32, 1/2 and all of K): chunk c's
 // columns of A and rows of B cross the link together, and the product
 // C (+)= A[:, c] B[c, :] over all rows starts once they are in, while the
 // next chunk crosses.  The first chunk is short, so that the first product
 // starts early; each later chunk is in before the product of the one before
-// it ends.  The last chunk's product runs in row blocks that shrink towards
-// the end (to 1/4, 1/2, 3/4, 7/8, 15/16 and all of the rows), each block's
+// it ends (measured on GB300: pitched copies of 512-byte rows run at 131
+// GB/s, of 6 KB rows and more at 203-208 GB/s).  The last chunk's product
+// runs in row blocks that shrink towards the end (to 1/2, 3/4, 7/8, 15/16
+// and all of the rows), each block's
 // rows of C going back over the link while the next block computes, so that
 // only the last, small block of C crosses after the last product.  Smaller
 // products run as one block: copies in, product, copy out.
@@ -69,7 +71,7 @@ int run_host(int M, int N, int K, const float* A, int lda, const float* B, int l
     long long kb[kHostMaxKc + 1] = {0};
     int nkc = 0;
     {
-        const int den = 32, num[kHostMaxKc] = {1, 4, 16, 32};
+        const int den = 32, num[kHostMaxKc] = {1, 5, 16, 32};
         for (int c = 0; c < kHostMaxKc; ++c) {
             const long long b = (!big || c == kHostMaxKc - 1) ? K : (static_cast<long long>(K) * num[c] / den) / 32 * 32;
             if (b > kb[nkc]) kb[++nkc] = b;
@@ -80,7 +82,7 @@ int run_host(int M, int N, int K, const float* A, int lda, const float* B, int l
     long long rb[kHostMaxBlk + 1] = {0};
     int nblk = 0;
     {
-        const int den = 16, num[kHostMaxBlk] = {4, 8, 12, 14, 15, 16};
+        const int den = 16, num[kHostMaxBlk] = {8, 12, 14, 15, 16, 16};
         for (int i = 0; i < kHostMaxBlk; ++i) {
             const long long b =
                 (!big || i == kHostMaxBlk - 1) ? M : (static_cast<long long>(M) * num[i] / den) / kBM * kBM;
