@@ -18,7 +18,7 @@ CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB_NAME = "libgb300_sgemm.so"
 SOURCES = ["sgemm_api.cu", "api_device.cu", "api_plan.cu", "api_ffma.cu", "api_tf32.cu", "api_host.cu", "sgemm_ffma_tma.cu", "sgemm_ffma_tma_wg.cu", "sgemm_ffma_tma_wide.cu", "sgemm_ffma_tma_fused.cu", "sgemm_ffma_tma_x.cu", "sgemm_ffma_tma_x16.cu",
-           "sgemm_ffma_cpasync.cu", "sgemm_ffma_scaled.cu", "sgemm_ffma_bt.cu", "sgemm_ffma_ldg.cu", "sgemm_small.cu", "sgemm_3xtf32.cu", "sgemm_3xtf32_direct.cu", "pack.cu", "peak.cu"]
+           "sgemm_ffma_cpasync.cu", "sgemm_ffma_scaled.cu", "sgemm_ffma_bt.cu", "sgemm_ffma_ldg.cu", "sgemm_ffma_res.cu", "sgemm_small.cu", "sgemm_3xtf32.cu", "sgemm_3xtf32_direct.cu", "pack.cu", "peak.cu"]
 # Kernels that split registers between warpgroups with setmaxnreg must be
 # built with exactly this many registers per thread (the split's total).
 REGSPLIT_SOURCES = ("sgemm_ffma_tma_wg.cu", "sgemm_ffma_tma_wide.cu")

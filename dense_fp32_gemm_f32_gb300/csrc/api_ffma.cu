@@ -82,8 +82,9 @@ int run_ffma(int M, int N, int K, const float* A, int lda, const float* B, int l
     }
     // (With a transposed A, make_plan rejects forced producer, tile, math,
     // and stage choices: the transposed-A kernels have one form.)
+    const bool scaled = scale && (scale->alpha != 1.f || scale->beta != 0.f);
     Plan pl;
-    rc = make_plan(*st, M, N, K, A, lda, B, ldb, opt, &pl, a_mn, b_nk);
+    rc = make_plan(*st, M, N, K, A, lda, B, ldb, opt, &pl, a_mn, b_nk, scaled);
     if (rc != SGEMM_OK) {
         a_t.release();
         return rc;
@@ -98,7 +99,7 @@ int run_ffma(int M, int N, int K, const float* A, int lda, const float* B, int l
         if (rc == SGEMM_ERR_CUDA && !(opt && opt->repack == 2)) {
             sgemm_options o = opt ? *opt : sgemm_options{};
             o.repack = 1;
-            rc = make_plan(*st, M, N, K, A, lda, B, ldb, &o, &pl, a_mn, b_nk);
+            rc = make_plan(*st, M, N, K, A, lda, B, ldb, &o, &pl, a_mn, b_nk, scaled);
         }
         if (rc != SGEMM_OK) {
             a_t.release();
@@ -111,8 +112,8 @@ int run_ffma(int M, int N, int K, const float* A, int lda, const float* B, int l
         a_t.release();
     };
 
-    const bool scaled = scale && (scale->alpha != 1.f || scale->beta != 0.f);
-    const KernelEntry k = pl.b_nk ? ffma_kernel_bnk(pl.a_mn, scaled)
+    const KernelEntry k = (pl.res && scaled) ? KernelEntry{nullptr, 0, 0}  // (make_plan rules this out)
+                          : pl.b_nk ? ffma_kernel_bnk(pl.a_mn, scaled)
                           : pl.a_mn ? (pl.bn == kBN ? ffma_kernel_amn(pl.stages, pl.math, scaled)
                                                   : scaled ? KernelEntry{nullptr, 0, 0} : ffma_kernel(pl))
                           : scaled ? (pl.producer == kProducerTmaX  ? ffma_kernel_tma_x(pl.stages, pl.math, true)
@@ -143,7 +144,20 @@ int run_ffma(int M, int N, int K, const float* A, int lda, const float* B, int l
             return rc;
         }
     }
-    if (is_tma(pl.producer)) {
+    // Residue-class maps (pl.res): four per operand, boxes of 36 k x 32 rows
+    // of A and 132 columns x 8 rows of B (see ResMaps).
+    ResMaps resA, resB;
+    std::memset(&resA, 0, sizeof resA);
+    std::memset(&resB, 0, sizeof resB);
+    int a_shift = 0, b_shift = 0;
+    if (pl.res) {
+        rc = encode_res(&resA, &a_shift, A, M, K, lda, kResABox, kBM / 4);
+        if (rc == SGEMM_OK) rc = encode_res(&resB, &b_shift, B, K, N, ldb, kResBBox, kBK / 4);
+        if (rc != SGEMM_OK) {
+            release_pack();
+            return rc;
+        }
+    } else if (is_tma(pl.producer)) {
         rc = pl.a_mn ? encode_2d(&tmA, A, M, K, lda, kBM, kBK, CU_TENSOR_MAP_SWIZZLE_NONE)  // {m, k} boxes of 128 x 32
              : pl.bk == kBK16 ? encode_2d(&tmA, A, K, M, lda, kBK16, kBM, CU_TENSOR_MAP_SWIZZLE_64B)
                               : encode_2d(&tmA, A, K, M, lda, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B);
@@ -179,6 +193,8 @@ int run_ffma(int M, int N, int K, const float* A, int lda, const float* B, int l
     prm.status = st->status_word;
     prm.alpha = scale ? scale->alpha : 1.f;
     prm.beta = scale ? scale->beta : 0.f;
+    prm.a_shift = a_shift;
+    prm.b_shift = b_shift;
     prm.sk = pl.sk;
     prm.sk_dp_tiles = pl.sk_dp_tiles;
     prm.sk_units = (static_cast<long long>(pl.tiles_n) * ceil_div(M, kBM) - pl.sk_dp_tiles) * pl.num_k_tiles;
@@ -243,7 +259,8 @@ int run_ffma(int M, int N, int K, const float* A, int lda, const float* B, int l
         }
         cfg.attrs = &attr;
         cfg.numAttrs = (pl.sk || ln.split > 1) ? 1 : 0;
-        void* args[4] = {&tmA, &tmB, &tmC, &prm};
+        void* args[4] = {pl.res ? static_cast<void*>(&resA) : &tmA, pl.res ? static_cast<void*>(&resB) : &tmB, &tmC,
+                         &prm};
         if (cudaLaunchKernelExC(&cfg, k.fn, args) != cudaSuccess) {
             (void)cudaGetLastError();
             sk_return(*st, cs, lease);
@@ -294,7 +311,7 @@ int run_ffma_noalloc(int M, int N, int K, const float* A, int lda, const float* 
     o.stream_k = K > 0 ? 2 : 1;
     o.split_k = K > 0 ? 0 : 1;
     o.tile_n = kBN;
-    o.repack = 1;  // repacking would allocate: misaligned operands take the cp.async producer
+    o.repack = 1;  // repacking would allocate: misaligned operands take the residue-class maps, else cp.async
     Plan pl;
     rc = make_plan(*st, M, N, K, A, lda, B, ldb, &o, &pl);
     if (rc != SGEMM_OK) return rc;
@@ -316,7 +333,15 @@ int run_ffma_noalloc(int M, int N, int K, const float* A, int lda, const float* 
         rc = encode_2d(&tmC, C, N, M, ldc, kBN, kBM, CU_TENSOR_MAP_SWIZZLE_NONE);
         if (rc != SGEMM_OK) return rc;
     }
-    if (is_tma(pl.producer)) {
+    ResMaps resA, resB;
+    std::memset(&resA, 0, sizeof resA);
+    std::memset(&resB, 0, sizeof resB);
+    int a_shift = 0, b_shift = 0;
+    if (pl.res) {
+        rc = encode_res(&resA, &a_shift, A, M, K, lda, kResABox, kBM / 4);
+        if (rc == SGEMM_OK) rc = encode_res(&resB, &b_shift, B, K, N, ldb, kResBBox, kBK / 4);
+        if (rc != SGEMM_OK) return rc;
+    } else if (is_tma(pl.producer)) {
         rc = encode_2d(&tmA, A, K, M, lda, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B);
         if (rc == SGEMM_OK) rc = encode_2d(&tmB, B, N, K, ldb, pl.bn, kBK, CU_TENSOR_MAP_SWIZZLE_NONE);
         if (rc != SGEMM_OK) return rc;
@@ -345,6 +370,8 @@ int run_ffma_noalloc(int M, int N, int K, const float* A, int lda, const float* 
     prm.tma_store = c_tma ? 1 : 0;
     prm.timeout_ns = kDefaultTimeoutNs;
     prm.status = st->status_word;
+    prm.a_shift = a_shift;
+    prm.b_shift = b_shift;
     prm.sk = pl.sk;
     prm.sk_dp_tiles = pl.sk_dp_tiles;
     prm.sk_units = (static_cast<long long>(pl.tiles_n) * ceil_div(M, kBM) - pl.sk_dp_tiles) * pl.num_k_tiles;
@@ -387,7 +414,8 @@ int run_ffma_noalloc(int M, int N, int K, const float* A, int lda, const float* 
     attr.val.cooperative = 1;
     cfg.attrs = &attr;
     cfg.numAttrs = pl.sk ? 1 : 0;
-    void* args[4] = {&tmA, &tmB, &tmC, &prm};
+    void* args[4] = {pl.res ? static_cast<void*>(&resA) : &tmA, pl.res ? static_cast<void*>(&resB) : &tmB, &tmC,
+                     &prm};
     if (cudaLaunchKernelExC(&cfg, k.fn, args) != cudaSuccess) {
         (void)cudaGetLastError();
         return SGEMM_ERR_CUDA;

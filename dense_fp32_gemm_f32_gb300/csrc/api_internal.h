@@ -91,6 +91,15 @@ inline long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
 // +23 %, 4095 x 4097 x 4099 and 8191 x 8193 x 8195 +30 %.
 constexpr double kRepackMinFlops = 1073741824.0;  // 2^30
 
+// Misaligned operands are read in place by the residue-class tensor maps
+// below 2MNK = kResMaxFlops and repacked from there on.  Measured on GB300
+// (both operands misaligned, TFLOP/s, class maps / repacked / cp.async):
+// 700 x 900 x 701 27.7 / 23.9 / 24.0, 1023 x 1025 x 1027 37.3 / 34.9 /
+// 32.2, 2047 x 2049 x 2051 58.2 / 57.9 / 45.5, 4095 x 4097 x 4099 64.4 /
+// 65.8 / 49.0, 8191 x 8193 x 8195 66.5 / 68.7 / 50.2: the copy's cost
+// fades with size while the class maps' extra producer work per slice stays.
+constexpr double kResMaxFlops = 34359738368.0;  // 2^35
+
 // Rows of tiles per group of the FFMA kernels' tile order (tile_rc): as many
 // as keep the group's A row panels within kGroupABytes, between 4 and 16.
 constexpr int kGroupRowsMax = 16, kGroupRowsMin = 4;
@@ -215,6 +224,7 @@ struct Plan {
     bool a_mn = false;    // A stored transposed (K x M): the transposed-A kernels
     bool b_nk = false;    // B stored transposed (N x K): the kernels with a B-transposing warp
     int bk = kBK;         // K slice depth (32, or 16 for sgemm_options.tile_k = 16)
+    bool res = false;     // A and B read through residue-class tensor maps (any alignment; see ResMaps)
 };
 
 // Epilogue scaling of the general entry: C = alpha * A B + beta * C.
@@ -238,9 +248,11 @@ bool is_tma(int producer);
 KernelEntry ffma_kernel(const Plan& pl);
 bool tma_ok(const float* p, int ld);
 int make_plan(const DeviceState& st, int M, int N, int K, const float* A, int lda, const float* B, int ldb,
-              const sgemm_options* opt, Plan* out, bool a_mn = false, bool b_nk = false);
+              const sgemm_options* opt, Plan* out, bool a_mn = false, bool b_nk = false, bool scaled = false);
 int encode_2d(CUtensorMap* map, const float* base, long long inner, long long outer, long long ld, int box_inner,
               int box_outer, CUtensorMapSwizzle swz);
+int encode_res(ResMaps* maps, int* shifts, const float* base, long long rows, long long cols, long long ld,
+               int box_inner, int box_outer);
 const char* describe_plan(const Plan& pl);
 bool small_problem(const DeviceState& st, int M, int N, int K);
 bool small_forced_ok(const sgemm_options* opt);

@@ -25,6 +25,9 @@ int validate(int M, int N, int K, const float* A, int lda, const float* B, int l
     if (M > 0 && K > 0 && !A) return SGEMM_ERR_INVALID_ARG;
     if (K > 0 && N > 0 && !B) return SGEMM_ERR_INVALID_ARG;
     if (M > 0 && N > 0 && !C) return SGEMM_ERR_INVALID_ARG;
+    // Every operand is an array of floats: 4-byte aligned.
+    if (((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B) | reinterpret_cast<uintptr_t>(C)) & 3u) != 0)
+        return SGEMM_ERR_INVALID_ARG;
     // Output tiles are numbered with a 32-bit int.
     if (((static_cast<long long>(M) + kBM - 1) / kBM) * (((static_cast<long long>(N) + kBN - 1) / kBN) + 1) >
         0x7fffffffLL)
@@ -77,6 +80,7 @@ KernelEntry ffma_kernel(const Plan& pl) {
                                                         : KernelEntry{nullptr, 0, 0};
     if (pl.producer == kProducerFused) return ffma_kernel_tma_fused(pl.stages, pl.math);
     if (pl.producer == kProducerLdg) return ffma_kernel_ldg(pl.stages, pl.math);
+    if (pl.res) return pl.producer == kProducerTmaX ? ffma_kernel_res(pl.stages, pl.math) : KernelEntry{nullptr, 0, 0};
     if (pl.producer == kProducerTmaX)
         return pl.bk == kBK16 ? ffma_kernel_tma_x16(pl.stages, pl.math) : ffma_kernel_tma_x(pl.stages, pl.math, false);
     if (pl.bn == kBNWide) return pl.producer == kProducerTmaWg ? ffma_kernel_tma_wide(pl.stages, pl.math)
@@ -107,7 +111,7 @@ bool tma_ok(const float* p, int ld) {
 
 // Chooses the variant.  Any field of `opt` that is non-zero forces that choice.
 int make_plan(const DeviceState& st, int M, int N, int K, const float* A, int lda, const float* B, int ldb,
-              const sgemm_options* opt, Plan* out, bool a_mn, bool b_nk) {
+              const sgemm_options* opt, Plan* out, bool a_mn, bool b_nk, bool scaled) {
     Plan pl;
     // B stored N x K (general entry only): tensor-map readable B, 128 x 128
     // tiles, 2 stages, paired FMA, and a transposing warp for B.
@@ -145,13 +149,32 @@ int make_plan(const DeviceState& st, int M, int N, int K, const float* A, int ld
     const int want_repack = opt ? opt->repack : 0;
     if (want_repack < 0 || want_repack > 2) return SGEMM_ERR_INVALID_ARG;
     const int misaligned = (a_mn || tma_ok(A, lda) ? 0 : 1) | (tma_ok(B, ldb) ? 0 : 2);
-    if (K > 0 && misaligned &&
+    // Residue-class tensor maps (operands of any alignment read in place):
+    // every class of rows mod 4 must hold a row of A and of B (M, K >= 4);
+    // the kernels have 128 x 128 tiles, 32-deep slices, 2 to 4 stages,
+    // paired FMA and the plain epilogue.  Automatic for misaligned operands
+    // below kResMaxFlops, and whenever copies are ruled out (repack = 1).
+    const double flops = 2.0 * static_cast<double>(M) * static_cast<double>(N) * static_cast<double>(K);
+    const bool res_ok = !a_mn && !b_nk && !scaled && M >= 4 && K >= 4 &&
+                        !(opt && opt->tile_n && opt->tile_n != kBN) &&
+                        !(opt && opt->tile_k && opt->tile_k != kBK) &&
+                        !(opt && opt->stages && (opt->stages < 2 || opt->stages > 4)) &&
+                        !(opt && opt->math && opt->math != kMathFfma2);
+    if (want_prod == SGEMM_PRODUCER_TMA_RES) {
+        if (!res_ok || want_repack == 2) return SGEMM_ERR_INVALID_ARG;
+        pl.res = true;
+    } else if (want_prod == SGEMM_PRODUCER_AUTO && misaligned && res_ok &&
+               (want_repack == 1 || (want_repack == 0 && flops < kResMaxFlops))) {
+        pl.res = true;
+    }
+    if (!pl.res && K > 0 && misaligned &&
         (want_repack == 2 || a_mn || b_nk ||  // (the transposed-operand kernels have no cp.async form)
-         (want_repack == 0 && want_prod == SGEMM_PRODUCER_AUTO &&
-          2.0 * static_cast<double>(M) * static_cast<double>(N) * static_cast<double>(K) >= kRepackMinFlops)))
+         (want_repack == 0 && want_prod == SGEMM_PRODUCER_AUTO && flops >= kRepackMinFlops)))
         pl.repack = misaligned;
     const bool aligned = K > 0 && (misaligned & ~pl.repack) == 0;
-    if (want_prod == SGEMM_PRODUCER_TMA) {
+    if (pl.res) {
+        pl.producer = kProducerTmaX;
+    } else if (want_prod == SGEMM_PRODUCER_TMA) {
         if (!aligned) return SGEMM_ERR_INVALID_ARG;
         pl.producer = kProducerTma;
     } else if (want_prod == SGEMM_PRODUCER_TMA_WG) {
@@ -229,6 +252,7 @@ int make_plan(const DeviceState& st, int M, int N, int K, const float* A, int ld
         (pl.stages < 2 || pl.stages > (pl.producer == kProducerTmaX && pl.bk == kBK16 ? 6 : 4)))
         return SGEMM_ERR_INVALID_ARG;
     if (pl.producer == kProducerTmaX && pl.bn != kBN) return SGEMM_ERR_INVALID_ARG;
+    if (pl.res && (pl.stages > 4 || pl.math != kMathFfma2 || pl.bk != kBK)) return SGEMM_ERR_INVALID_ARG;
     if (pl.producer == kProducerLdg && (pl.bn != kBN || pl.bk != kBK || pl.stages < 2 || pl.stages > 4))
         return SGEMM_ERR_INVALID_ARG;
     if (pl.bk == kBK16 && (pl.producer != kProducerTmaX || pl.stages == 5)) return SGEMM_ERR_INVALID_ARG;
@@ -362,6 +386,30 @@ int encode_2d(CUtensorMap* map, const float* base, long long inner, long long ou
     return r == CUDA_SUCCESS ? SGEMM_OK : SGEMM_ERR_CUDA;
 }
 
+// The four residue-class maps of a rows x cols operand with pitch ld (rows
+// >= 4, so that every class holds a row): class j holds rows j, j + 4,
+// ..., (rows - j + 3) / 4 of them, 4 ld floats apart; its map is based at the
+// 16-byte block boundary at or before row j's first element, t_j floats
+// before it, and spans cols + t_j floats per row, so that the row's last
+// element is the last inside the map.  shifts gets t_j in bits 2j, 2j + 1.
+// Boxes of box_inner x box_outer, no swizzle.
+int encode_res(ResMaps* maps, int* shifts, const float* base, long long rows, long long cols, long long ld,
+               int box_inner, int box_outer) {
+    if (rows < 4) return SGEMM_ERR_INVALID_ARG;
+    int sh = 0;
+    for (int j = 0; j < 4; ++j) {
+        const uintptr_t start = reinterpret_cast<uintptr_t>(base) + static_cast<uintptr_t>(j) * ld * 4;
+        const int t = static_cast<int>((start & 15u) >> 2);
+        const float* b = reinterpret_cast<const float*>(start - (start & 15u));
+        const int rc = encode_2d(&maps->m[j], b, cols + t, (rows - j + 3) / 4, 4 * ld, box_inner, box_outer,
+                                 CU_TENSOR_MAP_SWIZZLE_NONE);
+        if (rc != SGEMM_OK) return rc;
+        sh |= t << (2 * j);
+    }
+    *shifts = sh;
+    return SGEMM_OK;
+}
+
 const char* describe_plan(const Plan& pl) {
     static thread_local char buf[128];
     int n = std::snprintf(buf, sizeof buf, "%s/%s/s%d/st%d", producer_name(pl.producer),
@@ -379,7 +427,9 @@ const char* describe_plan(const Plan& pl) {
     if (pl.b_nk && n > 0 && n < static_cast<int>(sizeof buf))
         n += std::snprintf(buf + n, sizeof buf - n, "/bt");
     if (pl.bk != kBK && n > 0 && n < static_cast<int>(sizeof buf))
-        std::snprintf(buf + n, sizeof buf - n, "/k%d", pl.bk);
+        n += std::snprintf(buf + n, sizeof buf - n, "/k%d", pl.bk);
+    if (pl.res && n > 0 && n < static_cast<int>(sizeof buf))
+        std::snprintf(buf + n, sizeof buf - n, "/res");
     return buf;
 }
 

@@ -43,6 +43,11 @@ KernelEntry ffma_kernel_tma_x16(int stages, int math);
 // memory too) or, with `a_mn`, K x M; 2 stages, paired FMA, 128 x 128 tiles;
 // `scaled` selects the scaled epilogue.
 KernelEntry ffma_kernel_bnk(bool a_mn, bool scaled);
+// FFMA kernels on residue-class tensor maps (operands of any alignment, read
+// in place: four maps per operand, one per class of rows mod 4, and a
+// B-shifting producer warp); 128 x 128 tiles, paired FMA, plain epilogue;
+// stages {2,3,4}.
+KernelEntry ffma_kernel_res(int stages, int math);
 // FFMA kernels fed by loader warps (operands of any alignment, no tensor
 // maps): 128 x 128 tiles, paired FMA, plain epilogue; stages {2,3,4}.
 KernelEntry ffma_kernel_ldg(int stages, int math);

@@ -117,7 +117,7 @@ constexpr int kLoaderWarpsA = 2, kLoaderWarpsB = 2;
 // k for the consumers.  With the two A-transposing warps that is 12 warps,
 // whose 384 threads still get 168 registers each.
 constexpr int kTransposeWarpsB = 1;
-template <int PRODUCER, bool BNK = false>
+template <int PRODUCER, bool BNK = false>  // (BNK: any kernel with the B warp, also RES)
 __host__ __device__ constexpr int ffma_producer_warps() {
     return (PRODUCER == kProducerFused ? 0
             : PRODUCER == kProducerTma ? 1
@@ -166,6 +166,51 @@ __host__ __device__ constexpr int ffma_partial_bytes() {
     return kBM * BN * 4;  // one partial tile (split-K, stream-K)
 }
 
+// RES: operands of any alignment read by tensor maps over residue classes.
+// A tensor map needs a 16-byte aligned base and a row pitch that is a
+// multiple of 16 bytes.  Rows r = 4q + j of one residue class j (mod 4) lie
+// 4 ld floats = 16 ld bytes apart, a multiple of 16, so every row of a class
+// starts at the same offset t_j (0..3 floats) inside its 16-byte block: one
+// map per class, based at the block boundary before row j, addresses them
+// all.  Each stage loads, per class, a box starting at the block boundary
+// that covers the slice's elements wherever t_j puts them (32 k + 3 of A,
+// 128 columns + 3 of B: boxes of 36 and 132 floats); the A-transposing warps
+// read element k of row m at t_{m mod 4} + k, and one more producer warp
+// moves each B row left by its class's t in place, where the consumers read
+// it (row k of the slice: row k / 4 of class k mod 4's box).
+// Elements left of a row's start (the previous row's tail, already inside
+// the same 16-byte block) land in the box but are never read; the maps'
+// extents end at each row's last element, so everything past it reads as
+// the tensor map's zero fill.
+struct ResMaps {
+    CUtensorMap m[4];  // residue classes j = 0..3
+};
+template <bool RES>
+struct FfmaMap {
+    using type = CUtensorMap;
+};
+template <>
+struct FfmaMap<true> {
+    using type = ResMaps;
+};
+constexpr int kResABox = kBK + 4;                          // floats per A box row
+constexpr int kResBBox = kBN + 4;                          // floats per B box row
+constexpr int kResAPlaneBytes = (kBM / 4) * kResABox * 4;  // one class of an A slice: 32 rows (4608 B)
+constexpr int kResBPlaneBytes = (kBK / 4) * kResBBox * 4;  // one class of a B slice: 8 rows (4224 B)
+static_assert(kResAPlaneBytes % 128 == 0 && kResBPlaneBytes % 128 == 0, "tensor-copy destinations: 128-byte aligned");
+// A and B slices as loaded (A slices without RES: kStageABytes; B slices:
+// ffma_stage_b_bytes).
+__device__ __forceinline__ const CUtensorMap& res_map(const ResMaps& r, int j) { return r.m[j]; }
+__device__ __forceinline__ const CUtensorMap& res_map(const CUtensorMap& r, int) { return r; }
+template <bool RES, int BK = kBK>
+__host__ __device__ constexpr int ffma_load_a_bytes() {
+    return RES ? 4 * kResAPlaneBytes : kBM * BK * 4;
+}
+template <bool RES, int BN, int BK = kBK>
+__host__ __device__ constexpr int ffma_load_b_bytes() {
+    return RES ? 4 * kResBPlaneBytes : BK * BN * 4;
+}
+
 enum : int { kMathFfma = 1, kMathFfma2 = 2 };
 enum : unsigned { kStatusTimeout = 4u };
 
@@ -204,7 +249,9 @@ struct FfmaParams {
     unsigned int* status;  // per-device sticky status word (error bits)
     // Epilogue of the SCALED kernels: C = alpha * (A B) + beta * C (C is read
     // only when beta != 0).
-    float alpha, beta;
+    float alpha, beta;    // RES kernels: bits 2j, 2j + 1 hold t_j, the offset in floats of the rows
+    // of residue class j inside their 16-byte blocks (see ResMaps).
+    int a_shift, b_shift;
 };
 
 // Largest dynamic shared memory of a CTA on sm_100-family GPUs.
@@ -212,30 +259,34 @@ constexpr int kMaxSmemBytes = 232448;
 
 // XA: the stage also holds the transposed copy of its A slice (kProducerTmaX);
 // XB: and of its B slice (BNK).
-template <int STAGES, int BN = kBN, bool XA = false, bool XB = false, int BK = kBK>
+// RES: the slices as loaded are the residue-class boxes (and XB holds B
+// shifted into place).
+template <int STAGES, int BN = kBN, bool XA = false, bool XB = false, int BK = kBK, bool RES = false>
 __host__ __device__ constexpr int ffma_ring_bytes() {
-    return STAGES * (ffma_stage_bytes<BN, BK>() + (XA ? ffma_stage_a_bytes<BK>() : 0) +
-                     (XB ? ffma_stage_b_bytes<BN, BK>() : 0)) > ffma_partial_bytes<BN>()
-               ? STAGES * (ffma_stage_bytes<BN, BK>() + (XA ? ffma_stage_a_bytes<BK>() : 0) +
-                           (XB ? ffma_stage_b_bytes<BN, BK>() : 0))
+    return STAGES * (ffma_load_a_bytes<RES, BK>() + ffma_load_b_bytes<RES, BN, BK>() +
+                     (XA ? ffma_stage_a_bytes<BK>() : 0) + (XB ? ffma_stage_b_bytes<BN, BK>() : 0)) >
+                   ffma_partial_bytes<BN>()
+               ? STAGES * (ffma_load_a_bytes<RES, BK>() + ffma_load_b_bytes<RES, BN, BK>() +
+                           (XA ? ffma_stage_a_bytes<BK>() : 0) + (XB ? ffma_stage_b_bytes<BN, BK>() : 0))
                : ffma_partial_bytes<BN>();
 }
 
 // The kernels of the transposing producer with the plain epilogue write each
 // finished tile of C by a tensor-map store from a staging tile in shared
 // memory (when C's base and rows are 16-byte aligned), where it fits.
-template <int STAGES, int PRODUCER, int BN, bool SCALED, bool BNK, int BK = kBK>
+template <int STAGES, int PRODUCER, int BN, bool SCALED, bool BNK, int BK = kBK, bool RES = false>
 __host__ __device__ constexpr bool ffma_tma_store() {
     return (PRODUCER == kProducerTmaX || PRODUCER == kProducerLdg) && BN == kBN && !SCALED &&
-           ffma_ring_bytes<STAGES, BN, PRODUCER == kProducerTmaX, BNK, BK>() + ffma_partial_bytes<BN>() + 1024 +
-                   256 <=
+           ffma_ring_bytes<STAGES, BN, PRODUCER == kProducerTmaX, BNK, BK, RES>() +
+                   ffma_partial_bytes<BN>() + 1024 + 256 <=
                kMaxSmemBytes;
 }
 
-template <int STAGES, int BN = kBN, bool XA = false, bool XB = false, bool STG = false, int BK = kBK>
+template <int STAGES, int BN = kBN, bool XA = false, bool XB = false, bool STG = false, int BK = kBK,
+          bool RES = false>
 constexpr int ffma_smem_bytes() {
-    return ffma_ring_bytes<STAGES, BN, XA, XB, BK>() + (STG ? ffma_partial_bytes<BN>() : 0) + 1024 /*align*/ +
-           256 /*barriers*/;
+    return ffma_ring_bytes<STAGES, BN, XA, XB, BK, RES>() + (STG ? ffma_partial_bytes<BN>() : 0) +
+           1024 /*align*/ + 256 /*barriers*/;
 }
 
 // Output tile number -> (row of tiles tm, column of tiles tn).  Tiles are
@@ -286,10 +337,16 @@ __device__ __forceinline__ uint32_t swz128(int r, int c) {
 // or 16 (64-byte rows, 64-byte swizzle; the transposing producer on A and B
 // as stored only): half the shared memory per stage and twice the slices, so
 // that small problems' work divides into finer stream-K units.
+//
+// RES: A and B of any alignment through residue-class tensor maps (see
+// ResMaps; tmA and tmB are then four maps each, and FfmaParams a_shift,
+// b_shift hold the classes' offsets); the transposing producer, 128 x 128
+// tiles, A and B as stored, 32-deep slices.
 template <int STAGES, int PRODUCER, int MATH, int BN = kBN, bool SCALED = false, bool AMN = false, bool BNK = false,
-          int BK = kBK>
-__global__ void __launch_bounds__(ffma_threads<PRODUCER, BNK>(), ffma_min_blocks<PRODUCER>())
-    sgemm_ffma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+          int BK = kBK, bool RES = false>
+__global__ void __launch_bounds__(ffma_threads<PRODUCER, BNK || RES>(), ffma_min_blocks<PRODUCER>())
+    sgemm_ffma_kernel(const __grid_constant__ typename FfmaMap<RES>::type tmA,
+                      const __grid_constant__ typename FfmaMap<RES>::type tmB,
                       const __grid_constant__ CUtensorMap tmC, const FfmaParams p) {
     // 128 accumulators per thread need the consumer register budget of the
     // register split.
@@ -304,8 +361,10 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER, BNK>(), ffma_min_blocks
     constexpr bool kAT = AMN || kX || kLdg;  // consumers read A with m innermost
     static_assert(!BNK || (BN == kBN && (PRODUCER == kProducerTmaX || (PRODUCER == kProducerTma && AMN))),
                   "B stored N x K: 128 x 128 tiles, transposing producer");
-    constexpr int kXA = kX ? kTransposeWarps : 0;    // A-transposing warps
-    constexpr int kXB = BNK ? kTransposeWarpsB : 0;  // B-transposing warps
+    static_assert(!RES || (kX && BN == kBN && !AMN && !BNK && BK == kBK),
+                  "residue-class maps: the transposing producer, 128 x 128 tiles, A, B as stored");
+    constexpr int kXA = kX ? kTransposeWarps : 0;          // A-transposing warps
+    constexpr int kXB = (BNK || RES) ? kTransposeWarpsB : 0;  // B-transposing (BNK) or B-shifting (RES) warps
     static_assert((BN == kBN && !kFused) || (BN == kBNWide && PRODUCER == kProducerTmaWg) ||
                       (BN == kBNFused && kFused),
                   "tile width");
@@ -313,7 +372,9 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER, BNK>(), ffma_min_blocks
                   "16-deep slices: the transposing producer on A and B as stored");
     constexpr int kStageABytes = ffma_stage_a_bytes<BK>();  // (shadows the 32-deep figure)
     constexpr int kStageBBytes = ffma_stage_b_bytes<BN, BK>();
-    constexpr int kStageBytes = ffma_stage_bytes<BN, BK>();
+    constexpr int kALoadBytes = ffma_load_a_bytes<RES, BK>();       // A slice as loaded
+    constexpr int kBLoadBytes = ffma_load_b_bytes<RES, BN, BK>();   // B slice as loaded
+    constexpr int kStageBytes = kALoadBytes + kBLoadBytes;           // bytes the copies of a stage bring
     constexpr int kPartialBytes = ffma_partial_bytes<BN>();
     constexpr int CW = ffma_consumer_warps<PRODUCER>();  // computing warps
     constexpr int CT = 32 * CW;                          // computing threads
@@ -325,18 +386,24 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER, BNK>(), ffma_min_blocks
     const uint32_t raw_base = smem_addr(smem_raw);
     const uint32_t base = (raw_base + 1023u) & ~1023u;
     uint8_t* const smem = smem_raw + (base - raw_base);
-    constexpr int kRingBytes = ffma_ring_bytes<STAGES, BN, kX, BNK, BK>();
+    constexpr int kRingBytes = ffma_ring_bytes<STAGES, BN, kX, BNK, BK, RES>();
     // Staging tile of the tensor-map stores of C, after the ring.
-    constexpr bool kStg = ffma_tma_store<STAGES, PRODUCER, BN, SCALED, BNK, BK>();
+    constexpr bool kStg = ffma_tma_store<STAGES, PRODUCER, BN, SCALED, BNK, BK, RES>();
     constexpr int kStgOff = kRingBytes;
     // Ring: A slices (as loaded), [transposed A slices], B slices (as
     // loaded), [transposed B slices]; with loader warps, transposed A slices
     // and B slices.
-    constexpr int kTOff = kLdg ? 0 : STAGES * kStageABytes;            // transposed A (kX, kLdg)
-    constexpr int kBLoadOff = (kX ? 2 : 1) * STAGES * kStageABytes;    // B as loaded
-    constexpr int kBOff = kBLoadOff + (BNK ? STAGES * kStageBBytes : 0);  // B as the consumers read it
-    const uint32_t sA0 = base;                                         // STAGES x 16 KiB
-    const uint32_t sB0 = base + kBLoadOff;                             // STAGES x kStageBBytes
+    constexpr int kTOff = kLdg ? 0 : STAGES * kALoadBytes;             // transposed A (kX, kLdg)
+    constexpr int kBLoadOff = STAGES * kALoadBytes + (kX ? STAGES * kStageABytes : 0);  // B as loaded
+    constexpr int kBOff = kBLoadOff + (BNK ? STAGES * kBLoadBytes : 0);  // B as the consumers read it
+    constexpr int kBReadStage = BNK ? kStageBBytes : kBLoadBytes;       // its bytes per stage
+    // Row k of the B slice the consumers read: rows of BN floats, or (RES)
+    // row k / 4 of class k mod 4's box, moved into place.
+    auto b_row = [](int k) {
+        return RES ? (k & 3) * kResBPlaneBytes + (k >> 2) * (kResBBox * 4) : k * (BN * 4);
+    };
+    const uint32_t sA0 = base;                                         // STAGES x kALoadBytes
+    const uint32_t sB0 = base + kBLoadOff;                             // STAGES x kBLoadBytes
     const uint32_t bar0 = base + kRingBytes + (kStg ? kPartialBytes : 0);  // full[STAGES], empty[STAGES], tfull[STAGES]
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
@@ -407,8 +474,16 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER, BNK>(), ffma_min_blocks
         fence_mbarrier_init();
     }
     if (kTma && (kFused ? threadIdx.x == 0 : (is_producer && pw == 0 && lane == 0))) {
-        prefetch_tensormap(&tmA);
-        prefetch_tensormap(&tmB);
+        if constexpr (RES) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                prefetch_tensormap(&tmA.m[j]);
+                prefetch_tensormap(&tmB.m[j]);
+            }
+        } else {
+            prefetch_tensormap(&tmA);
+            prefetch_tensormap(&tmB);
+        }
     }
     if (split > 1) {
         cluster_sync_all();  // the whole cluster has started before any peer access
@@ -549,7 +624,17 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER, BNK>(), ffma_min_blocks
             // row (the 8 lanes of each wavefront hit 8 different chunk
             // positions), and each of its 4 floats is stored to row k at
             // column m (or n) (32 consecutive floats per store).
-            const bool xb = BNK && pw - 1 >= kXA;  // this warp transposes B
+            //
+            // RES: the A slice as loaded is four class planes (class j: rows
+            // m = 4q + j, q = 0..31, of kResABox floats, the row's element k
+            // at t_j + k), read element by element (lanes 4g .. 4g + 3 take
+            // one row of each class, 4 banks apart and shifted by their
+            // t_j); the B-shifting warp takes the slice's 32 rows k (class
+            // k mod 4, row k / 4 of its plane of kResBBox floats): lane l
+            // reads the aligned 16-byte vectors at 4l and 4l + 4 and keeps
+            // the 4 floats starting t_j into them (t_j is the same for the
+            // whole warp), one 16-byte store per lane and row.
+            const bool xb = (BNK || RES) && pw - 1 >= kXA;  // this warp transposes (RES: shifts) B
             const int qn = xb ? 4 : 4 / kTransposeWarps;
             const int q0 = xb ? 0 : (pw - 1) * qn;
             const int src_off = xb ? kBLoadOff : 0;
@@ -564,6 +649,52 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER, BNK>(), ffma_min_blocks
                     if (!mbar_wait_bounded_warp(full_bar(s), round & 1, tmo)) {
                         timed_out = true;
                         break;
+                    }
+                    if constexpr (RES) {
+                        if (xb) {
+                            // In place, a class (8 rows, one t) at a time:
+                            // the whole warp reads its rows before any lane
+                            // overwrites a vector a neighbour still reads.
+                            float* const plane0 = reinterpret_cast<float*>(smem + kBLoadOff + s * kBLoadBytes);
+#pragma unroll 1
+                            for (int j = 0; j < 4; ++j) {
+                                const int t = (p.b_shift >> (2 * j)) & 3;
+                                if (t == 0) continue;  // (warp-uniform) already in place
+                                float* const plane = plane0 + j * (kResBPlaneBytes / 4) + 4 * lane;
+                                float4 o[kBK / 4];
+#pragma unroll
+                                for (int q = 0; q < kBK / 4; ++q) {
+                                    const float4 v0 = *reinterpret_cast<const float4*>(plane + q * kResBBox);
+                                    const float4 v1 = *reinterpret_cast<const float4*>(plane + q * kResBBox + 4);
+                                    o[q] = t == 1   ? make_float4(v0.y, v0.z, v0.w, v1.x)
+                                           : t == 2 ? make_float4(v0.z, v0.w, v1.x, v1.y)
+                                                    : make_float4(v0.w, v1.x, v1.y, v1.z);
+                                }
+                                __syncwarp();
+#pragma unroll
+                                for (int q = 0; q < kBK / 4; ++q)
+                                    *reinterpret_cast<float4*>(plane + q * kResBBox) = o[q];
+                            }
+                            // These generic-proxy writes precede the slot's
+                            // next tensor copy (async proxy) into the same bytes.
+                            fence_proxy_async_smem();
+                        } else {
+                            const float* const raw = reinterpret_cast<const float*>(smem + s * kALoadBytes);
+                            float* const tr = reinterpret_cast<float*>(smem + kTOff + s * kStageABytes);
+                            const int j = lane & 3;
+                            const int t = (p.a_shift >> (2 * j)) & 3;
+#pragma unroll
+                            for (int qq = 0; qq < qn; ++qq) {
+                                const int m = lane + 32 * (q0 + qq);
+                                const float* const row = raw + j * (kResAPlaneBytes / 4) + (m >> 2) * kResABox + t;
+#pragma unroll
+                                for (int k = 0; k < kBK; ++k) tr[k * kBM + m] = row[k];
+                            }
+                        }
+                        __syncwarp();
+                        mbar_arrive(tfull_bar(s));
+                        if (lane == 0) mbar_arrive(empty_bar(s));
+                        continue;
                     }
                     const uint8_t* const raw = smem + src_off + s * kStageABytes;
                     float* const tr = reinterpret_cast<float*>(smem + dst_off + s * kStageABytes);
@@ -616,7 +747,19 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER, BNK>(), ffma_min_blocks
                 }
                 if (skip_here && it == p.skip_stage - 1) continue;
                 const int k0 = kt * BK;
-                if (kTma) {
+                if (RES) {
+                    // Four class boxes per operand (see ResMaps): A rows
+                    // m0 / 4 .. + 31 of each class from k0; B rows k0 / 4 ..
+                    // + 7 of each class from column n0.
+                    mbar_arrive_expect_tx(full_bar(s), kStageBytes);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        tma_load_2d(sA0 + s * kALoadBytes + j * kResAPlaneBytes, &res_map(tmA, j), full_bar(s), k0,
+                                    m0 >> 2);
+                        tma_load_2d(sB0 + s * kBLoadBytes + j * kResBPlaneBytes, &res_map(tmB, j), full_bar(s), n0,
+                                    k0 >> 2);
+                    }
+                } else if (kTma) {
                     mbar_arrive_expect_tx(full_bar(s), kStageBytes);
                     if (AMN) {
                         tma_load_2d(sA0 + s * kStageABytes, &tmA, full_bar(s), m0, k0);
@@ -964,7 +1107,7 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER, BNK>(), ffma_min_blocks
                     break;
                 }
                 const uint8_t* sa = smem_a + s * kStageABytes;
-                const uint8_t* sb = smem_b + s * kStageBBytes;
+                const uint8_t* sb = smem_b + s * kBReadStage;
 #pragma unroll
                 for (int kg = 0; kg < BK / 4; ++kg) {
                     const uint32_t xe = static_cast<uint32_t>(((kg ^ tm) & 7) << 4);
@@ -988,7 +1131,7 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER, BNK>(), ffma_min_blocks
                         float2 bp[TQ];
 #pragma unroll
                         for (int h = 0; h < H; ++h) {
-                            const float4 bv = *reinterpret_cast<const float4*>(sb + k * (BN * 4) + h * 128);
+                            const float4 bv = *reinterpret_cast<const float4*>(sb + b_row(k) + h * 128);
                             bp[2 * h] = make_float2(bv.x, bv.y);
                             bp[2 * h + 1] = make_float2(bv.z, bv.w);
                         }

@@ -34,7 +34,7 @@
  *    from the pool below instead;
  *  - from a stream-ordered pool the library creates on each device (cached
  *    up to 256 MiB between calls), freed in stream order at the end of each
- *    call: 16-byte pitched copies of misaligned operands (2MNK >= 2^30),
+ *    call: 16-byte pitched copies of misaligned operands (2MNK >= 2^35),
  *    A's transposed copy (sgemm_options.a_layout = 2), transposed copies of
  *    op(B) = B^T and of an op(A) = A^T the tensor maps cannot read
  *    (sgemm_f32_gemm), B's TF32 parts and the K-split partial tiles and
@@ -97,9 +97,10 @@ typedef enum sgemm_status {
  * (2MNK <= 2^28 with at most a quarter as many 128 x 128 tiles as SMs) the
  * 32 x 32-tile small-problem kernel; otherwise 128 x 128 tiles, TMA-fed when
  * A, B have 16-byte aligned bases and row strides (with two warps transposing
- * each A slice in shared memory); misaligned operands are first copied into
- * 16-byte pitched rows (2MNK >= 2^30) or read by a cp.async-fed variant
- * (smaller products).  The schedule is stream-K (one CTA per SM, the work
+ * each A slice in shared memory); misaligned operands are read in place
+ * through residue-class tensor maps (SGEMM_PRODUCER_TMA_RES; 2MNK < 2^35,
+ * M, K >= 4) or first copied into 16-byte pitched rows (larger products);
+ * where neither applies, a cp.async-fed variant reads them.  The schedule is stream-K (one CTA per SM, the work
  * after the last full wave dealt out as K slices) when there are at least two
  * (tile, K slice) units per SM, cluster split-K for smaller outputs.
  * (128 x 256 tiles, a copy of A transposed in HBM and a K-split second
@@ -110,6 +111,8 @@ typedef enum sgemm_status {
  *   B, ldb       device pointer to B, row stride in floats (ldb >= N)
  *   C, ldc       device pointer to C, row stride in floats (ldc >= N)
  *   stream       cudaStream_t as void*
+ * A, B and C must be 4-byte aligned (arrays of float); any other alignment
+ * returns SGEMM_ERR_INVALID_ARG.
  * A call enqueues the product kernel, preceded, when repacking, by one copy
  * kernel (into a buffer from the library's pool).  The stream-K partial tiles
  * and ready flags live in the scratch the library keeps per stream (its
@@ -145,7 +148,8 @@ int sgemm_f32(int M, int N, int K,
  * Same operation, arguments, accuracy contract and errors as sgemm_f32.  It
  * runs the small-problem kernel where sgemm_f32 would, else the FFMA kernel
  * with the stream-K schedule (K == 0: the plain grid, which needs no
- * scratch); misaligned operands are read by cp.async, never repacked.
+ * scratch); misaligned operands are read in place through the residue-class
+ * tensor maps (cp.async when M or K < 4), never repacked.
  *
  * Limits and rules:
  *  - The array holds the scratch of at most 160 CTAs: 160 x 64 KiB partial
@@ -272,6 +276,18 @@ enum {
                                     and store A transposed (m innermost) and B as it is;
                                     128 x 128 tiles, 2..4 stages (default 3).  Measured
                                     slower than repacking or cp.async, so only forced */
+    SGEMM_PRODUCER_TMA_RES = 8,  /* operands of any alignment (bases and row pitches that
+                                    are whole floats) read in place by tensor maps, four per
+                                    operand, one per residue class of rows mod 4: the rows of
+                                    a class all start at the same offset (0..3 floats) inside
+                                    their 16-byte blocks, so a map based at the block boundary
+                                    before the class's first row reads them all, a few floats
+                                    early; the two A-transposing warps of SGEMM_PRODUCER_TMA_X
+                                    skip those floats, and one more producer warp moves each
+                                    B row into place in shared memory.  Needs M >= 4 and
+                                    K >= 4; 128 x 128 tiles, paired FMA, 2 to 4 stages
+                                    (default 2).  The automatic choice for misaligned
+                                    operands (repack = 2 forces the copies instead) */
     SGEMM_PRODUCER_SMALL = 6     /* the small-problem kernel: one 8-warp CTA per 32 x 32 tile
                                     of C, K split across its warps in 32-deep chunks and the
                                     partials summed in a fixed order; bounds-checked 4-byte
@@ -327,8 +343,12 @@ typedef struct sgemm_options {
                              floats (a pool workspace of M x K4 and/or
                              K x N4 floats) and the product runs on the
                              tensor-map path; auto = on when no producer is
-                             forced and 2MNK >= 2^30, else such operands are
-                             read by the cp.async producer */
+                             forced and 2MNK >= 2^35 (below that the
+                             residue-class tensor maps read such operands in
+                             place), 1 = off (the residue-class maps at every
+                             size), either way the cp.async producer where
+                             the maps cannot run (M or K < 4, a forced
+                             choice they do not take) */
     int a_layout;         /* 0 = auto (A stays where it is: the automatic
                              producer transposes its slices in shared memory,
                              SGEMM_PRODUCER_TMA_X), 1 = read A as stored,

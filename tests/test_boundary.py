@@ -63,6 +63,9 @@ FAKE_A, FAKE_B, FAKE_C = 0x10000000, 0x20000000, 0x30000000  # never dereference
         (4, 4, 4, FAKE_A, 4, FAKE_B, 4, 0, 4),  # C NULL
         (4, 4, 4, FAKE_A, 4, FAKE_B, 4, FAKE_A + 32, 4),  # C overlaps A
         (4, 4, 4, FAKE_A, 4, FAKE_B, 4, FAKE_B - 16, 4),  # C overlaps B
+        (4, 4, 4, FAKE_A + 2, 4, FAKE_B, 4, FAKE_C, 4),  # A not float-aligned
+        (4, 4, 4, FAKE_A, 4, FAKE_B + 1, 4, FAKE_C, 4),  # B not float-aligned
+        (4, 4, 4, FAKE_A, 4, FAKE_B, 4, FAKE_C + 3, 4),  # C not float-aligned
         (2**31 - 1, 65536 * 128, 4, FAKE_A, 4, FAKE_B, 65536 * 128, 0x7000000000, 65536 * 128),  # tile count beyond int
     ],
 )

@@ -114,6 +114,9 @@ VARIANTS = (
     # loader warps (operands of any alignment; here aligned)
     + [dict(producer=7, stages=s) for s in (2, 3, 4)]
     + [dict(producer=7, split_k=2), dict(producer=7, stream_k=1, split_k=1), dict(producer=7, group_m=1)]
+    # residue-class tensor maps (operands of any alignment; here aligned)
+    + [dict(producer=8, stages=s) for s in (2, 3, 4)]
+    + [dict(producer=8, split_k=2), dict(producer=8, stream_k=1, split_k=1), dict(producer=8, group_m=1)]
     # A's slices with the L2 evict-last policy
     + [dict(l2_hint=h) for h in (1, 2, 3)] + [dict(l2_hint=2, group_m=2, stream_k=2), dict(l2_hint=3, producer=1)]
     # producer warpgroup with the setmaxnreg register split
@@ -363,12 +366,13 @@ def test_tensor_map_stores_of_c_and_guard_bands(opt, c_offset, N):
 @pytest.mark.parametrize("shape", [(190, 170, 260), (700, 900, 260)])
 def test_unaligned_bases(offsets, shape):
     """Bases that are not 16-byte aligned: the small-problem kernel (plain
-    loads) or, above its range, the cp.async producer."""
+    loads) or, above its range, the residue-class tensor maps."""
     oa, ob = offsets
     M, N, K = shape
     A, B = make_operands(M, N, K, "uniform", 9)
     dA, dB = to_device(A, offset=oa), to_device(B, offset=ob)
-    assert g.describe(dA, dB).startswith("small" if M < 256 else "cpasync")
+    d = g.describe(dA, dB)
+    assert d.startswith("small") if M < 256 else d.endswith("/res")
     C = g.sgemm_f32(dA, dB)
     torch.cuda.synchronize()
     C64, bound = oracle.gemm_f64(A.numpy(), B.numpy())
@@ -482,13 +486,13 @@ def test_variant_choice():
     assert desc(256, 256, 256) == "small/t32/w8" and desc(512, 512, 512) == "small/t32/w8"
     assert desc(300, 500, 701) == "small/t32/w8" and desc(64, 64, 64) == "small/t32/w8"
     assert desc(640, 640, 640).startswith("tmax/") and desc(1024, 1024, 128).startswith("tmax/")
-    # 1027-float rows are not 16-byte multiples: the operands are repacked
-    # into pitched rows and the tensor-map path runs; mid-sized products read
-    # the rows as they are with cp.async
-    assert desc(1023, 1025, 1027).startswith("tmax/") and desc(1023, 1025, 1027).endswith("/repackAB")
-    assert desc(700, 900, 701).startswith("cpasync/")
-    assert desc(2048, 2049, 2048).endswith("/repackB")
-    assert desc(8192, 8193, 8192).endswith("/repackB")
+    # 1027-float rows are not 16-byte multiples: below 2MNK = 2^35 the
+    # residue-class tensor maps read the rows in place; larger products
+    # repack them into pitched rows first
+    assert desc(1023, 1025, 1027).startswith("tmax/") and desc(1023, 1025, 1027).endswith("/res")
+    assert desc(700, 900, 701).startswith("tmax/") and desc(700, 900, 701).endswith("/res")
+    assert desc(2048, 2049, 2048).endswith("/res")
+    assert desc(4096, 4097, 4096).endswith("/repackB") and desc(8192, 8193, 8192).endswith("/repackB")
 
 
 # ---------------------------------------------------------------- A's layout
@@ -773,3 +777,82 @@ def test_loader_warps_any_alignment_every_element(offsets, pads):
         C64, bound = oracle.gemm_f64(A.numpy(), B.numpy(), with_bound=(dist != "int"))
         check(C.cpu().numpy(), C64, bound, exact=(dist == "int"), what=f"ldg {offsets} {pads} {dist}")
 
+
+
+# ---------------------------------------------------------------- residue-class tensor maps
+
+@pytest.mark.parametrize("shape", [(1024, 1024, 1024), (700, 900, 701), (1500, 1300, 2000)])
+def test_residue_maps_match_tensor_map_kernel_bitwise(shape):
+    """Aligned operands: the four class maps per operand bring the same
+    slices as one map, so the result equals the transposing-producer
+    kernel's bit for bit (same schedule, same order of multiply-adds)."""
+    M, N, K = shape
+    A, B = make_operands(M, N, K, "normal", 49)
+    ldb = (N + 3) // 4 * 4
+    lda = (K + 3) // 4 * 4
+    C_res = run(A, B, lda=lda, ldb=ldb, producer=8)
+    C_tma = run(A, B, lda=lda, ldb=ldb, producer=5)
+    assert np.array_equal(C_res, C_tma)
+
+
+@pytest.mark.parametrize("offsets", [(0, 0), (1, 0), (0, 2), (3, 1), (2, 3)])
+@pytest.mark.parametrize("pads", [(0, 0), (1, 3), (5, 2), (2, 0)])
+def test_residue_maps_any_alignment_every_element(offsets, pads):
+    """Bases 0-3 floats off a 16-byte boundary and rows of any length (pads
+    added to K and N, so that the four classes' offsets are all different,
+    pairwise equal or all equal): every element against the oracle, integer
+    inputs exactly; M, N, K ragged against the tiles and slices."""
+    M, N, K = 777, 1153, 611
+    oa, ob = offsets
+    lda, ldb = K + pads[0], N + pads[1]
+    for dist in ("uniform", "int"):
+        A, B = make_operands(M, N, K, dist, 50)
+        dA, dB = to_device(A, lda, offset=oa), to_device(B, ldb, offset=ob)
+        C = g.sgemm_f32_ex(dA, dB, producer=8)
+        torch.cuda.synchronize()
+        C64, bound = oracle.gemm_f64(A.numpy(), B.numpy(), with_bound=(dist != "int"))
+        check(C.cpu().numpy(), C64, bound, exact=(dist == "int"), what=f"res {offsets} {pads} {dist}")
+
+
+@pytest.mark.parametrize("shape", [(4, 1, 4), (5, 3, 7), (7, 130, 5), (4, 129, 33), (131, 257, 4), (6, 6, 97)])
+@pytest.mark.parametrize("opt", [dict(producer=8), dict(producer=8, stream_k=1, split_k=1)])
+def test_residue_maps_smallest_classes(shape, opt):
+    """The fewest rows the classes allow (M, K = 4: one row of A and of B per
+    class), classes of unequal length (M, K not multiples of 4), N below one
+    16-byte block, K below one slice; pitches K + 1 and N + 1, bases off by
+    one float."""
+    M, N, K = shape
+    for dist in ("uniform", "int"):
+        A, B = make_operands(M, N, K, dist, 51)
+        dA, dB = to_device(A, K + 1, offset=1), to_device(B, N + 1, offset=1)
+        C = g.sgemm_f32_ex(dA, dB, **opt)
+        torch.cuda.synchronize()
+        C64, bound = oracle.gemm_f64(A.numpy(), B.numpy(), with_bound=(dist != "int"))
+        check(C.cpu().numpy(), C64, bound, exact=(dist == "int"), what=f"res {shape} {opt} {dist}")
+
+
+@pytest.mark.parametrize("name", ["ragged_1023x1025x1027", "square_1024"])
+def test_residue_maps_named_problem_every_element(name):
+    """The ragged problem (rows of 1027 and 1025 floats) read in place by the
+    class maps, and an aligned one forced onto them; integer twins exactly."""
+    p = PROBLEMS[name]
+    for q in (p, p.int_variant()):
+        A, B = problem_operands(q)
+        C = run(A, B, producer=8)
+        C64, bound = oracle.gemm_f64(A.numpy(), B.numpy(), with_bound=(q is p))
+        check(C, C64, bound, exact=(q is not p), what=f"res {q.name}")
+
+
+def test_residue_maps_rejections():
+    """Classes need a row of A and of B each (M, K >= 4); the kernels have
+    128 x 128 tiles, 32-deep slices, paired FMA, 2 to 4 stages; a forced copy
+    contradicts the in-place read."""
+    A, B = make_operands(8, 8, 8, "uniform", 52)
+    dA, dB = to_device(A), to_device(B)
+    for bad in (dict(stages=5), dict(math=1), dict(tile_n=256), dict(tile_k=16), dict(repack=2)):
+        with pytest.raises(g._lib.SgemmError):
+            g.sgemm_f32_ex(dA, dB, producer=8, **bad)
+    for M, K in ((3, 8), (8, 3)):
+        A, B = make_operands(M, 8, K, "uniform", 53)
+        with pytest.raises(g._lib.SgemmError):
+            g.sgemm_f32_ex(to_device(A), to_device(B), producer=8)

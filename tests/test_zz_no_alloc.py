@@ -39,8 +39,9 @@ def test_noalloc_matches_sgemm_f32_on_two_calls_in_a_row(shapes):
     assert torch.cuda.is_available(), "GPU tests need a CUDA device"
     torch.cuda.set_device(0)
     for call, (M, N, K, a_offset) in enumerate(shapes):
-        # The second call has unaligned rows (cp.async producer) and a
-        # different shape: nothing of the first call's scratch may leak in.
+        # The second call has unaligned rows (read in place through the
+        # residue-class tensor maps) and a different shape: nothing of the
+        # first call's scratch may leak in.
         A, B = make_operands(M, N, K, "normal", 900 + call)
         dA, dB = to_device(A, offset=a_offset), to_device(B)
         C_noalloc = torch.full((M, N), float("nan"), device="cuda")
@@ -88,8 +89,7 @@ for op in ops:
 torch.cuda.synchronize()
 free0 = torch.cuda.mem_get_info()[0]
 # Calls on streams the library has not seen (sgemm_f32 would give each of
-# them its own stream-K scratch) and on the misaligned shape (sgemm_f32 would
-# take repack buffers from its pool at this size).
+# them its own stream-K scratch), also on the misaligned shape.
 for s in streams:
     for op in ops:
         call(op, s)
@@ -104,7 +104,7 @@ print(json.dumps({"free0": free0, "free1": free1}))
 def test_noalloc_calls_take_no_device_memory():
     """The property the entry point exists for: after the first calls (the
     one-time set-up and kernel loading), further calls, on new streams and on
-    a shape that sgemm_f32 would repack, leave the device's free memory
+    a shape with misaligned rows, leave the device's free memory
     unchanged.  Run in a fresh process, so that no earlier test's pool cache
     or scratch can hide an allocation."""
     import json
