@@ -627,13 +627,7 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER, BNK || RES>(), ffma_min
             //
             // RES: the A slice as loaded is four class planes (class j: rows
             // m = 4q + j, q = 0..31, of kResABox floats, the row's element k
-            // at t_j + k), read element by element (lanes 4g .. 4g + 3 take
-            // one row of each class, 4 banks apart and shifted by their
-            // t_j); the B-shifting warp takes the slice's 32 rows k (class
-            // k mod 4, row k / 4 of its plane of kResBBox floats): lane l
-            // reads the aligned 16-byte vectors at 4l and 4l + 4 and keeps
-            // the 4 floats starting t_j into them (t_j is the same for the
-            // whole warp), one 16-byte store per lane and row.
+            // at t_j + k); see the two branches below.
             const bool xb = (BNK || RES) && pw - 1 >= kXA;  // this warp transposes (RES: shifts) B
             const int qn = xb ? 4 : 4 / kTransposeWarps;
             const int q0 = xb ? 0 : (pw - 1) * qn;
@@ -679,16 +673,37 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER, BNK || RES>(), ffma_min
                             // next tensor copy (async proxy) into the same bytes.
                             fence_proxy_async_smem();
                         } else {
-                            const float* const raw = reinterpret_cast<const float*>(smem + s * kALoadBytes);
-                            float* const tr = reinterpret_cast<float*>(smem + kTOff + s * kStageABytes);
-                            const int j = lane & 3;
-                            const int t = (p.a_shift >> (2 * j)) & 3;
+                            // Lane l takes rows 4l .. 4l + 3 (row l of each
+                            // class plane, 144 bytes apart: the 8 lanes of a
+                            // wavefront read 8 different bank groups), warp x
+                            // the 4-k groups c = 4x .. 4x + 3: per group and
+                            // class two aligned vectors, kept from t_j on (t_j
+                            // is the same for the whole warp), then one
+                            // 16-byte store of the 4 rows per k.
+                            const float* const raw =
+                                reinterpret_cast<const float*>(smem + s * kALoadBytes) + lane * kResABox;
+                            float* const tr = reinterpret_cast<float*>(smem + kTOff + s * kStageABytes) + 4 * lane;
 #pragma unroll
-                            for (int qq = 0; qq < qn; ++qq) {
-                                const int m = lane + 32 * (q0 + qq);
-                                const float* const row = raw + j * (kResAPlaneBytes / 4) + (m >> 2) * kResABox + t;
+                            for (int cc = 0; cc < kBK / 4 / kTransposeWarps; ++cc) {
+                                const int c = (pw - 1) * (kBK / 4 / kTransposeWarps) + cc;
+                                float4 r[4];
 #pragma unroll
-                                for (int k = 0; k < kBK; ++k) tr[k * kBM + m] = row[k];
+                                for (int j = 0; j < 4; ++j) {
+                                    const int t = (p.a_shift >> (2 * j)) & 3;
+                                    const float* const row = raw + j * (kResAPlaneBytes / 4) + 4 * c;
+                                    const float4 v0 = *reinterpret_cast<const float4*>(row);
+                                    r[j] = v0;
+                                    if (t != 0) {
+                                        const float4 v1 = *reinterpret_cast<const float4*>(row + 4);
+                                        r[j] = t == 1   ? make_float4(v0.y, v0.z, v0.w, v1.x)
+                                               : t == 2 ? make_float4(v0.z, v0.w, v1.x, v1.y)
+                                                        : make_float4(v0.w, v1.x, v1.y, v1.z);
+                                    }
+                                }
+                                *reinterpret_cast<float4*>(tr + (4 * c + 0) * kBM) = make_float4(r[0].x, r[1].x, r[2].x, r[3].x);
+                                *reinterpret_cast<float4*>(tr + (4 * c + 1) * kBM) = make_float4(r[0].y, r[1].y, r[2].y, r[3].y);
+                                *reinterpret_cast<float4*>(tr + (4 * c + 2) * kBM) = make_float4(r[0].z, r[1].z, r[2].z, r[3].z);
+                                *reinterpret_cast<float4*>(tr + (4 * c + 3) * kBM) = make_float4(r[0].w, r[1].w, r[2].w, r[3].w);
                             }
                         }
                         __syncwarp();
