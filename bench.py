@@ -621,7 +621,10 @@ SWEEP_OPTIONS = [
     {"tile_k": 16, "stages": 2},
     {"tile_k": 16, "stages": 6},
     {"group_m": 1},
+    {"l2_hint": 1},
     {"l2_hint": 2},
+    {"producer": 8},
+    {"repack": 2},
 ]
 
 

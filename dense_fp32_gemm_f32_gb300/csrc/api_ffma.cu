@@ -187,6 +187,7 @@ int run_ffma(int M, int N, int K, const float* A, int lda, const float* B, int l
     prm.group_m = pl.group_m;
     prm.a_evict_last = pl.a_evict_last;
     prm.b_evict_first = pl.b_evict_first;
+    prm.c_evict_first = pl.c_evict_first;
     prm.tma_store = (k.tma_store && c_aligned) ? 1 : 0;
     prm.skip_stage = opt ? opt->debug_skip_stage : 0;
     prm.timeout_ns = (opt && opt->timeout_ns) ? opt->timeout_ns : kDefaultTimeoutNs;
@@ -367,6 +368,7 @@ int run_ffma_noalloc(int M, int N, int K, const float* A, int lda, const float* 
     prm.group_m = pl.group_m;
     prm.a_evict_last = pl.a_evict_last;
     prm.b_evict_first = pl.b_evict_first;
+    prm.c_evict_first = pl.c_evict_first;
     prm.tma_store = c_tma ? 1 : 0;
     prm.timeout_ns = kDefaultTimeoutNs;
     prm.status = st->status_word;

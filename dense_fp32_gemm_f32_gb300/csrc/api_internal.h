@@ -215,6 +215,7 @@ struct Plan {
     int group_m = 1;  // tile order: rows of tiles per group (tile_rc)
     int a_evict_last = 0;  // A's slices loaded with the L2 evict-last policy
     int b_evict_first = 0; // B's slices loaded with the L2 evict-first policy
+    int c_evict_first = 0; // C's tensor-map stores with the L2 evict-first policy
     int num_k_tiles = 0;
     int nlaunch = 1;
     Launch launch[2];

@@ -115,6 +115,12 @@ __device__ __forceinline__ uint64_t l2_policy_evict_first() {
 // 2-D tiled bulk copy this CTA's shared memory -> global through a tensor
 // map (elements outside the tensor are not written), added to the thread's
 // current bulk group.  c0 is the innermost coordinate in elements.
+__device__ __forceinline__ void tma_store_2d_hint(const void* map, uint32_t src, int c0, int c1, uint64_t policy) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group.L2::cache_hint [%0, {%2, %3}], [%1], %4;" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(src), "r"(c0), "r"(c1), "l"(policy)
+                 : "memory");
+}
 __device__ __forceinline__ void tma_store_2d(const void* map, uint32_t src, int c0, int c1) {
     asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
                      reinterpret_cast<uint64_t>(map)),

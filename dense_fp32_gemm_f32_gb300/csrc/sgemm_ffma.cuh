@@ -232,6 +232,7 @@ struct FfmaParams {
     int a_evict_last;      // A's slices are loaded with the L2 evict-last policy
     int b_evict_first;     // B's slices are loaded with the L2 evict-first policy
     int tma_store;         // finished tiles of C go out by tensor-map stores (kernels with a staging tile)
+    int c_evict_first;     // those stores carry the L2 evict-first policy
     // Stream-K schedule (sk != 0), one CTA per SM: CTA g first takes whole
     // tiles g, g + G, ... below sk_dp_tiles (data-parallel waves, raster
     // order), then an even share of the units (one K slice of one tile each)
@@ -1032,7 +1033,10 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER, BNK || RES>(), ffma_min
         fence_proxy_async_smem();  // the generic-proxy writes, visible to the TMA
         consumer_sync();
         if (threadIdx.x == 0) {
-            tma_store_2d(&tmC, smem_addr(stg), tn_ * BN, tm_ * kBM);
+            if (p.c_evict_first)
+                tma_store_2d_hint(&tmC, smem_addr(stg), tn_ * BN, tm_ * kBM, l2_policy_evict_first());
+            else
+                tma_store_2d(&tmC, smem_addr(stg), tn_ * BN, tm_ * kBM);
             bulk_commit_group();
         }
     };

@@ -366,12 +366,14 @@ typedef struct sgemm_options {
                              them per panel) and A row panels in L2; 1 = row
                              by row.  Larger than the rows of tiles: one
                              group. */
-    int l2_hint;          /* 0 = auto, 1 = no cache policy, 2 = A's slices
-                             loaded with the L2 evict-last policy (the A row
-                             panels of a tile group stay in L2 across its
-                             waves), 3 = that and B's slices with the
-                             evict-first policy; tensor-map producers on A
-                             and B as stored */
+    int l2_hint;          /* 0 = auto (= 4), 1 = no cache policy, 2 = A's
+                             slices loaded with the L2 evict-last policy (the
+                             A row panels of a tile group stay in L2 across
+                             its waves), 3 = that and B's slices with the
+                             evict-first policy (tensor-map producers on A
+                             and B as stored), 4 = C's tensor-map stores
+                             with the evict-first policy (the kernels that
+                             store finished tiles from a staging tile) */
     int tile_k;           /* 0 = auto (32), 32, or 16: depth of the K slices
                              the pipeline stages hold (16: the transposing
                              producer, SGEMM_PRODUCER_TMA_X, only; A slices

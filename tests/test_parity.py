@@ -118,7 +118,7 @@ VARIANTS = (
     + [dict(producer=8, stages=s) for s in (2, 3, 4)]
     + [dict(producer=8, split_k=2), dict(producer=8, stream_k=1, split_k=1), dict(producer=8, group_m=1)]
     # A's slices with the L2 evict-last policy
-    + [dict(l2_hint=h) for h in (1, 2, 3)] + [dict(l2_hint=2, group_m=2, stream_k=2), dict(l2_hint=3, producer=1)]
+    + [dict(l2_hint=h) for h in (1, 2, 3, 4)] + [dict(l2_hint=2, group_m=2, stream_k=2), dict(l2_hint=3, producer=1)]
     # producer warpgroup with the setmaxnreg register split
     + [dict(producer=3, math=m, stages=s, split_k=1, multicast=1) for m in (1, 2) for s in (1, 4, 6)]
     + [dict(producer=3, math=2, split_k=s, multicast=1) for s in (2, 4)]
