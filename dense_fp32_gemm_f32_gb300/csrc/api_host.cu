@@ -31,8 +31,8 @@ cudaError_t copy_rows(float* dst, long long ld_dst, const float* src, long long 
 // starts early; each later chunk is in before the product of the one before
 // it ends (measured on GB300: pitched copies of 512-byte rows run at 131
 // GB/s, of 6 KB rows and more at 203-208 GB/s).  The last chunk's product
-// runs in row blocks that shrink towards the end (to 1/2, 3/4, 7/8, 15/16
-// and all of the rows), each block's
+// runs in row blocks that shrink towards the end (to 5/8, 13/16, 15/16 and
+// all of the rows), each block's
 // rows of C going back over the link while the next block computes, so that
 // only the last, small block of C crosses after the last product.  Smaller
 // products run as one block: copies in, product, copy out.
@@ -82,7 +82,7 @@ int run_host(int M, int N, int K, const float* A, int lda, const float* B, int l
     long long rb[kHostMaxBlk + 1] = {0};
     int nblk = 0;
     {
-        const int den = 16, num[kHostMaxBlk] = {8, 12, 14, 15, 16, 16};
+        const int den = 16, num[kHostMaxBlk] = {10, 13, 15, 16, 16, 16};
         for (int i = 0; i < kHostMaxBlk; ++i) {
             const long long b =
                 (!big || i == kHostMaxBlk - 1) ? M : (static_cast<long long>(M) * num[i] / den) / kBM * kBM;

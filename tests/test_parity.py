@@ -427,7 +427,7 @@ def test_host_buffer_entry():
 
 @pytest.mark.parametrize("dist", ["uniform", "int"])
 def test_host_buffer_entry_row_blocks(dist):
-    """2048 x 1536 x 2048 (2^34 flop): four K chunks, the last in five row
+    """2048 x 1536 x 2048 (2^34 flop): four K chunks, the last in four row
     blocks, whose copies overlap the products; every element."""
     A, B = make_operands(2048, 1536, 2048, dist, 14)
     C = g.sgemm_f32_host(A.pin_memory(), B.pin_memory())
@@ -438,7 +438,7 @@ def test_host_buffer_entry_row_blocks(dist):
 @pytest.mark.parametrize("dist", ["uniform", "int"])
 def test_host_buffer_entry_ragged_chunks(dist):
     """1500 x 1300 x 2500: K chunks of 64, 320, 864 and 1252, the last in row
-    blocks of 640, 384, 256, 128 and 92 rows (the last one ragged against
+    blocks of 896, 256, 128, 128 and 92 rows (the last one ragged against
     the 128-row tiles); every element."""
     A, B = make_operands(1500, 1300, 2500, dist, 16)
     C = g.sgemm_f32_host(A.pin_memory(), B.pin_memory())
