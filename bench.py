@@ -5,6 +5,7 @@
     python bench.py --sweep [--sweep-workloads NAME ...]   # ablation table, one JSON line per run
     python bench.py --cpu-table [--cpu-seconds S]          # the oracle on every named problem
     python bench.py --e2e-only [--workload NAME]           # the host-buffer leg alone (profiling)
+    python bench.py --kernel-only [--workload NAME]        # the device leg alone (profiling)
 
 One step is one C = A x B call on the named workload (default: the square
 4096^3 problem with standard-normal inputs, seed 3).  Inputs are resident in
@@ -289,6 +290,42 @@ def run_e2e_only(args):
     dt = (time.perf_counter() - t0) / args.steps
     print(json.dumps({"leg": "e2e", "workload": p.name, "ms_per_step": 1e3 * dt,
                       "tflops": p.flops / dt / 1e12, "steps": args.steps, "warmup": args.warmup}), flush=True)
+    return 0
+
+
+def run_kernel_only(args):
+    """The device leg alone (sgemm_f32 on the named workload's inputs resident
+    in HBM, --warmup untimed then --steps timed calls, L2 flushed before
+    each), for profiling one configuration's kernel; prints one diagnostic
+    JSON line."""
+    import torch
+
+    import dense_fp32_gemm_f32_gb300 as g
+
+    torch.cuda.set_device(0)
+    p = PROBLEMS[args.workload]
+    A_cpu, B_cpu = problem_operands(p)
+    A, B = A_cpu.cuda(), B_cpu.cuda()
+    C = torch.empty((p.M, p.N), dtype=torch.float32, device="cuda")
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    for i in range(args.warmup):
+        flush.fill_(float(i))
+        g.sgemm_f32(A, B, C)
+    torch.cuda.synchronize()
+    ms = []
+    for i in range(args.steps):
+        flush.fill_(float(i))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        g.sgemm_f32(A, B, C)
+        e1.record()
+        ms.append((e0, e1))
+    torch.cuda.synchronize()
+    assert g.check_status() == 0
+    t = statistics.median(a.elapsed_time(b) for a, b in ms)
+    print(json.dumps({"leg": "kernel", "workload": p.name, "variant": g.describe(A, B, C), "ms_median": t,
+                      "tflops": p.flops / (t / 1e3) / 1e12, "steps": args.steps, "warmup": args.warmup}),
+          flush=True)
     return 0
 
 
@@ -725,6 +762,8 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=4.0, help="bounded sample per --cpu-table entry")
     ap.add_argument("--e2e-only", action="store_true",
                     help="time only the end-to-end leg (host buffers) of --workload; a diagnostic line")
+    ap.add_argument("--kernel-only", action="store_true",
+                    help="time only the device leg (sgemm_f32 on resident inputs) of --workload; a diagnostic line")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -733,6 +772,8 @@ def main(argv=None):
         return run_sweep(args)
     if args.e2e_only:
         return run_e2e_only(args)
+    if args.kernel_only:
+        return run_kernel_only(args)
     if args.cpu_table:
         return run_cpu_table(args)
     if world > 1:
