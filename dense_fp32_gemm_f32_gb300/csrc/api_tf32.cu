@@ -19,11 +19,13 @@ int run_3xtf32(int M, int N, int K, const float* A, int lda, const float* B, int
     DeviceState* st = nullptr;
     rc = current_device(&dev, &st);
     if (rc != SGEMM_OK) return rc;
-    // The tensor-core kernel is fed by tensor maps.  Operands the TMA cannot
-    // read (unaligned bases or row strides) are repacked into pitched rows
-    // when the product is large enough for that to pay (the same rule as
-    // sgemm_f32); otherwise they, and K == 0, take the FFMA kernel, which
-    // meets the same contract.
+    // The tensor-core kernels are fed by tensor maps.  Operands the TMA
+    // cannot read directly (unaligned bases or row strides) go to the
+    // split-tile kernel on residue-class maps (variant 1's tiles; M, K >= 4)
+    // when that is the variant anyway or the product is below 2^30 flop;
+    // larger products for the wide-tile variants are repacked into pitched
+    // rows first.  K == 0, and misaligned operands neither path takes, run
+    // the FFMA kernel, which meets the same contract.
     // Variant: 1 = split-tile kernel (all four TF32 parts in shared memory),
     // 2 = direct-A kernel (A's big part is the TMA tile itself), 3 = the
     // split-tile kernel on 128 x 256 tiles with K-slices of 16, 4 = variant
@@ -44,11 +46,17 @@ int run_3xtf32(int M, int N, int K, const float* A, int lda, const float* B, int
     if (force_s >= 2 && force_s > ceil_div(K, kTcBK)) return SGEMM_ERR_INVALID_ARG;  // a slice per part at least
     const cudaStream_t cs = static_cast<cudaStream_t>(stream);
     const int misaligned = (tma_ok(A, lda) ? 0 : 1) | (tma_ok(B, ldb) ? 0 : 2);
+    const double flops = 2.0 * static_cast<double>(M) * static_cast<double>(N) * static_cast<double>(K);
+    const bool variant_forced = opt && opt->math;
+    bool res = false;  // the residue-class maps (variant 1's kernel on them)
+    if (K >= 4 && M >= 4 && misaligned && (variant == 1 || (!variant_forced && flops < kRepackMinFlops))) {
+        res = true;
+        variant = 1;
+    }
     Repacked packed;
-    if (K > 0 && misaligned &&
-        2.0 * static_cast<double>(M) * static_cast<double>(N) * static_cast<double>(K) >= kRepackMinFlops)
+    if (!res && K > 0 && misaligned && flops >= kRepackMinFlops)
         (void)packed.make(dev, *st, misaligned, M, N, K, A, lda, B, ldb, cs);  // (on failure: the FFMA kernel)
-    if (K == 0 || !tma_ok(A, lda) || !tma_ok(B, ldb)) {
+    if (K == 0 || (!res && (!tma_ok(A, lda) || !tma_ok(B, ldb)))) {
         packed.release();
         return run_ffma(M, N, K, A, lda, B, ldb, C, ldc, stream, nullptr);
     }
@@ -92,7 +100,7 @@ int run_3xtf32(int M, int N, int K, const float* A, int lda, const float* B, int
             launches[0] = {wk, 256, 16, wide, 0, 0, pb};
         }
     } else {
-        const KernelEntry k = variant == 1 ? tf32x3_kernel() : tf32x3_direct_kernel();
+        const KernelEntry k = res ? tf32x3_res_kernel() : variant == 1 ? tf32x3_kernel() : tf32x3_direct_kernel();
         const long long tiles = tiles_m * ceil_div(N, kTcBN);
         // Variant 1 with at most half as many tiles as SMs: each tile's nk K
         // slices split among s = min(4, SMs / tiles, nk / 2) CTAs when the
@@ -143,11 +151,15 @@ int run_3xtf32(int M, int N, int K, const float* A, int lda, const float* B, int
         }
     }
 
-    // Variant 4: B's TF32 parts, transposed (N x K4), in a pool buffer.
+    // Variant 4: B's TF32 parts, transposed (N x Kp), in a pool buffer.  Rows
+    // of Kp = K rounded up to 32 floats start on 128-byte boundaries, so that
+    // each 64-byte box row the TMA reads lies in one 128-byte line (measured
+    // on GB300, 4096 x 4096 x 4099: 818 us with rows of K rounded up to 4
+    // floats, against 499 us at K = 4096).
     void* ws = nullptr;
     float *bt_big = nullptr, *bt_small = nullptr;
-    const long long K4 = (static_cast<long long>(K) + 3) / 4 * 4;
-    const size_t part = (static_cast<size_t>(N) * K4 * sizeof(float) + 255) & ~size_t{255};
+    const long long Kp = (static_cast<long long>(K) + 31) / 32 * 32;
+    const size_t part = (static_cast<size_t>(N) * Kp * sizeof(float) + 255) & ~size_t{255};
     if (launches[0].pb) {
         cudaMemPool_t pool = workspace_pool(dev, *st);
         if (!pool || cudaMallocFromPoolAsync(&ws, 2 * part, pool, cs) != cudaSuccess) {
@@ -164,7 +176,7 @@ int run_3xtf32(int M, int N, int K, const float* A, int lda, const float* B, int
     if (launches[0].pb) {
         bt_big = static_cast<float*>(ws);
         bt_small = reinterpret_cast<float*>(static_cast<char*>(ws) + part);
-        rc = split_transpose_b(B, ldb, K, N, bt_big, bt_small, K4, cs);
+        rc = split_transpose_b(B, ldb, K, N, bt_big, bt_small, Kp, cs);
         if (rc != SGEMM_OK) {
             (void)cudaFreeAsync(ws, cs);
             if (ws_split) (void)cudaFreeAsync(ws_split, cs);
@@ -179,14 +191,22 @@ int run_3xtf32(int M, int N, int K, const float* A, int lda, const float* B, int
         alignas(64) CUtensorMap tmA;
         alignas(64) CUtensorMap tmB;
         alignas(64) CUtensorMap tmB2;
+        std::memset(&tmB2, 0, sizeof tmB2);
+        ResMaps resA, resB;  // (res) boxes of 36 k x 32 rows of A, 132 columns x 8 rows of B
+        int a_shift = 0, b_shift = 0;
         const CUtensorMapSwizzle swz = ln.bk == 32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
-        rc = encode_2d(&tmA, A, K, M, lda, ln.bk, kTcBM, swz);
-        if (ln.pb) {  // {k, n} boxes of the transposed parts, swizzled like A
-            if (rc == SGEMM_OK) rc = encode_2d(&tmB, bt_big, K, N, K4, ln.bk, ln.bn, swz);
-            if (rc == SGEMM_OK) rc = encode_2d(&tmB2, bt_small, K, N, K4, ln.bk, ln.bn, swz);
+        if (res) {
+            rc = encode_res(&resA, &a_shift, A, M, K, lda, kResABox, kResTileRows / 4);
+            if (rc == SGEMM_OK) rc = encode_res(&resB, &b_shift, B, K, N, ldb, kResBBox, kResSliceK / 4);
         } else {
-            if (rc == SGEMM_OK) rc = encode_2d(&tmB, B, N, K, ldb, ln.bn, ln.bk, CU_TENSOR_MAP_SWIZZLE_NONE);
-            tmB2 = tmB;  // (unused)
+            rc = encode_2d(&tmA, A, K, M, lda, ln.bk, kTcBM, swz);
+            if (ln.pb) {  // {k, n} boxes of the transposed parts, swizzled like A
+                if (rc == SGEMM_OK) rc = encode_2d(&tmB, bt_big, K, N, Kp, ln.bk, ln.bn, swz);
+                if (rc == SGEMM_OK) rc = encode_2d(&tmB2, bt_small, K, N, Kp, ln.bk, ln.bn, swz);
+            } else {
+                if (rc == SGEMM_OK) rc = encode_2d(&tmB, B, N, K, ldb, ln.bn, ln.bk, CU_TENSOR_MAP_SWIZZLE_NONE);
+                tmB2 = tmB;  // (unused)
+            }
         }
         if (rc != SGEMM_OK) break;
 
@@ -206,6 +226,8 @@ int run_3xtf32(int M, int N, int K, const float* A, int lda, const float* B, int
         prm.skip_stage = opt ? opt->debug_skip_stage : 0;
         prm.timeout_ns = (opt && opt->timeout_ns) ? opt->timeout_ns : kDefaultTimeoutNs;
         prm.status = st->status_word;
+        prm.a_shift = a_shift;
+        prm.b_shift = b_shift;
 
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(static_cast<unsigned>(ln.grid), 1, 1);
@@ -213,7 +235,8 @@ int run_3xtf32(int M, int N, int K, const float* A, int lda, const float* B, int
         cfg.dynamicSmemBytes = static_cast<size_t>(ln.k.smem_bytes);
         cfg.stream = static_cast<cudaStream_t>(stream);
         cfg.numAttrs = 0;
-        void* args4[4] = {&tmA, &tmB, &tmB2, &prm};
+        void* args4[4] = {res ? static_cast<void*>(&resA) : &tmA, res ? static_cast<void*>(&resB) : &tmB, &tmB2,
+                          &prm};
         void* args3[3] = {&tmA, &tmB, &prm};  // (the direct-A kernel takes no second B map)
         if (cudaLaunchKernelExC(&cfg, ln.k.fn, variant == 2 ? args3 : args4) != cudaSuccess) {
             (void)cudaGetLastError();

@@ -62,6 +62,9 @@ KernelEntry tf32x3_direct_kernel();
 // The split-tile kernel on 128 x 256 tiles with K-slices of 16 (64-byte
 // swizzled operand rows, 256 tensor-memory columns).
 KernelEntry tf32x3_wide_kernel();
+// The split-tile kernel (128 x 128 tiles) on residue-class tensor maps:
+// operands of any alignment read in place; 2 raw stages.
+KernelEntry tf32x3_res_kernel();
 
 // Copies up to two operands (a null dst skips one): `rows` rows of `cols`
 // floats from `src` (pitch ld_src floats, any alignment) to `dst` (pitch

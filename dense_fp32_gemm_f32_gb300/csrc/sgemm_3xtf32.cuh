@@ -128,11 +128,17 @@ __device__ __forceinline__ void tc_split_finish(const TcParams& p, int local, in
 // the big part and tmB2 the small part, each loaded by the TMA into its slot
 // of the split stage (arriving on split_full with the split warps, which then
 // write A's parts only).  Without PB, tmB maps B as stored and tmB2 is unused.
-template <int BN, int BK, bool PB = false>
+//
+// RES: A and B of any alignment, read in place through residue-class maps
+// (tmA and tmB are four maps each; res_maps.cuh): the split warps take A's
+// 16-byte chunk (row m, k = 4c..4c+3) as the two aligned vectors of its class
+// box row that hold it, shifted by the class's t, and B's elements from their
+// class box rows at t + n.
+template <int BN, int BK, bool PB = false, bool RES = false>
 __global__ void __launch_bounds__(kTcThreads, 1)
-    sgemm_3xtf32_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+    sgemm_3xtf32_kernel(const __grid_constant__ MapsFor<RES> tmA, const __grid_constant__ MapsFor<RES> tmB,
                         const __grid_constant__ CUtensorMap tmB2, const TcParams p) {
-    using T = TcShape<BN, BK, PB>;
+    using T = TcShape<BN, BK, PB, RES>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_base = smem_addr(smem_raw);
     const uint32_t base = (raw_base + 1023u) & ~1023u;
@@ -186,8 +192,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tmem_relinquish_alloc_permit();
     }
     if (warp == 0 && lane == 0) {
-        prefetch_tensormap(&tmA);
-        prefetch_tensormap(&tmB);
+#pragma unroll
+        for (int j = 0; j < (RES ? 4 : 1); ++j) {
+            prefetch_tensormap(&res_map(tmA, j));
+            prefetch_tensormap(&res_map(tmB, j));
+        }
         if (PB) prefetch_tensormap(&tmB2);
     }
     tc_fence_before_sync();
@@ -226,7 +235,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 if (skip_here && kt == p.skip_stage - 1) continue;
                 const int kc = (kbase + kt) * BK;  // K coordinate of the slice
                 mbar_arrive_expect_tx(raw_full(r), T::kRawABytes + T::kRawBBytes);
-                tma_load_2d(rawA(r), &tmA, raw_full(r), kc, m0);
+                if (RES) {
+                    // Four class boxes per operand: A rows m0 / 4 .. + 31 of
+                    // each class from kc, B rows kc / 4 .. + 7 from n0.
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        tma_load_2d(rawA(r) + j * kResAPlaneBytes, &res_map(tmA, j), raw_full(r), kc, m0 >> 2);
+                        tma_load_2d(rawB(r) + j * kResBPlaneBytes, &res_map(tmB, j), raw_full(r), n0, kc >> 2);
+                    }
+                } else {
+                    tma_load_2d(rawA(r), &tmA, raw_full(r), kc, m0);
+                }
                 if (PB) {
                     const int s = kt % T::kSplitStages;
                     const uint32_t b_big = split(s) + 2 * T::kOpABytes;
@@ -234,7 +253,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     tma_load_2d(b_big, &tmB, split_full(s), kc, n0);
                     tma_load_2d(b_big + T::kOpBBytes, &tmB2, split_full(s), kc, n0);
                     issued_sround[s] = kt / T::kSplitStages;
-                } else {
+                } else if (!RES) {
                     tma_load_2d(rawB(r), &tmB, raw_full(r), n0, kc);
                 }
                 issued_round[r] = round;
@@ -294,10 +313,45 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             // Loads are issued back to back before any use, so their latencies overlap.
             float4 av[kAChunks];
+            if constexpr (RES) {
+                // Chunk q of the swizzled K-major A tile: row m = q / 8, k =
+                // 4c..4c+3 with c = (q mod 8) XOR (m mod 8).
+                float4 v0[kAChunks], v1[kAChunks];
 #pragma unroll
-            for (int j = 0; j < kAChunks; ++j) av[j] = lds128(rawA(r) + static_cast<uint32_t>((tt + kSplitThreads * j) * 16));
+                for (int j = 0; j < kAChunks; ++j) {
+                    const int q = tt + kSplitThreads * j;
+                    const int m = q >> 3, c = (q & 7) ^ (m & 7);
+                    const uint32_t src = rawA(r) + static_cast<uint32_t>((m & 3) * kResAPlaneBytes +
+                                                                         (m >> 2) * (kResABox * 4) + c * 16);
+                    v0[j] = lds128(src);
+                    v1[j] = lds128(src + 16);
+                }
+#pragma unroll
+                for (int j = 0; j < kAChunks; ++j) {
+                    const int t = res_shift(p.a_shift, ((tt + kSplitThreads * j) >> 3) & 3);
+                    av[j] = t == 0   ? v0[j]
+                            : t == 1 ? make_float4(v0[j].y, v0[j].z, v0[j].w, v1[j].x)
+                            : t == 2 ? make_float4(v0[j].z, v0[j].w, v1[j].x, v1[j].y)
+                                     : make_float4(v0[j].w, v1[j].x, v1[j].y, v1[j].z);
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < kAChunks; ++j)
+                    av[j] = lds128(rawA(r) + static_cast<uint32_t>((tt + kSplitThreads * j) * 16));
+            }
             float bv[PB ? 1 : kBGroups][4];
-            if constexpr (!PB) {
+            if constexpr (RES) {
+                // k = 4 (bc0 + c) + i: class i, row bc0 + c of its box, at t_i + bn.
+#pragma unroll
+                for (int c = 0; c < kBGroups; ++c)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        asm volatile("ld.shared.f32 %0, [%1];"
+                                     : "=f"(bv[c][i])
+                                     : "r"(rawB(r) + static_cast<uint32_t>(i * kResBPlaneBytes +
+                                                                           (bc0 + c) * (kResBBox * 4) +
+                                                                           4 * (res_shift(p.b_shift, i) + bn))));
+            } else if constexpr (!PB) {
                 const uint32_t rb = rawB(r) + static_cast<uint32_t>(bn * 4);
 #pragma unroll
                 for (int c = 0; c < kBGroups; ++c)

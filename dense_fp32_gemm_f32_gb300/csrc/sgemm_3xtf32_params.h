@@ -4,6 +4,8 @@
 
 #include <cstdint>
 
+#include "res_maps.cuh"
+
 namespace gb300 {
 
 constexpr int kTcBM = 128;
@@ -39,18 +41,23 @@ constexpr uint32_t kTcIdesc = (1u << 4) | (2u << 7) | (2u << 10) | (static_cast<
 // PB (pre-split B): B's TF32 parts come split and transposed from HBM (a
 // pass before the kernel), loaded by the TMA straight into the split stages;
 // the raw stages hold A only, so 4 raw and 4 split stages fit.
-template <int BN, int BK, bool PB = false>
+//
+// RES (<128, 32> only): A and B of any alignment through residue-class tensor
+// maps (res_maps.cuh); the raw stages hold the four class boxes of each
+// operand (18 + 16.5 KiB), so 2 raw stages fit beside the 2 split stages.
+template <int BN, int BK, bool PB = false, bool RES = false>
 struct TcShape {
-    static_assert((BN == 128 && BK == 32 && !PB) || (BN == 256 && BK == 16), "built shapes");
+    static_assert((BN == 128 && BK == 32 && !PB) || (BN == 256 && BK == 16 && !RES), "built shapes");
+    static_assert(!RES || (BN == kResTileCols && BK == kResSliceK), "residue-class box geometry");
     static constexpr int kBM = 128;
     static constexpr int kRowBytes = BK * 4;          // one K-major operand row
     static constexpr int kSwizzle = kRowBytes;        // 128- or 64-byte swizzle
-    static constexpr int kRawABytes = kBM * BK * 4;   // TMA A slice, swizzled rows
-    static constexpr int kRawBBytes = PB ? 0 : BK * BN * 4;  // TMA B slice, BN-float rows
+    static constexpr int kRawABytes = RES ? 4 * kResAPlaneBytes : kBM * BK * 4;  // TMA A slice, swizzled rows
+    static constexpr int kRawBBytes = PB ? 0 : RES ? 4 * kResBPlaneBytes : BK * BN * 4;  // TMA B slice, BN-float rows
     static constexpr int kOpABytes = kBM * BK * 4;    // one K-major A operand tile
     static constexpr int kOpBBytes = BN * BK * 4;     // one K-major B operand tile
     static constexpr int kSplitBytes = 2 * kOpABytes + 2 * kOpBBytes;  // A_big, A_small, B_big, B_small
-    static constexpr int kRawStages = BK == 32 ? 3 : 4;
+    static constexpr int kRawStages = RES ? 2 : BK == 32 ? 3 : 4;
     static constexpr int kSplitStages = PB ? 4 : 2;
     static constexpr int kRingBytes = kRawStages * (kRawABytes + kRawBBytes) + kSplitStages * kSplitBytes;
     static constexpr int kSmemBytes = kRingBytes + 1024 /*align*/ + 256 /*barriers*/;
@@ -62,6 +69,7 @@ struct TcShape {
 static_assert(TcShape<128, 32>::kSmemBytes == kTcSmemBytes, "variant 1 keeps its layout");
 static_assert(TcShape<256, 16>::kSmemBytes <= 227 * 1024, "shared memory of variant 3");
 static_assert(TcShape<256, 16, true>::kSmemBytes <= 227 * 1024, "shared memory of variant 4");
+static_assert(TcShape<128, 32, false, true>::kSmemBytes <= 227 * 1024, "shared memory of variant 1 on class maps");
 
 struct TcParams {
     int M, N, K;
@@ -82,6 +90,7 @@ struct TcParams {
     int skip_stage;   // debug: CTA 0's producer never issues K-slice skip_stage-1
     unsigned long long timeout_ns;
     unsigned int* status;
+    int a_shift, b_shift;  // residue-class maps: t_j of A's and B's classes (bits 2j, 2j + 1)
 };
 
 // ---- "direct-A" variant: the TF32 big part of A is the FP32 tile itself

@@ -58,6 +58,7 @@
 #include <cstdint>
 
 #include "ptx.cuh"
+#include "res_maps.cuh"
 
 namespace gb300 {
 
@@ -166,42 +167,16 @@ __host__ __device__ constexpr int ffma_partial_bytes() {
     return kBM * BN * 4;  // one partial tile (split-K, stream-K)
 }
 
-// RES: operands of any alignment read by tensor maps over residue classes.
-// A tensor map needs a 16-byte aligned base and a row pitch that is a
-// multiple of 16 bytes.  Rows r = 4q + j of one residue class j (mod 4) lie
-// 4 ld floats = 16 ld bytes apart, a multiple of 16, so every row of a class
-// starts at the same offset t_j (0..3 floats) inside its 16-byte block: one
-// map per class, based at the block boundary before row j, addresses them
-// all.  Each stage loads, per class, a box starting at the block boundary
-// that covers the slice's elements wherever t_j puts them (32 k + 3 of A,
-// 128 columns + 3 of B: boxes of 36 and 132 floats); the A-transposing warps
-// read element k of row m at t_{m mod 4} + k, and one more producer warp
-// moves each B row left by its class's t in place, where the consumers read
-// it (row k of the slice: row k / 4 of class k mod 4's box).
-// Elements left of a row's start (the previous row's tail, already inside
-// the same 16-byte block) land in the box but are never read; the maps'
-// extents end at each row's last element, so everything past it reads as
-// the tensor map's zero fill.
-struct ResMaps {
-    CUtensorMap m[4];  // residue classes j = 0..3
-};
+// RES (residue-class tensor maps for operands of any alignment): see
+// res_maps.cuh; the kernel's tiles are the maps' 128 x 128 tiles with
+// 32-deep slices.
+static_assert(kResTileRows == kBM && kResTileCols == kBN && kResSliceK == kBK, "residue-class box geometry");
 template <bool RES>
 struct FfmaMap {
-    using type = CUtensorMap;
+    using type = MapsFor<RES>;
 };
-template <>
-struct FfmaMap<true> {
-    using type = ResMaps;
-};
-constexpr int kResABox = kBK + 4;                          // floats per A box row
-constexpr int kResBBox = kBN + 4;                          // floats per B box row
-constexpr int kResAPlaneBytes = (kBM / 4) * kResABox * 4;  // one class of an A slice: 32 rows (4608 B)
-constexpr int kResBPlaneBytes = (kBK / 4) * kResBBox * 4;  // one class of a B slice: 8 rows (4224 B)
-static_assert(kResAPlaneBytes % 128 == 0 && kResBPlaneBytes % 128 == 0, "tensor-copy destinations: 128-byte aligned");
 // A and B slices as loaded (A slices without RES: kStageABytes; B slices:
 // ffma_stage_b_bytes).
-__device__ __forceinline__ const CUtensorMap& res_map(const ResMaps& r, int j) { return r.m[j]; }
-__device__ __forceinline__ const CUtensorMap& res_map(const CUtensorMap& r, int) { return r; }
 template <bool RES, int BK = kBK>
 __host__ __device__ constexpr int ffma_load_a_bytes() {
     return RES ? 4 * kResAPlaneBytes : kBM * BK * 4;
@@ -653,7 +628,7 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER, BNK || RES>(), ffma_min
                             float* const plane0 = reinterpret_cast<float*>(smem + kBLoadOff + s * kBLoadBytes);
 #pragma unroll 1
                             for (int j = 0; j < 4; ++j) {
-                                const int t = (p.b_shift >> (2 * j)) & 3;
+                                const int t = res_shift(p.b_shift, j);
                                 if (t == 0) continue;  // (warp-uniform) already in place
                                 float* const plane = plane0 + j * (kResBPlaneBytes / 4) + 4 * lane;
                                 float4 o[kBK / 4];
@@ -690,7 +665,7 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER, BNK || RES>(), ffma_min
                                 float4 r[4];
 #pragma unroll
                                 for (int j = 0; j < 4; ++j) {
-                                    const int t = (p.a_shift >> (2 * j)) & 3;
+                                    const int t = res_shift(p.a_shift, j);
                                     const float* const row = raw + j * (kResAPlaneBytes / 4) + 4 * c;
                                     const float4 v0 = *reinterpret_cast<const float4*>(row);
                                     r[j] = v0;

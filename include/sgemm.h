@@ -239,9 +239,12 @@ int sgemm_f32_gemm(int transa, int transb,
  * small = tf32(x - big), and three TF32 products (small*big + big*small +
  * big*big) are accumulated in float32 in tensor memory.  The dropped terms
  * are below 2^-22 |a||b| each.  The kernels read their operands through
- * tensor maps: operands without 16-byte aligned bases and row strides are
- * copied into pitched rows first when 2MNK >= 2^30; smaller such calls, and
- * K = 0, run the sgemm_f32 kernels.  Tiles of 128 x 256 when those number at
+ * tensor maps: operands without 16-byte aligned bases and row strides go to
+ * the 128 x 128 kernel on residue-class maps (four per operand, one per
+ * class of rows mod 4; M, K >= 4) when that kernel is the choice anyway or
+ * 2MNK < 2^30, and are copied into pitched rows first otherwise; K = 0, and
+ * misaligned calls with M or K < 4, run the sgemm_f32 kernels.  Tiles of
+ * 128 x 256 when those number at
  * least half the SMs (with B's TF32 parts split in a pass before the kernel
  * when M >= 1024), else 128 x 128 (see sgemm_3xtf32_ex).
  * Tensor cores are not on the pages' own path; this entry is reported
@@ -339,9 +342,9 @@ typedef struct sgemm_options {
                              CTAs x (128 KiB + 4 bytes)) */
     int repack;           /* 0 = auto, 1 = off, 2 = on: an operand whose base
                              or row pitch is not a multiple of 16 bytes is
-                             first copied into rows of ceil(width / 4) x 4
-                             floats (a pool workspace of M x K4 and/or
-                             K x N4 floats) and the product runs on the
+                             first copied into rows of ceil(width / 32) x 32
+                             floats (a pool workspace of M x K32 and/or
+                             K x N32 floats) and the product runs on the
                              tensor-map path; auto = on when no producer is
                              forced and 2MNK >= 2^35 (below that the
                              residue-class tensor maps read such operands in

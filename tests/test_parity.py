@@ -331,8 +331,10 @@ def test_leading_dimensions_and_guard_bands():
 
 
 @pytest.mark.parametrize("opt", [dict(), dict(producer=5, stages=3), dict(producer=5, stream_k=1, split_k=1),
-                                 dict(producer=5, split_k=2), dict(producer=5, stages=4)],
-                         ids=["auto", "stages3", "plain-grid", "split2", "stages4-no-staging"])
+                                 dict(producer=5, split_k=2), dict(producer=5, stages=4), dict(l2_hint=1),
+                                 dict(producer=8), dict(producer=8, stages=3), dict(producer=8, stages=4)],
+                         ids=["auto", "stages3", "plain-grid", "split2", "stages4-no-staging", "no-policy",
+                              "res", "res-stages3", "res-stages4-no-staging"])
 @pytest.mark.parametrize("c_offset,N", [(0, 1004), (0, 1001), (1, 1004)])
 def test_tensor_map_stores_of_c_and_guard_bands(opt, c_offset, N):
     """The 128 x 128 kernels that write finished tiles of C through a staging
@@ -856,3 +858,25 @@ def test_residue_maps_rejections():
         A, B = make_operands(M, 8, K, "uniform", 53)
         with pytest.raises(g._lib.SgemmError):
             g.sgemm_f32_ex(to_device(A), to_device(B), producer=8)
+
+
+@pytest.mark.parametrize("dist", ["uniform", "int"])
+def test_residue_maps_with_tensor_map_stores(dist):
+    """Misaligned A (rows of 4097 floats) and B (rows of 1005) read in place by
+    the class maps, with a K loop long enough (129 slices) for the finished
+    tiles to go out by tensor-map stores into a 16-byte aligned C with padded
+    rows; C's padding and the floats around it keep a sentinel."""
+    M, N, K = 600, 1004, 4100
+    A, B = make_operands(M, N, K, dist, 54)
+    dA, dB = to_device(A, 4101, offset=3), to_device(B, 1005, offset=2)
+    ldc, guard, sentinel = 1012, 64, -12345.0
+    store = torch.full((guard + M * ldc + guard,), sentinel, device="cuda")
+    dC = store[guard:guard + M * ldc].view(M, ldc)[:, :N]
+    assert g.describe(dA, dB, dC).endswith("/res")
+    g.sgemm_f32(dA, dB, dC)
+    torch.cuda.synchronize()
+    C64, bound = oracle.gemm_f64(A.numpy(), B.numpy(), with_bound=(dist != "int"))
+    check(dC.cpu().numpy(), C64, bound, exact=(dist == "int"), what=f"res + tma store {dist}")
+    s = store.cpu().numpy()
+    assert np.all(s[:guard] == sentinel) and np.all(s[-guard:] == sentinel)
+    assert np.all(store[guard:guard + M * ldc].view(M, ldc)[:, N:].cpu().numpy() == sentinel)

@@ -96,9 +96,10 @@ def test_named_problem_8192_sampled_rows(dist, variant):
 
 
 @pytest.mark.parametrize("variant", VARIANTS)
-def test_ragged_problem_repacked(variant):
-    """1023 x 1025 x 1027: rows of 1027 floats are not 16-byte multiples; the
-    operands are repacked into pitched rows and the tensor-core kernel runs."""
+def test_ragged_problem_misaligned_rows(variant):
+    """1023 x 1025 x 1027: rows of 1027 floats are not 16-byte multiples.  The
+    automatic choice and variant 1 read them in place through residue-class
+    tensor maps; variants 2-4 repack the operands into pitched rows first."""
     p = PROBLEMS["ragged_1023x1025x1027"]
     A, B = problem_operands(p)
     C64, bound = oracle.gemm_f64(A.numpy(), B.numpy())
@@ -108,12 +109,52 @@ def test_ragged_problem_repacked(variant):
           exact=True, what=p.name + " int")
 
 
-def test_small_misaligned_falls_back_and_matches():
-    """Small products with misaligned rows run the FFMA kernels (cp.async);
-    the contract is the same."""
-    A, B = make_operands(200, 301, 333, "uniform", 94)
-    C64, bound = oracle.gemm_f64(A.numpy(), B.numpy())
-    check(run(A, B), C64, bound, exact=False, what="200x301x333")
+def test_small_misaligned_on_class_maps_or_ffma():
+    """Small products with misaligned rows run the split-tile kernel on
+    residue-class maps; with fewer than 4 rows of A (a class without a row)
+    the FFMA kernels, under the same contract."""
+    for M, N, K in ((200, 301, 333), (3, 301, 333), (200, 301, 3)):
+        A, B = make_operands(M, N, K, "uniform", 94)
+        C64, bound = oracle.gemm_f64(A.numpy(), B.numpy())
+        check(run(A, B), C64, bound, exact=False, what=f"{M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("offsets", [(0, 0), (1, 0), (0, 2), (3, 1), (2, 3)])
+@pytest.mark.parametrize("pads", [(0, 0), (1, 3), (5, 2), (2, 0)])
+def test_residue_maps_any_alignment_every_element(offsets, pads):
+    """Bases 0-3 floats off a 16-byte boundary and rows of any length: the
+    split-tile kernel on residue-class maps (automatic below 2^30 flop, and
+    with its K split over 2 CTAs: 700 x 900 x 611 has 48 tiles); every element
+    against the oracle, integer inputs exactly."""
+    M, N, K = 700, 900, 611
+    oa, ob = offsets
+    lda, ldb = K + pads[0], N + pads[1]
+    for dist in ("uniform", "int"):
+        A, B = make_operands(M, N, K, dist, 55)
+        dA, dB = to_device(A, lda, offset=oa), to_device(B, ldb, offset=ob)
+        C = g.sgemm_3xtf32(dA, dB)
+        torch.cuda.synchronize()
+        C64, bound = oracle.gemm_f64(A.numpy(), B.numpy(), with_bound=(dist != "int"))
+        check(C.cpu().numpy(), C64, bound, exact=(dist == "int"), what=f"3xtf32 res {offsets} {pads} {dist}")
+
+
+@pytest.mark.parametrize("split_k", [1, 2, 3, 4])
+@pytest.mark.parametrize("shape", [(4, 5, 4), (7, 130, 33), (131, 257, 1027), (1023, 1025, 4099)])
+def test_residue_maps_forced_splits_and_smallest_classes(split_k, shape):
+    """Variant 1 on residue-class maps with the K split forced (1 = none, 2-4
+    parts), from the fewest rows the classes allow (M, K = 4) to a product
+    above 2^30 flop (forced variant 1 keeps the class maps there); pitches
+    K + 1 and N + 3, bases off by one and two floats."""
+    M, N, K = shape
+    if split_k > (K + 31) // 32:
+        pytest.skip("fewer K slices than parts")
+    for dist in ("uniform", "int"):
+        A, B = make_operands(M, N, K, dist, 56)
+        dA, dB = to_device(A, K + 1, offset=1), to_device(B, N + 3, offset=2)
+        C = g.sgemm_3xtf32_ex(dA, dB, variant=1, split_k=split_k)
+        torch.cuda.synchronize()
+        C64, bound = oracle.gemm_f64(A.numpy(), B.numpy(), with_bound=(dist != "int"))
+        check(C.cpu().numpy(), C64, bound, exact=(dist == "int"), what=f"3xtf32 res {shape} s{split_k} {dist}")
 
 
 @pytest.mark.parametrize("variant", VARIANTS)
