@@ -49,7 +49,7 @@ L2_FLUSH_BYTES = 512 << 20
 # lanes x 2 flops per FMA x 2070 MHz (maximum SM clock).
 SMS, FP32_LANES_PER_SM, SM_MAX_MHZ = 152, 128, 2070.0
 DERIVED_FP32_PEAK_TFLOPS = SMS * FP32_LANES_PER_SM * 2 * SM_MAX_MHZ * 1e6 / 1e12
-KERNEL_SOURCES = ["sgemm_ffma.cuh", "ptx.cuh", "sgemm_ffma_tma.cu", "sgemm_ffma_scaled.cu", "sgemm_ffma_tma_x.cu"]
+KERNEL_SOURCES = ["sgemm_ffma.cuh", "ptx.cuh", "res_maps.cuh", "sgemm_ffma_tma.cu", "sgemm_ffma_scaled.cu", "sgemm_ffma_tma_x.cu"]
 # Nominal dense TF32 tensor rate of GB300 (context for the three-product entry).
 TF32_DENSE_NOMINAL_TFLOPS = 1100.0
 
