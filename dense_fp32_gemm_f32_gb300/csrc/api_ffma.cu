@@ -145,7 +145,7 @@ int run_ffma(int M, int N, int K, const float* A, int lda, const float* B, int l
         }
     }
     // Residue-class maps (pl.res): four per operand, boxes of 36 k x 32 rows
-    // of A and 132 columns x 8 rows of B (see ResMaps).
+    // of A and 132 columns x 8 rows of B (res_maps.cuh).
     ResMaps resA, resB;
     std::memset(&resA, 0, sizeof resA);
     std::memset(&resB, 0, sizeof resB);

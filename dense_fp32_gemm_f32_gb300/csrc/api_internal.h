@@ -230,7 +230,7 @@ struct Plan {
     bool a_mn = false;    // A stored transposed (K x M): the transposed-A kernels
     bool b_nk = false;    // B stored transposed (N x K): the kernels with a B-transposing warp
     int bk = kBK;         // K slice depth (32, or 16 for sgemm_options.tile_k = 16)
-    bool res = false;     // A and B read through residue-class tensor maps (any alignment; see ResMaps)
+    bool res = false;     // A and B read through residue-class tensor maps (any alignment; res_maps.cuh)
 };
 
 // Epilogue scaling of the general entry: C = alpha * A B + beta * C.

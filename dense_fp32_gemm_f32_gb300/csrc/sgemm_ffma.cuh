@@ -225,8 +225,9 @@ struct FfmaParams {
     unsigned int* status;  // per-device sticky status word (error bits)
     // Epilogue of the SCALED kernels: C = alpha * (A B) + beta * C (C is read
     // only when beta != 0).
-    float alpha, beta;    // RES kernels: bits 2j, 2j + 1 hold t_j, the offset in floats of the rows
-    // of residue class j inside their 16-byte blocks (see ResMaps).
+    float alpha, beta;
+    // RES kernels: bits 2j, 2j + 1 hold t_j, the offset in floats of the rows
+    // of residue class j inside their 16-byte blocks (res_maps.cuh).
     int a_shift, b_shift;
 };
 
@@ -235,8 +236,8 @@ constexpr int kMaxSmemBytes = 232448;
 
 // XA: the stage also holds the transposed copy of its A slice (kProducerTmaX);
 // XB: and of its B slice (BNK).
-// RES: the slices as loaded are the residue-class boxes (and XB holds B
-// shifted into place).
+// RES: the slices as loaded are the residue-class boxes (B is shifted in
+// place, so RES needs no XB copy).
 template <int STAGES, int BN = kBN, bool XA = false, bool XB = false, int BK = kBK, bool RES = false>
 __host__ __device__ constexpr int ffma_ring_bytes() {
     return STAGES * (ffma_load_a_bytes<RES, BK>() + ffma_load_b_bytes<RES, BN, BK>() +
@@ -314,10 +315,10 @@ __device__ __forceinline__ uint32_t swz128(int r, int c) {
 // as stored only): half the shared memory per stage and twice the slices, so
 // that small problems' work divides into finer stream-K units.
 //
-// RES: A and B of any alignment through residue-class tensor maps (see
-// ResMaps; tmA and tmB are then four maps each, and FfmaParams a_shift,
-// b_shift hold the classes' offsets); the transposing producer, 128 x 128
-// tiles, A and B as stored, 32-deep slices.
+// RES: A and B of any alignment through residue-class tensor maps
+// (res_maps.cuh; tmA and tmB are then four maps each, and FfmaParams
+// a_shift, b_shift hold the classes' offsets); the transposing producer,
+// 128 x 128 tiles, A and B as stored, 32-deep slices.
 template <int STAGES, int PRODUCER, int MATH, int BN = kBN, bool SCALED = false, bool AMN = false, bool BNK = false,
           int BK = kBK, bool RES = false>
 __global__ void __launch_bounds__(ffma_threads<PRODUCER, BNK || RES>(), ffma_min_blocks<PRODUCER>())
@@ -739,7 +740,7 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER, BNK || RES>(), ffma_min
                 if (skip_here && it == p.skip_stage - 1) continue;
                 const int k0 = kt * BK;
                 if (RES) {
-                    // Four class boxes per operand (see ResMaps): A rows
+                    // Four class boxes per operand (res_maps.cuh): A rows
                     // m0 / 4 .. + 31 of each class from k0; B rows k0 / 4 ..
                     // + 7 of each class from column n0.
                     mbar_arrive_expect_tx(full_bar(s), kStageBytes);

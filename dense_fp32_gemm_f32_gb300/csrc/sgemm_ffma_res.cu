@@ -1,5 +1,5 @@
 // Instantiations of the FFMA kernel on residue-class tensor maps (operands of
-// any alignment read in place; see ResMaps): TMA producer warp, two
+// any alignment read in place; res_maps.cuh): TMA producer warp, two
 // A-transposing warps and one B-shifting warp; 128 x 128 tiles, paired FMA,
 // plain epilogue.
 #include "kernels.h"
