@@ -1016,12 +1016,46 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER, BNK || RES>(), ffma_min
             bulk_commit_group();
         }
     };
+    // C whose rows are not 16-byte addressable (a base or ldc off the
+    // 16-byte grid): the consumers stage the finished tile as for the
+    // tensor-map store, then write it out row by row, consumer warp w taking
+    // rows w, w + 8, ... and lane l the columns l, l + 32, l + 64, l + 96 of
+    // each, so that every store instruction writes 128 consecutive bytes
+    // (the 4-byte stores of the threads' own blocks write 4 rows x 8 groups
+    // of 4 floats an instruction).  Measured on GB300: 1023 x 1025 x 1027
+    // 56.4 us with C's rows of 1025 floats, 53.7 with the same rows padded to
+    // 1028 (16-byte stores).
+    auto store_c_rows = [&](int tile) {
+        int tm_, tn_;
+        tile_rc(tile, p.tiles_n, p.tiles_m, p.group_m, tm_, tn_);
+        float* const stg = reinterpret_cast<float*>(smem + kStgOff);
+        consumer_sync();  // every row of the previous tile has been read
+        const int col0 = wn * (BN / WN) + tn * 4;
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+#pragma unroll
+            for (int h = 0; h < H; ++h)
+                *reinterpret_cast<float4*>(stg + row_in_tile(i) * BN + col0 + 32 * h) =
+                    make_float4(acc[i][2 * h].x, acc[i][2 * h].y, acc[i][2 * h + 1].x, acc[i][2 * h + 1].y);
+        consumer_sync();
+        const int row0 = tm_ * kBM, c0 = tn_ * BN;
+        const int nval = min(BN, p.N - c0);
+        for (int r = warp; r < kBM && row0 + r < p.M; r += CW) {
+            float* const crow = p.C + static_cast<long long>(row0 + r) * p.ldc + c0;
+            const float* const srow = stg + r * BN;
+#pragma unroll
+            for (int c = lane; c < BN; c += 32)
+                if (c < nval) crow[c] = srow[c];
+        }
+    };
     auto store_c = [&](int tile) {
         if constexpr (SCALED) {
             store_c_scaled(tile);
         } else if constexpr (kStg) {
             if (p.tma_store) {
                 store_c_tma(tile);
+            } else if (!p.vec_store) {
+                store_c_rows(tile);
             } else {
                 store_c_plain(tile);
             }
