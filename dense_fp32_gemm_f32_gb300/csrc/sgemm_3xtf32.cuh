@@ -426,6 +426,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             float* wrow =
                 second ? p.ws + ((static_cast<long long>(local) * (ks - 1) + part - 1) * T::kBM + 32 * q + lane) * BN
                        : nullptr;
+            // C without 16-byte addressable rows: each 32 x 32 chunk passes
+            // through a patch of the (now idle) split stages, 33 floats a row,
+            // and goes out a row at a time, lane = column, so that a store
+            // instruction writes 128 consecutive bytes instead of one float
+            // in each of 32 rows.  (The MMAs that read the split stages have
+            // completed: acc_full.)
+            float* const patch =
+                reinterpret_cast<float*>(smem_raw + (split(0) - raw_base)) + (warp - 2) * (32 * 33);
 #pragma unroll
             for (int cc = 0; cc < kChunksPerWarp; ++cc) {
                 const int ch = half * kChunksPerWarp + cc;
@@ -439,18 +447,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         *reinterpret_cast<float4*>(wrow + 32 * ch + e) =
                             make_float4(__uint_as_float(v[e]), __uint_as_float(v[e + 1]), __uint_as_float(v[e + 2]),
                                         __uint_as_float(v[e + 3]));
-                } else if (row < p.M) {
-                    if (p.vec_store && col + 31 < p.N) {
+                } else if (p.vec_store && col + 31 < p.N) {  // (warp-uniform)
+                    if (row < p.M) {
 #pragma unroll
                         for (int e = 0; e < 32; e += 4)
                             *reinterpret_cast<float4*>(crow + col + e) =
                                 make_float4(__uint_as_float(v[e]), __uint_as_float(v[e + 1]),
                                             __uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
-                    } else {
-#pragma unroll
-                        for (int e = 0; e < 32; ++e)
-                            if (col + e < p.N) crow[col + e] = __uint_as_float(v[e]);
                     }
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) patch[lane * 33 + e] = __uint_as_float(v[e]);
+                    __syncwarp();
+                    const int r0 = m0 + 32 * q;
+                    for (int rr = 0; rr < 32 && r0 + rr < p.M; ++rr)
+                        if (col + lane < p.N)
+                            p.C[static_cast<long long>(r0 + rr) * p.ldc + col + lane] = patch[rr * 33 + lane];
+                    __syncwarp();  // the patch is read before the next chunk overwrites it
                 }
             }
         } else if (nkt > 0) {
