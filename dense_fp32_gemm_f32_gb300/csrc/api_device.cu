@@ -117,7 +117,8 @@ int init_device(int dev, DeviceState& st) {
                 if (set_smem_attr(ffma_kernel_scaled(prod, s, math)) != SGEMM_OK) return SGEMM_ERR_CUDA;
             if (set_smem_attr(ffma_kernel_tma_x16(s, math)) != SGEMM_OK) return SGEMM_ERR_CUDA;
             if (set_smem_attr(ffma_kernel_ldg(s, math)) != SGEMM_OK) return SGEMM_ERR_CUDA;
-            if (set_smem_attr(ffma_kernel_res(s, math)) != SGEMM_OK) return SGEMM_ERR_CUDA;
+            for (bool scaled : {false, true})
+                if (set_smem_attr(ffma_kernel_res(s, math, scaled)) != SGEMM_OK) return SGEMM_ERR_CUDA;
             for (bool scaled : {false, true}) {
                 if (set_smem_attr(ffma_kernel_bnk(s == 1, scaled)) != SGEMM_OK) return SGEMM_ERR_CUDA;
                 if (set_smem_attr(ffma_kernel_amn(s, math, scaled)) != SGEMM_OK) return SGEMM_ERR_CUDA;

@@ -112,7 +112,7 @@ int run_ffma(int M, int N, int K, const float* A, int lda, const float* B, int l
         a_t.release();
     };
 
-    const KernelEntry k = (pl.res && scaled) ? KernelEntry{nullptr, 0, 0}  // (make_plan rules this out)
+    const KernelEntry k = pl.res ? ffma_kernel_res(pl.stages, pl.math, scaled)
                           : pl.b_nk ? ffma_kernel_bnk(pl.a_mn, scaled)
                           : pl.a_mn ? (pl.bn == kBN ? ffma_kernel_amn(pl.stages, pl.math, scaled)
                                                   : scaled ? KernelEntry{nullptr, 0, 0} : ffma_kernel(pl))

@@ -151,11 +151,12 @@ int make_plan(const DeviceState& st, int M, int N, int K, const float* A, int ld
     const int misaligned = (a_mn || tma_ok(A, lda) ? 0 : 1) | (tma_ok(B, ldb) ? 0 : 2);
     // Residue-class tensor maps (operands of any alignment read in place):
     // every class of rows mod 4 must hold a row of A and of B (M, K >= 4);
-    // the kernels have 128 x 128 tiles, 32-deep slices, 2 to 4 stages,
-    // paired FMA and the plain epilogue.  Automatic for misaligned operands
-    // below kResMaxFlops, and whenever copies are ruled out (repack = 1).
+    // the kernels have 128 x 128 tiles, 32-deep slices and paired FMA, with
+    // the plain epilogue on 2 to 4 stages and the scaled one on 2.
+    // Automatic for misaligned operands below kResMaxFlops, and whenever
+    // copies are ruled out (repack = 1).
     const double flops = 2.0 * static_cast<double>(M) * static_cast<double>(N) * static_cast<double>(K);
-    const bool res_ok = !a_mn && !b_nk && !scaled && M >= 4 && K >= 4 &&
+    const bool res_ok = !a_mn && !b_nk && M >= 4 && K >= 4 && !(scaled && opt && opt->stages && opt->stages != 2) &&
                         !(opt && opt->tile_n && opt->tile_n != kBN) &&
                         !(opt && opt->tile_k && opt->tile_k != kBK) &&
                         !(opt && opt->stages && (opt->stages < 2 || opt->stages > 4)) &&
@@ -252,7 +253,8 @@ int make_plan(const DeviceState& st, int M, int N, int K, const float* A, int ld
         (pl.stages < 2 || pl.stages > (pl.producer == kProducerTmaX && pl.bk == kBK16 ? 6 : 4)))
         return SGEMM_ERR_INVALID_ARG;
     if (pl.producer == kProducerTmaX && pl.bn != kBN) return SGEMM_ERR_INVALID_ARG;
-    if (pl.res && (pl.stages > 4 || pl.math != kMathFfma2 || pl.bk != kBK)) return SGEMM_ERR_INVALID_ARG;
+    if (pl.res && (pl.stages > (scaled ? 2 : 4) || pl.math != kMathFfma2 || pl.bk != kBK))
+        return SGEMM_ERR_INVALID_ARG;
     if (pl.producer == kProducerLdg && (pl.bn != kBN || pl.bk != kBK || pl.stages < 2 || pl.stages > 4))
         return SGEMM_ERR_INVALID_ARG;
     if (pl.bk == kBK16 && (pl.producer != kProducerTmaX || pl.stages == 5)) return SGEMM_ERR_INVALID_ARG;

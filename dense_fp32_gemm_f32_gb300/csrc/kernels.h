@@ -45,9 +45,9 @@ KernelEntry ffma_kernel_tma_x16(int stages, int math);
 KernelEntry ffma_kernel_bnk(bool a_mn, bool scaled);
 // FFMA kernels on residue-class tensor maps (operands of any alignment, read
 // in place: four maps per operand, one per class of rows mod 4, and a
-// B-shifting producer warp); 128 x 128 tiles, paired FMA, plain epilogue;
-// stages {2,3,4}.
-KernelEntry ffma_kernel_res(int stages, int math);
+// B-shifting producer warp); 128 x 128 tiles, paired FMA; plain epilogue on
+// stages {2,3,4}, `scaled` (the general entry's epilogue) on 2.
+KernelEntry ffma_kernel_res(int stages, int math, bool scaled = false);
 // FFMA kernels fed by loader warps (operands of any alignment, no tensor
 // maps): 128 x 128 tiles, paired FMA, plain epilogue; stages {2,3,4}.
 KernelEntry ffma_kernel_ldg(int stages, int math);

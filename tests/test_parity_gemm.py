@@ -198,3 +198,24 @@ def test_transposed_b_skinny_every_element(ta, dist):
     C = run(A, B, None, alpha=1.0, beta=0.0, ta=ta, tb=1)
     ref, bound = oracle.gemm_general_f64(A, B, alpha=1.0, beta=0.0, transa=ta, transb=1, with_bound=dist != "int")
     check(C, ref, None if dist == "int" else bound, exact=dist == "int", what=f"skinny t{ta}1 {dist}")
+
+
+@pytest.mark.parametrize("dist", ["uniform", "int"])
+@pytest.mark.parametrize("offsets", [(0, 0, 0), (1, 3, 2)])
+def test_general_misaligned_rows_on_class_maps(dist, offsets):
+    """The ragged named shape in the stored order (rows of 1027 and 1025
+    floats, bases off the 16-byte grid by `offsets` floats): A and B read in
+    place through the residue-class maps with the scaled epilogue; integer
+    inputs with integer alpha and beta exactly."""
+    M, N, K = 1023, 1025, 1027
+    a, b = (x.numpy() for x in make_operands(M, N, K, dist, 211))
+    cin = make_operands(M, 1, N, dist, 212)[0].numpy()
+    alpha, beta = (2.0, -1.0) if dist == "int" else (0.75, -1.25)
+    oa, ob, oc = offsets
+    dA = to_device(torch.from_numpy(a), K, offset=oa)
+    dB = to_device(torch.from_numpy(b), N, offset=ob)
+    dC = to_device(torch.from_numpy(cin), N, offset=oc)
+    g.sgemm_f32_gemm(dA, dB, dC, alpha=alpha, beta=beta)
+    torch.cuda.synchronize()
+    ref, bound = oracle.gemm_general_f64(a, b, cin, alpha=alpha, beta=beta, transa=0, transb=0)
+    check(dC.cpu().numpy(), ref, bound, exact=(dist == "int"), what=f"class maps, scaled, {offsets} {dist}")
