@@ -435,6 +435,9 @@ int run_gemm(int transa, int transb, int M, int N, int K, float alpha, const flo
     if (product && M > 0 && !A) return SGEMM_ERR_INVALID_ARG;
     if (product && N > 0 && !B) return SGEMM_ERR_INVALID_ARG;
     if (M > 0 && N > 0 && !C) return SGEMM_ERR_INVALID_ARG;
+    // Arrays of float: 4-byte aligned (the copies below index them as such).
+    if (((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B) | reinterpret_cast<uintptr_t>(C)) & 3u) != 0)
+        return SGEMM_ERR_INVALID_ARG;
     const size_t cb = span_bytes(M, N, ldc);
     if (product && (ranges_overlap(C, cb, A, transa ? span_bytes(K, M, lda) : span_bytes(M, K, lda)) ||
                     ranges_overlap(C, cb, B, transb ? span_bytes(N, K, ldb) : span_bytes(K, N, ldb))))

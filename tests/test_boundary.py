@@ -131,6 +131,9 @@ def test_binding_rejects_cpu_tensors():
         (1, 1, 4, 4, 4, 1.0, 0, 4, FAKE_B, 4, 0.0, FAKE_C, 4),  # A NULL
         (0, 0, 4, 4, 4, 1.0, FAKE_A, 4, FAKE_B, 4, 1.0, 0, 4),  # C NULL
         (1, 0, 4, 4, 4, 1.0, FAKE_A, 4, FAKE_B, 4, 0.0, FAKE_A + 32, 4),  # C overlaps (transposed) A
+        (1, 1, 4, 4, 4, 1.0, FAKE_A + 2, 4, FAKE_B, 4, 0.0, FAKE_C, 4),  # A not float-aligned
+        (0, 1, 4, 4, 4, 1.0, FAKE_A, 4, FAKE_B + 1, 4, 0.0, FAKE_C, 4),  # B not float-aligned
+        (0, 0, 4, 4, 4, 1.0, FAKE_A, 4, FAKE_B, 4, 0.5, FAKE_C + 2, 4),  # C not float-aligned
     ],
 )
 def test_general_entry_invalid_arguments_rejected_on_host(args):
