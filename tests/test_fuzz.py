@@ -18,6 +18,7 @@ OPTIONS = [
     dict(stream_k=2), dict(stream_k=1), dict(split_k=2), dict(split_k=3), dict(tile_n=256), dict(tile_n=64),
     dict(a_layout=2), dict(a_layout=1), dict(repack=2), dict(math=1), dict(stages=3),
     dict(group_m=1), dict(group_m=3), dict(producer=5, stream_k=2), dict(a_layout=2, stream_k=2), dict(tile_n=256, stream_k=2), dict(producer=6),
+    dict(producer=8), dict(producer=8, stages=3), dict(producer=8, split_k=2), dict(repack=1), dict(l2_hint=4),
 ]
 
 
@@ -37,7 +38,7 @@ def _dim(rng):
     return int(rng.integers(1, 701))
 
 
-@pytest.mark.parametrize("case", range(48))
+@pytest.mark.parametrize("case", range(64))
 def test_fuzz_sgemm_f32_ex(case):
     rng = np.random.default_rng(1000 + case)
     M, N, K = _dim(rng), _dim(rng), _dim(rng)
