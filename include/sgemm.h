@@ -188,7 +188,7 @@ int sgemm_f32_noalloc(int M, int N, int K,
  * more are pipelined: K is cut into up to four growing chunks, each chunk's
  * columns of A and rows of B are copied in while the product of the chunk
  * before runs (C accumulating on the device), and the last chunk's product
- * runs in up to six shrinking blocks of whole 128-row tiles whose rows of C
+ * runs in up to five shrinking blocks of whole 128-row tiles whose rows of C
  * are copied out while the next block computes.  Smaller products run as
  * one block.  It returns once all of that is enqueued: C holds the result
  * after `stream` is synchronised (all copies are ordered before `stream`'s
