@@ -333,3 +333,28 @@ def test_timeout_is_reported_and_recovers(variant, split_k):
     assert g.check_status() == 0
     C64, bound = oracle.gemm_f64(A.numpy(), B.numpy())
     check(C.cpu().numpy(), C64, bound, exact=False, what="after timeout")
+
+
+@pytest.mark.parametrize("variant,split_k", [(0, 0), (1, 1), (1, 2), (3, 0), (4, 0), (4, 2)])
+@pytest.mark.parametrize("c_offset", [0, 1])
+def test_unaligned_output_guard_bands(variant, split_k, c_offset):
+    """C with rows of 1029 floats (and, with c_offset = 1, a base off the
+    16-byte grid) written by the epilogue's shared-memory patches (or the K
+    split's finishing CTA): every element against the oracle, and the row
+    padding and the floats around C keep their sentinel."""
+    M, N, K = 700, 1025, 600
+    A, B = make_operands(M, N, K, "uniform", 81)
+    ldc, guard, sentinel = 1029, 64 + c_offset, -12345.0
+    store = torch.full((guard + M * ldc + 64,), sentinel, device="cuda")
+    dC = store[guard:guard + M * ldc].view(M, ldc)[:, :N]
+    dA, dB = to_device(A), to_device(B, 1028)
+    if variant or split_k:
+        g.sgemm_3xtf32_ex(dA, dB, dC, variant=variant, split_k=split_k)
+    else:
+        g.sgemm_3xtf32(dA, dB, dC)
+    torch.cuda.synchronize()
+    C64, bound = oracle.gemm_f64(A.numpy(), B.numpy())
+    check(dC.cpu().numpy(), C64, bound, exact=False, what=f"3xtf32 v{variant} s{split_k} c+{c_offset}")
+    s = store.cpu().numpy()
+    assert np.all(s[:guard] == sentinel) and np.all(s[guard + M * ldc:] == sentinel)
+    assert np.all(store[guard:guard + M * ldc].view(M, ldc)[:, N:].cpu().numpy() == sentinel)
