@@ -880,3 +880,33 @@ def test_residue_maps_with_tensor_map_stores(dist):
     s = store.cpu().numpy()
     assert np.all(s[:guard] == sentinel) and np.all(s[-guard:] == sentinel)
     assert np.all(store[guard:guard + M * ldc].view(M, ldc)[:, N:].cpu().numpy() == sentinel)
+
+
+def test_cuda_graph_capture_on_residue_class_maps():
+    """A call on misaligned rows (the residue-class maps: four tensor maps per
+    operand, encoded at capture with the operands' addresses) captured in a
+    CUDA graph; each replay recomputes from the current contents."""
+    M, N, K = 1023, 1025, 1027
+    A, B = make_operands(M, N, K, "uniform", 57)
+    dA, dB = to_device(A, offset=1), to_device(B, offset=2)
+    dC = torch.empty((M, N), device="cuda")
+    assert g.describe(dA, dB, dC).endswith("/res")
+    g.sgemm_f32(dA, dB, dC)  # outside the capture first
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            g.sgemm_f32(dA, dB, dC, stream=s)
+    for seed in (58, 59):
+        A2, B2 = make_operands(M, N, K, "uniform", seed)
+        dA.copy_(A2)
+        dB.copy_(B2)
+        dC.fill_(float("nan"))
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            graph.replay()
+        torch.cuda.synchronize()
+        C64, bound = oracle.gemm_f64(A2.numpy(), B2.numpy())
+        check(dC.cpu().numpy(), C64, bound, exact=False, what=f"graph replay on class maps {seed}")
