@@ -910,3 +910,19 @@ def test_cuda_graph_capture_on_residue_class_maps():
         torch.cuda.synchronize()
         C64, bound = oracle.gemm_f64(A2.numpy(), B2.numpy())
         check(dC.cpu().numpy(), C64, bound, exact=False, what=f"graph replay on class maps {seed}")
+
+
+# ---------------------------------------------------------------- extreme shapes
+
+@pytest.mark.parametrize("shape,dist", [((1 << 20, 8, 64), "int"), ((8, 1 << 20, 64), "int"),
+                                        ((1 << 20, 8, 64), "uniform"), ((128, 128, 1 << 20), "uniform")])
+def test_extreme_shapes_every_element(shape, dist):
+    """A million rows (8192 rows of tiles), a million columns (8192 columns
+    of tiles, one tile row) and a million-deep K on one output tile (every
+    SM's stream-K share of 32768 slices, one finishing CTA adding 151 partial
+    tiles): every element against the oracle, integer inputs exactly."""
+    M, N, K = shape
+    A, B = make_operands(M, N, K, dist, 60)
+    C = run(A, B)
+    C64, bound = oracle.gemm_f64(A.numpy(), B.numpy(), with_bound=(dist != "int"))
+    check(C, C64, bound, exact=(dist == "int"), what=f"{shape} {dist}")
