@@ -926,3 +926,17 @@ def test_extreme_shapes_every_element(shape, dist):
     C = run(A, B)
     C64, bound = oracle.gemm_f64(A.numpy(), B.numpy(), with_bound=(dist != "int"))
     check(C, C64, bound, exact=(dist == "int"), what=f"{shape} {dist}")
+
+
+@pytest.mark.parametrize("dist", ["int", "uniform"])
+def test_extreme_shape_on_residue_class_maps(dist):
+    """A million rows of 63 floats times rows of 9 floats (neither a 16-byte
+    multiple): the residue-class maps over 8192 rows of tiles."""
+    M, N, K = 1 << 20, 9, 63
+    A, B = make_operands(M, N, K, dist, 61)
+    dA, dB = to_device(A), to_device(B)
+    assert g.describe(dA, dB).endswith("/res")
+    C = g.sgemm_f32(dA, dB)
+    torch.cuda.synchronize()
+    C64, bound = oracle.gemm_f64(A.numpy(), B.numpy(), with_bound=(dist != "int"))
+    check(C.cpu().numpy(), C64, bound, exact=(dist == "int"), what=f"res extreme {dist}")

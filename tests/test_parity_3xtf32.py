@@ -358,3 +358,16 @@ def test_unaligned_output_guard_bands(variant, split_k, c_offset):
     s = store.cpu().numpy()
     assert np.all(s[:guard] == sentinel) and np.all(s[guard + M * ldc:] == sentinel)
     assert np.all(store[guard:guard + M * ldc].view(M, ldc)[:, N:].cpu().numpy() == sentinel)
+
+
+@pytest.mark.parametrize("shape,dist", [((1 << 20, 8, 64), "int"), ((128, 128, 1 << 20), "uniform"),
+                                        ((1 << 20, 9, 63), "int")])
+def test_extreme_shapes_every_element(shape, dist):
+    """A million rows (aligned, and with rows of 63 and 9 floats on the
+    residue-class maps) and a million-deep K on one tile (its K split into
+    four parts): every element against the oracle, integer inputs exactly."""
+    M, N, K = shape
+    A, B = make_operands(M, N, K, dist, 62)
+    C = run(A, B)
+    C64, bound = oracle.gemm_f64(A.numpy(), B.numpy(), with_bound=(dist != "int"))
+    check(C, C64, bound, exact=(dist == "int"), what=f"3xtf32 {shape} {dist}")
