@@ -458,6 +458,19 @@ def test_host_buffer_entry_4096_every_element():
     check(C.numpy(), C64, bound, exact=False, what="host 4096")
 
 
+@pytest.mark.parametrize("dist", ["int", "uniform"])
+def test_host_buffer_entry_tall_pipelined(dist):
+    """262144 x 256 x 512 (2^36 flop) through the host-buffer entry: K chunks
+    of 64, 192 and 256 columns (the 1/32 boundary rounds down to nothing and
+    drops out), the last in row blocks of 163840, 49152, 32768 and 16384
+    rows; every element, integer inputs exactly."""
+    M, N, K = 1 << 18, 256, 512
+    A, B = make_operands(M, N, K, dist, 63)
+    C = g.sgemm_f32_host(A.pin_memory(), B.pin_memory())
+    C64, bound = oracle.gemm_f64(A.numpy(), B.numpy(), with_bound=(dist != "int"))
+    check(C.numpy(), C64, bound, exact=(dist == "int"), what=f"host tall {dist}")
+
+
 def test_host_buffer_entry_pitched_and_pageable():
     """Padded host rows (odd pitches) and pageable (not pinned) memory on the
     row-block path; the padding of C is left untouched."""
