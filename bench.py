@@ -661,7 +661,7 @@ SWEEP_OPTIONS = [
     {"l2_hint": 1},
     {"l2_hint": 2},
     {"producer": 8},
-    {"repack": 2},
+    {"edge": 1},
 ]
 
 

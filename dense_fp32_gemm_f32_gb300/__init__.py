@@ -127,10 +127,10 @@ def sgemm_3xtf32(A: torch.Tensor, B: torch.Tensor, out: torch.Tensor | None = No
 
 def sgemm_f32_ex(A, B, out=None, *, stream=None, producer=0, split_k=0, multicast=0, math=0, stages=0,
                  debug_skip_stage=0, timeout_ns=0, tail_split=0, stream_k=0, tile_n=0, repack=0,
-                 a_layout=0, group_m=0, l2_hint=0, tile_k=0) -> torch.Tensor:
+                 a_layout=0, group_m=0, l2_hint=0, tile_k=0, edge=0) -> torch.Tensor:
     """sgemm_f32 with forced variant choices (see struct sgemm_options)."""
     opt = Options(producer, split_k, multicast, math, stages, debug_skip_stage, timeout_ns, tail_split, stream_k,
-                  tile_n, repack, a_layout, group_m, l2_hint, tile_k)
+                  tile_n, repack, a_layout, group_m, l2_hint, tile_k, edge)
     return _call("sgemm_f32_ex", A, B, out, stream, opt)
 
 

@@ -47,6 +47,7 @@ class Options(ctypes.Structure):
         ("group_m", _i),
         ("l2_hint", _i),
         ("tile_k", _i),
+        ("edge", _i),
     ]
 
 

@@ -5,14 +5,16 @@
 
 namespace gb300 {
 
-// Scratch of sgemm_f32_noalloc: room for the stream-K partial tiles and
-// ready flags of up to kNoAllocMaxCtas CTAs (10 MiB + 640 bytes), a
-// file-scope device array so that the entry point needs no allocation.  Every
-// GPU that loads the library holds it until the process exits; all calls on a
-// device share it.
+// Scratch of sgemm_f32_noalloc: room for the stream-K partial tiles, ready
+// flags and thin-edge partial sums of up to kNoAllocMaxCtas CTAs (10 MiB +
+// 640 bytes + 320 KiB), a file-scope device array so that the entry point
+// needs no allocation.  Every GPU that loads the library holds it until the
+// process exits; all calls on a device share it.
 constexpr int kNoAllocMaxCtas = 160;
 constexpr size_t kNoAllocTileFloats = static_cast<size_t>(kBM) * kBN;  // 128 x 128 tiles only
-constexpr size_t kNoAllocFloats = kNoAllocMaxCtas * kNoAllocTileFloats + kNoAllocMaxCtas;
+constexpr size_t kNoAllocEdgeFloats = static_cast<size_t>(kConsumerThreads) * 2;  // FfmaParams ws_edge
+constexpr size_t kNoAllocFloats =
+    kNoAllocMaxCtas * kNoAllocTileFloats + kNoAllocMaxCtas + kNoAllocMaxCtas * kNoAllocEdgeFloats;
 static __device__ __align__(256) float g_noalloc_scratch[kNoAllocFloats];
 
 namespace detail {
@@ -199,34 +201,38 @@ int run_ffma(int M, int N, int K, const float* A, int lda, const float* B, int l
     prm.sk = pl.sk;
     prm.sk_dp_tiles = pl.sk_dp_tiles;
     prm.sk_units = (static_cast<long long>(pl.tiles_n) * ceil_div(M, kBM) - pl.sk_dp_tiles) * pl.num_k_tiles;
+    prm.ec = pl.ec;
     prm.ws = nullptr;
+    prm.ws_edge = nullptr;
     prm.flags = nullptr;
     prm.sk_seq = kSkSeqCaptured;
 
-    // Stream-K workspace: one partial tile and one flag per CTA, from the
-    // stream's own scratch (sk_lease) or, while the stream is being captured
-    // into a graph, from the library's stream-ordered pool for this call with
-    // its flags zeroed by a memset (stream order makes concurrent calls on
-    // different streams use different workspaces).
+    // Stream-K workspace: one partial tile and one flag per CTA (and, with a
+    // thin column edge, 256 partial column pairs), from the stream's own
+    // scratch (sk_lease) or, while the stream is being captured into a graph,
+    // from the library's stream-ordered pool for this call with its flags
+    // zeroed by a memset (stream order makes concurrent calls on different
+    // streams use different workspaces).
     void* ws = nullptr;
     SkLease lease;
     if (pl.sk) {
         const size_t G = static_cast<size_t>(pl.launch[0].tiles);
         const size_t tile_bytes = static_cast<size_t>(kBM) * pl.bn * sizeof(float);
-        if (sk_lease(*st, cs, G * tile_bytes, G, &lease) == SGEMM_OK) {
+        const size_t edge_bytes = pl.ec ? G * kConsumerThreads * sizeof(float2) : 0;
+        if (sk_lease(*st, cs, G * tile_bytes + edge_bytes, G, &lease) == SGEMM_OK) {
             prm.ws = lease.ws;
             prm.flags = lease.flags;
             prm.sk_seq = lease.seq;
         } else {
             cudaMemPool_t pool = workspace_pool(dev, *st);
-            if (!pool ||
-                cudaMallocFromPoolAsync(&ws, G * tile_bytes + G * sizeof(unsigned int), pool, cs) != cudaSuccess) {
+            if (!pool || cudaMallocFromPoolAsync(&ws, G * tile_bytes + edge_bytes + G * sizeof(unsigned int), pool,
+                                                 cs) != cudaSuccess) {
                 (void)cudaGetLastError();
                 release_pack();
                 return SGEMM_ERR_CUDA;
             }
             prm.ws = static_cast<float*>(ws);
-            prm.flags = reinterpret_cast<unsigned int*>(static_cast<char*>(ws) + G * tile_bytes);
+            prm.flags = reinterpret_cast<unsigned int*>(static_cast<char*>(ws) + G * tile_bytes + edge_bytes);
             if (cudaMemsetAsync(prm.flags, 0, G * sizeof(unsigned int), cs) != cudaSuccess) {
                 (void)cudaGetLastError();
                 (void)cudaFreeAsync(ws, cs);
@@ -234,6 +240,7 @@ int run_ffma(int M, int N, int K, const float* A, int lda, const float* B, int l
                 return SGEMM_ERR_CUDA;
             }
         }
+        if (pl.ec) prm.ws_edge = reinterpret_cast<float2*>(reinterpret_cast<char*>(prm.ws) + G * tile_bytes);
     }
 
     for (int l = 0; l < pl.nlaunch; ++l) {
@@ -386,6 +393,10 @@ int run_ffma_noalloc(int M, int N, int K, const float* A, int lda, const float* 
         // them ahead of each replay and the reserved number is used.
         prm.ws = st->noalloc_scratch;
         prm.flags = reinterpret_cast<unsigned int*>(st->noalloc_scratch + kNoAllocMaxCtas * kNoAllocTileFloats);
+        prm.ec = pl.ec;
+        prm.ws_edge = pl.ec ? reinterpret_cast<float2*>(st->noalloc_scratch + kNoAllocMaxCtas * kNoAllocTileFloats +
+                                                          kNoAllocMaxCtas)
+                            : nullptr;
         cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
         if (cudaStreamIsCapturing(cs, &cap) != cudaSuccess) {
             (void)cudaGetLastError();

@@ -231,6 +231,8 @@ struct Plan {
     bool b_nk = false;    // B stored transposed (N x K): the kernels with a B-transposing warp
     int bk = kBK;         // K slice depth (32, or 16 for sgemm_options.tile_k = 16)
     bool res = false;     // A and B read through residue-class tensor maps (any alignment; res_maps.cuh)
+    int ec = 0;           // thin column edge: the last N - 128 tiles_n columns, computed with the
+                          // last column of tiles (FfmaParams ec; stream-K only)
 };
 
 // Epilogue scaling of the general entry: C = alpha * A B + beta * C.

@@ -57,7 +57,8 @@ int validate(int M, int N, int K, const float* A, int lda, const float* B, int l
 
 bool options_force_variant(const sgemm_options* opt) {
     return opt && (opt->producer || opt->split_k || opt->multicast || opt->math || opt->stages || opt->tail_split ||
-                   opt->stream_k || opt->tile_n || opt->repack || opt->group_m || opt->l2_hint || opt->tile_k);
+                   opt->stream_k || opt->tile_n || opt->repack || opt->group_m || opt->l2_hint || opt->tile_k ||
+                   opt->edge);
 }
 
 // 0 = keep A as stored, 1 = copy it transposed; -1 = invalid option.
@@ -263,9 +264,6 @@ int make_plan(const DeviceState& st, int M, int N, int K, const float* A, int ld
     if (per_sm < 1) return SGEMM_ERR_UNSUPPORTED;
     const long long slots = static_cast<long long>(st.sm_count) * per_sm;
 
-    tiles_n = ceil_div(N, pl.bn);
-    const long long tiles = tiles_n * tiles_m;
-
     // Stream-K (decided first; see below for the schedule).  Automatic
     // whenever nothing else is forced and there are at least two (tile, K
     // slice) units per SM: measured on GB300 it beats the plain grid and
@@ -274,8 +272,28 @@ int make_plan(const DeviceState& st, int M, int N, int K, const float* A, int ld
     const int want_sk = opt ? opt->stream_k : 0;
     if (want_sk < 0 || want_sk > 2) return SGEMM_ERR_INVALID_ARG;
     const bool forced_other = opt && (opt->split_k || opt->tail_split > 1);
-    const bool use_sk = want_sk == 2 || (want_sk == 0 && !forced_other && pl.num_k_tiles > 0 &&
-                                         tiles * pl.num_k_tiles >= 2LL * slots);
+    auto stream_k_for = [&](long long tiles) {
+        return want_sk == 2 ||
+               (want_sk == 0 && !forced_other && pl.num_k_tiles > 0 && tiles * pl.num_k_tiles >= 2LL * slots);
+    };
+
+    // Thin column edge (sgemm_options.edge): when N mod 128 is 1 to
+    // kEdgeMaxCols, the stream-K launches of the transposing producer with
+    // the plain epilogue compute those columns with the last column of full
+    // tiles (FfmaParams ec) instead of giving them a column of tiles of their
+    // own, whose units would cost as much as full ones: 1023 x 1025 x 1027
+    // has 64 tiles of 33 K slices instead of 72 (14 units on the busiest SM
+    // instead of 16).
+    const int want_edge = opt ? opt->edge : 0;
+    if (want_edge < 0 || want_edge > 1) return SGEMM_ERR_INVALID_ARG;
+    const int ec = static_cast<int>(N % kBN);
+    const bool edge_ok = want_edge == 0 && pl.producer == kProducerTmaX && pl.bn == kBN && pl.bk == kBK &&
+                         !scaled && !a_mn && !b_nk && ec >= 1 && ec <= kEdgeMaxCols && N > kBN &&
+                         stream_k_for((N / kBN) * tiles_m);
+    tiles_n = edge_ok ? N / kBN : ceil_div(N, pl.bn);
+    const long long tiles = tiles_n * tiles_m;
+    const bool use_sk = stream_k_for(tiles);
+    pl.ec = edge_ok ? ec : 0;
 
     // Split-K over the whole grid, only when the tiles do not fill one wave:
     // pick s in 1..8 minimising (waves of clusters) x (K tiles per CTA).  (With
@@ -437,7 +455,9 @@ const char* describe_plan(const Plan& pl) {
     if (pl.bk != kBK && n > 0 && n < static_cast<int>(sizeof buf))
         n += std::snprintf(buf + n, sizeof buf - n, "/k%d", pl.bk);
     if (pl.res && n > 0 && n < static_cast<int>(sizeof buf))
-        std::snprintf(buf + n, sizeof buf - n, "/res");
+        n += std::snprintf(buf + n, sizeof buf - n, "/res");
+    if (pl.ec && n > 0 && n < static_cast<int>(sizeof buf))
+        std::snprintf(buf + n, sizeof buf - n, "/ec%d", pl.ec);
     return buf;
 }
 

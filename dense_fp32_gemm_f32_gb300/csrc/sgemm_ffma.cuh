@@ -186,6 +186,20 @@ __host__ __device__ constexpr int ffma_load_b_bytes() {
     return RES ? 4 * kResBPlaneBytes : BK * BN * 4;
 }
 
+// Thin column edge: when N mod 128 is 1 .. kEdgeMaxCols, those last columns
+// are not given a column of tiles of their own (nearly empty tiles that
+// would cost as much as full ones); the CTAs working on the last column of
+// full tiles compute them too, from the A slices they already hold and the
+// edge columns' B values, which an A-transposing warp copies into
+// shared memory per slice (kEdgeStageBytes: 32 k x 4 floats).  The
+// transposing producer on 32-deep slices, plain epilogue, stream-K only.
+constexpr int kEdgeMaxCols = 4;
+constexpr int kEdgeStageBytes = kBK * kEdgeMaxCols * 4;
+template <int STAGES, bool XA, bool XB, int BK>
+__host__ __device__ constexpr int ffma_edge_bytes() {
+    return (XA && !XB && BK == kBK) ? STAGES * kEdgeStageBytes : 0;
+}
+
 enum : int { kMathFfma = 1, kMathFfma2 = 2 };
 enum : unsigned { kStatusTimeout = 4u };
 
@@ -229,6 +243,12 @@ struct FfmaParams {
     // RES kernels: bits 2j, 2j + 1 hold t_j, the offset in floats of the rows
     // of residue class j inside their 16-byte blocks (res_maps.cuh).
     int a_shift, b_shift;
+    // Thin column edge (stream-K launches of the transposing producer with
+    // the plain epilogue): ec = N - 128 tiles_n columns, 1 .. kEdgeMaxCols,
+    // computed with the last column of tiles (0 = none).  ws_edge: gridDim.x
+    // x 256 partial sums (one column pair of one row per consumer thread).
+    int ec;
+    float2* ws_edge;
 };
 
 // Largest dynamic shared memory of a CTA on sm_100-family GPUs.
@@ -255,7 +275,8 @@ template <int STAGES, int PRODUCER, int BN, bool SCALED, bool BNK, int BK = kBK,
 __host__ __device__ constexpr bool ffma_tma_store() {
     return (PRODUCER == kProducerTmaX || PRODUCER == kProducerLdg) && BN == kBN && !SCALED &&
            ffma_ring_bytes<STAGES, BN, PRODUCER == kProducerTmaX, BNK, BK, RES>() +
-                   ffma_partial_bytes<BN>() + 1024 + 256 <=
+                   ffma_partial_bytes<BN>() + 1024 + 256 +
+                   ffma_edge_bytes<STAGES, PRODUCER == kProducerTmaX, BNK, BK>() <=
                kMaxSmemBytes;
 }
 
@@ -263,7 +284,7 @@ template <int STAGES, int BN = kBN, bool XA = false, bool XB = false, bool STG =
           bool RES = false>
 constexpr int ffma_smem_bytes() {
     return ffma_ring_bytes<STAGES, BN, XA, XB, BK, RES>() + (STG ? ffma_partial_bytes<BN>() : 0) +
-           1024 /*align*/ + 256 /*barriers*/;
+           1024 /*align*/ + 256 /*barriers*/ + ffma_edge_bytes<STAGES, XA, XB, BK>();
 }
 
 // Output tile number -> (row of tiles tm, column of tiles tn).  Tiles are
@@ -382,6 +403,10 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER, BNK || RES>(), ffma_min
     const uint32_t sA0 = base;                                         // STAGES x kALoadBytes
     const uint32_t sB0 = base + kBLoadOff;                             // STAGES x kBLoadBytes
     const uint32_t bar0 = base + kRingBytes + (kStg ? kPartialBytes : 0);  // full[STAGES], empty[STAGES], tfull[STAGES]
+    // Thin column edge (FfmaParams ec): B's edge values of each stage, rows of
+    // kEdgeMaxCols floats (zeros past N), after the barriers.
+    constexpr bool kEdge = kX && !BNK && BK == kBK && !SCALED;
+    constexpr int kEcOff = kRingBytes + (kStg ? kPartialBytes : 0) + 256;
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
     auto tfull_bar = [&](int s) { return bar0 + 8u * (2 * STAGES + s); };  // transposed A ready
@@ -610,13 +635,35 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER, BNK || RES>(), ffma_min
             const int q0 = xb ? 0 : (pw - 1) * qn;
             const int src_off = xb ? kBLoadOff : 0;
             const int dst_off = xb ? kBOff : kTOff;
+            // The first A-transposing warp also copies B's thin column edge
+            // (FfmaParams ec) for the slices of the last column of tiles: lane
+            // l reads row k0 + l's edge values before the slice's wait (their
+            // latency overlaps it) and stores them with the transposed slice.
+            const bool edge_loader = kEdge && p.ec > 0 && p.sk && pw == 1;
             int xit = 0;
             Work xwork = work0;
             int xtile, xkb, xke;
             while (!timed_out && xwork.next(xtile, xkb, xke)) {
+                bool edge_tile = false;
+                if (edge_loader) {
+                    int tm_, tn_;
+                    tile_rc(xtile, p.tiles_n, p.tiles_m, p.group_m, tm_, tn_);
+                    edge_tile = tn_ == p.tiles_n - 1;
+                }
                 for (int kt = xkb; kt < xke; ++kt, ++xit) {
                     const int s = xit % STAGES;
                     const int round = xit / STAGES;
+                    float4 eb = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (edge_tile) {
+                        const int k = kt * kBK + lane;
+                        if (k < p.K) {
+                            const float* const brow = p.B + static_cast<long long>(k) * p.ldb + p.tiles_n * kBN;
+                            eb.x = __ldg(brow);
+                            if (p.ec > 1) eb.y = __ldg(brow + 1);
+                            if (p.ec > 2) eb.z = __ldg(brow + 2);
+                            if (p.ec > 3) eb.w = __ldg(brow + 3);
+                        }
+                    }
                     if (!mbar_wait_bounded_warp(full_bar(s), round & 1, tmo)) {
                         timed_out = true;
                         break;
@@ -683,6 +730,7 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER, BNK || RES>(), ffma_min
                                 *reinterpret_cast<float4*>(tr + (4 * c + 3) * kBM) = make_float4(r[0].w, r[1].w, r[2].w, r[3].w);
                             }
                         }
+                        if (edge_tile) *reinterpret_cast<float4*>(smem + kEcOff + s * kEdgeStageBytes + 16 * lane) = eb;
                         __syncwarp();
                         mbar_arrive(tfull_bar(s));
                         if (lane == 0) mbar_arrive(empty_bar(s));
@@ -706,6 +754,7 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER, BNK || RES>(), ffma_min
                             tr[(4 * c + 3) * kBM + m] = v.w;
                         }
                     }
+                    if (edge_tile) *reinterpret_cast<float4*>(smem + kEcOff + s * kEdgeStageBytes + 16 * lane) = eb;
                     __syncwarp();
                     mbar_arrive(tfull_bar(s));           // transposed slice written (every lane)
                     if (lane == 0) mbar_arrive(empty_bar(s));  // slice as loaded read
@@ -849,6 +898,13 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER, BNK || RES>(), ffma_min
 #pragma unroll
         for (int q = 0; q < TQ; ++q) acc[i][q] = make_float2(0.f, 0.f);  // (K == 0: the empty sum)
     const int wm = kFused ? warp : warp >> 1, wn = kFused ? 0 : warp & 1;
+    // Thin column edge (kEdge, FfmaParams ec): in a segment of the last column
+    // of tiles, consumer thread (warp, lane) also sums row e_row of the tile
+    // times edge columns 2 e_pair and 2 e_pair + 1 (warps 4-7 only when there
+    // are more than two), one warp of each SM sub-partition for each pair.
+    float2 eacc = make_float2(0.f, 0.f);
+    const int e_row = (warp & 3) * 32 + lane;
+    const int e_pair = warp >> 2;
     const int tm = (lane & 1) | (((lane >> 2) & 1) << 1);
     const int tn = ((lane >> 1) & 1) | (((lane >> 3) & 1) << 1) | (((lane >> 4) & 1) << 2);
 
@@ -1063,6 +1119,17 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER, BNK || RES>(), ffma_min
             store_c_plain(tile);
         }
     };
+    // The thread's finished edge sums (kEdge): row e_row of the tile, columns
+    // 128 tiles_n + 2 e_pair (+ 1 when that is inside C).
+    auto store_edge = [&](int tile) {
+        int tm_, tn_;
+        tile_rc(tile, p.tiles_n, p.tiles_m, p.group_m, tm_, tn_);
+        const int r = tm_ * kBM + e_row;
+        if (r >= p.M) return;
+        float* const ce = p.C + static_cast<long long>(r) * p.ldc + p.tiles_n * kBN + 2 * e_pair;
+        ce[0] = eacc.x;
+        if (2 * e_pair + 1 < p.ec) ce[1] = eacc.y;
+    };
     // The TMA has finished the last store of this CTA (reading the staging
     // tile and writing C) before the CTA's shared memory is released.
     auto drain_stores = [&] {
@@ -1123,6 +1190,13 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER, BNK || RES>(), ffma_min
             for (int i = 0; i < 8; ++i)
 #pragma unroll
                 for (int q = 0; q < TQ; ++q) acc[i][q] = make_float2(0.f, 0.f);
+            bool e_work = false;  // (warp-uniform)
+            if (kEdge && p.ec > 0 && p.sk) {
+                int tm_, tn_;
+                tile_rc(tile, p.tiles_n, p.tiles_m, p.group_m, tm_, tn_);
+                e_work = tn_ == p.tiles_n - 1 && 2 * e_pair < p.ec;
+            }
+            eacc = make_float2(0.f, 0.f);
             if (SCALED && read_c && kb == 0 && (split <= 1 || crank == 0))
                 prefetch_c(tile);  // this CTA stores the tile
 
@@ -1185,6 +1259,25 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER, BNK || RES>(), ffma_min
                             }
                     }
                 }
+                if (kEdge && e_work) {
+                    // The edge columns' sums over this slice: A's row e_row at
+                    // each k (the transposed slice: 32 lanes, 128 consecutive
+                    // bytes) times the pair's B values (one broadcast); two
+                    // chains of 16 k.
+                    const float* const ta = reinterpret_cast<const float*>(smem + kTOff + s * kStageABytes) + e_row;
+                    const float2* const eb =
+                        reinterpret_cast<const float2*>(smem + kEcOff + s * kEdgeStageBytes) + e_pair;
+                    float2 e0 = make_float2(0.f, 0.f), e1 = make_float2(0.f, 0.f);
+#pragma unroll
+                    for (int k = 0; k < kBK; k += 2) {
+                        const float a0 = ta[k * kBM], a1 = ta[(k + 1) * kBM];
+                        const float2 b0 = eb[2 * k], b1 = eb[2 * (k + 1)];
+                        e0 = __ffma2_rn(make_float2(a0, a0), b0, e0);
+                        e1 = __ffma2_rn(make_float2(a1, a1), b1, e1);
+                    }
+                    eacc.x += e0.x + e1.x;
+                    eacc.y += e0.y + e1.y;
+                }
                 // Every load from stage s has returned (its values were
                 // consumed above): release the slot to the producer(s).
                 __syncwarp();
@@ -1204,6 +1297,7 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER, BNK || RES>(), ffma_min
                         __stcg(reinterpret_cast<float4*>(ws_mine) + (i * H + h) * CT + threadIdx.x,
                                make_float4(acc[i][2 * h].x, acc[i][2 * h].y, acc[i][2 * h + 1].x,
                                            acc[i][2 * h + 1].y));
+                if (e_work) __stcg(p.ws_edge + static_cast<size_t>(blockIdx.x) * CT + threadIdx.x, eacc);
                 consumer_sync();
                 if (threadIdx.x == 0) {
                     __threadfence();
@@ -1246,9 +1340,15 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER, BNK || RES>(), ffma_min
                                 acc[i][2 * h + 1].x += v.z;
                                 acc[i][2 * h + 1].y += v.w;
                             }
+                        if (e_work) {
+                            const float2 v = __ldcg(p.ws_edge + static_cast<size_t>(g2) * CT + threadIdx.x);
+                            eacc.x += v.x;
+                            eacc.y += v.y;
+                        }
                     }
                 }
                 store_c(tile);
+                if (e_work) store_edge(tile);
             }
         }
         if (kFused && threadIdx.x == 0) {

@@ -382,6 +382,15 @@ typedef struct sgemm_options {
                              producer, SGEMM_PRODUCER_TMA_X, only; A slices
                              of 64-byte rows with the 64-byte swizzle; 2, 3,
                              4 (default) or 6 stages) */
+    int edge;             /* 0 = auto, 1 = off.  Thin column edge: when N mod
+                             128 is 1 to 4 and the product runs stream-K on
+                             the transposing producer (SGEMM_PRODUCER_TMA_X
+                             or SGEMM_PRODUCER_TMA_RES, 32-deep slices, the
+                             plain epilogue), those last columns are computed
+                             by the CTAs working on the last column of full
+                             128 x 128 tiles instead of as a column of tiles
+                             of their own (the stream-K workspace then also
+                             holds 2 KiB of partial sums per CTA) */
 } sgemm_options;
 
 /* sgemm_f32 with forced choices.  Same contract; an unsupported combination

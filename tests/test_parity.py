@@ -374,7 +374,7 @@ def test_unaligned_bases(offsets, shape):
     A, B = make_operands(M, N, K, "uniform", 9)
     dA, dB = to_device(A, offset=oa), to_device(B, offset=ob)
     d = g.describe(dA, dB)
-    assert d.startswith("small") if M < 256 else d.endswith("/res")
+    assert d.startswith("small") if M < 256 else d.endswith("/res/ec4")
     C = g.sgemm_f32(dA, dB)
     torch.cuda.synchronize()
     C64, bound = oracle.gemm_f64(A.numpy(), B.numpy())
@@ -504,10 +504,13 @@ def test_variant_choice():
     # 1027-float rows are not 16-byte multiples: below 2MNK = 2^35 the
     # residue-class tensor maps read the rows in place; larger products
     # repack them into pitched rows first
-    assert desc(1023, 1025, 1027).startswith("tmax/") and desc(1023, 1025, 1027).endswith("/res")
-    assert desc(700, 900, 701).startswith("tmax/") and desc(700, 900, 701).endswith("/res")
-    assert desc(2048, 2049, 2048).endswith("/res")
-    assert desc(4096, 4097, 4096).endswith("/repackB") and desc(8192, 8193, 8192).endswith("/repackB")
+    # (and N mod 128 = 1 .. 4 columns past the last full column of tiles are
+    # computed with that column: "/ec<columns>")
+    assert desc(1023, 1025, 1027).startswith("tmax/") and desc(1023, 1025, 1027).endswith("/res/ec1")
+    assert desc(700, 900, 701).startswith("tmax/") and desc(700, 900, 701).endswith("/res/ec4")
+    assert desc(2048, 2049, 2048).endswith("/res/ec1") and desc(700, 901, 701).endswith("/res")
+    assert desc(4096, 4097, 4096).endswith("/repackB/ec1") and desc(8192, 8193, 8192).endswith("/repackB/ec1")
+    assert "/ec" not in desc(4096, 4096, 4096) and "/ec" not in desc(127, 129, 4096)
 
 
 # ---------------------------------------------------------------- A's layout
@@ -903,7 +906,7 @@ def test_cuda_graph_capture_on_residue_class_maps():
     A, B = make_operands(M, N, K, "uniform", 57)
     dA, dB = to_device(A, offset=1), to_device(B, offset=2)
     dC = torch.empty((M, N), device="cuda")
-    assert g.describe(dA, dB, dC).endswith("/res")
+    assert g.describe(dA, dB, dC).endswith("/res/ec1")  # (the edge's partial sums in the capture's workspace)
     g.sgemm_f32(dA, dB, dC)  # outside the capture first
     torch.cuda.synchronize()
     graph = torch.cuda.CUDAGraph()
@@ -923,6 +926,103 @@ def test_cuda_graph_capture_on_residue_class_maps():
         torch.cuda.synchronize()
         C64, bound = oracle.gemm_f64(A2.numpy(), B2.numpy())
         check(dC.cpu().numpy(), C64, bound, exact=False, what=f"graph replay on class maps {seed}")
+
+
+# ---------------------------------------------------------------- thin column edge
+
+@pytest.mark.parametrize("dist", ["uniform", "int"])
+@pytest.mark.parametrize("b_rows", ["exact", "padded"])
+@pytest.mark.parametrize("shape", [(1023, 1025, 1027), (2000, 130, 700), (3201, 515, 96), (1000, 644, 333),
+                                   (128, 2050, 4096), (300, 516, 4096)])
+def test_thin_column_edge(shape, b_rows, dist):
+    """N mod 128 = 1 .. 4 columns past the last full column of tiles,
+    computed by the CTAs working on that column (B's edge values copied per
+    slice by a transposing warp, the sums exchanged with the stream-K partial
+    tiles): B's rows of N floats or padded to a 16-byte multiple (the
+    residue-class maps wherever a row of A or B is not a 16-byte multiple,
+    else the plain tensor maps); one column of tiles (N = 130), a last row of
+    tiles holding one row and K of 3 slices (3201 x 515 x 96), one row of
+    tiles with K = 4096, and N = 516 with the tensor-map stores of C; every
+    element, integer inputs exactly."""
+    M, N, K = shape
+    A, B = make_operands(M, N, K, dist, 64)
+    ldb = N if b_rows == "exact" else (N + 3) // 4 * 4
+    dA, dB = to_device(A), to_device(B, ldb)
+    dC = to_device(torch.full((M, N), float("nan")))
+    d = g.describe(dA, dB, dC)
+    assert d.endswith(f"/ec{N % 128}") and ("/res" in d) == (ldb % 4 != 0 or K % 4 != 0), d
+    g.sgemm_f32(dA, dB, dC)
+    torch.cuda.synchronize()
+    C64, bound = oracle.gemm_f64(A.numpy(), B.numpy(), with_bound=(dist != "int"))
+    check(dC.cpu().numpy(), C64, bound, exact=(dist == "int"), what=f"edge {shape} ldb {ldb} {dist}")
+
+
+@pytest.mark.parametrize("dist", ["uniform", "int"])
+def test_thin_column_edge_with_whole_tiles(dist):
+    """4096 x 1281 x 256: 32 x 10 tiles, two waves, so that the first 152
+    tiles run whole (their edge sums stored directly) and the rest are dealt
+    out as K-slice units (edge sums exchanged); every element."""
+    M, N, K = 4096, 1281, 256
+    A, B = make_operands(M, N, K, dist, 65)
+    C = run(A, B)
+    C64, bound = oracle.gemm_f64(A.numpy(), B.numpy(), with_bound=(dist != "int"))
+    check(C, C64, bound, exact=(dist == "int"), what=f"edge with whole tiles {dist}")
+
+
+@pytest.mark.parametrize("c_offset", [0, 1])
+def test_thin_column_edge_guard_bands(c_offset):
+    """The edge columns' stores stop at N: C's rows padded to 1040 floats
+    (and, with c_offset = 1, a misaligned base: the staged row stores) hold a
+    sentinel past N = 1027 and around C that must survive."""
+    M, N, K = 700, 1027, 900
+    A, B = make_operands(M, N, K, "uniform", 66)
+    ldc, guard, sentinel = 1040, 64 + c_offset, -12345.0
+    store = torch.full((guard + M * ldc + 64,), sentinel, device="cuda")
+    dC = store[guard:guard + M * ldc].view(M, ldc)[:, :N]
+    dA, dB = to_device(A), to_device(B)
+    assert g.describe(dA, dB, dC).endswith("/ec3")
+    g.sgemm_f32(dA, dB, dC)
+    torch.cuda.synchronize()
+    C64, bound = oracle.gemm_f64(A.numpy(), B.numpy())
+    check(dC.cpu().numpy(), C64, bound, exact=False, what=f"edge guard bands {c_offset}")
+    s = store.cpu().numpy()
+    assert np.all(s[:guard] == sentinel) and np.all(s[guard + M * ldc:] == sentinel)
+    assert np.all(store[guard:guard + M * ldc].view(M, ldc)[:, N:].cpu().numpy() == sentinel)
+
+
+@pytest.mark.parametrize("opt", [dict(edge=1), dict(edge=1, producer=8), dict(stages=3), dict(stages=4),
+                                 dict(producer=8, stages=3), dict(math=1, repack=2), dict(group_m=1),
+                                 dict(stream_k=1, split_k=1), dict(split_k=2), dict(tile_n=64, repack=2),
+                                 dict(producer=2)])
+def test_thin_column_edge_forced_choices(opt):
+    """The edge fold under the other stage counts, scalar FFMA, repacked
+    operands and row-by-row tile order; switched off (edge = 1: a ninth
+    column of tiles) and not taken without stream-K or the transposing
+    producer (plain grid, cluster split-K, 128 x 64 tiles, cp.async)."""
+    M, N, K = 1023, 1025, 1027
+    A, B = make_operands(M, N, K, "int", 67)
+    C = run(A, B, **opt)
+    C64, _ = oracle.gemm_f64(A.numpy(), B.numpy(), with_bound=False)
+    check(C, C64, None, exact=True, what=f"edge forced {opt}")
+
+
+def test_thin_column_edge_option_is_checked():
+    A, B = make_operands(300, 257, 300, "uniform", 68)
+    with pytest.raises(g._lib.SgemmError):
+        g.sgemm_f32_ex(to_device(A), to_device(B), edge=2)
+    with pytest.raises(g._lib.SgemmError):
+        g.sgemm_f32_ex(to_device(A), to_device(B), edge=-1)
+
+
+@pytest.mark.parametrize("dist", ["uniform", "int"])
+def test_host_buffer_entry_thin_column_edge(dist):
+    """4096 x 1025 x 2048 through the host-buffer entry (K chunks, the
+    first a plain product of 256 x 2 units that computes the edge column with
+    the last column of tiles, the later ones accumulating); every element."""
+    A, B = make_operands(4096, 1025, 2048, dist, 69)
+    C = g.sgemm_f32_host(A.pin_memory(), B.pin_memory())
+    C64, bound = oracle.gemm_f64(A.numpy(), B.numpy(), with_bound=(dist != "int"))
+    check(C.numpy(), C64, bound, exact=(dist == "int"), what=f"host edge {dist}")
 
 
 # ---------------------------------------------------------------- extreme shapes
