@@ -118,11 +118,13 @@ int init_device(int dev, DeviceState& st) {
             if (set_smem_attr(ffma_kernel_tma_x16(s, math)) != SGEMM_OK) return SGEMM_ERR_CUDA;
             if (set_smem_attr(ffma_kernel_ldg(s, math)) != SGEMM_OK) return SGEMM_ERR_CUDA;
             for (bool scaled : {false, true})
-                if (set_smem_attr(ffma_kernel_res(s, math, scaled)) != SGEMM_OK) return SGEMM_ERR_CUDA;
+                for (bool edge : {false, true})
+                    if (set_smem_attr(ffma_kernel_res(s, math, scaled, edge)) != SGEMM_OK ||
+                        set_smem_attr(ffma_kernel_tma_x(s, math, scaled, edge)) != SGEMM_OK)
+                        return SGEMM_ERR_CUDA;
             for (bool scaled : {false, true}) {
                 if (set_smem_attr(ffma_kernel_bnk(s == 1, scaled)) != SGEMM_OK) return SGEMM_ERR_CUDA;
                 if (set_smem_attr(ffma_kernel_amn(s, math, scaled)) != SGEMM_OK) return SGEMM_ERR_CUDA;
-                if (set_smem_attr(ffma_kernel_tma_x(s, math, scaled)) != SGEMM_OK) return SGEMM_ERR_CUDA;
             }
         }
     }

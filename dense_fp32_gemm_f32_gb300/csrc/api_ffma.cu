@@ -114,7 +114,7 @@ int run_ffma(int M, int N, int K, const float* A, int lda, const float* B, int l
         a_t.release();
     };
 
-    const KernelEntry k = pl.res ? ffma_kernel_res(pl.stages, pl.math, scaled)
+    const KernelEntry k = pl.res ? ffma_kernel_res(pl.stages, pl.math, scaled, pl.ec > 0)
                           : pl.b_nk ? ffma_kernel_bnk(pl.a_mn, scaled)
                           : pl.a_mn ? (pl.bn == kBN ? ffma_kernel_amn(pl.stages, pl.math, scaled)
                                                   : scaled ? KernelEntry{nullptr, 0, 0} : ffma_kernel(pl))

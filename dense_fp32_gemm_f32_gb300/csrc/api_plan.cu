@@ -81,9 +81,12 @@ KernelEntry ffma_kernel(const Plan& pl) {
                                                         : KernelEntry{nullptr, 0, 0};
     if (pl.producer == kProducerFused) return ffma_kernel_tma_fused(pl.stages, pl.math);
     if (pl.producer == kProducerLdg) return ffma_kernel_ldg(pl.stages, pl.math);
-    if (pl.res) return pl.producer == kProducerTmaX ? ffma_kernel_res(pl.stages, pl.math) : KernelEntry{nullptr, 0, 0};
+    if (pl.res)
+        return pl.producer == kProducerTmaX ? ffma_kernel_res(pl.stages, pl.math, false, pl.ec > 0)
+                                            : KernelEntry{nullptr, 0, 0};
     if (pl.producer == kProducerTmaX)
-        return pl.bk == kBK16 ? ffma_kernel_tma_x16(pl.stages, pl.math) : ffma_kernel_tma_x(pl.stages, pl.math, false);
+        return pl.bk == kBK16 ? ffma_kernel_tma_x16(pl.stages, pl.math)
+                              : ffma_kernel_tma_x(pl.stages, pl.math, false, pl.ec > 0);
     if (pl.bn == kBNWide) return pl.producer == kProducerTmaWg ? ffma_kernel_tma_wide(pl.stages, pl.math)
                                                                 : KernelEntry{nullptr, 0, 0};
     switch (pl.producer) {
@@ -288,7 +291,8 @@ int make_plan(const DeviceState& st, int M, int N, int K, const float* A, int ld
     if (want_edge < 0 || want_edge > 1) return SGEMM_ERR_INVALID_ARG;
     const int ec = static_cast<int>(N % kBN);
     const bool edge_ok = want_edge == 0 && pl.producer == kProducerTmaX && pl.bn == kBN && pl.bk == kBK &&
-                         !scaled && !a_mn && !b_nk && ec >= 1 && ec <= kEdgeMaxCols && N > kBN &&
+                         pl.math == kMathFfma2 && !scaled && !a_mn && !b_nk && ec >= 1 && ec <= kEdgeMaxCols &&
+                         N > kBN &&
                          stream_k_for((N / kBN) * tiles_m);
     tiles_n = edge_ok ? N / kBN : ceil_div(N, pl.bn);
     const long long tiles = tiles_n * tiles_m;

@@ -24,8 +24,10 @@ KernelEntry ffma_kernel_tma_wide(int stages, int math);
 // The same on A stored transposed (K x M): 2 stages, paired FMA.
 KernelEntry ffma_kernel_tma_wide_amn(int stages, int math);
 // FFMA kernels with A transposed in shared memory by a second producer warp
-// (128 x 128 tiles, stages in {2,3,4}; scaled epilogue: 2 stages, paired FMA).
-KernelEntry ffma_kernel_tma_x(int stages, int math, bool scaled);
+// (128 x 128 tiles, stages in {2,3,4}; scaled epilogue: 2 stages, paired FMA);
+// `edge`: the instantiations that compute a thin column edge (FfmaParams ec;
+// paired FMA, plain epilogue).
+KernelEntry ffma_kernel_tma_x(int stages, int math, bool scaled, bool edge = false);
 // Fused-producer FFMA kernels: 4-warp CTAs (no producer warp; thread 0
 // issues the TMA copies), 128 x 64 tiles, two CTAs per SM; stages in {2,3,4}.
 KernelEntry ffma_kernel_tma_fused(int stages, int math);
@@ -46,8 +48,9 @@ KernelEntry ffma_kernel_bnk(bool a_mn, bool scaled);
 // FFMA kernels on residue-class tensor maps (operands of any alignment, read
 // in place: four maps per operand, one per class of rows mod 4, and a
 // B-shifting producer warp); 128 x 128 tiles, paired FMA; plain epilogue on
-// stages {2,3,4}, `scaled` (the general entry's epilogue) on 2.
-KernelEntry ffma_kernel_res(int stages, int math, bool scaled = false);
+// stages {2,3,4}, `scaled` (the general entry's epilogue) on 2; `edge` as for
+// ffma_kernel_tma_x.
+KernelEntry ffma_kernel_res(int stages, int math, bool scaled = false, bool edge = false);
 // FFMA kernels fed by loader warps (operands of any alignment, no tensor
 // maps): 128 x 128 tiles, paired FMA, plain epilogue; stages {2,3,4}.
 KernelEntry ffma_kernel_ldg(int stages, int math);

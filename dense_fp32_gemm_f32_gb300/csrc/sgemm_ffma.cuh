@@ -195,9 +195,9 @@ __host__ __device__ constexpr int ffma_load_b_bytes() {
 // transposing producer on 32-deep slices, plain epilogue, stream-K only.
 constexpr int kEdgeMaxCols = 4;
 constexpr int kEdgeStageBytes = kBK * kEdgeMaxCols * 4;
-template <int STAGES, bool XA, bool XB, int BK>
+template <int STAGES, bool EDGE>
 __host__ __device__ constexpr int ffma_edge_bytes() {
-    return (XA && !XB && BK == kBK) ? STAGES * kEdgeStageBytes : 0;
+    return EDGE ? STAGES * kEdgeStageBytes : 0;
 }
 
 enum : int { kMathFfma = 1, kMathFfma2 = 2 };
@@ -276,15 +276,15 @@ __host__ __device__ constexpr bool ffma_tma_store() {
     return (PRODUCER == kProducerTmaX || PRODUCER == kProducerLdg) && BN == kBN && !SCALED &&
            ffma_ring_bytes<STAGES, BN, PRODUCER == kProducerTmaX, BNK, BK, RES>() +
                    ffma_partial_bytes<BN>() + 1024 + 256 +
-                   ffma_edge_bytes<STAGES, PRODUCER == kProducerTmaX, BNK, BK>() <=
+                   ffma_edge_bytes<STAGES, PRODUCER == kProducerTmaX && !BNK && BK == kBK>() <=
                kMaxSmemBytes;
 }
 
 template <int STAGES, int BN = kBN, bool XA = false, bool XB = false, bool STG = false, int BK = kBK,
-          bool RES = false>
+          bool RES = false, bool EDGE = false>
 constexpr int ffma_smem_bytes() {
     return ffma_ring_bytes<STAGES, BN, XA, XB, BK, RES>() + (STG ? ffma_partial_bytes<BN>() : 0) +
-           1024 /*align*/ + 256 /*barriers*/ + ffma_edge_bytes<STAGES, XA, XB, BK>();
+           1024 /*align*/ + 256 /*barriers*/ + ffma_edge_bytes<STAGES, EDGE>();
 }
 
 // Output tile number -> (row of tiles tm, column of tiles tn).  Tiles are
@@ -340,8 +340,12 @@ __device__ __forceinline__ uint32_t swz128(int r, int c) {
 // (res_maps.cuh; tmA and tmB are then four maps each, and FfmaParams
 // a_shift, b_shift hold the classes' offsets); the transposing producer,
 // 128 x 128 tiles, A and B as stored, 32-deep slices.
+//
+// EDGE: the thin column edge (FfmaParams ec) is computed with the last
+// column of tiles; a separate instantiation, so that the kernels of every
+// other shape are compiled without its code.
 template <int STAGES, int PRODUCER, int MATH, int BN = kBN, bool SCALED = false, bool AMN = false, bool BNK = false,
-          int BK = kBK, bool RES = false>
+          int BK = kBK, bool RES = false, bool EDGE = false>
 __global__ void __launch_bounds__(ffma_threads<PRODUCER, BNK || RES>(), ffma_min_blocks<PRODUCER>())
     sgemm_ffma_kernel(const __grid_constant__ typename FfmaMap<RES>::type tmA,
                       const __grid_constant__ typename FfmaMap<RES>::type tmB,
@@ -405,7 +409,9 @@ __global__ void __launch_bounds__(ffma_threads<PRODUCER, BNK || RES>(), ffma_min
     const uint32_t bar0 = base + kRingBytes + (kStg ? kPartialBytes : 0);  // full[STAGES], empty[STAGES], tfull[STAGES]
     // Thin column edge (FfmaParams ec): B's edge values of each stage, rows of
     // kEdgeMaxCols floats (zeros past N), after the barriers.
-    constexpr bool kEdge = kX && !BNK && BK == kBK && !SCALED;
+    constexpr bool kEdge = EDGE;
+    static_assert(!EDGE || (kX && !BNK && BK == kBK && !SCALED), "thin column edge: the transposing producer, "
+                                                                  "32-deep slices, plain epilogue");
     constexpr int kEcOff = kRingBytes + (kStg ? kPartialBytes : 0) + 256;
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };

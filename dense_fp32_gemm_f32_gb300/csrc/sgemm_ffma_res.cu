@@ -7,21 +7,21 @@
 
 namespace gb300 {
 
-template <int S, bool SCALED = false>
+template <int S, bool SCALED = false, bool EDGE = false>
 static KernelEntry entry() {
     constexpr bool kStg = ffma_tma_store<S, kProducerTmaX, kBN, SCALED, false, kBK, true>();
     return {reinterpret_cast<const void*>(
-                &sgemm_ffma_kernel<S, kProducerTmaX, kMathFfma2, kBN, SCALED, false, false, kBK, true>),
-            ffma_smem_bytes<S, kBN, true, false, kStg, kBK, true>(), ffma_threads<kProducerTmaX, true>(), kStg};
+                &sgemm_ffma_kernel<S, kProducerTmaX, kMathFfma2, kBN, SCALED, false, false, kBK, true, EDGE>),
+            ffma_smem_bytes<S, kBN, true, false, kStg, kBK, true, EDGE>(), ffma_threads<kProducerTmaX, true>(), kStg};
 }
 
-KernelEntry ffma_kernel_res(int stages, int math, bool scaled) {
+KernelEntry ffma_kernel_res(int stages, int math, bool scaled, bool edge) {
     if (math != kMathFfma2) return {nullptr, 0, 0};
-    if (scaled) return stages == 2 ? entry<2, true>() : KernelEntry{nullptr, 0, 0};
+    if (scaled) return (stages == 2 && !edge) ? entry<2, true>() : KernelEntry{nullptr, 0, 0};
     switch (stages) {
-        case 2: return entry<2>();
-        case 3: return entry<3>();
-        case 4: return entry<4>();
+        case 2: return edge ? entry<2, false, true>() : entry<2>();
+        case 3: return edge ? entry<3, false, true>() : entry<3>();
+        case 4: return edge ? entry<4, false, true>() : entry<4>();
     }
     return {nullptr, 0, 0};
 }

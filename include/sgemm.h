@@ -153,8 +153,9 @@ int sgemm_f32(int M, int N, int K,
  *
  * Limits and rules:
  *  - The array holds the scratch of at most 160 CTAs: 160 x 64 KiB partial
- *    tiles + 160 flags = 10 MiB + 640 bytes on every GPU that loads the
- *    library, kept until the process exits.  A call uses one CTA per SM, at
+ *    tiles + 160 flags + 160 x 2 KiB thin-edge partial sums (see
+ *    sgemm_options.edge) = 10 MiB + 640 bytes + 320 KiB on every GPU that
+ *    loads the library, kept until the process exits.  A call uses one CTA per SM, at
  *    most 160 (a GPU with more SMs still gets a correct, slower result); the
  *    scratch a call needs is bounded by that count, not by M, N or K, and a
  *    call that would need more is rejected with SGEMM_ERR_INVALID_ARG.
@@ -328,7 +329,8 @@ typedef struct sgemm_options {
                              units; a tile shared by several CTAs is finished
                              by the CTA holding its first K slice from the
                              others' partial tiles.  Needs a workspace of
-                             CTAs x (partial tile + 4 bytes): the scratch
+                             CTAs x (partial tile + 4 bytes, + 2 KiB with a
+                             thin column edge, see edge): the scratch
                              the library keeps per stream (cudaMalloc'ed on
                              the stream's first such call), or, in a stream
                              capture, a pool workspace (see "Device memory
@@ -385,8 +387,9 @@ typedef struct sgemm_options {
     int edge;             /* 0 = auto, 1 = off.  Thin column edge: when N mod
                              128 is 1 to 4 and the product runs stream-K on
                              the transposing producer (SGEMM_PRODUCER_TMA_X
-                             or SGEMM_PRODUCER_TMA_RES, 32-deep slices, the
-                             plain epilogue), those last columns are computed
+                             or SGEMM_PRODUCER_TMA_RES, 32-deep slices,
+                             paired FMA, the plain epilogue), those last
+                             columns are computed
                              by the CTAs working on the last column of full
                              128 x 128 tiles instead of as a column of tiles
                              of their own (the stream-K workspace then also

@@ -991,13 +991,13 @@ def test_thin_column_edge_guard_bands(c_offset):
 
 
 @pytest.mark.parametrize("opt", [dict(edge=1), dict(edge=1, producer=8), dict(stages=3), dict(stages=4),
-                                 dict(producer=8, stages=3), dict(math=1, repack=2), dict(group_m=1),
+                                 dict(producer=8, stages=3), dict(repack=2), dict(math=1, repack=2), dict(group_m=1),
                                  dict(stream_k=1, split_k=1), dict(split_k=2), dict(tile_n=64, repack=2),
                                  dict(producer=2)])
 def test_thin_column_edge_forced_choices(opt):
-    """The edge fold under the other stage counts, scalar FFMA, repacked
-    operands and row-by-row tile order; switched off (edge = 1: a ninth
-    column of tiles) and not taken without stream-K or the transposing
+    """The edge fold under the other stage counts, repacked operands and
+    row-by-row tile order; switched off (edge = 1: a ninth column of tiles)
+    and not taken with scalar FFMA or without stream-K or the transposing
     producer (plain grid, cluster split-K, 128 x 64 tiles, cp.async)."""
     M, N, K = 1023, 1025, 1027
     A, B = make_operands(M, N, K, "int", 67)
