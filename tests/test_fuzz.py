@@ -19,6 +19,7 @@ OPTIONS = [
     dict(a_layout=2), dict(a_layout=1), dict(repack=2), dict(math=1), dict(stages=3),
     dict(group_m=1), dict(group_m=3), dict(producer=5, stream_k=2), dict(a_layout=2, stream_k=2), dict(tile_n=256, stream_k=2), dict(producer=6),
     dict(producer=8), dict(producer=8, stages=3), dict(producer=8, split_k=2), dict(repack=1), dict(l2_hint=4),
+    dict(edge=1),
 ]
 
 
