@@ -30,6 +30,19 @@ def test_headers_declare_the_abi():
     assert set(names) == set(_lib.SIGNATURES), "binding signatures and headers disagree"
 
 
+def test_options_struct_matches_the_header():
+    """The binding's struct sgemm_options has the header's fields, in the
+    header's order, with the header's types (int, uint64_t), so that a field
+    added on one side only cannot shift the others."""
+    text = open(os.path.join(ROOT, "include", "sgemm.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    body = re.search(r"typedef\s+struct\s+sgemm_options\s*\{(.*?)\}\s*sgemm_options\s*;", text, re.S).group(1)
+    fields = re.findall(r"(int|uint64_t)\s+(\w+)\s*;", body)
+    assert fields, "no fields parsed"
+    ctypes_of = {"int": ctypes.c_int, "uint64_t": ctypes.c_uint64}
+    assert [(n, ctypes_of[t]) for t, n in fields] == list(_lib.Options._fields_)
+
+
 def test_library_exports_every_declared_symbol():
     lib = _lib.load()
     for name in declared_functions():
