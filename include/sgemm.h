@@ -443,10 +443,18 @@ int sgemm_check_status(void* stream);
 const char* sgemm_status_string(int status);
 
 /* Describes the variant sgemm_f32 would launch for these sizes and pointers on
- * the current device, as a thread-local string such as "tma/ffma2/s1/st4"
- * (producer / math / split-K / stages), with "/tailS:T" appended
- * when T tail tiles run as a second launch split S ways.  Host-only; it
- * launches nothing, but sets up the current device on first use. */
+ * the current device, as a thread-local string such as
+ * "tmax/ffma2/s1/st2/sk152" (producer / math / split-K / stages), with, in
+ * this order when they apply: "/tailS:T" (T tail tiles run as a second
+ * launch split S ways), "/skG" (stream-K over G CTAs), "/nBN" (tiles BN
+ * wide, when not 128), "/repackA", "/repackB" or "/repackAB" (operands
+ * copied into pitched rows first), "/at" (A read transposed), "/bt" (B
+ * stored N x K), "/kBK" (BK-deep slices, when not 32), "/res" (residue-class
+ * tensor maps) and "/ecE" (E columns of a thin column edge computed with the
+ * last column of tiles; see sgemm_options.edge).  The small-problem kernel
+ * reads "small/t32/w8"; an empty output "noop"; arguments sgemm_f32 would
+ * refuse "invalid"; no usable device "unavailable".  Host-only; it launches
+ * nothing, but sets up the current device on first use. */
 const char* sgemm_describe(int M, int N, int K,
                            const float* A, int lda,
                            const float* B, int ldb,
