@@ -935,7 +935,7 @@ def test_cuda_graph_capture_on_residue_class_maps():
 @pytest.mark.parametrize("dist", ["uniform", "int"])
 @pytest.mark.parametrize("b_rows", ["exact", "padded"])
 @pytest.mark.parametrize("shape", [(1023, 1025, 1027), (2000, 130, 700), (3201, 515, 96), (1000, 644, 333),
-                                   (128, 2050, 4096), (300, 516, 4096)])
+                                   (128, 2050, 4096), (300, 516, 4096), (4, 1025, 65536), (129, 257, 8192)])
 def test_thin_column_edge(shape, b_rows, dist):
     """N mod 128 = 1 .. 4 columns past the last full column of tiles,
     computed by the CTAs working on that column (B's edge values copied per
@@ -944,7 +944,9 @@ def test_thin_column_edge(shape, b_rows, dist):
     residue-class maps wherever a row of A or B is not a 16-byte multiple,
     else the plain tensor maps); one column of tiles (N = 130), a last row of
     tiles holding one row and K of 3 slices (3201 x 515 x 96), one row of
-    tiles with K = 4096, and N = 516 with the tensor-map stores of C; every
+    tiles with K = 4096, N = 516 with the tensor-map stores of C, four rows
+    with K = 65536 (each edge tile's slices shared by every CTA) and two rows
+    of tiles, the second holding one row, on two columns of tiles; every
     element, integer inputs exactly."""
     M, N, K = shape
     A, B = make_operands(M, N, K, dist, 64)
